@@ -1,0 +1,239 @@
+"""Seeded synthetic inputs for the 2-bit MoE layer and for the NVFP4 re-quantizer.
+
+This module only draws random numbers and lays them out in the storage formats.
+It holds none of the layer's arithmetic (no dequantisation, no re-quantisation,
+no permutation, no expert math), so both the CUDA path and the CPU oracle can be
+fed from it without sharing any of the method.
+
+Workloads (shapes follow the models named on the vLLM-Moet pages: GLM-5.x and
+DeepSeek-V4-Flash experts, top-8 routing, hidden 6144/4096, expert intermediate
+2048; page "vLLM-Moet wiki", section "The kernels", and page "The v0.24.0 port",
+section "Our hooks"):
+
+  tiny            H=512  I=256  E=8   top-2 T=4     UE8M0 exponents in [-9,-6]  router logits
+  decode_t1       H=6144 I=2048 E=256 top-8 T=1     exponents in [-10,-6]       Zipf(1.1) routing
+  decode_t32      H=6144 I=2048 E=256 top-8 T=32    exponents in [-10,-6]       Zipf(1.1) routing
+  prefill_t8192   H=4096 I=2048 E=256 top-8 T=8192  exponents in [-10,-6]       router logits
+  requant_256     256 experts of NVFP4 gate/up [2048x6144] and down [6144x2048]
+
+Recipe (all numpy PCG64 via ``default_rng(seed)``):
+  * activations: standard normal fp32, rounded to bf16 (round to nearest even);
+    returned as the uint16 bit pattern.
+  * code planes: uniform random bytes (every 2-bit field is then uniform over the
+    four codes and independent); UE8M0 scale bytes 127 + integers(lo, hi+1).
+  * router "logits": standard normal (T, E) fp32, top-k by value with ties to the
+    lower id, weights = softmax over the k selected logits.
+  * router "zipf": expert popularity p_r proportional to r^-1.1 (r = 1..E), rank r
+    mapped to expert id perm[r-1] for perm = rng.permutation(E); each token draws
+    k distinct experts with those probabilities; weights = softmax of k standard
+    normal logits.
+  * NVFP4 tensors: e2m1 nibbles uniform over all 16 codes (uniform random bytes,
+    low nibble = even element), e4m3 block-16 scales 2^U(-6, 2) rounded to the
+    nearest e4m3fn value (ties to even mantissa), scale_2 = 2^-8 per tensor.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+
+@dataclasses.dataclass(frozen=True)
+class LayerConfig:
+    name: str
+    hidden: int          # H
+    inter: int           # I
+    num_experts: int     # E
+    top_k: int           # k
+    tokens: int          # T
+    exp_lo: int          # UE8M0 exponent range of the code planes
+    exp_hi: int
+    routing: str         # "logits" or "zipf"
+    seed: int
+
+    @property
+    def pairs(self) -> int:
+        return self.tokens * self.top_k
+
+    @property
+    def plane_bytes_per_expert(self) -> int:
+        H, I = self.hidden, self.inter
+        return 2 * I * (H // 4) + 2 * I * (H // 32) + H * (I // 4) + H * (I // 32)
+
+
+@dataclasses.dataclass(frozen=True)
+class RequantConfig:
+    name: str
+    num_experts: int
+    inter: int
+    hidden: int
+    seed: int
+
+
+CONFIGS = {
+    "tiny": LayerConfig("tiny", 512, 256, 8, 2, 4, -9, -6, "logits", 0),
+    "decode_t1": LayerConfig("decode_t1", 6144, 2048, 256, 8, 1, -10, -6, "zipf", 1),
+    "decode_t32": LayerConfig("decode_t32", 6144, 2048, 256, 8, 32, -10, -6, "zipf", 2),
+    "prefill_t8192": LayerConfig("prefill_t8192", 4096, 2048, 256, 8, 8192, -10, -6, "logits", 3),
+}
+REQUANT = RequantConfig("requant_256", 256, 2048, 6144, 4)
+
+
+def rng_for(seed: int) -> np.random.Generator:
+    return np.random.default_rng(seed)
+
+
+def random_bytes(rng: np.random.Generator, shape) -> np.ndarray:
+    n = int(np.prod(shape))
+    return np.frombuffer(rng.bytes(n), dtype=np.uint8).reshape(shape).copy()
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round finite fp32 values to bf16 (nearest, ties to even); uint16 bit patterns."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def activations(rng: np.random.Generator, T: int, H: int) -> np.ndarray:
+    return f32_to_bf16_bits(rng.standard_normal((T, H), dtype=np.float32))
+
+
+def code_planes(rng: np.random.Generator, E: int, H: int, I: int, exp_lo: int, exp_hi: int):
+    """Random 2-bit expert planes: codes uniform over the four codes, exponents uniform."""
+    w13_codes = random_bytes(rng, (E, 2 * I, H // 4))
+    w13_scales = (127 + rng.integers(exp_lo, exp_hi + 1, size=(E, 2 * I, H // 32))).astype(np.uint8)
+    w2_codes = random_bytes(rng, (E, H, I // 4))
+    w2_scales = (127 + rng.integers(exp_lo, exp_hi + 1, size=(E, H, I // 32))).astype(np.uint8)
+    return {"w13_codes": w13_codes, "w13_scales": w13_scales,
+            "w2_codes": w2_codes, "w2_scales": w2_scales}
+
+
+def _softmax_rows(z: np.ndarray) -> np.ndarray:
+    z = z.astype(np.float64)
+    z = z - z.max(axis=1, keepdims=True)
+    e = np.exp(z)
+    return (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+def routing_logits(rng: np.random.Generator, T: int, E: int, k: int):
+    logits = rng.standard_normal((T, E), dtype=np.float32)
+    ids = np.argsort(-logits, axis=1, kind="stable")[:, :k].astype(np.int32)
+    sel = np.take_along_axis(logits, ids, axis=1)
+    return ids, _softmax_rows(sel)
+
+
+def zipf_popularity(rng: np.random.Generator, E: int, s: float = 1.1) -> np.ndarray:
+    ranks = np.arange(1, E + 1, dtype=np.float64)
+    p_rank = ranks ** (-s)
+    p_rank /= p_rank.sum()
+    perm = rng.permutation(E)
+    p = np.empty(E, dtype=np.float64)
+    p[perm] = p_rank
+    return p
+
+
+def routing_zipf(rng: np.random.Generator, T: int, E: int, k: int, popularity=None):
+    p = zipf_popularity(rng, E) if popularity is None else popularity
+    ids = np.empty((T, k), dtype=np.int32)
+    for t in range(T):
+        ids[t] = rng.choice(E, size=k, replace=False, p=p)
+    weights = _softmax_rows(rng.standard_normal((T, k), dtype=np.float32))
+    return ids, weights
+
+
+def routing(rng: np.random.Generator, cfg: LayerConfig, T: int | None = None, popularity=None):
+    T = cfg.tokens if T is None else T
+    if cfg.routing == "logits":
+        return routing_logits(rng, T, cfg.num_experts, cfg.top_k)
+    return routing_zipf(rng, T, cfg.num_experts, cfg.top_k, popularity)
+
+
+@dataclasses.dataclass
+class LayerInputs:
+    cfg: LayerConfig
+    x: np.ndarray            # uint16 bf16 bits [T][H]
+    ids: np.ndarray          # int32 [T][k]
+    weights: np.ndarray      # float32 [T][k]
+    planes: dict             # the four uint8 sections
+
+
+def layer_inputs(cfg: LayerConfig, seed: int | None = None) -> LayerInputs:
+    """Inputs of one configuration: planes first, then activations, then routing."""
+    rng = rng_for(cfg.seed if seed is None else seed)
+    planes = code_planes(rng, cfg.num_experts, cfg.hidden, cfg.inter, cfg.exp_lo, cfg.exp_hi)
+    x = activations(rng, cfg.tokens, cfg.hidden)
+    ids, weights = routing(rng, cfg)
+    return LayerInputs(cfg, x, ids, weights, planes)
+
+
+def small_layer_inputs(H: int, I: int, E: int, k: int, T: int, seed: int,
+                       exp_lo: int = -9, exp_hi: int = -6, routing_kind: str = "logits") -> LayerInputs:
+    cfg = LayerConfig(f"H{H}_I{I}_E{E}_k{k}_T{T}", H, I, E, k, T, exp_lo, exp_hi, routing_kind, seed)
+    return layer_inputs(cfg)
+
+
+# --------------------------------------------------------------------------- NVFP4
+
+def _e4m3_positive_table():
+    """Values and bytes of the positive normal e4m3fn codes (exponent field 1..15)."""
+    vals, codes = [], []
+    for ef in range(1, 16):
+        for m in range(8):
+            if ef == 15 and m == 7:
+                continue  # the NaN code
+            vals.append((1.0 + m / 8.0) * 2.0 ** (ef - 7))
+            codes.append((ef << 3) | m)
+    return np.array(vals), np.array(codes, dtype=np.uint8)
+
+
+def e4m3_round_positive(v: np.ndarray) -> np.ndarray:
+    """Nearest positive normal e4m3fn byte to each value in [2^-6, 448] (ties: even mantissa)."""
+    vals, codes = _e4m3_positive_table()
+    v = np.asarray(v, dtype=np.float64)
+    hi = np.clip(np.searchsorted(vals, v, side="left"), 1, len(vals) - 1)
+    lo = hi - 1
+    dlo, dhi = v - vals[lo], vals[hi] - v
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & ((codes[hi] & 1) == 0))
+    out = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
+    exact = v == vals[hi]
+    return np.where(exact, codes[hi], out).astype(np.uint8)
+
+
+@dataclasses.dataclass
+class Nvfp4Tensors:
+    e2m1: np.ndarray      # uint8 [n][rows][K/2], low nibble = even element
+    e4m3: np.ndarray      # uint8 [n][rows][K/16]
+    scale_2: np.ndarray   # float32 [n]
+
+
+def nvfp4_tensors(rng: np.random.Generator, n: int, rows: int, K: int,
+                  scale_2: float = 2.0 ** -8) -> Nvfp4Tensors:
+    e2m1 = random_bytes(rng, (n, rows, K // 2))
+    e = rng.uniform(-6.0, 2.0, size=(n, rows, K // 16))
+    e4m3 = e4m3_round_positive(np.exp2(e))
+    return Nvfp4Tensors(e2m1, e4m3, np.full(n, scale_2, dtype=np.float32))
+
+
+def requant_inputs(cfg: RequantConfig = REQUANT, experts: int | None = None):
+    """The re-quantizer workload: (gate/up tensors, down tensors).
+
+    gate/up: 2*E tensors of [I][H] (expert e's gate is tensor 2e, its up tensor
+    2e+1, so the outputs land contiguously in the w13 planes); down: E tensors of
+    [H][I].  ``experts`` limits the draw to the first experts (same values as the
+    full draw for those experts: every expert has its own child seed).
+    """
+    E = cfg.num_experts if experts is None else experts
+    seeds = np.random.SeedSequence(cfg.seed).spawn(cfg.num_experts)
+    gu_list, dn_list = [], []
+    for e in range(E):
+        rng = np.random.default_rng(seeds[e])
+        gu_list.append(nvfp4_tensors(rng, 2, cfg.inter, cfg.hidden))
+        dn_list.append(nvfp4_tensors(rng, 1, cfg.hidden, cfg.inter))
+    gu = Nvfp4Tensors(np.concatenate([t.e2m1 for t in gu_list]),
+                      np.concatenate([t.e4m3 for t in gu_list]),
+                      np.concatenate([t.scale_2 for t in gu_list]))
+    dn = Nvfp4Tensors(np.concatenate([t.e2m1 for t in dn_list]),
+                      np.concatenate([t.e4m3 for t in dn_list]),
+                      np.concatenate([t.scale_2 for t in dn_list]))
+    return gu, dn

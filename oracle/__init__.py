@@ -1,0 +1,154 @@
+"""CPU oracle for the 2-bit MoE layer: ctypes wrappers around ``oracle.c``.
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / ``--impl reference`` legs may use it; the library
+and its Python binding never import it.
+
+Everything here marshals numpy arrays; the arithmetic lives in ``oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle_moe_w2.so")
+_lock = threading.Lock()
+_lib = None
+
+BAD_EXPERT_ID = 1
+BAD_SCALE = 2
+BAD_NVFP4 = 4
+
+_CFLAGS = ["-O2", "-std=c11", "-Wall", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C, no architecture flags)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
+            L.oracle_version.restype = ctypes.c_int
+            L.oracle_e2m1_value.argtypes = [ctypes.c_uint]
+            L.oracle_e2m1_value.restype = ctypes.c_double
+            L.oracle_e4m3_value.argtypes = [ctypes.c_uint]
+            L.oracle_e4m3_value.restype = ctypes.c_double
+            L.oracle_code_value.argtypes = [ctypes.c_uint]
+            L.oracle_code_value.restype = ctypes.c_double
+            L.oracle_bf16_from_double.argtypes = [ctypes.c_double]
+            L.oracle_bf16_from_double.restype = ctypes.c_uint16
+            L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            L.oracle_bf16_to_double.restype = ctypes.c_double
+            L.oracle_requant.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp]
+            L.oracle_requant.restype = u32
+            L.oracle_requant_blocks.argtypes = [vp, vp, vp, i64, i64, vp, i64, vp, vp]
+            L.oracle_requant_blocks.restype = u32
+            L.oracle_permute.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+            L.oracle_permute.restype = u32
+            L.oracle_forward_tokens.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                vp, i64, vp, vp]
+            L.oracle_forward_tokens.restype = u32
+            _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags.c_contiguous
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def e2m1_value(nib: int) -> float:
+    return lib().oracle_e2m1_value(nib)
+
+
+def e4m3_value(b: int) -> float:
+    return lib().oracle_e4m3_value(b)
+
+
+def code_value(c: int) -> float:
+    return lib().oracle_code_value(c)
+
+
+def bf16_from_double(v: float) -> int:
+    return lib().oracle_bf16_from_double(v)
+
+
+def bf16_to_double(h: int) -> float:
+    return lib().oracle_bf16_to_double(h)
+
+
+def requant(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray):
+    """e2m1 uint8 [n][rows][K/2], e4m3 uint8 [n][rows][K/16], scale_2 float32 [n]."""
+    n, rows, half_k = e2m1.shape
+    K = half_k * 2
+    e2m1 = np.ascontiguousarray(e2m1)
+    e4m3 = np.ascontiguousarray(e4m3)
+    s2 = np.ascontiguousarray(scale_2, dtype=np.float32)
+    codes = np.empty((n, rows, K // 4), np.uint8)
+    scales = np.empty((n, rows, K // 32), np.uint8)
+    st = lib().oracle_requant(_p(e2m1), _p(e4m3), _p(s2), n, rows, K, _p(codes), _p(scales))
+    return codes, scales, int(st)
+
+
+def requant_blocks(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray, block_ids):
+    """Selected blocks (flat index over n*rows*K/32) -> codes [nb][8], scales [nb]."""
+    n, rows, half_k = e2m1.shape
+    K = half_k * 2
+    ids = np.ascontiguousarray(block_ids, dtype=np.int64)
+    codes = np.empty((len(ids), 8), np.uint8)
+    scales = np.empty(len(ids), np.uint8)
+    s2 = np.ascontiguousarray(scale_2, dtype=np.float32)
+    st = lib().oracle_requant_blocks(_p(np.ascontiguousarray(e2m1)), _p(np.ascontiguousarray(e4m3)),
+                                     _p(s2), rows, K, _p(ids), len(ids), _p(codes), _p(scales))
+    return codes, scales, int(st)
+
+
+def permute(ids: np.ndarray, E: int):
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T, k = ids.shape
+    P = T * k
+    sorted_pairs = np.empty(P, np.int32)
+    inv = np.empty(P, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    st = lib().oracle_permute(_p(ids), T, k, E, _p(sorted_pairs), _p(inv), _p(offsets))
+    return sorted_pairs, inv, offsets, int(st)
+
+
+def forward_tokens(x: np.ndarray, ids: np.ndarray, weights: np.ndarray, planes: dict,
+                   tokens=None, want_h: bool = False):
+    """y (bf16 bits) for the listed tokens; x uint16 [T][H], ids int32 [T][k], weights f32 [T][k]."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    weights = np.ascontiguousarray(weights, dtype=np.float32)
+    T, H = x.shape
+    k = ids.shape[1]
+    E, two_i, _ = planes["w13_codes"].shape
+    I = two_i // 2
+    tok = np.arange(T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
+    y = np.empty((len(tok), H), np.uint16)
+    h = np.empty((len(tok), k, I), np.uint16) if want_h else None
+    st = lib().oracle_forward_tokens(
+        _p(x), _p(ids), _p(weights),
+        _p(planes["w13_codes"]), _p(planes["w13_scales"]), _p(planes["w2_codes"]), _p(planes["w2_scales"]),
+        E, H, I, k, _p(tok), len(tok), _p(y), _p(h) if want_h else None)
+    return (y, h, int(st)) if want_h else (y, int(st))
+
+
+def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
+    """Reinterpret bf16 bit patterns as float values (exact)."""
+    return (np.asarray(a, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)

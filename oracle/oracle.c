@@ -1,0 +1,349 @@
+/*
+ * CPU oracle for the 2-bit sign-symmetric MoE layer (vLLM-Moet) and its NVFP4
+ * re-quantizer.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the
+ * benchmark's CPU-baseline leg load this library; the product path never does.
+ *
+ * Plain, single-threaded loops in f64 (and exact 128-bit integer sums where an
+ * L2 comparison has to be exact).  No blocking, no fusion, no reordering beyond
+ * what each definition states.  Shares no source with the CUDA library.
+ *
+ * Sources (vLLM-Moet pages):
+ *   [wiki]  "vLLM-Moet wiki", section "2-bit expert planes": codebook {-4,-1,1,4},
+ *           sign-symmetric, chosen at the same L2 error.
+ *   [port]  "The v0.24.0 port", section "Our hooks", modelopt.py bullet: NVFP4 =
+ *           e2m1 codes x e4m3 block-16 scales x per-tensor scale_2, dequantized
+ *           to f64 exactly (all three factors representable), re-quantized to
+ *           the sign-symmetric codebook with UE8M0 block-32 output scales that
+ *           absorb scale_2.
+ *   [port]  same section, BASE-cache bullet: codes + UE8M0 scales, four
+ *           sections per expert slot.
+ *   [port]  same section, "Deterministic unpermute" bullet: valid sorted ids are
+ *           a permutation of token*top_k+j; outputs are placed per pair and
+ *           summed over j in a fixed order.
+ *
+ * Readings taken where the pages are silent (each one is listed in the design doc):
+ *   R1 code order: 2-bit code c = (sign << 1) | magnitude, i.e. 0:+1 1:+4 2:-1 3:-4.
+ *   R2 packing: 4 codes per byte along K, element 4b+q in bits 2q..2q+1 of byte b.
+ *   R3 scale search: the UE8M0 exponent u in [-126,125] that minimises the exact
+ *      L2 error with every element at its nearest code; ties go to the smaller u.
+ *   R4 nearest code: magnitude 4 iff |x| > 2.5*2^u (a tie goes to magnitude 1);
+ *      the code's sign is the sign bit of x, so -0 maps to -1.
+ *   R5 invalid input: scale_2 not a positive finite number, or an e4m3 NaN in
+ *      the block -> codes 0x00 and scale byte 0 for the block, status bit 4.
+ *   R6 forward: gate rows 0..I-1 and up rows I..2I-1 of w13; h = bf16(SiLU(g)*u);
+ *      the router weight multiplies the down projection; y = bf16(sum over j in
+ *      j order); all sums in f64.  Expert ids outside [0,E) contribute nothing
+ *      (status bit 1); a UE8M0 byte outside [1,252] zeroes its block (bit 2).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_BAD_EXPERT_ID 1u
+#define ORACLE_BAD_SCALE 2u
+#define ORACLE_BAD_NVFP4 4u
+
+typedef unsigned __int128 u128;
+
+int oracle_version(void) { return 1; }
+
+static void oracle_fail(const char *what)
+{
+    fprintf(stderr, "oracle: internal check failed: %s\n", what);
+    abort();
+}
+
+/* ---------------------------------------------------------------- value tables */
+
+/* e2m1: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa. */
+double oracle_e2m1_value(unsigned nib)
+{
+    unsigned s = (nib >> 3) & 1u, e = (nib >> 1) & 3u, m = nib & 1u;
+    double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, (int)e - 1);
+    return s ? -mag : mag;
+}
+
+/* e4m3fn: bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0 mantissa;
+ * S.1111.111 is NaN, there is no infinity. */
+double oracle_e4m3_value(unsigned b)
+{
+    unsigned s = (b >> 7) & 1u, e = (b >> 3) & 15u, m = b & 7u;
+    if (e == 15 && m == 7) return NAN;
+    double mag = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+    return s ? -mag : mag;
+}
+
+/* The sign-symmetric codebook under reading R1. */
+double oracle_code_value(unsigned c)
+{
+    static const double v[4] = {1.0, 4.0, -1.0, -4.0};
+    return v[c & 3u];
+}
+
+/* UE8M0 byte s -> 2^(s-127); the forward accepts s in [1,252] only. */
+static int ue8m0_valid(unsigned s) { return s >= 1 && s <= 252; }
+
+double oracle_bf16_to_double(uint16_t h)
+{
+    uint32_t bits = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &bits, 4);
+    return (double)f;
+}
+
+/* f64 -> bf16, one rounding, to nearest with ties to even. */
+uint16_t oracle_bf16_from_double(double v)
+{
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    int ex;
+    (void)frexp(a, &ex);                 /* a in [2^(ex-1), 2^ex) */
+    int q = (ex - 1 >= -126) ? ex - 8 : -133;   /* quantum: 8 significant bits, or subnormal */
+    double r = nearbyint(ldexp(a, -q)) ;  /* default rounding mode: to nearest even */
+    double rv = ldexp(r, q);
+    float f = (float)rv;                 /* exact (<= 8 significant bits) or overflow to inf */
+    uint32_t bits;
+    memcpy(&bits, &f, 4);
+    if (isinf(f)) return sign | 0x7F80;
+    return sign | (uint16_t)(bits >> 16);
+}
+
+/* ------------------------------------------------------------------ requant */
+
+/* One block of 32 NVFP4 elements -> 8 code bytes and one UE8M0 byte. */
+static uint32_t requant_block(const uint8_t *nib_bytes, const uint8_t *e4m3_pair, float scale_2,
+                              uint8_t *codes_out, uint8_t *scale_out)
+{
+    double s2 = (double)scale_2;
+    double sc[2] = {oracle_e4m3_value(e4m3_pair[0]), oracle_e4m3_value(e4m3_pair[1])};
+    if (!(s2 > 0.0) || isinf(s2) || isnan(sc[0]) || isnan(sc[1])) {
+        memset(codes_out, 0, 8);
+        *scale_out = 0;
+        return ORACLE_BAD_NVFP4;
+    }
+
+    /* Exact f64 dequantisation: each product has at most 2+4+24 significant bits. */
+    double x[32], a[32];
+    int neg[32];
+    double amax = 0.0, min_nz = INFINITY;
+    for (int i = 0; i < 32; ++i) {
+        unsigned nib = (nib_bytes[i / 2] >> (4 * (i % 2))) & 0xFu;
+        x[i] = oracle_e2m1_value(nib) * sc[i / 16] * s2;
+        neg[i] = signbit(x[i]) ? 1 : 0;
+        a[i] = fabs(x[i]);
+        if (a[i] > amax) amax = a[i];
+        if (a[i] > 0.0 && a[i] < min_nz) min_nz = a[i];
+    }
+
+    int u;
+    if (amax == 0.0) {
+        u = -126;   /* every candidate costs 32*4^u: the smallest scale wins */
+    } else {
+        /* Candidate window.  u > m+1 only moves every code further from every x;
+         * below 2^u < min_nz/12 the error grows as u falls (all nonzero
+         * elements saturate at 4*2^u).  lo = floor(log2 min_nz) - 5 is below
+         * that point, so [lo, m+1] holds the minimiser over all u in [-126,125]. */
+        int ex;
+        (void)frexp(amax, &ex);
+        int m = ex - 1;
+        (void)frexp(min_nz, &ex);
+        int mlo = ex - 1;
+        int hi = m + 1, lo = mlo - 5;
+        if (hi > 125) hi = 125;
+        if (hi < -126) hi = -126;
+        if (lo < -126) lo = -126;
+        if (lo > hi) lo = hi;
+
+        if (lo == hi) {
+            u = lo;
+        } else {
+            /* |x_i| = N_i * 2^c with N_i integer; c = lowest set bit of the block. */
+            int c = 1 << 30;
+            for (int i = 0; i < 32; ++i) {
+                if (a[i] == 0.0) continue;
+                int e2;
+                double f = frexp(a[i], &e2);
+                uint64_t M = (uint64_t)ldexp(f, 53);
+                int tz = __builtin_ctzll(M);
+                int low = e2 - 53 + tz;
+                if (low < c) c = low;
+            }
+            int e0 = (c < lo) ? c : lo;   /* common unit 2^e0 for every candidate */
+            if (c - e0 > 8) oracle_fail("requant: unit shift");
+            uint64_t A[32];
+            for (int i = 0; i < 32; ++i) {
+                double n = ldexp(a[i], -c);
+                if (n >= 9007199254740992.0) oracle_fail("requant: mantissa range");
+                A[i] = ((uint64_t)n) << (c - e0);
+            }
+            u128 best = 0;
+            int best_u = lo;
+            for (int cand = lo; cand <= hi; ++cand) {
+                if (cand - e0 > 58) oracle_fail("requant: candidate range");
+                double thr = 2.5 * ldexp(1.0, cand);
+                u128 sse = 0;
+                for (int i = 0; i < 32; ++i) {
+                    uint64_t mag = (a[i] > thr) ? 4u : 1u;
+                    uint64_t V = mag << (cand - e0);
+                    uint64_t d = (A[i] > V) ? A[i] - V : V - A[i];
+                    sse += (u128)d * (u128)d;
+                }
+                if (cand == lo || sse < best) {
+                    best = sse;
+                    best_u = cand;
+                }
+            }
+            u = best_u;
+        }
+    }
+
+    double thr = 2.5 * ldexp(1.0, u);
+    memset(codes_out, 0, 8);
+    for (int i = 0; i < 32; ++i) {
+        unsigned mag4 = (a[i] > thr) ? 1u : 0u;
+        unsigned code = ((unsigned)neg[i] << 1) | mag4;
+        codes_out[i / 4] |= (uint8_t)(code << (2 * (i % 4)));
+    }
+    *scale_out = (uint8_t)(u + 127);
+    return 0;
+}
+
+/* Whole tensors: e2m1 [n][rows][K/2], e4m3 [n][rows][K/16], scale_2 [n]
+ * -> codes [n][rows][K/4], ue8m0 [n][rows][K/32].  Returns status bits. */
+uint32_t oracle_requant(const uint8_t *e2m1, const uint8_t *e4m3, const float *scale_2,
+                        int64_t n, int64_t rows, int64_t K, uint8_t *codes, uint8_t *ue8m0)
+{
+    if (K % 32 != 0) return 0x80000000u;
+    uint32_t st = 0;
+    int64_t blocks_per_tensor = rows * (K / 32);
+    for (int64_t t = 0; t < n; ++t)
+        for (int64_t b = 0; b < blocks_per_tensor; ++b) {
+            int64_t g = t * blocks_per_tensor + b;
+            st |= requant_block(e2m1 + g * 16, e4m3 + g * 2, scale_2[t], codes + g * 8, ue8m0 + g);
+        }
+    return st;
+}
+
+/* Selected blocks only (flat block index over n*rows*K/32); outputs [nb][8], [nb]. */
+uint32_t oracle_requant_blocks(const uint8_t *e2m1, const uint8_t *e4m3, const float *scale_2,
+                               int64_t rows, int64_t K, const int64_t *block_ids, int64_t nb,
+                               uint8_t *codes, uint8_t *ue8m0)
+{
+    if (K % 32 != 0) return 0x80000000u;
+    uint32_t st = 0;
+    int64_t blocks_per_tensor = rows * (K / 32);
+    for (int64_t i = 0; i < nb; ++i) {
+        int64_t g = block_ids[i];
+        st |= requant_block(e2m1 + g * 16, e4m3 + g * 2, scale_2[g / blocks_per_tensor],
+                            codes + i * 8, ue8m0 + i);
+    }
+    return st;
+}
+
+/* ------------------------------------------------------------------ permute */
+
+/* Stable grouping of pairs p = t*k + j by expert id: for e = 0..E-1 in order,
+ * every pair of expert e in increasing p; out-of-range ids follow, in increasing
+ * p.  offsets[e] = first sorted slot of expert e, offsets[E] = valid pairs. */
+uint32_t oracle_permute(const int32_t *ids, int64_t T, int32_t k, int32_t E,
+                        int32_t *sorted_pairs, int32_t *inv_pairs, int32_t *offsets)
+{
+    int64_t P = T * k, q = 0;
+    uint32_t st = 0;
+    for (int32_t e = 0; e < E; ++e) {
+        offsets[e] = (int32_t)q;
+        for (int64_t p = 0; p < P; ++p)
+            if (ids[p] == e) sorted_pairs[q++] = (int32_t)p;
+    }
+    offsets[E] = (int32_t)q;
+    for (int64_t p = 0; p < P; ++p)
+        if (ids[p] < 0 || ids[p] >= E) {
+            sorted_pairs[q++] = (int32_t)p;
+            st |= ORACLE_BAD_EXPERT_ID;
+        }
+    for (int64_t i = 0; i < P; ++i) inv_pairs[sorted_pairs[i]] = (int32_t)i;
+    return st;
+}
+
+/* ------------------------------------------------------------------ forward */
+
+/* Dequantise one row of K weights: w = code_value * 2^(s-127). */
+static uint32_t dequant_row(const uint8_t *codes, const uint8_t *scales, int64_t K, double *out)
+{
+    uint32_t st = 0;
+    for (int64_t b = 0; b < K / 32; ++b) {
+        unsigned s = scales[b];
+        double scale = 0.0;
+        if (ue8m0_valid(s)) scale = ldexp(1.0, (int)s - 127);
+        else st |= ORACLE_BAD_SCALE;
+        for (int64_t i = b * 32; i < b * 32 + 32; ++i) {
+            unsigned c = (codes[i / 4] >> (2 * (i % 4))) & 3u;
+            out[i] = oracle_code_value(c) * scale;
+        }
+    }
+    return st;
+}
+
+static double dot(const double *a, const double *b, int64_t n)
+{
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) s += a[i] * b[i];
+    return s;
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* y for the listed tokens.  x bf16 [T][H], ids/weights [T][k]; planes as in the
+ * C ABI; y_out bf16 [ntok][H]; h_out (nullable) bf16 [ntok][k][I]. */
+uint32_t oracle_forward_tokens(const uint16_t *x, const int32_t *ids, const float *weights,
+                               const uint8_t *w13_codes, const uint8_t *w13_scales,
+                               const uint8_t *w2_codes, const uint8_t *w2_scales,
+                               int32_t E, int32_t H, int32_t I, int32_t k,
+                               const int64_t *tokens, int64_t ntok, uint16_t *y_out, uint16_t *h_out)
+{
+    if (H % 32 || I % 32) return 0x80000000u;
+    uint32_t st = 0;
+    double *xt = malloc(sizeof(double) * H), *row = malloc(sizeof(double) * (H > I ? H : I));
+    double *h = malloc(sizeof(double) * I), *acc = malloc(sizeof(double) * H);
+    if (!xt || !row || !h || !acc) oracle_fail("malloc");
+    for (int64_t it = 0; it < ntok; ++it) {
+        int64_t t = tokens[it];
+        for (int32_t i = 0; i < H; ++i) xt[i] = oracle_bf16_to_double(x[t * H + i]);
+        for (int32_t m = 0; m < H; ++m) acc[m] = 0.0;
+        for (int32_t j = 0; j < k; ++j) {
+            int32_t e = ids[t * k + j];
+            if (h_out)
+                for (int32_t n = 0; n < I; ++n) h_out[(it * k + j) * (int64_t)I + n] = 0;
+            if (e < 0 || e >= E) {
+                st |= ORACLE_BAD_EXPERT_ID;
+                continue;
+            }
+            double w = (double)weights[t * k + j];
+            for (int32_t n = 0; n < I; ++n) {
+                int64_t rg = (int64_t)e * 2 * I + n, ru = (int64_t)e * 2 * I + I + n;
+                st |= dequant_row(w13_codes + rg * (H / 4), w13_scales + rg * (H / 32), H, row);
+                double g = dot(row, xt, H);
+                st |= dequant_row(w13_codes + ru * (H / 4), w13_scales + ru * (H / 32), H, row);
+                double u = dot(row, xt, H);
+                uint16_t hb = oracle_bf16_from_double(silu(g) * u);
+                h[n] = oracle_bf16_to_double(hb);
+                if (h_out) h_out[(it * k + j) * (int64_t)I + n] = hb;
+            }
+            for (int32_t m = 0; m < H; ++m) {
+                int64_t r = (int64_t)e * H + m;
+                st |= dequant_row(w2_codes + r * (I / 4), w2_scales + r * (I / 32), I, row);
+                acc[m] += w * dot(row, h, I);
+            }
+        }
+        for (int32_t m = 0; m < H; ++m) y_out[it * H + m] = oracle_bf16_from_double(acc[m]);
+    }
+    free(xt);
+    free(row);
+    free(h);
+    free(acc);
+    return st;
+}

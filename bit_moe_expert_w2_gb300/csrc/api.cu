@@ -1,0 +1,185 @@
+// C ABI of libmoe_w2: host-side validation, workspace layout and launch order.
+// The entry points only enqueue work on the caller's stream; nothing here
+// allocates, frees or synchronises.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe_w2 {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int32_t kPrefillTileRows = 256;   // tokens per prefill tile (tcgen05 N <= 256)
+
+int g_sm_count[kMaxDevices];
+int g_cc_ok[kMaxDevices];   // 0 = unknown, 1 = ok, 2 = not sm_103
+std::mutex g_mu;
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+moe_w2_status check_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_W2_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_cc_ok[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MOE_W2_ERR_CUDA;
+        g_sm_count[dev] = sms;
+        g_cc_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return g_cc_ok[dev] == 1 ? MOE_W2_OK : MOE_W2_ERR_DEVICE;
+}
+
+bool layer_shape_ok(int32_t E, int32_t H, int32_t I)
+{
+    return E >= 1 && E <= MOE_W2_MAX_EXPERTS && H >= 256 && I >= 256 && H % 256 == 0 && I % 256 == 0 &&
+           (int64_t)H * I <= ((int64_t)1 << 31);
+}
+
+}  // namespace
+
+int sm_count()
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+    int sms = 148;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
+int64_t max_prefill_tiles(int64_t P, int32_t E) { return P / kPrefillTileRows + E + 1; }
+
+Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I)
+{
+    Workspace w{};
+    const int64_t P = (int64_t)T * k;
+    const bool decode = T <= MOE_W2_DECODE_MAX_TOKENS;
+    char* p = static_cast<char*>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char* r = p ? p + off : nullptr;
+        off += align256(bytes);
+        return r;
+    };
+    w.sorted = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * P));
+    w.inv = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * P));
+    w.offsets = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (E + 1)));
+    w.active = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * E));
+    w.active_count = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * 2));
+    w.tile_count = w.active_count + 1;
+    w.tiles = decode ? nullptr : reinterpret_cast<int4*>(take(sizeof(int4) * max_prefill_tiles(P, E)));
+    w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * (decode ? (int64_t)T : P) * H));
+    w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
+    w.stage = decode ? nullptr : reinterpret_cast<float*>(take(sizeof(float) * P * H));
+    w.bytes = off;
+    return w;
+}
+
+}  // namespace moe_w2
+
+using namespace moe_w2;
+
+extern "C" {
+
+int moe_w2_version(void) { return (0 << 16) | 1; }
+
+const char* moe_w2_status_string(moe_w2_status s)
+{
+    switch (s) {
+        case MOE_W2_OK: return "ok";
+        case MOE_W2_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_W2_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case MOE_W2_ERR_WORKSPACE: return "workspace too small";
+        case MOE_W2_ERR_CUDA: return "CUDA error";
+        case MOE_W2_ERR_DEVICE: return "device is not compute capability 10.3";
+    }
+    return "unknown status";
+}
+
+size_t moe_w2_forward_workspace_size(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t I)
+{
+    if (T < 0 || top_k < 1 || top_k > MOE_W2_MAX_TOP_K || !layer_shape_ok(E, H, I)) return 0;
+    if ((int64_t)T * top_k > MOE_W2_MAX_PAIRS) return 0;
+    return carve_workspace(nullptr, T, top_k, E, H, I).bytes;
+}
+
+moe_w2_status moe_w2_permute(const int32_t* topk_ids, int32_t T, int32_t top_k, int32_t E, int32_t* sorted_pairs,
+                             int32_t* inv_pairs, int32_t* expert_offsets, uint32_t* dev_status, void* stream)
+{
+    if (T < 0 || top_k < 1 || top_k > MOE_W2_MAX_TOP_K || E < 1 || E > MOE_W2_MAX_EXPERTS)
+        return MOE_W2_ERR_INVALID_ARG;
+    if ((int64_t)T * top_k > MOE_W2_MAX_PAIRS) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
+    if (!expert_offsets || (T > 0 && (!topk_ids || !sorted_pairs || !inv_pairs))) return MOE_W2_ERR_INVALID_ARG;
+    moe_w2_status st = check_device();
+    if (st != MOE_W2_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_permute(topk_ids, T, top_k, E, sorted_pairs, inv_pairs, expert_offsets, nullptr, nullptr,
+                                   nullptr, nullptr, 1, nullptr, nullptr, 0, dev_status, s);
+    return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
+}
+
+moe_w2_status moe_w2_forward(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                             const moe_w2_planes* w, int32_t T, int32_t top_k, void* y_bf16, void* workspace,
+                             size_t workspace_bytes, uint32_t* dev_status, void* stream)
+{
+    if (!w || T < 0 || top_k < 1 || top_k > MOE_W2_MAX_TOP_K) return MOE_W2_ERR_INVALID_ARG;
+    if (w->num_experts < 1 || w->num_experts > MOE_W2_MAX_EXPERTS) return MOE_W2_ERR_INVALID_ARG;
+    if (!layer_shape_ok(w->num_experts, w->hidden, w->inter)) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)T * top_k > MOE_W2_MAX_PAIRS) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_W2_OK;
+    if (!x_bf16 || !topk_ids || !topk_weights || !y_bf16 || !workspace || !w->w13_codes || !w->w13_scales ||
+        !w->w2_codes || !w->w2_scales)
+        return MOE_W2_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MOE_W2_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x_bf16) & 15) != 0 || (reinterpret_cast<uintptr_t>(y_bf16) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(w->w13_codes) & 15) != 0 || (reinterpret_cast<uintptr_t>(w->w2_codes) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(w->w13_scales) & 7) != 0 || (reinterpret_cast<uintptr_t>(w->w2_scales) & 7) != 0)
+        return MOE_W2_ERR_INVALID_ARG;
+    const int32_t E = w->num_experts, H = w->hidden, I = w->inter;
+    Workspace ws = carve_workspace(workspace, T, top_k, E, H, I);
+    if (workspace_bytes < ws.bytes) return MOE_W2_ERR_WORKSPACE;
+    moe_w2_status st = check_device();
+    if (st != MOE_W2_OK) return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool decode = T <= MOE_W2_DECODE_MAX_TOKENS;
+    const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+    uint16_t* y = static_cast<uint16_t*>(y_bf16);
+    cudaError_t e = launch_permute(topk_ids, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active, ws.active_count,
+                                   ws.tiles, ws.tile_count, kPrefillTileRows, decode ? x : nullptr,
+                                   decode ? ws.xa : nullptr, H, dev_status, s);
+    if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
+    if (decode)
+        e = launch_decode(ws.xa, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s);
+    else
+        e = launch_prefill(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s);
+    return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
+}
+
+moe_w2_status moe_w2_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float* scale_2, int64_t n,
+                             int64_t rows, int64_t K, uint8_t* codes, uint8_t* ue8m0, uint32_t* dev_status,
+                             void* stream)
+{
+    if (n < 0 || rows < 0 || K < 0) return MOE_W2_ERR_INVALID_ARG;
+    if (K % 32 != 0) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
+    if (n == 0 || rows == 0 || K == 0) return MOE_W2_OK;
+    if (rows > ((int64_t)1 << 40) / K || n > ((int64_t)1 << 50) / (rows * K)) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
+    if (!e2m1 || !e4m3 || !scale_2 || !codes || !ue8m0) return MOE_W2_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(e2m1) & 15) != 0 || (reinterpret_cast<uintptr_t>(e4m3) & 1) != 0 ||
+        (reinterpret_cast<uintptr_t>(codes) & 7) != 0 || (reinterpret_cast<uintptr_t>(scale_2) & 3) != 0)
+        return MOE_W2_ERR_INVALID_ARG;
+    moe_w2_status st = check_device();
+    if (st != MOE_W2_OK) return st;
+    cudaError_t e = launch_requant(e2m1, e4m3, scale_2, n, rows, K, codes, ue8m0, dev_status,
+                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,237 @@
+// Routing permutation: stable counting sort of pairs p = t*k + j by expert id.
+//
+// vLLM-Moet, page "The v0.24.0 port", section "Our hooks", deterministic
+// unpermute bullet: valid sorted ids are a permutation of token*top_k+j, which
+// lets the combine be a bijective placement plus a fixed-order sum.
+//
+// One CTA of 1024 threads does the whole permutation: warp w owns a contiguous
+// slice of pairs; pass 1 counts per (warp, expert) in shared memory, a scan turns
+// the counts into per-(warp, expert) write cursors, pass 2 walks each slice in
+// order and writes every pair at its cursor (ranks within a 32-pair step come
+// from match_any), so the result is the stable order without any sort network.
+// The same launch also emits the active-expert list (decode scheduling) and the
+// prefill tile list.  Extra CTAs of the launch re-lay x in T16 order (decode).
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace moe_w2 {
+
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ uint32_t lanemask_lt()
+{
+    uint32_t r;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(r));
+    return r;
+}
+
+// Exclusive scan of one int per thread over the CTA; *total = sum of all.
+__device__ int cta_exclusive_scan(int v, int* warp_tmp, int* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tmp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_tmp[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_tmp[lane] = w;
+    }
+    __syncthreads();
+    int base = warp ? warp_tmp[warp - 1] : 0;
+    int t = warp_tmp[kWarps - 1];
+    __syncthreads();
+    if (total) *total = t;
+    return base + x - v;
+}
+
+// x [rows][H] -> x_t16 [rows][H]: 4x4 transpose inside each group of 16.
+__device__ __forceinline__ void t16_group(const uint16_t* src, uint16_t* dst)
+{
+    uint4 a = *reinterpret_cast<const uint4*>(src);
+    uint4 b = *reinterpret_cast<const uint4*>(src + 8);
+    // natural words: a.x=(x0,x1) a.y=(x2,x3) a.z=(x4,x5) a.w=(x6,x7) b.x=(x8,x9) ...
+    uint4 o, p;
+    o.x = __byte_perm(a.x, a.z, 0x5410);  // (x0, x4)
+    o.y = __byte_perm(b.x, b.z, 0x5410);  // (x8, x12)
+    o.z = __byte_perm(a.x, a.z, 0x7632);  // (x1, x5)
+    o.w = __byte_perm(b.x, b.z, 0x7632);  // (x9, x13)
+    p.x = __byte_perm(a.y, a.w, 0x5410);  // (x2, x6)
+    p.y = __byte_perm(b.y, b.w, 0x5410);  // (x10, x14)
+    p.z = __byte_perm(a.y, a.w, 0x7632);  // (x3, x7)
+    p.w = __byte_perm(b.y, b.w, 0x7632);  // (x11, x15)
+    *reinterpret_cast<uint4*>(dst) = o;
+    *reinterpret_cast<uint4*>(dst + 8) = p;
+}
+
+__global__ void __launch_bounds__(kThreads) permute_kernel(
+    const int32_t* __restrict__ ids, int32_t P, int32_t E, int32_t* __restrict__ sorted,
+    int32_t* __restrict__ inv, int32_t* __restrict__ offsets, int32_t* __restrict__ active,
+    int32_t* __restrict__ active_count, int4* __restrict__ tiles, int32_t* __restrict__ tile_count,
+    int32_t tile_rows, const uint16_t* __restrict__ x, uint16_t* __restrict__ x_t16, int64_t n_groups,
+    uint32_t* status)
+{
+    if (blockIdx.x > 0) {
+        const int64_t stride = (int64_t)(gridDim.x - 1) * blockDim.x;
+        for (int64_t g = (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x; g < n_groups; g += stride)
+            t16_group(x + g * 16, x_t16 + g * 16);
+        return;
+    }
+
+    extern __shared__ int32_t smem[];
+    __shared__ int warp_tmp[kWarps];
+    __shared__ int sh_total;
+    const int nb = E + 1;                 // bin E collects out-of-range ids
+    int32_t* cnt = smem;                  // [kWarps][nb] counts, then write cursors
+    int32_t* soff = smem + kWarps * nb;   // [nb] exclusive offsets
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (int i = tid; i < kWarps * nb; i += kThreads) cnt[i] = 0;
+    __syncthreads();
+
+    const int chunk = (((P + kWarps - 1) / kWarps) + 31) & ~31;
+    const int p0 = warp * chunk;
+    const int p1 = min(P, p0 + chunk);
+    uint32_t bad = 0;
+
+    // pass 1: counts per (warp, expert)
+    for (int pb = p0; pb < p1; pb += 32 * 8) {
+        int e[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            int p = pb + u * 32 + lane;
+            e[u] = (p < p1) ? __ldg(ids + p) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (pb + u * 32 + lane >= p1) continue;
+            int b = e[u];
+            if ((unsigned)b >= (unsigned)E) { b = E; bad = 1; }
+            atomicAdd(&cnt[warp * nb + b], 1);
+        }
+    }
+    __syncthreads();
+
+    // per-expert totals; cnt becomes the exclusive prefix over warps
+    for (int b = tid; b < nb; b += kThreads) {
+        int run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            int c = cnt[w * nb + b];
+            cnt[w * nb + b] = run;
+            run += c;
+        }
+        soff[b] = run;   // total for now
+    }
+    __syncthreads();
+
+    // scans over bins (two bins per thread covers nb <= 2048)
+    const int b0 = 2 * tid, b1 = 2 * tid + 1;
+    const int t0 = (b0 < nb) ? soff[b0] : 0, t1 = (b1 < nb) ? soff[b1] : 0;
+    int ex = cta_exclusive_scan(t0 + t1, warp_tmp, nullptr);
+    __syncthreads();
+    if (b0 < nb) { soff[b0] = ex; offsets[b0] = ex; }
+    if (b1 < nb) { soff[b1] = ex + t0; offsets[b1] = ex + t0; }
+
+    if (active != nullptr) {
+        const int f0 = (b0 < E && t0 > 0), f1 = (b1 < E && t1 > 0);
+        int ea = cta_exclusive_scan(f0 + f1, warp_tmp, &sh_total);
+        if (f0) active[ea] = b0;
+        if (f1) active[ea + f0] = b1;
+        if (tid == 0) *active_count = sh_total;
+    }
+
+    if (tiles != nullptr) {
+        const int n0 = (b0 < E) ? (t0 + tile_rows - 1) / tile_rows : 0;
+        const int n1 = (b1 < E) ? (t1 + tile_rows - 1) / tile_rows : 0;
+        int et = cta_exclusive_scan(n0 + n1, warp_tmp, &sh_total);
+        __syncthreads();   // soff writes above are visible
+        for (int i = 0; i < n0; ++i) {
+            int r0 = (int)(((int64_t)i * t0) / n0), r1 = (int)(((int64_t)(i + 1) * t0) / n0);
+            tiles[et + i] = make_int4(b0, soff[b0] + r0, r1 - r0, 0);
+        }
+        for (int i = 0; i < n1; ++i) {
+            int r0 = (int)(((int64_t)i * t1) / n1), r1 = (int)(((int64_t)(i + 1) * t1) / n1);
+            tiles[et + n0 + i] = make_int4(b1, soff[b1] + r0, r1 - r0, 0);
+        }
+        if (tid == 0) *tile_count = sh_total;
+    }
+    __syncthreads();
+
+    // write cursors = expert offset + prefix over earlier warps
+    for (int i = tid; i < kWarps * nb; i += kThreads) cnt[i] += soff[i % nb];
+    __syncthreads();
+
+    // pass 2: stable scatter
+    const uint32_t lt = lanemask_lt();
+    for (int pb = p0; pb < p1; pb += 32 * 8) {
+        int e[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            int p = pb + u * 32 + lane;
+            e[u] = (p < p1) ? __ldg(ids + p) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (pb + u * 32 >= p1) break;   // warp-uniform
+            const int p = pb + u * 32 + lane;
+            const bool valid = p < p1;
+            int b = e[u];
+            if (valid && (unsigned)b >= (unsigned)E) b = E;
+            const int key = valid ? b : (nb + lane);
+            const uint32_t mask = __match_any_sync(0xffffffffu, key);
+            const int rank = __popc(mask & lt);
+            int pos = 0;
+            if (valid) pos = cnt[warp * nb + b] + rank;
+            __syncwarp();
+            if (valid) {
+                sorted[pos] = p;
+                inv[p] = pos;
+                if (rank == 0) cnt[warp * nb + b] += __popc(mask);
+            }
+            __syncwarp();
+        }
+    }
+    if (bad) flag_status(status, MOE_W2_DEV_BAD_EXPERT_ID);
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* sorted, int32_t* inv,
+                           int32_t* offsets, int32_t* active, int32_t* active_count, int4* tiles,
+                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16,
+                           int32_t H, uint32_t* status, cudaStream_t s)
+{
+    const int32_t P = T * k;
+    const size_t smem = sizeof(int32_t) * (size_t)(kWarps + 1) * (E + 1);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(sizeof(int32_t) * (kWarps + 1) * (MOE_W2_MAX_EXPERTS + 1)));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    int64_t n_groups = 0;
+    int extra = 0;
+    if (x != nullptr && x_t16 != nullptr) {
+        n_groups = (int64_t)T * H / 16;
+        extra = (int)std::min<int64_t>((n_groups + kThreads - 1) / kThreads, 4 * (int64_t)sm_count());
+    }
+    permute_kernel<<<1 + extra, kThreads, smem, s>>>(ids, P, E, sorted, inv, offsets, active, active_count, tiles,
+                                                     tile_count, tile_rows, x, x_t16, n_groups, status);
+    return cudaGetLastError();
+}
+
+}  // namespace moe_w2

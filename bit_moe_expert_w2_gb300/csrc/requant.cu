@@ -1,0 +1,242 @@
+// Load-time re-quantizer: modelopt NVFP4 (e2m1 x e4m3 block-16 x fp32 scale_2)
+// -> sign-symmetric 2-bit codes + UE8M0 block-32 scales, bit-exact.
+//
+// vLLM-Moet, page "The v0.24.0 port", section "Our hooks", modelopt.py bullet:
+// dequantize to f64 exactly (all three factors representable), re-quantize to
+// the {-4,-1,1,4} codebook, UE8M0 block-32 output scales absorb scale_2.  The
+// scale is the least-squares one (page "vLLM-Moet wiki", section "2-bit expert
+// planes": the symmetric codebook is chosen at the same L2 error).
+//
+// Exact integer formulation used here (no floating point decides anything):
+//   |x_i| = N_i * 2^c with N_i = n1_i * Q_h * 2^(f_h - c) an integer, where
+//   n1 = 2|e2m1| in {0,1,2,3,4,6,8,12}, Q_h = e4m3 integer mantissa * scale_2
+//   integer mantissa, f_h the half-block's binary exponent.  For a candidate u,
+//   SSE(u) - sum x^2 = 4^u (32 + 15 A) - 2^(u+1) 2^c (S + 3 S4), where A counts
+//   the elements at magnitude 4 (|x| > 2.5 * 2^u) and S, S4 sum N over all /
+//   over those elements.  Scaled by 4^-e (e = min(c, lo)) both terms are
+//   integers below 2^112 and are compared in 128-bit arithmetic.
+// Candidate window: u in [floor(log2 min|x|) - 5, floor(log2 max|x|) + 1] clamped
+// to [-126, 125] holds the minimiser over all u (above it every code moves away
+// from every element; below it all nonzero elements saturate and the error grows
+// as u falls).  Ties go to the smaller u, an exact code tie to magnitude 1, and
+// the code's sign is the element's sign bit.
+//
+// All elements of a half-block share Q_h and f_h, so an element's threshold
+// depends only on its e2m1 magnitude class (7 nonzero classes per half): the
+// kernel counts classes once (SWAR over nibbles) and evaluates each candidate
+// over the 14 classes instead of the 32 elements.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace moe_w2 {
+
+namespace {
+
+__device__ __forceinline__ int n1_of_class(int v)
+{
+    // 2 * |e2m1| for magnitude bits v = 0..7: 0, 0.5, 1, 1.5, 2, 3, 4, 6
+    return (v < 4) ? v : (v == 4 ? 4 : (v == 5 ? 6 : (v == 6 ? 8 : 12)));
+}
+
+// Number of nibbles of w (low 3 bits) equal to v, for v in 1..7.
+__device__ __forceinline__ int count_class(uint32_t w, uint32_t v)
+{
+    const uint32_t t = (w & 0x77777777u) ^ (v * 0x11111111u);
+    const uint32_t z = ~(t + 0x77777777u) & 0x88888888u;
+    return __popc(z);
+}
+
+// 8 nibbles -> 8 two-bit codes (16 bits).  ge: bit 3 of each nibble = magnitude 4;
+// sg: bit 3 of each nibble = negative.
+__device__ __forceinline__ uint32_t pack_codes(uint32_t ge, uint32_t sg)
+{
+    uint32_t x = ((ge >> 3) & 0x11111111u) | ((sg >> 2) & 0x22222222u);
+    x = (x | (x >> 2)) & 0x0F0F0F0Fu;
+    x = (x | (x >> 4)) & 0x00FF00FFu;
+    x = (x | (x >> 8)) & 0x0000FFFFu;
+    return x;
+}
+
+__device__ __forceinline__ int floor_log2_u64(uint64_t v) { return 63 - __clzll((long long)v); }
+
+struct Half {
+    uint32_t Q;      // e4m3 integer mantissa * scale_2 integer mantissa (0 if the scale is 0)
+    int f;           // binary exponent of the unit of Q (|x| = n1 * Q * 2^f)
+    uint32_t neg;    // e4m3 sign
+    bool nan;
+};
+
+__device__ __forceinline__ Half decode_half(uint32_t b, uint32_t S, int es)
+{
+    Half h;
+    const uint32_t E4 = (b >> 3) & 15u, m = b & 7u;
+    h.nan = (E4 == 15u && m == 7u);
+    h.neg = (b >> 7) & 1u;
+    const uint32_t M = E4 ? (8u + m) : m;
+    const int e4 = E4 ? (int)E4 - 10 : -9;   // value = M * 2^e4
+    h.Q = M * S;
+    h.f = e4 + es - 1;                       // n1 = 2|e2m1| carries the extra factor 2
+    return h;
+}
+
+__global__ void __launch_bounds__(256) requant_kernel(const uint8_t* __restrict__ e2m1,
+                                                      const uint8_t* __restrict__ e4m3,
+                                                      const float* __restrict__ scale_2, int64_t n_blocks,
+                                                      int64_t blocks_per_tensor, uint8_t* __restrict__ codes,
+                                                      uint8_t* __restrict__ ue8m0, uint32_t* status)
+{
+    uint32_t bad_any = 0;
+    for (int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < n_blocks;
+         blk += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tensor = blk / blocks_per_tensor;
+        const uint32_t sbits = __float_as_uint(__ldg(scale_2 + tensor));
+        const uint4 nib = ldg_stream_u4(e2m1 + blk * 16);
+        const uint32_t sc = ldg_u16(e4m3 + blk * 2);
+
+        // scale_2 = S * 2^es
+        const uint32_t sE = (sbits >> 23) & 0xFFu, sM = sbits & 0x7FFFFFu;
+        const bool s2_bad = (sbits >> 31) != 0u || sE == 0xFFu || (sE == 0u && sM == 0u);
+        const uint32_t S = sE ? (sM | 0x800000u) : sM;
+        const int es = sE ? (int)sE - 150 : -149;
+
+        Half hf[2] = {decode_half(sc & 0xFFu, S, es), decode_half(sc >> 8, S, es)};
+        if (s2_bad || hf[0].nan || hf[1].nan) {
+            *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(0u, 0u);
+            ue8m0[blk] = 0;
+            bad_any = 1;
+            continue;
+        }
+
+        const uint32_t w[4] = {nib.x, nib.y, nib.z, nib.w};   // half 0 = w[0..1], half 1 = w[2..3]
+
+        // class counts per half, and the unit exponent c
+        int cntv[2][8];
+        bool any[2];
+        for (int h = 0; h < 2; ++h) {
+            int tot = 0;
+#pragma unroll
+            for (int v = 1; v < 8; ++v) {
+                cntv[h][v] = count_class(w[2 * h], v) + count_class(w[2 * h + 1], v);
+                tot += cntv[h][v];
+            }
+            any[h] = tot > 0 && hf[h].Q != 0u;
+        }
+
+        int u;
+        int v0[2] = {8, 8};   // smallest magnitude class at magnitude 4, per half
+        if (!any[0] && !any[1]) {
+            u = -126;
+        } else {
+            const int c = (any[0] && any[1]) ? min(hf[0].f, hf[1].f) : (any[0] ? hf[0].f : hf[1].f);
+            uint64_t Qs[2];
+            uint64_t nmax = 0, nmin = ~0ull;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                Qs[h] = any[h] ? ((uint64_t)hf[h].Q << (hf[h].f - c)) : 0ull;
+                if (!any[h]) continue;
+                int vmax = 0, vmin = 8;
+#pragma unroll
+                for (int v = 7; v >= 1; --v)
+                    if (cntv[h][v] && vmax == 0) vmax = v;
+#pragma unroll
+                for (int v = 1; v < 8; ++v)
+                    if (cntv[h][v] && vmin == 8) vmin = v;
+                nmax = max(nmax, (uint64_t)n1_of_class(vmax) * Qs[h]);
+                nmin = min(nmin, (uint64_t)n1_of_class(vmin) * Qs[h]);
+            }
+            const int m = floor_log2_u64(nmax) + c, mlo = floor_log2_u64(nmin) + c;
+            int hi = min(125, max(-126, m + 1));
+            int lo = min(hi, max(-126, mlo - 5));
+            if (lo == hi) {
+                u = lo;
+            } else {
+                const int eref = min(c, lo);
+                const int C1 = c - eref + 1;   // |x| > 2.5*2^u  <=>  N << C1 > 5 << (u - eref)
+                uint64_t S_all = 0;
+                uint64_t Nc[2][8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int v = 1; v < 8; ++v) {
+                        Nc[h][v] = (uint64_t)n1_of_class(v) * Qs[h];
+                        S_all += (uint64_t)cntv[h][v] * Nc[h][v];
+                    }
+                __int128 best = 0;
+                int best_u = lo;
+                for (int cand = lo; cand <= hi; ++cand) {
+                    const int U = cand - eref;
+                    const uint64_t R = 5ull << U;
+                    int A = 0;
+                    uint64_t S4 = 0;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int v = 1; v < 8; ++v)
+                            if ((Nc[h][v] << C1) > R) {
+                                A += cntv[h][v];
+                                S4 += (uint64_t)cntv[h][v] * Nc[h][v];
+                            }
+                    const __int128 t1 = (__int128)(32 + 15 * A) << (2 * U);
+                    const __int128 t2 = (__int128)(S_all + 3 * S4) << (U + C1);
+                    const __int128 G = t1 - t2;
+                    if (cand == lo || G < best) {
+                        best = G;
+                        best_u = cand;
+                    }
+                }
+                u = best_u;
+            }
+            // magnitude-4 classes at the chosen u
+            if (u - min(c, u) <= 60) {
+                const int eref = min(c, u);
+                const int C1 = c - eref + 1;
+                const uint64_t R = 5ull << (u - eref);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (!any[h]) continue;
+                    int vv = 8;
+#pragma unroll
+                    for (int v = 7; v >= 1; --v)
+                        if ((((uint64_t)n1_of_class(v) * Qs[h]) << C1) > R) vv = v;
+                    v0[h] = vv;
+                }
+            }
+        }
+
+        // codes: magnitude 4 iff class >= v0, sign = e2m1 sign xor e4m3 sign
+        uint32_t out[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            uint32_t half16[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int wi = 2 * q + j, h = q;
+                const uint32_t ww = w[wi];
+                const uint32_t ge = ((ww & 0x77777777u) + (uint32_t)(8 - v0[h]) * 0x11111111u) & 0x88888888u;
+                const uint32_t sg = (ww ^ (hf[h].neg ? 0x88888888u : 0u)) & 0x88888888u;
+                half16[j] = pack_codes(ge, sg);
+            }
+            out[q] = half16[0] | (half16[1] << 16);
+        }
+        *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(out[0], out[1]);
+        ue8m0[blk] = (uint8_t)(u + 127);
+    }
+    if (bad_any) flag_status(status, MOE_W2_DEV_BAD_NVFP4);
+}
+
+}  // namespace
+
+cudaError_t launch_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float* scale_2, int64_t n, int64_t rows,
+                           int64_t K, uint8_t* codes, uint8_t* ue8m0, uint32_t* status, cudaStream_t s)
+{
+    const int64_t bpt = rows * (K / 32);
+    const int64_t nb = n * bpt;
+    if (nb == 0) return cudaSuccess;
+    const int64_t want = (nb + 255) / 256;
+    const int grid = (int)std::min<int64_t>(want, (int64_t)sm_count() * 8);
+    requant_kernel<<<grid, 256, 0, s>>>(e2m1, e4m3, scale_2, nb, bpt, codes, ue8m0, status);
+    return cudaGetLastError();
+}
+
+}  // namespace moe_w2

@@ -19,8 +19,9 @@ section "Our hooks"):
 Recipe (all numpy PCG64 via ``default_rng(seed)``):
   * activations: standard normal fp32, rounded to bf16 (round to nearest even);
     returned as the uint16 bit pattern.
-  * code planes: uniform random bytes (every 2-bit field is then uniform over the
-    four codes and independent); UE8M0 scale bytes 127 + integers(lo, hi+1).
+  * code planes: uniform random bytes (raw PCG64 words read as little-endian
+    bytes; every 2-bit field is then uniform over the four codes and
+    independent); UE8M0 scale bytes 127 + integers(lo, hi+1) drawn as uint8.
   * router "logits": standard normal (T, E) fp32, top-k by value with ties to the
     lower id, weights = softmax over the k selected logits.
   * router "zipf": expert popularity p_r proportional to r^-1.1 (r = 1..E), rank r
@@ -84,8 +85,10 @@ def rng_for(seed: int) -> np.random.Generator:
 
 
 def random_bytes(rng: np.random.Generator, shape) -> np.ndarray:
+    """Uniform random bytes: raw 64-bit PCG64 outputs read as little-endian bytes."""
     n = int(np.prod(shape))
-    return np.frombuffer(rng.bytes(n), dtype=np.uint8).reshape(shape).copy()
+    words = rng.bit_generator.random_raw((n + 7) // 8)
+    return words.view(np.uint8)[:n].reshape(shape)
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -99,12 +102,17 @@ def activations(rng: np.random.Generator, T: int, H: int) -> np.ndarray:
     return f32_to_bf16_bits(rng.standard_normal((T, H), dtype=np.float32))
 
 
+def ue8m0_bytes(rng: np.random.Generator, shape, exp_lo: int, exp_hi: int) -> np.ndarray:
+    """UE8M0 bytes 127 + e with e uniform over [exp_lo, exp_hi]."""
+    return rng.integers(127 + exp_lo, 127 + exp_hi + 1, size=shape, dtype=np.uint8)
+
+
 def code_planes(rng: np.random.Generator, E: int, H: int, I: int, exp_lo: int, exp_hi: int):
     """Random 2-bit expert planes: codes uniform over the four codes, exponents uniform."""
     w13_codes = random_bytes(rng, (E, 2 * I, H // 4))
-    w13_scales = (127 + rng.integers(exp_lo, exp_hi + 1, size=(E, 2 * I, H // 32))).astype(np.uint8)
+    w13_scales = ue8m0_bytes(rng, (E, 2 * I, H // 32), exp_lo, exp_hi)
     w2_codes = random_bytes(rng, (E, H, I // 4))
-    w2_scales = (127 + rng.integers(exp_lo, exp_hi + 1, size=(E, H, I // 32))).astype(np.uint8)
+    w2_scales = ue8m0_bytes(rng, (E, H, I // 32), exp_lo, exp_hi)
     return {"w13_codes": w13_codes, "w13_scales": w13_scales,
             "w2_codes": w2_codes, "w2_scales": w2_scales}
 
@@ -188,16 +196,14 @@ def _e4m3_positive_table():
 
 
 def e4m3_round_positive(v: np.ndarray) -> np.ndarray:
-    """Nearest positive normal e4m3fn byte to each value in [2^-6, 448] (ties: even mantissa)."""
-    vals, codes = _e4m3_positive_table()
+    """Nearest positive normal e4m3fn byte to each value in [2^-6, 448) (ties: even mantissa)."""
     v = np.asarray(v, dtype=np.float64)
-    hi = np.clip(np.searchsorted(vals, v, side="left"), 1, len(vals) - 1)
-    lo = hi - 1
-    dlo, dhi = v - vals[lo], vals[hi] - v
-    pick_hi = (dhi < dlo) | ((dhi == dlo) & ((codes[hi] & 1) == 0))
-    out = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
-    exact = v == vals[hi]
-    return np.where(exact, codes[hi], out).astype(np.uint8)
+    f, e = np.frexp(v)                      # v = f * 2^e, f in [0.5, 1)
+    m = np.rint((2.0 * f - 1.0) * 8.0)      # 3 mantissa bits of 1.m, ties to even
+    carry = m == 8.0
+    m = np.where(carry, 0.0, m).astype(np.int32)
+    ef = (e - 1 + 7 + carry).astype(np.int32)   # biased exponent field
+    return ((ef << 3) | m).astype(np.uint8)
 
 
 @dataclasses.dataclass

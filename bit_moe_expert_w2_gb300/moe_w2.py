@@ -1,0 +1,162 @@
+"""Python binding of libmoe_w2 (ctypes).  Argument marshalling only.
+
+Every step of the layer runs in the CUDA library: this module checks tensor
+shapes and dtypes, allocates outputs and workspace with torch when the caller
+did not, passes raw device pointers and the current CUDA stream, and turns a
+non-zero status into an exception.  There is no fallback: if the library is
+missing or the device is not sm_103, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+OK = 0
+DEV_BAD_EXPERT_ID = 1
+DEV_BAD_SCALE = 2
+DEV_BAD_NVFP4 = 4
+DECODE_MAX_TOKENS = 64
+
+
+class MoeW2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class Planes(ctypes.Structure):
+    _fields_ = [("w13_codes", ctypes.c_void_p), ("w13_scales", ctypes.c_void_p),
+                ("w2_codes", ctypes.c_void_p), ("w2_scales", ctypes.c_void_p),
+                ("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32)]
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libmoe_w2.so (building it first if it is missing and nvcc is present)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build()")
+        _build.build()
+    L = ctypes.CDLL(path)
+    vp, i32, i64, u32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_size_t
+    L.moe_w2_version.restype = ctypes.c_int
+    L.moe_w2_status_string.argtypes = [ctypes.c_int]
+    L.moe_w2_status_string.restype = ctypes.c_char_p
+    L.moe_w2_forward_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.moe_w2_forward_workspace_size.restype = sz
+    L.moe_w2_permute.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
+    L.moe_w2_permute.restype = ctypes.c_int
+    L.moe_w2_forward.argtypes = [vp, vp, vp, ctypes.POINTER(Planes), i32, i32, vp, vp, sz, vp, vp]
+    L.moe_w2_forward.restype = ctypes.c_int
+    L.moe_w2_requant.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
+    L.moe_w2_requant.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return load().moe_w2_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_cuda(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def make_planes(planes: dict) -> Planes:
+    """Planes struct from the four uint8 CUDA tensors w13_codes [E][2I][H/4], w13_scales [E][2I][H/32],
+    w2_codes [E][H][I/4], w2_scales [E][H][I/32]."""
+    for k in ("w13_codes", "w13_scales", "w2_codes", "w2_scales"):
+        _check_cuda(planes[k], k, torch.uint8)
+    E, two_i, h4 = planes["w13_codes"].shape
+    return Planes(planes["w13_codes"].data_ptr(), planes["w13_scales"].data_ptr(),
+                  planes["w2_codes"].data_ptr(), planes["w2_scales"].data_ptr(), E, h4 * 4, two_i // 2)
+
+
+def workspace_size(T: int, top_k: int, E: int, H: int, I: int) -> int:
+    return int(load().moe_w2_forward_workspace_size(T, top_k, E, H, I))
+
+
+def forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, planes, y=None,
+            workspace=None, status=None, stream=None) -> torch.Tensor:
+    """y = MoE layer(x) through moe_w2_forward.  x bf16 [T][H], ids int32 [T][k], weights f32 [T][k]."""
+    L = load()
+    _check_cuda(x, "x", torch.bfloat16)
+    _check_cuda(topk_ids, "topk_ids", torch.int32)
+    _check_cuda(topk_weights, "topk_weights", torch.float32)
+    p = planes if isinstance(planes, Planes) else make_planes(planes)
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    need = workspace_size(T, k, p.num_experts, p.hidden, p.inter)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    st = L.moe_w2_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), ctypes.byref(p), T, k, _ptr(y),
+                          _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    if st != OK:
+        raise MoeW2Error(st, "moe_w2_forward")
+    return y
+
+
+def permute(topk_ids: torch.Tensor, E: int, status=None, stream=None):
+    """(sorted_pairs, inv_pairs, expert_offsets) through moe_w2_permute."""
+    L = load()
+    _check_cuda(topk_ids, "topk_ids", torch.int32)
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    sorted_pairs = torch.empty(T * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    st = L.moe_w2_permute(_ptr(topk_ids), T, k, E, _ptr(sorted_pairs), _ptr(inv), _ptr(offsets), _ptr(status),
+                          _stream(stream))
+    if st != OK:
+        raise MoeW2Error(st, "moe_w2_permute")
+    return sorted_pairs, inv, offsets
+
+
+def requant(e2m1: torch.Tensor, e4m3: torch.Tensor, scale_2: torch.Tensor, codes=None, ue8m0=None,
+            status=None, stream=None):
+    """NVFP4 [n][rows][K/2] + [n][rows][K/16] + [n] -> (codes [n][rows][K/4], ue8m0 [n][rows][K/32])."""
+    L = load()
+    _check_cuda(e2m1, "e2m1", torch.uint8)
+    _check_cuda(e4m3, "e4m3", torch.uint8)
+    _check_cuda(scale_2, "scale_2", torch.float32)
+    n, rows, half_k = e2m1.shape
+    K = half_k * 2
+    if codes is None:
+        codes = torch.empty((n, rows, K // 4), dtype=torch.uint8, device=e2m1.device)
+    if ue8m0 is None:
+        ue8m0 = torch.empty((n, rows, K // 32), dtype=torch.uint8, device=e2m1.device)
+    st = L.moe_w2_requant(_ptr(e2m1), _ptr(e4m3), _ptr(scale_2), n, rows, K, _ptr(codes), _ptr(ue8m0),
+                          _ptr(status), _stream(stream))
+    if st != OK:
+        raise MoeW2Error(st, "moe_w2_requant")
+    return codes, ue8m0

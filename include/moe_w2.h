@@ -1,0 +1,157 @@
+/*
+ * moe_w2 — routed-expert MoE layer with 2-bit sign-symmetric expert weights,
+ * for NVIDIA GB300 (sm_103a).  C ABI: plain pointers, sizes and a CUDA stream.
+ *
+ * What the library computes (vLLM-Moet pages):
+ *   - "vLLM-Moet wiki", section "2-bit expert planes": routed experts stored as
+ *     2-bit codes from the sign-symmetric codebook {-4,-1,1,4};
+ *   - "vLLM-Moet wiki", section "The kernels": the 2-bit MoE GEMM (in-register
+ *     code expansion feeding tensor cores), deterministic, graph-capture safe;
+ *   - "The v0.24.0 port", section "Our hooks": moe_w2_forward in the quant
+ *     method's apply hook; the modelopt NVFP4 loader that dequantizes
+ *     e2m1 x e4m3 block-16 x scale_2 exactly in f64 and re-quantizes to the
+ *     codebook with UE8M0 block-32 scales absorbing scale_2; codes + UE8M0
+ *     scales as four sections per expert slot; the deterministic unpermute
+ *     (bijective per-pair placement + fixed-order sum over top_k).
+ *
+ * Plane format (the four sections per expert):
+ *   w13_codes  uint8 [E][2I][H/4]   rows 0..I-1 = gate, rows I..2I-1 = up
+ *   w13_scales uint8 [E][2I][H/32]
+ *   w2_codes   uint8 [E][H][I/4]    down projection
+ *   w2_scales  uint8 [E][H][I/32]
+ *   Weight (r, kk) = code_value(c) * 2^(s - 127) with
+ *     c = (codes[r][kk/4] >> (2*(kk%4))) & 3, code_value = {+1, +4, -1, -4}[c]
+ *     (c = sign<<1 | magnitude), s = scales[r][kk/32] in [1, 252].
+ *
+ * Conventions for every entry point:
+ *   - Every buffer is owned by the caller and lives in device memory unless
+ *     stated otherwise.  The library allocates nothing, frees nothing and
+ *     never synchronises: work is enqueued on `stream` (a cudaStream_t, NULL =
+ *     the legacy default stream) and completes asynchronously.  No entry point
+ *     reads a device value on the host, so all of them can be captured in a
+ *     CUDA graph.
+ *   - Host-side argument checks return a status code and enqueue nothing.
+ *   - Device-side input errors never trap: they OR a bit into *dev_status
+ *     (a device uint32 the caller zeroes and reads back; NULL = do not report)
+ *     and the offending contribution is replaced as documented per bit.
+ *   - Results are deterministic: identical inputs give bitwise identical outputs.
+ *   - Requires a device of compute capability 10.3 (GB300).
+ */
+#ifndef MOE_W2_H
+#define MOE_W2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_W2_OK = 0,
+    MOE_W2_ERR_INVALID_ARG = 1,       /* null pointer, negative size, top_k or E out of range */
+    MOE_W2_ERR_UNSUPPORTED_SHAPE = 2, /* H or I not a multiple of 256, K not a multiple of 32, too many pairs */
+    MOE_W2_ERR_WORKSPACE = 3,         /* workspace smaller than moe_w2_forward_workspace_size() */
+    MOE_W2_ERR_CUDA = 4,              /* a CUDA call or kernel launch failed (cudaGetLastError) */
+    MOE_W2_ERR_DEVICE = 5             /* the current device is not compute capability 10.3 */
+} moe_w2_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define MOE_W2_DEV_BAD_EXPERT_ID 1u   /* topk id outside [0,E): that pair contributes 0 */
+#define MOE_W2_DEV_BAD_SCALE 2u       /* UE8M0 byte outside [1,252] in a plane: that block counts as 0 */
+#define MOE_W2_DEV_BAD_NVFP4 4u       /* requant input: e4m3 NaN in a block, or scale_2 not a positive
+                                         finite number: the block's codes are 0x00 and its scale byte 0 */
+
+/* Limits checked on the host. */
+#define MOE_W2_MAX_EXPERTS 1024
+#define MOE_W2_MAX_TOP_K 16
+#define MOE_W2_MAX_PAIRS (1 << 21)    /* T * top_k */
+#define MOE_W2_DECODE_MAX_TOKENS 64   /* T <= 64 runs the decode kernels, larger T the prefill kernels */
+
+/* Device pointers to one layer's planes (layout above). */
+typedef struct {
+    const uint8_t *w13_codes;
+    const uint8_t *w13_scales;
+    const uint8_t *w2_codes;
+    const uint8_t *w2_scales;
+    int32_t num_experts; /* E */
+    int32_t hidden;      /* H, multiple of 256 */
+    int32_t inter;       /* I, multiple of 256 */
+} moe_w2_planes;
+
+/* Bytes of device workspace moe_w2_forward needs for these sizes (0 if the sizes
+ * are invalid).  The workspace holds the permutation, the expert-sorted and
+ * re-laid-out activations, the SiLU(gate)*up intermediate h (bf16, P x I) and,
+ * for T > MOE_W2_DECODE_MAX_TOKENS, the fp32 per-pair staging of the
+ * deterministic combine (P x H).  Its contents need no initialisation. */
+size_t moe_w2_forward_workspace_size(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t I);
+
+/*
+ * Routing permutation ("The v0.24.0 port", "Our hooks", deterministic
+ * unpermute bullet: valid sorted ids are a permutation of token*top_k+j).
+ *   topk_ids       int32 [T][top_k]   expert of pair p = t*top_k + j
+ *   sorted_pairs   int32 [T*top_k]    pair ids grouped by expert: expert 0's pairs
+ *                                     in increasing p, then expert 1's, ...; pairs
+ *                                     with an id outside [0,E) come last (in
+ *                                     increasing p) and set MOE_W2_DEV_BAD_EXPERT_ID
+ *   inv_pairs      int32 [T*top_k]    inv_pairs[sorted_pairs[q]] = q
+ *   expert_offsets int32 [E+1]        first slot of each expert; [E] = valid pairs
+ * T = 0 is a no-op.  Bit-exact and deterministic (a stable counting sort).
+ */
+moe_w2_status moe_w2_permute(const int32_t *topk_ids, int32_t T, int32_t top_k, int32_t E,
+                             int32_t *sorted_pairs, int32_t *inv_pairs, int32_t *expert_offsets,
+                             uint32_t *dev_status, void *stream);
+
+/*
+ * Routed-expert forward ("vLLM-Moet wiki", "The kernels"; "The v0.24.0 port",
+ * "Our hooks"): for every token t and slot j with e = topk_ids[t][j],
+ *     g = W_gate[e] x_t,  u = W_up[e] x_t            (fp32 accumulation)
+ *     h = bf16(SiLU(g) * u)
+ *     y_t = bf16( sum_j topk_weights[t][j] * (W_down[e] h) )   (fp32)
+ *   x_bf16        bf16 [T][H]
+ *   topk_ids      int32 [T][top_k]
+ *   topk_weights  float [T][top_k]
+ *   w             host pointer to the plane pointers (read during the call only)
+ *   y_bf16        bf16 [T][H] (written; may not alias x)
+ *   workspace     device buffer of at least moe_w2_forward_workspace_size() bytes,
+ *                 256-byte aligned, used by this call until it completes on `stream`
+ * T = 0 is a no-op.  Pairs with an id outside [0,E) contribute 0
+ * (MOE_W2_DEV_BAD_EXPERT_ID); blocks with a UE8M0 byte outside [1,252] count
+ * as 0 (MOE_W2_DEV_BAD_SCALE).  T <= 64 uses the decode kernels (CUDA cores +
+ * mma.sync, planes streamed once per active expert); larger T the prefill
+ * kernels (TMA + tcgen05 with accumulators in tensor memory).
+ */
+moe_w2_status moe_w2_forward(const void *x_bf16, const int32_t *topk_ids, const float *topk_weights,
+                             const moe_w2_planes *w, int32_t T, int32_t top_k, void *y_bf16,
+                             void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream);
+
+/*
+ * Load-time re-quantizer ("The v0.24.0 port", "Our hooks", modelopt.py
+ * bullet): modelopt NVFP4 tensors -> 2-bit planes.
+ *   e2m1     uint8 [n][rows][K/2]   two e2m1 nibbles per byte, low nibble = even element
+ *   e4m3     uint8 [n][rows][K/16]  e4m3fn block-16 scales
+ *   scale_2  float [n]              per-tensor scale (device memory)
+ *   codes    uint8 [n][rows][K/4]   output codes (plane format above)
+ *   ue8m0    uint8 [n][rows][K/32]  output UE8M0 bytes, s = u + 127
+ * Per block of 32 consecutive elements x_i = e2m1_i * e4m3 * scale_2 (exact),
+ * the output is the u in [-126,125] minimising sum_i (x_i - v_i 2^u)^2 exactly,
+ * with every v_i the nearest of {-4,-1,1,4} (|x| > 2.5*2^u -> magnitude 4, else
+ * 1; the code's sign is x's sign bit, so -0 -> -1); ties between scales go to
+ * the smaller u.  Bit-exact.  Invalid blocks: see MOE_W2_DEV_BAD_NVFP4.
+ * K must be a multiple of 32; n*rows*K/32 blocks must fit in int64.
+ */
+moe_w2_status moe_w2_requant(const uint8_t *e2m1, const uint8_t *e4m3, const float *scale_2,
+                             int64_t n, int64_t rows, int64_t K, uint8_t *codes, uint8_t *ue8m0,
+                             uint32_t *dev_status, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *moe_w2_status_string(moe_w2_status s);
+
+/* Library version, (major << 16) | minor. */
+int moe_w2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_W2_H */

@@ -1,0 +1,56 @@
+"""The C ABI library builds, loads and exports every entry point declared in
+include/moe_w2.h; host-side argument checks answer without a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+from bit_moe_expert_w2_gb300 import moe_w2
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe_w2.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_w2_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    L = moe_w2.load()
+    names = _declared()
+    assert {"moe_w2_forward", "moe_w2_permute", "moe_w2_requant", "moe_w2_forward_workspace_size"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version():
+    L = moe_w2.load()
+    assert L.moe_w2_version() >= 1
+    for s in range(6):
+        assert moe_w2.status_string(s)
+
+
+def test_workspace_size_rules():
+    assert moe_w2.workspace_size(1, 8, 256, 6144, 2048) > 0
+    assert moe_w2.workspace_size(8192, 8, 256, 4096, 2048) > 8192 * 8 * 4096 * 4   # fp32 staging
+    assert moe_w2.workspace_size(4, 2, 8, 500, 256) == 0      # H not a multiple of 256
+    assert moe_w2.workspace_size(4, 17, 8, 512, 256) == 0     # top_k > 16
+    assert moe_w2.workspace_size(4, 2, 2000, 512, 256) == 0   # E > 1024
+    assert moe_w2.workspace_size(-1, 2, 8, 512, 256) == 0
+
+
+def test_host_validation_without_device():
+    L = moe_w2.load()
+    p = moe_w2.Planes(0, 0, 0, 0, 8, 512, 256)
+    # null planes pointer, bad top_k, bad shape: rejected on the host
+    assert L.moe_w2_forward(None, None, None, None, 1, 2, None, None, 0, None, None) == 1
+    assert L.moe_w2_forward(None, None, None, ctypes.byref(p), 1, 0, None, None, 0, None, None) == 1
+    bad = moe_w2.Planes(0, 0, 0, 0, 8, 500, 256)
+    assert L.moe_w2_forward(None, None, None, ctypes.byref(bad), 1, 2, None, None, 0, None, None) == 2
+    # T = 0 is a no-op
+    assert L.moe_w2_forward(None, None, None, ctypes.byref(p), 0, 2, None, None, 0, None, None) == 0
+    # requant: K not a multiple of 32, and the empty call
+    assert L.moe_w2_requant(None, None, None, 1, 1, 48, None, None, None, None) == 2
+    assert L.moe_w2_requant(None, None, None, 0, 4, 64, None, None, None, None) == 0
+    # permute: top_k out of range
+    assert L.moe_w2_permute(None, 4, 0, 8, None, None, None, None, None) == 1

@@ -1,0 +1,103 @@
+"""GPU parity of the decode path (T <= 64) of moe_w2_forward against the oracle.
+
+Bar: relative L2 <= 1e-3 and max abs <= 1e-2 * max|oracle| on the layer output
+(bf16), over every token for the small and single-token cases and over sampled
+tokens at T = 32; repeated runs must be bitwise identical.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_moe_expert_w2_gb300 import inputs, moe_w2
+from tests.helpers import assert_close_layer, from_dev_bf16, planes_to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(lay: inputs.LayerInputs, planes_dev=None, ids=None, weights=None):
+    planes_dev = planes_dev or planes_to_dev(lay.planes)
+    ids = lay.ids if ids is None else ids
+    weights = lay.weights if weights is None else weights
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = moe_w2.forward(to_dev_bf16(lay.x), torch.from_numpy(ids).cuda(), torch.from_numpy(weights).cuda(),
+                       planes_dev, status=st)
+    return from_dev_bf16(y), int(st.item())
+
+
+def test_tiny_config_all_tokens():
+    lay = inputs.layer_inputs(inputs.CONFIGS["tiny"])
+    y, st = _run(lay)
+    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes)
+    assert st == rst == 0
+    assert_close_layer(y, ref, "tiny")
+
+
+@pytest.mark.parametrize("H,I,E,k,T,seed", [(256, 256, 4, 1, 1, 1), (512, 256, 8, 2, 3, 2), (768, 512, 16, 4, 17, 3),
+                                            (1024, 768, 8, 8, 64, 4), (512, 512, 2, 2, 64, 5),
+                                            (256, 1024, 64, 16, 40, 6)])
+def test_small_shapes_all_tokens(H, I, E, k, T, seed):
+    # (512,512,2,2,64): each expert gets ~64 pairs -> several 32-pair passes
+    lay = inputs.small_layer_inputs(H, I, E, k, T, seed)
+    y, st = _run(lay)
+    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes)
+    assert st == rst == 0
+    assert_close_layer(y, ref, f"H{H} I{I} E{E} k{k} T{T}")
+
+
+def test_duplicates_invalid_ids_and_zero_weights():
+    lay = inputs.small_layer_inputs(512, 256, 8, 4, 6, 11)
+    ids = lay.ids.copy()
+    w = lay.weights.copy()
+    ids[0] = [3, 3, 3, 1]          # the same expert three times
+    ids[1, 2] = -1                  # invalid -> contributes 0
+    ids[2, 0] = 8
+    w[3, :] = 0.0                   # a token with all-zero weights
+    y, st = _run(lay, ids=ids, weights=w)
+    ref, rst = oracle.forward_tokens(lay.x, ids, w, lay.planes)
+    assert st == rst == moe_w2.DEV_BAD_EXPERT_ID
+    assert_close_layer(y, ref, "duplicates/invalid")
+    assert np.all(y[3] == 0)
+
+
+def test_bad_scale_bytes_zero_their_blocks():
+    lay = inputs.small_layer_inputs(512, 256, 4, 2, 4, 12)
+    planes = {k: v.copy() for k, v in lay.planes.items()}
+    planes["w13_scales"][1, 5, 3] = 0
+    planes["w2_scales"][2, 7, 1] = 255
+    planes["w2_scales"][0, 100, 0] = 253
+    y, st = _run(lay, planes_dev=planes_to_dev(planes))
+    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, planes)
+    assert rst == moe_w2.DEV_BAD_SCALE
+    assert st & moe_w2.DEV_BAD_SCALE
+    assert_close_layer(y, ref, "bad scales")
+
+
+@pytest.fixture(scope="module")
+def decode_t32():
+    lay = inputs.layer_inputs(inputs.CONFIGS["decode_t32"])
+    return lay, planes_to_dev(lay.planes)
+
+
+def test_decode_t1_full_size():
+    lay = inputs.layer_inputs(inputs.CONFIGS["decode_t1"])
+    y, st = _run(lay)
+    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes)
+    assert st == rst == 0
+    assert_close_layer(y, ref, "decode T=1")
+
+
+def test_decode_t32_full_size_sampled(decode_t32):
+    lay, pd = decode_t32
+    y, st = _run(lay, planes_dev=pd)
+    tokens = np.array([0, 13, 31])
+    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes, tokens=tokens)
+    assert st == rst == 0
+    assert_close_layer(y[tokens], ref, "decode T=32")
+
+
+def test_decode_deterministic_repeats(decode_t32):
+    lay, pd = decode_t32
+    ys = [_run(lay, planes_dev=pd)[0] for _ in range(6)]
+    for y in ys[1:]:
+        assert np.array_equal(y, ys[0])

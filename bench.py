@@ -1,0 +1,518 @@
+#!/usr/bin/env python
+"""Benchmark of the 2-bit MoE layer (moe_w2_forward) and the NVFP4 re-quantizer.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Default workload: decode_t1 (H=6144, I=2048, E=256, top-8, T=1, Zipf(1.1)
+routing), the single-token decode step.  One step = one moe_w2_forward of one
+batch: permutation, gate_up with SiLU*up, down with the weighted combine.
+
+Timing: inputs are resident in HBM; every step replays a captured CUDA graph of
+the forward whose phase events (moe_w2_forward_traced) give the step time and
+the time of each kernel; L2 is flushed (a 512 MiB write) before every step,
+outside the timed events.  Routings rotate over a pool, so consecutive steps
+touch different experts.  "e2e" times the same call with the step's inputs
+copied from pinned host memory and y copied back inside the timed events.
+
+--impl reference runs the CPU oracle (plain single-threaded C) on a bounded
+sample of the same workload on this host; it never touches the GPU.
+Multi-GPU (torchrun): independent replicas, one per GPU (the layer has no
+cross-GPU step on one box); value = all ranks' tokens / slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from bit_moe_expert_w2_gb300 import inputs  # noqa: E402
+
+METRIC = "w2 MoE layer tokens/s; plane HBM GB/s (decode), TFLOP/s (prefill) vs peak"
+DEFAULT_CONFIG = "decode_t1"
+POOL = 16
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def file_sha(rel: str) -> str:
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None if
+    the summary is missing or the kernel's source changed since the capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            d = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    if d.get("workload") != workload or d.get("source_sha") != file_sha(d["source"]):
+        return None
+    return d.get("traffic_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def oracle_layer_rate(lay: inputs.LayerInputs, budget_s: float, max_tokens: int | None = None):
+    """Tokens/s of the oracle on whole tokens of this workload (single thread)."""
+    import oracle
+    oracle.lib()
+    done, t0 = 0, time.perf_counter()
+    T = lay.x.shape[0]
+    while True:
+        tok = np.array([done % T], np.int64)
+        oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes, tokens=tok)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_tokens is not None and done >= max_tokens):
+            return done / el, done, el
+
+
+def oracle_requant_rate(gu: inputs.Nvfp4Tensors, budget_s: float):
+    """Elements/s of the oracle requant on whole tensors (single thread)."""
+    import oracle
+    oracle.lib()
+    done_el, t0, i = 0, time.perf_counter(), 0
+    while True:
+        sl = slice(i % gu.e2m1.shape[0], i % gu.e2m1.shape[0] + 1)
+        oracle.requant(gu.e2m1[sl], gu.e4m3[sl], gu.scale_2[sl])
+        done_el += gu.e2m1[sl].size * 2
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done_el / el, i, el
+
+
+# ------------------------------------------------------------------ layer benchmark
+
+def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
+    import torch
+    from bit_moe_expert_w2_gb300 import moe_w2
+
+    dev = torch.device("cuda", local)
+    lay = inputs.layer_inputs(cfg)
+    T, H, I, E, k = cfg.tokens, cfg.hidden, cfg.inter, cfg.num_experts, cfg.top_k
+    decode = T <= moe_w2.DECODE_MAX_TOKENS
+    pool = POOL if decode else 2
+
+    # step inputs: the configuration's own batch first, then fresh draws of the same recipe
+    rng = np.random.default_rng(cfg.seed + 1000)
+    pop = inputs.zipf_popularity(np.random.default_rng(cfg.seed + 2000), E) if cfg.routing == "zipf" else None
+    batches = [(lay.x, lay.ids, lay.weights)]
+    for _ in range(pool - 1):
+        x = inputs.activations(rng, T, H)
+        ids, w = inputs.routing(rng, cfg, popularity=pop)
+        batches.append((x, ids, w))
+
+    planes = {kk: torch.from_numpy(v).to(dev) for kk, v in lay.planes.items()}
+    P = moe_w2.make_planes(planes)
+    ws_bytes = moe_w2.workspace_size(T, k, E, H, I)
+    work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def to_dev(x, ids, w):
+        return (torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16),
+                torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev))
+
+    dev_batches = [to_dev(*b) for b in batches]
+    ys = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(pool)]
+    # algorithmic plane bytes each step reads: every distinct expert's four sections, once
+    w13_b = 2 * I * (H // 4 + H // 32)
+    w2_b = H * (I // 4 + I // 32)
+    distinct = [len(np.unique(b[1][(b[1] >= 0) & (b[1] < E)])) for b in batches]
+
+    L = moe_w2.load()
+    stream = torch.cuda.Stream(device=dev)
+    n_ev = 4
+
+    def make_events():
+        # torch only reports elapsed time for events it has recorded once itself;
+        # the library re-records them (as graph nodes) on every replay
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    def call(i, evs, s):
+        x, ids, w = dev_batches[i]
+        ev_ptrs = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in evs])
+        st = L.moe_w2_forward_traced(moe_w2._ptr(x), moe_w2._ptr(ids), moe_w2._ptr(w), ctypes.byref(P), T, k,
+                                     moe_w2._ptr(ys[i]), moe_w2._ptr(work), work.numel(), moe_w2._ptr(status),
+                                     ctypes.c_void_p(s.cuda_stream), ev_ptrs)
+        if st != 0:
+            raise moe_w2.MoeW2Error(st, "moe_w2_forward_traced")
+
+    # graphs: one per pool entry, each with its own phase events
+    graphs, events = [], []
+    with torch.cuda.stream(stream):
+        for i in range(pool):            # warm the library's one-time queries outside capture
+            evs = make_events()
+            call(i, evs, stream)
+        torch.cuda.synchronize(dev)
+        for i in range(pool):
+            evs = make_events()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                call(i, evs, stream)
+            graphs.append(g)
+            events.append(evs)
+    torch.cuda.synchronize(dev)
+
+    def run_steps(nsteps, record):
+        tot = np.zeros(n_ev - 1)
+        steps_total = 0.0
+        per_step = []
+        done = 0
+        while done < nsteps:
+            m = min(pool, nsteps - done)
+            with torch.cuda.stream(stream):
+                for j in range(m):
+                    flush.zero_()
+                    graphs[(done + j) % pool].replay()
+            stream.synchronize()
+            for j in range(m):
+                evs = events[(done + j) % pool]
+                ph = [evs[q].elapsed_time(evs[q + 1]) for q in range(n_ev - 1)]
+                step = evs[0].elapsed_time(evs[n_ev - 1])
+                if record:
+                    tot += ph
+                    steps_total += step
+                    per_step.append(((done + j) % pool, step, ph))
+            done += m
+        return steps_total, tot, per_step
+
+    run_steps(max(args.warmup, 3), False)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        steps_ms, phase_ms, per_step = run_steps(args.steps, True)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    steps_ms_max = max_over_ranks(steps_ms, world)
+    K = args.steps
+    value = world * T * K / (steps_ms_max / 1e3)
+    st_val = int(status.item())
+    if st_val != 0:
+        raise RuntimeError(f"device status {st_val} during the benchmark")
+
+    pk = peaks()
+    plane_bytes = sum(distinct[i] * (w13_b + w2_b) for i, _, _ in per_step)
+    gu_bytes = sum(distinct[i] * w13_b for i, _, _ in per_step)
+    res = {"ms_per_step": steps_ms / K}
+    if decode:
+        achieved = gu_bytes / (phase_ms[1] / 1e3) / 1e9
+        res["roofline"] = {"kernel": "decode_gate_up_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                           "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                           "peak_source": pk["source"],
+                           "traffic": ncu_traffic("decode_gate_up_kernel", cfg.name)}
+        res["plane_gbs_step"] = round(plane_bytes / (steps_ms / 1e3) / 1e9, 1)
+        res["plane_frac_step"] = round(plane_bytes / (steps_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)
+    else:
+        flops_gu = 2.0 * T * k * 2 * I * H
+        achieved = flops_gu / (phase_ms[1] / 1e3) / 1e12 * K
+        res["roofline"] = {"kernel": "prefill_gate_up_kernel", "bound": "tensor", "achieved": round(achieved, 1),
+                           "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                           "frac": round(achieved / pk["bf16_tflops"], 4), "peak_source": pk["source"],
+                           "traffic": ncu_traffic("prefill_gate_up_kernel", cfg.name)}
+        res["layer_tflops"] = round(6.0 * T * k * H * I * K / (steps_ms / 1e3) / 1e12, 1)
+    res["phase_ms_per_step"] = {"permute": round(phase_ms[0] / K, 5), "gate_up": round(phase_ms[1] / K, 5),
+                                "down_combine": round(phase_ms[2] / K, 5)}
+    res["distinct_experts_per_step"] = round(float(np.mean([distinct[i] for i, _, _ in per_step])), 2)
+    res["clocks"] = clk.summary()
+    res["wall_s"] = round(wall, 3)
+    res["kernels_per_step"] = 3 if decode else 5
+
+    # end to end: pinned host inputs -> device -> forward -> y back to pinned host
+    hx = [torch.from_numpy(b[0].view(np.int16)).pin_memory() for b in batches]
+    hid = [torch.from_numpy(b[1]).pin_memory() for b in batches]
+    hw = [torch.from_numpy(b[2]).pin_memory() for b in batches]
+    hy = [torch.empty((T, H), dtype=torch.int16).pin_memory() for _ in range(pool)]
+    dx = torch.empty((T, H), dtype=torch.int16, device=dev)
+    did = torch.empty((T, k), dtype=torch.int32, device=dev)
+    dw = torch.empty((T, k), dtype=torch.float32, device=dev)
+    dy = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(pool)]
+    e_end = [torch.cuda.Event(enable_timing=True) for _ in range(pool)]
+
+    def e2e_step(i):
+        e_start[i].record(stream)
+        dx.copy_(hx[i], non_blocking=True)
+        did.copy_(hid[i], non_blocking=True)
+        dw.copy_(hw[i], non_blocking=True)
+        st = L.moe_w2_forward(moe_w2._ptr(dx), moe_w2._ptr(did), moe_w2._ptr(dw), ctypes.byref(P), T, k,
+                              moe_w2._ptr(dy), moe_w2._ptr(work), work.numel(), moe_w2._ptr(status),
+                              ctypes.c_void_p(stream.cuda_stream))
+        if st != 0:
+            raise moe_w2.MoeW2Error(st, "moe_w2_forward")
+        hy[i].copy_(dy.view(torch.int16), non_blocking=True)
+        e_end[i].record(stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(pool):
+            e2e_step(i)
+    stream.synchronize()
+    e2e_ms, done = 0.0, 0
+    barrier(world)
+    while done < args.steps:
+        m = min(pool, args.steps - done)
+        with torch.cuda.stream(stream):
+            for j in range(m):
+                flush.zero_()
+                e2e_step(j)
+        stream.synchronize()
+        e2e_ms += sum(e_start[j].elapsed_time(e_end[j]) for j in range(m))
+        done += m
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    bytes_in = batches[0][0].nbytes + batches[0][1].nbytes + batches[0][2].nbytes
+    res["e2e"] = {"value": round(world * T * args.steps / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+                  "h2d_bytes_per_step": int(bytes_in), "d2h_bytes_per_step": int(T * H * 2)}
+    res["gpu_launches"] = res["kernels_per_step"] * args.steps
+    res["value"] = value
+    return res, lay
+
+
+def requant_bench(args, world, rank, local):
+    import torch
+    from bit_moe_expert_w2_gb300 import moe_w2
+    dev = torch.device("cuda", local)
+    gu, dn = inputs.requant_inputs()
+    dgu = [torch.from_numpy(a).to(dev) for a in (gu.e2m1, gu.e4m3, gu.scale_2)]
+    ddn = [torch.from_numpy(a).to(dev) for a in (dn.e2m1, dn.e4m3, dn.scale_2)]
+    cgu = torch.empty((gu.e2m1.shape[0], gu.e2m1.shape[1], gu.e2m1.shape[2] // 2), dtype=torch.uint8, device=dev)
+    sgu = torch.empty((gu.e2m1.shape[0], gu.e2m1.shape[1], gu.e2m1.shape[2] // 16), dtype=torch.uint8, device=dev)
+    cdn = torch.empty((dn.e2m1.shape[0], dn.e2m1.shape[1], dn.e2m1.shape[2] // 2), dtype=torch.uint8, device=dev)
+    sdn = torch.empty((dn.e2m1.shape[0], dn.e2m1.shape[1], dn.e2m1.shape[2] // 16), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def step(e0=None, e1=None):
+        if e0 is not None:
+            e0.record(stream)
+        moe_w2.requant(*dgu, codes=cgu, ue8m0=sgu, status=status, stream=stream)
+        moe_w2.requant(*ddn, codes=cdn, ue8m0=sdn, status=status, stream=stream)
+        if e1 is not None:
+            e1.record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                flush.zero_()
+                step(e0, e1)
+        stream.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs)
+    ms = max_over_ranks(ms, world)
+    elems = gu.e2m1.size * 2 + dn.e2m1.size * 2
+    moved = sum(a.nbytes for a in (gu.e2m1, gu.e4m3, dn.e2m1, dn.e4m3)) + elems // 4 + elems // 32
+    pk = peaks()
+    gbs = moved * args.steps / (ms / 1e3) / 1e9
+    res = {"ms_per_step": ms / args.steps, "value": world * elems * args.steps / (ms / 1e3),
+           "roofline": {"kernel": "requant_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                        "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                        "peak_source": pk["source"], "traffic": ncu_traffic("requant_kernel", "requant_256")},
+           "clocks": clk.summary(), "gpu_launches": 2 * args.steps}
+    return res, gu
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=[*inputs.CONFIGS, inputs.REQUANT.name])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = {"decode_t1": 1000, "decode_t32": 500, "prefill_t8192": 50}.get(args.config, 10)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    cores = len(os.sched_getaffinity(0))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        return reference_arm(args, cores)
+
+    world, rank, local = dist_setup(args)
+    if args.config == inputs.REQUANT.name:
+        res, gu = requant_bench(args, world, rank, local)
+        metric_unit = "elements/s"
+        workload = f"{inputs.REQUANT.name}: 256 experts NVFP4 gate/up 2x[2048x6144] + down [6144x2048] -> 2-bit planes"
+    else:
+        cfg = inputs.CONFIGS[args.config]
+        res, lay = layer_bench(args, cfg, world, rank, local)
+        metric_unit = "tokens/s"
+        workload = (f"{cfg.name}: H={cfg.hidden} I={cfg.inter} E={cfg.num_experts} top-{cfg.top_k} "
+                    f"T={cfg.tokens} routing={cfg.routing}")
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": round(res.pop("value"), 3), "unit": metric_unit, "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(res.pop("ms_per_step"), 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; shapes of the pages' models)",
+            "config": {"workload": workload, "l2": "flushed before every step (512 MiB write, untimed)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}}
+    line.update(res)
+    if not args.no_cpu_baseline and world == 1:
+        if args.config == inputs.REQUANT.name:
+            v, n, el = oracle_requant_rate(gu, args.cpu_budget)
+            line["cpu_baseline"] = {"value": round(v, 1), "unit": "elements/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"{n} whole gate/up tensors in {el:.1f} s"}
+        else:
+            v, n, el = oracle_layer_rate(lay, args.cpu_budget)
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"{n} whole tokens of {args.config} in {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def reference_arm(args, cores):
+    """The oracle timed on this host's cores on a bounded sample of the workload."""
+    budget = 90.0
+    if args.config == inputs.REQUANT.name:
+        gu, _ = inputs.requant_inputs(experts=4)
+        v, n, el = oracle_requant_rate(gu, budget / 3)
+        unit, sample = "elements/s", f"{n} whole gate/up tensors of {args.config} in {el:.1f} s"
+        steps = n
+    else:
+        cfg = inputs.CONFIGS[args.config]
+        lay = inputs.layer_inputs(cfg)
+        # warm-up tokens, then timed tokens until the step count or the budget is reached
+        oracle_layer_rate(lay, 0.0, max_tokens=1)
+        v, n, el = oracle_layer_rate(lay, budget, max_tokens=args.steps)
+        unit, sample = "tokens/s", f"{n} whole tokens of {args.config} in {el:.1f} s"
+        steps = n
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": unit, "n_gpus": 0,
+            "steps": steps, "warmup": 1, "ms_per_step": round(el / max(steps, 1) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": args.config, "sample": sample},
+            "cpu_baseline": {"value": round(v, 4), "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "host_cores_available": cores}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

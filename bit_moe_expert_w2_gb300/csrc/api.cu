@@ -125,9 +125,10 @@ moe_w2_status moe_w2_permute(const int32_t* topk_ids, int32_t T, int32_t top_k, 
     return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
 }
 
-moe_w2_status moe_w2_forward(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
-                             const moe_w2_planes* w, int32_t T, int32_t top_k, void* y_bf16, void* workspace,
-                             size_t workspace_bytes, uint32_t* dev_status, void* stream)
+moe_w2_status moe_w2_forward_traced(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                                    const moe_w2_planes* w, int32_t T, int32_t top_k, void* y_bf16,
+                                    void* workspace, size_t workspace_bytes, uint32_t* dev_status, void* stream,
+                                    void* const* phase_events)
 {
     if (!w || T < 0 || top_k < 1 || top_k > MOE_W2_MAX_TOP_K) return MOE_W2_ERR_INVALID_ARG;
     if (w->num_experts < 1 || w->num_experts > MOE_W2_MAX_EXPERTS) return MOE_W2_ERR_INVALID_ARG;
@@ -152,15 +153,27 @@ moe_w2_status moe_w2_forward(const void* x_bf16, const int32_t* topk_ids, const 
     const bool decode = T <= MOE_W2_DECODE_MAX_TOKENS;
     const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
     uint16_t* y = static_cast<uint16_t*>(y_bf16);
+    PhaseEvents ev{};
+    for (int i = 0; i < 4; ++i) ev.e[i] = phase_events ? static_cast<cudaEvent_t>(phase_events[i]) : nullptr;
+    if (ev.record(0, s) != cudaSuccess) return MOE_W2_ERR_CUDA;
     cudaError_t e = launch_permute(topk_ids, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active, ws.active_count,
                                    ws.tiles, ws.tile_count, kPrefillTileRows, decode ? x : nullptr,
                                    decode ? ws.xa : nullptr, H, dev_status, s);
     if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
     if (decode)
-        e = launch_decode(ws.xa, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s);
+        e = launch_decode(ws.xa, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
     else
-        e = launch_prefill(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s);
-    return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
+        e = launch_prefill(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
+    if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
+    return ev.record(3, s) == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
+}
+
+moe_w2_status moe_w2_forward(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                             const moe_w2_planes* w, int32_t T, int32_t top_k, void* y_bf16, void* workspace,
+                             size_t workspace_bytes, uint32_t* dev_status, void* stream)
+{
+    return moe_w2_forward_traced(x_bf16, topk_ids, topk_weights, w, T, top_k, y_bf16, workspace, workspace_bytes,
+                                 dev_status, stream, nullptr);
 }
 
 moe_w2_status moe_w2_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float* scale_2, int64_t n,

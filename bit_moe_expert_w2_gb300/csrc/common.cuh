@@ -113,6 +113,21 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
 int64_t max_prefill_tiles(int64_t P, int32_t E);
 
 // ------------------------------------------------------------------ launches
+// Optional profiling events recorded between phases (see moe_w2_forward_traced).
+// During stream capture the events become external record nodes, so each graph
+// replay records them and cudaEventElapsedTime works on replays.
+struct PhaseEvents {
+    cudaEvent_t e[4];
+    cudaError_t record(int i, cudaStream_t s) const
+    {
+        if (!e[i]) return cudaSuccess;
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t r = cudaStreamIsCapturing(s, &cs);
+        if (r != cudaSuccess) return r;
+        return cudaEventRecordWithFlags(e[i], s, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0);
+    }
+};
+
 cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* sorted, int32_t* inv,
                            int32_t* offsets, int32_t* active, int32_t* active_count, int4* tiles,
                            int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16,
@@ -120,11 +135,11 @@ cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, 
 
 cudaError_t launch_decode(const uint16_t* x_t16, const int32_t* ids, const float* weights,
                           const moe_w2_planes& w, int32_t T, int32_t k, const Workspace& ws, uint16_t* y,
-                          uint32_t* status, cudaStream_t s);
+                          uint32_t* status, cudaStream_t s, const PhaseEvents& ev);
 
 cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* weights, const moe_w2_planes& w,
                            int32_t T, int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status,
-                           cudaStream_t s);
+                           cudaStream_t s, const PhaseEvents& ev);
 
 cudaError_t launch_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float* scale_2, int64_t n,
                            int64_t rows, int64_t K, uint8_t* codes, uint8_t* ue8m0, uint32_t* status,

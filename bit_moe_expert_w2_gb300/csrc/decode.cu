@@ -310,7 +310,7 @@ constexpr int kDownWarps = 8;
 
 cudaError_t launch_decode(const uint16_t* x_t16, const int32_t* ids, const float* weights, const moe_w2_planes& w,
                           int32_t T, int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status,
-                          cudaStream_t s)
+                          cudaStream_t s, const PhaseEvents& ev)
 {
     (void)ids;
     const int32_t E = w.num_experts, H = w.hidden, I = w.inter;
@@ -324,10 +324,14 @@ cudaError_t launch_decode(const uint16_t* x_t16, const int32_t* ids, const float
         if (occ_gu < 1) occ_gu = 1;
     }
     const int grid_gu = (int)std::min<int64_t>(max_items, (int64_t)sm_count() * occ_gu);
+    cudaError_t e = ev.record(1, s);
+    if (e != cudaSuccess) return e;
     decode_gate_up_kernel<kGateUpWarps><<<grid_gu, kGateUpWarps * 32, 0, s>>>(
         x_t16, ws.sorted, ws.offsets, ws.active, ws.active_count, w.w13_codes, w.w13_scales, H, I, k, ws.h,
         status);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = ev.record(2, s);
     if (e != cudaSuccess) return e;
 
     const size_t smem = sizeof(float) * kDownWarps * 16 * T;

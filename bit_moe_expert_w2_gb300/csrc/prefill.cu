@@ -1,12 +1,422 @@
-// Prefill path placeholder (tcgen05 kernels land next).
-#include "common.cuh"
+// Prefill path (T > 64): grouped expert GEMMs on the 5th-generation tensor cores.
+//
+// vLLM-Moet, page "vLLM-Moet wiki", section "The kernels": 2-bit codes expanded
+// in the kernel and fed to block-scaled tensor-core MMAs; the prefill GEMM is
+// load-issue-bound on SM120, which their fragment-major activation repack
+// ("AFRAG", page "The v0.24.0 port", section "Our hooks") addressed.  Here the
+// activation tiles arrive by TMA (no per-thread load issue at all) and the
+// weight codes are expanded by four warps straight into the UMMA operand layout.
+// Page "The v0.24.0 port", "Deterministic unpermute" bullet: each pair's output
+// is placed in its own slot and the k slots of a token are summed in a fixed
+// order (no atomics).
+//
+// Launch sequence: gather (x rows in expert order, T16 layout) -> gate_up GEMM
+// with the SiLU(gate)*up epilogue -> down GEMM whose epilogue multiplies by the
+// router weight and stores the pair's fp32 row in its slot -> combine.
+//
+// GEMM kernel (one template, two epilogues).  Work item = (tile of <= 256 pairs
+// of one expert, block of 128 weight rows).  For gate_up the 128 A rows are 64
+// gate rows interleaved with their 64 up rows (A row 2i = gate i, 2i+1 = up i),
+// so each gate/up pair of accumulator rows sits in adjacent TMEM lanes of one
+// warp.  D[128 x N] (fp32) lives in tensor memory: lanes = weight rows,
+// columns = pairs.
+//   warps 0-3  expand the A tile (thread r = A row r) into the 128B-swizzled
+//              smem layout, then run the epilogue for their 32 TMEM lanes
+//   warp 4     TMA producer of the B tiles (activations, 16 rows per copy)
+//   warp 5     MMA issuer (one thread): 4 x tcgen05.mma (K = 16) per stage
+#include <algorithm>
+#include <mutex>
+
+#include "tc.cuh"
 
 namespace moe_w2 {
 
-cudaError_t launch_prefill(const uint16_t*, const int32_t*, const float*, const moe_w2_planes&, int32_t, int32_t,
-                           const Workspace&, uint16_t*, uint32_t*, cudaStream_t)
+namespace {
+
+constexpr int kBK = 64;                  // K per pipeline stage
+constexpr int kStages = 4;
+constexpr int kRowsA = 128;              // UMMA M
+constexpr int kMaxN = 256;               // pairs per tile (UMMA N <= 256)
+constexpr int kExpThreads = 128;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = kRowsA * 128;
+constexpr uint32_t kBBytes = kMaxN * 128;
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024;
+constexpr uint32_t kTmemCols = 256;
+
+struct GemmParams {
+    const uint8_t* codes;    // plane codes of this projection [E][rows_per_expert][K/4]
+    const uint8_t* scales;   // [E][rows_per_expert][K/32]
+    int32_t K;
+    int32_t rows_per_expert;
+    int32_t I;               // gate_up: index of the first up row
+    int32_t H;               // down: y width (stage row length)
+    int32_t row_blocks;      // items per tile
+    const int4* tiles;
+    const int32_t* tile_count;
+    uint16_t* h_t16;         // gate_up output [P][I]
+    float* stage;            // down output [P][H]
+    const int32_t* sorted;
+    const float* weights;
+    uint32_t* status;
+};
+
+__device__ __forceinline__ uint32_t word_i(const uint4& q, int i)
 {
-    return cudaErrorNotSupported;
+    return i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
+}
+
+template <bool kGateUp>
+__global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap,
+                                                                      GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kStages];
+    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t dfull_bar;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+    __shared__ uint2 lut_tab[256];
+
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const uint32_t smem_base = smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    for (int s = tid; s < 256; s += kThreads) {
+        ScaleLut l = make_lut((uint32_t)s);
+        lut_tab[s] = make_uint2(l.lut, l.lo);
+    }
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), kExpThreads + 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        mbar_init(smem_u32(&dfull_bar), 1);
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    volatile int* abort = &abort_flag;
+
+    const int n_items = *p.tile_count * p.row_blocks;
+    const int nk = p.K / kBK;
+
+    if (warp < 4) {
+        // ------------------------------------------------ expanders + epilogue
+        const int r = tid;   // A row
+        uint32_t g = 0, items_done = 0, lut_min = 0xFFFFFFFFu;
+        for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+            const int4 tile = p.tiles[it / p.row_blocks];
+            const int rb = it % p.row_blocks;
+            const int e = tile.x, q0 = tile.y, nrows = tile.z;
+            int row;
+            if (kGateUp) row = (r & 1 ? p.I : 0) + rb * 64 + (r >> 1);
+            else row = rb * kRowsA + r;
+            const int64_t grow = (int64_t)e * p.rows_per_expert + row;
+            const uint8_t* rc = p.codes + grow * (p.K / 4);
+            const uint8_t* rs = p.scales + grow * (p.K / 32);
+
+            uint4 q[4];
+            uint32_t sc[4];
+#pragma unroll
+            for (int d = 0; d < 4; ++d) {   // K is a multiple of 256: nk >= 4 and nk % 4 == 0
+                q[d] = ldg_stream_u4(rc + d * 16);
+                sc[d] = ldg_u16(rs + d * 2);
+            }
+            bool ok = true;
+            for (int kb = 0; kb < nk && ok; kb += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int kk = kb + u;
+                    const uint4 cq = q[u];
+                    const uint32_t cs = sc[u];
+                    if (kk + 4 < nk) {
+                        q[u] = ldg_stream_u4(rc + (kk + 4) * 16);
+                        sc[u] = ldg_u16(rs + (kk + 4) * 2);
+                    }
+                    const uint32_t slot = g % kStages, ph = (g / kStages) & 1u;
+                    if (!mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint2 L0 = lut_tab[cs & 0xFF], L1 = lut_tab[cs >> 8];
+                    lut_min = min(lut_min, min(L0.x, L1.x));
+                    uint8_t* a_tile = smem + slot * kStageBytes;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t w = word_i(cq, i);
+                        const ScaleLut L = (i < 2) ? ScaleLut{L0.x, L0.y} : ScaleLut{L1.x, L1.y};
+                        const uint32_t s0 = code_selector<0>(w), s1 = code_selector<1>(w);
+                        const uint32_t s2 = code_selector<2>(w), s3 = code_selector<3>(w);
+                        uint4 c0, c1;
+                        c0.x = expand_pair(L, s0);
+                        c0.y = expand_pair(L, s0 >> 16);
+                        c0.z = expand_pair(L, s1);
+                        c0.w = expand_pair(L, s1 >> 16);
+                        c1.x = expand_pair(L, s2);
+                        c1.y = expand_pair(L, s2 >> 16);
+                        c1.z = expand_pair(L, s3);
+                        c1.w = expand_pair(L, s3 >> 16);
+                        *reinterpret_cast<uint4*>(a_tile + sw128_offset(r, 2 * i)) = c0;
+                        *reinterpret_cast<uint4*>(a_tile + sw128_offset(r, 2 * i + 1)) = c1;
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(smem_u32(&full_bar[slot]));
+                    ++g;
+                }
+            }
+            if (*abort) break;
+
+            // epilogue: D rows 32*warp .. 32*warp+31, columns = pairs of the tile
+            if (!mbar_wait(smem_u32(&dfull_bar), items_done & 1u, abort)) break;
+            ++items_done;
+            tc_fence_after();
+            const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+            for (int c0 = 0; c0 < nrows; c0 += 32) {
+                float v[32];
+                tmem_ld32(lane_base + c0, v);
+                if (kGateUp) {
+                    const int n = rb * 64 + (r >> 1);
+                    const int pos = t16_pos(n);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float up = __shfl_down_sync(0xffffffffu, v[j], 1);
+                        if (!(r & 1) && c0 + j < nrows) {
+                            __nv_bfloat16 hb = __float2bfloat16_rn(silu_f(v[j]) * up);
+                            p.h_t16[(int64_t)(q0 + c0 + j) * p.I + pos] = *reinterpret_cast<uint16_t*>(&hb);
+                        }
+                    }
+                } else {
+                    const int m = rb * kRowsA + r;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (c0 + j < nrows) {
+                            const int pr = p.sorted[q0 + c0 + j];
+                            p.stage[(int64_t)pr * p.H + m] = p.weights[pr] * v[j];
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+        }
+        if (lut_min == 0) flag_status(p.status, MOE_W2_DEV_BAD_SCALE);
+    } else if (warp == 4) {
+        // ------------------------------------------------ TMA producer (B tiles)
+        if (lane == 0) {
+            prefetch_tmap(&bmap);
+            uint32_t g = 0;
+            for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+                const int4 tile = p.tiles[it / p.row_blocks];
+                const int q0 = tile.y, npad = (tile.z + 15) & ~15;
+                for (int kk = 0; kk < nk; ++kk) {
+                    const uint32_t slot = g % kStages, ph = (g / kStages) & 1u;
+                    if (!mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort)) break;
+                    const uint32_t fb = smem_u32(&full_bar[slot]);
+                    mbar_arrive_expect_tx(fb, (uint32_t)npad * 128u);
+                    const uint32_t b_tile = smem_base + slot * kStageBytes + kABytes;
+                    for (int j = 0; j < npad / 16; ++j) tma_load_2d(b_tile + j * 2048u, &bmap, kk * kBK, q0 + 16 * j, fb);
+                    ++g;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t g = 0;
+            for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+                const int4 tile = p.tiles[it / p.row_blocks];
+                const uint32_t npad = (tile.z + 15) & ~15;
+                const uint32_t idesc = idesc_bf16_f32(kRowsA, npad);
+                for (int kk = 0; kk < nk; ++kk) {
+                    const uint32_t slot = g % kStages, ph = (g / kStages) & 1u;
+                    if (!mbar_wait(smem_u32(&full_bar[slot]), ph, abort)) break;
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_base + slot * kStageBytes;
+                    const uint64_t ad = smem_desc_sw128(a_addr), bd = smem_desc_sw128(a_addr + kABytes);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        umma_f16_ss(tmem, ad + 2 * k4, bd + 2 * k4, idesc, (kk | k4) != 0);
+                    umma_commit(smem_u32(&empty_bar[slot]));
+                    ++g;
+                }
+                umma_commit(smem_u32(&dfull_bar));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (tid == 0 && abort_flag) flag_status(p.status, kDevPipelineTimeout);
+}
+
+// x rows in expert order, T16 layout: xs[q] = T16(x[sorted[q] / k]) for q < valid pairs.
+__global__ void gather_t16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted,
+                                  const int32_t* __restrict__ offsets, int32_t E, int32_t k, int32_t H,
+                                  uint16_t* __restrict__ xs)
+{
+    const int64_t groups = (int64_t)offsets[E] * (H / 16);
+    const int gpr = H / 16;
+    for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups;
+         gi += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t q = gi / gpr;
+        const int gcol = (int)(gi % gpr);
+        const uint16_t* src = x + (int64_t)(sorted[q] / k) * H + gcol * 16;
+        uint4 a = *reinterpret_cast<const uint4*>(src);
+        uint4 b = *reinterpret_cast<const uint4*>(src + 8);
+        uint4 o, t;
+        o.x = __byte_perm(a.x, a.z, 0x5410);
+        o.y = __byte_perm(b.x, b.z, 0x5410);
+        o.z = __byte_perm(a.x, a.z, 0x7632);
+        o.w = __byte_perm(b.x, b.z, 0x7632);
+        t.x = __byte_perm(a.y, a.w, 0x5410);
+        t.y = __byte_perm(b.y, b.w, 0x5410);
+        t.z = __byte_perm(a.y, a.w, 0x7632);
+        t.w = __byte_perm(b.y, b.w, 0x7632);
+        uint16_t* dst = xs + q * H + gcol * 16;
+        *reinterpret_cast<uint4*>(dst) = o;
+        *reinterpret_cast<uint4*>(dst + 8) = t;
+    }
+}
+
+// y[t][m] = bf16( sum over j = 0..k-1 (valid ids only) of stage[t*k + j][m] ), j in order.
+__global__ void combine_kernel(const float* __restrict__ stage, const int32_t* __restrict__ ids, int32_t T,
+                               int32_t k, int32_t E, int32_t H, uint16_t* __restrict__ y)
+{
+    const int per_row = H / 8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)T * per_row;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / per_row;
+        const int m = (int)(i % per_row) * 8;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < k; ++j) {
+            const int e = ids[t * k + j];
+            if ((unsigned)e >= (unsigned)E) continue;
+            const float4* src = reinterpret_cast<const float4*>(stage + (t * k + j) * H + m);
+            const float4 a = src[0], b = src[1];
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
+        uint4 o;
+        uint32_t* ow = &o.x;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            __nv_bfloat162 pr = __floats2bfloat162_rn(acc[2 * v], acc[2 * v + 1]);
+            ow[v] = *reinterpret_cast<uint32_t*>(&pr);
+        }
+        *reinterpret_cast<uint4*>(y + t * H + m) = o;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_encode_mu;
+
+cudaError_t get_encoder()
+{
+    std::lock_guard<std::mutex> lk(g_encode_mu);
+    if (g_encode) return cudaSuccess;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return cudaSuccess;
+}
+
+// 2-D bf16 tensor [rows][cols] (row-major), box = 64 columns x 16 rows, 128B swizzle.
+cudaError_t make_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols)
+{
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* weights, const moe_w2_planes& w,
+                           int32_t T, int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status, cudaStream_t s,
+                           const PhaseEvents& ev)
+{
+    const int32_t E = w.num_experts, H = w.hidden, I = w.inter;
+    const int64_t P = (int64_t)T * k;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(tc_expert_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(tc_expert_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const int sms = sm_count();
+
+    const int64_t groups = P * (H / 16);
+    gather_t16_kernel<<<(int)std::min<int64_t>((groups + 255) / 256, (int64_t)sms * 8), 256, 0, s>>>(
+        x, ws.sorted, ws.offsets, E, k, H, ws.xa);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    CUtensorMap xmap, hmap;
+    if ((e = make_bf16_map(&xmap, ws.xa, P, H)) != cudaSuccess) return e;
+    if ((e = make_bf16_map(&hmap, ws.h, P, I)) != cudaSuccess) return e;
+
+    if ((e = ev.record(1, s)) != cudaSuccess) return e;
+    GemmParams gp{};
+    gp.codes = w.w13_codes;
+    gp.scales = w.w13_scales;
+    gp.K = H;
+    gp.rows_per_expert = 2 * I;
+    gp.I = I;
+    gp.H = H;
+    gp.row_blocks = I / 64;
+    gp.tiles = ws.tiles;
+    gp.tile_count = ws.tile_count;
+    gp.h_t16 = ws.h;
+    gp.stage = ws.stage;
+    gp.sorted = ws.sorted;
+    gp.weights = weights;
+    gp.status = status;
+    const int64_t max_items = max_prefill_tiles(P, E) * (I / 64);
+    tc_expert_gemm_kernel<true><<<(int)std::min<int64_t>(sms, max_items), kThreads, kSmemBytes, s>>>(xmap, gp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    if ((e = ev.record(2, s)) != cudaSuccess) return e;
+    GemmParams dp = gp;
+    dp.codes = w.w2_codes;
+    dp.scales = w.w2_scales;
+    dp.K = I;
+    dp.rows_per_expert = H;
+    dp.row_blocks = H / kRowsA;
+    const int64_t max_items_d = max_prefill_tiles(P, E) * (H / kRowsA);
+    tc_expert_gemm_kernel<false><<<(int)std::min<int64_t>(sms, max_items_d), kThreads, kSmemBytes, s>>>(hmap, dp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    const int64_t cthreads = (int64_t)T * (H / 8);
+    combine_kernel<<<(int)std::min<int64_t>((cthreads + 255) / 256, (int64_t)sms * 8), 256, 0, s>>>(
+        ws.stage, ids, T, k, E, H, y);
+    return cudaGetLastError();
 }
 
 }  // namespace moe_w2

@@ -126,6 +126,20 @@ moe_w2_status moe_w2_forward(const void *x_bf16, const int32_t *topk_ids, const 
                              void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream);
 
 /*
+ * moe_w2_forward with phase events, for profiling: identical work and results.
+ *   phase_events  host array of 4 cudaEvent_t (or NULL entries); event i is
+ *                 recorded on `stream` before phase i: 0 = before the
+ *                 permutation, 1 = before the gate_up kernel(s), 2 = before the
+ *                 down kernel(s), 3 = after the last kernel.  On the prefill
+ *                 path the gather is part of phase 0..1 and the combine of 2..3.
+ * cudaEventRecord failures return MOE_W2_ERR_CUDA.
+ */
+moe_w2_status moe_w2_forward_traced(const void *x_bf16, const int32_t *topk_ids, const float *topk_weights,
+                                    const moe_w2_planes *w, int32_t T, int32_t top_k, void *y_bf16,
+                                    void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                                    void *stream, void *const *phase_events);
+
+/*
  * Load-time re-quantizer ("The v0.24.0 port", "Our hooks", modelopt.py
  * bullet): modelopt NVFP4 tensors -> 2-bit planes.
  *   e2m1     uint8 [n][rows][K/2]   two e2m1 nibbles per byte, low nibble = even element

@@ -11,7 +11,8 @@ namespace moe_w2 {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int32_t kPrefillTileRows = 256;   // tokens per prefill tile (tcgen05 N <= 256)
+constexpr int32_t kPrefillTileRows = 256;   // pairs per prefill tile (tcgen05 N <= 256)
+constexpr int32_t kDecodeTileRows = 64;     // pairs per decode tile
 
 int g_sm_count[kMaxDevices];
 int g_cc_ok[kMaxDevices];   // 0 = unknown, 1 = ok, 2 = not sm_103
@@ -54,7 +55,10 @@ int sm_count()
     return sms;
 }
 
-int64_t max_prefill_tiles(int64_t P, int32_t E) { return P / kPrefillTileRows + E + 1; }
+int64_t max_tiles(int64_t P, int32_t E, bool decode)
+{
+    return P / (decode ? kDecodeTileRows : kPrefillTileRows) + E + 1;
+}
 
 Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I)
 {
@@ -74,10 +78,10 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
     w.active = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * E));
     w.active_count = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * 2));
     w.tile_count = w.active_count + 1;
-    w.tiles = decode ? nullptr : reinterpret_cast<int4*>(take(sizeof(int4) * max_prefill_tiles(P, E)));
-    w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * (decode ? (int64_t)T : P) * H));
+    w.tiles = reinterpret_cast<int4*>(take(sizeof(int4) * max_tiles(P, E, decode)));
+    w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * H));
     w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
-    w.stage = decode ? nullptr : reinterpret_cast<float*>(take(sizeof(float) * P * H));
+    w.stage = reinterpret_cast<float*>(take(sizeof(float) * P * H));
     w.bytes = off;
     return w;
 }
@@ -121,7 +125,7 @@ moe_w2_status moe_w2_permute(const int32_t* topk_ids, int32_t T, int32_t top_k, 
     if (st != MOE_W2_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_permute(topk_ids, T, top_k, E, sorted_pairs, inv_pairs, expert_offsets, nullptr, nullptr,
-                                   nullptr, nullptr, 1, nullptr, nullptr, 0, dev_status, s);
+                                   nullptr, nullptr, 1, dev_status, s);
     return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
 }
 
@@ -157,11 +161,11 @@ moe_w2_status moe_w2_forward_traced(const void* x_bf16, const int32_t* topk_ids,
     for (int i = 0; i < 4; ++i) ev.e[i] = phase_events ? static_cast<cudaEvent_t>(phase_events[i]) : nullptr;
     if (ev.record(0, s) != cudaSuccess) return MOE_W2_ERR_CUDA;
     cudaError_t e = launch_permute(topk_ids, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active, ws.active_count,
-                                   ws.tiles, ws.tile_count, kPrefillTileRows, decode ? x : nullptr,
-                                   decode ? ws.xa : nullptr, H, dev_status, s);
+                                   ws.tiles, ws.tile_count, decode ? kDecodeTileRows : kPrefillTileRows, dev_status,
+                                   s);
     if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
     if (decode)
-        e = launch_decode(ws.xa, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
+        e = launch_decode(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
     else
         e = launch_prefill(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
     if (e != cudaSuccess) return MOE_W2_ERR_CUDA;

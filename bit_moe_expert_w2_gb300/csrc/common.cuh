@@ -99,18 +99,18 @@ struct Workspace {
     int32_t* sorted;       // [P]
     int32_t* inv;          // [P]
     int32_t* offsets;      // [E+1]
-    int32_t* active;       // [E] active experts ascending, [E] = count (stored at active_count)
+    int32_t* active;       // [E] active experts ascending
     int32_t* active_count; // [1]
-    int4* tiles;           // prefill tiles (expert, q0, rows, 0)
+    int4* tiles;           // GEMM tiles (expert, first slot, pairs, 0)
     int32_t* tile_count;   // [1]
-    uint16_t* xa;          // decode: x in T16 layout [T][H]; prefill: expert-sorted x in T16 layout [P][H]
-    uint16_t* h;           // [P][I] T16 layout
-    float* stage;          // prefill only: [P][H]
+    uint16_t* xa;          // activation rows in expert order, T16 layout [P][H]
+    uint16_t* h;           // SiLU(gate)*up rows in expert order, T16 layout [P][I]
+    float* stage;          // per-pair outputs times router weight, slot t*k+j [P][H]
     size_t bytes;
 };
 
 Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I);
-int64_t max_prefill_tiles(int64_t P, int32_t E);
+int64_t max_tiles(int64_t P, int32_t E, bool decode);
 
 // ------------------------------------------------------------------ launches
 // Optional profiling events recorded between phases (see moe_w2_forward_traced).
@@ -130,10 +130,9 @@ struct PhaseEvents {
 
 cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* sorted, int32_t* inv,
                            int32_t* offsets, int32_t* active, int32_t* active_count, int4* tiles,
-                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16,
-                           int32_t H, uint32_t* status, cudaStream_t s);
+                           int32_t* tile_count, int32_t tile_rows, uint32_t* status, cudaStream_t s);
 
-cudaError_t launch_decode(const uint16_t* x_t16, const int32_t* ids, const float* weights,
+cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* weights,
                           const moe_w2_planes& w, int32_t T, int32_t k, const Workspace& ws, uint16_t* y,
                           uint32_t* status, cudaStream_t s, const PhaseEvents& ev);
 

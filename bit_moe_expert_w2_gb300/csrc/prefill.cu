@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
                     }
                     const uint2 L0 = lut_tab[cs & 0xFF], L1 = lut_tab[cs >> 8];
                     lut_min = min(lut_min, min(L0.x, L1.x));
-                    uint8_t* a_tile = smem + slot * kStageBytes;
+                    const uint32_t a_tile = smem_base + slot * kStageBytes;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const uint32_t w = word_i(cq, i);
@@ -165,8 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
                         c1.y = expand_pair(L, s2 >> 16);
                         c1.z = expand_pair(L, s3);
                         c1.w = expand_pair(L, s3 >> 16);
-                        *reinterpret_cast<uint4*>(a_tile + sw128_offset(r, 2 * i)) = c0;
-                        *reinterpret_cast<uint4*>(a_tile + sw128_offset(r, 2 * i + 1)) = c1;
+                        sts_u4(a_tile + sw128_offset(r, 2 * i), c0);
+                        sts_u4(a_tile + sw128_offset(r, 2 * i + 1), c1);
                     }
                     fence_proxy_async_smem();
                     mbar_arrive(smem_u32(&full_bar[slot]));
@@ -261,97 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     if (tid == 0 && abort_flag) flag_status(p.status, kDevPipelineTimeout);
 }
 
-// x rows in expert order, T16 layout: xs[q] = T16(x[sorted[q] / k]) for q < valid pairs.
-__global__ void gather_t16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted,
-                                  const int32_t* __restrict__ offsets, int32_t E, int32_t k, int32_t H,
-                                  uint16_t* __restrict__ xs)
-{
-    const int64_t groups = (int64_t)offsets[E] * (H / 16);
-    const int gpr = H / 16;
-    for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups;
-         gi += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t q = gi / gpr;
-        const int gcol = (int)(gi % gpr);
-        const uint16_t* src = x + (int64_t)(sorted[q] / k) * H + gcol * 16;
-        uint4 a = *reinterpret_cast<const uint4*>(src);
-        uint4 b = *reinterpret_cast<const uint4*>(src + 8);
-        uint4 o, t;
-        o.x = __byte_perm(a.x, a.z, 0x5410);
-        o.y = __byte_perm(b.x, b.z, 0x5410);
-        o.z = __byte_perm(a.x, a.z, 0x7632);
-        o.w = __byte_perm(b.x, b.z, 0x7632);
-        t.x = __byte_perm(a.y, a.w, 0x5410);
-        t.y = __byte_perm(b.y, b.w, 0x5410);
-        t.z = __byte_perm(a.y, a.w, 0x7632);
-        t.w = __byte_perm(b.y, b.w, 0x7632);
-        uint16_t* dst = xs + q * H + gcol * 16;
-        *reinterpret_cast<uint4*>(dst) = o;
-        *reinterpret_cast<uint4*>(dst + 8) = t;
-    }
-}
-
-// y[t][m] = bf16( sum over j = 0..k-1 (valid ids only) of stage[t*k + j][m] ), j in order.
-__global__ void combine_kernel(const float* __restrict__ stage, const int32_t* __restrict__ ids, int32_t T,
-                               int32_t k, int32_t E, int32_t H, uint16_t* __restrict__ y)
-{
-    const int per_row = H / 8;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)T * per_row;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = i / per_row;
-        const int m = (int)(i % per_row) * 8;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
-            const int e = ids[t * k + j];
-            if ((unsigned)e >= (unsigned)E) continue;
-            const float4* src = reinterpret_cast<const float4*>(stage + (t * k + j) * H + m);
-            const float4 a = src[0], b = src[1];
-            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-        }
-        uint4 o;
-        uint32_t* ow = &o.x;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            __nv_bfloat162 pr = __floats2bfloat162_rn(acc[2 * v], acc[2 * v + 1]);
-            ow[v] = *reinterpret_cast<uint32_t*>(&pr);
-        }
-        *reinterpret_cast<uint4*>(y + t * H + m) = o;
-    }
-}
-
-// ------------------------------------------------------------------ host side
-
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::mutex g_encode_mu;
-
-cudaError_t get_encoder()
-{
-    std::lock_guard<std::mutex> lk(g_encode_mu);
-    if (g_encode) return cudaSuccess;
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess) return e;
-    if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    return cudaSuccess;
-}
-
-// 2-D bf16 tensor [rows][cols] (row-major), box = 64 columns x 16 rows, 128B swizzle.
-cudaError_t make_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols)
-{
-    cudaError_t e = get_encoder();
-    if (e != cudaSuccess) return e;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, 16};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 }  // namespace
 
 cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* weights, const moe_w2_planes& w,
@@ -372,15 +281,12 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
     }
     const int sms = sm_count();
 
-    const int64_t groups = P * (H / 16);
-    gather_t16_kernel<<<(int)std::min<int64_t>((groups + 255) / 256, (int64_t)sms * 8), 256, 0, s>>>(
-        x, ws.sorted, ws.offsets, E, k, H, ws.xa);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_gather(x, ws.sorted, ws.offsets, E, k, H, P, ws.xa, s);
     if (e != cudaSuccess) return e;
 
     CUtensorMap xmap, hmap;
-    if ((e = make_bf16_map(&xmap, ws.xa, P, H)) != cudaSuccess) return e;
-    if ((e = make_bf16_map(&hmap, ws.h, P, I)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&xmap, ws.xa, true, P, H, 64, 16, true)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&hmap, ws.h, true, P, I, 64, 16, true)) != cudaSuccess) return e;
 
     if ((e = ev.record(1, s)) != cudaSuccess) return e;
     GemmParams gp{};
@@ -398,7 +304,7 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
     gp.sorted = ws.sorted;
     gp.weights = weights;
     gp.status = status;
-    const int64_t max_items = max_prefill_tiles(P, E) * (I / 64);
+    const int64_t max_items = max_tiles(P, E, false) * (I / 64);
     tc_expert_gemm_kernel<true><<<(int)std::min<int64_t>(sms, max_items), kThreads, kSmemBytes, s>>>(xmap, gp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -409,14 +315,11 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
     dp.K = I;
     dp.rows_per_expert = H;
     dp.row_blocks = H / kRowsA;
-    const int64_t max_items_d = max_prefill_tiles(P, E) * (H / kRowsA);
+    const int64_t max_items_d = max_tiles(P, E, false) * (H / kRowsA);
     tc_expert_gemm_kernel<false><<<(int)std::min<int64_t>(sms, max_items_d), kThreads, kSmemBytes, s>>>(hmap, dp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-    const int64_t cthreads = (int64_t)T * (H / 8);
-    combine_kernel<<<(int)std::min<int64_t>((cthreads + 255) / 256, (int64_t)sms * 8), 256, 0, s>>>(
-        ws.stage, ids, T, k, E, H, y);
-    return cudaGetLastError();
+    return launch_combine(ws.stage, ids, T, k, E, H, y, s);
 }
 
 }  // namespace moe_w2

@@ -334,7 +334,9 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
     res["distinct_experts_per_step"] = round(float(np.mean([distinct[i] for i, _, _ in per_step])), 2)
     res["clocks"] = clk.summary()
     res["wall_s"] = round(wall, 3)
-    res["kernels_per_step"] = 5   # permute, gather, gate_up, down, combine
+    # decode: permute (+ x transpose), gate_up, down (+ combine);
+    # prefill: permute, gather, gate_up, down, combine
+    res["kernels_per_step"] = 3 if decode else 5
 
     # end to end: pinned host inputs -> device -> forward -> y back to pinned host
     hx = [torch.from_numpy(b[0].view(np.int16)).pin_memory() for b in batches]

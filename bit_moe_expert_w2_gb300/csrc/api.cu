@@ -12,7 +12,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int32_t kPrefillTileRows = 256;   // pairs per prefill tile (tcgen05 N <= 256)
-constexpr int32_t kDecodeTileRows = 64;     // pairs per decode tile
+constexpr int32_t kDecodeTileRows = 16;     // pairs per decode tile
 
 int g_sm_count[kMaxDevices];
 int g_cc_ok[kMaxDevices];   // 0 = unknown, 1 = ok, 2 = not sm_103
@@ -79,7 +79,8 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
     w.active_count = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * 2));
     w.tile_count = w.active_count + 1;
     w.tiles = reinterpret_cast<int4*>(take(sizeof(int4) * max_tiles(P, E, decode)));
-    w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * H));
+    w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (H / 32)));
+    w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * (decode ? (int64_t)T : P) * H));
     w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
     w.stage = reinterpret_cast<float*>(take(sizeof(float) * P * H));
     w.bytes = off;
@@ -125,7 +126,7 @@ moe_w2_status moe_w2_permute(const int32_t* topk_ids, int32_t T, int32_t top_k, 
     if (st != MOE_W2_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_permute(topk_ids, T, top_k, E, sorted_pairs, inv_pairs, expert_offsets, nullptr, nullptr,
-                                   nullptr, nullptr, 1, dev_status, s);
+                                   nullptr, nullptr, 1, nullptr, nullptr, 0, nullptr, 0, nullptr, dev_status, s);
     return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
 }
 
@@ -161,8 +162,9 @@ moe_w2_status moe_w2_forward_traced(const void* x_bf16, const int32_t* topk_ids,
     for (int i = 0; i < 4; ++i) ev.e[i] = phase_events ? static_cast<cudaEvent_t>(phase_events[i]) : nullptr;
     if (ev.record(0, s) != cudaSuccess) return MOE_W2_ERR_CUDA;
     cudaError_t e = launch_permute(topk_ids, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active, ws.active_count,
-                                   ws.tiles, ws.tile_count, decode ? kDecodeTileRows : kPrefillTileRows, dev_status,
-                                   s);
+                                   ws.tiles, ws.tile_count, decode ? kDecodeTileRows : kPrefillTileRows,
+                                   decode ? x : nullptr, decode ? ws.xa : nullptr, H, ws.counters,
+                                   decode ? H / 32 : 0, decode ? y : nullptr, dev_status, s);
     if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
     if (decode)
         e = launch_decode(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);

@@ -103,7 +103,8 @@ struct Workspace {
     int32_t* active_count; // [1]
     int4* tiles;           // GEMM tiles (expert, first slot, pairs, 0)
     int32_t* tile_count;   // [1]
-    uint16_t* xa;          // activation rows in expert order, T16 layout [P][H]
+    uint16_t* xa;          // prefill: activation rows in expert order [P][H]; decode: x per token [T][H]; T16 layout
+    int32_t* counters;     // decode: per 32-row block of y, CTAs done (last one runs the combine)
     uint16_t* h;           // SiLU(gate)*up rows in expert order, T16 layout [P][I]
     float* stage;          // per-pair outputs times router weight, slot t*k+j [P][H]
     size_t bytes;
@@ -130,7 +131,8 @@ struct PhaseEvents {
 
 cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* sorted, int32_t* inv,
                            int32_t* offsets, int32_t* active, int32_t* active_count, int4* tiles,
-                           int32_t* tile_count, int32_t tile_rows, uint32_t* status, cudaStream_t s);
+                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16, int32_t H,
+                           int32_t* counters, int32_t n_counters, uint16_t* y, uint32_t* status, cudaStream_t s);
 
 cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* weights,
                           const moe_w2_planes& w, int32_t T, int32_t k, const Workspace& ws, uint16_t* y,

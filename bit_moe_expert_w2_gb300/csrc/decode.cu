@@ -1,70 +1,73 @@
 // Decode path (T <= 64): the 2-bit planes of every active expert are streamed
-// from HBM once per layer; tensor cores do the dot products.
+// from HBM once per layer, expanded in registers and fed to tensor-core MMAs.
 //
 // vLLM-Moet, page "vLLM-Moet wiki", section "The kernels": codes expanded in
 // registers through a byte-permute lookup table and fed to tensor-core MMAs;
 // section "FP4 recovery": decode is HBM-bound, the 2-bit read is the cost.  Page
 // "The v0.24.0 port", section "Benchmarks": tokens grouped by expert, so each
 // active expert's weights are read once per step however many tokens use it.
+// Page "The v0.24.0 port", "Deterministic unpermute" bullet: per-pair results
+// are placed in their own slot and summed over top_k in a fixed order.
 //
-// GB300 design.  The legacy mma.sync path is far too slow on sm_103 for a GEMV
-// that wastes most of N, and expanding the weights into shared memory would need
-// ~2 bytes of st.shared per code at HBM rate.  So the expanded A operand goes to
-// tensor memory instead:
-//   TMA        one producer thread streams 128-row x 128-code tiles of the packed
-//              codes into a deep shared ring (12 stages, 48 KB per CTA, released
-//              by the expanders once a tile is in TMEM);
-//              another streams the pairs' activation rows (expert order, T16
-//              layout) into 128B-swizzled B tiles;
-//   expanders  two warpgroups, alternating stages; thread r owns A row r: it
-//              reads its 32 code bytes, expands them with one byte-permute per
-//              weight pair (scale folded into a per-block table) and writes the
-//              64 bf16 pairs into its TMEM lane with tcgen05.st;
-//   MMA        one thread issues tcgen05.mma (A from TMEM, B from shared memory,
-//              D in TMEM): 8 x (M=128, N=pairs padded to 16, K=16) per stage;
-//   epilogue   the expanders read D back: SiLU(gate)*up -> h (gate_up), or
-//              router weight * D -> the pair's fp32 slot (down); a small
-//              combine kernel then sums each token's k slots in a fixed order.
-// Work item = (tile of <= 64 pairs of one expert, 128 weight rows).  For gate_up
-// the A rows interleave gate and up rows (A row 2i = gate i, 2i+1 = up i).
+// Why mma.sync here and not tcgen05: with N = a handful of pairs, every
+// tcgen05.mma (M=128, K=16) of a CTA costs ~105 cycles whatever N is (measured
+// on GB300), which caps a CTA far below HBM rate, while mma.sync m16n8k16 keeps
+// the weights in registers and reaches the full tensor rate with enough warps.
+// The expansion is integer work (~0.75 byte-permute/logic op per weight plus
+// shifts written as multiplies) and the kernel is sized to keep ~16 warps per SM
+// streaming codes through a per-thread cp.async ring (3 chunks deep).
+//
+// Per 256-wide K chunk a row is 64 code bytes; thread c of a quad owns bytes
+// [16c, 16c+16), i.e. four 16-code words; MMA (word i, r) takes codes (r, r+4)
+// and (r+8, r+12) of word i from every thread of the quad, which is what the
+// T16 activation layout stores next to each other (one 64-bit load per B
+// fragment).
+//
+// Work item = (tile of <= 16 pairs of one expert, 32 weight rows).  A warp holds
+// two m16 tiles; the four warps of a CTA split K and reduce in shared memory in
+// warp order.  gate_up: m-tile t = gate rows n0+8t.. (A rows 0-7) and the
+// matching up rows (A rows 8-15), so gate and up of one (row, pair) meet in one
+// thread for the SiLU(gate)*up epilogue.  down: 32 consecutive rows of W_down;
+// the epilogue multiplies by the router weight and writes the pair's fp32 slot;
+// the last CTA to finish a 32-row block of y sums the k slots of every token in
+// j order and writes y (counter per row block, reset by the permutation kernel).
 #include <algorithm>
-#include <mutex>
 
-#include "tc.cuh"
+#include "common.cuh"
 
 namespace moe_w2 {
 
 namespace {
 
-constexpr int kKS = 128;                  // K per stage
-constexpr int kSC = 12;                   // code-tile ring (HBM latency cover: 48 KB per CTA)
-constexpr int kSB = 3;                    // activation-tile ring (L2-resident rows)
-constexpr int kSA = 3;                    // TMEM A ring
-constexpr int kMaxN = 64;                 // pairs per decode tile
-constexpr int kGroups = 2;                // expander warpgroups
-constexpr int kThreads = kGroups * 128 + 96;   // + code producer, B producer, MMA issuer
-constexpr uint32_t kCodeBytes = 128 * 32;          // 128 rows x 32 code bytes
-constexpr uint32_t kBAtom = kMaxN * 128;           // 64 bf16 of K for kMaxN rows
-constexpr uint32_t kBBytes = 2 * kBAtom;           // K = 128: two 128-byte atoms
-constexpr uint32_t kSmemBytes = kSC * kCodeBytes + kSB * kBBytes + 1024;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kDCol = 0;                      // D: columns [0, 64)
-constexpr uint32_t kACol = 64;                     // A ring: 3 x 64 columns
+#ifndef MOE_W2_DEC_MIN_CTAS
+#define MOE_W2_DEC_MIN_CTAS 4        // CTAs per SM the register budget is sized for
+#endif
+constexpr int kChunk = 256;   // K elements per chunk
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxNT = 2;     // n-tiles of 8 pairs per item (tiles of <= 16 pairs)
 
-struct DecodeParams {
+struct DecArgs {
+    const uint8_t* codes;      // [E][rows_per_expert][K/4]
+    const uint8_t* scales;     // [E][rows_per_expert][K/32]
     int32_t K;
-    int32_t rows_per_expert;   // 2I or H
+    int32_t rows_per_expert;
     int32_t I;
     int32_t H;
-    int32_t k;                 // top_k (pair -> token)
+    int32_t T;
+    int32_t k;
+    int32_t E;
     int32_t row_blocks;
-    const uint8_t* scales;     // [E][rows_per_expert][K/32]
     const int4* tiles;
     const int32_t* tile_count;
     const int32_t* sorted;
     const float* weights;
+    const int32_t* ids;
+    const uint16_t* act;       // B rows: x_t16 per token (gate_up) or h_t16 per pair (down)
     uint16_t* h_t16;           // gate_up output [P][I]
     float* stage;              // down output [P][H]
+    int32_t* counters;         // down: per 32-row block of y
+    uint16_t* y;
     uint32_t* status;
 };
 
@@ -73,271 +76,285 @@ __device__ __forceinline__ uint32_t word_of(const uint4& q, int i)
     return i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
 }
 
-// Expand one 16-code word into 8 bf16 pairs in T16 storage order.
-__device__ __forceinline__ void expand_word(uint32_t w, const ScaleLut& L, uint32_t* o)
+// Selector words of a 16-code word: S_r = ((w shifted to put code r at bits
+// 4-5) & 0x30303030) | 0x04040404.  The shifts are written as multiplies so they
+// can issue on the FMA pipe next to the byte-permutes and logic ops.
+__device__ __forceinline__ void selectors(uint32_t w, uint32_t& s0, uint32_t& s1, uint32_t& s2, uint32_t& s3)
 {
-    const uint32_t s0 = code_selector<0>(w), s1 = code_selector<1>(w);
-    const uint32_t s2 = code_selector<2>(w), s3 = code_selector<3>(w);
-    o[0] = expand_pair(L, s0);
-    o[1] = expand_pair(L, s0 >> 16);
-    o[2] = expand_pair(L, s1);
-    o[3] = expand_pair(L, s1 >> 16);
-    o[4] = expand_pair(L, s2);
-    o[5] = expand_pair(L, s2 >> 16);
-    o[6] = expand_pair(L, s3);
-    o[7] = expand_pair(L, s3 >> 16);
+    s0 = ((w * 16u) & 0x30303030u) | 0x04040404u;
+    s1 = ((w * 4u) & 0x30303030u) | 0x04040404u;
+    s2 = (w & 0x30303030u) | 0x04040404u;
+    s3 = (__umulhi(w, 0x40000000u) & 0x30303030u) | 0x04040404u;
+}
+
+// Per-thread asynchronous copies global -> shared (each thread later reads back
+// exactly the bytes it copied, so a thread-local wait_group is the only sync).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ uint4 lds128(uint32_t a)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a) : "memory");
+    return r;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a)
+{
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a) : "memory");
+    return r;
+}
+
+// Per-warp ring of kDepth chunks: [slot][row a][lane] 16 code bytes, and
+// [slot][row a][lane] the 8 UE8M0 bytes of the chunk (lane-major so the 128-bit
+// reads of a warp are conflict-free).
+constexpr int kDepth = 3;
+constexpr uint32_t kRingCodeBytes = 4 * 32 * 16;   // per slot
+constexpr uint32_t kRingScaleBytes = 4 * 32 * 8;
+constexpr uint32_t kRingSlot = kRingCodeBytes + kRingScaleBytes;
+constexpr uint32_t kRingWarp = kDepth * kRingSlot;
+
+struct Rows {
+    uint4 q[4];       // 16 code bytes of the thread's 4 rows (A rows g, g+8, 16+g, 24+g)
+    uint32_t sc[4];   // their two UE8M0 bytes for this chunk
+};
+
+__device__ __forceinline__ void load_rows(Rows& R, const uint8_t* const (&cp)[4], const uint8_t* const (&sp)[4],
+                                          int ch, int c)
+{
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        R.q[a] = ldg_stream_u4(cp[a] + ch * 64 + c * 16);
+        R.sc[a] = ldg_u16(sp[a] + ch * 8 + c * 2);
+    }
+}
+
+template <bool kGateUp, int NT>
+__device__ __forceinline__ void run_item(const DecArgs& p, const uint2* lut, float (*red)[2][kMaxNT][32][4],
+                                         uint32_t ring_base, int e, int q0, int nrows, int rb, uint32_t& lut_min)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    const int nch = p.K / kChunk;
+    const int64_t rowb = p.K / 4, srowb = p.K / 32;
+
+    // the thread's four A rows: m-tile 0 -> (g, g+8), m-tile 1 -> (16+g, 24+g)
+    int64_t row[4];
+    if (kGateUp) {
+        const int64_t base = (int64_t)e * p.rows_per_expert + rb * 16;
+        row[0] = base + g;            // gate n0+g
+        row[1] = base + p.I + g;      // up   n0+g
+        row[2] = base + 8 + g;        // gate n0+8+g
+        row[3] = base + p.I + 8 + g;  // up   n0+8+g
+    } else {
+        const int64_t base = (int64_t)e * p.rows_per_expert + rb * 32;
+        row[0] = base + g;
+        row[1] = base + 8 + g;
+        row[2] = base + 16 + g;
+        row[3] = base + 24 + g;
+    }
+    const uint8_t* cp[4];
+    const uint8_t* sp[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        cp[a] = p.codes + row[a] * rowb;
+        sp[a] = p.scales + row[a] * srowb;
+    }
+    // B rows: pair j = 8*nt + g of the tile
+    const uint16_t* brow[NT];
+    bool bval[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int j = nt * 8 + g;
+        bval[nt] = j < nrows;
+        int64_t br = 0;
+        if (bval[nt]) br = kGateUp ? (int64_t)(__ldg(p.sorted + q0 + j) / p.k) : (int64_t)(q0 + j);
+        brow[nt] = p.act + br * p.K;
+    }
+
+    float acc[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+
+    // ring of this warp's chunks ch = warp + kWarps * idx
+    const uint32_t ring = ring_base + (uint32_t)warp * kRingWarp;
+    auto issue = [&](int idx) {
+        const int chq = warp + kWarps * idx;
+        if (chq < nch) {
+            const uint32_t slot = ring + (uint32_t)(idx % kDepth) * kRingSlot;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                cp_async16(slot + (uint32_t)(a * 32 + lane) * 16, cp[a] + chq * 64 + c * 16);
+                cp_async8(slot + kRingCodeBytes + (uint32_t)(a * 32 + lane) * 8, sp[a] + chq * 8);
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int d = 0; d < kDepth - 1; ++d) issue(d);
+    for (int idx = 0; warp + kWarps * idx < nch; ++idx) {
+        const int ch = warp + kWarps * idx;
+        issue(idx + kDepth - 1);
+        cp_async_wait<kDepth - 1>();
+        const uint32_t slot = ring + (uint32_t)(idx % kDepth) * kRingSlot;
+        Rows cur;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            cur.q[a] = lds128(slot + (uint32_t)(a * 32 + lane) * 16);
+            const uint2 s8 = lds64(slot + kRingCodeBytes + (uint32_t)(a * 32 + lane) * 8);
+            const uint32_t wsc = (c & 2) ? s8.y : s8.x;
+            cur.sc[a] = (c & 1) ? (wsc >> 16) : (wsc & 0xFFFFu);
+        }
+        uint2 L[4][2];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            L[a][0] = lut[cur.sc[a] & 0xFF];
+            L[a][1] = lut[cur.sc[a] >> 8];
+            lut_min = min(lut_min, min(L[a][0].x, L[a][1].x));
+        }
+        const int boff = ch * kChunk + c * 64;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint4 B0[NT], B1[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (bval[nt]) {
+                    B0[nt] = ldg_u4(brow[nt] + boff + i * 16);
+                    B1[nt] = ldg_u4(brow[nt] + boff + i * 16 + 8);
+                } else {
+                    B0[nt] = make_uint4(0, 0, 0, 0);
+                    B1[nt] = make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const uint32_t wa = word_of(cur.q[2 * mt], i), wb = word_of(cur.q[2 * mt + 1], i);
+                const uint2 la = L[2 * mt][i >> 1], lb = L[2 * mt + 1][i >> 1];
+                const ScaleLut LA{la.x, la.y}, LB{lb.x, lb.y};
+                uint32_t sa[4], sb[4];
+                selectors(wa, sa[0], sa[1], sa[2], sa[3]);
+                selectors(wb, sb[0], sb[1], sb[2], sb[3]);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    uint32_t afrag[4];
+                    afrag[0] = expand_pair(LA, sa[r]);
+                    afrag[1] = expand_pair(LB, sb[r]);
+                    afrag[2] = expand_pair(LA, __umulhi(sa[r], 0x10000u));
+                    afrag[3] = expand_pair(LB, __umulhi(sb[r], 0x10000u));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint4& Bv = (r < 2) ? B0[nt] : B1[nt];
+                        mma_bf16_16816(acc[mt][nt], afrag, (r & 1) ? Bv.z : Bv.x, (r & 1) ? Bv.w : Bv.y);
+                    }
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+
+    // split-K reduction in warp order
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) red[warp][mt][nt][lane][v] = acc[mt][nt][v];
+    __syncthreads();
+    // warp w finalises m-tile (w & 1), n-tile (w >> 1)
+    const int mt = warp & 1;
+    for (int nt = warp >> 1; nt < NT; nt += 2) {
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) s += red[w][mt][nt][lane][q];
+            v[q] = s;
+        }
+        if (kGateUp) {
+            const int pos = t16_pos(rb * 16 + mt * 8 + g);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = nt * 8 + 2 * c + h;
+                if (j < nrows) {
+                    __nv_bfloat16 hb = __float2bfloat16_rn(silu_f(v[h]) * v[2 + h]);
+                    p.h_t16[(int64_t)(q0 + j) * p.I + pos] = *reinterpret_cast<uint16_t*>(&hb);
+                }
+            }
+        } else {
+            const int m = rb * 32 + mt * 16 + g;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = nt * 8 + 2 * c + h;
+                if (j < nrows) {
+                    const int pr = __ldg(p.sorted + q0 + j);
+                    const float wt = __ldg(p.weights + pr);
+                    p.stage[(int64_t)pr * p.H + m] = wt * v[h];
+                    p.stage[(int64_t)pr * p.H + m + 8] = wt * v[2 + h];
+                }
+            }
+        }
+    }
+    __syncthreads();
 }
 
 template <bool kGateUp>
-__global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const __grid_constant__ CUtensorMap cmap,
-                                                             const __grid_constant__ CUtensorMap bmap,
-                                                             DecodeParams p)
+__global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS) decode_kernel(DecArgs p)
 {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t cfull_bar[kSC];    // code tile landed (TMA bytes)
-    __shared__ __align__(8) uint64_t cempty_bar[kSC];   // code tile consumed by its expander group (128)
-    __shared__ __align__(8) uint64_t bfull_bar[kSB];    // activation tile landed (TMA bytes)
-    __shared__ __align__(8) uint64_t bempty_bar[kSB];   // MMAs reading it done (commit)
-    __shared__ __align__(8) uint64_t afull_bar[kSA];    // expanded A in TMEM (128)
-    __shared__ __align__(8) uint64_t aempty_bar[kSA];   // MMAs reading it done (commit)
-    __shared__ __align__(8) uint64_t dfull_bar;         // accumulator complete (commit)
-    __shared__ __align__(8) uint64_t dempty_bar;        // epilogue done reading D (256)
-    __shared__ uint32_t tmem_base_sh;
-    __shared__ int abort_flag;
-    __shared__ uint2 lut_tab[256];
-
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t* b_ring = smem;                           // kSB x 16 KB (1 KB aligned)
-    uint8_t* code_ring = smem + kSB * kBBytes;        // kSC x 4 KB
-    const uint32_t code_ring_s = smem_u32(code_ring), b_ring_s = smem_u32(b_ring);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    for (int s = tid; s < 256; s += kThreads) {
+    __shared__ uint2 lut[256];
+    __shared__ float red[kWarps][2][kMaxNT][32][4];
+    __shared__ int last_flag;
+    extern __shared__ __align__(16) uint8_t ring_smem[];   // kWarps * kRingWarp bytes
+    const uint32_t ring_base = (uint32_t)__cvta_generic_to_shared(ring_smem);
+    for (int s = threadIdx.x; s < 256; s += kThreads) {
         ScaleLut l = make_lut((uint32_t)s);
-        lut_tab[s] = make_uint2(l.lut, l.lo);
+        lut[s] = make_uint2(l.lut, l.lo);
     }
-    if (tid == 0) {
-        for (int s = 0; s < kSC; ++s) {
-            mbar_init(smem_u32(&cfull_bar[s]), 1);
-            mbar_init(smem_u32(&cempty_bar[s]), 128);
-        }
-        for (int s = 0; s < kSB; ++s) {
-            mbar_init(smem_u32(&bfull_bar[s]), 1);
-            mbar_init(smem_u32(&bempty_bar[s]), 1);
-        }
-        for (int s = 0; s < kSA; ++s) {
-            mbar_init(smem_u32(&afull_bar[s]), 128);
-            mbar_init(smem_u32(&aempty_bar[s]), 1);
-        }
-        mbar_init(smem_u32(&dfull_bar), 1);
-        mbar_init(smem_u32(&dempty_bar), kGroups * 128);
-        abort_flag = 0;
-        mbar_fence_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_base_sh;
-    volatile int* abort = &abort_flag;
 
-    const int n_items = *p.tile_count * p.row_blocks;
-    const int nk = p.K / kKS;
-
-    if (warp < kGroups * 4) {
-        // ------------------------------------------------ expanders + epilogue
-        const int grp = warp >> 2, r = tid & 127, wq = warp & 3;
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * wq) << 16);
-        // A row r sits in code-tile row crow; its two 16-byte chunks are read in
-        // the order (sw, sw^1) so 8 consecutive threads touch 8 distinct banks.
-        const int crow = kGateUp ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;
-        const int sw = kGateUp ? (r & 1) : ((r >> 2) & 1);
-        uint32_t g = 0, items_done = 0, lut_min = 0xFFFFFFFFu;
-        for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
-            const int4 tile = p.tiles[it / p.row_blocks];
-            const int rb = it % p.row_blocks;
-            const int e = tile.x, q0 = tile.y, nrows = tile.z;
-            const int row = kGateUp ? ((r & 1 ? p.I : 0) + rb * 64 + (r >> 1)) : rb * 128 + r;
-            const uint32_t* rs =
-                reinterpret_cast<const uint32_t*>(p.scales + ((int64_t)e * p.rows_per_expert + row) * (p.K / 32));
-            // stage gs = g + kk belongs to group gs % kGroups
-            const int kk0 = (int)(((uint32_t)grp + kGroups - (g % kGroups)) % kGroups);
-            uint32_t sq[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) sq[u] = (kk0 + kGroups * u < nk) ? __ldg(rs + kk0 + kGroups * u) : 0u;
-
-            bool ok = true;
-            for (int kb = kk0; kb < nk && ok; kb += 4 * kGroups) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int kk = kb + kGroups * u;
-                    if (kk >= nk) break;
-                    const uint32_t sc = sq[u];
-                    sq[u] = (kk + 4 * kGroups < nk) ? __ldg(rs + kk + 4 * kGroups) : 0u;
-                    const uint32_t gs = g + kk;
-                    const uint32_t cs = gs % kSC, cph = (gs / kSC) & 1u;
-                    const uint32_t as = gs % kSA, aph = (gs / kSA) & 1u;
-                    if (!mbar_wait(smem_u32(&cfull_bar[cs]), cph, abort)) {
-                        ok = false;
-                        break;
+    const int n_tiles = *p.tile_count;
+    const int n_items = n_tiles * p.row_blocks;
+    uint32_t lut_min = 0xFFFFFFFFu;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int4 tile = p.tiles[it / p.row_blocks];
+        const int rb = it % p.row_blocks;
+        const int nt = (tile.z + 7) >> 3;
+        if (nt == 1) run_item<kGateUp, 1>(p, lut, red, ring_base, tile.x, tile.y, tile.z, rb, lut_min);
+        else run_item<kGateUp, 2>(p, lut, red, ring_base, tile.x, tile.y, tile.z, rb, lut_min);
+        if (!kGateUp) {
+            // The last of the n_tiles items that wrote rows [32 rb, 32 rb + 32) of
+            // the pair slots sums them into y (fixed j order per token).
+            __threadfence();
+            if (threadIdx.x == 0) last_flag = (atomicAdd(p.counters + rb, 1) == n_tiles - 1);
+            __syncthreads();
+            if (last_flag) {
+                __threadfence();
+                for (int i = threadIdx.x; i < p.T * 32; i += kThreads) {
+                    const int t = i >> 5, m = rb * 32 + (i & 31);
+                    float s = 0.f;
+                    for (int j = 0; j < p.k; ++j) {
+                        const int ej = __ldg(p.ids + t * p.k + j);
+                        if ((unsigned)ej < (unsigned)p.E) s += __ldcg(p.stage + (int64_t)(t * p.k + j) * p.H + m);
                     }
-                    const uint32_t ct = code_ring_s + cs * kCodeBytes + crow * 32;
-                    const uint4 f = lds_u4(ct + 16 * sw);
-                    const uint4 s2 = lds_u4(ct + 16 * (sw ^ 1));
-                    const uint4 ch0 = sw ? s2 : f, ch1 = sw ? f : s2;
-                    const uint2 t0 = lut_tab[sc & 0xFF], t1 = lut_tab[(sc >> 8) & 0xFF];
-                    const uint2 t2 = lut_tab[(sc >> 16) & 0xFF], t3 = lut_tab[sc >> 24];
-                    lut_min = min(lut_min, min(min(t0.x, t1.x), min(t2.x, t3.x)));
-                    if (!mbar_wait(smem_u32(&aempty_bar[as]), aph ^ 1u, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    uint32_t regs[32];
-                    expand_word(ch0.x, ScaleLut{t0.x, t0.y}, regs + 0);
-                    expand_word(ch0.y, ScaleLut{t0.x, t0.y}, regs + 8);
-                    expand_word(ch0.z, ScaleLut{t1.x, t1.y}, regs + 16);
-                    expand_word(ch0.w, ScaleLut{t1.x, t1.y}, regs + 24);
-                    const uint32_t acol = lane_addr + kACol + as * 64;
-                    tmem_st32_sync(acol, regs);
-                    expand_word(ch1.x, ScaleLut{t2.x, t2.y}, regs + 0);
-                    expand_word(ch1.y, ScaleLut{t2.x, t2.y}, regs + 8);
-                    expand_word(ch1.z, ScaleLut{t3.x, t3.y}, regs + 16);
-                    expand_word(ch1.w, ScaleLut{t3.x, t3.y}, regs + 24);
-                    tmem_st32_sync(acol + 32, regs);
-                    tc_fence_before();
-                    mbar_arrive(smem_u32(&afull_bar[as]));
-                    // Release the code tile only once its bytes are in TMEM.  Releasing
-                    // right after the shared loads let the next TMA fill of the slot
-                    // corrupt rows that were still being read (seen at T=32 with two
-                    // CTAs per SM); this ordering was verified race-free.
-                    mbar_arrive(smem_u32(&cempty_bar[cs]));
+                    __nv_bfloat16 yb = __float2bfloat16_rn(s);
+                    p.y[(int64_t)t * p.H + m] = *reinterpret_cast<uint16_t*>(&yb);
                 }
+                if (threadIdx.x == 0) p.counters[rb] = 0;
             }
-            g += nk;
-            if (!ok || *abort) break;
-
-            // epilogue: this group's 32 accumulator columns (pairs c0 .. c0+31)
-            if (!mbar_wait(smem_u32(&dfull_bar), items_done & 1u, abort)) break;
-            ++items_done;
-            tc_fence_after();
-            for (int c0 = 32 * grp; c0 < nrows; c0 += 32 * kGroups) {
-                float v[32];
-                tmem_ld32(lane_addr + kDCol + c0, v);
-                if (kGateUp) {
-                    const int pos = t16_pos(rb * 64 + (r >> 1));
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float up = __shfl_down_sync(0xffffffffu, v[j], 1);
-                        if (!(r & 1) && c0 + j < nrows) {
-                            __nv_bfloat16 hb = __float2bfloat16_rn(silu_f(v[j]) * up);
-                            p.h_t16[(int64_t)(q0 + c0 + j) * p.I + pos] = *reinterpret_cast<uint16_t*>(&hb);
-                        }
-                    }
-                } else {
-                    const int m = rb * 128 + r;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if (c0 + j < nrows) {
-                            const int pr = __ldg(p.sorted + q0 + c0 + j);
-                            p.stage[(int64_t)pr * p.H + m] = __ldg(p.weights + pr) * v[j];
-                        }
-                    }
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(smem_u32(&dempty_bar));
-        }
-        if (lut_min == 0) flag_status(p.status, MOE_W2_DEV_BAD_SCALE);
-    } else if (warp == kGroups * 4) {
-        // ------------------------------------------------ code-tile producer (TMA)
-        if (lane == 0) {
-            prefetch_tmap(&cmap);
-            uint32_t g = 0;
-            for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
-                const int4 tile = p.tiles[it / p.row_blocks];
-                const int rb = it % p.row_blocks;
-                const int e = tile.x;
-                const int rowA = kGateUp ? e * p.rows_per_expert + rb * 64 : e * p.rows_per_expert + rb * 128;
-                const int rowB = kGateUp ? rowA + p.I : rowA + 64;
-                for (int kk = 0; kk < nk; ++kk) {
-                    const uint32_t gs = g + kk, cs = gs % kSC, ph = (gs / kSC) & 1u;
-                    if (!mbar_wait(smem_u32(&cempty_bar[cs]), ph ^ 1u, abort)) break;
-                    const uint32_t fb = smem_u32(&cfull_bar[cs]);
-                    mbar_arrive_expect_tx(fb, kCodeBytes);
-                    const uint32_t cdst = code_ring_s + cs * kCodeBytes;
-                    tma_load_2d(cdst, &cmap, kk * 32, rowA, fb);
-                    tma_load_2d(cdst + 64 * 32, &cmap, kk * 32, rowB, fb);
-                }
-                g += nk;
-            }
-        }
-    } else if (warp == kGroups * 4 + 1) {
-        // ------------------------------------------------ activation-tile producer (TMA)
-        if (lane == 0) {
-            prefetch_tmap(&bmap);
-            uint32_t g = 0;
-            for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
-                const int4 tile = p.tiles[it / p.row_blocks];
-                const int q0 = tile.y, npad = (tile.z + 15) & ~15;
-                for (int kk = 0; kk < nk; ++kk) {
-                    const uint32_t gs = g + kk, bs = gs % kSB, ph = (gs / kSB) & 1u;
-                    if (!mbar_wait(smem_u32(&bempty_bar[bs]), ph ^ 1u, abort)) break;
-                    const uint32_t fb = smem_u32(&bfull_bar[bs]);
-                    mbar_arrive_expect_tx(fb, (uint32_t)npad * 256u);
-                    const uint32_t bdst = b_ring_s + bs * kBBytes;
-                    for (int a = 0; a < 2; ++a)
-                        for (int j = 0; j < npad / 16; ++j)
-                            tma_load_2d(bdst + a * kBAtom + j * 2048u, &bmap, kk * kKS + a * 64, q0 + 16 * j, fb);
-                }
-                g += nk;
-            }
-        }
-    } else {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t g = 0, items = 0;
-            for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
-                const int4 tile = p.tiles[it / p.row_blocks];
-                const uint32_t npad = (tile.z + 15) & ~15;
-                const uint32_t idesc = idesc_bf16_f32(128, npad);
-                if (!mbar_wait(smem_u32(&dempty_bar), (items & 1u) ^ 1u, abort)) break;
-                tc_fence_after();
-                for (int kk = 0; kk < nk; ++kk) {
-                    const uint32_t gs = g + kk;
-                    const uint32_t as = gs % kSA, aph = (gs / kSA) & 1u;
-                    const uint32_t bs = gs % kSB, bph = (gs / kSB) & 1u;
-                    if (!mbar_wait(smem_u32(&afull_bar[as]), aph, abort) ||
-                        !mbar_wait(smem_u32(&bfull_bar[bs]), bph, abort))
-                        break;
-                    tc_fence_after();
-                    const uint32_t a_t = tmem + kACol + as * 64;
-                    const uint32_t b_s = b_ring_s + bs * kBBytes;
-#pragma unroll
-                    for (int k16 = 0; k16 < 8; ++k16)
-                        umma_f16_ts(tmem + kDCol, a_t + 8 * k16,
-                                    smem_desc_sw128(b_s + (k16 >> 2) * kBAtom) + 2 * (k16 & 3), idesc,
-                                    (kk | k16) != 0);
-                    umma_commit(smem_u32(&aempty_bar[as]));
-                    umma_commit(smem_u32(&bempty_bar[bs]));
-                }
-                umma_commit(smem_u32(&dfull_bar));
-                ++items;
-                g += nk;
-            }
+            __syncthreads();
         }
     }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
-    }
-    if (tid == 0 && abort_flag) flag_status(p.status, kDevPipelineTimeout);
+    if (lut_min == 0) flag_status(p.status, MOE_W2_DEV_BAD_SCALE);
 }
 
 }  // namespace
@@ -346,62 +363,60 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
                           int32_t T, int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status, cudaStream_t s,
                           const PhaseEvents& ev)
 {
+    (void)x;
     const int32_t E = w.num_experts, H = w.hidden, I = w.inter;
     const int64_t P = (int64_t)T * k;
-    // 100 KB of dynamic shared memory keeps it at two CTAs per SM (2 x 256 TMEM columns)
-    constexpr int kDynSmem = 100 * 1024;
-    static_assert(kSmemBytes <= kDynSmem, "shared-memory budget");
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kDynSmem);
+    constexpr int kDyn = kWarps * kRingWarp;
+    static int occ = 0;
+    if (occ == 0) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(tc_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+        e = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<true>, kThreads, kDyn);
+        if (e != cudaSuccess) return e;
+        occ = std::max(occ, 1);
     }
-    const int sms = sm_count();
-    cudaError_t e = launch_gather(x, ws.sorted, ws.offsets, E, k, H, P, ws.xa, s);
-    if (e != cudaSuccess) return e;
+    const int64_t grid_max = (int64_t)sm_count() * occ;
+    const int64_t tiles = max_tiles(P, E, true);
 
-    CUtensorMap c13, c2, xmap, hmap;
-    if ((e = make_tmap_2d(&c13, w.w13_codes, false, (int64_t)E * 2 * I, H / 4, 32, 64, false)) != cudaSuccess) return e;
-    if ((e = make_tmap_2d(&c2, w.w2_codes, false, (int64_t)E * H, I / 4, 32, 64, false)) != cudaSuccess) return e;
-    if ((e = make_tmap_2d(&xmap, ws.xa, true, P, H, 64, 16, true)) != cudaSuccess) return e;
-    if ((e = make_tmap_2d(&hmap, ws.h, true, P, I, 64, 16, true)) != cudaSuccess) return e;
-
-    DecodeParams gp{};
+    DecArgs gp{};
+    gp.codes = w.w13_codes;
+    gp.scales = w.w13_scales;
     gp.K = H;
     gp.rows_per_expert = 2 * I;
     gp.I = I;
     gp.H = H;
+    gp.T = T;
     gp.k = k;
-    gp.row_blocks = I / 64;
-    gp.scales = w.w13_scales;
+    gp.E = E;
+    gp.row_blocks = I / 16;
     gp.tiles = ws.tiles;
     gp.tile_count = ws.tile_count;
     gp.sorted = ws.sorted;
     gp.weights = weights;
+    gp.ids = ids;
+    gp.act = ws.xa;
     gp.h_t16 = ws.h;
     gp.stage = ws.stage;
+    gp.counters = ws.counters;
+    gp.y = y;
     gp.status = status;
-    const int64_t tiles = max_tiles(P, E, true);
-    if ((e = ev.record(1, s)) != cudaSuccess) return e;
-    tc_decode_kernel<true><<<(int)std::min<int64_t>(tiles * (I / 64), 2 * (int64_t)sms), kThreads, kDynSmem, s>>>(
-        c13, xmap, gp);
+    cudaError_t e = ev.record(1, s);
+    if (e != cudaSuccess) return e;
+    decode_kernel<true><<<(int)std::min<int64_t>(tiles * gp.row_blocks, grid_max), kThreads, kDyn, s>>>(gp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-    DecodeParams dp = gp;
+    DecArgs dp = gp;
+    dp.codes = w.w2_codes;
+    dp.scales = w.w2_scales;
     dp.K = I;
     dp.rows_per_expert = H;
-    dp.row_blocks = H / 128;
-    dp.scales = w.w2_scales;
+    dp.row_blocks = H / 32;
+    dp.act = ws.h;
     if ((e = ev.record(2, s)) != cudaSuccess) return e;
-    tc_decode_kernel<false><<<(int)std::min<int64_t>(tiles * (H / 128), 2 * (int64_t)sms), kThreads, kDynSmem, s>>>(
-        c2, hmap, dp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    (void)ids;
-    return launch_combine(ws.stage, ids, T, k, E, H, y, s);
+    decode_kernel<false><<<(int)std::min<int64_t>(tiles * dp.row_blocks, grid_max), kThreads, kDyn, s>>>(dp);
+    return cudaGetLastError();
 }
 
 }  // namespace moe_w2

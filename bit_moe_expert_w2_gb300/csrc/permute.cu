@@ -10,7 +10,10 @@
 // order and writes every pair at its cursor (ranks within a 32-pair step come
 // from match_any), so the result is the stable order without any sort network.
 // The same launch also emits the active-expert list (decode scheduling) and the
-// GEMM tile list (expert, first slot, pairs) with at most tile_rows pairs per tile.
+// GEMM tile list (expert, first slot, pairs) with at most tile_rows pairs per tile.  Extra CTAs of the
+// launch re-lay x in T16 order for the decode kernels.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe_w2 {
@@ -56,12 +59,41 @@ __device__ int cta_exclusive_scan(int v, int* warp_tmp, int* total)
     return base + x - v;
 }
 
+// x [rows][H] -> x_t16 [rows][H]: 4x4 transpose inside each group of 16.
+__device__ __forceinline__ void t16_group(const uint16_t* src, uint16_t* dst)
+{
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(src + 8));
+    // natural words: a.x=(x0,x1) a.y=(x2,x3) a.z=(x4,x5) a.w=(x6,x7) b.x=(x8,x9) ...
+    uint4 o, p;
+    o.x = __byte_perm(a.x, a.z, 0x5410);  // (x0, x4)
+    o.y = __byte_perm(b.x, b.z, 0x5410);  // (x8, x12)
+    o.z = __byte_perm(a.x, a.z, 0x7632);  // (x1, x5)
+    o.w = __byte_perm(b.x, b.z, 0x7632);  // (x9, x13)
+    p.x = __byte_perm(a.y, a.w, 0x5410);  // (x2, x6)
+    p.y = __byte_perm(b.y, b.w, 0x5410);  // (x10, x14)
+    p.z = __byte_perm(a.y, a.w, 0x7632);  // (x3, x7)
+    p.w = __byte_perm(b.y, b.w, 0x7632);  // (x11, x15)
+    *reinterpret_cast<uint4*>(dst) = o;
+    *reinterpret_cast<uint4*>(dst + 8) = p;
+}
+
 __global__ void __launch_bounds__(kThreads) permute_kernel(
     const int32_t* __restrict__ ids, int32_t P, int32_t E, int32_t* __restrict__ sorted,
     int32_t* __restrict__ inv, int32_t* __restrict__ offsets, int32_t* __restrict__ active,
     int32_t* __restrict__ active_count, int4* __restrict__ tiles, int32_t* __restrict__ tile_count,
-    int32_t tile_rows, uint32_t* status)
+    int32_t tile_rows, const uint16_t* __restrict__ x, uint16_t* __restrict__ x_t16, int64_t n_groups,
+    int32_t* __restrict__ counters, int32_t n_counters, uint16_t* __restrict__ y, int64_t y_elems,
+    uint32_t* status)
 {
+    if (blockIdx.x > 0) {
+        // extra CTAs: x in T16 order (decode reads activation rows per pair from it)
+        const int64_t stride = (int64_t)(gridDim.x - 1) * blockDim.x;
+        for (int64_t g = (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x; g < n_groups; g += stride)
+            t16_group(x + g * 16, x_t16 + g * 16);
+        return;
+    }
+    for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
     extern __shared__ int32_t smem[];
     __shared__ int warp_tmp[kWarps];
     __shared__ int sh_total;
@@ -124,6 +156,12 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
         if (tid == 0) *active_count = sh_total;
     }
 
+    if (y != nullptr) {
+        // no valid pair at all: nothing will write y, so it is zeroed here
+        __syncthreads();
+        if (soff[E] == 0)
+            for (int64_t i = tid; i < y_elems; i += kThreads) y[i] = 0;
+    }
     if (tiles != nullptr) {
         const int n0 = (b0 < E) ? (t0 + tile_rows - 1) / tile_rows : 0;
         const int n1 = (b1 < E) ? (t1 + tile_rows - 1) / tile_rows : 0;
@@ -182,7 +220,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
 
 cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* sorted, int32_t* inv,
                            int32_t* offsets, int32_t* active, int32_t* active_count, int4* tiles,
-                           int32_t* tile_count, int32_t tile_rows, uint32_t* status, cudaStream_t s)
+                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16, int32_t H,
+                           int32_t* counters, int32_t n_counters, uint16_t* y, uint32_t* status, cudaStream_t s)
 {
     const int32_t P = T * k;
     const size_t smem = sizeof(int32_t) * (size_t)(kWarps + 1) * (E + 1);
@@ -193,8 +232,15 @@ cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    permute_kernel<<<1, kThreads, smem, s>>>(ids, P, E, sorted, inv, offsets, active, active_count, tiles,
-                                             tile_count, tile_rows, status);
+    int64_t n_groups = 0;
+    int extra = 0;
+    if (x != nullptr && x_t16 != nullptr) {
+        n_groups = (int64_t)T * H / 16;
+        extra = (int)std::min<int64_t>((n_groups + kThreads - 1) / kThreads, 4 * (int64_t)sm_count());
+    }
+    permute_kernel<<<1 + extra, kThreads, smem, s>>>(ids, P, E, sorted, inv, offsets, active, active_count, tiles,
+                                                     tile_count, tile_rows, x, x_t16, n_groups, counters,
+                                                     n_counters, y, y ? (int64_t)T * H : 0, status);
     return cudaGetLastError();
 }
 

@@ -81,9 +81,10 @@ typedef struct {
 
 /* Bytes of device workspace moe_w2_forward needs for these sizes (0 if the sizes
  * are invalid).  The workspace holds the permutation, the expert-sorted and
- * re-laid-out activations, the SiLU(gate)*up intermediate h (bf16, P x I) and,
- * for T > MOE_W2_DECODE_MAX_TOKENS, the fp32 per-pair staging of the
- * deterministic combine (P x H).  Its contents need no initialisation. */
+ * re-laid-out activations, the SiLU(gate)*up intermediate h (bf16, P x I), the
+ * fp32 per-pair staging of the deterministic combine (P x H) and the decode
+ * path's per-row-block completion counters.  Its contents need no
+ * initialisation: every call writes each part before reading it. */
 size_t moe_w2_forward_workspace_size(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t I);
 
 /*

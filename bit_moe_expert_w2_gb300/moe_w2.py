@@ -22,6 +22,7 @@ DEV_BAD_EXPERT_ID = 1
 DEV_BAD_SCALE = 2
 DEV_BAD_NVFP4 = 4
 DECODE_MAX_TOKENS = 64
+NOALLOC_WORKSPACE_BYTES = 4 << 20   # MOE_W2_NOALLOC_WORKSPACE_BYTES
 
 
 class MoeW2Error(RuntimeError):
@@ -61,6 +62,8 @@ def load(build_if_missing: bool = True):
     L.moe_w2_permute.restype = ctypes.c_int
     L.moe_w2_forward.argtypes = [vp, vp, vp, ctypes.POINTER(Planes), i32, i32, vp, vp, sz, vp, vp]
     L.moe_w2_forward.restype = ctypes.c_int
+    L.moe_w2_forward_noalloc.argtypes = [vp, vp, vp, ctypes.POINTER(Planes), i32, i32, vp, vp, vp]
+    L.moe_w2_forward_noalloc.restype = ctypes.c_int
     L.moe_w2_requant.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
     L.moe_w2_requant.restype = ctypes.c_int
     _lib = L
@@ -123,6 +126,26 @@ def forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
                           _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
     if st != OK:
         raise MoeW2Error(st, "moe_w2_forward")
+    return y
+
+
+def forward_noalloc(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, planes, y=None,
+                    status=None, stream=None) -> torch.Tensor:
+    """moe_w2_forward_noalloc: the forward with its scratch in the library's own device array
+    (for callers that cannot allocate device memory).  Pass y to allocate nothing here either."""
+    L = load()
+    _check_cuda(x, "x", torch.bfloat16)
+    _check_cuda(topk_ids, "topk_ids", torch.int32)
+    _check_cuda(topk_weights, "topk_weights", torch.float32)
+    p = planes if isinstance(planes, Planes) else make_planes(planes)
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    st = L.moe_w2_forward_noalloc(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), ctypes.byref(p), T, k, _ptr(y),
+                                  _ptr(status), _stream(stream))
+    if st != OK:
+        raise MoeW2Error(st, "moe_w2_forward_noalloc")
     return y
 
 

@@ -25,11 +25,12 @@
  *
  * Conventions for every entry point:
  *   - Every buffer is owned by the caller and lives in device memory unless
- *     stated otherwise.  The library allocates nothing, frees nothing and
- *     never synchronises: work is enqueued on `stream` (a cudaStream_t, NULL =
+ *     stated otherwise (moe_w2_forward_noalloc's scratch is the library's).
+ *     The library allocates nothing, frees nothing and never synchronises:
+ *     work is enqueued on `stream` (a cudaStream_t, NULL =
  *     the legacy default stream) and completes asynchronously.  No entry point
  *     reads a device value on the host, so all of them can be captured in a
- *     CUDA graph.
+ *     CUDA graph (this remark does not extend to moe_w2_forward_noalloc).
  *   - Host-side argument checks return a status code and enqueue nothing.
  *   - Device-side input errors never trap: they OR a bit into *dev_status
  *     (a device uint32 the caller zeroes and reads back; NULL = do not report)
@@ -139,6 +140,31 @@ moe_w2_status moe_w2_forward_traced(const void *x_bf16, const int32_t *topk_ids,
                                     const moe_w2_planes *w, int32_t T, int32_t top_k, void *y_bf16,
                                     void *workspace, size_t workspace_bytes, uint32_t *dev_status,
                                     void *stream, void *const *phase_events);
+
+/*
+ * moe_w2_forward without a caller-supplied workspace, for callers that cannot
+ * allocate device memory where they run the layer (an allocator that may not
+ * grow, device memory already handed out in full, or a point where an
+ * allocation would synchronise the device).  The paper has no counterpart:
+ * it is an interface addition of this library.
+ * Same arguments, results and status codes as moe_w2_forward, minus
+ * workspace and workspace_bytes: the scratch is a device array of
+ * MOE_W2_NOALLOC_WORKSPACE_BYTES that the library owns; each GPU that loads
+ * the library's device code holds it until the process exits.
+ *   - Sizes whose moe_w2_forward_workspace_size() exceeds
+ *     MOE_W2_NOALLOC_WORKSPACE_BYTES return MOE_W2_ERR_WORKSPACE and enqueue
+ *     nothing (at H=6144, I=2048, E=256, top_k=8 that is T > 17).
+ *   - The first call on each device looks up the array's address
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *     first call before any stream capture starts.
+ *   - Every call on a device uses the same array, so calls that may run at
+ *     the same time race: order them (e.g. issue them on one stream).
+ *   - Nothing in the array needs to start at zero.
+ */
+#define MOE_W2_NOALLOC_WORKSPACE_BYTES (4u << 20)
+moe_w2_status moe_w2_forward_noalloc(const void *x_bf16, const int32_t *topk_ids, const float *topk_weights,
+                                     const moe_w2_planes *w, int32_t T, int32_t top_k, void *y_bf16,
+                                     uint32_t *dev_status, void *stream);
 
 /*
  * Load-time re-quantizer ("The v0.24.0 port", "Our hooks", modelopt.py

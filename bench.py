@@ -447,7 +447,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = {"decode_t1": 1000, "decode_t32": 500, "prefill_t8192": 50}.get(args.config, 10)
+        args.steps = {"decode_t1": 4000, "decode_t32": 1000, "prefill_t8192": 100,
+                      "decode_t1_e32": 4000, "prefill_t1024_e32": 400}.get(args.config, 10)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -13,9 +13,11 @@
 // tcgen05.mma (M=128, K=16) of a CTA costs ~105 cycles whatever N is (measured
 // on GB300), which caps a CTA far below HBM rate, while mma.sync m16n8k16 keeps
 // the weights in registers and reaches the full tensor rate with enough warps.
-// The expansion is integer work (~0.75 byte-permute/logic op per weight plus
-// shifts written as multiplies) and the kernel is sized to keep ~16 warps per SM
-// streaming codes through a per-thread cp.async ring (3 chunks deep).
+// The expansion is integer work split over two pipes: per 16-code word two
+// masks and eight byte-permutes on the ALU pipe, and the eight selector words as
+// multiply-adds on the FMA pipe (the multipliers are kernel parameters, so they
+// stay multiply-adds instead of becoming ALU shifts).  Codes stream through a
+// per-warp cp.async ring (3 chunks deep).
 //
 // Per 256-wide K chunk a row is 64 code bytes; thread c of a quad owns bytes
 // [16c, 16c+16), i.e. four 16-code words; MMA (word i, r) takes codes (r, r+4)
@@ -69,6 +71,7 @@ struct DecArgs {
     int32_t* counters;         // down: per 32-row block of y
     uint16_t* y;
     uint32_t* status;
+    uint32_t mul[8];           // 16, 4, 2^30, 2^20, 2^18, 2^14, -, - (selector multipliers)
 };
 
 __device__ __forceinline__ uint32_t word_of(const uint4& q, int i)
@@ -76,19 +79,70 @@ __device__ __forceinline__ uint32_t word_of(const uint4& q, int i)
     return i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
 }
 
-// Selector words of a 16-code word: S_r = ((w shifted to put code r at bits
-// 4-5) & 0x30303030) | 0x04040404.  The shifts are written as multiplies so they
-// can issue on the FMA pipe next to the byte-permutes and logic ops.
-__device__ __forceinline__ void selectors(uint32_t w, uint32_t& s0, uint32_t& s1, uint32_t& s2, uint32_t& s3)
+__device__ __forceinline__ uint32_t mad_lo(uint32_t a, uint32_t b, uint32_t c)
 {
-    s0 = ((w * 16u) & 0x30303030u) | 0x04040404u;
-    s1 = ((w * 4u) & 0x30303030u) | 0x04040404u;
-    s2 = (w & 0x30303030u) | 0x04040404u;
-    s3 = (__umulhi(w, 0x40000000u) & 0x30303030u) | 0x04040404u;
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// Byte-permute with the selector used as is: every selector nibble built below
+// has bit 3 clear, so it needs no masking (the __byte_perm intrinsic promises to
+// use only 3 bits of each nibble).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
 }
 
-// Per-thread asynchronous copies global -> shared (each thread later reads back
-// exactly the bytes it copied, so a thread-local wait_group is the only sync).
+// Selector words of a 16-code word w (code i in bits 2i..2i+1) for the bf16
+// pairs (c_r, c_{r+4}) [lo] and (c_{r+8}, c_{r+12}) [hi].  In each selector byte
+// the high nibble is the code (0..3: a byte of the lut word) and the low nibble
+// is 4 | (any two bits) (a byte of the lo word); the byte-permute reads only the
+// low 16 bits of a selector, so only those are kept exact.  From
+//   mp  = (w & 0x33333333) | 0x04040404   codes 4b, 4b+2 of byte b, plus 4 per byte
+//   m2p = (w & 0xCCCCCCCC) | 0x10101010   codes 4b+1, 4b+3, plus 0x10 per byte
+// (one logic op each) the eight selectors are
+//   lo: r=0 mp*16 - 0x3C3C3C3C   r=1 m2p*4 - 0x3C3C3C3C   r=2 mp   r=3 m2p >> 2
+//   hi: r=0 (mp >> 12) - 0x3C3C  r=1 (m2p >> 14) - 0x3C3C  r=2 mp >> 16   r=3 m2p >> 18
+// (the subtractions remove the shifted 0x04/0x10 fill, leaving 0x04 per byte).
+// mp >> 16 is a shift on the ALU pipe; the other six are multiply-adds (right
+// shifts as the high word of a product) on the FMA pipe, which keeps the two
+// pipes about equally loaded next to the eight byte-permutes.
+struct Masks {
+    uint32_t mp, m2p;
+};
+__device__ __forceinline__ Masks word_masks(uint32_t w)
+{
+    return Masks{(w & 0x33333333u) | 0x04040404u, (w & 0xCCCCCCCCu) | 0x10101010u};
+}
+constexpr uint32_t kFixLo = 0xC3C3C3C4u;   // -0x3C3C3C3C
+constexpr uint32_t kFixHi = 0xFFFFC3C4u;   // -0x3C3C
+template <int R>
+__device__ __forceinline__ uint32_t sel_lo(const Masks& s, const uint32_t (&mul)[8])
+{
+    if (R == 0) return mad_lo(s.mp, mul[0], kFixLo);
+    if (R == 1) return mad_lo(s.m2p, mul[1], kFixLo);
+    if (R == 2) return s.mp;
+    return mad_hi(s.m2p, mul[2], 0u);
+}
+template <int R>
+__device__ __forceinline__ uint32_t sel_hi(const Masks& s, const uint32_t (&mul)[8])
+{
+    if (R == 0) return mad_hi(s.mp, mul[3], kFixHi);
+    if (R == 1) return mad_hi(s.m2p, mul[4], kFixHi);
+    if (R == 2) return s.mp >> 16;
+    return mad_hi(s.m2p, mul[5], 0u);
+}
+
+// Per-thread asynchronous copies global -> shared; the issuing thread's
+// wait_group plus a warp barrier orders them before the warp reads them back.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -112,34 +166,27 @@ __device__ __forceinline__ uint2 lds64(uint32_t a)
     asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a) : "memory");
     return r;
 }
+__device__ __forceinline__ uint32_t lds8(uint32_t a)
+{
+    uint32_t r;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(r) : "r"(a) : "memory");
+    return r;
+}
 
-// Per-warp ring of kDepth chunks: [slot][row a][lane] 16 code bytes, and
-// [slot][row a][lane] the 8 UE8M0 bytes of the chunk (lane-major so the 128-bit
-// reads of a warp are conflict-free).
+// Per-warp ring of kDepth chunks.  Slot layout: codes [row a][lane] 16 bytes
+// (lane-major, so a warp's 128-bit reads are conflict-free), then scales
+// [row a][g] the chunk's 8 UE8M0 bytes of the quad's row (copied by lane c = 0;
+// thread c reads bytes 2c and 2c+1).
 constexpr int kDepth = 3;
 constexpr uint32_t kRingCodeBytes = 4 * 32 * 16;   // per slot
-constexpr uint32_t kRingScaleBytes = 4 * 32 * 8;
+constexpr uint32_t kRingScaleBytes = 4 * 8 * 8;
 constexpr uint32_t kRingSlot = kRingCodeBytes + kRingScaleBytes;
 constexpr uint32_t kRingWarp = kDepth * kRingSlot;
 
-struct Rows {
-    uint4 q[4];       // 16 code bytes of the thread's 4 rows (A rows g, g+8, 16+g, 24+g)
-    uint32_t sc[4];   // their two UE8M0 bytes for this chunk
-};
-
-__device__ __forceinline__ void load_rows(Rows& R, const uint8_t* const (&cp)[4], const uint8_t* const (&sp)[4],
-                                          int ch, int c)
-{
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        R.q[a] = ldg_stream_u4(cp[a] + ch * 64 + c * 16);
-        R.sc[a] = ldg_u16(sp[a] + ch * 8 + c * 2);
-    }
-}
-
 template <bool kGateUp, int NT>
-__device__ __forceinline__ void run_item(const DecArgs& p, const uint2* lut, float (*red)[2][kMaxNT][32][4],
-                                         uint32_t ring_base, int e, int q0, int nrows, int rb, uint32_t& lut_min)
+__device__ __forceinline__ void run_item(const DecArgs& p, const uint32_t (&mul)[8], uint32_t lut_base,
+                                         float (*red)[2][kMaxNT][32][4], uint32_t ring_base, int e, int q0,
+                                         int nrows, int rb, uint32_t& lut_and)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -161,23 +208,22 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const uint2* lut, flo
         row[2] = base + 16 + g;
         row[3] = base + 24 + g;
     }
+    // global sources of this warp's first chunk; each later chunk is kWarps chunks on
     const uint8_t* cp[4];
     const uint8_t* sp[4];
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-        cp[a] = p.codes + row[a] * rowb;
-        sp[a] = p.scales + row[a] * srowb;
+        cp[a] = p.codes + row[a] * rowb + warp * 64 + c * 16;
+        sp[a] = p.scales + row[a] * srowb + warp * 8;
     }
-    // B rows: pair j = 8*nt + g of the tile
+    // B rows: pair j = 8*nt + g of the tile.  Columns past the tile's pairs read
+    // pair 0's row (always valid); their results are never stored.
     const uint16_t* brow[NT];
-    bool bval[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        const int j = nt * 8 + g;
-        bval[nt] = j < nrows;
-        int64_t br = 0;
-        if (bval[nt]) br = kGateUp ? (int64_t)(__ldg(p.sorted + q0 + j) / p.k) : (int64_t)(q0 + j);
-        brow[nt] = p.act + br * p.K;
+        const int j = nt * 8 + g < nrows ? nt * 8 + g : 0;
+        const int64_t br = kGateUp ? (int64_t)(__ldg(p.sorted + q0 + j) / p.k) : (int64_t)(q0 + j);
+        brow[nt] = p.act + br * p.K + warp * kChunk + c * 64;
     }
 
     float acc[2][NT][4];
@@ -188,77 +234,84 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const uint2* lut, flo
 
     // ring of this warp's chunks ch = warp + kWarps * idx
     const uint32_t ring = ring_base + (uint32_t)warp * kRingWarp;
-    auto issue = [&](int idx) {
-        const int chq = warp + kWarps * idx;
-        if (chq < nch) {
-            const uint32_t slot = ring + (uint32_t)(idx % kDepth) * kRingSlot;
+    const int my_chunks = nch > warp ? (nch - warp + kWarps - 1) / kWarps : 0;
+    uint32_t wr_slot = ring;
+    int issued = 0;
+    auto issue = [&]() {
+        if (issued < my_chunks) {
+            const int64_t off = (int64_t)issued * (kWarps * 64);
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                cp_async16(slot + (uint32_t)(a * 32 + lane) * 16, cp[a] + chq * 64 + c * 16);
-                cp_async8(slot + kRingCodeBytes + (uint32_t)(a * 32 + lane) * 8, sp[a] + chq * 8);
+            for (int a = 0; a < 4; ++a) cp_async16(wr_slot + (uint32_t)(a * 32 + lane) * 16, cp[a] + off);
+            if (c == 0) {
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+                    cp_async8(wr_slot + kRingCodeBytes + (uint32_t)(a * 8 + g) * 8, sp[a] + (int64_t)issued * (kWarps * 8));
             }
         }
         cp_async_commit();
+        ++issued;
+        wr_slot = wr_slot + kRingSlot == ring + kRingWarp ? ring : wr_slot + kRingSlot;
     };
 #pragma unroll
-    for (int d = 0; d < kDepth - 1; ++d) issue(d);
-    for (int idx = 0; warp + kWarps * idx < nch; ++idx) {
-        const int ch = warp + kWarps * idx;
-        issue(idx + kDepth - 1);
+    for (int d = 0; d < kDepth - 1; ++d) issue();
+    uint32_t rd_slot = ring;
+    for (int idx = 0; idx < my_chunks; ++idx) {
+        issue();
         cp_async_wait<kDepth - 1>();
-        const uint32_t slot = ring + (uint32_t)(idx % kDepth) * kRingSlot;
-        Rows cur;
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            cur.q[a] = lds128(slot + (uint32_t)(a * 32 + lane) * 16);
-            const uint2 s8 = lds64(slot + kRingCodeBytes + (uint32_t)(a * 32 + lane) * 8);
-            const uint32_t wsc = (c & 2) ? s8.y : s8.x;
-            cur.sc[a] = (c & 1) ? (wsc >> 16) : (wsc & 0xFFFFu);
-        }
+        __syncwarp();
+        uint4 q[4];
         uint2 L[4][2];
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            L[a][0] = lut[cur.sc[a] & 0xFF];
-            L[a][1] = lut[cur.sc[a] >> 8];
-            lut_min = min(lut_min, min(L[a][0].x, L[a][1].x));
+            q[a] = lds128(rd_slot + (uint32_t)(a * 32 + lane) * 16);
+            const uint32_t sa = rd_slot + kRingCodeBytes + (uint32_t)(a * 8 + g) * 8 + 2 * c;
+            L[a][0] = lds64(lut_base + lds8(sa) * 8u);
+            L[a][1] = lds64(lut_base + lds8(sa + 1) * 8u);
+            lut_and &= L[a][0].x & L[a][1].x;
         }
-        const int boff = ch * kChunk + c * 64;
+        const uint16_t* bsrc[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) bsrc[nt] = brow[nt] + (int64_t)idx * (kWarps * kChunk);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             uint4 B0[NT], B1[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                if (bval[nt]) {
-                    B0[nt] = ldg_u4(brow[nt] + boff + i * 16);
-                    B1[nt] = ldg_u4(brow[nt] + boff + i * 16 + 8);
-                } else {
-                    B0[nt] = make_uint4(0, 0, 0, 0);
-                    B1[nt] = make_uint4(0, 0, 0, 0);
-                }
+                B0[nt] = ldg_u4(bsrc[nt] + i * 16);
+                B1[nt] = ldg_u4(bsrc[nt] + i * 16 + 8);
             }
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
-                const uint32_t wa = word_of(cur.q[2 * mt], i), wb = word_of(cur.q[2 * mt + 1], i);
+                const Masks ma = word_masks(word_of(q[2 * mt], i)), mb = word_masks(word_of(q[2 * mt + 1], i));
                 const uint2 la = L[2 * mt][i >> 1], lb = L[2 * mt + 1][i >> 1];
-                const ScaleLut LA{la.x, la.y}, LB{lb.x, lb.y};
-                uint32_t sa[4], sb[4];
-                selectors(wa, sa[0], sa[1], sa[2], sa[3]);
-                selectors(wb, sb[0], sb[1], sb[2], sb[3]);
+                uint32_t afrag[4][4];
+                afrag[0][0] = prmt(la.x, la.y, sel_lo<0>(ma, mul));
+                afrag[0][1] = prmt(lb.x, lb.y, sel_lo<0>(mb, mul));
+                afrag[0][2] = prmt(la.x, la.y, sel_hi<0>(ma, mul));
+                afrag[0][3] = prmt(lb.x, lb.y, sel_hi<0>(mb, mul));
+                afrag[1][0] = prmt(la.x, la.y, sel_lo<1>(ma, mul));
+                afrag[1][1] = prmt(lb.x, lb.y, sel_lo<1>(mb, mul));
+                afrag[1][2] = prmt(la.x, la.y, sel_hi<1>(ma, mul));
+                afrag[1][3] = prmt(lb.x, lb.y, sel_hi<1>(mb, mul));
+                afrag[2][0] = prmt(la.x, la.y, sel_lo<2>(ma, mul));
+                afrag[2][1] = prmt(lb.x, lb.y, sel_lo<2>(mb, mul));
+                afrag[2][2] = prmt(la.x, la.y, sel_hi<2>(ma, mul));
+                afrag[2][3] = prmt(lb.x, lb.y, sel_hi<2>(mb, mul));
+                afrag[3][0] = prmt(la.x, la.y, sel_lo<3>(ma, mul));
+                afrag[3][1] = prmt(lb.x, lb.y, sel_lo<3>(mb, mul));
+                afrag[3][2] = prmt(la.x, la.y, sel_hi<3>(ma, mul));
+                afrag[3][3] = prmt(lb.x, lb.y, sel_hi<3>(mb, mul));
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    uint32_t afrag[4];
-                    afrag[0] = expand_pair(LA, sa[r]);
-                    afrag[1] = expand_pair(LB, sb[r]);
-                    afrag[2] = expand_pair(LA, __umulhi(sa[r], 0x10000u));
-                    afrag[3] = expand_pair(LB, __umulhi(sb[r], 0x10000u));
+                for (int r = 0; r < 4; ++r)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const uint4& Bv = (r < 2) ? B0[nt] : B1[nt];
-                        mma_bf16_16816(acc[mt][nt], afrag, (r & 1) ? Bv.z : Bv.x, (r & 1) ? Bv.w : Bv.y);
+                        mma_bf16_16816(acc[mt][nt], afrag[r], (r & 1) ? Bv.z : Bv.x, (r & 1) ? Bv.w : Bv.y);
                     }
-                }
             }
         }
+        __syncwarp();
+        rd_slot = rd_slot + kRingSlot == ring + kRingWarp ? ring : rd_slot + kRingSlot;
     }
     cp_async_wait<0>();
 
@@ -316,21 +369,27 @@ __global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS) decode_kernel(D
     __shared__ int last_flag;
     extern __shared__ __align__(16) uint8_t ring_smem[];   // kWarps * kRingWarp bytes
     const uint32_t ring_base = (uint32_t)__cvta_generic_to_shared(ring_smem);
+    const uint32_t lut_base = (uint32_t)__cvta_generic_to_shared(lut);
     for (int s = threadIdx.x; s < 256; s += kThreads) {
         ScaleLut l = make_lut((uint32_t)s);
         lut[s] = make_uint2(l.lut, l.lo);
     }
+    uint32_t mul[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mul[i] = p.mul[i];
     __syncthreads();
 
     const int n_tiles = *p.tile_count;
     const int n_items = n_tiles * p.row_blocks;
-    uint32_t lut_min = 0xFFFFFFFFu;
+    // AND of every lut word used: a valid scale's lut word has bit 31 set, an
+    // invalid one is 0, so the AND is 0 exactly when a bad scale byte was read.
+    uint32_t lut_and = 0xFFFFFFFFu;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const int4 tile = p.tiles[it / p.row_blocks];
         const int rb = it % p.row_blocks;
         const int nt = (tile.z + 7) >> 3;
-        if (nt == 1) run_item<kGateUp, 1>(p, lut, red, ring_base, tile.x, tile.y, tile.z, rb, lut_min);
-        else run_item<kGateUp, 2>(p, lut, red, ring_base, tile.x, tile.y, tile.z, rb, lut_min);
+        if (nt == 1) run_item<kGateUp, 1>(p, mul, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
+        else run_item<kGateUp, 2>(p, mul, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
         if (!kGateUp) {
             // The last of the n_tiles items that wrote rows [32 rb, 32 rb + 32) of
             // the pair slots sums them into y (fixed j order per token).
@@ -354,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS) decode_kernel(D
             __syncthreads();
         }
     }
-    if (lut_min == 0) flag_status(p.status, MOE_W2_DEV_BAD_SCALE);
+    if (lut_and == 0) flag_status(p.status, MOE_W2_DEV_BAD_SCALE);
 }
 
 }  // namespace
@@ -402,6 +461,8 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     gp.counters = ws.counters;
     gp.y = y;
     gp.status = status;
+    const uint32_t mul[8] = {16u, 4u, 1u << 30, 1u << 20, 1u << 18, 1u << 14, 0u, 0u};
+    for (int i = 0; i < 8; ++i) gp.mul[i] = mul[i];
     cudaError_t e = ev.record(1, s);
     if (e != cudaSuccess) return e;
     decode_kernel<true><<<(int)std::min<int64_t>(tiles * gp.row_blocks, grid_max), kThreads, kDyn, s>>>(gp);

@@ -15,6 +15,8 @@ section "Our hooks"):
   decode_t32      H=6144 I=2048 E=256 top-8 T=32    exponents in [-10,-6]       Zipf(1.1) routing
   prefill_t8192   H=4096 I=2048 E=256 top-8 T=8192  exponents in [-10,-6]       router logits
   requant_256     256 experts of NVFP4 gate/up [2048x6144] and down [6144x2048]
+  decode_t1_e32, prefill_t1024_e32: the decode_t1 / prefill_t8192 layers over 32 experts
+                  (same per-launch kernel work; small enough for multi-pass profiling)
 
 Recipe (all numpy PCG64 via ``default_rng(seed)``):
   * activations: standard normal fp32, rounded to bf16 (round to nearest even);
@@ -76,6 +78,11 @@ CONFIGS = {
     "decode_t1": LayerConfig("decode_t1", 6144, 2048, 256, 8, 1, -10, -6, "zipf", 1),
     "decode_t32": LayerConfig("decode_t32", 6144, 2048, 256, 8, 32, -10, -6, "zipf", 2),
     "prefill_t8192": LayerConfig("prefill_t8192", 4096, 2048, 256, 8, 8192, -10, -6, "logits", 3),
+    # Small cases with the same per-launch kernel work, for multi-pass profiler captures:
+    # a T=1 step streams 8 experts' planes whatever E is, and T=1024 over 32 experts gives
+    # the same 256 pairs per expert as T=8192 over 256 experts (an eighth of the tiles).
+    "decode_t1_e32": LayerConfig("decode_t1_e32", 6144, 2048, 32, 8, 1, -10, -6, "zipf", 5),
+    "prefill_t1024_e32": LayerConfig("prefill_t1024_e32", 4096, 2048, 32, 8, 1024, -10, -6, "logits", 6),
 }
 REQUANT = RequantConfig("requant_256", 256, 2048, 6144, 4)
 

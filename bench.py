@@ -8,9 +8,11 @@ routing), the single-token decode step.  One step = one moe_w2_forward of one
 batch: permutation, gate_up with SiLU*up, down with the weighted combine.
 
 Timing: inputs are resident in HBM; every step replays a captured CUDA graph of
-the forward whose phase events (moe_w2_forward_traced) give the step time and
-the time of each kernel; L2 is flushed (a 512 MiB write) before every step,
-outside the timed events.  Routings rotate over a pool, so consecutive steps
+the forward, timed by CUDA events recorded on the launching stream around the
+replay (step time, `value`).  A second timed pass over the same steps replays
+graphs of moe_w2_forward_traced, whose phase events give each kernel's time (the
+roofline line); its step time is reported as ms_per_step_traced.  L2 is flushed
+(a 512 MiB write) before every step, outside the timed events.  Routings rotate over a pool, so consecutive steps
 touch different experts.  "e2e" times the same call with the step's inputs
 copied from pinned host memory and y copied back inside the timed events.
 
@@ -42,6 +44,7 @@ from bit_moe_expert_w2_gb300 import inputs  # noqa: E402
 
 METRIC = "w2 MoE layer tokens/s; plane HBM GB/s (decode), TFLOP/s (prefill) vs peak"
 DEFAULT_CONFIG = "decode_t1"
+TRACE_EAGER = os.environ.get("MOE_W2_BENCH_TRACE", "eager") == "eager"
 POOL = 16
 
 
@@ -254,24 +257,40 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
         if st != 0:
             raise moe_w2.MoeW2Error(st, "moe_w2_forward_traced")
 
-    # graphs: one per pool entry, each with its own phase events
-    graphs, events = [], []
+    def call_plain(i, s):
+        x, ids, w = dev_batches[i]
+        st = L.moe_w2_forward(moe_w2._ptr(x), moe_w2._ptr(ids), moe_w2._ptr(w), ctypes.byref(P), T, k,
+                              moe_w2._ptr(ys[i]), moe_w2._ptr(work), work.numel(), moe_w2._ptr(status),
+                              ctypes.c_void_p(s.cuda_stream))
+        if st != 0:
+            raise moe_w2.MoeW2Error(st, "moe_w2_forward")
+
+    # two graphs per pool entry: the plain forward (timed for the step time and
+    # `value`) and the traced forward with phase events (timed for the per-kernel
+    # breakdown and the roofline), so the event nodes never count in the step time
+    graphs, graphs_traced, events = [], [], []
     with torch.cuda.stream(stream):
         for i in range(pool):            # warm the library's one-time queries outside capture
             evs = make_events()
             call(i, evs, stream)
+            call_plain(i, stream)
         torch.cuda.synchronize(dev)
         for i in range(pool):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                call_plain(i, stream)
+            graphs.append(g)
             evs = make_events()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 call(i, evs, stream)
-            graphs.append(g)
+            graphs_traced.append(g)
             events.append(evs)
     torch.cuda.synchronize(dev)
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(pool)]
 
     def run_steps(nsteps, record):
-        tot = np.zeros(n_ev - 1)
+        """Plain graphs; CUDA events on the stream around each replay (L2 flush outside)."""
         steps_total = 0.0
         per_step = []
         done = 0
@@ -280,27 +299,53 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
             with torch.cuda.stream(stream):
                 for j in range(m):
                     flush.zero_()
+                    step_ev[j][0].record(stream)
                     graphs[(done + j) % pool].replay()
+                    step_ev[j][1].record(stream)
+            stream.synchronize()
+            for j in range(m):
+                step = step_ev[j][0].elapsed_time(step_ev[j][1])
+                if record:
+                    steps_total += step
+                    per_step.append(((done + j) % pool, step))
+            done += m
+        return steps_total, per_step
+
+    def run_traced(nsteps, eager=TRACE_EAGER):
+        """Traced steps: per-phase times from the events between the kernels.  Eager
+        launches (queued behind the L2 flush, so the GPU never waits on the host)
+        by default; graph replays with event nodes otherwise."""
+        tot = np.zeros(n_ev - 1)
+        steps_total = 0.0
+        done = 0
+        while done < nsteps:
+            m = min(pool, nsteps - done)
+            with torch.cuda.stream(stream):
+                for j in range(m):
+                    flush.zero_()
+                    if eager:
+                        call((done + j) % pool, events[(done + j) % pool], stream)
+                    else:
+                        graphs_traced[(done + j) % pool].replay()
             stream.synchronize()
             for j in range(m):
                 evs = events[(done + j) % pool]
-                ph = [evs[q].elapsed_time(evs[q + 1]) for q in range(n_ev - 1)]
-                step = evs[0].elapsed_time(evs[n_ev - 1])
-                if record:
-                    tot += ph
-                    steps_total += step
-                    per_step.append(((done + j) % pool, step, ph))
+                tot += [evs[q].elapsed_time(evs[q + 1]) for q in range(n_ev - 1)]
+                steps_total += evs[0].elapsed_time(evs[n_ev - 1])
             done += m
-        return steps_total, tot, per_step
+        return steps_total, tot
 
     run_steps(max(args.warmup, 3), False)
+    run_traced(max(args.warmup, 3))
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
-        steps_ms, phase_ms, per_step = run_steps(args.steps, True)
+        steps_ms, per_step = run_steps(args.steps, True)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
+        traced_ms, phase_ms = run_traced(args.steps)
+        torch.cuda.synchronize(dev)
     barrier(world)
     steps_ms_max = max_over_ranks(steps_ms, world)
     K = args.steps
@@ -310,9 +355,9 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
         raise RuntimeError(f"device status {st_val} during the benchmark")
 
     pk = peaks()
-    plane_bytes = sum(distinct[i] * (w13_b + w2_b) for i, _, _ in per_step)
-    gu_bytes = sum(distinct[i] * w13_b for i, _, _ in per_step)
-    res = {"ms_per_step": steps_ms / K}
+    plane_bytes = sum(distinct[i] * (w13_b + w2_b) for i, _ in per_step)
+    gu_bytes = sum(distinct[i] * w13_b for i, _ in per_step)
+    res = {"ms_per_step": steps_ms / K, "ms_per_step_traced": traced_ms / K}
     if decode:
         achieved = gu_bytes / (phase_ms[1] / 1e3) / 1e9
         res["roofline"] = {"kernel": "decode_gate_up_kernel", "bound": "hbm", "achieved": round(achieved, 1),
@@ -331,7 +376,7 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
         res["layer_tflops"] = round(6.0 * T * k * H * I * K / (steps_ms / 1e3) / 1e12, 1)
     res["phase_ms_per_step"] = {"permute": round(phase_ms[0] / K, 5), "gate_up": round(phase_ms[1] / K, 5),
                                 "down_combine": round(phase_ms[2] / K, 5)}
-    res["distinct_experts_per_step"] = round(float(np.mean([distinct[i] for i, _, _ in per_step])), 2)
+    res["distinct_experts_per_step"] = round(float(np.mean([distinct[i] for i, _ in per_step])), 2)
     res["clocks"] = clk.summary()
     res["wall_s"] = round(wall, 3)
     # decode: permute (+ x transpose), gate_up, down (+ combine);

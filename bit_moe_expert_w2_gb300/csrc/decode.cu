@@ -49,6 +49,10 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxNT = 2;     // n-tiles of 8 pairs per item (tiles of <= 16 pairs)
 
+struct SelConst {
+    uint32_t m33, c04, mcc, c10, fix, k16, k4, s2, s16, s18;
+};
+
 struct DecArgs {
     const uint8_t* codes;      // [E][rows_per_expert][K/4]
     const uint8_t* scales;     // [E][rows_per_expert][K/32]
@@ -71,7 +75,7 @@ struct DecArgs {
     int32_t* counters;         // down: per 32-row block of y
     uint16_t* y;
     uint32_t* status;
-    uint32_t mul[8];           // 16, 4, 2^30, 2^20, 2^18, 2^14, -, - (selector multipliers)
+    SelConst sc;               // selector constants (see selectors())
 };
 
 __device__ __forceinline__ uint32_t word_of(const uint4& q, int i)
@@ -85,10 +89,17 @@ __device__ __forceinline__ uint32_t mad_lo(uint32_t a, uint32_t b, uint32_t c)
     asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
-__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c)
+__device__ __forceinline__ uint32_t shr(uint32_t a, uint32_t n)
 {
     uint32_t d;
-    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    asm("shr.b32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(n));
+    return d;
+}
+// (a & b) | c in one logic op
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
 // Byte-permute with the selector used as is: every selector nibble built below
@@ -100,45 +111,46 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
 }
+// A value the compiler cannot see through: keeps a constant in a register, so
+// every instruction below takes it as a register operand (instructions with two
+// immediates would otherwise be split in two, or need a move per use).
+__device__ __forceinline__ uint32_t opaque(uint32_t v)
+{
+    asm volatile("" : "+r"(v));
+    return v;
+}
 
 // Selector words of a 16-code word w (code i in bits 2i..2i+1) for the bf16
 // pairs (c_r, c_{r+4}) [lo] and (c_{r+8}, c_{r+12}) [hi].  In each selector byte
 // the high nibble is the code (0..3: a byte of the lut word) and the low nibble
 // is 4 | (any two bits) (a byte of the lo word); the byte-permute reads only the
-// low 16 bits of a selector, so only those are kept exact.  From
+// low 16 bits of a selector, so only those need to be exact.  From
 //   mp  = (w & 0x33333333) | 0x04040404   codes 4b, 4b+2 of byte b, plus 4 per byte
 //   m2p = (w & 0xCCCCCCCC) | 0x10101010   codes 4b+1, 4b+3, plus 0x10 per byte
 // (one logic op each) the eight selectors are
 //   lo: r=0 mp*16 - 0x3C3C3C3C   r=1 m2p*4 - 0x3C3C3C3C   r=2 mp   r=3 m2p >> 2
-//   hi: r=0 (mp >> 12) - 0x3C3C  r=1 (m2p >> 14) - 0x3C3C  r=2 mp >> 16   r=3 m2p >> 18
-// (the subtractions remove the shifted 0x04/0x10 fill, leaving 0x04 per byte).
-// mp >> 16 is a shift on the ALU pipe; the other six are multiply-adds (right
-// shifts as the high word of a product) on the FMA pipe, which keeps the two
-// pipes about equally loaded next to the eight byte-permutes.
+//   hi: the lo selector of the same r shifted right by 16 (r=3: m2p >> 18)
+// (the subtractions remove the shifted fill and leave 0x04 per byte).  Per word:
+// 2 logic ops, 5 shifts and 8 byte-permutes on the ALU pipe, 2 multiply-adds on
+// the FMA pipe.  Right shifts stay shifts: as the high word of a product they
+// would run on the FMA pipe at a quarter of its rate.
 struct Masks {
     uint32_t mp, m2p;
 };
-__device__ __forceinline__ Masks word_masks(uint32_t w)
+__device__ __forceinline__ Masks word_masks(uint32_t w, const SelConst& k)
 {
-    return Masks{(w & 0x33333333u) | 0x04040404u, (w & 0xCCCCCCCCu) | 0x10101010u};
+    return Masks{and_or(w, k.m33, k.c04), and_or(w, k.mcc, k.c10)};
 }
-constexpr uint32_t kFixLo = 0xC3C3C3C4u;   // -0x3C3C3C3C
-constexpr uint32_t kFixHi = 0xFFFFC3C4u;   // -0x3C3C
-template <int R>
-__device__ __forceinline__ uint32_t sel_lo(const Masks& s, const uint32_t (&mul)[8])
+__device__ __forceinline__ void selectors(const Masks& s, const SelConst& k, uint32_t (&lo)[4], uint32_t (&hi)[4])
 {
-    if (R == 0) return mad_lo(s.mp, mul[0], kFixLo);
-    if (R == 1) return mad_lo(s.m2p, mul[1], kFixLo);
-    if (R == 2) return s.mp;
-    return mad_hi(s.m2p, mul[2], 0u);
-}
-template <int R>
-__device__ __forceinline__ uint32_t sel_hi(const Masks& s, const uint32_t (&mul)[8])
-{
-    if (R == 0) return mad_hi(s.mp, mul[3], kFixHi);
-    if (R == 1) return mad_hi(s.m2p, mul[4], kFixHi);
-    if (R == 2) return s.mp >> 16;
-    return mad_hi(s.m2p, mul[5], 0u);
+    lo[0] = mad_lo(s.mp, k.k16, k.fix);
+    lo[1] = mad_lo(s.m2p, k.k4, k.fix);
+    lo[2] = s.mp;
+    lo[3] = shr(s.m2p, k.s2);
+    hi[0] = shr(lo[0], k.s16);
+    hi[1] = shr(lo[1], k.s16);
+    hi[2] = shr(s.mp, k.s16);
+    hi[3] = shr(s.m2p, k.s18);
 }
 
 // Per-thread asynchronous copies global -> shared; the issuing thread's
@@ -184,7 +196,7 @@ constexpr uint32_t kRingSlot = kRingCodeBytes + kRingScaleBytes;
 constexpr uint32_t kRingWarp = kDepth * kRingSlot;
 
 template <bool kGateUp, int NT>
-__device__ __forceinline__ void run_item(const DecArgs& p, const uint32_t (&mul)[8], uint32_t lut_base,
+__device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, uint32_t lut_base,
                                          float (*red)[2][kMaxNT][32][4], uint32_t ring_base, int e, int q0,
                                          int nrows, int rb, uint32_t& lut_and)
 {
@@ -282,25 +294,19 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const uint32_t (&mul)
             }
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
-                const Masks ma = word_masks(word_of(q[2 * mt], i)), mb = word_masks(word_of(q[2 * mt + 1], i));
+                const Masks ma = word_masks(word_of(q[2 * mt], i), k), mb = word_masks(word_of(q[2 * mt + 1], i), k);
                 const uint2 la = L[2 * mt][i >> 1], lb = L[2 * mt + 1][i >> 1];
+                uint32_t alo[4], ahi[4], blo[4], bhi[4];
+                selectors(ma, k, alo, ahi);
+                selectors(mb, k, blo, bhi);
                 uint32_t afrag[4][4];
-                afrag[0][0] = prmt(la.x, la.y, sel_lo<0>(ma, mul));
-                afrag[0][1] = prmt(lb.x, lb.y, sel_lo<0>(mb, mul));
-                afrag[0][2] = prmt(la.x, la.y, sel_hi<0>(ma, mul));
-                afrag[0][3] = prmt(lb.x, lb.y, sel_hi<0>(mb, mul));
-                afrag[1][0] = prmt(la.x, la.y, sel_lo<1>(ma, mul));
-                afrag[1][1] = prmt(lb.x, lb.y, sel_lo<1>(mb, mul));
-                afrag[1][2] = prmt(la.x, la.y, sel_hi<1>(ma, mul));
-                afrag[1][3] = prmt(lb.x, lb.y, sel_hi<1>(mb, mul));
-                afrag[2][0] = prmt(la.x, la.y, sel_lo<2>(ma, mul));
-                afrag[2][1] = prmt(lb.x, lb.y, sel_lo<2>(mb, mul));
-                afrag[2][2] = prmt(la.x, la.y, sel_hi<2>(ma, mul));
-                afrag[2][3] = prmt(lb.x, lb.y, sel_hi<2>(mb, mul));
-                afrag[3][0] = prmt(la.x, la.y, sel_lo<3>(ma, mul));
-                afrag[3][1] = prmt(lb.x, lb.y, sel_lo<3>(mb, mul));
-                afrag[3][2] = prmt(la.x, la.y, sel_hi<3>(ma, mul));
-                afrag[3][3] = prmt(lb.x, lb.y, sel_hi<3>(mb, mul));
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    afrag[r][0] = prmt(la.x, la.y, alo[r]);
+                    afrag[r][1] = prmt(lb.x, lb.y, blo[r]);
+                    afrag[r][2] = prmt(la.x, la.y, ahi[r]);
+                    afrag[r][3] = prmt(lb.x, lb.y, bhi[r]);
+                }
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -374,9 +380,17 @@ __global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS) decode_kernel(D
         ScaleLut l = make_lut((uint32_t)s);
         lut[s] = make_uint2(l.lut, l.lo);
     }
-    uint32_t mul[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mul[i] = p.mul[i];
+    SelConst k;
+    k.m33 = opaque(p.sc.m33);
+    k.c04 = opaque(p.sc.c04);
+    k.mcc = opaque(p.sc.mcc);
+    k.c10 = opaque(p.sc.c10);
+    k.fix = opaque(p.sc.fix);
+    k.k16 = opaque(p.sc.k16);
+    k.k4 = opaque(p.sc.k4);
+    k.s2 = opaque(p.sc.s2);
+    k.s16 = opaque(p.sc.s16);
+    k.s18 = opaque(p.sc.s18);
     __syncthreads();
 
     const int n_tiles = *p.tile_count;
@@ -388,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS) decode_kernel(D
         const int4 tile = p.tiles[it / p.row_blocks];
         const int rb = it % p.row_blocks;
         const int nt = (tile.z + 7) >> 3;
-        if (nt == 1) run_item<kGateUp, 1>(p, mul, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
-        else run_item<kGateUp, 2>(p, mul, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
+        if (nt == 1) run_item<kGateUp, 1>(p, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
+        else run_item<kGateUp, 2>(p, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
         if (!kGateUp) {
             // The last of the n_tiles items that wrote rows [32 rb, 32 rb + 32) of
             // the pair slots sums them into y (fixed j order per token).
@@ -461,8 +475,7 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     gp.counters = ws.counters;
     gp.y = y;
     gp.status = status;
-    const uint32_t mul[8] = {16u, 4u, 1u << 30, 1u << 20, 1u << 18, 1u << 14, 0u, 0u};
-    for (int i = 0; i < 8; ++i) gp.mul[i] = mul[i];
+    gp.sc = SelConst{0x33333333u, 0x04040404u, 0xCCCCCCCCu, 0x10101010u, 0xC3C3C3C4u, 16u, 4u, 2u, 16u, 18u};
     cudaError_t e = ev.record(1, s);
     if (e != cudaSuccess) return e;
     decode_kernel<true><<<(int)std::min<int64_t>(tiles * gp.row_blocks, grid_max), kThreads, kDyn, s>>>(gp);

@@ -30,33 +30,44 @@ __device__ __forceinline__ uint32_t lanemask_lt()
     return r;
 }
 
-// Exclusive scan of one int per thread over the CTA; *total = sum of all.
-__device__ int cta_exclusive_scan(int v, int* warp_tmp, int* total)
+// Exclusive scan over the CTA of three ints per thread at once (one pass of
+// shuffles and two barriers for all three); tot[] receives the three totals.
+__device__ int3 cta_exclusive_scan3(int3 v, int3* warp_tmp, int3* tot)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
+    int3 x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        const int yx = __shfl_up_sync(0xffffffffu, x.x, o);
+        const int yy = __shfl_up_sync(0xffffffffu, x.y, o);
+        const int yz = __shfl_up_sync(0xffffffffu, x.z, o);
+        if (lane >= o) {
+            x.x += yx;
+            x.y += yy;
+            x.z += yz;
+        }
     }
     if (lane == 31) warp_tmp[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int w = warp_tmp[lane];
+        int3 w = warp_tmp[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
+            const int yx = __shfl_up_sync(0xffffffffu, w.x, o);
+            const int yy = __shfl_up_sync(0xffffffffu, w.y, o);
+            const int yz = __shfl_up_sync(0xffffffffu, w.z, o);
+            if (lane >= o) {
+                w.x += yx;
+                w.y += yy;
+                w.z += yz;
+            }
         }
         warp_tmp[lane] = w;
     }
     __syncthreads();
-    int base = warp ? warp_tmp[warp - 1] : 0;
-    int t = warp_tmp[kWarps - 1];
-    __syncthreads();
-    if (total) *total = t;
-    return base + x - v;
+    const int3 base = warp ? warp_tmp[warp - 1] : make_int3(0, 0, 0);
+    *tot = warp_tmp[kWarps - 1];
+    return make_int3(base.x + x.x - v.x, base.y + x.y - v.y, base.z + x.z - v.z);
 }
 
 // x [rows][H] -> x_t16 [rows][H]: 4x4 transpose inside each group of 16.
@@ -95,22 +106,24 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
     }
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
     extern __shared__ int32_t smem[];
-    __shared__ int warp_tmp[kWarps];
-    __shared__ int sh_total;
+    __shared__ int3 warp_tmp[kWarps];
+    int3 sh_tot;   // totals of the fused scan (same value in every thread)
     const int nb = E + 1;                 // bin E collects out-of-range ids
-    int32_t* cnt = smem;                  // [kWarps][nb] counts, then write cursors
-    int32_t* soff = smem + kWarps * nb;   // [nb] exclusive offsets
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // slices of 32-pair multiples, one per warp; only as many as P needs
+    const int chunk = (((P + kWarps - 1) / kWarps) + 31) & ~31;
+    const int n_slices = chunk ? (P + chunk - 1) / chunk : 0;
+    int32_t* cnt = smem;                    // [n_slices][nb] counts, then write cursors
+    int32_t* soff = smem + kWarps * nb;     // [nb] per-expert totals, then exclusive offsets
 
-    for (int i = tid; i < kWarps * nb; i += kThreads) cnt[i] = 0;
+    for (int i = tid; i < n_slices * nb; i += kThreads) cnt[i] = 0;
     __syncthreads();
 
-    const int chunk = (((P + kWarps - 1) / kWarps) + 31) & ~31;
     const int p0 = warp * chunk;
     const int p1 = min(P, p0 + chunk);
     uint32_t bad = 0;
 
-    // pass 1: counts per (warp, expert)
+    // pass 1: counts per (slice, expert)
     for (int pb = p0; pb < p1; pb += 32 * 8) {
         int e[8];
 #pragma unroll
@@ -128,59 +141,53 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
     }
     __syncthreads();
 
-    // per-expert totals; cnt becomes the exclusive prefix over warps
+    // per-expert totals; cnt becomes the exclusive prefix over slices
     for (int b = tid; b < nb; b += kThreads) {
         int run = 0;
-        for (int w = 0; w < kWarps; ++w) {
+        for (int w = 0; w < n_slices; ++w) {
             int c = cnt[w * nb + b];
             cnt[w * nb + b] = run;
             run += c;
         }
-        soff[b] = run;   // total for now
+        soff[b] = run;
     }
     __syncthreads();
 
-    // scans over bins (two bins per thread covers nb <= 2048)
+    // one fused scan over bins (two bins per thread covers nb <= 2048) of
+    // (pairs, active flags, tiles)
     const int b0 = 2 * tid, b1 = 2 * tid + 1;
     const int t0 = (b0 < nb) ? soff[b0] : 0, t1 = (b1 < nb) ? soff[b1] : 0;
-    int ex = cta_exclusive_scan(t0 + t1, warp_tmp, nullptr);
-    __syncthreads();
-    if (b0 < nb) { soff[b0] = ex; offsets[b0] = ex; }
-    if (b1 < nb) { soff[b1] = ex + t0; offsets[b1] = ex + t0; }
-
+    const int f0 = (b0 < E && t0 > 0), f1 = (b1 < E && t1 > 0);
+    const int n0 = (tiles != nullptr && b0 < E) ? (t0 + tile_rows - 1) / tile_rows : 0;
+    const int n1 = (tiles != nullptr && b1 < E) ? (t1 + tile_rows - 1) / tile_rows : 0;
+    const int3 ex = cta_exclusive_scan3(make_int3(t0 + t1, f0 + f1, n0 + n1), warp_tmp, &sh_tot);
+    if (b0 < nb) { soff[b0] = ex.x; offsets[b0] = ex.x; }
+    if (b1 < nb) { soff[b1] = ex.x + t0; offsets[b1] = ex.x + t0; }
     if (active != nullptr) {
-        const int f0 = (b0 < E && t0 > 0), f1 = (b1 < E && t1 > 0);
-        int ea = cta_exclusive_scan(f0 + f1, warp_tmp, &sh_total);
-        if (f0) active[ea] = b0;
-        if (f1) active[ea + f0] = b1;
-        if (tid == 0) *active_count = sh_total;
-    }
-
-    if (y != nullptr) {
-        // no valid pair at all: nothing will write y, so it is zeroed here
-        __syncthreads();
-        if (soff[E] == 0)
-            for (int64_t i = tid; i < y_elems; i += kThreads) y[i] = 0;
+        if (f0) active[ex.y] = b0;
+        if (f1) active[ex.y + f0] = b1;
+        if (tid == 0) *active_count = sh_tot.y;
     }
     if (tiles != nullptr) {
-        const int n0 = (b0 < E) ? (t0 + tile_rows - 1) / tile_rows : 0;
-        const int n1 = (b1 < E) ? (t1 + tile_rows - 1) / tile_rows : 0;
-        int et = cta_exclusive_scan(n0 + n1, warp_tmp, &sh_total);
-        __syncthreads();   // soff writes above are visible
         for (int i = 0; i < n0; ++i) {
             int r0 = (int)(((int64_t)i * t0) / n0), r1 = (int)(((int64_t)(i + 1) * t0) / n0);
-            tiles[et + i] = make_int4(b0, soff[b0] + r0, r1 - r0, 0);
+            tiles[ex.z + i] = make_int4(b0, ex.x + r0, r1 - r0, 0);
         }
         for (int i = 0; i < n1; ++i) {
             int r0 = (int)(((int64_t)i * t1) / n1), r1 = (int)(((int64_t)(i + 1) * t1) / n1);
-            tiles[et + n0 + i] = make_int4(b1, soff[b1] + r0, r1 - r0, 0);
+            tiles[ex.z + n0 + i] = make_int4(b1, ex.x + t0 + r0, r1 - r0, 0);
         }
-        if (tid == 0) *tile_count = sh_total;
+        if (tid == 0) *tile_count = sh_tot.z;
     }
     __syncthreads();
+    // no valid pair at all (offset of the invalid-id bin is 0): nothing will
+    // write y, so it is zeroed here
+    if (y != nullptr && soff[E] == 0)
+        for (int64_t i = tid; i < y_elems; i += kThreads) y[i] = 0;
 
-    // write cursors = expert offset + prefix over earlier warps
-    for (int i = tid; i < kWarps * nb; i += kThreads) cnt[i] += soff[i % nb];
+    // write cursors = expert offset + prefix over earlier slices
+    for (int w = 0; w < n_slices; ++w)
+        for (int b = tid; b < nb; b += kThreads) cnt[w * nb + b] += soff[b];
     __syncthreads();
 
     // pass 2: stable scatter

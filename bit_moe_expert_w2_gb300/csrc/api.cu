@@ -79,7 +79,7 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
     w.active_count = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * 2));
     w.tile_count = w.active_count + 1;
     w.tiles = reinterpret_cast<int4*>(take(sizeof(int4) * max_tiles(P, E, decode)));
-    w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (H / 32)));
+    w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (H / 32 + max_tiles(P, E, decode) + 1)));
     w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * (decode ? (int64_t)T : P) * H));
     w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
     w.stage = reinterpret_cast<float*>(take(sizeof(float) * P * H));
@@ -164,7 +164,8 @@ moe_w2_status moe_w2_forward_traced(const void* x_bf16, const int32_t* topk_ids,
     cudaError_t e = launch_permute(topk_ids, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active, ws.active_count,
                                    ws.tiles, ws.tile_count, decode ? kDecodeTileRows : kPrefillTileRows,
                                    decode ? x : nullptr, decode ? ws.xa : nullptr, H, ws.counters,
-                                   decode ? H / 32 : 0, decode ? y : nullptr, dev_status, s);
+                                   decode ? (int32_t)(H / 32 + max_tiles((int64_t)T * top_k, E, true) + 1) : 0,
+                                   decode ? y : nullptr, dev_status, s);
     if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
     if (decode)
         e = launch_decode(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);

@@ -104,7 +104,9 @@ struct Workspace {
     int4* tiles;           // GEMM tiles (expert, first slot, pairs, 0)
     int32_t* tile_count;   // [1]
     uint16_t* xa;          // prefill: activation rows in expert order [P][H]; decode: x per token [T][H]; T16 layout
-    int32_t* counters;     // decode: per 32-row block of y, CTAs done (last one runs the combine)
+    int32_t* counters;     // decode: per 32-row block of y, CTAs done (last one runs the combine),
+                           // then per tile, gate_up row blocks done (down items wait for their tile),
+                           // then the decode item queue
     uint16_t* h;           // SiLU(gate)*up rows in expert order, T16 layout [P][I]
     float* stage;          // per-pair outputs times router weight, slot t*k+j [P][H]
     size_t bytes;

@@ -35,7 +35,7 @@
 // j order and writes y (counter per row block, reset by the permutation kernel).
 #include <algorithm>
 
-#include "common.cuh"
+#include "tc.cuh"
 
 namespace moe_w2 {
 
@@ -77,6 +77,23 @@ struct DecArgs {
     uint32_t* status;
     SelConst sc;               // selector constants (see selectors())
 };
+
+// Coherent 128-bit load (plain ld.global) for data another CTA of the same
+// launch wrote: the reader's CTA observed the writer's release with a GPU-scope
+// acquire followed by a CTA barrier, so these loads see the data.  The
+// non-coherent read-only path (ld.global.nc) is not allowed for it.
+__device__ __forceinline__ uint4 ldg_coherent_u4(const void* p)
+{
+    uint4 r;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_acquire(const int32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ uint32_t word_of(const uint4& q, int i)
 {
@@ -289,8 +306,13 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, ui
             uint4 B0[NT], B1[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                B0[nt] = ldg_u4(bsrc[nt] + i * 16);
-                B1[nt] = ldg_u4(bsrc[nt] + i * 16 + 8);
+                if (kGateUp) {   // x in T16 order, written by an earlier launch
+                    B0[nt] = ldg_u4(bsrc[nt] + i * 16);
+                    B1[nt] = ldg_u4(bsrc[nt] + i * 16 + 8);
+                } else {         // h, written by the gate_up items of this launch
+                    B0[nt] = ldg_coherent_u4(bsrc[nt] + i * 16);
+                    B1[nt] = ldg_coherent_u4(bsrc[nt] + i * 16 + 8);
+                }
             }
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
@@ -367,12 +389,25 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, ui
     __syncthreads();
 }
 
-template <bool kGateUp>
-__global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS) decode_kernel(DecArgs p)
+// One persistent, co-resident grid runs the whole decode layer.  Items come
+// from one queue: indices [0, n_gu) are gate_up items (tile, 16 gate + 16 up
+// rows), [n_gu, n_gu + n_dn) down items (tile, 32 rows of y).  CTA c starts with
+// item c and then takes the next free index from a global counter (taken one
+// item ahead, so the atomic's latency hides behind the current item); a CTA
+// that runs out of gate_up work moves straight on to down work.  A down item of
+// tile t needs h of every row of t, so it waits until the tile's gate_up counter
+// reaches the number of gate_up row blocks.  Every gate_up index is handed out
+// before any down index and all CTAs are resident at once (cooperative launch),
+// so the waits always end; each is still bounded and gives up with the
+// pipeline-timeout status bit.  Which CTA runs an item never changes its result.
+__global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS)
+decode_layer_kernel(DecArgs gu, DecArgs dn, int32_t* __restrict__ gu_done, int32_t* __restrict__ queue)
 {
     __shared__ uint2 lut[256];
     __shared__ float red[kWarps][2][kMaxNT][32][4];
     __shared__ int last_flag;
+    __shared__ int abort_flag;
+    __shared__ int next_item;
     extern __shared__ __align__(16) uint8_t ring_smem[];   // kWarps * kRingWarp bytes
     const uint32_t ring_base = (uint32_t)__cvta_generic_to_shared(ring_smem);
     const uint32_t lut_base = (uint32_t)__cvta_generic_to_shared(lut);
@@ -380,54 +415,91 @@ __global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS) decode_kernel(D
         ScaleLut l = make_lut((uint32_t)s);
         lut[s] = make_uint2(l.lut, l.lo);
     }
+    if (threadIdx.x == 0) abort_flag = 0;
     SelConst k;
-    k.m33 = opaque(p.sc.m33);
-    k.c04 = opaque(p.sc.c04);
-    k.mcc = opaque(p.sc.mcc);
-    k.c10 = opaque(p.sc.c10);
-    k.fix = opaque(p.sc.fix);
-    k.k16 = opaque(p.sc.k16);
-    k.k4 = opaque(p.sc.k4);
-    k.s2 = opaque(p.sc.s2);
-    k.s16 = opaque(p.sc.s16);
-    k.s18 = opaque(p.sc.s18);
+    k.m33 = opaque(gu.sc.m33);
+    k.c04 = opaque(gu.sc.c04);
+    k.mcc = opaque(gu.sc.mcc);
+    k.c10 = opaque(gu.sc.c10);
+    k.fix = opaque(gu.sc.fix);
+    k.k16 = opaque(gu.sc.k16);
+    k.k4 = opaque(gu.sc.k4);
+    k.s2 = opaque(gu.sc.s2);
+    k.s16 = opaque(gu.sc.s16);
+    k.s18 = opaque(gu.sc.s18);
     __syncthreads();
 
-    const int n_tiles = *p.tile_count;
-    const int n_items = n_tiles * p.row_blocks;
+    const int n_tiles = *gu.tile_count;
+    const int n_gu = n_tiles * gu.row_blocks;
+    const int n_all = n_gu + n_tiles * dn.row_blocks;
     // AND of every lut word used: a valid scale's lut word has bit 31 set, an
     // invalid one is 0, so the AND is 0 exactly when a bad scale byte was read.
     uint32_t lut_and = 0xFFFFFFFFu;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const int4 tile = p.tiles[it / p.row_blocks];
-        const int rb = it % p.row_blocks;
-        const int nt = (tile.z + 7) >> 3;
-        if (nt == 1) run_item<kGateUp, 1>(p, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
-        else run_item<kGateUp, 2>(p, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
-        if (!kGateUp) {
+
+    int it = blockIdx.x;
+    while (it < n_all) {
+        // the item after this one (read after the barriers of this item)
+        if (threadIdx.x == 0) next_item = (int)gridDim.x + atomicAdd(queue, 1);
+        if (it < n_gu) {
+            // gate_up: h = SiLU(gate) * up
+            const int ti = it / gu.row_blocks;
+            const int4 tile = gu.tiles[ti];
+            const int rb = it % gu.row_blocks;
+            if (tile.z <= 8) run_item<true, 1>(gu, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
+            else run_item<true, 2>(gu, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
+            // run_item ends with a CTA barrier after its h stores
+            if (threadIdx.x == 0) {
+                __threadfence();
+                atomicAdd(gu_done + ti, 1);
+            }
+        } else {
+            // down (+ combine): stage slot = w * (W_down h)
+            const int id = it - n_gu;
+            const int ti = id / dn.row_blocks;
+            const int4 tile = dn.tiles[ti];
+            const int rb = id % dn.row_blocks;
+            if (threadIdx.x == 0 && (int)ld_acquire(gu_done + ti) < gu.row_blocks) {
+                const long long t0 = clock64();
+                while ((int)ld_acquire(gu_done + ti) < gu.row_blocks) {
+                    if (clock64() - t0 > kWaitLimitCycles) {
+                        abort_flag = 1;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+            }
+            __syncthreads();
+            if (abort_flag) {
+                if (threadIdx.x == 0) flag_status(dn.status, kDevPipelineTimeout);
+                break;
+            }
+            if (tile.z <= 8) run_item<false, 1>(dn, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
+            else run_item<false, 2>(dn, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
             // The last of the n_tiles items that wrote rows [32 rb, 32 rb + 32) of
             // the pair slots sums them into y (fixed j order per token).
             __threadfence();
-            if (threadIdx.x == 0) last_flag = (atomicAdd(p.counters + rb, 1) == n_tiles - 1);
+            if (threadIdx.x == 0) last_flag = (atomicAdd(dn.counters + rb, 1) == n_tiles - 1);
             __syncthreads();
             if (last_flag) {
                 __threadfence();
-                for (int i = threadIdx.x; i < p.T * 32; i += kThreads) {
+                for (int i = threadIdx.x; i < dn.T * 32; i += kThreads) {
                     const int t = i >> 5, m = rb * 32 + (i & 31);
                     float s = 0.f;
-                    for (int j = 0; j < p.k; ++j) {
-                        const int ej = __ldg(p.ids + t * p.k + j);
-                        if ((unsigned)ej < (unsigned)p.E) s += __ldcg(p.stage + (int64_t)(t * p.k + j) * p.H + m);
+                    for (int j = 0; j < dn.k; ++j) {
+                        const int ej = __ldg(dn.ids + t * dn.k + j);
+                        if ((unsigned)ej < (unsigned)dn.E) s += __ldcg(dn.stage + (int64_t)(t * dn.k + j) * dn.H + m);
                     }
                     __nv_bfloat16 yb = __float2bfloat16_rn(s);
-                    p.y[(int64_t)t * p.H + m] = *reinterpret_cast<uint16_t*>(&yb);
+                    dn.y[(int64_t)t * dn.H + m] = *reinterpret_cast<uint16_t*>(&yb);
                 }
-                if (threadIdx.x == 0) p.counters[rb] = 0;
+                if (threadIdx.x == 0) dn.counters[rb] = 0;
             }
             __syncthreads();
         }
+        it = next_item;
+        __syncthreads();   // everyone has read next_item before thread 0 overwrites it
     }
-    if (lut_and == 0) flag_status(p.status, MOE_W2_DEV_BAD_SCALE);
+    if (lut_and == 0) flag_status(gu.status, MOE_W2_DEV_BAD_SCALE);
 }
 
 }  // namespace
@@ -442,15 +514,12 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     constexpr int kDyn = kWarps * kRingWarp;
     static int occ = 0;
     if (occ == 0) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
+        cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<true>, kThreads, kDyn);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_layer_kernel, kThreads, kDyn);
         if (e != cudaSuccess) return e;
         occ = std::max(occ, 1);
     }
-    const int64_t grid_max = (int64_t)sm_count() * occ;
     const int64_t tiles = max_tiles(P, E, true);
 
     DecArgs gp{};
@@ -476,10 +545,6 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     gp.y = y;
     gp.status = status;
     gp.sc = SelConst{0x33333333u, 0x04040404u, 0xCCCCCCCCu, 0x10101010u, 0xC3C3C3C4u, 16u, 4u, 2u, 16u, 18u};
-    cudaError_t e = ev.record(1, s);
-    if (e != cudaSuccess) return e;
-    decode_kernel<true><<<(int)std::min<int64_t>(tiles * gp.row_blocks, grid_max), kThreads, kDyn, s>>>(gp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     DecArgs dp = gp;
     dp.codes = w.w2_codes;
@@ -488,9 +553,20 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     dp.rows_per_expert = H;
     dp.row_blocks = H / 32;
     dp.act = ws.h;
-    if ((e = ev.record(2, s)) != cudaSuccess) return e;
-    decode_kernel<false><<<(int)std::min<int64_t>(tiles * dp.row_blocks, grid_max), kThreads, kDyn, s>>>(dp);
-    return cudaGetLastError();
+    int32_t* gu_done = ws.counters + H / 32;   // [tiles], zeroed by the permutation kernel
+    int32_t* queue = gu_done + tiles;          // item queue, zeroed by the permutation kernel
+
+    // every CTA resident at once: at most occupancy x SMs, and no more than the
+    // larger phase has items
+    const int64_t grid = std::min<int64_t>((int64_t)sm_count() * occ,
+                                           tiles * std::max<int64_t>(gp.row_blocks, dp.row_blocks));
+    cudaError_t e = ev.record(1, s);
+    if (e != cudaSuccess) return e;
+    if ((e = ev.record(2, s)) != cudaSuccess) return e;   // one kernel: phases 1 and 2 coincide
+    void* args[] = {&gp, &dp, &gu_done, &queue};
+    e = cudaLaunchCooperativeKernel((const void*)decode_layer_kernel, dim3((unsigned)grid), dim3(kThreads), args,
+                                    (size_t)kDyn, s);
+    return e;
 }
 
 }  // namespace moe_w2

@@ -82,6 +82,98 @@ __device__ __forceinline__ uint32_t expand_pair(const ScaleLut& l, uint32_t sel)
     return __byte_perm(l.lut, l.lo, sel);
 }
 
+// ------------------------------------------------------------------ selector words (both GEMM paths)
+struct SelConst {
+    uint32_t m33, c04, mcc, c10, fix, k16, k4, s2, s16, s18;
+};
+
+__device__ __forceinline__ uint32_t mad_lo(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t shr(uint32_t a, uint32_t n)
+{
+    uint32_t d;
+    asm("shr.b32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(n));
+    return d;
+}
+// (a & b) | c in one logic op
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// Byte-permute with the selector used as is: every selector nibble built below
+// has bit 3 clear, so it needs no masking (the __byte_perm intrinsic promises to
+// use only 3 bits of each nibble).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+// A value the compiler cannot see through: keeps a constant in a register, so
+// every instruction below takes it as a register operand (instructions with two
+// immediates would otherwise be split in two, or need a move per use).
+__device__ __forceinline__ uint32_t opaque(uint32_t v)
+{
+    asm volatile("" : "+r"(v));
+    return v;
+}
+
+// Selector words of a 16-code word w (code i in bits 2i..2i+1) for the bf16
+// pairs (c_r, c_{r+4}) [lo] and (c_{r+8}, c_{r+12}) [hi].  In each selector byte
+// the high nibble is the code (0..3: a byte of the lut word) and the low nibble
+// is 4 | (any two bits) (a byte of the lo word); the byte-permute reads only the
+// low 16 bits of a selector, so only those need to be exact.  From
+//   mp  = (w & 0x33333333) | 0x04040404   codes 4b, 4b+2 of byte b, plus 4 per byte
+//   m2p = (w & 0xCCCCCCCC) | 0x10101010   codes 4b+1, 4b+3, plus 0x10 per byte
+// (one logic op each) the eight selectors are
+//   lo: r=0 mp*16 - 0x3C3C3C3C   r=1 m2p*4 - 0x3C3C3C3C   r=2 mp   r=3 m2p >> 2
+//   hi: the lo selector of the same r shifted right by 16 (r=3: m2p >> 18)
+// (the subtractions remove the shifted fill and leave 0x04 per byte).  Per word:
+// 2 logic ops, 5 shifts and 8 byte-permutes on the ALU pipe, 2 multiply-adds on
+// the FMA pipe.  Right shifts stay shifts: as the high word of a product they
+// would run on the FMA pipe at a quarter of its rate.
+struct Masks {
+    uint32_t mp, m2p;
+};
+__device__ __forceinline__ Masks word_masks(uint32_t w, const SelConst& k)
+{
+    return Masks{and_or(w, k.m33, k.c04), and_or(w, k.mcc, k.c10)};
+}
+__device__ __forceinline__ void selectors(const Masks& s, const SelConst& k, uint32_t (&lo)[4], uint32_t (&hi)[4])
+{
+    lo[0] = mad_lo(s.mp, k.k16, k.fix);
+    lo[1] = mad_lo(s.m2p, k.k4, k.fix);
+    lo[2] = s.mp;
+    lo[3] = shr(s.m2p, k.s2);
+    hi[0] = shr(lo[0], k.s16);
+    hi[1] = shr(lo[1], k.s16);
+    hi[2] = shr(s.mp, k.s16);
+    hi[3] = shr(s.m2p, k.s18);
+}
+
+// The selector constants as opaque registers (loaded once per thread).
+__device__ __forceinline__ SelConst sel_const_regs()
+{
+    SelConst k;
+    k.m33 = opaque(0x33333333u);
+    k.c04 = opaque(0x04040404u);
+    k.mcc = opaque(0xCCCCCCCCu);
+    k.c10 = opaque(0x10101010u);
+    k.fix = opaque(0xC3C3C3C4u);
+    k.k16 = opaque(16u);
+    k.k4 = opaque(4u);
+    k.s2 = opaque(2u);
+    k.s16 = opaque(16u);
+    k.s18 = opaque(18u);
+    return k;
+}
+
 // ------------------------------------------------------------------ mma.sync (decode)
 __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1)
 {
@@ -92,7 +184,7 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // ------------------------------------------------------------------ workspace
 struct Workspace {

@@ -49,10 +49,6 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxNT = 2;     // n-tiles of 8 pairs per item (tiles of <= 16 pairs)
 
-struct SelConst {
-    uint32_t m33, c04, mcc, c10, fix, k16, k4, s2, s16, s18;
-};
-
 struct DecArgs {
     const uint8_t* codes;      // [E][rows_per_expert][K/4]
     const uint8_t* scales;     // [E][rows_per_expert][K/32]
@@ -75,7 +71,6 @@ struct DecArgs {
     int32_t* counters;         // down: per 32-row block of y
     uint16_t* y;
     uint32_t* status;
-    SelConst sc;               // selector constants (see selectors())
 };
 
 // Coherent 128-bit load (plain ld.global) for data another CTA of the same
@@ -98,76 +93,6 @@ __device__ __forceinline__ uint32_t ld_acquire(const int32_t* p)
 __device__ __forceinline__ uint32_t word_of(const uint4& q, int i)
 {
     return i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
-}
-
-__device__ __forceinline__ uint32_t mad_lo(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t shr(uint32_t a, uint32_t n)
-{
-    uint32_t d;
-    asm("shr.b32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(n));
-    return d;
-}
-// (a & b) | c in one logic op
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-// Byte-permute with the selector used as is: every selector nibble built below
-// has bit 3 clear, so it needs no masking (the __byte_perm intrinsic promises to
-// use only 3 bits of each nibble).
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
-{
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-// A value the compiler cannot see through: keeps a constant in a register, so
-// every instruction below takes it as a register operand (instructions with two
-// immediates would otherwise be split in two, or need a move per use).
-__device__ __forceinline__ uint32_t opaque(uint32_t v)
-{
-    asm volatile("" : "+r"(v));
-    return v;
-}
-
-// Selector words of a 16-code word w (code i in bits 2i..2i+1) for the bf16
-// pairs (c_r, c_{r+4}) [lo] and (c_{r+8}, c_{r+12}) [hi].  In each selector byte
-// the high nibble is the code (0..3: a byte of the lut word) and the low nibble
-// is 4 | (any two bits) (a byte of the lo word); the byte-permute reads only the
-// low 16 bits of a selector, so only those need to be exact.  From
-//   mp  = (w & 0x33333333) | 0x04040404   codes 4b, 4b+2 of byte b, plus 4 per byte
-//   m2p = (w & 0xCCCCCCCC) | 0x10101010   codes 4b+1, 4b+3, plus 0x10 per byte
-// (one logic op each) the eight selectors are
-//   lo: r=0 mp*16 - 0x3C3C3C3C   r=1 m2p*4 - 0x3C3C3C3C   r=2 mp   r=3 m2p >> 2
-//   hi: the lo selector of the same r shifted right by 16 (r=3: m2p >> 18)
-// (the subtractions remove the shifted fill and leave 0x04 per byte).  Per word:
-// 2 logic ops, 5 shifts and 8 byte-permutes on the ALU pipe, 2 multiply-adds on
-// the FMA pipe.  Right shifts stay shifts: as the high word of a product they
-// would run on the FMA pipe at a quarter of its rate.
-struct Masks {
-    uint32_t mp, m2p;
-};
-__device__ __forceinline__ Masks word_masks(uint32_t w, const SelConst& k)
-{
-    return Masks{and_or(w, k.m33, k.c04), and_or(w, k.mcc, k.c10)};
-}
-__device__ __forceinline__ void selectors(const Masks& s, const SelConst& k, uint32_t (&lo)[4], uint32_t (&hi)[4])
-{
-    lo[0] = mad_lo(s.mp, k.k16, k.fix);
-    lo[1] = mad_lo(s.m2p, k.k4, k.fix);
-    lo[2] = s.mp;
-    lo[3] = shr(s.m2p, k.s2);
-    hi[0] = shr(lo[0], k.s16);
-    hi[1] = shr(lo[1], k.s16);
-    hi[2] = shr(s.mp, k.s16);
-    hi[3] = shr(s.m2p, k.s18);
 }
 
 // Per-thread asynchronous copies global -> shared; the issuing thread's
@@ -416,17 +341,7 @@ decode_layer_kernel(DecArgs gu, DecArgs dn, int32_t* __restrict__ gu_done, int32
         lut[s] = make_uint2(l.lut, l.lo);
     }
     if (threadIdx.x == 0) abort_flag = 0;
-    SelConst k;
-    k.m33 = opaque(gu.sc.m33);
-    k.c04 = opaque(gu.sc.c04);
-    k.mcc = opaque(gu.sc.mcc);
-    k.c10 = opaque(gu.sc.c10);
-    k.fix = opaque(gu.sc.fix);
-    k.k16 = opaque(gu.sc.k16);
-    k.k4 = opaque(gu.sc.k4);
-    k.s2 = opaque(gu.sc.s2);
-    k.s16 = opaque(gu.sc.s16);
-    k.s18 = opaque(gu.sc.s18);
+    const SelConst k = sel_const_regs();
     __syncthreads();
 
     const int n_tiles = *gu.tile_count;
@@ -544,7 +459,6 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     gp.counters = ws.counters;
     gp.y = y;
     gp.status = status;
-    gp.sc = SelConst{0x33333333u, 0x04040404u, 0xCCCCCCCCu, 0x10101010u, 0xC3C3C3C4u, 16u, 4u, 2u, 16u, 18u};
 
     DecArgs dp = gp;
     dp.codes = w.w2_codes;

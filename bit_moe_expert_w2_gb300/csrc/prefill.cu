@@ -19,11 +19,14 @@
 // gate rows interleaved with their 64 up rows (A row 2i = gate i, 2i+1 = up i),
 // so each gate/up pair of accumulator rows sits in adjacent TMEM lanes of one
 // warp.  D[128 x N] (fp32) lives in tensor memory: lanes = weight rows,
-// columns = pairs.
+// columns = pairs; two such accumulators (all 512 columns) let the epilogue of
+// one item run while the next item's main loop fills the other.
 //   warps 0-3  expand the A tile (thread r = A row r) into the 128B-swizzled
-//              smem layout, then run the epilogue for their 32 TMEM lanes
+//              smem layout; each thread streams its row's codes from global
+//              memory 8 stages ahead, continuing across items
 //   warp 4     TMA producer of the B tiles (activations, 16 rows per copy)
 //   warp 5     MMA issuer (one thread): 4 x tcgen05.mma (K = 16) per stage
+//   warps 6-9  epilogue: TMEM lanes 32*(warp % 4) .. +31
 #include <algorithm>
 #include <mutex>
 
@@ -38,12 +41,13 @@ constexpr int kStages = 4;
 constexpr int kRowsA = 128;              // UMMA M
 constexpr int kMaxN = 256;               // pairs per tile (UMMA N <= 256)
 constexpr int kExpThreads = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kPre = 8;                  // code prefetch distance (stages)
 constexpr uint32_t kABytes = kRowsA * 128;
 constexpr uint32_t kBBytes = kMaxN * 128;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;            // two accumulators of kMaxN columns
 
 struct GemmParams {
     const uint8_t* codes;    // plane codes of this projection [E][rows_per_expert][K/4]
@@ -67,6 +71,20 @@ __device__ __forceinline__ uint32_t word_i(const uint4& q, int i)
     return i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
 }
 
+// Row pointers of expansion thread r for item `it` (codes and scales of its A row).
+template <bool kGateUp>
+__device__ __forceinline__ void item_row(const GemmParams& p, int it, int r, const uint8_t*& rc, const uint8_t*& rs)
+{
+    const int4 tile = p.tiles[it / p.row_blocks];
+    const int rb = it % p.row_blocks;
+    int row;
+    if (kGateUp) row = (r & 1 ? p.I : 0) + rb * 64 + (r >> 1);
+    else row = rb * kRowsA + r;
+    const int64_t grow = (int64_t)tile.x * p.rows_per_expert + row;
+    rc = p.codes + grow * (p.K / 4);
+    rs = p.scales + grow * (p.K / 32);
+}
+
 template <bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap,
                                                                       GemmParams p)
@@ -74,7 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
-    __shared__ __align__(8) uint64_t dfull_bar;
+    __shared__ __align__(8) uint64_t dfull_bar[2];
+    __shared__ __align__(8) uint64_t dempty_bar[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     __shared__ uint2 lut_tab[256];
@@ -92,7 +111,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
             mbar_init(smem_u32(&full_bar[s]), kExpThreads + 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
-        mbar_init(smem_u32(&dfull_bar), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&dfull_bar[b]), 1);
+            mbar_init(smem_u32(&dempty_bar[b]), kExpThreads);
+        }
         abort_flag = 0;
         mbar_fence_init();
     }
@@ -108,104 +130,70 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
 
     const int n_items = *p.tile_count * p.row_blocks;
     const int nk = p.K / kBK;
+    // items of this CTA: blockIdx.x + n * gridDim.x, n = 0 .. my_items-1
+    const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
     if (warp < 4) {
-        // ------------------------------------------------ expanders + epilogue
+        // ------------------------------------------------ expanders
         const int r = tid;   // A row
-        uint32_t g = 0, items_done = 0, lut_min = 0xFFFFFFFFu;
-        for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
-            const int4 tile = p.tiles[it / p.row_blocks];
-            const int rb = it % p.row_blocks;
-            const int e = tile.x, q0 = tile.y, nrows = tile.z;
-            int row;
-            if (kGateUp) row = (r & 1 ? p.I : 0) + rb * 64 + (r >> 1);
-            else row = rb * kRowsA + r;
-            const int64_t grow = (int64_t)e * p.rows_per_expert + row;
-            const uint8_t* rc = p.codes + grow * (p.K / 4);
-            const uint8_t* rs = p.scales + grow * (p.K / 32);
-
-            uint4 q[4];
-            uint32_t sc[4];
-#pragma unroll
-            for (int d = 0; d < 4; ++d) {   // K is a multiple of 256: nk >= 4 and nk % 4 == 0
-                q[d] = ldg_stream_u4(rc + d * 16);
-                sc[d] = ldg_u16(rs + d * 2);
-            }
-            bool ok = true;
-            for (int kb = 0; kb < nk && ok; kb += 4) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int kk = kb + u;
-                    const uint4 cq = q[u];
-                    const uint32_t cs = sc[u];
-                    if (kk + 4 < nk) {
-                        q[u] = ldg_stream_u4(rc + (kk + 4) * 16);
-                        sc[u] = ldg_u16(rs + (kk + 4) * 2);
-                    }
-                    const uint32_t slot = g % kStages, ph = (g / kStages) & 1u;
-                    if (!mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint2 L0 = lut_tab[cs & 0xFF], L1 = lut_tab[cs >> 8];
-                    lut_min = min(lut_min, min(L0.x, L1.x));
-                    const uint32_t a_tile = smem_base + slot * kStageBytes;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t w = word_i(cq, i);
-                        const ScaleLut L = (i < 2) ? ScaleLut{L0.x, L0.y} : ScaleLut{L1.x, L1.y};
-                        const uint32_t s0 = code_selector<0>(w), s1 = code_selector<1>(w);
-                        const uint32_t s2 = code_selector<2>(w), s3 = code_selector<3>(w);
-                        uint4 c0, c1;
-                        c0.x = expand_pair(L, s0);
-                        c0.y = expand_pair(L, s0 >> 16);
-                        c0.z = expand_pair(L, s1);
-                        c0.w = expand_pair(L, s1 >> 16);
-                        c1.x = expand_pair(L, s2);
-                        c1.y = expand_pair(L, s2 >> 16);
-                        c1.z = expand_pair(L, s3);
-                        c1.w = expand_pair(L, s3 >> 16);
-                        sts_u4(a_tile + sw128_offset(r, 2 * i), c0);
-                        sts_u4(a_tile + sw128_offset(r, 2 * i + 1), c1);
-                    }
-                    fence_proxy_async_smem();
-                    mbar_arrive(smem_u32(&full_bar[slot]));
-                    ++g;
+        const SelConst k = sel_const_regs();
+        uint32_t lut_min = 0xFFFFFFFFu;
+        const int64_t total = (int64_t)my_items * nk;   // stages this CTA runs
+        // fetch cursor: stage f = (item fi, k-stage fk) of this thread's row
+        int fi = 0, fk = 0;
+        const uint8_t *rc = nullptr, *rs = nullptr;
+        if (my_items > 0) item_row<kGateUp>(p, blockIdx.x, r, rc, rs);
+        auto fetch = [&](uint4& q, uint32_t& sc) {
+            if (fi < my_items) {
+                q = ldg_stream_u4(rc + fk * 16);
+                sc = ldg_u16(rs + fk * 2);
+                if (++fk == nk) {
+                    fk = 0;
+                    if (++fi < my_items) item_row<kGateUp>(p, blockIdx.x + fi * (int)gridDim.x, r, rc, rs);
                 }
             }
-            if (*abort) break;
-
-            // epilogue: D rows 32*warp .. 32*warp+31, columns = pairs of the tile
-            if (!mbar_wait(smem_u32(&dfull_bar), items_done & 1u, abort)) break;
-            ++items_done;
-            tc_fence_after();
-            const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
-            for (int c0 = 0; c0 < nrows; c0 += 32) {
-                float v[32];
-                tmem_ld32(lane_base + c0, v);
-                if (kGateUp) {
-                    const int n = rb * 64 + (r >> 1);
-                    const int pos = t16_pos(n);
+        };
+        uint4 q[kPre];
+        uint32_t sc[kPre];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float up = __shfl_down_sync(0xffffffffu, v[j], 1);
-                        if (!(r & 1) && c0 + j < nrows) {
-                            __nv_bfloat16 hb = __float2bfloat16_rn(silu_f(v[j]) * up);
-                            p.h_t16[(int64_t)(q0 + c0 + j) * p.I + pos] = *reinterpret_cast<uint16_t*>(&hb);
-                        }
-                    }
-                } else {
-                    const int m = rb * kRowsA + r;
+        for (int d = 0; d < kPre; ++d) fetch(q[d], sc[d]);
+        bool ok = true;
+        for (int64_t g0 = 0; g0 < total && ok; g0 += kPre) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if (c0 + j < nrows) {
-                            const int pr = p.sorted[q0 + c0 + j];
-                            p.stage[(int64_t)pr * p.H + m] = p.weights[pr] * v[j];
-                        }
-                    }
+            for (int u = 0; u < kPre; ++u) {
+                const int64_t g = g0 + u;
+                if (g >= total) break;
+                const uint4 cq = q[u];
+                const uint32_t cs = sc[u];
+                fetch(q[u], sc[u]);
+                const uint32_t slot = (uint32_t)(g % kStages), ph = (uint32_t)((g / kStages) & 1);
+                if (!mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort)) {
+                    ok = false;
+                    break;
                 }
+                const uint2 L0 = lut_tab[cs & 0xFF], L1 = lut_tab[cs >> 8];
+                lut_min = min(lut_min, min(L0.x, L1.x));
+                const uint32_t a_tile = smem_base + slot * kStageBytes;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint2 L = (i < 2) ? L0 : L1;
+                    uint32_t lo[4], hi[4];
+                    selectors(word_masks(word_i(cq, i), k), k, lo, hi);
+                    uint4 c0, c1;
+                    c0.x = prmt(L.x, L.y, lo[0]);
+                    c0.y = prmt(L.x, L.y, hi[0]);
+                    c0.z = prmt(L.x, L.y, lo[1]);
+                    c0.w = prmt(L.x, L.y, hi[1]);
+                    c1.x = prmt(L.x, L.y, lo[2]);
+                    c1.y = prmt(L.x, L.y, hi[2]);
+                    c1.z = prmt(L.x, L.y, lo[3]);
+                    c1.w = prmt(L.x, L.y, hi[3]);
+                    sts_u4(a_tile + sw128_offset(r, 2 * i), c0);
+                    sts_u4(a_tile + sw128_offset(r, 2 * i + 1), c1);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&full_bar[slot]));
             }
-            tc_fence_before();
         }
         if (lut_min == 0) flag_status(p.status, MOE_W2_DEV_BAD_SCALE);
     } else if (warp == 4) {
@@ -213,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         if (lane == 0) {
             prefetch_tmap(&bmap);
             uint32_t g = 0;
-            for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+            for (int n = 0; n < my_items && !*abort; ++n) {
+                const int it = blockIdx.x + n * (int)gridDim.x;
                 const int4 tile = p.tiles[it / p.row_blocks];
                 const int q0 = tile.y, npad = (tile.z + 15) & ~15;
                 for (int kk = 0; kk < nk; ++kk) {
@@ -227,14 +216,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
                 }
             }
         }
-    } else {
+    } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t g = 0;
-            for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+            for (int n = 0; n < my_items && !*abort; ++n) {
+                const int it = blockIdx.x + n * (int)gridDim.x;
                 const int4 tile = p.tiles[it / p.row_blocks];
                 const uint32_t npad = (tile.z + 15) & ~15;
                 const uint32_t idesc = idesc_bf16_f32(kRowsA, npad);
+                const uint32_t b = n & 1;
+                // accumulator b is free once the epilogue of item n-2 drained it
+                if (!mbar_wait(smem_u32(&dempty_bar[b]), ((n >> 1) & 1u) ^ 1u, abort)) break;
+                tc_fence_after();
+                const uint32_t acc = tmem + b * kMaxN;
                 for (int kk = 0; kk < nk; ++kk) {
                     const uint32_t slot = g % kStages, ph = (g / kStages) & 1u;
                     if (!mbar_wait(smem_u32(&full_bar[slot]), ph, abort)) break;
@@ -243,12 +238,60 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
                     const uint64_t ad = smem_desc_sw128(a_addr), bd = smem_desc_sw128(a_addr + kABytes);
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4)
-                        umma_f16_ss(tmem, ad + 2 * k4, bd + 2 * k4, idesc, (kk | k4) != 0);
+                        umma_f16_ss(acc, ad + 2 * k4, bd + 2 * k4, idesc, (kk | k4) != 0);
                     umma_commit(smem_u32(&empty_bar[slot]));
                     ++g;
                 }
-                umma_commit(smem_u32(&dfull_bar));
+                umma_commit(smem_u32(&dfull_bar[b]));
             }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 6-9)
+        const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+        const int r = 32 * quarter + lane;      // A row
+        for (int n = 0; n < my_items && !*abort; ++n) {
+            const int it = blockIdx.x + n * (int)gridDim.x;
+            const int4 tile = p.tiles[it / p.row_blocks];
+            const int rb = it % p.row_blocks;
+            const int q0 = tile.y, nrows = tile.z;
+            const uint32_t b = n & 1;
+            if (!mbar_wait(smem_u32(&dfull_bar[b]), (n >> 1) & 1u, abort)) break;
+            tc_fence_after();
+            const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + b * kMaxN;
+            for (int c0 = 0; c0 < nrows; c0 += 32) {
+                float v[32];
+                tmem_ld32(lane_base + c0, v);
+                if (kGateUp) {
+                    const int nn = rb * 64 + (r >> 1);
+                    const int pos = t16_pos(nn);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float up = __shfl_down_sync(0xffffffffu, v[j], 1);
+                        if (!(r & 1) && c0 + j < nrows) {
+                            __nv_bfloat16 hb = __float2bfloat16_rn(silu_f(v[j]) * up);
+                            p.h_t16[(int64_t)(q0 + c0 + j) * p.I + pos] = *reinterpret_cast<uint16_t*>(&hb);
+                        }
+                    }
+                } else {
+                    // lane j fetches column c0+j's pair id and router weight once;
+                    // shuffles hand them to every lane
+                    const int m = rb * kRowsA + r;
+                    int my_pr = 0;
+                    float my_w = 0.f;
+                    if (c0 + lane < nrows) {
+                        my_pr = __ldg(p.sorted + q0 + c0 + lane);
+                        my_w = __ldg(p.weights + my_pr);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int pr = __shfl_sync(0xffffffffu, my_pr, j);
+                        const float wt = __shfl_sync(0xffffffffu, my_w, j);
+                        if (c0 + j < nrows) p.stage[(int64_t)pr * p.H + m] = wt * v[j];
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&dempty_bar[b]));
         }
     }
 

@@ -22,11 +22,13 @@
 // columns = pairs; two such accumulators (all 512 columns) let the epilogue of
 // one item run while the next item's main loop fills the other.
 //   warps 0-3  expand the A tile (thread r = A row r) into the 128B-swizzled
-//              smem layout; each thread streams its row's codes from global
-//              memory 8 stages ahead, continuing across items
-//   warp 4     TMA producer of the B tiles (activations, 16 rows per copy)
+//              smem layout, from raw codes in shared memory (scale bytes are
+//              loaded per thread one superstage ahead)
+//   warp 4     TMA producer of the B tiles (activations, 64 pair rows per copy)
 //   warp 5     MMA issuer (one thread): 4 x tcgen05.mma (K = 16) per stage
 //   warps 6-9  epilogue: TMEM lanes 32*(warp % 4) .. +31
+//   warp 10    TMA producer of the raw code tiles: one superstage (4 stages,
+//              64 code bytes per A row) at a time, two superstages ahead
 #include <algorithm>
 #include <mutex>
 
@@ -40,13 +42,17 @@ constexpr int kBK = 64;                  // K per pipeline stage
 constexpr int kStages = 4;
 constexpr int kRowsA = 128;              // UMMA M
 constexpr int kMaxN = 256;               // pairs per tile (UMMA N <= 256)
+constexpr int kBRows = 64;               // pair rows per B TMA box
 constexpr int kExpThreads = 128;
-constexpr int kThreads = 320;
-constexpr int kPre = 8;                  // code prefetch distance (stages)
+constexpr int kThreads = 352;
+constexpr int kSuper = 4;                // stages per code superstage (256 K, 64 code bytes per row)
+constexpr int kCSlots = 2;               // code superstages in flight
 constexpr uint32_t kABytes = kRowsA * 128;
 constexpr uint32_t kBBytes = kMaxN * 128;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024;
+constexpr uint32_t kCodeRowBytes = kSuper * 16;          // code bytes per A row per superstage
+constexpr uint32_t kCodeBytes = kRowsA * kCodeRowBytes;   // one superstage of raw codes, 64B-swizzled rows
+constexpr uint32_t kSmemBytes = kStages * kStageBytes + kCSlots * kCodeBytes + 1024;
 constexpr uint32_t kTmemCols = 512;            // two accumulators of kMaxN columns
 
 struct GemmParams {
@@ -87,6 +93,7 @@ __device__ __forceinline__ void item_row(const GemmParams& p, int it, int r, con
 
 template <bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap,
+                                                                      const __grid_constant__ CUtensorMap cmap,
                                                                       GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -94,6 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     __shared__ __align__(8) uint64_t empty_bar[kStages];
     __shared__ __align__(8) uint64_t dfull_bar[2];
     __shared__ __align__(8) uint64_t dempty_bar[2];
+    __shared__ __align__(8) uint64_t cfull_bar[kCSlots];
+    __shared__ __align__(8) uint64_t cempty_bar[kCSlots];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     __shared__ uint2 lut_tab[256];
@@ -115,6 +124,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
             mbar_init(smem_u32(&dfull_bar[b]), 1);
             mbar_init(smem_u32(&dempty_bar[b]), kExpThreads);
         }
+        for (int c = 0; c < kCSlots; ++c) {
+            mbar_init(smem_u32(&cfull_bar[c]), 1);
+            mbar_init(smem_u32(&cempty_bar[c]), kExpThreads);
+        }
         abort_flag = 0;
         mbar_fence_init();
     }
@@ -133,40 +146,51 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     // items of this CTA: blockIdx.x + n * gridDim.x, n = 0 .. my_items-1
     const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
+    const int n_super = (nk + kSuper - 1) / kSuper;   // code superstages per item
+    const uint32_t code_base = smem_base + kStages * kStageBytes;
+
     if (warp < 4) {
         // ------------------------------------------------ expanders
         const int r = tid;   // A row
         const SelConst k = sel_const_regs();
         uint32_t lut_min = 0xFFFFFFFFu;
-        const int64_t total = (int64_t)my_items * nk;   // stages this CTA runs
-        // fetch cursor: stage f = (item fi, k-stage fk) of this thread's row
-        int fi = 0, fk = 0;
-        const uint8_t *rc = nullptr, *rs = nullptr;
-        if (my_items > 0) item_row<kGateUp>(p, blockIdx.x, r, rc, rs);
-        auto fetch = [&](uint4& q, uint32_t& sc) {
-            if (fi < my_items) {
-                q = ldg_stream_u4(rc + fk * 16);
-                sc = ldg_u16(rs + fk * 2);
-                if (++fk == nk) {
-                    fk = 0;
-                    if (++fi < my_items) item_row<kGateUp>(p, blockIdx.x + fi * (int)gridDim.x, r, rc, rs);
-                }
-            }
+        // this thread's row inside the code tile: gate_up puts gate rows in the
+        // first 64 rows of the tile and up rows in the next 64
+        const int trow = kGateUp ? ((r & 1) * 64 + (r >> 1)) : r;
+        const uint32_t trow_addr = (uint32_t)trow * kCodeRowBytes;
+        const uint32_t swz = (uint32_t)((trow >> 1) & 3);   // 64-byte swizzle: chunk j at j ^ ((row / 2) % 4)
+        // scale bytes of superstage su of item n (one 8-byte load: 4 stages x 2 bytes)
+        auto load_scales = [&](int n, int su, uint2& s0) {
+            const int it = blockIdx.x + n * (int)gridDim.x;
+            const uint8_t *rc, *rs;
+            item_row<kGateUp>(p, it, r, rc, rs);
+            s0 = __ldg(reinterpret_cast<const uint2*>(rs + su * kSuper * 2));
         };
-        uint4 q[kPre];
-        uint32_t sc[kPre];
+        int n = 0, su = 0;           // current (item, superstage)
+        uint2 sa = make_uint2(0, 0);
+        if (my_items > 0) load_scales(0, 0, sa);
+        uint32_t g = 0, u = 0;       // stage and superstage counters of the whole stream
+        bool ok = my_items > 0;
+        while (ok) {
+            // prefetch the next superstage's scale bytes
+            int n2 = n, su2 = su + 1;
+            if (su2 == n_super) {
+                su2 = 0;
+                ++n2;
+            }
+            uint2 na = make_uint2(0, 0);
+            if (n2 < my_items) load_scales(n2, su2, na);
+
+            const uint32_t cslot = u % kCSlots;
+            if (!mbar_wait(smem_u32(&cfull_bar[cslot]), (u / kCSlots) & 1u, abort)) break;
+            const uint32_t ctile = code_base + cslot * kCodeBytes + trow_addr;
+            const int s_end = min(kSuper, nk - su * kSuper);
 #pragma unroll
-        for (int d = 0; d < kPre; ++d) fetch(q[d], sc[d]);
-        bool ok = true;
-        for (int64_t g0 = 0; g0 < total && ok; g0 += kPre) {
-#pragma unroll
-            for (int u = 0; u < kPre; ++u) {
-                const int64_t g = g0 + u;
-                if (g >= total) break;
-                const uint4 cq = q[u];
-                const uint32_t cs = sc[u];
-                fetch(q[u], sc[u]);
-                const uint32_t slot = (uint32_t)(g % kStages), ph = (uint32_t)((g / kStages) & 1);
+            for (int s = 0; s < kSuper; ++s) {
+                if (s >= s_end) break;
+                const uint32_t slot = g % kStages, ph = (g / kStages) & 1u;
+                const uint4 cq = lds_u4(ctile + ((((uint32_t)s) ^ swz) << 4));
+                const uint32_t cs = ((s & 2 ? sa.y : sa.x) >> (16 * (s & 1))) & 0xFFFFu;
                 if (!mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort)) {
                     ok = false;
                     break;
@@ -193,7 +217,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&full_bar[slot]));
+                ++g;
             }
+            if (!ok) break;
+            mbar_arrive(smem_u32(&cempty_bar[cslot]));   // this thread is done reading the code tile
+            ++u;
+            n = n2;
+            su = su2;
+            sa = na;
+            if (n >= my_items) break;
         }
         if (lut_min == 0) flag_status(p.status, MOE_W2_DEV_BAD_SCALE);
     } else if (warp == 4) {
@@ -204,14 +236,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
             for (int n = 0; n < my_items && !*abort; ++n) {
                 const int it = blockIdx.x + n * (int)gridDim.x;
                 const int4 tile = p.tiles[it / p.row_blocks];
-                const int q0 = tile.y, npad = (tile.z + 15) & ~15;
+                // boxes of kBRows pair rows; rows past the tile's pairs are loaded
+                // too (the MMA reads only the first npad) or zero-filled past P
+                const int q0 = tile.y, nbox = (tile.z + kBRows - 1) / kBRows;
                 for (int kk = 0; kk < nk; ++kk) {
                     const uint32_t slot = g % kStages, ph = (g / kStages) & 1u;
                     if (!mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort)) break;
                     const uint32_t fb = smem_u32(&full_bar[slot]);
-                    mbar_arrive_expect_tx(fb, (uint32_t)npad * 128u);
+                    mbar_arrive_expect_tx(fb, (uint32_t)nbox * kBRows * 128u);
                     const uint32_t b_tile = smem_base + slot * kStageBytes + kABytes;
-                    for (int j = 0; j < npad / 16; ++j) tma_load_2d(b_tile + j * 2048u, &bmap, kk * kBK, q0 + 16 * j, fb);
+                    for (int j = 0; j < nbox; ++j)
+                        tma_load_2d(b_tile + j * kBRows * 128u, &bmap, kk * kBK, q0 + kBRows * j, fb);
                     ++g;
                 }
             }
@@ -243,6 +278,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
                     ++g;
                 }
                 umma_commit(smem_u32(&dfull_bar[b]));
+            }
+        }
+    } else if (warp == 10) {
+        // ------------------------------------------------ TMA producer (raw code tiles)
+        if (lane == 0) {
+            prefetch_tmap(&cmap);
+            uint32_t u = 0;
+            for (int n = 0; n < my_items && !*abort; ++n) {
+                const int it = blockIdx.x + n * (int)gridDim.x;
+                const int4 tile = p.tiles[it / p.row_blocks];
+                const int rb = it % p.row_blocks;
+                const int64_t ebase = (int64_t)tile.x * p.rows_per_expert;
+                for (int su = 0; su < n_super; ++su) {
+                    const uint32_t cslot = u % kCSlots;
+                    if (!mbar_wait(smem_u32(&cempty_bar[cslot]), ((u / kCSlots) & 1u) ^ 1u, abort)) break;
+                    const uint32_t fb = smem_u32(&cfull_bar[cslot]);
+                    mbar_arrive_expect_tx(fb, kCodeBytes);
+                    const uint32_t dst = code_base + cslot * kCodeBytes;
+                    const int x = su * (int)kCodeRowBytes;   // byte column of the superstage
+                    if (kGateUp) {
+                        tma_load_2d(dst, &cmap, x, (int)(ebase + rb * 64), fb);
+                        tma_load_2d(dst + 64 * kCodeRowBytes, &cmap, x, (int)(ebase + p.I + rb * 64), fb);
+                    } else {
+                        tma_load_2d(dst, &cmap, x, (int)(ebase + rb * kRowsA), fb);
+                    }
+                    ++u;
+                }
             }
         }
     } else {
@@ -327,9 +389,16 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
     cudaError_t e = launch_gather(x, ws.sorted, ws.offsets, E, k, H, P, ws.xa, s);
     if (e != cudaSuccess) return e;
 
-    CUtensorMap xmap, hmap;
-    if ((e = make_tmap_2d(&xmap, ws.xa, true, P, H, 64, 16, true)) != cudaSuccess) return e;
-    if ((e = make_tmap_2d(&hmap, ws.h, true, P, I, 64, 16, true)) != cudaSuccess) return e;
+    CUtensorMap xmap, hmap, c13map, c2map;
+    if ((e = make_tmap_2d(&xmap, ws.xa, true, P, H, 64, kBRows, 128)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&hmap, ws.h, true, P, I, 64, kBRows, 128)) != cudaSuccess) return e;
+    // raw code tiles: 64 bytes (256 codes) x 64 rows (gate_up: gate and up halves) or 128 rows
+    if ((e = make_tmap_2d(&c13map, w.w13_codes, false, (int64_t)E * 2 * I, H / 4, kCodeRowBytes, 64, 64)) !=
+        cudaSuccess)
+        return e;
+    if ((e = make_tmap_2d(&c2map, w.w2_codes, false, (int64_t)E * H, I / 4, kCodeRowBytes, kRowsA, 64)) !=
+        cudaSuccess)
+        return e;
 
     if ((e = ev.record(1, s)) != cudaSuccess) return e;
     GemmParams gp{};
@@ -348,7 +417,7 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
     gp.weights = weights;
     gp.status = status;
     const int64_t max_items = max_tiles(P, E, false) * (I / 64);
-    tc_expert_gemm_kernel<true><<<(int)std::min<int64_t>(sms, max_items), kThreads, kSmemBytes, s>>>(xmap, gp);
+    tc_expert_gemm_kernel<true><<<(int)std::min<int64_t>(sms, max_items), kThreads, kSmemBytes, s>>>(xmap, c13map, gp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     if ((e = ev.record(2, s)) != cudaSuccess) return e;
@@ -359,7 +428,7 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
     dp.rows_per_expert = H;
     dp.row_blocks = H / kRowsA;
     const int64_t max_items_d = max_tiles(P, E, false) * (H / kRowsA);
-    tc_expert_gemm_kernel<false><<<(int)std::min<int64_t>(sms, max_items_d), kThreads, kSmemBytes, s>>>(hmap, dp);
+    tc_expert_gemm_kernel<false><<<(int)std::min<int64_t>(sms, max_items_d), kThreads, kSmemBytes, s>>>(hmap, c2map, dp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     return launch_combine(ws.stage, ids, T, k, E, H, y, s);

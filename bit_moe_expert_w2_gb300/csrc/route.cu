@@ -100,7 +100,7 @@ cudaError_t get_encoder()
 }  // namespace
 
 cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, bool bf16, int64_t rows, int64_t cols, uint32_t box_cols,
-                         uint32_t box_rows, bool swizzle128)
+                         uint32_t box_rows, int swizzle_bytes)
 {
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
@@ -111,7 +111,9 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, bool bf16, int64_t 
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

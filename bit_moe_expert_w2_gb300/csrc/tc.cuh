@@ -227,7 +227,7 @@ namespace moe_w2 {
 
 // 2-D tensor map [rows][cols] (row-major) of bf16 or uint8, box {box_cols, box_rows}.
 cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, bool bf16, int64_t rows, int64_t cols,
-                         uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+                         uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
 cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted, const int32_t* offsets, int32_t E, int32_t k,
                           int32_t H, int64_t P, uint16_t* xs, cudaStream_t s);
 cudaError_t launch_combine(const float* stage, const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t H,

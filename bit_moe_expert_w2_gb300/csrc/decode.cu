@@ -13,21 +13,25 @@
 // tcgen05.mma (M=128, K=16) of a CTA costs ~105 cycles whatever N is (measured
 // on GB300), which caps a CTA far below HBM rate, while mma.sync m16n8k16 keeps
 // the weights in registers and reaches the full tensor rate with enough warps.
-// The expansion is integer work split over two pipes: per 16-code word two
-// masks and eight byte-permutes on the ALU pipe, and the eight selector words as
-// multiply-adds on the FMA pipe (the multipliers are kernel parameters, so they
-// stay multiply-adds instead of becoming ALU shifts).  Codes stream through a
-// per-warp cp.async ring (3 chunks deep).
+// The expansion is integer work on the ALU pipe (two masks, five shifts and
+// eight byte-permutes per 16 codes) plus two multiply-adds on the FMA pipe.
+//
+// One kernel runs the whole layer (gate_up, then down with the combine).  Work
+// item = (tile of <= 16 pairs of one expert, 32 weight rows).  Each CTA has four
+// consumer warps that split K of an item (256-element chunks, round robin) and
+// reduce in shared memory in warp order, and one producer warp that runs ahead
+// through the CTA's items: it takes items from a global queue, publishes each
+// item's tile through a small shared-memory ring, and streams every chunk's code
+// bytes (TMA: 32 rows x 64 bytes) and scale bytes (one 8-byte cp.async per row)
+// into a ring of chunk slots.  Consumers only wait on a slot's barrier, read it
+// from shared memory and release it, so the loads of the next item overlap the
+// end of the current one.
 //
 // Per 256-wide K chunk a row is 64 code bytes; thread c of a quad owns bytes
 // [16c, 16c+16), i.e. four 16-code words; MMA (word i, r) takes codes (r, r+4)
 // and (r+8, r+12) of word i from every thread of the quad, which is what the
 // T16 activation layout stores next to each other (one 64-bit load per B
-// fragment).
-//
-// Work item = (tile of <= 16 pairs of one expert, 32 weight rows).  A warp holds
-// two m16 tiles; the four warps of a CTA split K and reduce in shared memory in
-// warp order.  gate_up: m-tile t = gate rows n0+8t.. (A rows 0-7) and the
+// fragment).  gate_up: m-tile t = gate rows n0+8t.. (A rows 0-7) and the
 // matching up rows (A rows 8-15), so gate and up of one (row, pair) meet in one
 // thread for the SiLU(gate)*up epilogue.  down: 32 consecutive rows of W_down;
 // the epilogue multiplies by the router weight and writes the pair's fp32 slot;
@@ -44,10 +48,17 @@ namespace {
 #ifndef MOE_W2_DEC_MIN_CTAS
 #define MOE_W2_DEC_MIN_CTAS 4        // CTAs per SM the register budget is sized for
 #endif
-constexpr int kChunk = 256;   // K elements per chunk
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kMaxNT = 2;     // n-tiles of 8 pairs per item (tiles of <= 16 pairs)
+constexpr int kChunk = 256;          // K elements per chunk
+constexpr int kWarps = 4;            // consumer warps
+constexpr int kThreads = (kWarps + 1) * 32;   // + the producer warp
+constexpr int kMaxNT = 2;            // n-tiles of 8 pairs per item (tiles of <= 16 pairs)
+constexpr int kSlots = 16;           // chunk slots (four per consumer warp; a power of two)
+constexpr uint32_t kSlotCodeBytes = 32 * 64;   // 32 rows x 64 code bytes
+constexpr uint32_t kSlotScaleBytes = 32 * 8;   // 32 rows x 8 UE8M0 bytes
+constexpr uint32_t kSlotBytes = kSlotCodeBytes + kSlotScaleBytes;   // a multiple of 128
+constexpr uint32_t kRingBytes = kSlots * kSlotBytes;
+constexpr int kInfo = 16;            // published items in flight
+constexpr uint32_t kConsumerBarrier = 1;       // named barrier id of the consumer warps
 
 struct DecArgs {
     const uint8_t* codes;      // [E][rows_per_expert][K/4]
@@ -73,21 +84,39 @@ struct DecArgs {
     uint32_t* status;
 };
 
-// Coherent 128-bit load (plain ld.global) for data another CTA of the same
-// launch wrote: the reader's CTA observed the writer's release with a GPU-scope
-// acquire followed by a CTA barrier, so these loads see the data.  The
-// non-coherent read-only path (ld.global.nc) is not allowed for it.
-__device__ __forceinline__ uint4 ldg_coherent_u4(const void* p)
-{
-    uint4 r;
-    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
-}
+struct SharedState {
+    uint64_t full[kSlots];      // producer -> consumers: slot filled (expect_tx arrival + 32 cp.async arrivals)
+    uint64_t empty[kSlots];     // consumer warp -> producer: slot read
+    uint64_t info_full[kInfo];  // producer -> consumers: item published
+    uint64_t info_empty[kInfo]; // consumer warps -> producer: item finished
+    int4 info[kInfo];           // (item index, or -1 at the end; expert; first slot; pairs)
+    uint2 lut[256];
+    float red[kWarps][2][kMaxNT][32][4];
+    int4 cur_info;              // the item the consumer warps work on
+    int last_flag;
+    int stop;
+    int abort_flag;
+};
+
 __device__ __forceinline__ uint32_t ld_acquire(const int32_t* p)
 {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+__device__ __forceinline__ void consumer_sync()
+{
+    asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrier), "n"(kWarps * 32) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+// The barrier gets one arrival once all of this thread's earlier cp.async copies
+// have landed (its expected count includes that arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& q, int i)
@@ -95,80 +124,28 @@ __device__ __forceinline__ uint32_t word_of(const uint4& q, int i)
     return i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
 }
 
-// Per-thread asynchronous copies global -> shared; the issuing thread's
-// wait_group plus a warp barrier orders them before the warp reads them back.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-__device__ __forceinline__ uint4 lds128(uint32_t a)
-{
-    uint4 r;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a) : "memory");
-    return r;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t a)
-{
-    uint2 r;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a) : "memory");
-    return r;
-}
-__device__ __forceinline__ uint32_t lds8(uint32_t a)
-{
-    uint32_t r;
-    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(r) : "r"(a) : "memory");
-    return r;
-}
-
-// Per-warp ring of kDepth chunks.  Slot layout: codes [row a][lane] 16 bytes
-// (lane-major, so a warp's 128-bit reads are conflict-free), then scales
-// [row a][g] the chunk's 8 UE8M0 bytes of the quad's row (copied by lane c = 0;
-// thread c reads bytes 2c and 2c+1).
-constexpr int kDepth = 3;
-constexpr uint32_t kRingCodeBytes = 4 * 32 * 16;   // per slot
-constexpr uint32_t kRingScaleBytes = 4 * 8 * 8;
-constexpr uint32_t kRingSlot = kRingCodeBytes + kRingScaleBytes;
-constexpr uint32_t kRingWarp = kDepth * kRingSlot;
-
+// One item on the consumer warps: K chunks ch = warp, warp + 4, ... from ring
+// slots (qbase + ch) % kSlots, then the split-K reduction and the epilogue.
 template <bool kGateUp, int NT>
-__device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, uint32_t lut_base,
-                                         float (*red)[2][kMaxNT][32][4], uint32_t ring_base, int e, int q0,
-                                         int nrows, int rb, uint32_t& lut_and)
+__device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, SharedState& sh, const uint8_t* ring,
+                                         uint32_t qbase, int q0, int nrows, int rb, uint32_t& lut_and)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
     const int nch = p.K / kChunk;
-    const int64_t rowb = p.K / 4, srowb = p.K / 32;
-
-    // the thread's four A rows: m-tile 0 -> (g, g+8), m-tile 1 -> (16+g, 24+g)
-    int64_t row[4];
+    // slot rows of the thread's four A rows: m-tile 0 -> (g, g+8), m-tile 1 -> (16+g, 24+g);
+    // gate_up slot rows 0-15 are gate rows n0.., 16-31 the matching up rows
+    int srow[4];
     if (kGateUp) {
-        const int64_t base = (int64_t)e * p.rows_per_expert + rb * 16;
-        row[0] = base + g;            // gate n0+g
-        row[1] = base + p.I + g;      // up   n0+g
-        row[2] = base + 8 + g;        // gate n0+8+g
-        row[3] = base + p.I + 8 + g;  // up   n0+8+g
+        srow[0] = g;
+        srow[1] = 16 + g;
+        srow[2] = 8 + g;
+        srow[3] = 24 + g;
     } else {
-        const int64_t base = (int64_t)e * p.rows_per_expert + rb * 32;
-        row[0] = base + g;
-        row[1] = base + 8 + g;
-        row[2] = base + 16 + g;
-        row[3] = base + 24 + g;
-    }
-    // global sources of this warp's first chunk; each later chunk is kWarps chunks on
-    const uint8_t* cp[4];
-    const uint8_t* sp[4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        cp[a] = p.codes + row[a] * rowb + warp * 64 + c * 16;
-        sp[a] = p.scales + row[a] * srowb + warp * 8;
+        srow[0] = g;
+        srow[1] = 8 + g;
+        srow[2] = 16 + g;
+        srow[3] = 24 + g;
     }
     // B rows: pair j = 8*nt + g of the tile.  Columns past the tile's pairs read
     // pair 0's row (always valid); their results are never stored.
@@ -177,7 +154,7 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, ui
     for (int nt = 0; nt < NT; ++nt) {
         const int j = nt * 8 + g < nrows ? nt * 8 + g : 0;
         const int64_t br = kGateUp ? (int64_t)(__ldg(p.sorted + q0 + j) / p.k) : (int64_t)(q0 + j);
-        brow[nt] = p.act + br * p.K + warp * kChunk + c * 64;
+        brow[nt] = p.act + br * p.K + c * 64;
     }
 
     float acc[2][NT][4];
@@ -186,62 +163,42 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, ui
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
 
-    // ring of this warp's chunks ch = warp + kWarps * idx
-    const uint32_t ring = ring_base + (uint32_t)warp * kRingWarp;
-    const int my_chunks = nch > warp ? (nch - warp + kWarps - 1) / kWarps : 0;
-    uint32_t wr_slot = ring;
-    int issued = 0;
-    auto issue = [&]() {
-        if (issued < my_chunks) {
-            const int64_t off = (int64_t)issued * (kWarps * 64);
-#pragma unroll
-            for (int a = 0; a < 4; ++a) cp_async16(wr_slot + (uint32_t)(a * 32 + lane) * 16, cp[a] + off);
-            if (c == 0) {
-#pragma unroll
-                for (int a = 0; a < 4; ++a)
-                    cp_async8(wr_slot + kRingCodeBytes + (uint32_t)(a * 8 + g) * 8, sp[a] + (int64_t)issued * (kWarps * 8));
-            }
-        }
-        cp_async_commit();
-        ++issued;
-        wr_slot = wr_slot + kRingSlot == ring + kRingWarp ? ring : wr_slot + kRingSlot;
-    };
-#pragma unroll
-    for (int d = 0; d < kDepth - 1; ++d) issue();
-    uint32_t rd_slot = ring;
-    for (int idx = 0; idx < my_chunks; ++idx) {
-        issue();
-        cp_async_wait<kDepth - 1>();
-        __syncwarp();
-        uint4 q[4];
+    volatile int* abort = &sh.abort_flag;
+    for (int ch = warp; ch < nch; ch += kWarps) {
+        const uint32_t q = qbase + (uint32_t)ch;
+        const uint32_t slot = q % kSlots;
+        if (!mbar_wait(smem_u32(&sh.full[slot]), (q / kSlots) & 1u, abort)) break;
+        // plain (compiler-schedulable) shared loads: the wait above is a compiler barrier
+        const uint8_t* sp = ring + slot * kSlotBytes;
+        uint4 qw[4];
         uint2 L[4][2];
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            q[a] = lds128(rd_slot + (uint32_t)(a * 32 + lane) * 16);
-            const uint32_t sa = rd_slot + kRingCodeBytes + (uint32_t)(a * 8 + g) * 8 + 2 * c;
-            L[a][0] = lds64(lut_base + lds8(sa) * 8u);
-            L[a][1] = lds64(lut_base + lds8(sa + 1) * 8u);
+            qw[a] = *reinterpret_cast<const uint4*>(sp + srow[a] * 64 + c * 16);
+            const uint8_t* sb = sp + kSlotCodeBytes + srow[a] * 8 + 2 * c;
+            L[a][0] = sh.lut[sb[0]];
+            L[a][1] = sh.lut[sb[1]];
             lut_and &= L[a][0].x & L[a][1].x;
         }
         const uint16_t* bsrc[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) bsrc[nt] = brow[nt] + (int64_t)idx * (kWarps * kChunk);
+        for (int nt = 0; nt < NT; ++nt) bsrc[nt] = brow[nt] + (int64_t)ch * kChunk;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             uint4 B0[NT], B1[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                if (kGateUp) {   // x in T16 order, written by an earlier launch
-                    B0[nt] = ldg_u4(bsrc[nt] + i * 16);
-                    B1[nt] = ldg_u4(bsrc[nt] + i * 16 + 8);
-                } else {         // h, written by the gate_up items of this launch
-                    B0[nt] = ldg_coherent_u4(bsrc[nt] + i * 16);
-                    B1[nt] = ldg_coherent_u4(bsrc[nt] + i * 16 + 8);
+                if (kGateUp) {   // x in T16 order, written by an earlier launch: read-only path
+                    B0[nt] = __ldg(reinterpret_cast<const uint4*>(bsrc[nt] + i * 16));
+                    B1[nt] = __ldg(reinterpret_cast<const uint4*>(bsrc[nt] + i * 16 + 8));
+                } else {         // h, written by gate_up items of this launch: coherent loads
+                    B0[nt] = *reinterpret_cast<const uint4*>(bsrc[nt] + i * 16);
+                    B1[nt] = *reinterpret_cast<const uint4*>(bsrc[nt] + i * 16 + 8);
                 }
             }
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
-                const Masks ma = word_masks(word_of(q[2 * mt], i), k), mb = word_masks(word_of(q[2 * mt + 1], i), k);
+                const Masks ma = word_masks(word_of(qw[2 * mt], i), k), mb = word_masks(word_of(qw[2 * mt + 1], i), k);
                 const uint2 la = L[2 * mt][i >> 1], lb = L[2 * mt + 1][i >> 1];
                 uint32_t alo[4], ahi[4], blo[4], bhi[4];
                 selectors(ma, k, alo, ahi);
@@ -264,9 +221,8 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, ui
             }
         }
         __syncwarp();
-        rd_slot = rd_slot + kRingSlot == ring + kRingWarp ? ring : rd_slot + kRingSlot;
+        if (lane == 0) mbar_arrive(smem_u32(&sh.empty[slot]));
     }
-    cp_async_wait<0>();
 
     // split-K reduction in warp order
 #pragma unroll
@@ -274,18 +230,18 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, ui
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int v = 0; v < 4; ++v) red[warp][mt][nt][lane][v] = acc[mt][nt][v];
-    __syncthreads();
+            for (int v = 0; v < 4; ++v) sh.red[warp][mt][nt][lane][v] = acc[mt][nt][v];
+    consumer_sync();
     // warp w finalises m-tile (w & 1), n-tile (w >> 1)
     const int mt = warp & 1;
     for (int nt = warp >> 1; nt < NT; nt += 2) {
         float v[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int e = 0; e < 4; ++e) {
             float s = 0.f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) s += red[w][mt][nt][lane][q];
-            v[q] = s;
+            for (int w = 0; w < kWarps; ++w) s += sh.red[w][mt][nt][lane][e];
+            v[e] = s;
         }
         if (kGateUp) {
             const int pos = t16_pos(rb * 16 + mt * 8 + g);
@@ -311,110 +267,187 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, ui
             }
         }
     }
-    __syncthreads();
+    consumer_sync();
 }
 
 // One persistent, co-resident grid runs the whole decode layer.  Items come
 // from one queue: indices [0, n_gu) are gate_up items (tile, 16 gate + 16 up
-// rows), [n_gu, n_gu + n_dn) down items (tile, 32 rows of y).  CTA c starts with
-// item c and then takes the next free index from a global counter (taken one
-// item ahead, so the atomic's latency hides behind the current item); a CTA
-// that runs out of gate_up work moves straight on to down work.  A down item of
-// tile t needs h of every row of t, so it waits until the tile's gate_up counter
-// reaches the number of gate_up row blocks.  Every gate_up index is handed out
-// before any down index and all CTAs are resident at once (cooperative launch),
-// so the waits always end; each is still bounded and gives up with the
-// pipeline-timeout status bit.  Which CTA runs an item never changes its result.
+// rows), [n_gu, n_all) down items (tile, 32 rows of y).  CTA c starts with item
+// c; its producer warp then takes the next free index from a global counter.
+// A down item of tile t needs h of every row of t, so the producer waits until
+// the tile's gate_up counter reaches the number of gate_up row blocks before it
+// publishes the item.  Every gate_up index is handed out before any down index
+// and all CTAs are resident at once (cooperative launch), so the waits always
+// end; each is still bounded and gives up with the pipeline-timeout status bit.
+// Which CTA runs an item never changes its result.
 __global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS)
-decode_layer_kernel(DecArgs gu, DecArgs dn, int32_t* __restrict__ gu_done, int32_t* __restrict__ queue)
+decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_constant__ CUtensorMap dn_map,
+                    DecArgs gu, DecArgs dn, int32_t* __restrict__ gu_done, int32_t* __restrict__ queue)
 {
-    __shared__ uint2 lut[256];
-    __shared__ float red[kWarps][2][kMaxNT][32][4];
-    __shared__ int last_flag;
-    __shared__ int abort_flag;
-    __shared__ int next_item;
-    extern __shared__ __align__(16) uint8_t ring_smem[];   // kWarps * kRingWarp bytes
-    const uint32_t ring_base = (uint32_t)__cvta_generic_to_shared(ring_smem);
-    const uint32_t lut_base = (uint32_t)__cvta_generic_to_shared(lut);
-    for (int s = threadIdx.x; s < 256; s += kThreads) {
+    __shared__ SharedState sh;
+    extern __shared__ uint8_t dyn_smem[];   // kRingBytes + 128 (aligned below)
+    // 128-byte aligned ring; offsetting the shared array itself keeps the
+    // pointer in the shared window (plain loads from it compile to shared loads)
+    const uint32_t pad = (128u - (smem_u32(dyn_smem) & 127u)) & 127u;
+    const uint8_t* ring = dyn_smem + pad;
+    const uint32_t ring_addr = smem_u32(dyn_smem) + pad;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int s = tid; s < 256; s += kThreads) {
         ScaleLut l = make_lut((uint32_t)s);
-        lut[s] = make_uint2(l.lut, l.lo);
+        sh.lut[s] = make_uint2(l.lut, l.lo);
     }
-    if (threadIdx.x == 0) abort_flag = 0;
-    const SelConst k = sel_const_regs();
+    if (tid == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(smem_u32(&sh.full[s]), 1 + 32);
+            mbar_init(smem_u32(&sh.empty[s]), 1);
+        }
+        for (int s = 0; s < kInfo; ++s) {
+            mbar_init(smem_u32(&sh.info_full[s]), 1);
+            mbar_init(smem_u32(&sh.info_empty[s]), kWarps);
+        }
+        sh.abort_flag = 0;
+        mbar_fence_init();
+    }
     __syncthreads();
+    volatile int* abort = &sh.abort_flag;
 
     const int n_tiles = *gu.tile_count;
     const int n_gu = n_tiles * gu.row_blocks;
     const int n_all = n_gu + n_tiles * dn.row_blocks;
-    // AND of every lut word used: a valid scale's lut word has bit 31 set, an
-    // invalid one is 0, so the AND is 0 exactly when a bad scale byte was read.
-    uint32_t lut_and = 0xFFFFFFFFu;
 
-    int it = blockIdx.x;
-    while (it < n_all) {
-        // the item after this one (read after the barriers of this item)
-        if (threadIdx.x == 0) next_item = (int)gridDim.x + atomicAdd(queue, 1);
-        if (it < n_gu) {
-            // gate_up: h = SiLU(gate) * up
-            const int ti = it / gu.row_blocks;
-            const int4 tile = gu.tiles[ti];
-            const int rb = it % gu.row_blocks;
-            if (tile.z <= 8) run_item<true, 1>(gu, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
-            else run_item<true, 2>(gu, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
-            // run_item ends with a CTA barrier after its h stores
-            if (threadIdx.x == 0) {
-                __threadfence();
-                atomicAdd(gu_done + ti, 1);
+    if (warp == kWarps) {
+        // ------------------------------------------------ producer warp
+        if (lane == 0) {
+            prefetch_tmap(&gu_map);
+            prefetch_tmap(&dn_map);
+        }
+        uint32_t q = 0;
+        int it = blockIdx.x;
+        for (int n = 0;; ++n) {
+            const uint32_t islot = (uint32_t)n % kInfo;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(smem_u32(&sh.info_empty[islot]), ((uint32_t)(n / kInfo) & 1u) ^ 1u, abort);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            if (it >= n_all) {
+                if (lane == 0) {
+                    sh.info[islot] = make_int4(-1, 0, 0, 0);
+                    mbar_arrive(smem_u32(&sh.info_full[islot]));
+                }
+                break;
             }
-        } else {
-            // down (+ combine): stage slot = w * (W_down h)
-            const int id = it - n_gu;
-            const int ti = id / dn.row_blocks;
-            const int4 tile = dn.tiles[ti];
-            const int rb = id % dn.row_blocks;
-            if (threadIdx.x == 0 && (int)ld_acquire(gu_done + ti) < gu.row_blocks) {
+            const bool is_gu = it < n_gu;
+            const DecArgs& P = is_gu ? gu : dn;
+            const int id = is_gu ? it : it - n_gu;
+            const int ti = id / P.row_blocks, rb = id % P.row_blocks;
+            const int4 tile = P.tiles[ti];
+            if (!is_gu && lane == 0 && (int)ld_acquire(gu_done + ti) < gu.row_blocks) {
                 const long long t0 = clock64();
                 while ((int)ld_acquire(gu_done + ti) < gu.row_blocks) {
                     if (clock64() - t0 > kWaitLimitCycles) {
-                        abort_flag = 1;
+                        *abort = 1;
                         break;
                     }
                     __nanosleep(256);
                 }
             }
-            __syncthreads();
-            if (abort_flag) {
-                if (threadIdx.x == 0) flag_status(dn.status, kDevPipelineTimeout);
-                break;
+            if (__shfl_sync(0xffffffffu, *abort, 0)) break;
+            if (lane == 0) {
+                sh.info[islot] = make_int4(it, tile.x, tile.y, tile.z);
+                mbar_arrive(smem_u32(&sh.info_full[islot]));
             }
-            if (tile.z <= 8) run_item<false, 1>(dn, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
-            else run_item<false, 2>(dn, k, lut_base, red, ring_base, tile.x, tile.y, tile.z, rb, lut_and);
-            // The last of the n_tiles items that wrote rows [32 rb, 32 rb + 32) of
-            // the pair slots sums them into y (fixed j order per token).
-            __threadfence();
-            if (threadIdx.x == 0) last_flag = (atomicAdd(dn.counters + rb, 1) == n_tiles - 1);
-            __syncthreads();
-            if (last_flag) {
-                __threadfence();
-                for (int i = threadIdx.x; i < dn.T * 32; i += kThreads) {
-                    const int t = i >> 5, m = rb * 32 + (i & 31);
-                    float s = 0.f;
-                    for (int j = 0; j < dn.k; ++j) {
-                        const int ej = __ldg(dn.ids + t * dn.k + j);
-                        if ((unsigned)ej < (unsigned)dn.E) s += __ldcg(dn.stage + (int64_t)(t * dn.k + j) * dn.H + m);
+            // the item's rows: TMA rows, and this lane's scale row
+            const int64_t ebase = (int64_t)tile.x * P.rows_per_expert;
+            int64_t srow;
+            if (is_gu) srow = ebase + (lane < 16 ? rb * 16 + lane : P.I + rb * 16 + (lane - 16));
+            else srow = ebase + rb * 32 + lane;
+            const uint8_t* ssrc = P.scales + srow * (P.K / 32);
+            const int nch = P.K / kChunk;
+            for (int ch = 0; ch < nch; ++ch, ++q) {
+                const uint32_t slot = q % kSlots;
+                if (lane == 0) ok = mbar_wait(smem_u32(&sh.empty[slot]), ((q / kSlots) & 1u) ^ 1u, abort);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                const uint32_t fb = smem_u32(&sh.full[slot]);
+                const uint32_t dst = ring_addr + slot * kSlotBytes;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(fb, kSlotCodeBytes);
+                    if (is_gu) {
+                        tma_load_2d(dst, &gu_map, ch * 64, (int)(ebase + rb * 16), fb);
+                        tma_load_2d(dst + 16 * 64, &gu_map, ch * 64, (int)(ebase + P.I + rb * 16), fb);
+                    } else {
+                        tma_load_2d(dst, &dn_map, ch * 64, (int)(ebase + rb * 32), fb);
                     }
-                    __nv_bfloat16 yb = __float2bfloat16_rn(s);
-                    dn.y[(int64_t)t * dn.H + m] = *reinterpret_cast<uint16_t*>(&yb);
                 }
-                if (threadIdx.x == 0) dn.counters[rb] = 0;
+                cp_async8(dst + kSlotCodeBytes + lane * 8, ssrc + ch * 8);
+                cp_async_arrive_noinc(fb);
             }
-            __syncthreads();
+            if (!ok) break;
+            int nxt = 0;
+            if (lane == 0) nxt = (int)gridDim.x + atomicAdd(queue, 1);
+            it = __shfl_sync(0xffffffffu, nxt, 0);
         }
-        it = next_item;
-        __syncthreads();   // everyone has read next_item before thread 0 overwrites it
+        asm volatile("cp.async.wait_all;" ::: "memory");   // no copy of this warp outlives the CTA
+    } else {
+        // ------------------------------------------------ consumer warps
+        const SelConst k = sel_const_regs();
+        // AND of every lut word used: a valid scale's lut word has bit 31 set, an
+        // invalid one is 0, so the AND is 0 exactly when a bad scale byte was read.
+        uint32_t lut_and = 0xFFFFFFFFu;
+        uint32_t qbase = 0;
+        for (int n = 0;; ++n) {
+            // one thread waits for the next item and decides whether to stop; the
+            // barrier hands both to every consumer warp, so all four always take
+            // the same path and meet at the same barriers
+            const uint32_t islot = (uint32_t)n % kInfo;
+            if (tid == 0) {
+                const bool ok = mbar_wait(smem_u32(&sh.info_full[islot]), (uint32_t)(n / kInfo) & 1u, abort);
+                sh.cur_info = ok ? sh.info[islot] : make_int4(-1, 0, 0, 0);
+                sh.stop = !ok || *abort;
+            }
+            consumer_sync();
+            const int4 info = sh.cur_info;
+            if (sh.stop || info.x < 0) break;
+            if (info.x < n_gu) {
+                const int rb = info.x % gu.row_blocks;
+                if (info.w <= 8) run_item<true, 1>(gu, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
+                else run_item<true, 2>(gu, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
+                qbase += (uint32_t)(gu.K / kChunk);
+                // run_item ends with a consumer barrier after its h stores
+                if (tid == 0) {
+                    __threadfence();
+                    atomicAdd(gu_done + info.x / gu.row_blocks, 1);
+                }
+            } else {
+                const int rb = (info.x - n_gu) % dn.row_blocks;
+                if (info.w <= 8) run_item<false, 1>(dn, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
+                else run_item<false, 2>(dn, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
+                qbase += (uint32_t)(dn.K / kChunk);
+                // The last of the n_tiles items that wrote rows [32 rb, 32 rb + 32) of
+                // the pair slots sums them into y (fixed j order per token).
+                __threadfence();
+                if (tid == 0) sh.last_flag = (atomicAdd(dn.counters + rb, 1) == n_tiles - 1);
+                consumer_sync();
+                if (sh.last_flag) {
+                    __threadfence();
+                    for (int i = tid; i < dn.T * 32; i += kWarps * 32) {
+                        const int t = i >> 5, m = rb * 32 + (i & 31);
+                        float s = 0.f;
+                        for (int j = 0; j < dn.k; ++j) {
+                            const int ej = __ldg(dn.ids + t * dn.k + j);
+                            if ((unsigned)ej < (unsigned)dn.E) s += __ldcg(dn.stage + (int64_t)(t * dn.k + j) * dn.H + m);
+                        }
+                        __nv_bfloat16 yb = __float2bfloat16_rn(s);
+                        dn.y[(int64_t)t * dn.H + m] = *reinterpret_cast<uint16_t*>(&yb);
+                    }
+                    if (tid == 0) dn.counters[rb] = 0;
+                }
+                consumer_sync();
+            }
+            if (lane == 0) mbar_arrive(smem_u32(&sh.info_empty[islot]));
+        }
+        if (lut_and == 0) flag_status(gu.status, MOE_W2_DEV_BAD_SCALE);
     }
-    if (lut_and == 0) flag_status(gu.status, MOE_W2_DEV_BAD_SCALE);
+    if (tid == 0 && *abort) flag_status(gu.status, kDevPipelineTimeout);
 }
 
 }  // namespace
@@ -426,7 +459,7 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     (void)x;
     const int32_t E = w.num_experts, H = w.hidden, I = w.inter;
     const int64_t P = (int64_t)T * k;
-    constexpr int kDyn = kWarps * kRingWarp;
+    constexpr int kDyn = kRingBytes + 128;
     static int occ = 0;
     if (occ == 0) {
         cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
@@ -470,14 +503,20 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     int32_t* gu_done = ws.counters + H / 32;   // [tiles], zeroed by the permutation kernel
     int32_t* queue = gu_done + tiles;          // item queue, zeroed by the permutation kernel
 
+    // code tiles: 64 bytes (256 codes) x 16 rows (gate_up: gate and up halves
+    // separately) or x 32 rows (down)
+    CUtensorMap gu_map, dn_map;
+    cudaError_t e = make_tmap_2d(&gu_map, w.w13_codes, false, (int64_t)E * 2 * I, H / 4, 64, 16, 0);
+    if (e != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&dn_map, w.w2_codes, false, (int64_t)E * H, I / 4, 64, 32, 0)) != cudaSuccess) return e;
+
     // every CTA resident at once: at most occupancy x SMs, and no more than the
     // larger phase has items
     const int64_t grid = std::min<int64_t>((int64_t)sm_count() * occ,
                                            tiles * std::max<int64_t>(gp.row_blocks, dp.row_blocks));
-    cudaError_t e = ev.record(1, s);
-    if (e != cudaSuccess) return e;
+    if ((e = ev.record(1, s)) != cudaSuccess) return e;
     if ((e = ev.record(2, s)) != cudaSuccess) return e;   // one kernel: phases 1 and 2 coincide
-    void* args[] = {&gp, &dp, &gu_done, &queue};
+    void* args[] = {&gu_map, &dn_map, &gp, &dp, &gu_done, &queue};
     e = cudaLaunchCooperativeKernel((const void*)decode_layer_kernel, dim3((unsigned)grid), dim3(kThreads), args,
                                     (size_t)kDyn, s);
     return e;

@@ -423,9 +423,13 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 else run_item<false, 2>(dn, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
                 qbase += (uint32_t)(dn.K / kChunk);
                 // The last of the n_tiles items that wrote rows [32 rb, 32 rb + 32) of
-                // the pair slots sums them into y (fixed j order per token).
-                __threadfence();
-                if (tid == 0) sh.last_flag = (atomicAdd(dn.counters + rb, 1) == n_tiles - 1);
+                // the pair slots sums them into y (fixed j order per token).  run_item
+                // ended with a consumer barrier after the stage stores, so one fence by
+                // the counting thread releases all of them (fences are cumulative).
+                if (tid == 0) {
+                    __threadfence();
+                    sh.last_flag = (atomicAdd(dn.counters + rb, 1) == n_tiles - 1);
+                }
                 consumer_sync();
                 if (sh.last_flag) {
                     __threadfence();

@@ -483,7 +483,30 @@ def requant_bench(args, world, rank, local):
            "roofline": {"kernel": "requant_kernel", "bound": "hbm", "achieved": round(gbs, 1),
                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                         "peak_source": pk["source"], "traffic": ncu_traffic("requant_kernel", "requant_256")},
-           "clocks": clk.summary(), "gpu_launches": 2 * args.steps}
+           "clocks": clk.summary(), "gpu_launches": 2 * args.steps, "dtype": "int64 (exact)"}
+
+    # end to end: the NVFP4 tensors from pinned host memory, requant, planes back to pinned host memory
+    hin = [torch.from_numpy(a).pin_memory() for a in (gu.e2m1, gu.e4m3, gu.scale_2, dn.e2m1, dn.e4m3, dn.scale_2)]
+    hout = [torch.empty(t.shape, dtype=torch.uint8).pin_memory() for t in (cgu, sgu, cdn, sdn)]
+    e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in e_evs:
+            flush.zero_()
+            e0.record(stream)
+            for d, h in zip(dgu + ddn, hin):
+                d.copy_(h, non_blocking=True)
+            moe_w2.requant(*dgu, codes=cgu, ue8m0=sgu, status=status, stream=stream)
+            moe_w2.requant(*ddn, codes=cdn, ue8m0=sdn, status=status, stream=stream)
+            for h, d in zip(hout, (cgu, sgu, cdn, sdn)):
+                h.copy_(d, non_blocking=True)
+            e1.record(stream)
+    stream.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e_evs), world)
+    res["e2e"] = {"value": round(world * elems * args.steps / (e2e_ms / 1e3), 2), "unit": "elements/s",
+                  "h2d_bytes_per_step": int(sum(h.nbytes for h in hin)),
+                  "d2h_bytes_per_step": int(sum(h.nbytes for h in hout))}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during the requant benchmark")
     return res, gu
 
 
@@ -525,7 +548,7 @@ def main():
         return
     line = {"metric": METRIC, "value": round(res.pop("value"), 3), "unit": metric_unit, "n_gpus": world,
             "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(res.pop("ms_per_step"), 6),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": res.pop("dtype", "bf16"),
             "data": "synthetic (seeded; shapes of the pages' models)",
             "config": {"workload": workload, "l2": "flushed before every step (512 MiB write, untimed)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}}

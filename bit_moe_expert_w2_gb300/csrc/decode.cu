@@ -270,16 +270,16 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, Sh
     consumer_sync();
 }
 
-// One persistent, co-resident grid runs the whole decode layer.  Items come
-// from one queue: indices [0, n_gu) are gate_up items (tile, 16 gate + 16 up
-// rows), [n_gu, n_all) down items (tile, 32 rows of y).  CTA c starts with item
-// c; its producer warp then takes the next free index from a global counter.
-// A down item of tile t needs h of every row of t, so the producer waits until
-// the tile's gate_up counter reaches the number of gate_up row blocks before it
-// publishes the item.  Every gate_up index is handed out before any down index
-// and all CTAs are resident at once (cooperative launch), so the waits always
-// end; each is still bounded and gives up with the pipeline-timeout status bit.
-// Which CTA runs an item never changes its result.
+// One persistent grid runs the whole decode layer.  Items come from one queue:
+// indices [0, n_gu) are gate_up items (tile, 16 gate + 16 up rows), [n_gu, n_all)
+// down items (tile, 32 rows of y).  Each CTA's producer warp takes every item,
+// the first included, from a global counter, so only CTAs that are running hold
+// items.  A down item of tile t needs h of every row of t, so the producer waits
+// until the tile's gate_up counter reaches the number of gate_up row blocks
+// before it publishes the item; every gate_up index is handed out before any
+// down index and is held by a running CTA, so the waits always end (each is
+// still bounded and gives up with the pipeline-timeout status bit).  Which CTA
+// runs an item never changes its result.
 __global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS)
 decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_constant__ CUtensorMap dn_map,
                     DecArgs gu, DecArgs dn, int32_t* __restrict__ gu_done, int32_t* __restrict__ queue)
@@ -311,6 +311,10 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
     __syncthreads();
     volatile int* abort = &sh.abort_flag;
 
+    // Launched as a programmatic dependent of the permutation kernel: the setup
+    // above overlaps it; everything it writes (tiles, counters, x in T16 order)
+    // is read only after this wait.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n_tiles = *gu.tile_count;
     const int n_gu = n_tiles * gu.row_blocks;
     const int n_all = n_gu + n_tiles * dn.row_blocks;
@@ -322,7 +326,9 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
             prefetch_tmap(&dn_map);
         }
         uint32_t q = 0;
-        int it = blockIdx.x;
+        int it = 0;
+        if (lane == 0) it = atomicAdd(queue, 1);
+        it = __shfl_sync(0xffffffffu, it, 0);
         for (int n = 0;; ++n) {
             const uint32_t islot = (uint32_t)n % kInfo;
             int ok = 1;
@@ -383,7 +389,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
             }
             if (!ok) break;
             int nxt = 0;
-            if (lane == 0) nxt = (int)gridDim.x + atomicAdd(queue, 1);
+            if (lane == 0) nxt = atomicAdd(queue, 1);
             it = __shfl_sync(0xffffffffu, nxt, 0);
         }
         asm volatile("cp.async.wait_all;" ::: "memory");   // no copy of this warp outlives the CTA
@@ -514,16 +520,23 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     if (e != cudaSuccess) return e;
     if ((e = make_tmap_2d(&dn_map, w.w2_codes, false, (int64_t)E * H, I / 4, 64, 32, 0)) != cudaSuccess) return e;
 
-    // every CTA resident at once: at most occupancy x SMs, and no more than the
-    // larger phase has items
+    // at most occupancy x SMs (all resident at once when the GPU is otherwise
+    // idle), and no more than the larger phase has items
     const int64_t grid = std::min<int64_t>((int64_t)sm_count() * occ,
                                            tiles * std::max<int64_t>(gp.row_blocks, dp.row_blocks));
     if ((e = ev.record(1, s)) != cudaSuccess) return e;
     if ((e = ev.record(2, s)) != cudaSuccess) return e;   // one kernel: phases 1 and 2 coincide
-    void* args[] = {&gu_map, &dn_map, &gp, &dp, &gu_done, &queue};
-    e = cudaLaunchCooperativeKernel((const void*)decode_layer_kernel, dim3((unsigned)grid), dim3(kThreads), args,
-                                    (size_t)kDyn, s);
-    return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)kDyn;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // may start before the permutation ends
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_layer_kernel, gu_map, dn_map, gp, dp, gu_done, queue);
 }
 
 }  // namespace moe_w2

@@ -97,6 +97,9 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
     int32_t* __restrict__ counters, int32_t n_counters, uint16_t* __restrict__ y, int64_t y_elems,
     uint32_t* status)
 {
+    // the decode layer kernel may launch now; it waits for this grid to finish
+    // before it reads anything written here
+    asm volatile("griddepcontrol.launch_dependents;");
     if (blockIdx.x > 0) {
         // extra CTAs: x in T16 order (decode reads activation rows per pair from it)
         const int64_t stride = (int64_t)(gridDim.x - 1) * blockDim.x;

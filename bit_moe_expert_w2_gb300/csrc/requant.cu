@@ -23,8 +23,9 @@
 //
 // All elements of a half-block share Q_h and f_h, so an element's threshold
 // depends only on its e2m1 magnitude class (7 nonzero classes per half): the
-// kernel counts classes once (SWAR over nibbles) and evaluates each candidate
-// over the 14 classes instead of the 32 elements.
+// kernel counts classes once (SWAR over nibbles), computes each class's
+// threshold exponent tau (the largest u at which it is at magnitude 4) once, and
+// evaluates each candidate from 14 integer comparisons against tau.
 #include <algorithm>
 
 #include "common.cuh"
@@ -146,36 +147,98 @@ __global__ void __launch_bounds__(256) requant_kernel(const uint8_t* __restrict_
                 nmin = min(nmin, (uint64_t)n1_of_class(vmin) * Qs[h]);
             }
             const int m = floor_log2_u64(nmax) + c, mlo = floor_log2_u64(nmin) + c;
+            // Threshold of each class: the largest u at which it is at magnitude 4.
+            // |x| > 2.5 * 2^u  <=>  N > 5 * 2^(u-c-1); with L = floor(log2 N) the largest
+            // k with 5 * 2^k < N is L-2 when 4N > 5 * 2^L, else L-3; tau = k + c + 1.
+            int tau[2][8];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int v = 1; v < 8; ++v) {
+                    const uint64_t N = (uint64_t)n1_of_class(v) * Qs[h];
+                    if (!any[h] || N == 0) {
+                        tau[h][v] = -100000;
+                        continue;
+                    }
+                    const int L = floor_log2_u64(N);
+                    tau[h][v] = ((N << 2) > (5ull << L) ? L - 2 : L - 3) + c + 1;
+                }
             int hi = min(125, max(-126, m + 1));
             int lo = min(hi, max(-126, mlo - 5));
+            {
+                // Dominated low candidates.  While u <= tau_min every nonzero element
+                // is at magnitude 4, so SSE(u) = f(2^u) with f(e) = sum (a_i - 4e)^2 +
+                // n0 e^2, minimal at e* = 4 sum a / (16 n + n0); f(2e) < f(e) exactly
+                // when e < 2 e* / 3, and SSE(u+1) <= f(2^(u+1)) (nearest codes never do
+                // worse than magnitude 4).  Hence every u <= tau_min with
+                // 3 (16 n + n0) 2^u < 8 sum a is strictly worse than u+1 and the search
+                // can start at min(tau_min + 1, smallest u without that property).
+                int n_nz = 0, tau_min = 1 << 20, tau_max = -(1 << 20);
+                uint64_t S_nz = 0;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int v = 1; v < 8; ++v)
+                        if (any[h] && cntv[h][v]) {
+                            n_nz += cntv[h][v];
+                            S_nz += (uint64_t)cntv[h][v] * ((uint64_t)n1_of_class(v) * Qs[h]);
+                            tau_min = min(tau_min, tau[h][v]);
+                            tau_max = max(tau_max, tau[h][v]);
+                        }
+                // smallest e with D 2^e >= Num (|x| = N 2^c, so sum a = S_nz 2^c, u = e + c)
+                const uint64_t D = 3ull * (uint64_t)(16 * n_nz + (32 - n_nz));
+                const uint64_t Num = 8ull * S_nz;
+                int e = floor_log2_u64(Num) - floor_log2_u64(D) - 1;
+                auto reaches = [&](int ee) {
+                    return ee >= 0 ? ((unsigned __int128)D << ee) >= (unsigned __int128)Num
+                                   : (unsigned __int128)D >= ((unsigned __int128)Num << (-ee));
+                };
+                while (!reaches(e)) ++e;
+                const int lo_new = min(tau_min + 1, e + c);
+                lo = min(hi, max(lo, lo_new));
+                // Dominated high candidates.  Above tau_max every element is at
+                // magnitude 1, SSE(u) = g(2^u) with g(e) = sum over all 32 of (a_i - e)^2;
+                // g(e/2) < g(e) exactly when 24 e > sum a, and SSE(u-1) <= g(2^(u-1)).
+                // Hence every u > tau_max with 24 2^u > sum a is strictly worse than u-1:
+                // the search can stop at max(tau_max, largest u with 24 2^u <= sum a).
+                int f = floor_log2_u64(S_nz) - 4;   // largest f with 24 2^f <= S_nz (f >= L-5)
+                auto fits = [&](int ff) {
+                    return ff >= 0 ? ((unsigned __int128)24 << ff) <= (unsigned __int128)S_nz
+                                   : (unsigned __int128)24 <= ((unsigned __int128)S_nz << (-ff));
+                };
+                while (!fits(f)) --f;
+                while (fits(f + 1)) ++f;
+                hi = max(lo, min(hi, max(tau_max, f + c)));
+            }
             if (lo == hi) {
                 u = lo;
             } else {
                 const int eref = min(c, lo);
-                const int C1 = c - eref + 1;   // |x| > 2.5*2^u  <=>  N << C1 > 5 << (u - eref)
+                const int C1 = c - eref + 1;
                 uint64_t S_all = 0;
-                uint64_t Nc[2][8];
+                uint64_t cN[2][8];   // count * N of each class
+                int cc[2][8];        // count of each class
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int v = 1; v < 8; ++v) {
-                        Nc[h][v] = (uint64_t)n1_of_class(v) * Qs[h];
-                        S_all += (uint64_t)cntv[h][v] * Nc[h][v];
+                        cc[h][v] = any[h] ? cntv[h][v] : 0;
+                        cN[h][v] = (uint64_t)cc[h][v] * ((uint64_t)n1_of_class(v) * Qs[h]);
+                        S_all += cN[h][v];
                     }
                 __int128 best = 0;
                 int best_u = lo;
                 for (int cand = lo; cand <= hi; ++cand) {
                     const int U = cand - eref;
-                    const uint64_t R = 5ull << U;
                     int A = 0;
                     uint64_t S4 = 0;
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
                         for (int v = 1; v < 8; ++v)
-                            if ((Nc[h][v] << C1) > R) {
-                                A += cntv[h][v];
-                                S4 += (uint64_t)cntv[h][v] * Nc[h][v];
+                            if (tau[h][v] >= cand) {
+                                A += cc[h][v];
+                                S4 += cN[h][v];
                             }
                     const __int128 t1 = (__int128)(32 + 15 * A) << (2 * U);
                     const __int128 t2 = (__int128)(S_all + 3 * S4) << (U + C1);
@@ -187,20 +250,15 @@ __global__ void __launch_bounds__(256) requant_kernel(const uint8_t* __restrict_
                 }
                 u = best_u;
             }
-            // magnitude-4 classes at the chosen u
-            if (u - min(c, u) <= 60) {
-                const int eref = min(c, u);
-                const int C1 = c - eref + 1;
-                const uint64_t R = 5ull << (u - eref);
+            // magnitude-4 classes at the chosen u: the smallest class whose threshold reaches u
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (!any[h]) continue;
-                    int vv = 8;
+            for (int h = 0; h < 2; ++h) {
+                if (!any[h]) continue;
+                int vv = 8;
 #pragma unroll
-                    for (int v = 7; v >= 1; --v)
-                        if ((((uint64_t)n1_of_class(v) * Qs[h]) << C1) > R) vv = v;
-                    v0[h] = vv;
-                }
+                for (int v = 7; v >= 1; --v)
+                    if (tau[h][v] >= u) vv = v;
+                v0[h] = vv;
             }
         }
 

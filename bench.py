@@ -358,14 +358,16 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
     plane_bytes = sum(distinct[i] * (w13_b + w2_b) for i, _ in per_step)
     res = {"ms_per_step": steps_ms / K, "ms_per_step_traced": traced_ms / K}
     if decode:
-        # one kernel (decode_layer_kernel) streams the w13 and w2 planes of every
-        # active expert; its time is phases 1 + 2 (phase 1 is empty on this path)
-        layer_kernel_ms = phase_ms[1] + phase_ms[2]
+        # one kernel streams the w13 and w2 planes of every active expert; its
+        # time is phase 1 (phase 2: the combine kernel, empty when the layer
+        # kernel combines itself)
+        kname = moe_w2.decode_kernel(T, k)
+        layer_kernel_ms = phase_ms[1]
         achieved = plane_bytes / (layer_kernel_ms / 1e3) / 1e9
-        res["roofline"] = {"kernel": "decode_layer_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+        res["roofline"] = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
                            "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                            "peak_source": pk["source"],
-                           "traffic": ncu_traffic("decode_layer_kernel", cfg.name)}
+                           "traffic": ncu_traffic(kname, cfg.name)}
         res["plane_gbs_step"] = round(plane_bytes / (steps_ms / 1e3) / 1e9, 1)
         res["plane_frac_step"] = round(plane_bytes / (steps_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)
     else:
@@ -377,17 +379,17 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
                            "traffic": ncu_traffic("prefill_gate_up_kernel", cfg.name)}
         res["layer_tflops"] = round(6.0 * T * k * H * I * K / (steps_ms / 1e3) / 1e12, 1)
     if decode:
-        res["phase_ms_per_step"] = {"permute": round(phase_ms[0] / K, 5),
-                                    "layer": round((phase_ms[1] + phase_ms[2]) / K, 5)}
+        res["phase_ms_per_step"] = {"permute": round(phase_ms[0] / K, 5), "layer": round(phase_ms[1] / K, 5),
+                                    "combine": round(phase_ms[2] / K, 5)}
     else:
         res["phase_ms_per_step"] = {"permute_gather": round(phase_ms[0] / K, 5), "gate_up": round(phase_ms[1] / K, 5),
                                     "down_combine": round(phase_ms[2] / K, 5)}
     res["distinct_experts_per_step"] = round(float(np.mean([distinct[i] for i, _ in per_step])), 2)
     res["clocks"] = clk.summary()
     res["wall_s"] = round(wall, 3)
-    # decode: permute (+ x transpose), the layer kernel (gate_up, down, combine);
+    # decode: permute (+ x as e4m3 rows), the layer kernel (gate_up, down), combine;
     # prefill: permute, gather, gate_up, down, combine
-    res["kernels_per_step"] = 2 if decode else 5
+    res["kernels_per_step"] = (2 if moe_w2.decode_kernel(T, k) == "decode_mma_kernel" else 3) if decode else 5
 
     # end to end: pinned host inputs -> device -> forward -> y back to pinned host
     hx = [torch.from_numpy(b[0].view(np.int16)).pin_memory() for b in batches]

@@ -12,7 +12,14 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int32_t kPrefillTileRows = 256;   // pairs per prefill tile (tcgen05 N <= 256)
-constexpr int32_t kDecodeTileRows = 16;     // pairs per decode tile
+constexpr int32_t kDecodeTileRows = 8;      // pairs per decode tile (MMA N = 16: hi and lo row per pair)
+constexpr int32_t kDecodeMmaTileRows = 16;  // pairs per tile of the mma.sync decode kernel
+constexpr int64_t kDecodeMmaMaxPairs = 32;  // steps with at most this many pairs take the mma.sync kernel
+constexpr int64_t kDecodeTargetItems = 1200; // down items per step that keep every CTA busy
+constexpr int64_t kDecodeMinRange = 4;       // gate_up range: chunks at least
+constexpr int64_t kDecodeMaxRanges = 1024;   // gate_up ranges at most, for a step with ceil(P/8) tiles
+constexpr int32_t kDecodeMinSegChunks = 4;   // at least 4 chunks of 128 K per decode item
+constexpr int64_t kDecodeMaxSegments = 16;   // K segments per row block
 
 int g_sm_count[kMaxDevices];
 int g_cc_ok[kMaxDevices];   // 0 = unknown, 1 = ok, 2 = not sm_103
@@ -60,6 +67,44 @@ int64_t max_tiles(int64_t P, int32_t E, bool decode)
     return P / (decode ? kDecodeTileRows : kPrefillTileRows) + E + 1;
 }
 
+DecodeSplit decode_split(int64_t P, int32_t E, int32_t H, int32_t I)
+{
+    DecodeSplit d{};
+    // gate_up: the chunks of all (tile, 64-row block) units are cut into at most
+    // kDecodeMaxRanges ranges of at least kDecodeMinRange chunks (the device
+    // picks the count from the tile count).  A unit of nch chunks then meets at
+    // most ceil(nch / len) + 1 ranges, len the shortest range, which is at
+    // least the minimum and at least (chunks of ceil(P / 8) tiles) / max ranges.
+    const int64_t nch_gu = H / 128, rbg = I / 64;
+    const int64_t tiles_min = std::max<int64_t>(1, (P + 7) / 8);
+    const int64_t len = std::max<int64_t>(kDecodeMinRange, tiles_min * rbg * nch_gu / kDecodeMaxRanges);
+    d.gu_min_range = (int32_t)len;
+    d.s_gu = (int32_t)std::min<int64_t>(nch_gu, (nch_gu + len - 1) / len + 1);
+    // down: each 128-row block's K in s_dn equal segments, as many as keep a
+    // small step's down phase in several short items per CTA
+    const int64_t tiles = std::max<int64_t>(1, std::min<int64_t>(P, E));
+    const int32_t nch_dn = I / 128;
+    const int64_t rbd = H / 128;
+    int64_t want = (kDecodeTargetItems + tiles * rbd - 1) / (tiles * rbd);
+    want = std::min<int64_t>(want, std::max<int64_t>(1, 64 / std::max<int64_t>(1, P)));
+    want = std::max<int64_t>(1, std::min<int64_t>({want, (int64_t)std::max(1, nch_dn / kDecodeMinSegChunks),
+                                                    (int64_t)kDecodeMaxSegments}));
+    d.l_dn = (int32_t)((nch_dn + want - 1) / want);
+    d.l_dn = (d.l_dn + 3) & ~3;   // segments start on a scale-word group (4 chunks = 16 scale bytes per row)
+    d.s_dn = (nch_dn + d.l_dn - 1) / d.l_dn;
+    d.g_gu = d.g_dn = 2;
+    return d;
+}
+
+bool decode_use_mma(int64_t P) { return P <= kDecodeMmaMaxPairs; }
+
+int64_t decode_counter_count(int64_t P, int32_t E, int32_t H, int32_t I)
+{
+    if (decode_use_mma(P)) return H / 32 + max_tiles(P, E, true) + 1;   // row blocks of y, tiles, queue
+    const int64_t mt = max_tiles(P, E, true);
+    return mt * (I / 64) + 1;
+}
+
 Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I)
 {
     Workspace w{};
@@ -79,10 +124,25 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
     w.active_count = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * 2));
     w.tile_count = w.active_count + 1;
     w.tiles = reinterpret_cast<int4*>(take(sizeof(int4) * max_tiles(P, E, decode)));
-    w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (H / 32 + max_tiles(P, E, decode) + 1)));
-    w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * (decode ? (int64_t)T : P) * H));
-    w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
-    w.stage = reinterpret_cast<float*>(take(sizeof(float) * P * H));
+    if (decode && decode_use_mma(P)) {
+        w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * decode_counter_count(P, E, H, I)));
+        w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * T * H));
+        w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
+        w.stage = reinterpret_cast<float*>(take(sizeof(float) * P * H));
+    } else if (decode) {
+        w.split = decode_split(P, E, H, I);
+        w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * decode_counter_count(P, E, H, I)));
+        w.x8 = reinterpret_cast<uint8_t*>(take((size_t)2 * T * H));
+        w.sx8 = reinterpret_cast<uint8_t*>(take((size_t)2 * T * (H / 32)));
+        w.h8 = reinterpret_cast<uint8_t*>(take((size_t)2 * P * I));
+        w.sh8 = reinterpret_cast<uint8_t*>(take((size_t)2 * P * (I / 32)));
+        w.gu_part = reinterpret_cast<float*>(take(sizeof(float) * w.split.s_gu * P * 2 * I));
+        w.stage = reinterpret_cast<float*>(take(sizeof(float) * w.split.s_dn * P * H));
+    } else {
+        w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * H));
+        w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
+        w.stage = reinterpret_cast<float*>(take(sizeof(float) * P * H));
+    }
     w.bytes = off;
     return w;
 }
@@ -126,7 +186,8 @@ moe_w2_status moe_w2_permute(const int32_t* topk_ids, int32_t T, int32_t top_k, 
     if (st != MOE_W2_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_permute(topk_ids, T, top_k, E, sorted_pairs, inv_pairs, expert_offsets, nullptr, nullptr,
-                                   nullptr, nullptr, 1, nullptr, nullptr, 0, nullptr, 0, nullptr, dev_status, s);
+                                   nullptr, nullptr, 1, nullptr, nullptr, nullptr, nullptr, 0, nullptr, 0, nullptr,
+                                   dev_status, s);
     return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
 }
 
@@ -161,13 +222,19 @@ moe_w2_status moe_w2_forward_traced(const void* x_bf16, const int32_t* topk_ids,
     PhaseEvents ev{};
     for (int i = 0; i < 4; ++i) ev.e[i] = phase_events ? static_cast<cudaEvent_t>(phase_events[i]) : nullptr;
     if (ev.record(0, s) != cudaSuccess) return MOE_W2_ERR_CUDA;
+    const int64_t P = (int64_t)T * top_k;
+    const bool mma = decode && decode_use_mma(P);
     cudaError_t e = launch_permute(topk_ids, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active, ws.active_count,
-                                   ws.tiles, ws.tile_count, decode ? kDecodeTileRows : kPrefillTileRows,
-                                   decode ? x : nullptr, decode ? ws.xa : nullptr, H, ws.counters,
-                                   decode ? (int32_t)(H / 32 + max_tiles((int64_t)T * top_k, E, true) + 1) : 0,
-                                   decode ? y : nullptr, dev_status, s);
+                                   ws.tiles, ws.tile_count,
+                                   !decode ? kPrefillTileRows : mma ? kDecodeMmaTileRows : kDecodeTileRows,
+                                   decode ? x : nullptr, mma ? ws.xa : nullptr, decode && !mma ? ws.x8 : nullptr,
+                                   decode && !mma ? ws.sx8 : nullptr, H, ws.counters,
+                                   decode ? (int32_t)decode_counter_count(P, E, H, I) : 0, decode ? y : nullptr,
+                                   dev_status, s);
     if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
-    if (decode)
+    if (mma)
+        e = launch_decode_mma(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
+    else if (decode)
         e = launch_decode(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
     else
         e = launch_prefill(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);

@@ -3,6 +3,8 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "moe_w2.h"
@@ -19,6 +21,34 @@ namespace moe_w2 {
 // mma.sync B fragment is one 64-bit load and a UMMA smem row is written in
 // storage order.
 __host__ __device__ __forceinline__ int t16_pos(int n) { return (n & ~15) | ((n & 3) << 2) | ((n >> 2) & 3); }
+
+// Decode activation operands (x for gate_up, h for down) enter the block-scaled
+// e4m3 MMA as two e4m3 rows per activation row, hi = e4m3(v) and
+// lo = e4m3(v - hi) with v = a / 2^(s-127), one UE8M0 byte s per 32 elements
+// (2^(s-127) = 2^(floor(log2 amax) - 7), so |v| < 256).  hi + lo equals v exactly
+// whenever |a| >= amax * 2^-9 (8 significant bits, as in bf16), and within
+// amax * 2^-17 otherwise.  Inside every group of 16 elements, stored byte p holds
+// element e4_elem(p): the code expansion emits per 16-code word the codes
+// 0,2,4,6 | 8,10,12,14 | 1,3,5,7 | 9,11,13,15, and B must follow the same K order.
+__host__ __device__ __forceinline__ int e4_elem(int p) { return ((p & 3) << 1) | (((p >> 2) & 1) << 3) | (p >> 3); }
+__host__ __device__ __forceinline__ int e4_pos(int e) { return ((e & 1) << 3) | (((e >> 3) & 1) << 2) | ((e >> 1) & 3); }
+
+// UE8M0 byte of a 32-element activation block with maximum magnitude amax.
+__device__ __forceinline__ uint32_t act_scale_byte(float amax)
+{
+    if (!(amax > 0.f)) return 127u;   // all zeros (or not a number: the values carry it)
+    const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+    return (uint32_t)min(254, max(1, ex - 7));
+}
+// 2^(127 - s): the factor that takes the block's values to the e4m3 range.
+__device__ __forceinline__ float act_inv_scale(uint32_t s) { return __uint_as_float((254u - s) << 23); }
+// hi = e4m3(v) and lo = e4m3(v - hi), both rounded to nearest even.
+__device__ __forceinline__ void act_split(float v, uint32_t& hi, uint32_t& lo)
+{
+    hi = __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)hi, __NV_E4M3);
+    lo = __nv_cvt_float_to_fp8(v - __half2float(__half(hr)), __NV_SATFINITE, __NV_E4M3);
+}
 
 // ------------------------------------------------------------------ status
 __device__ __forceinline__ void flag_status(uint32_t* st, uint32_t bits)
@@ -187,6 +217,22 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // ------------------------------------------------------------------ workspace
+// Decode split of K: a decode work item is (tile of <= 8 pairs of one expert,
+// 128 weight rows, a range of K chunks of 128).  gate_up K is cut into equal
+// ranges of the whole phase (one per CTA of a full GPU), down K into equal
+// segments per row block; both chosen so that a one-token step keeps every CTA
+// busy.
+struct DecodeSplit {
+    int32_t s_gu;         // gate_up: contributing items per 64-row block at most (K = H in ranges)
+    int32_t gu_min_range; // gate_up: chunks per range at least (the kernel makes no shorter ranges)
+    int32_t s_dn, l_dn;   // down: segments, chunks per segment (K = I; l a multiple of 4)
+    int32_t g_gu, g_dn;   // chunks per scale-word group (4: 16-byte copies, 2: 8-byte), set at launch
+};
+DecodeSplit decode_split(int64_t P, int32_t E, int32_t H, int32_t I);
+// Steps with at most this many pairs take the bf16 mma.sync decode kernel
+// (decode_mma.cu); larger decode steps the block-scaled e4m3 kernel (decode.cu).
+bool decode_use_mma(int64_t P);
+
 struct Workspace {
     int32_t* sorted;       // [P]
     int32_t* inv;          // [P]
@@ -195,17 +241,27 @@ struct Workspace {
     int32_t* active_count; // [1]
     int4* tiles;           // GEMM tiles (expert, first slot, pairs, 0)
     int32_t* tile_count;   // [1]
-    uint16_t* xa;          // prefill: activation rows in expert order [P][H]; decode: x per token [T][H]; T16 layout
-    int32_t* counters;     // decode: per 32-row block of y, CTAs done (last one runs the combine),
-                           // then per tile, gate_up row blocks done (down items wait for their tile),
-                           // then the decode item queue
+    int32_t* counters;     // decode, zeroed by the permutation kernel: per (tile, 64-row block of h) K
+                           // segments done, plus one once h of the block is written [max_tiles][I/64];
+                           // the item queue [1]
+    // prefill, and the mma.sync decode kernel
+    uint16_t* xa;          // activation rows, T16 layout: prefill in expert order [P][H], decode per token [T][H]
     uint16_t* h;           // SiLU(gate)*up rows in expert order, T16 layout [P][I]
-    float* stage;          // per-pair outputs times router weight, slot t*k+j [P][H]
+    float* stage;          // per-pair outputs times router weight, slot t*k+j: prefill [P][H],
+                           // decode [s_dn][P][H] (one slab per K segment of down)
+    // decode
+    uint8_t* x8;           // e4m3 activation rows of x, 2 per token [2T][H]
+    uint8_t* sx8;          // their UE8M0 bytes [2T][H/32]
+    uint8_t* h8;           // e4m3 activation rows of h, 2 per pair (expert order) [2P][I]
+    uint8_t* sh8;          // their UE8M0 bytes [2P][I/32]
+    float* gu_part;        // gate_up partial sums per K segment [s_gu][P][2I]
+    DecodeSplit split;
     size_t bytes;
 };
 
 Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I);
 int64_t max_tiles(int64_t P, int32_t E, bool decode);
+int64_t decode_counter_count(int64_t P, int32_t E, int32_t H, int32_t I);
 
 // ------------------------------------------------------------------ launches
 // Optional profiling events recorded between phases (see moe_w2_forward_traced).
@@ -225,9 +281,13 @@ struct PhaseEvents {
 
 cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* sorted, int32_t* inv,
                            int32_t* offsets, int32_t* active, int32_t* active_count, int4* tiles,
-                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16, int32_t H,
-                           int32_t* counters, int32_t n_counters, uint16_t* y, uint32_t* status, cudaStream_t s);
+                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16, uint8_t* x8,
+                           uint8_t* sx8, int32_t H, int32_t* counters, int32_t n_counters, uint16_t* y,
+                           uint32_t* status, cudaStream_t s);
 
+cudaError_t launch_decode_mma(const uint16_t* x, const int32_t* ids, const float* weights,
+                              const moe_w2_planes& w, int32_t T, int32_t k, const Workspace& ws, uint16_t* y,
+                              uint32_t* status, cudaStream_t s, const PhaseEvents& ev);
 cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* weights,
                           const moe_w2_planes& w, int32_t T, int32_t k, const Workspace& ws, uint16_t* y,
                           uint32_t* status, cudaStream_t s, const PhaseEvents& ev);

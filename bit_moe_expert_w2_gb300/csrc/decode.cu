@@ -1,42 +1,54 @@
 // Decode path (T <= 64): the 2-bit planes of every active expert are streamed
-// from HBM once per layer, expanded in registers and fed to tensor-core MMAs.
+// from HBM once per layer and multiplied on the tensor cores in block-scaled FP8.
 //
 // vLLM-Moet, page "vLLM-Moet wiki", section "The kernels": codes expanded in
-// registers through a byte-permute lookup table and fed to tensor-core MMAs;
-// section "FP4 recovery": decode is HBM-bound, the 2-bit read is the cost.  Page
-// "The v0.24.0 port", section "Benchmarks": tokens grouped by expert, so each
-// active expert's weights are read once per step however many tokens use it.
-// Page "The v0.24.0 port", "Deterministic unpermute" bullet: per-pair results
-// are placed in their own slot and summed over top_k in a fixed order.
+// registers through a byte-permute lookup table and fed to block-scaled
+// tensor-core MMAs; section "FP4 recovery": decode is HBM-bound, the 2-bit read
+// is the cost.  Page "The v0.24.0 port", section "Benchmarks": tokens grouped by
+// expert, so each active expert's weights are read once per step however many
+// tokens use it.  Page "The v0.24.0 port", "Deterministic unpermute" bullet:
+// per-pair results are placed in their own slot and summed in a fixed order.
 //
-// Why mma.sync here and not tcgen05: with N = a handful of pairs, every
-// tcgen05.mma (M=128, K=16) of a CTA costs ~105 cycles whatever N is (measured
-// on GB300), which caps a CTA far below HBM rate, while mma.sync m16n8k16 keeps
-// the weights in registers and reaches the full tensor rate with enough warps.
-// The expansion is integer work on the ALU pipe (two masks, five shifts and
-// eight byte-permutes per 16 codes) plus two multiply-adds on the FMA pipe.
+// Why block-scaled e4m3 (tcgen05.mma kind::mxf8f6f4, scale_vec::1X): a weight is
+// +-1 or +-4 times 2^(s-127) with one UE8M0 byte s per 32 K of a row, which is
+// an e4m3 value (0x38, 0x48, 0xB8, 0xC8) under an MX block scale.  The tensor
+// core applies s itself, so the expansion is one byte per code: per 16-code word
+// two masks, three shifts and four byte-permutes against one constant table
+// (folding s into bf16 instead takes eight byte-permutes plus per-block table
+// lookups).  Activations enter as two e4m3 rows each (act_split), which keeps
+// their bf16 precision.
 //
-// One kernel runs the whole layer (gate_up, then down with the combine).  Work
-// item = (tile of <= 16 pairs of one expert, 32 weight rows).  Each CTA has four
-// consumer warps that split K of an item (256-element chunks, round robin) and
-// reduce in shared memory in warp order, and one producer warp that runs ahead
-// through the CTA's items: it takes items from a global queue, publishes each
-// item's tile through a small shared-memory ring, and streams every chunk's code
-// bytes (TMA: 32 rows x 64 bytes) and scale bytes (one 8-byte cp.async per row)
-// into a ring of chunk slots.  Consumers only wait on a slot's barrier, read it
-// from shared memory and release it, so the loads of the next item overlap the
-// end of the current one.
-//
-// Per 256-wide K chunk a row is 64 code bytes; thread c of a quad owns bytes
-// [16c, 16c+16), i.e. four 16-code words; MMA (word i, r) takes codes (r, r+4)
-// and (r+8, r+12) of word i from every thread of the quad, which is what the
-// T16 activation layout stores next to each other (one 64-bit load per B
-// fragment).  gate_up: m-tile t = gate rows n0+8t.. (A rows 0-7) and the
-// matching up rows (A rows 8-15), so gate and up of one (row, pair) meet in one
-// thread for the SiLU(gate)*up epilogue.  down: 32 consecutive rows of W_down;
-// the epilogue multiplies by the router weight and writes the pair's fp32 slot;
-// the last CTA to finish a 32-row block of y sums the k slots of every token in
-// j order and writes y (counter per row block, reset by the permutation kernel).
+// Work item = (tile of <= 8 pairs of one expert, 128 weight rows, K segment).
+// gate_up rows: 64 gate rows and the matching 64 up rows; down rows: 128 rows of
+// W_down.  Each CTA has six warps:
+//   warp 4     producer: takes items from a global queue, publishes them, and
+//              streams every 128-K chunk into a ring of shared-memory slots:
+//              code bytes by TMA (128 rows x 32 bytes, 32B-swizzled), the
+//              item's 16 activation rows (written straight into the
+//              128B-swizzled UMMA layout) by cp.async, and at the first chunk of
+//              every group of 4 (or 2) chunks the group's scale words of all
+//              rows, one 16-byte (8-byte) cp.async per row
+//   warps 0-3  consumers, one per TMEM lane quadrant and one thread per weight
+//              row: expand the row's 128 codes of a chunk to e4m3 and store them
+//              with the row's scale word into TMEM, plus this quadrant's copy of
+//              the activation scale words
+//   warp 5     MMA issuer (one thread): 4 x tcgen05.mma (M=128, N=16, K=32) per
+//              chunk into one of two TMEM accumulators
+//   warp 6     finisher: the cross-CTA part of every gate_up epilogue
+// An item's accumulator is read by the consumer warps after the first chunk of
+// the next item (it is double-buffered), warp by warp with no CTA-wide barrier:
+//   gate_up  partial sums of the K segment -> gu_part; the finisher counts the
+//            segment, and the last of the S segments of a (tile, 64-row block)
+//            sums them in segment order, writes h = bf16(SiLU(g) * u) as e4m3
+//            activation rows and marks the block ready
+//   down     w * partial -> stage[segment][pair]
+// A separate combine kernel, launched as a programmatic dependent, sums every
+// token's slots in (j, segment) order and writes y.
+// A down item reads only the h row blocks of its K segment.  Its producer
+// publishes the item, then waits (bounded) until each of those blocks is marked
+// ready before loading its chunks, so the consumers see a down item coming and
+// store a pending gate_up epilogue before they block on its data.  Every wait is bounded; on a timeout the kernel raises the pipeline
+// status bit, drains its MMAs, frees its tensor memory and returns.
 #include <algorithm>
 
 #include "tc.cuh"
@@ -45,419 +57,607 @@ namespace moe_w2 {
 
 namespace {
 
-#ifndef MOE_W2_DEC_MIN_CTAS
-#define MOE_W2_DEC_MIN_CTAS 4        // CTAs per SM the register budget is sized for
-#endif
-constexpr int kChunk = 256;          // K elements per chunk
-constexpr int kWarps = 4;            // consumer warps
-constexpr int kThreads = (kWarps + 1) * 32;   // + the producer warp
-constexpr int kMaxNT = 2;            // n-tiles of 8 pairs per item (tiles of <= 16 pairs)
-constexpr int kSlots = 16;           // chunk slots (four per consumer warp; a power of two)
-constexpr uint32_t kSlotCodeBytes = 32 * 64;   // 32 rows x 64 code bytes
-constexpr uint32_t kSlotScaleBytes = 32 * 8;   // 32 rows x 8 UE8M0 bytes
-constexpr uint32_t kSlotBytes = kSlotCodeBytes + kSlotScaleBytes;   // a multiple of 128
-constexpr uint32_t kRingBytes = kSlots * kSlotBytes;
-constexpr int kInfo = 16;            // published items in flight
-constexpr uint32_t kConsumerBarrier = 1;       // named barrier id of the consumer warps
+constexpr int kChunk = 128;                          // K per chunk: 4 MMAs of K = 32 (one scale block each)
+constexpr int kRows = 128;                           // weight rows per item (MMA M)
+constexpr int kTilePairs = 8;                        // pairs per tile
+constexpr int kN = 2 * kTilePairs;                   // MMA N: hi and lo activation row per pair
+constexpr int kCWarps = 4;                           // consumer warps
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kFinisherWarp = 6;
+constexpr int kThreads = 7 * 32;
+constexpr int kSlots = 6;                            // chunk slots
+constexpr uint32_t kCodeBytes = kRows * 32;          // 128 rows x 32 code bytes, 32B-swizzled
+constexpr uint32_t kBOff = kCodeBytes;               // 16 activation rows x 128 bytes, 128B-swizzled
+constexpr uint32_t kSlotBytes = kBOff + kN * 128;    // 6144, a multiple of 1024
+constexpr uint32_t kSfbOff = kRows * 16;             // scale area of a slot: 128 rows x 16 bytes of
+constexpr uint32_t kSfSlotBytes = kSfbOff + kN * 16; // weight-row scale words, then 16 activation rows
+constexpr uint32_t kRingBytes = kSlots * (kSlotBytes + kSfSlotBytes);
+constexpr int kInfo = 8;                             // published items in flight
+constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kColD = 0;                        // accumulators: 2 x 16 columns
+constexpr uint32_t kColA = 32;                       // A stages: 2 x 32 columns
+constexpr uint32_t kColSfa = 96;                     // stage s, quadrant w: column 96 + 4s + w
+constexpr uint32_t kColSfb = 104;                    // stage s: column 104 + 4s
+// (scale-factor operands start on a 4-column boundary: an M = 128 tile's A
+// scales span 4 columns, one per lane quadrant)
+constexpr uint32_t kLut = 0xC8B84838u;               // e4m3 of +1, +4, -1, -4 (code 0..3)
+constexpr int32_t kHReady = 1 << 20;                 // added to a row block's counter once its h is written
 
-struct DecArgs {
-    const uint8_t* codes;      // [E][rows_per_expert][K/4]
-    const uint8_t* scales;     // [E][rows_per_expert][K/32]
-    int32_t K;
-    int32_t rows_per_expert;
-    int32_t I;
-    int32_t H;
-    int32_t T;
-    int32_t k;
-    int32_t E;
-    int32_t row_blocks;
+struct LayerArgs {
+    const uint8_t* w13_scales;   // [E][2I][H/32]
+    const uint8_t* w2_scales;    // [E][H][I/32]
+    int32_t H, I, T, k, E;
+    DecodeSplit split;
+    int64_t P;
     const int4* tiles;
     const int32_t* tile_count;
     const int32_t* sorted;
     const float* weights;
     const int32_t* ids;
-    const uint16_t* act;       // B rows: x_t16 per token (gate_up) or h_t16 per pair (down)
-    uint16_t* h_t16;           // gate_up output [P][I]
-    float* stage;              // down output [P][H]
-    int32_t* counters;         // down: per 32-row block of y
+    const uint8_t* x8;           // [2T][H]
+    const uint8_t* sx8;          // [2T][H/32]
+    uint8_t* h8;                 // [2P][I]
+    uint8_t* sh8;                // [2P][I/32]
+    float* gu_part;              // [s_gu][P][2I]
+    float* stage;                // [s_dn][P][H]
+    int32_t* gu_seg;             // [tiles][I/64]: contributing items done; + kHReady once h is written
+    int32_t* queue;
     uint16_t* y;
     uint32_t* status;
 };
 
 struct SharedState {
-    uint64_t full[kSlots];      // producer -> consumers: slot filled (expect_tx arrival + 32 cp.async arrivals)
-    uint64_t empty[kSlots];     // consumer warp -> producer: slot read
-    uint64_t info_full[kInfo];  // producer -> consumers: item published
-    uint64_t info_empty[kInfo]; // consumer warps -> producer: item finished
-    int4 info[kInfo];           // (item index, or -1 at the end; expert; first slot; pairs)
-    uint2 lut[256];
-    float red[kWarps][2][kMaxNT][32][4];
-    int4 cur_info;              // the item the consumer warps work on
-    int last_flag;
-    int stop;
+    uint64_t full[kSlots];       // producer -> consumers, MMA: slot filled (tx bytes + 32 cp.async arrivals)
+    uint64_t empty[kSlots];      // MMA commit -> producer: slot read
+    uint64_t a_full[2];          // consumer warps -> MMA: A stage written
+    uint64_t a_empty[2];         // MMA commit -> consumers: A stage read
+    uint64_t d_full[2];          // MMA commit -> consumers: accumulator complete
+    uint64_t d_empty[2];         // consumer warps -> MMA: accumulator read
+    uint64_t info_full[kInfo];   // producer -> consumers, MMA: item published
+    uint64_t info_empty[kInfo];  // consumers, MMA, finisher -> producer: item done with
+    uint64_t epi[kInfo];         // consumer warps -> finisher: item's partial sums stored
+    uint64_t drain;
+    int info[kInfo][12];         // published items (Item fields; kind -1 at the end)
+    uint32_t tmem;
     int abort_flag;
 };
 
-__device__ __forceinline__ uint32_t ld_acquire(const int32_t* p)
+// A work item: one tile, 128 weight rows (gate_up: a 64-row block of gate and
+// of up; down: a 128-row block of W_down) and the K chunks [c0, c1).
+//   gate_up  K is cut into ranges of the whole phase's chunk sequence, one
+//            range per queue entry, of equal length; a range may start and end
+//            inside a row block, so a row block has cnt contributing items,
+//            seg = 0 .. cnt-1 in K order
+//   down     a row block's K is cut into s_dn segments of l_dn chunks
+struct Item {
+    int kind;   // 1 gate_up, 0 down, -1 end
+    int ti, rb, seg, c0, c1, cnt, expert, q0, nrows;
+};
+
+__device__ __forceinline__ void put_item(int* dst, const Item& m)
 {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    dst[0] = m.kind; dst[1] = m.ti; dst[2] = m.rb; dst[3] = m.seg; dst[4] = m.c0;
+    dst[5] = m.c1; dst[6] = m.cnt; dst[7] = m.expert; dst[8] = m.q0; dst[9] = m.nrows;
+}
+__device__ __forceinline__ Item get_item(const int* src)
+{
+    Item m;
+    m.kind = src[0]; m.ti = src[1]; m.rb = src[2]; m.seg = src[3]; m.c0 = src[4];
+    m.c1 = src[5]; m.cnt = src[6]; m.expert = src[7]; m.q0 = src[8]; m.nrows = src[9];
+    return m;
+}
+
+// Range r of n_ranges over c_total chunks: [r c_total / n_ranges, (r+1) c_total / n_ranges).
+__device__ __forceinline__ int64_t range_start(int64_t r, int64_t c_total, int64_t n_ranges)
+{
+    return r * c_total / n_ranges;
+}
+// The range holding chunk f (the last r with range_start(r) <= f).
+__device__ __forceinline__ int64_t range_of(int64_t f, int64_t c_total, int64_t n_ranges)
+{
+    return ((f + 1) * n_ranges - 1) / c_total;
+}
+
+__device__ __forceinline__ int32_t ld_acquire(const int32_t* p)
+{
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void consumer_sync()
+__device__ __forceinline__ uint32_t lds_u32(uint32_t saddr)
 {
-    asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrier), "n"(kWarps * 32) : "memory");
-}
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-}
-// The barrier gets one arrival once all of this thread's earlier cp.async copies
-// have landed (its expected count includes that arrival).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+    uint32_t r;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(saddr) : "memory");
+    return r;
 }
 
-__device__ __forceinline__ uint32_t word_of(const uint4& q, int i)
+// Nonzero when a byte of the scale word s is outside [1, 252] (may also flag a
+// valid byte above an invalid one; the caller re-checks byte by byte).
+__device__ __forceinline__ uint32_t scale_word_suspect(uint32_t s)
 {
-    return i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
+    const uint32_t d = s - 0x01010101u;
+    return ((d & 0x7F7F7F7Fu) + 0x04040404u) & d & 0x80808080u;
 }
 
-// One item on the consumer warps: K chunks ch = warp, warp + 4, ... from ring
-// slots (qbase + ch) % kSlots, then the split-K reduction and the epilogue.
-template <bool kGateUp, int NT>
-__device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, SharedState& sh, const uint8_t* ring,
-                                         uint32_t qbase, int q0, int nrows, int rb, uint32_t& lut_and)
+// Consumer side of an item's epilogue, one warp (its 32 weight rows): the
+// accumulator rows as partial sums in global memory, then one arrival on the
+// item's epi barrier for the finisher warp.
+__device__ __noinline__ void epilogue_store(const LayerArgs& a, SharedState& sh, uint32_t tq, const Item& it, int n,
+                                            volatile int* abort)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, c = lane & 3;
-    const int nch = p.K / kChunk;
-    // slot rows of the thread's four A rows: m-tile 0 -> (g, g+8), m-tile 1 -> (16+g, 24+g);
-    // gate_up slot rows 0-15 are gate rows n0.., 16-31 the matching up rows
-    int srow[4];
-    if (kGateUp) {
-        srow[0] = g;
-        srow[1] = 16 + g;
-        srow[2] = 8 + g;
-        srow[3] = 24 + g;
+    const int lane = threadIdx.x & 31, m = threadIdx.x;
+    const uint32_t b = (uint32_t)n & 1u;
+    // every lane waits (each acquires); the outcome is made warp-uniform before
+    // the .sync.aligned tensor-memory load
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.d_full[b]), ((uint32_t)n >> 1) & 1u, abort))) return;
+    tc_fence_after();
+    float v[16];
+    tmem_ld16(tq + kColD + 16 * b, v);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sh.d_empty[b]));
+    const int64_t P = a.P;
+    if (it.kind == 1) {
+        const int I2 = 2 * a.I;
+        const int col = m < 64 ? 64 * it.rb + m : a.I + 64 * it.rb + (m - 64);
+        float* dst = a.gu_part + ((int64_t)it.seg * P + it.q0) * I2 + col;
+#pragma unroll
+        for (int j = 0; j < kTilePairs; ++j)
+            if (j < it.nrows) dst[(int64_t)j * I2] = v[2 * j] + v[2 * j + 1];
     } else {
-        srow[0] = g;
-        srow[1] = 8 + g;
-        srow[2] = 16 + g;
-        srow[3] = 24 + g;
-    }
-    // B rows: pair j = 8*nt + g of the tile.  Columns past the tile's pairs read
-    // pair 0's row (always valid); their results are never stored.
-    const uint16_t* brow[NT];
+        const int row = 128 * it.rb + m;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int j = nt * 8 + g < nrows ? nt * 8 + g : 0;
-        const int64_t br = kGateUp ? (int64_t)(__ldg(p.sorted + q0 + j) / p.k) : (int64_t)(q0 + j);
-        brow[nt] = p.act + br * p.K + c * 64;
-    }
-
-    float acc[2][NT][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
-
-    volatile int* abort = &sh.abort_flag;
-    for (int ch = warp; ch < nch; ch += kWarps) {
-        const uint32_t q = qbase + (uint32_t)ch;
-        const uint32_t slot = q % kSlots;
-        if (!mbar_wait(smem_u32(&sh.full[slot]), (q / kSlots) & 1u, abort)) break;
-        // plain (compiler-schedulable) shared loads: the wait above is a compiler barrier
-        const uint8_t* sp = ring + slot * kSlotBytes;
-        uint4 qw[4];
-        uint2 L[4][2];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            qw[a] = *reinterpret_cast<const uint4*>(sp + srow[a] * 64 + c * 16);
-            const uint8_t* sb = sp + kSlotCodeBytes + srow[a] * 8 + 2 * c;
-            L[a][0] = sh.lut[sb[0]];
-            L[a][1] = sh.lut[sb[1]];
-            lut_and &= L[a][0].x & L[a][1].x;
-        }
-        const uint16_t* bsrc[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) bsrc[nt] = brow[nt] + (int64_t)ch * kChunk;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint4 B0[NT], B1[NT];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                if (kGateUp) {   // x in T16 order, written by an earlier launch: read-only path
-                    B0[nt] = __ldg(reinterpret_cast<const uint4*>(bsrc[nt] + i * 16));
-                    B1[nt] = __ldg(reinterpret_cast<const uint4*>(bsrc[nt] + i * 16 + 8));
-                } else {         // h, written by gate_up items of this launch: coherent loads
-                    B0[nt] = *reinterpret_cast<const uint4*>(bsrc[nt] + i * 16);
-                    B1[nt] = *reinterpret_cast<const uint4*>(bsrc[nt] + i * 16 + 8);
-                }
+        for (int j = 0; j < kTilePairs; ++j)
+            if (j < it.nrows) {
+                const int pr = __ldg(a.sorted + it.q0 + j);
+                a.stage[((int64_t)it.seg * P + pr) * a.H + row] = __ldg(a.weights + pr) * (v[2 * j] + v[2 * j + 1]);
             }
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                const Masks ma = word_masks(word_of(qw[2 * mt], i), k), mb = word_masks(word_of(qw[2 * mt + 1], i), k);
-                const uint2 la = L[2 * mt][i >> 1], lb = L[2 * mt + 1][i >> 1];
-                uint32_t alo[4], ahi[4], blo[4], bhi[4];
-                selectors(ma, k, alo, ahi);
-                selectors(mb, k, blo, bhi);
-                uint32_t afrag[4][4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    afrag[r][0] = prmt(la.x, la.y, alo[r]);
-                    afrag[r][1] = prmt(lb.x, lb.y, blo[r]);
-                    afrag[r][2] = prmt(la.x, la.y, ahi[r]);
-                    afrag[r][3] = prmt(lb.x, lb.y, bhi[r]);
-                }
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const uint4& Bv = (r < 2) ? B0[nt] : B1[nt];
-                        mma_bf16_16816(acc[mt][nt], afrag[r], (r & 1) ? Bv.z : Bv.x, (r & 1) ? Bv.w : Bv.y);
-                    }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.empty[slot]));
     }
-
-    // split-K reduction in warp order
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int v = 0; v < 4; ++v) sh.red[warp][mt][nt][lane][v] = acc[mt][nt][v];
-    consumer_sync();
-    // warp w finalises m-tile (w & 1), n-tile (w >> 1)
-    const int mt = warp & 1;
-    for (int nt = warp >> 1; nt < NT; nt += 2) {
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float s = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) s += sh.red[w][mt][nt][lane][e];
-            v[e] = s;
-        }
-        if (kGateUp) {
-            const int pos = t16_pos(rb * 16 + mt * 8 + g);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int j = nt * 8 + 2 * c + h;
-                if (j < nrows) {
-                    __nv_bfloat16 hb = __float2bfloat16_rn(silu_f(v[h]) * v[2 + h]);
-                    p.h_t16[(int64_t)(q0 + j) * p.I + pos] = *reinterpret_cast<uint16_t*>(&hb);
-                }
-            }
-        } else {
-            const int m = rb * 32 + mt * 16 + g;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int j = nt * 8 + 2 * c + h;
-                if (j < nrows) {
-                    const int pr = __ldg(p.sorted + q0 + j);
-                    const float wt = __ldg(p.weights + pr);
-                    p.stage[(int64_t)pr * p.H + m] = wt * v[h];
-                    p.stage[(int64_t)pr * p.H + m + 8] = wt * v[2 + h];
-                }
-            }
-        }
-    }
-    consumer_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sh.epi[(uint32_t)n % kInfo]));
 }
 
-// One persistent grid runs the whole decode layer.  Items come from one queue:
-// indices [0, n_gu) are gate_up items (tile, 16 gate + 16 up rows), [n_gu, n_all)
-// down items (tile, 32 rows of y).  Each CTA's producer warp takes every item,
-// the first included, from a global counter, so only CTAs that are running hold
-// items.  A down item of tile t needs h of every row of t, so the producer waits
-// until the tile's gate_up counter reaches the number of gate_up row blocks
-// before it publishes the item; every gate_up index is handed out before any
-// down index and is held by a running CTA, so the waits always end (each is
-// still bounded and gives up with the pipeline-timeout status bit).  Which CTA
-// runs an item never changes its result.
-__global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS)
+// Finisher side of a gate_up item's epilogue (one warp), once the four
+// consumer warps have stored its partial sums: count the item at its
+// (tile, 64-row block); the last of the block's cnt items sums their partial
+// sums in K order, writes h = bf16(SiLU(g) * u) as e4m3 activation rows and
+// marks the block ready.  The fence after the barrier wait orders every store the barrier
+// made visible to this warp before the counter update (fences are cumulative).
+__device__ __noinline__ void finish_gate_up(const LayerArgs& a, const Item& it)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t P = a.P;
+    int32_t* cnt = a.gu_seg + it.ti * (a.I / 64) + it.rb;
+    int last = 0;
+    if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(cnt, 1) == it.cnt - 1;
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    const int I2 = 2 * a.I;
+    // indices 64 rb + 32 blk + lane; one activation scale block per blk
+    for (int blk = 0; blk < 2; ++blk) {
+        const int i = 64 * it.rb + 32 * blk + lane;
+        const int pos = (i & ~15) | e4_pos(i & 15);
+        for (int j = 0; j < it.nrows; ++j) {
+            const int64_t q = it.q0 + j;
+            float g = 0.f, u = 0.f;
+#pragma unroll 4
+            for (int sg = 0; sg < it.cnt; ++sg) {   // contributing items in K order
+                const float* src = a.gu_part + ((int64_t)sg * P + q) * I2;
+                g += __ldcg(src + i);
+                u += __ldcg(src + a.I + i);
+            }
+            const float hv = __bfloat162float(__float2bfloat16_rn(silu_f(g) * u));
+            const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
+            const uint32_t s8 = act_scale_byte(__uint_as_float(amax_bits));
+            uint32_t hi, lo;
+            act_split(hv * act_inv_scale(s8), hi, lo);
+            a.h8[(2 * q) * a.I + pos] = (uint8_t)hi;
+            a.h8[(2 * q + 1) * a.I + pos] = (uint8_t)lo;
+            if (lane == 0) {
+                a.sh8[(2 * q) * (a.I / 32) + i / 32] = (uint8_t)s8;
+                a.sh8[(2 * q + 1) * (a.I / 32) + i / 32] = (uint8_t)s8;
+            }
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence();
+        atomicAdd(cnt, kHReady);   // h of the block is ready
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 4)
 decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_constant__ CUtensorMap dn_map,
-                    DecArgs gu, DecArgs dn, int32_t* __restrict__ gu_done, int32_t* __restrict__ queue)
+                    const LayerArgs a)
 {
     __shared__ SharedState sh;
-    extern __shared__ uint8_t dyn_smem[];   // kRingBytes + 128 (aligned below)
-    // 128-byte aligned ring; offsetting the shared array itself keeps the
-    // pointer in the shared window (plain loads from it compile to shared loads)
-    const uint32_t pad = (128u - (smem_u32(dyn_smem) & 127u)) & 127u;
-    const uint8_t* ring = dyn_smem + pad;
-    const uint32_t ring_addr = smem_u32(dyn_smem) + pad;
+    extern __shared__ uint8_t dyn_smem[];   // kRingBytes + 1024 (aligned below)
+    const uint32_t ring_addr = (smem_u32(dyn_smem) + 1023u) & ~1023u;
+    const uint32_t sf_addr = ring_addr + kSlots * kSlotBytes;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int s = tid; s < 256; s += kThreads) {
-        ScaleLut l = make_lut((uint32_t)s);
-        sh.lut[s] = make_uint2(l.lut, l.lo);
-    }
     if (tid == 0) {
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1 + 32);
             mbar_init(smem_u32(&sh.empty[s]), 1);
         }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&sh.a_full[s]), kCWarps);
+            mbar_init(smem_u32(&sh.a_empty[s]), 1);
+            mbar_init(smem_u32(&sh.d_full[s]), 1);
+            mbar_init(smem_u32(&sh.d_empty[s]), kCWarps);
+        }
         for (int s = 0; s < kInfo; ++s) {
             mbar_init(smem_u32(&sh.info_full[s]), 1);
-            mbar_init(smem_u32(&sh.info_empty[s]), kWarps);
+            mbar_init(smem_u32(&sh.info_empty[s]), kCWarps + 2);
+            mbar_init(smem_u32(&sh.epi[s]), kCWarps);
         }
+        mbar_init(smem_u32(&sh.drain), 1);
         sh.abort_flag = 0;
         mbar_fence_init();
     }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&sh.tmem), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(&gu_map);
+        prefetch_tmap(&dn_map);
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = sh.tmem;
     volatile int* abort = &sh.abort_flag;
 
     // Launched as a programmatic dependent of the permutation kernel: the setup
-    // above overlaps it; everything it writes (tiles, counters, x in T16 order)
-    // is read only after this wait.
+    // above overlaps it; everything it writes (tiles, counters, x8) is read
+    // only after this wait.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int n_tiles = *gu.tile_count;
-    const int n_gu = n_tiles * gu.row_blocks;
-    const int n_all = n_gu + n_tiles * dn.row_blocks;
+    // the combine kernel may be scheduled now (it waits for this grid to finish)
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int n_tiles = *a.tile_count;
+    const int rbg = a.I / 64, rbd = a.H / 128;
+    const int nch_gu = a.H / kChunk, nch_dn = a.I / kChunk;
+    // gate_up: the chunk sequence of all (tile, 64-row block) units in ranges
+    const int64_t c_gu = (int64_t)n_tiles * rbg * nch_gu;
+    // ranges no shorter than the host's minimum, which bounds the contributing
+    // items of a row block (the gu_part slots)
+    const int64_t r_gu =
+        c_gu > 0 ? max((int64_t)1, min((int64_t)gridDim.x, c_gu / a.split.gu_min_range)) : 0;
+    const int64_t n_dn = (int64_t)n_tiles * rbd * a.split.s_dn;
 
-    if (warp == kWarps) {
-        // ------------------------------------------------ producer warp
-        if (lane == 0) {
-            prefetch_tmap(&gu_map);
-            prefetch_tmap(&dn_map);
-        }
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------ producer
+        // Queue entries [0, r_gu) are gate_up ranges, then down items; every
+        // gate_up range is handed out before any down item.
         uint32_t q = 0;
-        int it = 0;
-        if (lane == 0) it = atomicAdd(queue, 1);
-        it = __shfl_sync(0xffffffffu, it, 0);
-        for (int n = 0;; ++n) {
+        int n = 0;
+        bool ok = true;
+        // publish one item; false when the pipeline gave up
+        auto publish = [&](const Item& m) {
             const uint32_t islot = (uint32_t)n % kInfo;
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(smem_u32(&sh.info_empty[islot]), ((uint32_t)(n / kInfo) & 1u) ^ 1u, abort);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            if (it >= n_all) {
-                if (lane == 0) {
-                    sh.info[islot] = make_int4(-1, 0, 0, 0);
-                    mbar_arrive(smem_u32(&sh.info_full[islot]));
-                }
-                break;
-            }
-            const bool is_gu = it < n_gu;
-            const DecArgs& P = is_gu ? gu : dn;
-            const int id = is_gu ? it : it - n_gu;
-            const int ti = id / P.row_blocks, rb = id % P.row_blocks;
-            const int4 tile = P.tiles[ti];
-            if (!is_gu && lane == 0 && (int)ld_acquire(gu_done + ti) < gu.row_blocks) {
-                const long long t0 = clock64();
-                while ((int)ld_acquire(gu_done + ti) < gu.row_blocks) {
-                    if (clock64() - t0 > kWaitLimitCycles) {
-                        *abort = 1;
-                        break;
-                    }
-                    __nanosleep(256);
-                }
-            }
-            if (__shfl_sync(0xffffffffu, *abort, 0)) break;
+            int w = 1;
+            if (lane == 0) w = mbar_wait(smem_u32(&sh.info_empty[islot]), (((uint32_t)n / kInfo) & 1u) ^ 1u, abort);
+            if (!__shfl_sync(0xffffffffu, w, 0)) return false;
             if (lane == 0) {
-                sh.info[islot] = make_int4(it, tile.x, tile.y, tile.z);
+                put_item(sh.info[islot], m);
                 mbar_arrive(smem_u32(&sh.info_full[islot]));
             }
-            // the item's rows: TMA rows, and this lane's scale row
-            const int64_t ebase = (int64_t)tile.x * P.rows_per_expert;
-            int64_t srow;
-            if (is_gu) srow = ebase + (lane < 16 ? rb * 16 + lane : P.I + rb * 16 + (lane - 16));
-            else srow = ebase + rb * 32 + lane;
-            const uint8_t* ssrc = P.scales + srow * (P.K / 32);
-            const int nch = P.K / kChunk;
-            for (int ch = 0; ch < nch; ++ch, ++q) {
+            ++n;
+            return true;
+        };
+        // stream the chunks of a published item into the ring
+        auto stream = [&](const Item& m) {
+            if (m.kind == 0) {
+                // the h row blocks this K range reads (64 rows each; two per
+                // chunk) must be written before their rows are copied: lane r
+                // watches blocks 2 c0 + r, 2 c0 + r + 32, ...
+                const int32_t* hs = a.gu_seg + m.ti * rbg;
+                const int hb0 = 2 * m.c0, hb1 = 2 * m.c1;
+                auto all_ready = [&]() {
+                    bool r = true;
+                    for (int hb = hb0 + lane; hb < hb1; hb += 32) r = r && ld_acquire(hs + hb) >= kHReady;
+                    return __all_sync(0xffffffffu, r);
+                };
+                if (!all_ready()) {
+                    const long long t0 = clock64();
+                    bool timed_out = false;
+                    while (!all_ready()) {
+                        if (__shfl_sync(0xffffffffu, *abort, 0)) break;
+                        if (clock64() - t0 > kWaitLimitCycles) {
+                            timed_out = true;
+                            break;
+                        }
+                        __nanosleep(128);
+                    }
+                    if (timed_out && lane == 0) *abort = 1;
+                }
+                __syncwarp();   // every lane's copies come after the lanes' acquires
+                if (__shfl_sync(0xffffffffu, *abort, 0)) return false;
+            }
+            const bool gu = m.kind == 1;
+            // tokens of the tile's pairs (lane j < 8 holds pair j's), gate_up only
+            const int tok = (gu && lane < m.nrows) ? __ldg(a.sorted + m.q0 + lane) / a.k : 0;
+            // this lane's copy sources: 4 weight-row scale rows, 4 activation
+            // pieces of 16 bytes (row n = p / 8, piece p % 8), lanes < 16 one
+            // activation scale row
+            const uint8_t* sc = gu ? a.w13_scales : a.w2_scales;
+            const int64_t kb = (gu ? a.H : a.I) / 32;
+            const int G = gu ? a.split.g_gu : a.split.g_dn;   // chunks per scale-word group
+            const int64_t erow = (int64_t)m.expert * (gu ? 2 * a.I : a.H);
+            const uint8_t* sfa_src[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = lane + 32 * i;
+                const int64_t wr = gu ? (r < 64 ? 64 * m.rb + r : a.I + 64 * m.rb + (r - 64)) : 128 * m.rb + r;
+                sfa_src[i] = sc + (erow + wr) * kb;
+            }
+            const uint8_t* act = gu ? a.x8 : a.h8;
+            const uint8_t* sact = gu ? a.sx8 : a.sh8;
+            const int64_t kact = gu ? a.H : a.I;
+            const uint8_t* bsrc[4];
+            uint32_t bdst[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int p = lane + 32 * i, nb = p >> 3, j = nb >> 1;
+                const int tj = __shfl_sync(0xffffffffu, tok, j);
+                bdst[i] = kBOff + sw128_offset((uint32_t)nb, (uint32_t)(p & 7));
+                const int64_t row = gu ? 2 * (int64_t)tj + (nb & 1) : 2 * (int64_t)(m.q0 + j) + (nb & 1);
+                bsrc[i] = j < m.nrows ? act + row * kact + (p & 7) * 16 : nullptr;
+            }
+            const uint8_t* sfb_src = nullptr;
+            {
+                const int j = (lane >> 1) & 7;
+                const int tj = __shfl_sync(0xffffffffu, tok, j);
+                const int64_t row = gu ? 2 * (int64_t)tj + (lane & 1) : 2 * (int64_t)(m.q0 + j) + (lane & 1);
+                if (lane < kN && j < m.nrows) sfb_src = sact + row * (kact / 32);
+            }
+            for (int ch = m.c0; ch < m.c1; ++ch, ++q) {
                 const uint32_t slot = q % kSlots;
-                if (lane == 0) ok = mbar_wait(smem_u32(&sh.empty[slot]), ((q / kSlots) & 1u) ^ 1u, abort);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                const uint32_t fb = smem_u32(&sh.full[slot]);
-                const uint32_t dst = ring_addr + slot * kSlotBytes;
+                int w = 1;
+                if (lane == 0) w = mbar_wait(smem_u32(&sh.empty[slot]), ((q / kSlots) & 1u) ^ 1u, abort);
+                if (!__shfl_sync(0xffffffffu, w, 0)) return false;
+                const uint32_t base = ring_addr + slot * kSlotBytes, fb = smem_u32(&sh.full[slot]);
+                const uint32_t sfbase = sf_addr + slot * kSfSlotBytes;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(fb, kSlotCodeBytes);
-                    if (is_gu) {
-                        tma_load_2d(dst, &gu_map, ch * 64, (int)(ebase + rb * 16), fb);
-                        tma_load_2d(dst + 16 * 64, &gu_map, ch * 64, (int)(ebase + P.I + rb * 16), fb);
+                    mbar_arrive_expect_tx(fb, kCodeBytes);
+                    if (gu) {
+                        tma_load_2d(base, &gu_map, ch * 32, (int)(erow + 64 * m.rb), fb);
+                        tma_load_2d(base + 64 * 32, &gu_map, ch * 32, (int)(erow + a.I + 64 * m.rb), fb);
                     } else {
-                        tma_load_2d(dst, &dn_map, ch * 64, (int)(ebase + rb * 32), fb);
+                        tma_load_2d(base, &dn_map, ch * 32, (int)(erow + 128 * m.rb), fb);
                     }
                 }
-                cp_async8(dst + kSlotCodeBytes + lane * 8, ssrc + ch * 8);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (bsrc[i] != nullptr) cp_async16(base + bdst[i], bsrc[i] + ch * 128);
+                // scale words move in groups of G chunks aligned to the row (16 or
+                // 8 bytes); a group is copied at its first chunk, or at the item's
+                // first chunk when the item starts inside it
+                if ((ch & (G - 1)) == 0 || ch == m.c0) {
+                    const int gch = ch & ~(G - 1);
+                    if (G == 4) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) cp_async16(sfbase + (lane + 32 * i) * 16, sfa_src[i] + gch * 4);
+                        if (sfb_src != nullptr) cp_async16(sfbase + kSfbOff + lane * 16, sfb_src + gch * 4);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) cp_async8(sfbase + (lane + 32 * i) * 16, sfa_src[i] + gch * 4);
+                        if (sfb_src != nullptr) cp_async8(sfbase + kSfbOff + lane * 16, sfb_src + gch * 4);
+                    }
+                }
                 cp_async_arrive_noinc(fb);
             }
+            return true;
+        };
+        for (;;) {
+            int it = 0;
+            if (lane == 0) it = atomicAdd(a.queue, 1);
+            it = __shfl_sync(0xffffffffu, it, 0);
+            if (it < r_gu) {
+                // gate_up range: every piece inside one (tile, row block) unit is an item
+                const int64_t f0 = range_start(it, c_gu, r_gu), f1 = range_start(it + 1, c_gu, r_gu);
+                for (int64_t f = f0; f < f1 && ok;) {
+                    const int64_t u = f / nch_gu;
+                    Item m;
+                    m.kind = 1;
+                    m.ti = (int)(u / rbg);
+                    m.rb = (int)(u % rbg);
+                    m.c0 = (int)(f - u * nch_gu);
+                    m.c1 = (int)min((int64_t)nch_gu, m.c0 + (f1 - f));
+                    const int64_t first = range_of(u * nch_gu, c_gu, r_gu);
+                    m.seg = (int)(it - first);
+                    m.cnt = (int)(range_of((u + 1) * nch_gu - 1, c_gu, r_gu) - first + 1);
+                    const int4 t = a.tiles[m.ti];
+                    m.expert = t.x;
+                    m.q0 = t.y;
+                    m.nrows = t.z;
+                    ok = publish(m) && stream(m);
+                    f += m.c1 - m.c0;
+                }
+            } else if (it < r_gu + n_dn) {
+                // down: (tile, segment, row block), so the first down items read
+                // the first h row blocks
+                const int64_t id = it - r_gu;
+                Item m;
+                m.kind = 0;
+                m.ti = (int)(id / (rbd * a.split.s_dn));
+                const int rem = (int)(id % (rbd * a.split.s_dn));
+                m.rb = rem % rbd;
+                m.seg = rem / rbd;
+                m.c0 = m.seg * a.split.l_dn;
+                m.c1 = min(nch_dn, m.c0 + a.split.l_dn);
+                m.cnt = a.split.s_dn;
+                const int4 t = a.tiles[m.ti];
+                m.expert = t.x;
+                m.q0 = t.y;
+                m.nrows = t.z;
+                ok = publish(m) && stream(m);
+            } else {
+                Item m{};
+                m.kind = -1;
+                publish(m);
+                break;
+            }
             if (!ok) break;
-            int nxt = 0;
-            if (lane == 0) nxt = atomicAdd(queue, 1);
-            it = __shfl_sync(0xffffffffu, nxt, 0);
         }
         asm volatile("cp.async.wait_all;" ::: "memory");   // no copy of this warp outlives the CTA
-    } else {
-        // ------------------------------------------------ consumer warps
-        const SelConst k = sel_const_regs();
-        // AND of every lut word used: a valid scale's lut word has bit 31 set, an
-        // invalid one is 0, so the AND is 0 exactly when a bad scale byte was read.
-        uint32_t lut_and = 0xFFFFFFFFu;
-        uint32_t qbase = 0;
-        for (int n = 0;; ++n) {
-            // one thread waits for the next item and decides whether to stop; the
-            // barrier hands both to every consumer warp, so all four always take
-            // the same path and meet at the same barriers
-            const uint32_t islot = (uint32_t)n % kInfo;
-            if (tid == 0) {
-                const bool ok = mbar_wait(smem_u32(&sh.info_full[islot]), (uint32_t)(n / kInfo) & 1u, abort);
-                sh.cur_info = ok ? sh.info[islot] : make_int4(-1, 0, 0, 0);
-                sh.stop = !ok || *abort;
-            }
-            consumer_sync();
-            const int4 info = sh.cur_info;
-            if (sh.stop || info.x < 0) break;
-            if (info.x < n_gu) {
-                const int rb = info.x % gu.row_blocks;
-                if (info.w <= 8) run_item<true, 1>(gu, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
-                else run_item<true, 2>(gu, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
-                qbase += (uint32_t)(gu.K / kChunk);
-                // run_item ends with a consumer barrier after its h stores
-                if (tid == 0) {
-                    __threadfence();
-                    atomicAdd(gu_done + info.x / gu.row_blocks, 1);
-                }
-            } else {
-                const int rb = (info.x - n_gu) % dn.row_blocks;
-                if (info.w <= 8) run_item<false, 1>(dn, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
-                else run_item<false, 2>(dn, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
-                qbase += (uint32_t)(dn.K / kChunk);
-                // The last of the n_tiles items that wrote rows [32 rb, 32 rb + 32) of
-                // the pair slots sums them into y (fixed j order per token).  run_item
-                // ended with a consumer barrier after the stage stores, so one fence by
-                // the counting thread releases all of them (fences are cumulative).
-                if (tid == 0) {
-                    __threadfence();
-                    sh.last_flag = (atomicAdd(dn.counters + rb, 1) == n_tiles - 1);
-                }
-                consumer_sync();
-                if (sh.last_flag) {
-                    __threadfence();
-                    for (int i = tid; i < dn.T * 32; i += kWarps * 32) {
-                        const int t = i >> 5, m = rb * 32 + (i & 31);
-                        float s = 0.f;
-                        for (int j = 0; j < dn.k; ++j) {
-                            const int ej = __ldg(dn.ids + t * dn.k + j);
-                            if ((unsigned)ej < (unsigned)dn.E) s += __ldcg(dn.stage + (int64_t)(t * dn.k + j) * dn.H + m);
-                        }
-                        __nv_bfloat16 yb = __float2bfloat16_rn(s);
-                        dn.y[(int64_t)t * dn.H + m] = *reinterpret_cast<uint16_t*>(&yb);
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t q = 0;
+            for (int n = 0;; ++n) {
+                const uint32_t islot = (uint32_t)n % kInfo;
+                if (!mbar_wait(smem_u32(&sh.info_full[islot]), ((uint32_t)n / kInfo) & 1u, abort)) break;
+                const Item m = get_item(sh.info[islot]);
+                mbar_arrive(smem_u32(&sh.info_empty[islot]));
+                if (m.kind < 0) break;
+                const uint32_t b = (uint32_t)n & 1u;
+                if (!mbar_wait(smem_u32(&sh.d_empty[b]), (((uint32_t)n >> 1) & 1u) ^ 1u, abort)) break;
+                tc_fence_after();
+                bool ok = true;
+                for (int ch = m.c0; ch < m.c1; ++ch, ++q) {
+                    const uint32_t slot = q % kSlots, st = q & 1u;
+                    if (!mbar_wait(smem_u32(&sh.full[slot]), (q / kSlots) & 1u, abort) ||
+                        !mbar_wait(smem_u32(&sh.a_full[st]), (q >> 1) & 1u, abort)) {
+                        ok = false;
+                        break;
                     }
-                    if (tid == 0) dn.counters[rb] = 0;
+                    tc_fence_after();
+                    fence_proxy_async_smem();   // activation rows came by cp.async (generic proxy)
+                    const uint64_t bd = smem_desc_sw128(ring_addr + slot * kSlotBytes + kBOff);
+#pragma unroll
+                    for (uint32_t t = 0; t < 4; ++t)
+                        umma_mxf8_ts(tm + kColD + 16 * b, tm + kColA + 32 * st + 8 * t, bd + 2 * t,
+                                     idesc_mxf8_e4m3(kRows, kN, t, t), tm + kColSfa + 4 * st, tm + kColSfb + 4 * st,
+                                     (ch != m.c0 || t != 0) ? 1u : 0u);
+                    umma_commit(smem_u32(&sh.a_empty[st]));
+                    umma_commit(smem_u32(&sh.empty[slot]));
                 }
-                consumer_sync();
+                if (!ok) break;
+                umma_commit(smem_u32(&sh.d_full[b]));
             }
-            if (lane == 0) mbar_arrive(smem_u32(&sh.info_empty[islot]));
+            // every MMA of this CTA has completed before its tensor memory is freed
+            umma_commit(smem_u32(&sh.drain));
+            volatile int never = 0;
+            if (!mbar_wait(smem_u32(&sh.drain), 0u, &never)) *abort = 1;
         }
-        if (lut_and == 0) flag_status(gu.status, MOE_W2_DEV_BAD_SCALE);
+    } else if (warp == kFinisherWarp) {
+        // ------------------------------------------------ finisher
+        for (int n = 0;; ++n) {
+            const uint32_t islot = (uint32_t)n % kInfo;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.info_full[islot]), ((uint32_t)n / kInfo) & 1u, abort)))
+                break;
+            const Item m = get_item(sh.info[islot]);
+            if (m.kind < 0) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.info_empty[islot]));
+                break;
+            }
+            // released only after this wait: the consumers cannot arrive for the
+            // item kInfo places later before this phase of epi[islot] is seen
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.epi[islot]), ((uint32_t)n / kInfo) & 1u, abort)))
+                break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.info_empty[islot]));
+            if (m.kind == 1) finish_gate_up(a, m);
+        }
+    } else {
+        // ------------------------------------------------ consumers
+        const uint32_t lut = opaque(kLut), m33 = opaque(0x33333333u);
+        const int m = tid;   // weight row of the item
+        const uint32_t tq = tm + ((uint32_t)(32 * warp) << 16);
+        const uint32_t swz = ((uint32_t)m >> 2) & 1u;   // 32B swizzle of this code row
+        uint32_t q = 0, bad_scale = 0;
+        uint4 sfa_g = make_uint4(0, 0, 0, 0), sfb_g = make_uint4(0, 0, 0, 0);   // scale words of the group
+        Item prev{};
+        int prev_n = 0, have_prev = 0;
+        for (int n = 0;; ++n) {
+            const uint32_t islot = (uint32_t)n % kInfo;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.info_full[islot]), ((uint32_t)n / kInfo) & 1u, abort)))
+                break;
+            const Item cur = get_item(sh.info[islot]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.info_empty[islot]));
+            if (cur.kind < 0) break;
+            if (have_prev && cur.kind == 0) {   // before blocking on a down item's data
+                epilogue_store(a, sh, tq, prev, prev_n, abort);
+                have_prev = 0;
+            }
+            const int G = cur.kind == 1 ? a.split.g_gu : a.split.g_dn;
+            bool ok = true;
+            for (int ch = cur.c0; ch < cur.c1; ++ch, ++q) {
+                const uint32_t slot = q % kSlots, st = q & 1u;
+                const bool got = mbar_wait(smem_u32(&sh.full[slot]), (q / kSlots) & 1u, abort) &&
+                                 mbar_wait(smem_u32(&sh.a_empty[st]), ((q >> 1) & 1u) ^ 1u, abort);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sb = ring_addr + slot * kSlotBytes;
+                const uint4 w0 = lds_u4(sb + m * 32 + (swz << 4));
+                const uint4 w1 = lds_u4(sb + m * 32 + ((swz ^ 1u) << 4));
+                const int gi = ch & (G - 1);
+                if (gi == 0 || ch == cur.c0) {
+                    const uint32_t sfs = sf_addr + slot * kSfSlotBytes;
+                    sfa_g = lds_u4(sfs + m * 16);
+                    sfb_g = lds_u4(sfs + kSfbOff + (lane & 15) * 16);
+                }
+                uint32_t sfa = gi == 0 ? sfa_g.x : gi == 1 ? sfa_g.y : gi == 2 ? sfa_g.z : sfa_g.w;
+                const uint32_t sfb = gi == 0 ? sfb_g.x : gi == 1 ? sfb_g.y : gi == 2 ? sfb_g.z : sfb_g.w;
+                const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                uint32_t r[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t mp = wd[i] & m33, m2 = (wd[i] >> 2) & m33;
+                    r[4 * i + 0] = prmt(lut, lut, mp);          // codes 0, 2, 4, 6
+                    r[4 * i + 1] = prmt(lut, lut, mp >> 16);    // codes 8, 10, 12, 14
+                    r[4 * i + 2] = prmt(lut, lut, m2);          // codes 1, 3, 5, 7
+                    r[4 * i + 3] = prmt(lut, lut, m2 >> 16);    // codes 9, 11, 13, 15
+                }
+                if (scale_word_suspect(sfa)) {
+                    // an invalid scale byte: that block counts as zero
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t sbyte = (sfa >> (8 * t)) & 0xFFu;
+                        if (sbyte - 1u > 251u) {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) r[8 * t + c] = 0u;
+                            sfa = (sfa & ~(0xFFu << (8 * t))) | (127u << (8 * t));
+                            bad_scale = 1;
+                        }
+                    }
+                }
+                tmem_st_stage(tq + kColA + 32 * st, r, tq + kColSfa + 4 * st + warp, sfa, tq + kColSfb + 4 * st, sfb);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.a_full[st]));
+                if (ch == cur.c0 && have_prev) {
+                    epilogue_store(a, sh, tq, prev, prev_n, abort);
+                    have_prev = 0;
+                }
+            }
+            if (!ok) break;
+            prev = cur;
+            prev_n = n;
+            have_prev = 1;
+        }
+        if (have_prev && !*abort) epilogue_store(a, sh, tq, prev, prev_n, abort);
+        if (bad_scale) flag_status(a.status, MOE_W2_DEV_BAD_SCALE);
     }
-    if (tid == 0 && *abort) flag_status(gu.status, kDevPipelineTimeout);
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tm, kTmemCols);
+    }
+    if (tid == 0 && *abort) flag_status(a.status, kDevPipelineTimeout);
 }
 
 }  // namespace
@@ -469,63 +669,72 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     (void)x;
     const int32_t E = w.num_experts, H = w.hidden, I = w.inter;
     const int64_t P = (int64_t)T * k;
-    constexpr int kDyn = kRingBytes + 128;
+    constexpr int kDyn = kRingBytes + 1024;
     static int occ = 0;
     if (occ == 0) {
         cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_layer_kernel, kThreads, kDyn);
+        // all of the unified L1 as shared memory: four CTAs per SM (their tensor
+        // memory, 4 x 128 columns, fills the SM's)
+        e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        occ = std::max(occ, 1);
+        // CTAs per SM from this kernel's own resources (the occupancy query
+        // reports one CTA per SM for any kernel that allocates tensor memory,
+        // although four 128-column CTAs do run side by side)
+        cudaFuncAttributes fa{};
+        if ((e = cudaFuncGetAttributes(&fa, decode_layer_kernel)) != cudaSuccess) return e;
+        int dev = 0, smem_sm = 0, resv = 0, regs_sm = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess)
+            return e;
+        const int by_smem = smem_sm / (kDyn + (int)fa.sharedSizeBytes + resv);
+        const int regs_cta = ((fa.numRegs * 32 + 255) / 256) * 256 * (kThreads / 32);
+        const int by_regs = regs_cta > 0 ? regs_sm / regs_cta : 1;
+        occ = std::max(1, std::min({by_smem, by_regs, (int)(512 / kTmemCols)}));
     }
-    const int64_t tiles = max_tiles(P, E, true);
+    const int64_t mt = max_tiles(P, E, true);
 
-    DecArgs gp{};
-    gp.codes = w.w13_codes;
-    gp.scales = w.w13_scales;
-    gp.K = H;
-    gp.rows_per_expert = 2 * I;
-    gp.I = I;
-    gp.H = H;
-    gp.T = T;
-    gp.k = k;
-    gp.E = E;
-    gp.row_blocks = I / 16;
-    gp.tiles = ws.tiles;
-    gp.tile_count = ws.tile_count;
-    gp.sorted = ws.sorted;
-    gp.weights = weights;
-    gp.ids = ids;
-    gp.act = ws.xa;
-    gp.h_t16 = ws.h;
-    gp.stage = ws.stage;
-    gp.counters = ws.counters;
-    gp.y = y;
-    gp.status = status;
+    LayerArgs a{};
+    a.w13_scales = w.w13_scales;
+    a.w2_scales = w.w2_scales;
+    a.H = H;
+    a.I = I;
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.split = ws.split;
+    // scale words move in 16-byte groups (4 chunks) where rows and the base allow it
+    a.split.g_gu = (H % 512 == 0 && (reinterpret_cast<uintptr_t>(w.w13_scales) & 15) == 0) ? 4 : 2;
+    a.split.g_dn = (I % 512 == 0 && (reinterpret_cast<uintptr_t>(w.w2_scales) & 15) == 0) ? 4 : 2;
+    a.P = P;
+    a.tiles = ws.tiles;
+    a.tile_count = ws.tile_count;
+    a.sorted = ws.sorted;
+    a.weights = weights;
+    a.ids = ids;
+    a.x8 = ws.x8;
+    a.sx8 = ws.sx8;
+    a.h8 = ws.h8;
+    a.sh8 = ws.sh8;
+    a.gu_part = ws.gu_part;
+    a.stage = ws.stage;
+    a.gu_seg = ws.counters;                    // zeroed by the permutation kernel
+    a.queue = a.gu_seg + mt * (I / 64);
+    a.y = y;
+    a.status = status;
 
-    DecArgs dp = gp;
-    dp.codes = w.w2_codes;
-    dp.scales = w.w2_scales;
-    dp.K = I;
-    dp.rows_per_expert = H;
-    dp.row_blocks = H / 32;
-    dp.act = ws.h;
-    int32_t* gu_done = ws.counters + H / 32;   // [tiles], zeroed by the permutation kernel
-    int32_t* queue = gu_done + tiles;          // item queue, zeroed by the permutation kernel
-
-    // code tiles: 64 bytes (256 codes) x 16 rows (gate_up: gate and up halves
-    // separately) or x 32 rows (down)
+    // code tiles: 32 bytes (128 codes) x 64 rows (gate_up: gate and up halves
+    // separately) or x 128 rows (down), 32B-swizzled
     CUtensorMap gu_map, dn_map;
-    cudaError_t e = make_tmap_2d(&gu_map, w.w13_codes, false, (int64_t)E * 2 * I, H / 4, 64, 16, 0);
+    cudaError_t e = make_tmap_2d(&gu_map, w.w13_codes, false, (int64_t)E * 2 * I, H / 4, 32, 64, 32);
     if (e != cudaSuccess) return e;
-    if ((e = make_tmap_2d(&dn_map, w.w2_codes, false, (int64_t)E * H, I / 4, 64, 32, 0)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&dn_map, w.w2_codes, false, (int64_t)E * H, I / 4, 32, 128, 32)) != cudaSuccess) return e;
 
-    // at most occupancy x SMs (all resident at once when the GPU is otherwise
-    // idle), and no more than the larger phase has items
-    const int64_t grid = std::min<int64_t>((int64_t)sm_count() * occ,
-                                           tiles * std::max<int64_t>(gp.row_blocks, dp.row_blocks));
+    const int grid = sm_count() * occ;
     if ((e = ev.record(1, s)) != cudaSuccess) return e;
-    if ((e = ev.record(2, s)) != cudaSuccess) return e;   // one kernel: phases 1 and 2 coincide
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
@@ -536,7 +745,10 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_layer_kernel, gu_map, dn_map, gp, dp, gu_done, queue);
+    if ((e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, gu_map, dn_map, a)) != cudaSuccess) return e;
+    if ((e = ev.record(2, s)) != cudaSuccess) return e;
+    // y = the slots of every token summed over j and the K segments of down
+    return launch_combine(ws.stage, ids, T, k, E, H, a.split.s_dn, P * H, true, y, s);
 }
 
 }  // namespace moe_w2

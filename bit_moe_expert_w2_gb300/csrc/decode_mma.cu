@@ -1,0 +1,533 @@
+// Decode path for the smallest steps (few pairs, see decode_use_mma): the 2-bit
+// planes of every active expert are streamed from HBM once per layer, expanded
+// to bf16 in registers and fed to mma.sync tensor-core MMAs.
+//
+// vLLM-Moet, page "vLLM-Moet wiki", section "The kernels": codes expanded in
+// registers through a byte-permute lookup table and fed to tensor-core MMAs;
+// section "FP4 recovery": decode is HBM-bound, the 2-bit read is the cost.  Page
+// "The v0.24.0 port", section "Benchmarks": tokens grouped by expert, so each
+// active expert's weights are read once per step however many tokens use it.
+// Page "The v0.24.0 port", "Deterministic unpermute" bullet: per-pair results
+// are placed in their own slot and summed over top_k in a fixed order.
+//
+// Why mma.sync here and not tcgen05: with N = a handful of pairs, every
+// tcgen05.mma (M=128, K=16) of a CTA costs ~105 cycles whatever N is (measured
+// on GB300), which caps a CTA far below HBM rate, while mma.sync m16n8k16 keeps
+// the weights in registers and reaches the full tensor rate with enough warps.
+// The expansion is integer work on the ALU pipe (two masks, five shifts and
+// eight byte-permutes per 16 codes) plus two multiply-adds on the FMA pipe.
+//
+// One kernel runs the whole layer (gate_up, then down with the combine).  Work
+// item = (tile of <= 16 pairs of one expert, 32 weight rows).  Each CTA has four
+// consumer warps that split K of an item (256-element chunks, round robin) and
+// reduce in shared memory in warp order, and one producer warp that runs ahead
+// through the CTA's items: it takes items from a global queue, publishes each
+// item's tile through a small shared-memory ring, and streams every chunk's code
+// bytes (TMA: 32 rows x 64 bytes) and scale bytes (one 8-byte cp.async per row)
+// into a ring of chunk slots.  Consumers only wait on a slot's barrier, read it
+// from shared memory and release it, so the loads of the next item overlap the
+// end of the current one.
+//
+// Per 256-wide K chunk a row is 64 code bytes; thread c of a quad owns bytes
+// [16c, 16c+16), i.e. four 16-code words; MMA (word i, r) takes codes (r, r+4)
+// and (r+8, r+12) of word i from every thread of the quad, which is what the
+// T16 activation layout stores next to each other (one 64-bit load per B
+// fragment).  gate_up: m-tile t = gate rows n0+8t.. (A rows 0-7) and the
+// matching up rows (A rows 8-15), so gate and up of one (row, pair) meet in one
+// thread for the SiLU(gate)*up epilogue.  down: 32 consecutive rows of W_down;
+// the epilogue multiplies by the router weight and writes the pair's fp32 slot;
+// the last CTA to finish a 32-row block of y sums the k slots of every token in
+// j order and writes y (counter per row block, reset by the permutation kernel).
+#include <algorithm>
+
+#include "tc.cuh"
+
+namespace moe_w2 {
+
+namespace {
+
+#ifndef MOE_W2_DEC_MIN_CTAS
+#define MOE_W2_DEC_MIN_CTAS 4        // CTAs per SM the register budget is sized for
+#endif
+constexpr int kChunk = 256;          // K elements per chunk
+constexpr int kWarps = 4;            // consumer warps
+constexpr int kThreads = (kWarps + 1) * 32;   // + the producer warp
+constexpr int kMaxNT = 2;            // n-tiles of 8 pairs per item (tiles of <= 16 pairs)
+constexpr int kSlots = 16;           // chunk slots (four per consumer warp; a power of two)
+constexpr uint32_t kSlotCodeBytes = 32 * 64;   // 32 rows x 64 code bytes
+constexpr uint32_t kSlotScaleBytes = 32 * 8;   // 32 rows x 8 UE8M0 bytes
+constexpr uint32_t kSlotBytes = kSlotCodeBytes + kSlotScaleBytes;   // a multiple of 128
+constexpr uint32_t kRingBytes = kSlots * kSlotBytes;
+constexpr int kInfo = 16;            // published items in flight
+constexpr uint32_t kConsumerBarrier = 1;       // named barrier id of the consumer warps
+
+struct DecArgs {
+    const uint8_t* codes;      // [E][rows_per_expert][K/4]
+    const uint8_t* scales;     // [E][rows_per_expert][K/32]
+    int32_t K;
+    int32_t rows_per_expert;
+    int32_t I;
+    int32_t H;
+    int32_t T;
+    int32_t k;
+    int32_t E;
+    int32_t row_blocks;
+    const int4* tiles;
+    const int32_t* tile_count;
+    const int32_t* sorted;
+    const float* weights;
+    const int32_t* ids;
+    const uint16_t* act;       // B rows: x_t16 per token (gate_up) or h_t16 per pair (down)
+    uint16_t* h_t16;           // gate_up output [P][I]
+    float* stage;              // down output [P][H]
+    int32_t* counters;         // down: per 32-row block of y
+    uint16_t* y;
+    uint32_t* status;
+};
+
+struct SharedState {
+    uint64_t full[kSlots];      // producer -> consumers: slot filled (expect_tx arrival + 32 cp.async arrivals)
+    uint64_t empty[kSlots];     // consumer warp -> producer: slot read
+    uint64_t info_full[kInfo];  // producer -> consumers: item published
+    uint64_t info_empty[kInfo]; // consumer warps -> producer: item finished
+    int4 info[kInfo];           // (item index, or -1 at the end; expert; first slot; pairs)
+    uint2 lut[256];
+    float red[kWarps][2][kMaxNT][32][4];
+    int4 cur_info;              // the item the consumer warps work on
+    int last_flag;
+    int stop;
+    int abort_flag;
+};
+
+__device__ __forceinline__ uint32_t ld_acquire(const int32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void consumer_sync()
+{
+    asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrier), "n"(kWarps * 32) : "memory");
+}
+__device__ __forceinline__ uint32_t word_of(const uint4& q, int i)
+{
+    return i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
+}
+
+// One item on the consumer warps: K chunks ch = warp, warp + 4, ... from ring
+// slots (qbase + ch) % kSlots, then the split-K reduction and the epilogue.
+template <bool kGateUp, int NT>
+__device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, SharedState& sh, const uint8_t* ring,
+                                         uint32_t qbase, int q0, int nrows, int rb, uint32_t& lut_and)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    const int nch = p.K / kChunk;
+    // slot rows of the thread's four A rows: m-tile 0 -> (g, g+8), m-tile 1 -> (16+g, 24+g);
+    // gate_up slot rows 0-15 are gate rows n0.., 16-31 the matching up rows
+    int srow[4];
+    if (kGateUp) {
+        srow[0] = g;
+        srow[1] = 16 + g;
+        srow[2] = 8 + g;
+        srow[3] = 24 + g;
+    } else {
+        srow[0] = g;
+        srow[1] = 8 + g;
+        srow[2] = 16 + g;
+        srow[3] = 24 + g;
+    }
+    // B rows: pair j = 8*nt + g of the tile.  Columns past the tile's pairs read
+    // pair 0's row (always valid); their results are never stored.
+    const uint16_t* brow[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int j = nt * 8 + g < nrows ? nt * 8 + g : 0;
+        const int64_t br = kGateUp ? (int64_t)(__ldg(p.sorted + q0 + j) / p.k) : (int64_t)(q0 + j);
+        brow[nt] = p.act + br * p.K + c * 64;
+    }
+
+    float acc[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+
+    volatile int* abort = &sh.abort_flag;
+    for (int ch = warp; ch < nch; ch += kWarps) {
+        const uint32_t q = qbase + (uint32_t)ch;
+        const uint32_t slot = q % kSlots;
+        if (!mbar_wait(smem_u32(&sh.full[slot]), (q / kSlots) & 1u, abort)) break;
+        // plain (compiler-schedulable) shared loads: the wait above is a compiler barrier
+        const uint8_t* sp = ring + slot * kSlotBytes;
+        uint4 qw[4];
+        uint2 L[4][2];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            qw[a] = *reinterpret_cast<const uint4*>(sp + srow[a] * 64 + c * 16);
+            const uint8_t* sb = sp + kSlotCodeBytes + srow[a] * 8 + 2 * c;
+            L[a][0] = sh.lut[sb[0]];
+            L[a][1] = sh.lut[sb[1]];
+            lut_and &= L[a][0].x & L[a][1].x;
+        }
+        const uint16_t* bsrc[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) bsrc[nt] = brow[nt] + (int64_t)ch * kChunk;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint4 B0[NT], B1[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (kGateUp) {   // x in T16 order, written by an earlier launch: read-only path
+                    B0[nt] = __ldg(reinterpret_cast<const uint4*>(bsrc[nt] + i * 16));
+                    B1[nt] = __ldg(reinterpret_cast<const uint4*>(bsrc[nt] + i * 16 + 8));
+                } else {         // h, written by gate_up items of this launch: coherent loads
+                    B0[nt] = *reinterpret_cast<const uint4*>(bsrc[nt] + i * 16);
+                    B1[nt] = *reinterpret_cast<const uint4*>(bsrc[nt] + i * 16 + 8);
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const Masks ma = word_masks(word_of(qw[2 * mt], i), k), mb = word_masks(word_of(qw[2 * mt + 1], i), k);
+                const uint2 la = L[2 * mt][i >> 1], lb = L[2 * mt + 1][i >> 1];
+                uint32_t alo[4], ahi[4], blo[4], bhi[4];
+                selectors(ma, k, alo, ahi);
+                selectors(mb, k, blo, bhi);
+                uint32_t afrag[4][4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    afrag[r][0] = prmt(la.x, la.y, alo[r]);
+                    afrag[r][1] = prmt(lb.x, lb.y, blo[r]);
+                    afrag[r][2] = prmt(la.x, la.y, ahi[r]);
+                    afrag[r][3] = prmt(lb.x, lb.y, bhi[r]);
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint4& Bv = (r < 2) ? B0[nt] : B1[nt];
+                        mma_bf16_16816(acc[mt][nt], afrag[r], (r & 1) ? Bv.z : Bv.x, (r & 1) ? Bv.w : Bv.y);
+                    }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.empty[slot]));
+    }
+
+    // split-K reduction in warp order
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) sh.red[warp][mt][nt][lane][v] = acc[mt][nt][v];
+    consumer_sync();
+    // warp w finalises m-tile (w & 1), n-tile (w >> 1)
+    const int mt = warp & 1;
+    for (int nt = warp >> 1; nt < NT; nt += 2) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) s += sh.red[w][mt][nt][lane][e];
+            v[e] = s;
+        }
+        if (kGateUp) {
+            const int pos = t16_pos(rb * 16 + mt * 8 + g);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = nt * 8 + 2 * c + h;
+                if (j < nrows) {
+                    __nv_bfloat16 hb = __float2bfloat16_rn(silu_f(v[h]) * v[2 + h]);
+                    p.h_t16[(int64_t)(q0 + j) * p.I + pos] = *reinterpret_cast<uint16_t*>(&hb);
+                }
+            }
+        } else {
+            const int m = rb * 32 + mt * 16 + g;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = nt * 8 + 2 * c + h;
+                if (j < nrows) {
+                    const int pr = __ldg(p.sorted + q0 + j);
+                    const float wt = __ldg(p.weights + pr);
+                    p.stage[(int64_t)pr * p.H + m] = wt * v[h];
+                    p.stage[(int64_t)pr * p.H + m + 8] = wt * v[2 + h];
+                }
+            }
+        }
+    }
+    consumer_sync();
+}
+
+// One persistent grid runs the whole decode layer.  Items come from one queue:
+// indices [0, n_gu) are gate_up items (tile, 16 gate + 16 up rows), [n_gu, n_all)
+// down items (tile, 32 rows of y).  Each CTA's producer warp takes every item,
+// the first included, from a global counter, so only CTAs that are running hold
+// items.  A down item of tile t needs h of every row of t, so the producer waits
+// until the tile's gate_up counter reaches the number of gate_up row blocks
+// before it publishes the item; every gate_up index is handed out before any
+// down index and is held by a running CTA, so the waits always end (each is
+// still bounded and gives up with the pipeline-timeout status bit).  Which CTA
+// runs an item never changes its result.
+__global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS)
+decode_mma_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_constant__ CUtensorMap dn_map,
+                    DecArgs gu, DecArgs dn, int32_t* __restrict__ gu_done, int32_t* __restrict__ queue)
+{
+    __shared__ SharedState sh;
+    extern __shared__ uint8_t dyn_smem[];   // kRingBytes + 128 (aligned below)
+    // 128-byte aligned ring; offsetting the shared array itself keeps the
+    // pointer in the shared window (plain loads from it compile to shared loads)
+    const uint32_t pad = (128u - (smem_u32(dyn_smem) & 127u)) & 127u;
+    const uint8_t* ring = dyn_smem + pad;
+    const uint32_t ring_addr = smem_u32(dyn_smem) + pad;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int s = tid; s < 256; s += kThreads) {
+        ScaleLut l = make_lut((uint32_t)s);
+        sh.lut[s] = make_uint2(l.lut, l.lo);
+    }
+    if (tid == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(smem_u32(&sh.full[s]), 1 + 32);
+            mbar_init(smem_u32(&sh.empty[s]), 1);
+        }
+        for (int s = 0; s < kInfo; ++s) {
+            mbar_init(smem_u32(&sh.info_full[s]), 1);
+            mbar_init(smem_u32(&sh.info_empty[s]), kWarps);
+        }
+        sh.abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    volatile int* abort = &sh.abort_flag;
+
+    // Launched as a programmatic dependent of the permutation kernel: the setup
+    // above overlaps it; everything it writes (tiles, counters, x in T16 order)
+    // is read only after this wait.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int n_tiles = *gu.tile_count;
+    const int n_gu = n_tiles * gu.row_blocks;
+    const int n_all = n_gu + n_tiles * dn.row_blocks;
+
+    if (warp == kWarps) {
+        // ------------------------------------------------ producer warp
+        if (lane == 0) {
+            prefetch_tmap(&gu_map);
+            prefetch_tmap(&dn_map);
+        }
+        uint32_t q = 0;
+        int it = 0;
+        if (lane == 0) it = atomicAdd(queue, 1);
+        it = __shfl_sync(0xffffffffu, it, 0);
+        for (int n = 0;; ++n) {
+            const uint32_t islot = (uint32_t)n % kInfo;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(smem_u32(&sh.info_empty[islot]), ((uint32_t)(n / kInfo) & 1u) ^ 1u, abort);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            if (it >= n_all) {
+                if (lane == 0) {
+                    sh.info[islot] = make_int4(-1, 0, 0, 0);
+                    mbar_arrive(smem_u32(&sh.info_full[islot]));
+                }
+                break;
+            }
+            const bool is_gu = it < n_gu;
+            const DecArgs& P = is_gu ? gu : dn;
+            const int id = is_gu ? it : it - n_gu;
+            const int ti = id / P.row_blocks, rb = id % P.row_blocks;
+            const int4 tile = P.tiles[ti];
+            if (!is_gu && lane == 0 && (int)ld_acquire(gu_done + ti) < gu.row_blocks) {
+                const long long t0 = clock64();
+                while ((int)ld_acquire(gu_done + ti) < gu.row_blocks) {
+                    if (clock64() - t0 > kWaitLimitCycles) {
+                        *abort = 1;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+            }
+            if (__shfl_sync(0xffffffffu, *abort, 0)) break;
+            if (lane == 0) {
+                sh.info[islot] = make_int4(it, tile.x, tile.y, tile.z);
+                mbar_arrive(smem_u32(&sh.info_full[islot]));
+            }
+            // the item's rows: TMA rows, and this lane's scale row
+            const int64_t ebase = (int64_t)tile.x * P.rows_per_expert;
+            int64_t srow;
+            if (is_gu) srow = ebase + (lane < 16 ? rb * 16 + lane : P.I + rb * 16 + (lane - 16));
+            else srow = ebase + rb * 32 + lane;
+            const uint8_t* ssrc = P.scales + srow * (P.K / 32);
+            const int nch = P.K / kChunk;
+            for (int ch = 0; ch < nch; ++ch, ++q) {
+                const uint32_t slot = q % kSlots;
+                if (lane == 0) ok = mbar_wait(smem_u32(&sh.empty[slot]), ((q / kSlots) & 1u) ^ 1u, abort);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                const uint32_t fb = smem_u32(&sh.full[slot]);
+                const uint32_t dst = ring_addr + slot * kSlotBytes;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(fb, kSlotCodeBytes);
+                    if (is_gu) {
+                        tma_load_2d(dst, &gu_map, ch * 64, (int)(ebase + rb * 16), fb);
+                        tma_load_2d(dst + 16 * 64, &gu_map, ch * 64, (int)(ebase + P.I + rb * 16), fb);
+                    } else {
+                        tma_load_2d(dst, &dn_map, ch * 64, (int)(ebase + rb * 32), fb);
+                    }
+                }
+                cp_async8(dst + kSlotCodeBytes + lane * 8, ssrc + ch * 8);
+                cp_async_arrive_noinc(fb);
+            }
+            if (!ok) break;
+            int nxt = 0;
+            if (lane == 0) nxt = atomicAdd(queue, 1);
+            it = __shfl_sync(0xffffffffu, nxt, 0);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");   // no copy of this warp outlives the CTA
+    } else {
+        // ------------------------------------------------ consumer warps
+        const SelConst k = sel_const_regs();
+        // AND of every lut word used: a valid scale's lut word has bit 31 set, an
+        // invalid one is 0, so the AND is 0 exactly when a bad scale byte was read.
+        uint32_t lut_and = 0xFFFFFFFFu;
+        uint32_t qbase = 0;
+        for (int n = 0;; ++n) {
+            // one thread waits for the next item and decides whether to stop; the
+            // barrier hands both to every consumer warp, so all four always take
+            // the same path and meet at the same barriers
+            const uint32_t islot = (uint32_t)n % kInfo;
+            if (tid == 0) {
+                const bool ok = mbar_wait(smem_u32(&sh.info_full[islot]), (uint32_t)(n / kInfo) & 1u, abort);
+                sh.cur_info = ok ? sh.info[islot] : make_int4(-1, 0, 0, 0);
+                sh.stop = !ok || *abort;
+            }
+            consumer_sync();
+            const int4 info = sh.cur_info;
+            if (sh.stop || info.x < 0) break;
+            if (info.x < n_gu) {
+                const int rb = info.x % gu.row_blocks;
+                if (info.w <= 8) run_item<true, 1>(gu, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
+                else run_item<true, 2>(gu, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
+                qbase += (uint32_t)(gu.K / kChunk);
+                // run_item ends with a consumer barrier after its h stores
+                if (tid == 0) {
+                    __threadfence();
+                    atomicAdd(gu_done + info.x / gu.row_blocks, 1);
+                }
+            } else {
+                const int rb = (info.x - n_gu) % dn.row_blocks;
+                if (info.w <= 8) run_item<false, 1>(dn, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
+                else run_item<false, 2>(dn, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
+                qbase += (uint32_t)(dn.K / kChunk);
+                // The last of the n_tiles items that wrote rows [32 rb, 32 rb + 32) of
+                // the pair slots sums them into y (fixed j order per token).  run_item
+                // ended with a consumer barrier after the stage stores, so one fence by
+                // the counting thread releases all of them (fences are cumulative).
+                if (tid == 0) {
+                    __threadfence();
+                    sh.last_flag = (atomicAdd(dn.counters + rb, 1) == n_tiles - 1);
+                }
+                consumer_sync();
+                if (sh.last_flag) {
+                    __threadfence();
+                    for (int i = tid; i < dn.T * 32; i += kWarps * 32) {
+                        const int t = i >> 5, m = rb * 32 + (i & 31);
+                        float s = 0.f;
+                        for (int j = 0; j < dn.k; ++j) {
+                            const int ej = __ldg(dn.ids + t * dn.k + j);
+                            if ((unsigned)ej < (unsigned)dn.E) s += __ldcg(dn.stage + (int64_t)(t * dn.k + j) * dn.H + m);
+                        }
+                        __nv_bfloat16 yb = __float2bfloat16_rn(s);
+                        dn.y[(int64_t)t * dn.H + m] = *reinterpret_cast<uint16_t*>(&yb);
+                    }
+                    if (tid == 0) dn.counters[rb] = 0;
+                }
+                consumer_sync();
+            }
+            if (lane == 0) mbar_arrive(smem_u32(&sh.info_empty[islot]));
+        }
+        if (lut_and == 0) flag_status(gu.status, MOE_W2_DEV_BAD_SCALE);
+    }
+    if (tid == 0 && *abort) flag_status(gu.status, kDevPipelineTimeout);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mma(const uint16_t* x, const int32_t* ids, const float* weights, const moe_w2_planes& w,
+                          int32_t T, int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status, cudaStream_t s,
+                          const PhaseEvents& ev)
+{
+    (void)x;
+    const int32_t E = w.num_experts, H = w.hidden, I = w.inter;
+    const int64_t P = (int64_t)T * k;
+    constexpr int kDyn = kRingBytes + 128;
+    static int occ = 0;
+    if (occ == 0) {
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_mma_kernel, kThreads, kDyn);
+        if (e != cudaSuccess) return e;
+        occ = std::max(occ, 1);
+    }
+    const int64_t tiles = max_tiles(P, E, true);
+
+    DecArgs gp{};
+    gp.codes = w.w13_codes;
+    gp.scales = w.w13_scales;
+    gp.K = H;
+    gp.rows_per_expert = 2 * I;
+    gp.I = I;
+    gp.H = H;
+    gp.T = T;
+    gp.k = k;
+    gp.E = E;
+    gp.row_blocks = I / 16;
+    gp.tiles = ws.tiles;
+    gp.tile_count = ws.tile_count;
+    gp.sorted = ws.sorted;
+    gp.weights = weights;
+    gp.ids = ids;
+    gp.act = ws.xa;
+    gp.h_t16 = ws.h;
+    gp.stage = ws.stage;
+    gp.counters = ws.counters;
+    gp.y = y;
+    gp.status = status;
+
+    DecArgs dp = gp;
+    dp.codes = w.w2_codes;
+    dp.scales = w.w2_scales;
+    dp.K = I;
+    dp.rows_per_expert = H;
+    dp.row_blocks = H / 32;
+    dp.act = ws.h;
+    int32_t* gu_done = ws.counters + H / 32;   // [tiles], zeroed by the permutation kernel
+    int32_t* queue = gu_done + tiles;          // item queue, zeroed by the permutation kernel
+
+    // code tiles: 64 bytes (256 codes) x 16 rows (gate_up: gate and up halves
+    // separately) or x 32 rows (down)
+    CUtensorMap gu_map, dn_map;
+    cudaError_t e = make_tmap_2d(&gu_map, w.w13_codes, false, (int64_t)E * 2 * I, H / 4, 64, 16, 0);
+    if (e != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&dn_map, w.w2_codes, false, (int64_t)E * H, I / 4, 64, 32, 0)) != cudaSuccess) return e;
+
+    // at most occupancy x SMs (all resident at once when the GPU is otherwise
+    // idle), and no more than the larger phase has items
+    const int64_t grid = std::min<int64_t>((int64_t)sm_count() * occ,
+                                           tiles * std::max<int64_t>(gp.row_blocks, dp.row_blocks));
+    if ((e = ev.record(1, s)) != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)kDyn;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // may start before the permutation ends
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, decode_mma_kernel, gu_map, dn_map, gp, dp, gu_done, queue)) != cudaSuccess)
+        return e;
+    return ev.record(2, s);   // the combine is inside the kernel: phase 3 is empty
+}
+
+}  // namespace moe_w2

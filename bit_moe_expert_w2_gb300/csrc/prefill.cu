@@ -431,7 +431,7 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
     tc_expert_gemm_kernel<false><<<(int)std::min<int64_t>(sms, max_items_d), kThreads, kSmemBytes, s>>>(hmap, c2map, dp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-    return launch_combine(ws.stage, ids, T, k, E, H, y, s);
+    return launch_combine(ws.stage, ids, T, k, E, H, 1, 0, false, y, s);
 }
 
 }  // namespace moe_w2

@@ -9,6 +9,7 @@
 //            the T16 layout the GEMM kernels read (TMA-friendly contiguous rows
 //            per expert)
 //   combine  y[t] = bf16(sum_{j=0..k-1} stage[t*k + j]) over valid pairs, j in order
+//            (decode: per slot also over the K segments of down, in order)
 #include <algorithm>
 #include <mutex>
 
@@ -47,28 +48,39 @@ __global__ void gather_t16_kernel(const uint16_t* __restrict__ x, const int32_t*
     }
 }
 
+// y[t] = bf16(sum over valid j, then over K segments, of stage[seg][t*k + j]).
+// Launched as a programmatic dependent of the kernel that writes stage: it waits
+// for that grid before reading (a no-op for an ordinary launch).
 __global__ void combine_kernel(const float* __restrict__ stage, const int32_t* __restrict__ ids, int32_t T,
-                               int32_t k, int32_t E, int32_t H, uint16_t* __restrict__ y)
+                               int32_t k, int32_t E, int32_t H, int32_t n_seg, int64_t seg_stride,
+                               uint16_t* __restrict__ y)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int per_row = H / 8;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)T * per_row;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t t = i / per_row;
         const int m = (int)(i % per_row) * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
-            const int e = __ldg(ids + t * k + j);
-            if ((unsigned)e >= (unsigned)E) continue;
-            const float4* src = reinterpret_cast<const float4*>(stage + (t * k + j) * H + m);
-            const float4 a = src[0], b = src[1];
-            acc[0] += a.x;
-            acc[1] += a.y;
-            acc[2] += a.z;
-            acc[3] += a.w;
-            acc[4] += b.x;
-            acc[5] += b.y;
-            acc[6] += b.z;
-            acc[7] += b.w;
+        uint32_t valid = 0;   // bit j: slot j has an expert (k <= 16)
+        for (int j = 0; j < k; ++j) valid |= (uint32_t)((unsigned)__ldg(ids + t * k + j) < (unsigned)E) << j;
+        // slots in (j, segment) order; unrolled so that several loads are in flight
+        const int nks = k * n_seg;
+#pragma unroll 4
+        for (int x = 0; x < nks; ++x) {
+            const int j = x / n_seg, sg = x - j * n_seg;
+            if ((valid >> j) & 1u) {
+                const float4* src = reinterpret_cast<const float4*>(stage + sg * seg_stride + (t * k + j) * H + m);
+                const float4 a = __ldcg(src), b = __ldcg(src + 1);
+                acc[0] += a.x;
+                acc[1] += a.y;
+                acc[2] += a.z;
+                acc[3] += a.w;
+                acc[4] += b.x;
+                acc[5] += b.y;
+                acc[6] += b.z;
+                acc[7] += b.w;
+            }
         }
         uint4 o;
         uint32_t* ow = &o.x;
@@ -113,6 +125,7 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, bool bf16, int64_t 
                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                           : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                          : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
                                                 : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -128,12 +141,20 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted, const int32_
 }
 
 cudaError_t launch_combine(const float* stage, const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t H,
-                           uint16_t* y, cudaStream_t s)
+                           int32_t n_seg, int64_t seg_stride, bool programmatic, uint16_t* y, cudaStream_t s)
 {
     const int64_t threads = (int64_t)T * (H / 8);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((threads + 255) / 256, (int64_t)sm_count() * 8));
-    combine_kernel<<<grid, 256, 0, s>>>(stage, ids, T, k, E, H, y);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, stage, ids, T, k, E, H, n_seg, seg_stride, y);
 }
 
 }  // namespace moe_w2

@@ -214,6 +214,89 @@ __device__ __forceinline__ void tmem_st32_sync(uint32_t taddr, const uint32_t (&
         : "memory");
 }
 
+// ------------------------------------------------------------------ block-scaled e4m3 (decode)
+//
+// tcgen05.mma kind::mxf8f6f4 with UE8M0 block scales, one scale per 32 K per
+// row of A and per row of B (scale_vec::1X), A read from tensor memory.  Layouts
+// measured on GB300 with an in-bounds probe of the instruction:
+//  - A (M = 128): lane m holds row m; column j, byte b holds K index 4j + b.
+//  - A scales: the scale of row m is read from lane m of the column
+//    (scale_A_tmem + m / 32), byte = a_sf_id.  So the warp owning lanes
+//    32w..32w+31 writes its rows' scale words into column scale_A_tmem + w.
+//  - B scales: the scale of B row n is read from lane n % 32 of column
+//    scale_B_tmem in the lane quadrant of the output row, byte = b_sf_id, so
+//    every quadrant holds a copy.
+// Instruction descriptor (block-scaled form): b_sf_id bits 4-5, A/B format bits
+// 7-9 / 10-12 (0 = e4m3), N >> 3 in bits 17-22, scale format bit 23 (1 = UE8M0),
+// M >> 4 in bits 24-28, a_sf_id bits 29-30; K-major A and B, dense, fp32 D.
+__host__ __device__ __forceinline__ uint32_t idesc_mxf8_e4m3(uint32_t M, uint32_t N, uint32_t a_sf, uint32_t b_sf)
+{
+    return (b_sf << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (a_sf << 29);
+}
+__device__ __forceinline__ void umma_mxf8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// 32 columns of A plus one column of A scales and one of B scales from this
+// warp's registers into its TMEM lane quadrant, completed before returning (the
+// registers are read until tcgen05.wait::st, so store and wait share one asm).
+__device__ __forceinline__ void tmem_st_stage(uint32_t ta, const uint32_t (&r)[32], uint32_t tsa, uint32_t sa,
+                                              uint32_t tsb, uint32_t sb)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+        "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%33], {%34};\n"
+        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%35], {%36};\n"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(ta),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(tsa), "r"(sa), "r"(tsb), "r"(sb)
+        : "memory");
+}
+
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (load and wait in one asm).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------------ non-bulk async copies
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+// The barrier gets one arrival once all of this thread's earlier cp.async copies
+// have landed (its expected count includes that arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // 1-D-in-rows byte tile copy: box {inner bytes, rows} of a 2-D uint8 tensor.
 __device__ __forceinline__ void tma_load_2d_u8(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
                                                uint32_t bar)
@@ -231,6 +314,6 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, bool bf16, int64_t 
 cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted, const int32_t* offsets, int32_t E, int32_t k,
                           int32_t H, int64_t P, uint16_t* xs, cudaStream_t s);
 cudaError_t launch_combine(const float* stage, const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t H,
-                           uint16_t* y, cudaStream_t s);
+                           int32_t n_seg, int64_t seg_stride, bool programmatic, uint16_t* y, cudaStream_t s);
 
 }  // namespace moe_w2

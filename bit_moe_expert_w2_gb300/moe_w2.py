@@ -22,6 +22,7 @@ DEV_BAD_EXPERT_ID = 1
 DEV_BAD_SCALE = 2
 DEV_BAD_NVFP4 = 4
 DECODE_MAX_TOKENS = 64
+DECODE_MMA_MAX_PAIRS = 32           # decode steps with at most this many pairs run decode_mma_kernel
 NOALLOC_WORKSPACE_BYTES = 4 << 20   # MOE_W2_NOALLOC_WORKSPACE_BYTES
 
 
@@ -35,6 +36,11 @@ class Planes(ctypes.Structure):
     _fields_ = [("w13_codes", ctypes.c_void_p), ("w13_scales", ctypes.c_void_p),
                 ("w2_codes", ctypes.c_void_p), ("w2_scales", ctypes.c_void_p),
                 ("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32)]
+
+
+def decode_kernel(T: int, top_k: int) -> str:
+    """Name of the kernel that runs the layer of a decode step (T <= DECODE_MAX_TOKENS)."""
+    return "decode_mma_kernel" if T * top_k <= DECODE_MMA_MAX_PAIRS else "decode_layer_kernel"
 
 
 def lib_path() -> str:

@@ -14,7 +14,7 @@ constexpr int kMaxDevices = 64;
 constexpr int32_t kPrefillTileRows = 256;   // pairs per prefill tile (tcgen05 N <= 256)
 constexpr int32_t kDecodeTileRows = 8;      // pairs per decode tile (MMA N = 16: hi and lo row per pair)
 constexpr int32_t kDecodeMmaTileRows = 16;  // pairs per tile of the mma.sync decode kernel
-constexpr int64_t kDecodeMmaMaxPairs = 32;  // steps with at most this many pairs take the mma.sync kernel
+constexpr int64_t kDecodeMmaMaxPairs = 16;  // steps with at most this many pairs take the mma.sync kernel
 constexpr int64_t kDecodeTargetItems = 1200; // down items per step that keep every CTA busy
 constexpr int64_t kDecodeMinRange = 4;       // gate_up range: chunks at least
 constexpr int64_t kDecodeMaxRanges = 1024;   // gate_up ranges at most, for a step with ceil(P/8) tiles

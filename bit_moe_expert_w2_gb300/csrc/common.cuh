@@ -28,10 +28,12 @@ __host__ __device__ __forceinline__ int t16_pos(int n) { return (n & ~15) | ((n 
 // (2^(s-127) = 2^(floor(log2 amax) - 7), so |v| < 256).  hi + lo equals v exactly
 // whenever |a| >= amax * 2^-9 (8 significant bits, as in bf16), and within
 // amax * 2^-17 otherwise.  Inside every group of 16 elements, stored byte p holds
-// element e4_elem(p): the code expansion emits per 16-code word the codes
-// 0,2,4,6 | 8,10,12,14 | 1,3,5,7 | 9,11,13,15, and B must follow the same K order.
-__host__ __device__ __forceinline__ int e4_elem(int p) { return ((p & 3) << 1) | (((p >> 2) & 1) << 3) | (p >> 3); }
-__host__ __device__ __forceinline__ int e4_pos(int e) { return ((e & 1) << 3) | (((e >> 3) & 1) << 2) | ((e >> 1) & 3); }
+// element e4_elem(p) = 4(p & 3) + (p >> 2): the code expansion turns a 16-code
+// word into four registers, register j holding codes j, j+4, j+8, j+12 in its
+// bytes, and TMEM column j byte b is K index 4j + b, so B follows the same
+// transposed K order.  The map is its own inverse.
+__host__ __device__ __forceinline__ int e4_elem(int p) { return ((p & 3) << 2) | ((p >> 2) & 3); }
+__host__ __device__ __forceinline__ int e4_pos(int e) { return ((e & 3) << 2) | ((e >> 2) & 3); }
 
 // UE8M0 byte of a 32-element activation block with maximum magnitude amax.
 __device__ __forceinline__ uint32_t act_scale_byte(float amax)

@@ -9,15 +9,16 @@
 // tokens use it.  Page "The v0.24.0 port", "Deterministic unpermute" bullet:
 // per-pair results are placed in their own slot and summed in a fixed order.
 //
-// Why block-scaled e4m3 (tcgen05.mma kind::mxf8f6f4, scale_vec::1X): a weight is
-// +-1 or +-4 times 2^(s-127) with one UE8M0 byte s per 32 K of a row, which is
-// an e4m3 value (0x38, 0x48, 0xB8, 0xC8) under an MX block scale.  The tensor
-// core applies s itself, so the expansion is one byte per code: per 16-code word
-// two masks, three shifts and four byte-permutes against one constant table
+// Why block-scaled MX operands (tcgen05.mma kind::mxf8f6f4, scale_vec::1X): a
+// weight is +-1 or +-4 times 2^(s-127) with one UE8M0 byte s per 32 K of a row,
+// which is an e2m1 value under an MX block scale.  The tensor core applies s
+// itself, so the expansion is one byte per code: A is fed as e2m1 in 8-bit
+// containers, where the byte of code c is (c << 4) | 0x08, so per 16-code word
+// it takes three masks, three shifts and four adds or ors, with no table
 // (folding s into bf16 instead takes eight byte-permutes plus per-block table
 // lookups).  Activations enter as two e4m3 rows each (act_split), which keeps
 // their bf16 precision.
-//
+
 // Work item = (tile of <= 8 pairs of one expert, 128 weight rows, K segment).
 // gate_up rows: 64 gate rows and the matching 64 up rows; down rows: 128 rows of
 // W_down.  Each CTA has six warps:
@@ -29,7 +30,7 @@
 //              every group of 4 (or 2) chunks the group's scale words of all
 //              rows, one 16-byte (8-byte) cp.async per row
 //   warps 0-3  consumers, one per TMEM lane quadrant and one thread per weight
-//              row: expand the row's 128 codes of a chunk to e4m3 and store them
+//              row: expand the row's 128 codes of a chunk to e2m1 bytes and store them
 //              with the row's scale word into TMEM, plus this quadrant's copy of
 //              the activation scale words
 //   warp 5     MMA issuer (one thread): 4 x tcgen05.mma (M=128, N=16, K=32) per
@@ -81,7 +82,6 @@ constexpr uint32_t kColSfa = 96;                     // stage s, quadrant w: col
 constexpr uint32_t kColSfb = 104;                    // stage s: column 104 + 4s
 // (scale-factor operands start on a 4-column boundary: an M = 128 tile's A
 // scales span 4 columns, one per lane quadrant)
-constexpr uint32_t kLut = 0xC8B84838u;               // e4m3 of +1, +4, -1, -4 (code 0..3)
 constexpr int32_t kHReady = 1 << 20;                 // added to a row block's counter once its h is written
 
 struct LayerArgs {
@@ -170,6 +170,39 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t saddr)
     uint32_t r;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(saddr) : "memory");
     return r;
+}
+
+// Position in a ring of N slots: slot q % N and phase bit (q / N) & 1 of the
+// running chunk count q, stepped without a division.
+template <uint32_t N>
+struct RingPos {
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ void step()
+    {
+        if (++slot == N) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// Four e2m1 container words from one word of 16 codes: byte b of r_j holds code
+// 4b + j as (c << 4) | 0x08 (c in bits 5:4, bit 3 set: +1, +4, -1, -4).  Per word
+// four and-or operations and three shifts; the compiler issues the two left
+// shifts as multiplies, so the work splits 5:2 between the ALU and FMA pipes
+// (measured instruction counts).
+__device__ __forceinline__ void expand_e2m1(uint32_t w, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+{
+    asm("{\n\t.reg .b32 t0, t1, t3;\n\t"
+        "shl.b32 t0, %4, 4;\n\t"
+        "lop3.b32 %0, t0, 0x30303030, 0x08080808, 0xEA;\n\t"   // (x & m) | c
+        "shl.b32 t1, %4, 2;\n\t"
+        "lop3.b32 %1, t1, 0x30303030, 0x08080808, 0xEA;\n\t"
+        "lop3.b32 %2, %4, 0x30303030, 0x08080808, 0xEA;\n\t"
+        "shr.b32 t3, %4, 2;\n\t"
+        "lop3.b32 %3, t3, 0x30303030, 0x08080808, 0xEA;\n\t}"
+        : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+        : "r"(w));
 }
 
 // Nonzero when a byte of the scale word s is outside [1, 252] (may also flag a
@@ -335,6 +368,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
         // Queue entries [0, r_gu) are gate_up ranges, then down items; every
         // gate_up range is handed out before any down item.
         uint32_t q = 0;
+        RingPos<kSlots> rp;
         int n = 0;
         bool ok = true;
         // publish one item; false when the pipeline gave up
@@ -416,10 +450,10 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 const int64_t row = gu ? 2 * (int64_t)tj + (lane & 1) : 2 * (int64_t)(m.q0 + j) + (lane & 1);
                 if (lane < kN && j < m.nrows) sfb_src = sact + row * (kact / 32);
             }
-            for (int ch = m.c0; ch < m.c1; ++ch, ++q) {
-                const uint32_t slot = q % kSlots;
+            for (int ch = m.c0; ch < m.c1; ++ch, ++q, rp.step()) {
+                const uint32_t slot = rp.slot;
                 int w = 1;
-                if (lane == 0) w = mbar_wait(smem_u32(&sh.empty[slot]), ((q / kSlots) & 1u) ^ 1u, abort);
+                if (lane == 0) w = mbar_wait(smem_u32(&sh.empty[slot]), rp.phase ^ 1u, abort);
                 if (!__shfl_sync(0xffffffffu, w, 0)) return false;
                 const uint32_t base = ring_addr + slot * kSlotBytes, fb = smem_u32(&sh.full[slot]);
                 const uint32_t sfbase = sf_addr + slot * kSfSlotBytes;
@@ -436,9 +470,9 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 for (int i = 0; i < 4; ++i)
                     if (bsrc[i] != nullptr) cp_async16(base + bdst[i], bsrc[i] + ch * 128);
                 // scale words move in groups of G chunks aligned to the row (16 or
-                // 8 bytes); a group is copied at its first chunk, or at the item's
-                // first chunk when the item starts inside it
-                if ((ch & (G - 1)) == 0 || ch == m.c0) {
+                // 8 bytes); every slot gets the group holding its chunk, so a
+                // consumer reads word ch % G of its own slot
+                {
                     const int gch = ch & ~(G - 1);
                     if (G == 4) {
 #pragma unroll
@@ -510,6 +544,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t q = 0;
+            RingPos<kSlots> rp;
             for (int n = 0;; ++n) {
                 const uint32_t islot = (uint32_t)n % kInfo;
                 if (!mbar_wait(smem_u32(&sh.info_full[islot]), ((uint32_t)n / kInfo) & 1u, abort)) break;
@@ -520,10 +555,9 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 if (!mbar_wait(smem_u32(&sh.d_empty[b]), (((uint32_t)n >> 1) & 1u) ^ 1u, abort)) break;
                 tc_fence_after();
                 bool ok = true;
-                for (int ch = m.c0; ch < m.c1; ++ch, ++q) {
-                    const uint32_t slot = q % kSlots, st = q & 1u;
-                    if (!mbar_wait(smem_u32(&sh.full[slot]), (q / kSlots) & 1u, abort) ||
-                        !mbar_wait(smem_u32(&sh.a_full[st]), (q >> 1) & 1u, abort)) {
+                for (int ch = m.c0; ch < m.c1; ++ch, ++q, rp.step()) {
+                    const uint32_t slot = rp.slot, st = q & 1u;
+                    if (!mbar_wait2(smem_u32(&sh.full[slot]), rp.phase, smem_u32(&sh.a_full[st]), (q >> 1) & 1u, abort)) {
                         ok = false;
                         break;
                     }
@@ -533,7 +567,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
 #pragma unroll
                     for (uint32_t t = 0; t < 4; ++t)
                         umma_mxf8_ts(tm + kColD + 16 * b, tm + kColA + 32 * st + 8 * t, bd + 2 * t,
-                                     idesc_mxf8_e4m3(kRows, kN, t, t), tm + kColSfa + 4 * st, tm + kColSfb + 4 * st,
+                                     idesc_mxf_e2m1_e4m3(kRows, kN, t, t), tm + kColSfa + 4 * st, tm + kColSfb + 4 * st,
                                      (ch != m.c0 || t != 0) ? 1u : 0u);
                     umma_commit(smem_u32(&sh.a_empty[st]));
                     umma_commit(smem_u32(&sh.empty[slot]));
@@ -568,12 +602,11 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
         }
     } else {
         // ------------------------------------------------ consumers
-        const uint32_t lut = opaque(kLut), m33 = opaque(0x33333333u);
         const int m = tid;   // weight row of the item
         const uint32_t tq = tm + ((uint32_t)(32 * warp) << 16);
         const uint32_t swz = ((uint32_t)m >> 2) & 1u;   // 32B swizzle of this code row
         uint32_t q = 0, bad_scale = 0;
-        uint4 sfa_g = make_uint4(0, 0, 0, 0), sfb_g = make_uint4(0, 0, 0, 0);   // scale words of the group
+        RingPos<kSlots> rp;
         Item prev{};
         int prev_n = 0, have_prev = 0;
         for (int n = 0;; ++n) {
@@ -590,10 +623,10 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
             }
             const int G = cur.kind == 1 ? a.split.g_gu : a.split.g_dn;
             bool ok = true;
-            for (int ch = cur.c0; ch < cur.c1; ++ch, ++q) {
-                const uint32_t slot = q % kSlots, st = q & 1u;
-                const bool got = mbar_wait(smem_u32(&sh.full[slot]), (q / kSlots) & 1u, abort) &&
-                                 mbar_wait(smem_u32(&sh.a_empty[st]), ((q >> 1) & 1u) ^ 1u, abort);
+            for (int ch = cur.c0; ch < cur.c1; ++ch, ++q, rp.step()) {
+                const uint32_t slot = rp.slot, st = q & 1u;
+                const bool got = mbar_wait2(smem_u32(&sh.full[slot]), rp.phase, smem_u32(&sh.a_empty[st]),
+                                            ((q >> 1) & 1u) ^ 1u, abort);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
@@ -602,23 +635,14 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 const uint32_t sb = ring_addr + slot * kSlotBytes;
                 const uint4 w0 = lds_u4(sb + m * 32 + (swz << 4));
                 const uint4 w1 = lds_u4(sb + m * 32 + ((swz ^ 1u) << 4));
-                const int gi = ch & (G - 1);
-                if (gi == 0 || ch == cur.c0) {
-                    const uint32_t sfs = sf_addr + slot * kSfSlotBytes;
-                    sfa_g = lds_u4(sfs + m * 16);
-                    sfb_g = lds_u4(sfs + kSfbOff + (lane & 15) * 16);
-                }
-                uint32_t sfa = gi == 0 ? sfa_g.x : gi == 1 ? sfa_g.y : gi == 2 ? sfa_g.z : sfa_g.w;
-                const uint32_t sfb = gi == 0 ? sfb_g.x : gi == 1 ? sfb_g.y : gi == 2 ? sfb_g.z : sfb_g.w;
+                const uint32_t sfs = sf_addr + slot * kSfSlotBytes + 4u * (uint32_t)(ch & (G - 1));
+                uint32_t sfa = lds_u32(sfs + m * 16);
+                const uint32_t sfb = lds_u32(sfs + kSfbOff + (lane & 15) * 16);
                 const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                 uint32_t r[32];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const uint32_t mp = wd[i] & m33, m2 = (wd[i] >> 2) & m33;
-                    r[4 * i + 0] = prmt(lut, lut, mp);          // codes 0, 2, 4, 6
-                    r[4 * i + 1] = prmt(lut, lut, mp >> 16);    // codes 8, 10, 12, 14
-                    r[4 * i + 2] = prmt(lut, lut, m2);          // codes 1, 3, 5, 7
-                    r[4 * i + 3] = prmt(lut, lut, m2 >> 16);    // codes 9, 11, 13, 15
+                    expand_e2m1(wd[i], r[4 * i + 0], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
                 }
                 if (scale_word_suspect(sfa)) {
                     // an invalid scale byte: that block counts as zero

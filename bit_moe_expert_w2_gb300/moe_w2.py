@@ -22,8 +22,8 @@ DEV_BAD_EXPERT_ID = 1
 DEV_BAD_SCALE = 2
 DEV_BAD_NVFP4 = 4
 DECODE_MAX_TOKENS = 64
-DECODE_MMA_MAX_PAIRS = 32           # decode steps with at most this many pairs run decode_mma_kernel
-NOALLOC_WORKSPACE_BYTES = 4 << 20   # MOE_W2_NOALLOC_WORKSPACE_BYTES
+DECODE_MMA_MAX_PAIRS = 16           # decode steps with at most this many pairs run decode_mma_kernel
+NOALLOC_WORKSPACE_BYTES = 8 << 20   # MOE_W2_NOALLOC_WORKSPACE_BYTES
 
 
 class MoeW2Error(RuntimeError):

@@ -153,7 +153,7 @@ moe_w2_status moe_w2_forward_traced(const void *x_bf16, const int32_t *topk_ids,
  * the library's device code holds it until the process exits.
  *   - Sizes whose moe_w2_forward_workspace_size() exceeds
  *     MOE_W2_NOALLOC_WORKSPACE_BYTES return MOE_W2_ERR_WORKSPACE and enqueue
- *     nothing (at H=6144, I=2048, E=256, top_k=8 that is T > 4).
+ *     nothing (at H=6144, I=2048, E=256, top_k=8 that is T > 9).
  *   - The first call on each device looks up the array's address
  *     (cudaGetSymbolAddress, with that device current) and keeps it; make that
  *     first call before any stream capture starts.
@@ -161,7 +161,7 @@ moe_w2_status moe_w2_forward_traced(const void *x_bf16, const int32_t *topk_ids,
  *     the same time race: order them (e.g. issue them on one stream).
  *   - Nothing in the array needs to start at zero.
  */
-#define MOE_W2_NOALLOC_WORKSPACE_BYTES (4u << 20)
+#define MOE_W2_NOALLOC_WORKSPACE_BYTES (8u << 20)
 moe_w2_status moe_w2_forward_noalloc(const void *x_bf16, const int32_t *topk_ids, const float *topk_weights,
                                      const moe_w2_planes *w, int32_t T, int32_t top_k, void *y_bf16,
                                      uint32_t *dev_status, void *stream);

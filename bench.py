@@ -361,7 +361,7 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
         # one kernel streams the w13 and w2 planes of every active expert; its
         # time is phase 1 (phase 2: the combine kernel, empty when the layer
         # kernel combines itself)
-        kname = moe_w2.decode_kernel(T, k)
+        kname = moe_w2.decode_kernel(T, k, H, I)
         layer_kernel_ms = phase_ms[1]
         achieved = plane_bytes / (layer_kernel_ms / 1e3) / 1e9
         res["roofline"] = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
@@ -389,7 +389,7 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
     res["wall_s"] = round(wall, 3)
     # decode: permute (+ x as e4m3 rows), the layer kernel (gate_up, down), combine;
     # prefill: permute, gather, gate_up, down, combine
-    res["kernels_per_step"] = (2 if moe_w2.decode_kernel(T, k) == "decode_mma_kernel" else 3) if decode else 5
+    res["kernels_per_step"] = (2 if moe_w2.decode_kernel(T, k, H, I) == "decode_mma_kernel" else 3) if decode else 5
 
     # end to end: pinned host inputs -> device -> forward -> y back to pinned host
     hx = [torch.from_numpy(b[0].view(np.int16)).pin_memory() for b in batches]

@@ -92,15 +92,19 @@ DecodeSplit decode_split(int64_t P, int32_t E, int32_t H, int32_t I)
     d.l_dn = (int32_t)((nch_dn + want - 1) / want);
     d.l_dn = (d.l_dn + 3) & ~3;   // segments start on a scale-word group (4 chunks = 16 scale bytes per row)
     d.s_dn = (nch_dn + d.l_dn - 1) / d.l_dn;
-    d.g_gu = d.g_dn = 2;
     return d;
 }
 
-bool decode_use_mma(int64_t P) { return P <= kDecodeMmaMaxPairs; }
+// The block-scaled kernel loads weight-row scale groups by TMA, whose rows
+// (H/32, I/32 bytes) must be multiples of 16 bytes.
+bool decode_use_mma(int64_t P, int32_t H, int32_t I)
+{
+    return P <= kDecodeMmaMaxPairs || H % 512 != 0 || I % 512 != 0;
+}
 
 int64_t decode_counter_count(int64_t P, int32_t E, int32_t H, int32_t I)
 {
-    if (decode_use_mma(P)) return H / 32 + max_tiles(P, E, true) + 1;   // row blocks of y, tiles, queue
+    if (decode_use_mma(P, H, I)) return H / 32 + max_tiles(P, E, true) + 1;   // row blocks of y, tiles, queue
     const int64_t mt = max_tiles(P, E, true);
     return mt * (I / 64) + 1;
 }
@@ -124,7 +128,7 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
     w.active_count = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * 2));
     w.tile_count = w.active_count + 1;
     w.tiles = reinterpret_cast<int4*>(take(sizeof(int4) * max_tiles(P, E, decode)));
-    if (decode && decode_use_mma(P)) {
+    if (decode && decode_use_mma(P, H, I)) {
         w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * decode_counter_count(P, E, H, I)));
         w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * T * H));
         w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
@@ -207,7 +211,7 @@ moe_w2_status moe_w2_forward_traced(const void* x_bf16, const int32_t* topk_ids,
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MOE_W2_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(x_bf16) & 15) != 0 || (reinterpret_cast<uintptr_t>(y_bf16) & 15) != 0 ||
         (reinterpret_cast<uintptr_t>(w->w13_codes) & 15) != 0 || (reinterpret_cast<uintptr_t>(w->w2_codes) & 15) != 0 ||
-        (reinterpret_cast<uintptr_t>(w->w13_scales) & 7) != 0 || (reinterpret_cast<uintptr_t>(w->w2_scales) & 7) != 0)
+        (reinterpret_cast<uintptr_t>(w->w13_scales) & 15) != 0 || (reinterpret_cast<uintptr_t>(w->w2_scales) & 15) != 0)
         return MOE_W2_ERR_INVALID_ARG;
     const int32_t E = w->num_experts, H = w->hidden, I = w->inter;
     Workspace ws = carve_workspace(workspace, T, top_k, E, H, I);
@@ -223,7 +227,7 @@ moe_w2_status moe_w2_forward_traced(const void* x_bf16, const int32_t* topk_ids,
     for (int i = 0; i < 4; ++i) ev.e[i] = phase_events ? static_cast<cudaEvent_t>(phase_events[i]) : nullptr;
     if (ev.record(0, s) != cudaSuccess) return MOE_W2_ERR_CUDA;
     const int64_t P = (int64_t)T * top_k;
-    const bool mma = decode && decode_use_mma(P);
+    const bool mma = decode && decode_use_mma(P, H, I);
     cudaError_t e = launch_permute(topk_ids, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active, ws.active_count,
                                    ws.tiles, ws.tile_count,
                                    !decode ? kPrefillTileRows : mma ? kDecodeMmaTileRows : kDecodeTileRows,

@@ -228,12 +228,11 @@ struct DecodeSplit {
     int32_t s_gu;         // gate_up: contributing items per 64-row block at most (K = H in ranges)
     int32_t gu_min_range; // gate_up: chunks per range at least (the kernel makes no shorter ranges)
     int32_t s_dn, l_dn;   // down: segments, chunks per segment (K = I; l a multiple of 4)
-    int32_t g_gu, g_dn;   // chunks per scale-word group (4: 16-byte copies, 2: 8-byte), set at launch
 };
 DecodeSplit decode_split(int64_t P, int32_t E, int32_t H, int32_t I);
 // Steps with at most this many pairs take the bf16 mma.sync decode kernel
 // (decode_mma.cu); larger decode steps the block-scaled e4m3 kernel (decode.cu).
-bool decode_use_mma(int64_t P);
+bool decode_use_mma(int64_t P, int32_t H, int32_t I);
 
 struct Workspace {
     int32_t* sorted;       // [P]

@@ -305,6 +305,7 @@ __device__ __noinline__ void finish_gate_up(const LayerArgs& a, const Item& it)
 
 __global__ void __launch_bounds__(kThreads, 4)
 decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_constant__ CUtensorMap dn_map,
+                    const __grid_constant__ CUtensorMap gu_sf_map, const __grid_constant__ CUtensorMap dn_sf_map,
                     const LayerArgs a)
 {
     __shared__ SharedState sh;
@@ -339,6 +340,8 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tmap(&gu_map);
         prefetch_tmap(&dn_map);
+        prefetch_tmap(&gu_sf_map);
+        prefetch_tmap(&dn_sf_map);
     }
     tc_fence_before();
     __syncthreads();
@@ -416,20 +419,9 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
             const bool gu = m.kind == 1;
             // tokens of the tile's pairs (lane j < 8 holds pair j's), gate_up only
             const int tok = (gu && lane < m.nrows) ? __ldg(a.sorted + m.q0 + lane) / a.k : 0;
-            // this lane's copy sources: 4 weight-row scale rows, 4 activation
-            // pieces of 16 bytes (row n = p / 8, piece p % 8), lanes < 16 one
-            // activation scale row
-            const uint8_t* sc = gu ? a.w13_scales : a.w2_scales;
-            const int64_t kb = (gu ? a.H : a.I) / 32;
-            const int G = gu ? a.split.g_gu : a.split.g_dn;   // chunks per scale-word group
+            // this lane's copy sources: 4 activation pieces of 16 bytes (row
+            // n = p / 8, piece p % 8), lanes < 16 one activation scale row
             const int64_t erow = (int64_t)m.expert * (gu ? 2 * a.I : a.H);
-            const uint8_t* sfa_src[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = lane + 32 * i;
-                const int64_t wr = gu ? (r < 64 ? 64 * m.rb + r : a.I + 64 * m.rb + (r - 64)) : 128 * m.rb + r;
-                sfa_src[i] = sc + (erow + wr) * kb;
-            }
             const uint8_t* act = gu ? a.x8 : a.h8;
             const uint8_t* sact = gu ? a.sx8 : a.sh8;
             const int64_t kact = gu ? a.H : a.I;
@@ -457,33 +449,29 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 if (!__shfl_sync(0xffffffffu, w, 0)) return false;
                 const uint32_t base = ring_addr + slot * kSlotBytes, fb = smem_u32(&sh.full[slot]);
                 const uint32_t sfbase = sf_addr + slot * kSfSlotBytes;
+                // the 16-byte group of scale words (4 chunks) holding this chunk's
+                // word, for every weight row; every slot gets its own copy, so a
+                // consumer reads word ch % 4 of its own slot
+                const int gx = (ch & ~3) * 4;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(fb, kCodeBytes);
+                    mbar_arrive_expect_tx(fb, kCodeBytes + kRows * 16);
                     if (gu) {
-                        tma_load_2d(base, &gu_map, ch * 32, (int)(erow + 64 * m.rb), fb);
-                        tma_load_2d(base + 64 * 32, &gu_map, ch * 32, (int)(erow + a.I + 64 * m.rb), fb);
+                        const int rg = (int)(erow + 64 * m.rb), ru = (int)(erow + a.I + 64 * m.rb);
+                        tma_load_2d(base, &gu_map, ch * 32, rg, fb);
+                        tma_load_2d(base + 64 * 32, &gu_map, ch * 32, ru, fb);
+                        tma_load_2d(sfbase, &gu_sf_map, gx, rg, fb);
+                        tma_load_2d(sfbase + 64 * 16, &gu_sf_map, gx, ru, fb);
                     } else {
-                        tma_load_2d(base, &dn_map, ch * 32, (int)(erow + 128 * m.rb), fb);
+                        const int rd = (int)(erow + 128 * m.rb);
+                        tma_load_2d(base, &dn_map, ch * 32, rd, fb);
+                        tma_load_2d(sfbase, &dn_sf_map, gx, rd, fb);
                     }
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (bsrc[i] != nullptr) cp_async16(base + bdst[i], bsrc[i] + ch * 128);
-                // scale words move in groups of G chunks aligned to the row (16 or
-                // 8 bytes); every slot gets the group holding its chunk, so a
-                // consumer reads word ch % G of its own slot
-                {
-                    const int gch = ch & ~(G - 1);
-                    if (G == 4) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) cp_async16(sfbase + (lane + 32 * i) * 16, sfa_src[i] + gch * 4);
-                        if (sfb_src != nullptr) cp_async16(sfbase + kSfbOff + lane * 16, sfb_src + gch * 4);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) cp_async8(sfbase + (lane + 32 * i) * 16, sfa_src[i] + gch * 4);
-                        if (sfb_src != nullptr) cp_async8(sfbase + kSfbOff + lane * 16, sfb_src + gch * 4);
-                    }
-                }
+                // the activation rows' scale groups (lanes < 16, one row each)
+                if (sfb_src != nullptr) cp_async16(sfbase + kSfbOff + lane * 16, sfb_src + gx);
                 cp_async_arrive_noinc(fb);
             }
             return true;
@@ -621,7 +609,6 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 epilogue_store(a, sh, tq, prev, prev_n, abort);
                 have_prev = 0;
             }
-            const int G = cur.kind == 1 ? a.split.g_gu : a.split.g_dn;
             bool ok = true;
             for (int ch = cur.c0; ch < cur.c1; ++ch, ++q, rp.step()) {
                 const uint32_t slot = rp.slot, st = q & 1u;
@@ -635,7 +622,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 const uint32_t sb = ring_addr + slot * kSlotBytes;
                 const uint4 w0 = lds_u4(sb + m * 32 + (swz << 4));
                 const uint4 w1 = lds_u4(sb + m * 32 + ((swz ^ 1u) << 4));
-                const uint32_t sfs = sf_addr + slot * kSfSlotBytes + 4u * (uint32_t)(ch & (G - 1));
+                const uint32_t sfs = sf_addr + slot * kSfSlotBytes + 4u * (uint32_t)(ch & 3);
                 uint32_t sfa = lds_u32(sfs + m * 16);
                 const uint32_t sfb = lds_u32(sfs + kSfbOff + (lane & 15) * 16);
                 const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -730,9 +717,6 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     a.k = k;
     a.E = E;
     a.split = ws.split;
-    // scale words move in 16-byte groups (4 chunks) where rows and the base allow it
-    a.split.g_gu = (H % 512 == 0 && (reinterpret_cast<uintptr_t>(w.w13_scales) & 15) == 0) ? 4 : 2;
-    a.split.g_dn = (I % 512 == 0 && (reinterpret_cast<uintptr_t>(w.w2_scales) & 15) == 0) ? 4 : 2;
     a.P = P;
     a.tiles = ws.tiles;
     a.tile_count = ws.tile_count;
@@ -756,6 +740,13 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     cudaError_t e = make_tmap_2d(&gu_map, w.w13_codes, false, (int64_t)E * 2 * I, H / 4, 32, 64, 32);
     if (e != cudaSuccess) return e;
     if ((e = make_tmap_2d(&dn_map, w.w2_codes, false, (int64_t)E * H, I / 4, 32, 128, 32)) != cudaSuccess) return e;
+    // scale groups: 16 bytes (4 chunks) x 64 rows (gate_up) or x 128 rows (down);
+    // rows of H/32 and I/32 bytes are multiples of 16 (H, I multiples of 512)
+    CUtensorMap gu_sf_map, dn_sf_map;
+    if ((e = make_tmap_2d(&gu_sf_map, w.w13_scales, false, (int64_t)E * 2 * I, H / 32, 16, 64, 0)) != cudaSuccess)
+        return e;
+    if ((e = make_tmap_2d(&dn_sf_map, w.w2_scales, false, (int64_t)E * H, I / 32, 16, 128, 0)) != cudaSuccess)
+        return e;
 
     const int grid = sm_count() * occ;
     if ((e = ev.record(1, s)) != cudaSuccess) return e;
@@ -769,7 +760,7 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, gu_map, dn_map, a)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, gu_map, dn_map, gu_sf_map, dn_sf_map, a)) != cudaSuccess) return e;
     if ((e = ev.record(2, s)) != cudaSuccess) return e;
     // y = the slots of every token summed over j and the K segments of down
     return launch_combine(ws.stage, ids, T, k, E, H, a.split.s_dn, P * H, true, y, s);

@@ -38,9 +38,11 @@ class Planes(ctypes.Structure):
                 ("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32)]
 
 
-def decode_kernel(T: int, top_k: int) -> str:
-    """Name of the kernel that runs the layer of a decode step (T <= DECODE_MAX_TOKENS)."""
-    return "decode_mma_kernel" if T * top_k <= DECODE_MMA_MAX_PAIRS else "decode_layer_kernel"
+def decode_kernel(T: int, top_k: int, H: int, I: int) -> str:
+    """Name of the kernel that runs the layer of a decode step (T <= DECODE_MAX_TOKENS): the
+    block-scaled kernel needs more than DECODE_MMA_MAX_PAIRS pairs and H, I multiples of 512."""
+    small = T * top_k <= DECODE_MMA_MAX_PAIRS or H % 512 != 0 or I % 512 != 0
+    return "decode_mma_kernel" if small else "decode_layer_kernel"
 
 
 def lib_path() -> str:

@@ -117,11 +117,16 @@ moe_w2_status moe_w2_permute(const int32_t *topk_ids, int32_t T, int32_t top_k, 
  *   y_bf16        bf16 [T][H] (written; may not alias x)
  *   workspace     device buffer of at least moe_w2_forward_workspace_size() bytes,
  *                 256-byte aligned, used by this call until it completes on `stream`
+ * x_bf16, y_bf16 and the four plane pointers must be 16-byte aligned
+ * (MOE_W2_ERR_INVALID_ARG otherwise).
  * T = 0 is a no-op.  Pairs with an id outside [0,E) contribute 0
  * (MOE_W2_DEV_BAD_EXPERT_ID); blocks with a UE8M0 byte outside [1,252] count
- * as 0 (MOE_W2_DEV_BAD_SCALE).  T <= 64 uses the decode kernels (CUDA cores +
- * mma.sync, planes streamed once per active expert); larger T the prefill
- * kernels (TMA + tcgen05 with accumulators in tensor memory).
+ * as 0 (MOE_W2_DEV_BAD_SCALE).  T <= 64 uses the decode kernels, which stream
+ * the planes of every active expert once per step: steps of more than 16 pairs
+ * with H and I multiples of 512 a block-scaled tcgen05 kernel (codes expanded
+ * to e2m1, activations as two e4m3 rows), the rest a bf16 mma.sync kernel;
+ * larger T the prefill kernels (TMA + tcgen05 with accumulators in tensor
+ * memory).
  */
 moe_w2_status moe_w2_forward(const void *x_bf16, const int32_t *topk_ids, const float *topk_weights,
                              const moe_w2_planes *w, int32_t T, int32_t top_k, void *y_bf16,

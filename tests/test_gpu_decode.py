@@ -33,11 +33,15 @@ def test_tiny_config_all_tokens():
     assert_close_layer(y, ref, "tiny")
 
 
+# Steps of more than 16 pairs with H and I multiples of 512 run the block-scaled
+# tcgen05 kernel; the rest the mma.sync kernel (both kinds are listed).
 @pytest.mark.parametrize("H,I,E,k,T,seed", [(256, 256, 4, 1, 1, 1), (512, 256, 8, 2, 3, 2), (768, 512, 16, 4, 17, 3),
                                             (1024, 768, 8, 8, 64, 4), (512, 512, 2, 2, 64, 5),
-                                            (256, 1024, 64, 16, 40, 6)])
+                                            (256, 1024, 64, 16, 40, 6), (1024, 512, 16, 4, 17, 7),
+                                            (512, 1024, 64, 16, 40, 8), (1536, 1024, 8, 8, 64, 9),
+                                            (512, 512, 4, 1, 17, 10)])
 def test_small_shapes_all_tokens(H, I, E, k, T, seed):
-    # (512,512,2,2,64): each expert gets ~64 pairs -> several 32-pair passes
+    # (512,512,2,2,64): each expert gets ~64 pairs -> several tiles per expert
     lay = inputs.small_layer_inputs(H, I, E, k, T, seed)
     y, st = _run(lay)
     ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes)
@@ -60,12 +64,16 @@ def test_duplicates_invalid_ids_and_zero_weights():
     assert np.all(y[3] == 0)
 
 
-def test_bad_scale_bytes_zero_their_blocks():
-    lay = inputs.small_layer_inputs(512, 256, 4, 2, 4, 12)
+@pytest.mark.parametrize("H,I,T,seed", [(512, 256, 4, 12), (512, 512, 16, 13)])
+def test_bad_scale_bytes_zero_their_blocks(H, I, T, seed):
+    # (512, 256, T=4): the mma.sync kernel; (512, 512, T=16, 32 pairs): the block-scaled kernel
+    lay = inputs.small_layer_inputs(H, I, 4, 2, T, seed)
+    assert moe_w2.decode_kernel(T, 2, H, I) == ("decode_mma_kernel" if I == 256 else "decode_layer_kernel")
     planes = {k: v.copy() for k, v in lay.planes.items()}
     planes["w13_scales"][1, 5, 3] = 0
     planes["w2_scales"][2, 7, 1] = 255
     planes["w2_scales"][0, 100, 0] = 253
+    planes["w13_scales"][3, 2 * I - 1, H // 32 - 1] = 0   # last block of the last up row
     y, st = _run(lay, planes_dev=planes_to_dev(planes))
     ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, planes)
     assert rst == moe_w2.DEV_BAD_SCALE

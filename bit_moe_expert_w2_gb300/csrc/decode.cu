@@ -358,12 +358,17 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
     const int n_tiles = *a.tile_count;
     const int rbg = a.I / 64, rbd = a.H / 128;
     const int nch_gu = a.H / kChunk, nch_dn = a.I / kChunk;
-    // gate_up: the chunk sequence of all (tile, 64-row block) units in ranges
-    const int64_t c_gu = (int64_t)n_tiles * rbg * nch_gu;
-    // ranges no shorter than the host's minimum, which bounds the contributing
-    // items of a row block (the gu_part slots)
-    const int64_t r_gu =
-        c_gu > 0 ? max((int64_t)1, min((int64_t)gridDim.x, c_gu / a.split.gu_min_range)) : 0;
+    // gate_up: the chunk sequence of all (tile, 64-row block) units in ranges.
+    // With at least one unit per CTA every unit is one range (its whole K), so
+    // the units finish in queue order and the down items of early tiles find
+    // their h ready; with fewer units K is split into ranges no shorter than
+    // the host's minimum, which bounds the contributing items of a row block
+    // (the gu_part slots).
+    const int64_t n_units = (int64_t)n_tiles * rbg;
+    const int64_t c_gu = n_units * nch_gu;
+    const int64_t r_gu = c_gu <= 0                     ? 0
+                         : n_units >= (int64_t)gridDim.x ? n_units
+                                                         : max((int64_t)1, min((int64_t)gridDim.x, c_gu / a.split.gu_min_range));
     const int64_t n_dn = (int64_t)n_tiles * rbd * a.split.s_dn;
 
     if (warp == kProducerWarp) {

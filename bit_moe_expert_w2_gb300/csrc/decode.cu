@@ -461,11 +461,11 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, kCodeBytes + kRows * 16);
                     if (gu) {
-                        const int rg = (int)(erow + 64 * m.rb), ru = (int)(erow + a.I + 64 * m.rb);
-                        tma_load_2d(base, &gu_map, ch * 32, rg, fb);
-                        tma_load_2d(base + 64 * 32, &gu_map, ch * 32, ru, fb);
-                        tma_load_2d(sfbase, &gu_sf_map, gx, rg, fb);
-                        tma_load_2d(sfbase + 64 * 16, &gu_sf_map, gx, ru, fb);
+                        // one box holds the row block's 64 gate rows, then its 64 up
+                        // rows (planes 2e and 2e + 1 of the w13 plane seen as 2E
+                        // planes of I rows)
+                        tma_load_3d(base, &gu_map, ch * 32, 64 * m.rb, 2 * m.expert, fb);
+                        tma_load_3d(sfbase, &gu_sf_map, gx, 64 * m.rb, 2 * m.expert, fb);
                     } else {
                         const int rd = (int)(erow + 128 * m.rb);
                         tma_load_2d(base, &dn_map, ch * 32, rd, fb);
@@ -739,16 +739,17 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     a.y = y;
     a.status = status;
 
-    // code tiles: 32 bytes (128 codes) x 64 rows (gate_up: gate and up halves
-    // separately) or x 128 rows (down), 32B-swizzled
+    // code tiles: 32 bytes (128 codes) x 128 rows, 32B-swizzled; gate_up as a
+    // 3-D box {32 bytes, 64 rows, 2 planes} over the w13 plane seen as 2E planes
+    // (gate, up) of I rows, down as a 2-D box of 128 rows
     CUtensorMap gu_map, dn_map;
-    cudaError_t e = make_tmap_2d(&gu_map, w.w13_codes, false, (int64_t)E * 2 * I, H / 4, 32, 64, 32);
+    cudaError_t e = make_tmap_3d_u8(&gu_map, w.w13_codes, 2 * (int64_t)E, I, H / 4, 32, 64, 2, 32);
     if (e != cudaSuccess) return e;
     if ((e = make_tmap_2d(&dn_map, w.w2_codes, false, (int64_t)E * H, I / 4, 32, 128, 32)) != cudaSuccess) return e;
     // scale groups: 16 bytes (4 chunks) x 64 rows (gate_up) or x 128 rows (down);
     // rows of H/32 and I/32 bytes are multiples of 16 (H, I multiples of 512)
     CUtensorMap gu_sf_map, dn_sf_map;
-    if ((e = make_tmap_2d(&gu_sf_map, w.w13_scales, false, (int64_t)E * 2 * I, H / 32, 16, 64, 0)) != cudaSuccess)
+    if ((e = make_tmap_3d_u8(&gu_sf_map, w.w13_scales, 2 * (int64_t)E, I, H / 32, 16, 64, 2, 0)) != cudaSuccess)
         return e;
     if ((e = make_tmap_2d(&dn_sf_map, w.w2_scales, false, (int64_t)E * H, I / 32, 16, 128, 0)) != cudaSuccess)
         return e;

@@ -100,6 +100,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -328,6 +337,11 @@ namespace moe_w2 {
 // 2-D tensor map [rows][cols] (row-major) of bf16 or uint8, box {box_cols, box_rows}.
 cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, bool bf16, int64_t rows, int64_t cols,
                          uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
+// 3-D tensor map of uint8 [planes][rows][cols] (row-major, planes contiguous),
+// box {box_cols, box_rows, box_planes}: e.g. the gate and up halves of an
+// expert's w13 plane as two consecutive planes of I rows.
+cudaError_t make_tmap_3d_u8(CUtensorMap* map, const void* base, int64_t planes, int64_t rows, int64_t cols,
+                            uint32_t box_cols, uint32_t box_rows, uint32_t box_planes, int swizzle_bytes);
 cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted, const int32_t* offsets, int32_t E, int32_t k,
                           int32_t H, int64_t P, uint16_t* xs, cudaStream_t s);
 cudaError_t launch_combine(const float* stage, const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t H,

@@ -230,8 +230,9 @@ struct DecodeSplit {
     int32_t s_dn, l_dn;   // down: segments, chunks per segment (K = I; l a multiple of 4)
 };
 DecodeSplit decode_split(int64_t P, int32_t E, int32_t H, int32_t I);
-// Steps with at most this many pairs take the bf16 mma.sync decode kernel
-// (decode_mma.cu); larger decode steps the block-scaled e4m3 kernel (decode.cu).
+// True when a decode step of P pairs takes the bf16 mma.sync decode kernel
+// (decode_mma.cu): few pairs, or H or I not a multiple of 512; otherwise the
+// block-scaled kernel (decode.cu) runs it.
 bool decode_use_mma(int64_t P, int32_t H, int32_t I);
 
 struct Workspace {

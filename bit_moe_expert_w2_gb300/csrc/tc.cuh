@@ -232,7 +232,7 @@ __device__ __forceinline__ void tmem_st32_sync(uint32_t taddr, const uint32_t (&
         : "memory");
 }
 
-// ------------------------------------------------------------------ block-scaled e4m3 (decode)
+// ------------------------------------------------------------------ block-scaled MMA (decode)
 //
 // tcgen05.mma kind::mxf8f6f4 with UE8M0 block scales, one scale per 32 K per
 // row of A and per row of B (scale_vec::1X), A read from tensor memory.  Layouts

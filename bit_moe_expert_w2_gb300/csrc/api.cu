@@ -12,13 +12,13 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int32_t kPrefillTileRows = 256;   // pairs per prefill tile (tcgen05 N <= 256)
-constexpr int32_t kDecodeTileRows = 8;      // pairs per decode tile (MMA N = 16: hi and lo row per pair)
+constexpr int32_t kDecodeTileRows = 3;      // pairs per decode tile (MMA N = 16: kActDigits rows per pair)
 constexpr int32_t kDecodeMmaTileRows = 16;  // pairs per tile of the mma.sync decode kernel
 constexpr int64_t kDecodeMmaMaxPairs = 16;  // steps with at most this many pairs take the mma.sync kernel
 constexpr int64_t kDecodeTargetItems = 1200; // down items per step that keep every CTA busy
-constexpr int64_t kDecodeMinRange = 4;       // gate_up range: chunks at least
-constexpr int64_t kDecodeMaxRanges = 1024;   // gate_up ranges at most, for a step with ceil(P/8) tiles
-constexpr int32_t kDecodeMinSegChunks = 4;   // at least 4 chunks of 128 K per decode item
+constexpr int64_t kDecodeMinRange = 4;       // gate_up range: chunks (256 K) at least
+constexpr int64_t kDecodeMaxRanges = 1024;   // gate_up ranges at most, for a step with the fewest tiles
+constexpr int32_t kDecodeMinSegChunks = 2;   // at least 2 chunks of 256 K per decode item
 constexpr int64_t kDecodeMaxSegments = 16;   // K segments per row block
 
 int g_sm_count[kMaxDevices];
@@ -74,23 +74,22 @@ DecodeSplit decode_split(int64_t P, int32_t E, int32_t H, int32_t I)
     // kDecodeMaxRanges ranges of at least kDecodeMinRange chunks (the device
     // picks the count from the tile count).  A unit of nch chunks then meets at
     // most ceil(nch / len) + 1 ranges, len the shortest range, which is at
-    // least the minimum and at least (chunks of ceil(P / 8) tiles) / max ranges.
-    const int64_t nch_gu = H / 128, rbg = I / 64;
-    const int64_t tiles_min = std::max<int64_t>(1, (P + 7) / 8);
+    // least the minimum and at least (chunks of ceil(P / kDecodeTileRows) tiles) / max ranges.
+    const int64_t nch_gu = H / 256, rbg = I / 64;
+    const int64_t tiles_min = std::max<int64_t>(1, (P + kDecodeTileRows - 1) / kDecodeTileRows);
     const int64_t len = std::max<int64_t>(kDecodeMinRange, tiles_min * rbg * nch_gu / kDecodeMaxRanges);
     d.gu_min_range = (int32_t)len;
     d.s_gu = (int32_t)std::min<int64_t>(nch_gu, (nch_gu + len - 1) / len + 1);
     // down: each 128-row block's K in s_dn equal segments, as many as keep a
     // small step's down phase in several short items per CTA
     const int64_t tiles = std::max<int64_t>(1, std::min<int64_t>(P, E));
-    const int32_t nch_dn = I / 128;
+    const int32_t nch_dn = I / 256;
     const int64_t rbd = H / 128;
     int64_t want = (kDecodeTargetItems + tiles * rbd - 1) / (tiles * rbd);
     want = std::min<int64_t>(want, std::max<int64_t>(1, 64 / std::max<int64_t>(1, P)));
     want = std::max<int64_t>(1, std::min<int64_t>({want, (int64_t)std::max(1, nch_dn / kDecodeMinSegChunks),
                                                     (int64_t)kDecodeMaxSegments}));
     d.l_dn = (int32_t)((nch_dn + want - 1) / want);
-    d.l_dn = (d.l_dn + 3) & ~3;   // segments start on a scale-word group (4 chunks = 16 scale bytes per row)
     d.s_dn = (nch_dn + d.l_dn - 1) / d.l_dn;
     return d;
 }
@@ -136,10 +135,10 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
     } else if (decode) {
         w.split = decode_split(P, E, H, I);
         w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * decode_counter_count(P, E, H, I)));
-        w.x8 = reinterpret_cast<uint8_t*>(take((size_t)2 * T * H));
-        w.sx8 = reinterpret_cast<uint8_t*>(take((size_t)2 * T * (H / 32)));
-        w.h8 = reinterpret_cast<uint8_t*>(take((size_t)2 * P * I));
-        w.sh8 = reinterpret_cast<uint8_t*>(take((size_t)2 * P * (I / 32)));
+        w.xd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * T * (H / 2)));
+        w.sxd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * T * (H / 32)));
+        w.hd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * P * (I / 2)));
+        w.shd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * P * (I / 32)));
         w.gu_part = reinterpret_cast<float*>(take(sizeof(float) * w.split.s_gu * P * 2 * I));
         w.stage = reinterpret_cast<float*>(take(sizeof(float) * w.split.s_dn * P * H));
     } else {
@@ -231,8 +230,8 @@ moe_w2_status moe_w2_forward_traced(const void* x_bf16, const int32_t* topk_ids,
     cudaError_t e = launch_permute(topk_ids, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active, ws.active_count,
                                    ws.tiles, ws.tile_count,
                                    !decode ? kPrefillTileRows : mma ? kDecodeMmaTileRows : kDecodeTileRows,
-                                   decode ? x : nullptr, mma ? ws.xa : nullptr, decode && !mma ? ws.x8 : nullptr,
-                                   decode && !mma ? ws.sx8 : nullptr, H, ws.counters,
+                                   decode ? x : nullptr, mma ? ws.xa : nullptr, decode && !mma ? ws.xd : nullptr,
+                                   decode && !mma ? ws.sxd : nullptr, H, ws.counters,
                                    decode ? (int32_t)decode_counter_count(P, E, H, I) : 0, decode ? y : nullptr,
                                    dev_status, s);
     if (e != cudaSuccess) return MOE_W2_ERR_CUDA;

@@ -23,33 +23,47 @@ namespace moe_w2 {
 __host__ __device__ __forceinline__ int t16_pos(int n) { return (n & ~15) | ((n & 3) << 2) | ((n >> 2) & 3); }
 
 // Decode activation operands (x for gate_up, h for down) enter the block-scaled
-// e4m3 MMA as two e4m3 rows per activation row, hi = e4m3(v) and
-// lo = e4m3(v - hi) with v = a / 2^(s-127), one UE8M0 byte s per 32 elements
-// (2^(s-127) = 2^(floor(log2 amax) - 7), so |v| < 256).  hi + lo equals v exactly
-// whenever |a| >= amax * 2^-9 (8 significant bits, as in bf16), and within
-// amax * 2^-17 otherwise.  Inside every group of 16 elements, stored byte p holds
-// element e4_elem(p) = 4(p & 3) + (p >> 2): the code expansion turns a 16-code
-// word into four registers, register j holding codes j, j+4, j+8, j+12 in its
-// bytes, and TMEM column j byte b is K index 4j + b, so B follows the same
-// transposed K order.  The map is its own inverse.
-__host__ __device__ __forceinline__ int e4_elem(int p) { return ((p & 3) << 2) | ((p >> 2) & 3); }
-__host__ __device__ __forceinline__ int e4_pos(int e) { return ((e & 3) << 2) | ((e >> 2) & 3); }
+// MMA (e2m1 x e2m1, kind::mxf4) as kActDigits rows of packed e2m1 "digits" per
+// activation row, each digit row with its own UE8M0 byte per 32 elements:
+//   a = sum_r d_r * 2^(s_r - 127) + residual,
+// where row r encodes, rounded to the nearest e2m1 value, what rows 0..r-1 left
+// over, scaled so that the block's largest leftover maps into (3, 6].  A row
+// shrinks the leftover about tenfold: five rows put a matrix-vector product
+// within ~2e-5 (relative L2) of the one with the exact activations, and the
+// layer output (where h is rounded to bf16 in between) within ~3e-4; four rows
+// would leave ~1e-3 there.
+// Inside every group of 16 elements, packed position p (nibble p & 1 of byte
+// p >> 1 of the row) holds element fp4_elem(p) = 2 (p & 7) + (p >> 3): the code
+// expansion puts the even codes of a 16-code word in one TMEM column and the odd
+// codes in the next, and the MMA reads column j nibble i as K index 8 j + i.
+constexpr int kActDigits = 5;
+__host__ __device__ __forceinline__ int fp4_elem(int p) { return ((p & 7) << 1) | (p >> 3); }
+__host__ __device__ __forceinline__ int fp4_pos(int e) { return ((e & 1) << 3) | (e >> 1); }
 
-// UE8M0 byte of a 32-element activation block with maximum magnitude amax.
-__device__ __forceinline__ uint32_t act_scale_byte(float amax)
+// UE8M0 byte s of a digit row whose block's largest magnitude is amax: the
+// smallest power of two 2^(s-127) with amax / 2^(s-127) <= 6 (so the block's
+// values map into (3, 6]), within [1, 253].
+__device__ __forceinline__ uint32_t digit_scale_byte(float amax)
 {
     if (!(amax > 0.f)) return 127u;   // all zeros (or not a number: the values carry it)
-    const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
-    return (uint32_t)min(254, max(1, ex - 7));
+    const uint32_t b = __float_as_uint(amax);
+    const int ex = (int)((b >> 23) & 0xFFu);   // amax = m 2^(ex - 127), m in [1, 2)
+    // amax / 2^(ex - 129) = 4 m <= 6 while m <= 1.5; above, one step up (2 m in (3, 4))
+    const int s = ex - 2 + ((b & 0x7FFFFFu) > 0x400000u ? 1 : 0);
+    return (uint32_t)min(253, max(1, s));
 }
-// 2^(127 - s): the factor that takes the block's values to the e4m3 range.
-__device__ __forceinline__ float act_inv_scale(uint32_t s) { return __uint_as_float((254u - s) << 23); }
-// hi = e4m3(v) and lo = e4m3(v - hi), both rounded to nearest even.
-__device__ __forceinline__ void act_split(float v, uint32_t& hi, uint32_t& lo)
+// 2^(s - 127) and 2^(127 - s) for s in [1, 253].
+__device__ __forceinline__ float digit_scale(uint32_t s) { return __uint_as_float(s << 23); }
+__device__ __forceinline__ float digit_inv_scale(uint32_t s) { return __uint_as_float((254u - s) << 23); }
+// Nearest e2m1 value of v (ties to the even mantissa; |v| above 6 gives 6): the
+// nibble (sign in bit 3, magnitude index of 0, .5, 1, 1.5, 2, 3, 4, 6) and its value.
+__device__ __forceinline__ uint32_t e2m1_digit(float v, float& val)
 {
-    hi = __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
-    const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)hi, __NV_E4M3);
-    lo = __nv_cvt_float_to_fp8(v - __half2float(__half(hr)), __NV_SATFINITE, __NV_E4M3);
+    const float a = fminf(fabsf(v), 6.f);
+    const float q = a < 2.f ? rintf(a * 2.f) * 0.5f : a < 4.f ? rintf(a) : rintf(a * 0.5f) * 2.f;
+    const uint32_t mi = q < 2.f ? (uint32_t)(q * 2.f) : q < 4.f ? (uint32_t)q + 2u : q < 5.f ? 6u : 7u;
+    val = v < 0.f ? -q : q;
+    return mi | (v < 0.f && mi != 0u ? 8u : 0u);
 }
 
 // ------------------------------------------------------------------ status
@@ -252,10 +266,10 @@ struct Workspace {
     float* stage;          // per-pair outputs times router weight, slot t*k+j: prefill [P][H],
                            // decode [s_dn][P][H] (one slab per K segment of down)
     // decode
-    uint8_t* x8;           // e4m3 activation rows of x, 2 per token [2T][H]
-    uint8_t* sx8;          // their UE8M0 bytes [2T][H/32]
-    uint8_t* h8;           // e4m3 activation rows of h, 2 per pair (expert order) [2P][I]
-    uint8_t* sh8;          // their UE8M0 bytes [2P][I/32]
+    uint8_t* xd;           // e2m1 digit rows of x, kActDigits per token [5T][H/2]
+    uint8_t* sxd;          // their UE8M0 bytes [5T][H/32]
+    uint8_t* hd;           // e2m1 digit rows of h, kActDigits per pair (expert order) [5P][I/2]
+    uint8_t* shd;          // their UE8M0 bytes [5P][I/32]
     float* gu_part;        // gate_up partial sums per K segment [s_gu][P][2I]
     DecodeSplit split;
     size_t bytes;
@@ -283,8 +297,8 @@ struct PhaseEvents {
 
 cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* sorted, int32_t* inv,
                            int32_t* offsets, int32_t* active, int32_t* active_count, int4* tiles,
-                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16, uint8_t* x8,
-                           uint8_t* sx8, int32_t H, int32_t* counters, int32_t n_counters, uint16_t* y,
+                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16, uint8_t* xd,
+                           uint8_t* sxd, int32_t H, int32_t* counters, int32_t n_counters, uint16_t* y,
                            uint32_t* status, cudaStream_t s);
 
 cudaError_t launch_decode_mma(const uint16_t* x, const int32_t* ids, const float* weights,

@@ -9,39 +9,38 @@
 // tokens use it.  Page "The v0.24.0 port", "Deterministic unpermute" bullet:
 // per-pair results are placed in their own slot and summed in a fixed order.
 //
-// Why block-scaled MX operands (tcgen05.mma kind::mxf8f6f4, scale_vec::1X): a
+// Why block-scaled fp4 operands (tcgen05.mma kind::mxf4, scale_vec::2X): a
 // weight is +-1 or +-4 times 2^(s-127) with one UE8M0 byte s per 32 K of a row,
 // which is an e2m1 value under an MX block scale.  The tensor core applies s
-// itself, so the expansion is one byte per code: A is fed as e2m1 in 8-bit
-// containers, where the byte of code c is (c << 4) | 0x08, so per 16-code word
-// it takes three masks, three shifts and four adds or ors, with no table
-// (folding s into bf16 instead takes eight byte-permutes plus per-block table
-// lookups).  Activations enter as two e4m3 rows each (act_split), which keeps
-// their bf16 precision.
+// itself, so the expansion is one nibble per code, (c << 2) | 2: per 16-code
+// word one shift and two and-or operations, with no table.  Activations enter
+// as kActDigits rows of e2m1 digits each (fp4_elem order, digit_scale_byte),
+// which keeps a matrix-vector product within ~2e-4 of the exact one.  Packed
+// operands halve the MMAs (K = 64 each) and the tensor-memory bytes per code,
+// so a chunk covers 256 K of a row in the same 32 columns.
 
-// Work item = (tile of <= 8 pairs of one expert, 128 weight rows, K segment).
+// Work item = (tile of <= 3 pairs of one expert, 128 weight rows, K segment).
 // gate_up rows: 64 gate rows and the matching 64 up rows; down rows: 128 rows of
 // W_down.  Each CTA has six warps:
 //   warp 4     producer: takes items from a global queue, publishes them, and
-//              streams every 128-K chunk into a ring of shared-memory slots:
-//              code bytes by TMA (128 rows x 32 bytes, 32B-swizzled), the
-//              item's 16 activation rows (written straight into the
-//              128B-swizzled UMMA layout) by cp.async, and at the first chunk of
-//              every group of 4 (or 2) chunks the group's scale words of all
-//              rows, one 16-byte (8-byte) cp.async per row
+//              streams every 256-K chunk into a ring of shared-memory slots:
+//              code bytes by TMA (128 rows x 64 bytes, 64B-swizzled) with the
+//              16-byte scale group (2 chunks) of every weight row, the item's 16
+//              digit rows (written straight into the 128B-swizzled UMMA layout)
+//              and their scale groups by cp.async
 //   warps 0-3  consumers, one per TMEM lane quadrant and one thread per weight
-//              row: expand the row's 128 codes of a chunk to e2m1 bytes and store them
-//              with the row's scale word into TMEM, plus this quadrant's copy of
-//              the activation scale words
-//   warp 5     MMA issuer (one thread): 4 x tcgen05.mma (M=128, N=16, K=32) per
+//              row: expand the row's 256 codes of a chunk to packed e2m1 and store
+//              them with the row's two scale words into TMEM, plus this
+//              quadrant's copy of the digit rows' scale words
+//   warp 5     MMA issuer (one thread): 4 x tcgen05.mma (M=128, N=16, K=64) per
 //              chunk into one of two TMEM accumulators
 //   warp 6     finisher: the cross-CTA part of every gate_up epilogue
 // An item's accumulator is read by the consumer warps after the first chunk of
 // the next item (it is double-buffered), warp by warp with no CTA-wide barrier:
 //   gate_up  partial sums of the K segment -> gu_part; the finisher counts the
 //            segment, and the last of the S segments of a (tile, 64-row block)
-//            sums them in segment order, writes h = bf16(SiLU(g) * u) as e4m3
-//            activation rows and marks the block ready
+//            sums them in segment order, writes h = bf16(SiLU(g) * u) as digit
+//            rows and marks the block ready
 //   down     w * partial -> stage[segment][pair]
 // A separate combine kernel, launched as a programmatic dependent, sums every
 // token's slots in (j, segment) order and writes y.
@@ -58,30 +57,31 @@ namespace moe_w2 {
 
 namespace {
 
-constexpr int kChunk = 128;                          // K per chunk: 4 MMAs of K = 32 (one scale block each)
+constexpr int kChunk = 256;                          // K per chunk: 4 MMAs of K = 64 (two scale blocks each)
 constexpr int kRows = 128;                           // weight rows per item (MMA M)
-constexpr int kTilePairs = 8;                        // pairs per tile
-constexpr int kN = 2 * kTilePairs;                   // MMA N: hi and lo activation row per pair
+constexpr int kTilePairs = 3;                        // pairs per tile
+constexpr int kN = 16;                               // MMA N: the digit rows of every pair (15), padded
+static_assert(kActDigits * kTilePairs <= kN, "a tile's digit rows must fit the MMA N");
 constexpr int kCWarps = 4;                           // consumer warps
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kFinisherWarp = 6;
 constexpr int kThreads = 7 * 32;
-constexpr int kSlots = 6;                            // chunk slots
-constexpr uint32_t kCodeBytes = kRows * 32;          // 128 rows x 32 code bytes, 32B-swizzled
-constexpr uint32_t kBOff = kCodeBytes;               // 16 activation rows x 128 bytes, 128B-swizzled
-constexpr uint32_t kSlotBytes = kBOff + kN * 128;    // 6144, a multiple of 1024
-constexpr uint32_t kSfbOff = kRows * 16;             // scale area of a slot: 128 rows x 16 bytes of
-constexpr uint32_t kSfSlotBytes = kSfbOff + kN * 16; // weight-row scale words, then 16 activation rows
+constexpr int kSlots = 4;                            // chunk slots
+constexpr uint32_t kCodeBytes = kRows * 64;          // 128 rows x 64 code bytes, 64B-swizzled
+constexpr uint32_t kBOff = kCodeBytes;               // 16 digit rows x 128 bytes (256 e2m1), 128B-swizzled
+constexpr uint32_t kSlotBytes = kBOff + kN * 128;    // 10240, a multiple of 1024
+constexpr uint32_t kSfbOff = kRows * 16;             // scale area of a slot: 16-byte groups (2 chunks) of the
+constexpr uint32_t kSfSlotBytes = kSfbOff + kN * 16; // 128 weight rows, then of the 16 digit rows
 constexpr uint32_t kRingBytes = kSlots * (kSlotBytes + kSfSlotBytes);
 constexpr int kInfo = 8;                             // published items in flight
 constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kColD = 0;                        // accumulators: 2 x 16 columns
-constexpr uint32_t kColA = 32;                       // A stages: 2 x 32 columns
-constexpr uint32_t kColSfa = 96;                     // stage s, quadrant w: column 96 + 4s + w
-constexpr uint32_t kColSfb = 104;                    // stage s: column 104 + 4s
+constexpr uint32_t kColA = 32;                       // A stages: 2 x 32 columns (256 K of e2m1)
+constexpr uint32_t kColSfa = 96;                     // stage s, word w, quadrant q: column 96 + 8s + 4w + q
+constexpr uint32_t kColSfb = 112;                    // stage s, word w: column 112 + 8s + 4w
 // (scale-factor operands start on a 4-column boundary: an M = 128 tile's A
-// scales span 4 columns, one per lane quadrant)
+// scales span 4 columns, one per lane quadrant; a chunk has two scale words)
 constexpr int32_t kHReady = 1 << 20;                 // added to a row block's counter once its h is written
 
 struct LayerArgs {
@@ -95,10 +95,10 @@ struct LayerArgs {
     const int32_t* sorted;
     const float* weights;
     const int32_t* ids;
-    const uint8_t* x8;           // [2T][H]
-    const uint8_t* sx8;          // [2T][H/32]
-    uint8_t* h8;                 // [2P][I]
-    uint8_t* sh8;                // [2P][I/32]
+    const uint8_t* xd;           // [5T][H/2] digit rows of x
+    const uint8_t* sxd;          // [5T][H/32]
+    uint8_t* hd;                 // [5P][I/2] digit rows of h
+    uint8_t* shd;                // [5P][I/32]
     float* gu_part;              // [s_gu][P][2I]
     float* stage;                // [s_dn][P][H]
     int32_t* gu_seg;             // [tiles][I/64]: contributing items done; + kHReady once h is written
@@ -186,22 +186,17 @@ struct RingPos {
     }
 };
 
-// Four e2m1 container words from one word of 16 codes: byte b of r_j holds code
-// 4b + j as (c << 4) | 0x08 (c in bits 5:4, bit 3 set: +1, +4, -1, -4).  Per word
-// four and-or operations and three shifts; the compiler issues the two left
-// shifts as multiplies, so the work splits 5:2 between the ALU and FMA pipes
-// (measured instruction counts).
-__device__ __forceinline__ void expand_e2m1(uint32_t w, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+// Two words of packed e2m1 from one word of 16 codes: nibble n of r0 holds code
+// 2n and nibble n of r1 code 2n + 1, each as (c << 2) | 2 (c in bits 3:2: +1,
+// +4, -1, -4).  One shift and two and-or operations per word; the compiler
+// issues the shift as a multiply (FMA pipe).
+__device__ __forceinline__ void expand_fp4(uint32_t w, uint32_t& r0, uint32_t& r1)
 {
-    asm("{\n\t.reg .b32 t0, t1, t3;\n\t"
-        "shl.b32 t0, %4, 4;\n\t"
-        "lop3.b32 %0, t0, 0x30303030, 0x08080808, 0xEA;\n\t"   // (x & m) | c
-        "shl.b32 t1, %4, 2;\n\t"
-        "lop3.b32 %1, t1, 0x30303030, 0x08080808, 0xEA;\n\t"
-        "lop3.b32 %2, %4, 0x30303030, 0x08080808, 0xEA;\n\t"
-        "shr.b32 t3, %4, 2;\n\t"
-        "lop3.b32 %3, t3, 0x30303030, 0x08080808, 0xEA;\n\t}"
-        : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+    asm("{\n\t.reg .b32 t0;\n\t"
+        "shl.b32 t0, %2, 2;\n\t"
+        "lop3.b32 %0, t0, 0xCCCCCCCC, 0x22222222, 0xEA;\n\t"   // (x & m) | c
+        "lop3.b32 %1, %2, 0xCCCCCCCC, 0x22222222, 0xEA;\n\t}"
+        : "=r"(r0), "=r"(r1)
         : "r"(w));
 }
 
@@ -211,6 +206,15 @@ __device__ __forceinline__ uint32_t scale_word_suspect(uint32_t s)
 {
     const uint32_t d = s - 0x01010101u;
     return ((d & 0x7F7F7F7Fu) + 0x04040404u) & d & 0x80808080u;
+}
+
+// A pair's accumulator row: the sum of its kActDigits digit columns.
+__device__ __forceinline__ float pair_sum(const float (&v)[16], int j)
+{
+    float s = 0.f;
+#pragma unroll
+    for (int d = 0; d < kActDigits; ++d) s += v[kActDigits * j + d];
+    return s;
 }
 
 // Consumer side of an item's epilogue, one warp (its 32 weight rows): the
@@ -237,14 +241,14 @@ __device__ __noinline__ void epilogue_store(const LayerArgs& a, SharedState& sh,
         float* dst = a.gu_part + ((int64_t)it.seg * P + it.q0) * I2 + col;
 #pragma unroll
         for (int j = 0; j < kTilePairs; ++j)
-            if (j < it.nrows) dst[(int64_t)j * I2] = v[2 * j] + v[2 * j + 1];
+            if (j < it.nrows) dst[(int64_t)j * I2] = pair_sum(v, j);
     } else {
         const int row = 128 * it.rb + m;
 #pragma unroll
         for (int j = 0; j < kTilePairs; ++j)
             if (j < it.nrows) {
                 const int pr = __ldg(a.sorted + it.q0 + j);
-                a.stage[((int64_t)it.seg * P + pr) * a.H + row] = __ldg(a.weights + pr) * (v[2 * j] + v[2 * j + 1]);
+                a.stage[((int64_t)it.seg * P + pr) * a.H + row] = __ldg(a.weights + pr) * pair_sum(v, j);
             }
     }
     __syncwarp();
@@ -254,8 +258,8 @@ __device__ __noinline__ void epilogue_store(const LayerArgs& a, SharedState& sh,
 // Finisher side of a gate_up item's epilogue (one warp), once the four
 // consumer warps have stored its partial sums: count the item at its
 // (tile, 64-row block); the last of the block's cnt items sums their partial
-// sums in K order, writes h = bf16(SiLU(g) * u) as e4m3 activation rows and
-// marks the block ready.  The fence after the barrier wait orders every store the barrier
+// sums in K order, writes h = bf16(SiLU(g) * u) as digit rows and marks the
+// block ready.  The fence after the barrier wait orders every store the barrier
 // made visible to this warp before the counter update (fences are cumulative).
 __device__ __noinline__ void finish_gate_up(const LayerArgs& a, const Item& it)
 {
@@ -270,10 +274,12 @@ __device__ __noinline__ void finish_gate_up(const LayerArgs& a, const Item& it)
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __threadfence();
     const int I2 = 2 * a.I;
-    // indices 64 rb + 32 blk + lane; one activation scale block per blk
+    // indices 64 rb + 32 blk + lane; one activation scale block per blk.  The
+    // lane's element sits at packed position pos of the block; the other nibble
+    // of its byte belongs to lane ^ 2, and the lane with the low nibble writes.
+    const int pos = (lane & 16) | fp4_pos(lane & 15);
     for (int blk = 0; blk < 2; ++blk) {
         const int i = 64 * it.rb + 32 * blk + lane;
-        const int pos = (i & ~15) | e4_pos(i & 15);
         for (int j = 0; j < it.nrows; ++j) {
             const int64_t q = it.q0 + j;
             float g = 0.f, u = 0.f;
@@ -283,16 +289,18 @@ __device__ __noinline__ void finish_gate_up(const LayerArgs& a, const Item& it)
                 g += __ldcg(src + i);
                 u += __ldcg(src + a.I + i);
             }
-            const float hv = __bfloat162float(__float2bfloat16_rn(silu_f(g) * u));
-            const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
-            const uint32_t s8 = act_scale_byte(__uint_as_float(amax_bits));
-            uint32_t hi, lo;
-            act_split(hv * act_inv_scale(s8), hi, lo);
-            a.h8[(2 * q) * a.I + pos] = (uint8_t)hi;
-            a.h8[(2 * q + 1) * a.I + pos] = (uint8_t)lo;
-            if (lane == 0) {
-                a.sh8[(2 * q) * (a.I / 32) + i / 32] = (uint8_t)s8;
-                a.sh8[(2 * q + 1) * (a.I / 32) + i / 32] = (uint8_t)s8;
+            float v = __bfloat162float(__float2bfloat16_rn(silu_f(g) * u));
+#pragma unroll
+            for (int d = 0; d < kActDigits; ++d) {
+                const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
+                const uint32_t sd = digit_scale_byte(__uint_as_float(amax_bits));
+                float qv;
+                const uint32_t nib = e2m1_digit(v * digit_inv_scale(sd), qv);
+                v -= qv * digit_scale(sd);
+                const uint32_t other = __shfl_xor_sync(0xffffffffu, nib, 2);
+                const int64_t row = kActDigits * q + d;
+                if ((pos & 1) == 0) a.hd[row * (a.I / 2) + (i & ~31) / 2 + (pos >> 1)] = (uint8_t)(nib | (other << 4));
+                if (lane == 0) a.shd[row * (a.I / 32) + i / 32] = (uint8_t)sd;
             }
         }
     }
@@ -350,7 +358,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
     volatile int* abort = &sh.abort_flag;
 
     // Launched as a programmatic dependent of the permutation kernel: the setup
-    // above overlaps it; everything it writes (tiles, counters, x8) is read
+    // above overlaps it; everything it writes (tiles, counters, x digits) is read
     // only after this wait.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // the combine kernel may be scheduled now (it waits for this grid to finish)
@@ -395,11 +403,11 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
         // stream the chunks of a published item into the ring
         auto stream = [&](const Item& m) {
             if (m.kind == 0) {
-                // the h row blocks this K range reads (64 rows each; two per
+                // the h row blocks this K range reads (64 rows each; four per
                 // chunk) must be written before their rows are copied: lane r
-                // watches blocks 2 c0 + r, 2 c0 + r + 32, ...
+                // watches blocks 4 c0 + r, 4 c0 + r + 32, ...
                 const int32_t* hs = a.gu_seg + m.ti * rbg;
-                const int hb0 = 2 * m.c0, hb1 = 2 * m.c1;
+                const int hb0 = (kChunk / 64) * m.c0, hb1 = (kChunk / 64) * m.c1;
                 auto all_ready = [&]() {
                     bool r = true;
                     for (int hb = hb0 + lane; hb < hb1; hb += 32) r = r && ld_acquire(hs + hb) >= kHReady;
@@ -422,29 +430,30 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 if (__shfl_sync(0xffffffffu, *abort, 0)) return false;
             }
             const bool gu = m.kind == 1;
-            // tokens of the tile's pairs (lane j < 8 holds pair j's), gate_up only
+            // tokens of the tile's pairs (lane j < kTilePairs holds pair j's), gate_up only
             const int tok = (gu && lane < m.nrows) ? __ldg(a.sorted + m.q0 + lane) / a.k : 0;
-            // this lane's copy sources: 4 activation pieces of 16 bytes (row
-            // n = p / 8, piece p % 8), lanes < 16 one activation scale row
+            // this lane's copy sources: 4 pieces of 16 bytes of the digit rows
+            // (row n = p / 8 = kActDigits * pair + digit, piece p % 8), lanes < 16
+            // one digit row's scale bytes
             const int64_t erow = (int64_t)m.expert * (gu ? 2 * a.I : a.H);
-            const uint8_t* act = gu ? a.x8 : a.h8;
-            const uint8_t* sact = gu ? a.sx8 : a.sh8;
+            const uint8_t* act = gu ? a.xd : a.hd;
+            const uint8_t* sact = gu ? a.sxd : a.shd;
             const int64_t kact = gu ? a.H : a.I;
             const uint8_t* bsrc[4];
             uint32_t bdst[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int p = lane + 32 * i, nb = p >> 3, j = nb >> 1;
+                const int p = lane + 32 * i, nb = p >> 3, j = nb / kActDigits, d = nb % kActDigits;
                 const int tj = __shfl_sync(0xffffffffu, tok, j);
                 bdst[i] = kBOff + sw128_offset((uint32_t)nb, (uint32_t)(p & 7));
-                const int64_t row = gu ? 2 * (int64_t)tj + (nb & 1) : 2 * (int64_t)(m.q0 + j) + (nb & 1);
-                bsrc[i] = j < m.nrows ? act + row * kact + (p & 7) * 16 : nullptr;
+                const int64_t row = (int64_t)kActDigits * (gu ? (int64_t)tj : (int64_t)(m.q0 + j)) + d;
+                bsrc[i] = j < m.nrows ? act + row * (kact / 2) + (p & 7) * 16 : nullptr;
             }
             const uint8_t* sfb_src = nullptr;
             {
-                const int j = (lane >> 1) & 7;
+                const int j = lane / kActDigits, d = lane % kActDigits;
                 const int tj = __shfl_sync(0xffffffffu, tok, j);
-                const int64_t row = gu ? 2 * (int64_t)tj + (lane & 1) : 2 * (int64_t)(m.q0 + j) + (lane & 1);
+                const int64_t row = (int64_t)kActDigits * (gu ? (int64_t)tj : (int64_t)(m.q0 + j)) + d;
                 if (lane < kN && j < m.nrows) sfb_src = sact + row * (kact / 32);
             }
             for (int ch = m.c0; ch < m.c1; ++ch, ++q, rp.step()) {
@@ -454,21 +463,21 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 if (!__shfl_sync(0xffffffffu, w, 0)) return false;
                 const uint32_t base = ring_addr + slot * kSlotBytes, fb = smem_u32(&sh.full[slot]);
                 const uint32_t sfbase = sf_addr + slot * kSfSlotBytes;
-                // the 16-byte group of scale words (4 chunks) holding this chunk's
-                // word, for every weight row; every slot gets its own copy, so a
-                // consumer reads word ch % 4 of its own slot
-                const int gx = (ch & ~3) * 4;
+                // the 16-byte group of scale bytes (2 chunks) holding this chunk's
+                // two words, for every weight row; every slot gets its own copy, so
+                // a consumer reads words 2 (ch % 2) and 2 (ch % 2) + 1 of its own slot
+                const int gx = (ch & ~1) * 8;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, kCodeBytes + kRows * 16);
                     if (gu) {
                         // one box holds the row block's 64 gate rows, then its 64 up
                         // rows (planes 2e and 2e + 1 of the w13 plane seen as 2E
                         // planes of I rows)
-                        tma_load_3d(base, &gu_map, ch * 32, 64 * m.rb, 2 * m.expert, fb);
+                        tma_load_3d(base, &gu_map, ch * 64, 64 * m.rb, 2 * m.expert, fb);
                         tma_load_3d(sfbase, &gu_sf_map, gx, 64 * m.rb, 2 * m.expert, fb);
                     } else {
                         const int rd = (int)(erow + 128 * m.rb);
-                        tma_load_2d(base, &dn_map, ch * 32, rd, fb);
+                        tma_load_2d(base, &dn_map, ch * 64, rd, fb);
                         tma_load_2d(sfbase, &dn_sf_map, gx, rd, fb);
                     }
                 }
@@ -557,10 +566,14 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                     tc_fence_after();
                     fence_proxy_async_smem();   // activation rows came by cp.async (generic proxy)
                     const uint64_t bd = smem_desc_sw128(ring_addr + slot * kSlotBytes + kBOff);
+                    // MMA t: K 64t..64t+63 of the chunk = A columns 8t..8t+7 of the
+                    // stage, 32 bytes of every B row, scale word t / 2, bytes
+                    // 2 (t % 2) and 2 (t % 2) + 1
 #pragma unroll
                     for (uint32_t t = 0; t < 4; ++t)
-                        umma_mxf8_ts(tm + kColD + 16 * b, tm + kColA + 32 * st + 8 * t, bd + 2 * t,
-                                     idesc_mxf_e2m1_e4m3(kRows, kN, t, t), tm + kColSfa + 4 * st, tm + kColSfb + 4 * st,
+                        umma_mxf4_ts(tm + kColD + 16 * b, tm + kColA + 32 * st + 8 * t, bd + 2 * t,
+                                     idesc_mxf4(kRows, kN, 2 * (t & 1), 2 * (t & 1)),
+                                     tm + kColSfa + 8 * st + 4 * (t >> 1), tm + kColSfb + 8 * st + 4 * (t >> 1),
                                      (ch != m.c0 || t != 0) ? 1u : 0u);
                     umma_commit(smem_u32(&sh.a_empty[st]));
                     umma_commit(smem_u32(&sh.empty[slot]));
@@ -597,7 +610,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
         // ------------------------------------------------ consumers
         const int m = tid;   // weight row of the item
         const uint32_t tq = tm + ((uint32_t)(32 * warp) << 16);
-        const uint32_t swz = ((uint32_t)m >> 2) & 1u;   // 32B swizzle of this code row
+        const uint32_t swz = ((uint32_t)m >> 1) & 3u;   // 64B swizzle of this code row
         uint32_t q = 0, bad_scale = 0;
         RingPos<kSlots> rp;
         Item prev{};
@@ -624,32 +637,41 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sb = ring_addr + slot * kSlotBytes;
-                const uint4 w0 = lds_u4(sb + m * 32 + (swz << 4));
-                const uint4 w1 = lds_u4(sb + m * 32 + ((swz ^ 1u) << 4));
-                const uint32_t sfs = sf_addr + slot * kSfSlotBytes + 4u * (uint32_t)(ch & 3);
-                uint32_t sfa = lds_u32(sfs + m * 16);
-                const uint32_t sfb = lds_u32(sfs + kSfbOff + (lane & 15) * 16);
-                const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                // the row's 64 code bytes (16-byte unit u of the row at u ^ swz)
+                const uint32_t sb = ring_addr + slot * kSlotBytes + m * 64;
+                uint32_t wd[16];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint4 v = lds_u4(sb + ((u ^ swz) << 4));
+                    wd[4 * u] = v.x;
+                    wd[4 * u + 1] = v.y;
+                    wd[4 * u + 2] = v.z;
+                    wd[4 * u + 3] = v.w;
+                }
+                // the chunk's two scale words of this row and of the digit rows
+                const uint32_t sfs = sf_addr + slot * kSfSlotBytes + 8u * (uint32_t)(ch & 1);
+                uint2 sfa = lds_u2(sfs + m * 16);
+                const uint2 sfb = lds_u2(sfs + kSfbOff + (lane & 15) * 16);
                 uint32_t r[32];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    expand_e2m1(wd[i], r[4 * i + 0], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
-                }
-                if (scale_word_suspect(sfa)) {
-                    // an invalid scale byte: that block counts as zero
+                for (int i = 0; i < 16; ++i) expand_fp4(wd[i], r[2 * i], r[2 * i + 1]);
+                if (scale_word_suspect(sfa.x) | scale_word_suspect(sfa.y)) {
+                    // an invalid scale byte: that 32-element block (4 registers) counts as zero
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint32_t sbyte = (sfa >> (8 * t)) & 0xFFu;
-                        if (sbyte - 1u > 251u) {
+                    for (int t = 0; t < 8; ++t) {
+                        uint32_t& wv = t < 4 ? sfa.x : sfa.y;
+                        const int sh = 8 * (t & 3);
+                        if (((wv >> sh) & 0xFFu) - 1u > 251u) {
 #pragma unroll
-                            for (int c = 0; c < 8; ++c) r[8 * t + c] = 0u;
-                            sfa = (sfa & ~(0xFFu << (8 * t))) | (127u << (8 * t));
+                            for (int c = 0; c < 4; ++c) r[4 * t + c] = 0u;
+                            wv = (wv & ~(0xFFu << sh)) | (127u << sh);
                             bad_scale = 1;
                         }
                     }
                 }
-                tmem_st_stage(tq + kColA + 32 * st, r, tq + kColSfa + 4 * st + warp, sfa, tq + kColSfb + 4 * st, sfb);
+                tmem_st_stage4(tq + kColA + 32 * st, r, tq + kColSfa + 8 * st + warp, sfa.x,
+                               tq + kColSfa + 8 * st + 4 + warp, sfa.y, tq + kColSfb + 8 * st, sfb.x,
+                               tq + kColSfb + 8 * st + 4, sfb.y);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh.a_full[st]));
@@ -728,10 +750,10 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     a.sorted = ws.sorted;
     a.weights = weights;
     a.ids = ids;
-    a.x8 = ws.x8;
-    a.sx8 = ws.sx8;
-    a.h8 = ws.h8;
-    a.sh8 = ws.sh8;
+    a.xd = ws.xd;
+    a.sxd = ws.sxd;
+    a.hd = ws.hd;
+    a.shd = ws.shd;
     a.gu_part = ws.gu_part;
     a.stage = ws.stage;
     a.gu_seg = ws.counters;                    // zeroed by the permutation kernel
@@ -739,14 +761,14 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     a.y = y;
     a.status = status;
 
-    // code tiles: 32 bytes (128 codes) x 128 rows, 32B-swizzled; gate_up as a
-    // 3-D box {32 bytes, 64 rows, 2 planes} over the w13 plane seen as 2E planes
+    // code tiles: 64 bytes (256 codes) x 128 rows, 64B-swizzled; gate_up as a
+    // 3-D box {64 bytes, 64 rows, 2 planes} over the w13 plane seen as 2E planes
     // (gate, up) of I rows, down as a 2-D box of 128 rows
     CUtensorMap gu_map, dn_map;
-    cudaError_t e = make_tmap_3d_u8(&gu_map, w.w13_codes, 2 * (int64_t)E, I, H / 4, 32, 64, 2, 32);
+    cudaError_t e = make_tmap_3d_u8(&gu_map, w.w13_codes, 2 * (int64_t)E, I, H / 4, 64, 64, 2, 64);
     if (e != cudaSuccess) return e;
-    if ((e = make_tmap_2d(&dn_map, w.w2_codes, false, (int64_t)E * H, I / 4, 32, 128, 32)) != cudaSuccess) return e;
-    // scale groups: 16 bytes (4 chunks) x 64 rows (gate_up) or x 128 rows (down);
+    if ((e = make_tmap_2d(&dn_map, w.w2_codes, false, (int64_t)E * H, I / 4, 64, 128, 64)) != cudaSuccess) return e;
+    // scale groups: 16 bytes (2 chunks) x 64 rows (gate_up) or x 128 rows (down);
     // rows of H/32 and I/32 bytes are multiples of 16 (H, I multiples of 512)
     CUtensorMap gu_sf_map, dn_sf_map;
     if ((e = make_tmap_3d_u8(&gu_sf_map, w.w13_scales, 2 * (int64_t)E, I, H / 32, 16, 64, 2, 0)) != cudaSuccess)

@@ -12,8 +12,8 @@
 // The same launch also emits the active-expert list (decode scheduling) and the
 // GEMM tile list (expert, first slot, pairs) with at most tile_rows pairs per
 // tile.  Extra CTAs of the launch write x as the decode kernels read it: in T16
-// order (mma.sync kernel) or as block-scaled e4m3 activation rows (two per
-// token, see act_split).
+// order (mma.sync kernel) or as rows of packed e2m1 digits with UE8M0 bytes per
+// 32 elements (block-scaled kernel, kActDigits rows per token).
 #include <algorithm>
 
 #include "common.cuh"
@@ -92,45 +92,39 @@ __device__ __forceinline__ void t16_group(const uint16_t* src, uint16_t* dst)
     *reinterpret_cast<uint4*>(dst + 8) = p;
 }
 
-// Four elements of a 32-element block of token t, one of 8 threads of the
-// block (lanes 8c..8c+7 of a warp hold block c of the warp): rows 2t (hi) and
-// 2t+1 (lo) of x8, e4m3 in the e4_elem order, and the block's UE8M0 byte in
-// both rows of sx8.  Thread r of the block writes stored bytes 4r..4r+3.
-__device__ __forceinline__ void x8_quarter(const uint16_t* __restrict__ x, int64_t blk, int r, bool live, int32_t H,
-                                           uint8_t* __restrict__ x8, uint8_t* __restrict__ sx8)
+// Two elements of a 32-element block of token t, one of 16 threads of the block
+// (lanes 16c..16c+15 of a warp hold block c of the warp): byte r of the block in
+// each of the token's kActDigits digit rows of xd (packed positions 2r and 2r+1,
+// in the fp4_elem order), and from thread 0 the rows' UE8M0 bytes in sxd.
+__device__ __forceinline__ void x_digits(const uint16_t* __restrict__ x, int64_t blk, int r, bool live, int32_t H,
+                                         uint8_t* __restrict__ xd, uint8_t* __restrict__ sxd)
 {
     const int bpr = H / 32;
     const int64_t t = blk / bpr;
     const int c = (int)(blk % bpr);
-    // stored bytes 4r..4r+3 hold elements g*16 + e4_elem(p) for p = (4r..4r+3) & 15, g = r >> 2
-    float f[4];
-    float amax = 0.f;
+    float v[2];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int p = 4 * r + u;
-        const int e = (p & ~15) | e4_elem(p & 15);
-        f[u] = live ? __uint_as_float((uint32_t)__ldg(x + t * H + c * 32 + e) << 16) : 0.f;
-        amax = fmaxf(amax, fabsf(f[u]));
+    for (int h = 0; h < 2; ++h) {
+        const int pos = 2 * r + h;
+        const int e = (pos & 16) | fp4_elem(pos & 15);
+        v[h] = live ? __uint_as_float((uint32_t)__ldg(x + t * H + c * 32 + e) << 16) : 0.f;
     }
-    // block maximum over the 8 threads of the block
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const uint32_t s = act_scale_byte(amax);
-    const float inv = act_inv_scale(s);
-    uint32_t hi = 0, lo = 0;
+    for (int d = 0; d < kActDigits; ++d) {
+        // the block's largest leftover over the 16 threads of the block
+        float amax = fmaxf(fabsf(v[0]), fabsf(v[1]));
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        uint32_t h, l;
-        act_split(f[u] * inv, h, l);
-        hi |= h << (8 * u);
-        lo |= l << (8 * u);
-    }
-    if (!live) return;
-    *reinterpret_cast<uint32_t*>(x8 + (2 * t) * H + c * 32 + 4 * r) = hi;
-    *reinterpret_cast<uint32_t*>(x8 + (2 * t + 1) * H + c * 32 + 4 * r) = lo;
-    if (r == 0) {
-        sx8[(2 * t) * bpr + c] = (uint8_t)s;
-        sx8[(2 * t + 1) * bpr + c] = (uint8_t)s;
+        for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const uint32_t s = digit_scale_byte(amax);
+        const float inv = digit_inv_scale(s), sc = digit_scale(s);
+        float q0, q1;
+        const uint32_t n0 = e2m1_digit(v[0] * inv, q0), n1 = e2m1_digit(v[1] * inv, q1);
+        v[0] -= q0 * sc;
+        v[1] -= q1 * sc;
+        if (live) {
+            xd[(kActDigits * t + d) * (H / 2) + c * 16 + r] = (uint8_t)(n0 | (n1 << 4));
+            if (r == 0) sxd[(kActDigits * t + d) * bpr + c] = (uint8_t)s;
+        }
     }
 }
 
@@ -138,8 +132,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
     const int32_t* __restrict__ ids, int32_t P, int32_t E, int32_t* __restrict__ sorted,
     int32_t* __restrict__ inv, int32_t* __restrict__ offsets, int32_t* __restrict__ active,
     int32_t* __restrict__ active_count, int4* __restrict__ tiles, int32_t* __restrict__ tile_count,
-    int32_t tile_rows, const uint16_t* __restrict__ x, uint16_t* __restrict__ x_t16, uint8_t* __restrict__ x8,
-    uint8_t* __restrict__ sx8, int32_t H, int64_t n_blocks, int32_t* __restrict__ counters, int32_t n_counters,
+    int32_t tile_rows, const uint16_t* __restrict__ x, uint16_t* __restrict__ x_t16, uint8_t* __restrict__ xd,
+    uint8_t* __restrict__ sxd, int32_t H, int64_t n_blocks, int32_t* __restrict__ counters, int32_t n_counters,
     uint16_t* __restrict__ y, int64_t y_elems, uint32_t* status)
 {
     // the decode layer kernel may launch now; it waits for this grid to finish
@@ -154,12 +148,12 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
         return;
     }
     if (blockIdx.x > 0) {
-        // extra CTAs: the decode kernel's e4m3 activation rows of every token,
-        // 8 threads per 32-element block (warp-uniform trip count)
-        const int64_t stride = (int64_t)(gridDim.x - 1) * (blockDim.x / 8);
-        const int64_t nb_pad = (n_blocks + 3) & ~(int64_t)3;
-        for (int64_t b = (int64_t)(blockIdx.x - 1) * (blockDim.x / 8) + (threadIdx.x >> 3); b < nb_pad; b += stride)
-            x8_quarter(x, b < n_blocks ? b : 0, threadIdx.x & 7, b < n_blocks, H, x8, sx8);
+        // extra CTAs: the block-scaled decode kernel's digit rows of every
+        // token, 16 threads per 32-element block (warp-uniform trip count)
+        const int64_t stride = (int64_t)(gridDim.x - 1) * (blockDim.x / 16);
+        const int64_t nb_pad = (n_blocks + 1) & ~(int64_t)1;
+        for (int64_t b = (int64_t)(blockIdx.x - 1) * (blockDim.x / 16) + (threadIdx.x >> 4); b < nb_pad; b += stride)
+            x_digits(x, b < n_blocks ? b : 0, threadIdx.x & 15, b < n_blocks, H, xd, sxd);
         return;
     }
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
@@ -285,8 +279,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
 
 cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* sorted, int32_t* inv,
                            int32_t* offsets, int32_t* active, int32_t* active_count, int4* tiles,
-                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16, uint8_t* x8,
-                           uint8_t* sx8, int32_t H, int32_t* counters, int32_t n_counters, uint16_t* y,
+                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16, uint8_t* xd,
+                           uint8_t* sxd, int32_t H, int32_t* counters, int32_t n_counters, uint16_t* y,
                            uint32_t* status, cudaStream_t s)
 {
     const int32_t P = T * k;
@@ -303,12 +297,12 @@ cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, 
     if (x != nullptr && x_t16 != nullptr) {
         n_blocks = (int64_t)T * H / 32;
         extra = (int)std::min<int64_t>((n_blocks * 2 + kThreads - 1) / kThreads, 4 * (int64_t)sm_count());
-    } else if (x != nullptr && x8 != nullptr) {
+    } else if (x != nullptr && xd != nullptr) {
         n_blocks = (int64_t)T * H / 32;
-        extra = (int)std::min<int64_t>((n_blocks * 8 + kThreads - 1) / kThreads, 4 * (int64_t)sm_count());
+        extra = (int)std::min<int64_t>((n_blocks * 16 + kThreads - 1) / kThreads, 4 * (int64_t)sm_count());
     }
     permute_kernel<<<1 + extra, kThreads, smem, s>>>(ids, P, E, sorted, inv, offsets, active, active_count, tiles,
-                                                     tile_count, tile_rows, x, x_t16, x8, sx8, H, n_blocks,
+                                                     tile_count, tile_rows, x, x_t16, xd, sxd, H, n_blocks,
                                                      counters, n_counters, y, y ? (int64_t)T * H : 0, status);
     return cudaGetLastError();
 }

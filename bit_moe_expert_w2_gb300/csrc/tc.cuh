@@ -84,6 +84,12 @@ __device__ __forceinline__ uint4 lds_u4(uint32_t saddr)
                  : "memory");
     return r;
 }
+__device__ __forceinline__ uint2 lds_u2(uint32_t saddr)
+{
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(saddr) : "memory");
+    return r;
+}
 __device__ __forceinline__ void sts_u4(uint32_t saddr, const uint4& v)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -234,57 +240,61 @@ __device__ __forceinline__ void tmem_st32_sync(uint32_t taddr, const uint32_t (&
 
 // ------------------------------------------------------------------ block-scaled MMA (decode)
 //
-// tcgen05.mma kind::mxf8f6f4 with UE8M0 block scales, one scale per 32 K per
-// row of A and per row of B (scale_vec::1X), A read from tensor memory.  Layouts
-// measured on GB300 with an in-bounds probe of the instruction:
-//  - A (M = 128): lane m holds row m; column j, byte b holds K index 4j + b.
-//  - A scales: the scale of row m is read from lane m of the column
-//    (scale_A_tmem + m / 32), byte = a_sf_id.  So the warp owning lanes
-//    32w..32w+31 writes its rows' scale words into column scale_A_tmem + w.
-//  - B scales: the scale of B row n is read from lane n % 32 of column
-//    scale_B_tmem in the lane quadrant of the output row, byte = b_sf_id, so
+// tcgen05.mma kind::mxf4 (A and B packed e2m1, two per byte) with UE8M0 block
+// scales, one per 32 K per row of A and per row of B (scale_vec::2X: an MMA of K
+// = 64 takes two consecutive scale bytes), A read from tensor memory.  Layouts
+// measured on GB300 with in-bounds probes of the instruction (M = 128, N = 16):
+//  - A: lane m holds row m; column j, nibble i (bits 4i..4i+3) holds K index
+//    8j + i, so one MMA reads 8 columns.
+//  - B (shared memory, K-major, 128B-swizzled rows): nibble h (low first) of
+//    byte b holds K index 2b + h; one MMA reads 32 bytes of each row.
+//  - A scales: the scale word of row m is read from lane m of the column
+//    (scale_A_tmem + m / 32); bytes sf_id and sf_id + 1 (sf_id 0 or 2) scale K
+//    0..31 and 32..63 of the MMA.  So the warp owning lanes 32w..32w+31 writes
+//    its rows' scale words into column scale_A_tmem + w.
+//  - B scales: the scale word of B row n is read from lane n % 32 of column
+//    scale_B_tmem in the lane quadrant of the output row, same byte use, so
 //    every quadrant holds a copy.
+//  - Scale-factor columns start on a 4-column boundary (an odd column raised a
+//    misaligned-address fault).
 // Instruction descriptor (block-scaled form): b_sf_id bits 4-5, A/B format bits
-// 7-9 / 10-12 (0 = e4m3), N >> 3 in bits 17-22, scale format bit 23 (1 = UE8M0),
-// M >> 4 in bits 24-28, a_sf_id bits 29-30; K-major A and B, dense, fp32 D.
-__host__ __device__ __forceinline__ uint32_t idesc_mxf8_e4m3(uint32_t M, uint32_t N, uint32_t a_sf, uint32_t b_sf)
+// 7-9 / 10-12 (1 = e2m1 for kind::mxf4), N >> 3 in bits 17-22, scale format bit
+// 23 (1 = UE8M0), M >> 4 in bits 24-28, a_sf_id bits 29-30; K-major A and B,
+// dense, fp32 D.
+__host__ __device__ __forceinline__ uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32_t a_sf, uint32_t b_sf)
 {
-    return (b_sf << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (a_sf << 29);
+    return (b_sf << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (a_sf << 29);
 }
-// Same form with A in e2m1 (format 5) held in 8-bit containers, B in e4m3.  Measured
-// on GB300: the MMA reads bits [5:0] of each A byte as sign, two exponent bits and
-// three mantissa bits, so an e2m1 value sits in bits [5:2] with bits [1:0] zero and
-// bits [7:6] are ignored; byte 0x08 is +1, 0x18 is +4, 0x28 is -1, 0x38 is -4.
-__host__ __device__ __forceinline__ uint32_t idesc_mxf_e2m1_e4m3(uint32_t M, uint32_t N, uint32_t a_sf, uint32_t b_sf)
-{
-    return idesc_mxf8_e4m3(M, N, a_sf, b_sf) | (5u << 7);
-}
-__device__ __forceinline__ void umma_mxf8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void umma_mxf4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
 {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n}\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], [%1], %2, %3, [%4], [%5], p;\n}\n"
         ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
 
-// 32 columns of A plus one column of A scales and one of B scales from this
-// warp's registers into its TMEM lane quadrant, completed before returning (the
-// registers are read until tcgen05.wait::st, so store and wait share one asm).
-__device__ __forceinline__ void tmem_st_stage(uint32_t ta, const uint32_t (&r)[32], uint32_t tsa, uint32_t sa,
-                                              uint32_t tsb, uint32_t sb)
+// 32 columns of A, two columns of A scale words and two of B scale words from
+// this warp's registers into its TMEM lane quadrant, completed before returning
+// (the registers are read until tcgen05.wait::st, so store and wait share one asm).
+__device__ __forceinline__ void tmem_st_stage4(uint32_t ta, const uint32_t (&r)[32], uint32_t tsa0, uint32_t sa0,
+                                               uint32_t tsa1, uint32_t sa1, uint32_t tsb0, uint32_t sb0, uint32_t tsb1,
+                                               uint32_t sb1)
 {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
         "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
         "tcgen05.st.sync.aligned.32x32b.x1.b32 [%33], {%34};\n"
         "tcgen05.st.sync.aligned.32x32b.x1.b32 [%35], {%36};\n"
+        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%37], {%38};\n"
+        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%39], {%40};\n"
         "tcgen05.wait::st.sync.aligned;" ::"r"(ta),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
         "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
-        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(tsa), "r"(sa), "r"(tsb), "r"(sb)
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(tsa0), "r"(sa0), "r"(tsa1), "r"(sa1),
+        "r"(tsb0), "r"(sb0), "r"(tsb1), "r"(sb1)
         : "memory");
 }
 

@@ -158,7 +158,7 @@ moe_w2_status moe_w2_forward_traced(const void *x_bf16, const int32_t *topk_ids,
  * the library's device code holds it until the process exits.
  *   - Sizes whose moe_w2_forward_workspace_size() exceeds
  *     MOE_W2_NOALLOC_WORKSPACE_BYTES return MOE_W2_ERR_WORKSPACE and enqueue
- *     nothing (at H=6144, I=2048, E=256, top_k=8 that is T > 9).
+ *     nothing (at H=6144, I=2048, E=256, top_k=8 that is T > 16).
  *   - The first call on each device looks up the array's address
  *     (cudaGetSymbolAddress, with that device current) and keeps it; make that
  *     first call before any stream capture starts.

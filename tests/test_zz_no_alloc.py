@@ -79,10 +79,10 @@ def test_two_calls_in_a_row_match_forward(H, I, E, k, T_a, T_b, seed):
 def test_sizes_past_the_static_workspace_are_refused():
     L = moe_w2.load()
     H, I, E, k = 6144, 2048, 256, 8
-    assert moe_w2.workspace_size(9, k, E, H, I) <= moe_w2.NOALLOC_WORKSPACE_BYTES
-    assert moe_w2.workspace_size(10, k, E, H, I) > moe_w2.NOALLOC_WORKSPACE_BYTES
+    assert moe_w2.workspace_size(16, k, E, H, I) <= moe_w2.NOALLOC_WORKSPACE_BYTES
+    assert moe_w2.workspace_size(17, k, E, H, I) > moe_w2.NOALLOC_WORKSPACE_BYTES
     # the size check comes before any pointer is used: nothing is enqueued
     planes = moe_w2.Planes(None, None, None, None, E, H, I)
-    st = L.moe_w2_forward_noalloc(None, None, None, ctypes.byref(planes), 10, k, None, None, None)
+    st = L.moe_w2_forward_noalloc(None, None, None, ctypes.byref(planes), 17, k, None, None, None)
     assert st == MOE_W2_ERR_WORKSPACE
     assert moe_w2.status_string(st) == "workspace too small"

@@ -391,9 +391,9 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
     # prefill: permute, gather, gate_up, down, combine
     res["kernels_per_step"] = (2 if moe_w2.decode_kernel(T, k, H, I) == "decode_mma_kernel" else 3) if decode else 5
     # arithmetic of the layer's contractions: the block-scaled decode kernel multiplies e2m1
-    # weights by e4m3 activation pairs (hi + lo) under UE8M0 block scales; the others bf16
+    # weights by five e2m1 digit rows per activation row under UE8M0 block scales; the others bf16
     block_scaled = decode and moe_w2.decode_kernel(T, k, H, I) == "decode_layer_kernel"
-    res["dtype"] = "e2m1 x e4m3 block-scaled, fp32 accumulation" if block_scaled else "bf16, fp32 accumulation"
+    res["dtype"] = "e2m1 x e2m1 digits block-scaled, fp32 accumulation" if block_scaled else "bf16, fp32 accumulation"
 
     # end to end: pinned host inputs -> device -> forward -> y back to pinned host
     hx = [torch.from_numpy(b[0].view(np.int16)).pin_memory() for b in batches]

@@ -56,40 +56,40 @@ __global__ void combine_kernel(const float* __restrict__ stage, const int32_t* _
                                uint16_t* __restrict__ y)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int per_row = H / 8;
+    // one thread per 4 consecutive outputs of a token; its k * n_seg slots are
+    // loaded in batches of 8 (all loads of a batch in flight together) and
+    // summed in (j, segment) order
+    const int per_row = H / 4;
+    const int nks = k * n_seg;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)T * per_row;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t t = i / per_row;
-        const int m = (int)(i % per_row) * 8;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const int m = (int)(i % per_row) * 4;
         uint32_t valid = 0;   // bit j: slot j has an expert (k <= 16)
         for (int j = 0; j < k; ++j) valid |= (uint32_t)((unsigned)__ldg(ids + t * k + j) < (unsigned)E) << j;
-        // slots in (j, segment) order; unrolled so that several loads are in flight
-        const int nks = k * n_seg;
-#pragma unroll 4
-        for (int x = 0; x < nks; ++x) {
-            const int j = x / n_seg, sg = x - j * n_seg;
-            if ((valid >> j) & 1u) {
-                const float4* src = reinterpret_cast<const float4*>(stage + sg * seg_stride + (t * k + j) * H + m);
-                const float4 a = __ldcg(src), b = __ldcg(src + 1);
-                acc[0] += a.x;
-                acc[1] += a.y;
-                acc[2] += a.z;
-                acc[3] += a.w;
-                acc[4] += b.x;
-                acc[5] += b.y;
-                acc[6] += b.z;
-                acc[7] += b.w;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int x0 = 0; x0 < nks; x0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int x = x0 + u, j = x / n_seg, sg = x - j * n_seg;
+                v[u] = (x < nks && ((valid >> j) & 1u))
+                           ? __ldcg(reinterpret_cast<const float4*>(stage + sg * seg_stride + (t * k + j) * H + m))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                acc.x += v[u].x;
+                acc.y += v[u].y;
+                acc.z += v[u].z;
+                acc.w += v[u].w;
             }
         }
-        uint4 o;
-        uint32_t* ow = &o.x;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            __nv_bfloat162 pr = __floats2bfloat162_rn(acc[2 * v], acc[2 * v + 1]);
-            ow[v] = *reinterpret_cast<uint32_t*>(&pr);
-        }
-        *reinterpret_cast<uint4*>(y + t * H + m) = o;
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 o;
+        o.x = *reinterpret_cast<const uint32_t*>(&lo);
+        o.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(y + t * H + m) = o;
     }
 }
 
@@ -162,7 +162,7 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted, const int32_
 cudaError_t launch_combine(const float* stage, const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t H,
                            int32_t n_seg, int64_t seg_stride, bool programmatic, uint16_t* y, cudaStream_t s)
 {
-    const int64_t threads = (int64_t)T * (H / 8);
+    const int64_t threads = (int64_t)T * (H / 4);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((threads + 255) / 256, (int64_t)sm_count() * 8));
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid);

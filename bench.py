@@ -395,23 +395,28 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
     block_scaled = decode and moe_w2.decode_kernel(T, k, H, I) == "decode_layer_kernel"
     res["dtype"] = "e2m1 x e2m1 digits block-scaled, fp32 accumulation" if block_scaled else "bf16, fp32 accumulation"
 
-    # end to end: pinned host inputs -> device -> forward -> y back to pinned host
-    hx = [torch.from_numpy(b[0].view(np.int16)).pin_memory() for b in batches]
-    hid = [torch.from_numpy(b[1]).pin_memory() for b in batches]
-    hw = [torch.from_numpy(b[2]).pin_memory() for b in batches]
+    # end to end: pinned host inputs -> device -> forward -> y back to pinned host.  A step's
+    # x, ids and weights sit back to back in one pinned buffer, so they cross in one copy
+    nx, ni = T * H * 2, T * k * 4
+    def packed(b):
+        buf = torch.empty(nx + 2 * ni, dtype=torch.uint8).pin_memory()
+        buf[:nx].copy_(torch.from_numpy(b[0].view(np.uint8).reshape(-1)))
+        buf[nx:nx + ni].copy_(torch.from_numpy(b[1].view(np.uint8).reshape(-1)))
+        buf[nx + ni:].copy_(torch.from_numpy(b[2].view(np.uint8).reshape(-1)))
+        return buf
+    hin = [packed(b) for b in batches]
     hy = [torch.empty((T, H), dtype=torch.int16).pin_memory() for _ in range(pool)]
-    dx = torch.empty((T, H), dtype=torch.int16, device=dev)
-    did = torch.empty((T, k), dtype=torch.int32, device=dev)
-    dw = torch.empty((T, k), dtype=torch.float32, device=dev)
+    din = torch.empty(nx + 2 * ni, dtype=torch.uint8, device=dev)
+    dx = din[:nx].view(torch.int16).view(T, H)
+    did = din[nx:nx + ni].view(torch.int32).view(T, k)
+    dw = din[nx + ni:].view(torch.float32).view(T, k)
     dy = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     e_start = [torch.cuda.Event(enable_timing=True) for _ in range(pool)]
     e_end = [torch.cuda.Event(enable_timing=True) for _ in range(pool)]
 
     def e2e_step(i):
         e_start[i].record(stream)
-        dx.copy_(hx[i], non_blocking=True)
-        did.copy_(hid[i], non_blocking=True)
-        dw.copy_(hw[i], non_blocking=True)
+        din.copy_(hin[i], non_blocking=True)
         st = L.moe_w2_forward(moe_w2._ptr(dx), moe_w2._ptr(did), moe_w2._ptr(dw), ctypes.byref(P), T, k,
                               moe_w2._ptr(dy), moe_w2._ptr(work), work.numel(), moe_w2._ptr(status),
                               ctypes.c_void_p(stream.cuda_stream))

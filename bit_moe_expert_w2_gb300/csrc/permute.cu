@@ -32,6 +32,75 @@ __device__ __forceinline__ uint32_t lanemask_lt()
     return r;
 }
 
+// The whole permutation of a step of at most 32 pairs by one warp (lane p holds
+// pair p): the same outputs as the CTA path below, without its barriers.  Bins:
+// expert id, E for out-of-range ids, E + 1 for lanes past P (never stored).
+// Returns the number of valid pairs (to every lane).
+__device__ int warp_permute(const int32_t* __restrict__ ids, int32_t P, int32_t E, int32_t* __restrict__ sorted,
+                            int32_t* __restrict__ inv, int32_t* __restrict__ offsets, int32_t* __restrict__ active,
+                            int32_t* __restrict__ active_count, int4* __restrict__ tiles,
+                            int32_t* __restrict__ tile_count, int32_t tile_rows, int* s_bin, uint32_t* status)
+{
+    const int lane = threadIdx.x & 31;
+    int b = E + 1;
+    if (lane < P) {
+        const int e = __ldg(ids + lane);
+        b = (unsigned)e < (unsigned)E ? e : E;
+    }
+    if (__any_sync(0xffffffffu, lane < P && b == E) && lane == 0) flag_status(status, MOE_W2_DEV_BAD_EXPERT_ID);
+    // stable rank inside the bin, and the pairs of lower bins
+    const uint32_t same = __match_any_sync(0xffffffffu, b);
+    const int rank = __popc(same & lanemask_lt());
+    const bool lead = rank == 0 && b < E;   // first pair of an active expert
+    const int cnt = __popc(same);
+    const int ntl = lead && tiles != nullptr ? (cnt + tile_rows - 1) / tile_rows : 0;
+    int less = 0, act_before = 0, tiles_before = 0;
+    for (int i = 0; i < 32; ++i) {
+        const int bi = __shfl_sync(0xffffffffu, b, i);
+        const int li = __shfl_sync(0xffffffffu, (int)lead, i);
+        const int ti = __shfl_sync(0xffffffffu, ntl, i);
+        less += bi < b;
+        act_before += (li && bi < b);
+        tiles_before += (li && bi < b) ? ti : 0;
+    }
+    const int pos = less + rank;
+    if (lane < P) {
+        sorted[pos] = lane;
+        inv[lane] = pos;
+        s_bin[pos] = b;
+    }
+    __syncwarp();
+    const int sb = lane < P ? s_bin[lane] : E + 1;   // bins in sorted order, nondecreasing
+    // offsets[bin] = sorted bins below bin (a binary search over the warp's 32)
+    const int last = __shfl_sync(0xffffffffu, sb, 31);
+    for (int base = 0; base <= E; base += 32) {
+        const int bin = base + lane;
+        int lo = 0;
+#pragma unroll
+        for (int st = 16; st >= 1; st >>= 1)
+            if (__shfl_sync(0xffffffffu, sb, lo + st - 1) < bin) lo += st;
+        if (last < bin) lo = 32;
+        if (bin <= E) offsets[bin] = lo;
+    }
+    const int n_valid = __popc(__ballot_sync(0xffffffffu, lane < P && b < E));
+    if (active != nullptr) {
+        if (lead) active[act_before] = b;
+        const int n_act = __popc(__ballot_sync(0xffffffffu, lead));
+        if (lane == 0) *active_count = n_act;
+    }
+    if (tiles != nullptr) {
+        for (int i = 0; i < ntl; ++i) {
+            const int r0 = (int)(((int64_t)i * cnt) / ntl), r1 = (int)(((int64_t)(i + 1) * cnt) / ntl);
+            tiles[tiles_before + i] = make_int4(b, less + r0, r1 - r0, 0);
+        }
+        int tot = ntl;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (lane == 0) *tile_count = tot;
+    }
+    return n_valid;
+}
+
 // Exclusive scan over the CTA of three ints per thread at once (one pass of
 // shuffles and two barriers for all three); tot[] receives the three totals.
 __device__ int3 cta_exclusive_scan3(int3 v, int3* warp_tmp, int3* tot)
@@ -157,6 +226,20 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
         return;
     }
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
+    if (P <= 32) {
+        // a small step: one warp permutes; the CTA zeroes y if no pair is valid
+        __shared__ int s_bin[32];
+        __shared__ int s_valid;
+        if (threadIdx.x < 32) {
+            const int n_valid = warp_permute(ids, P, E, sorted, inv, offsets, active, active_count, tiles,
+                                             tile_count, tile_rows, s_bin, status);
+            if (threadIdx.x == 0) s_valid = n_valid;
+        }
+        __syncthreads();
+        if (y != nullptr && s_valid == 0)
+            for (int64_t i = threadIdx.x; i < y_elems; i += kThreads) y[i] = 0;
+        return;
+    }
     extern __shared__ int32_t smem[];
     __shared__ int3 warp_tmp[kWarps];
     int3 sh_tot;   // totals of the fused scan (same value in every thread)

@@ -31,6 +31,22 @@ def test_permute_bit_exact(T, k, E, seed):
     assert int(st.item()) == rst == 0
 
 
+@pytest.mark.parametrize("T,k,E", [(3, 8, 64), (4, 8, 256), (2, 16, 40), (33, 1, 5)])
+def test_permute_small_steps_with_invalid_and_repeated_ids(T, k, E):
+    # steps of at most 32 pairs take the one-warp path, 33 the CTA path
+    rng = np.random.default_rng(T * 100 + k)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    ids.flat[1] = -1
+    ids.flat[-1] = E
+    ids.flat[2] = ids.flat[0]
+    st = _status()
+    s, inv, off = moe_w2.permute(torch.from_numpy(ids).cuda(), E, status=st)
+    rs, rinv, roff, rst = oracle.permute(ids, E)
+    assert np.array_equal(s.cpu().numpy(), rs) and np.array_equal(inv.cpu().numpy(), rinv)
+    assert np.array_equal(off.cpu().numpy(), roff)
+    assert int(st.item()) == rst == moe_w2.DEV_BAD_EXPERT_ID
+
+
 def test_permute_invalid_ids_and_zipf_routing():
     rng = np.random.default_rng(9)
     ids, _ = inputs.routing_zipf(rng, 32, 256, 8)

@@ -6,7 +6,7 @@
 // handed out in full, or code that runs where an allocation would have to
 // synchronise the device.  They cannot provide the workspace moe_w2_forward
 // asks for, so this entry point takes its scratch from g_noalloc_workspace
-// below instead.  The paper has no counterpart to it.
+// below instead.  The pages describe no such entry point.
 //
 // Set-up: the first call on each device, with that device current, looks up
 // the array's device address with cudaGetSymbolAddress and keeps it; later

@@ -150,7 +150,7 @@ moe_w2_status moe_w2_forward_traced(const void *x_bf16, const int32_t *topk_ids,
  * moe_w2_forward without a caller-supplied workspace, for callers that cannot
  * allocate device memory where they run the layer (an allocator that may not
  * grow, device memory already handed out in full, or a point where an
- * allocation would synchronise the device).  The paper has no counterpart:
+ * allocation would synchronise the device).  The pages describe no such entry point:
  * it is an interface addition of this library.
  * Same arguments, results and status codes as moe_w2_forward, minus
  * workspace and workspace_bytes: the scratch is a device array of

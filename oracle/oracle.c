@@ -21,7 +21,7 @@
  *           a permutation of token*top_k+j; outputs are placed per pair and
  *           summed over j in a fixed order.
  *
- * Readings taken where the pages are silent (each one is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   R1 code order: 2-bit code c = (sign << 1) | magnitude, i.e. 0:+1 1:+4 2:-1 3:-4.
  *   R2 packing: 4 codes per byte along K, element 4b+q in bits 2q..2q+1 of byte b.
  *   R3 scale search: the UE8M0 exponent u in [-126,125] that minimises the exact

@@ -165,13 +165,6 @@ __device__ __forceinline__ int32_t ld_acquire(const int32_t* p)
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ uint32_t lds_u32(uint32_t saddr)
-{
-    uint32_t r;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(saddr) : "memory");
-    return r;
-}
-
 // Position in a ring of N slots: slot q % N and phase bit (q / N) & 1 of the
 // running chunk count q, stepped without a division.
 template <uint32_t N>

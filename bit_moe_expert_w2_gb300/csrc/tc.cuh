@@ -322,22 +322,11 @@ __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src)
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
 // The barrier gets one arrival once all of this thread's earlier cp.async copies
 // have landed (its expected count includes that arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
 {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// 1-D-in-rows byte tile copy: box {inner bytes, rows} of a 2-D uint8 tensor.
-__device__ __forceinline__ void tma_load_2d_u8(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
-                                               uint32_t bar)
-{
-    tma_load_2d(dst, map, c0, c1, bar);
 }
 
 }  // namespace moe_w2

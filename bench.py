@@ -545,16 +545,14 @@ def main():
         return reference_arm(args, cores)
 
     world, rank, local = dist_setup(args)
+    workload = workload_name(args.config)
     if args.config == inputs.REQUANT.name:
         res, gu = requant_bench(args, world, rank, local)
         metric_unit = "elements/s"
-        workload = f"{inputs.REQUANT.name}: 256 experts NVFP4 gate/up 2x[2048x6144] + down [6144x2048] -> 2-bit planes"
     else:
         cfg = inputs.CONFIGS[args.config]
         res, lay = layer_bench(args, cfg, world, rank, local)
         metric_unit = "tokens/s"
-        workload = (f"{cfg.name}: H={cfg.hidden} I={cfg.inter} E={cfg.num_experts} top-{cfg.top_k} "
-                    f"T={cfg.tokens} routing={cfg.routing}")
     if rank != 0:
         return
     line = {"metric": METRIC, "value": round(res.pop("value"), 3), "unit": metric_unit, "n_gpus": world,
@@ -576,6 +574,15 @@ def main():
     print(json.dumps(line), flush=True)
 
 
+def workload_name(config: str) -> str:
+    """The workload string of a config, the same on both arms."""
+    if config == inputs.REQUANT.name:
+        return f"{inputs.REQUANT.name}: 256 experts NVFP4 gate/up 2x[2048x6144] + down [6144x2048] -> 2-bit planes"
+    cfg = inputs.CONFIGS[config]
+    return (f"{cfg.name}: H={cfg.hidden} I={cfg.inter} E={cfg.num_experts} top-{cfg.top_k} "
+            f"T={cfg.tokens} routing={cfg.routing}")
+
+
 def reference_arm(args, cores):
     """The oracle timed on this host's cores on a bounded sample of the workload."""
     budget = 90.0
@@ -588,14 +595,15 @@ def reference_arm(args, cores):
         cfg = inputs.CONFIGS[args.config]
         lay = inputs.layer_inputs(cfg)
         # warm-up tokens, then timed tokens until the step count or the budget is reached
-        oracle_layer_rate(lay, 0.0, max_tokens=1)
+        oracle_layer_rate(lay, float("inf"), max_tokens=max(args.warmup, 3))
         v, n, el = oracle_layer_rate(lay, budget, max_tokens=args.steps)
         unit, sample = "tokens/s", f"{n} whole tokens of {args.config} in {el:.1f} s"
         steps = n
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": unit, "n_gpus": 0,
-            "steps": steps, "warmup": 1, "ms_per_step": round(el / max(steps, 1) * 1e3, 3), "higher_is_better": True,
+            "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": round(el / max(steps, 1) * 1e3, 3),
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": args.config, "sample": sample},
+            "config": {"workload": workload_name(args.config), "sample": sample},
             "cpu_baseline": {"value": round(v, 4), "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "host_cores_available": cores}

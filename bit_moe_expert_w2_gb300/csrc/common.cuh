@@ -233,15 +233,16 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // ------------------------------------------------------------------ workspace
-// Decode split of K: a decode work item is (tile of <= 8 pairs of one expert,
-// 128 weight rows, a range of K chunks of 128).  gate_up K is cut into equal
-// ranges of the whole phase (one per CTA of a full GPU), down K into equal
-// segments per row block; both chosen so that a one-token step keeps every CTA
-// busy.
+// Decode split of K for the block-scaled kernel: a work item is (tile of <= 3
+// pairs of one expert, 128 weight rows, a range of K chunks of 256).  For
+// gate_up the 128 rows are 64 gate rows and their 64 up rows; when the units
+// are fewer than the CTAs their chunks are cut into equal ranges of the whole
+// phase, one per CTA.  Down K is cut into equal segments per 128-row block.
+// Both keep every CTA of a small step busy.
 struct DecodeSplit {
     int32_t s_gu;         // gate_up: contributing items per 64-row block at most (K = H in ranges)
     int32_t gu_min_range; // gate_up: chunks per range at least (the kernel makes no shorter ranges)
-    int32_t s_dn, l_dn;   // down: segments, chunks per segment (K = I; l a multiple of 4)
+    int32_t s_dn, l_dn;   // down: segments, chunks per segment (K = I)
 };
 DecodeSplit decode_split(int64_t P, int32_t E, int32_t H, int32_t I);
 // True when a decode step of P pairs takes the bf16 mma.sync decode kernel

@@ -10,7 +10,6 @@ namespace moe_w2 {
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 constexpr int32_t kPrefillTileRows = 256;   // pairs per prefill tile (tcgen05 N <= 256)
 constexpr int32_t kDecodeTileRows = 3;      // pairs per decode tile (MMA N = 16: kActDigits rows per pair)
 constexpr int32_t kDecodeMmaTileRows = 16;  // pairs per tile of the mma.sync decode kernel
@@ -51,6 +50,12 @@ bool layer_shape_ok(int32_t E, int32_t H, int32_t I)
 }
 
 }  // namespace
+
+std::mutex& init_mutex()
+{
+    static std::mutex mu;
+    return mu;
+}
 
 int sm_count()
 {

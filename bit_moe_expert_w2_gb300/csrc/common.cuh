@@ -7,6 +7,8 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "moe_w2.h"
 
 namespace moe_w2 {
@@ -318,5 +320,25 @@ cudaError_t launch_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float
                            cudaStream_t s);
 
 int sm_count();
+
+// One-time set-up per device (kernel attributes, occupancy), safe under
+// concurrent calls: kernel attributes belong to a device's context, so each
+// device the library runs on gets its own.  `done` is the call site's table;
+// init(dev) runs under one library-wide mutex until it first succeeds, and
+// `dev` receives the current device.
+constexpr int kMaxDevices = 64;
+std::mutex& init_mutex();
+template <class F>
+cudaError_t once_per_device(bool (&done)[kMaxDevices], int& dev, F&& init)
+{
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(init_mutex());
+    if (done[dev]) return cudaSuccess;
+    e = init(dev);
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
+}
 
 }  // namespace moe_w2

@@ -701,8 +701,10 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     const int32_t E = w.num_experts, H = w.hidden, I = w.inter;
     const int64_t P = (int64_t)T * k;
     constexpr int kDyn = kRingBytes + 1024;
-    static int occ = 0;
-    if (occ == 0) {
+    static bool ready[kMaxDevices];
+    static int occ_of[kMaxDevices];
+    int dev = 0;
+    cudaError_t e0 = once_per_device(ready, dev, [&](int d) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
         if (e != cudaSuccess) return e;
         // all of the unified L1 as shared memory: four CTAs per SM (their tensor
@@ -715,17 +717,19 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
         // although four 128-column CTAs do run side by side)
         cudaFuncAttributes fa{};
         if ((e = cudaFuncGetAttributes(&fa, decode_layer_kernel)) != cudaSuccess) return e;
-        int dev = 0, smem_sm = 0, resv = 0, regs_sm = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess)
+        int smem_sm = 0, resv = 0, regs_sm = 0;
+        if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, d)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, d)) != cudaSuccess)
             return e;
         const int by_smem = smem_sm / (kDyn + (int)fa.sharedSizeBytes + resv);
         const int regs_cta = ((fa.numRegs * 32 + 255) / 256) * 256 * (kThreads / 32);
         const int by_regs = regs_cta > 0 ? regs_sm / regs_cta : 1;
-        occ = std::max(1, std::min({by_smem, by_regs, (int)(512 / kTmemCols)}));
-    }
+        occ_of[d] = std::max(1, std::min({by_smem, by_regs, (int)(512 / kTmemCols)}));
+        return cudaSuccess;
+    });
+    if (e0 != cudaSuccess) return e0;
+    const int occ = occ_of[dev];
     const int64_t mt = max_tiles(P, E, true);
 
     LayerArgs a{};

@@ -460,14 +460,20 @@ cudaError_t launch_decode_mma(const uint16_t* x, const int32_t* ids, const float
     const int32_t E = w.num_experts, H = w.hidden, I = w.inter;
     const int64_t P = (int64_t)T * k;
     constexpr int kDyn = kRingBytes + 128;
-    static int occ = 0;
-    if (occ == 0) {
+    static bool ready[kMaxDevices];
+    static int occ_of[kMaxDevices];
+    int dev = 0;
+    cudaError_t e0 = once_per_device(ready, dev, [&](int d) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
         if (e != cudaSuccess) return e;
+        int occ = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_mma_kernel, kThreads, kDyn);
         if (e != cudaSuccess) return e;
-        occ = std::max(occ, 1);
-    }
+        occ_of[d] = std::max(occ, 1);
+        return cudaSuccess;
+    });
+    if (e0 != cudaSuccess) return e0;
+    const int occ = occ_of[dev];
     const int64_t tiles = max_tiles(P, E, true);
 
     DecArgs gp{};

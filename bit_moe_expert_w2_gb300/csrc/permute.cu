@@ -368,13 +368,13 @@ cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, 
 {
     const int32_t P = T * k;
     const size_t smem = sizeof(int32_t) * (size_t)(kWarps + 1) * (E + 1);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(sizeof(int32_t) * (kWarps + 1) * (MOE_W2_MAX_EXPERTS + 1)));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static bool ready[kMaxDevices];
+    int dev = 0;
+    cudaError_t e0 = once_per_device(ready, dev, [](int) {
+        return cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(sizeof(int32_t) * (kWarps + 1) * (MOE_W2_MAX_EXPERTS + 1)));
+    });
+    if (e0 != cudaSuccess) return e0;
     int64_t n_blocks = 0;
     int extra = 0;
     if (x != nullptr && x_t16 != nullptr) {

@@ -30,7 +30,6 @@
 //   warp 10    TMA producer of the raw code tiles: one superstage (4 stages,
 //              64 code bytes per A row) at a time, two superstages ahead
 #include <algorithm>
-#include <mutex>
 
 #include "tc.cuh"
 
@@ -374,16 +373,16 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
 {
     const int32_t E = w.num_experts, H = w.hidden, I = w.inter;
     const int64_t P = (int64_t)T * k;
-    static bool attr_done = false;
-    if (!attr_done) {
+    static bool ready[kMaxDevices];
+    int dev = 0;
+    cudaError_t e0 = once_per_device(ready, dev, [](int) {
         cudaError_t e = cudaFuncSetAttribute(tc_expert_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(tc_expert_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+        return cudaFuncSetAttribute(tc_expert_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemBytes);
+    });
+    if (e0 != cudaSuccess) return e0;
     const int sms = sm_count();
 
     cudaError_t e = launch_gather(x, ws.sorted, ws.offsets, E, k, H, P, ws.xa, s);

@@ -36,6 +36,11 @@
  *     (a device uint32 the caller zeroes and reads back; NULL = do not report)
  *     and the offending contribution is replaced as documented per bit.
  *   - Results are deterministic: identical inputs give bitwise identical outputs.
+ *   - Host threads may call the entry points concurrently, on any device and
+ *     stream, as long as concurrent calls do not share a workspace or an
+ *     output buffer.  The one-time set-up of each kernel on each device
+ *     (shared-memory attributes, occupancy) happens on the first call there,
+ *     serialised by a lock inside the library.
  *   - Requires a device of compute capability 10.3 (GB300).
  */
 #ifndef MOE_W2_H

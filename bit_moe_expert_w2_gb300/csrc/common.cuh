@@ -82,12 +82,6 @@ __device__ __forceinline__ uint4 ldg_stream_u4(const void* p)
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
     return r;
 }
-__device__ __forceinline__ uint4 ldg_u4(const void* p)
-{
-    uint4 r;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
-}
 __device__ __forceinline__ uint32_t ldg_u16(const void* p)
 {
     unsigned short r;
@@ -114,20 +108,6 @@ __device__ __forceinline__ ScaleLut make_lut(uint32_t s)
     r.lut = ok ? (h * 0x01010101u + 0x81800100u) : 0u;
     r.lo = ok ? ((s & 1u) * 0x80808080u) : 0u;
     return r;
-}
-
-// Selector for bf16 pairs (c_r, c_{r+4}) in the low half and (c_{r+8}, c_{r+12})
-// in the high half of a 16-code word w (code i in bits 2i..2i+1).  Byte-perm
-// nibbles: 4 (any of 4..7) picks the low byte, the code picks its high byte.
-template <int R>
-__device__ __forceinline__ uint32_t code_selector(uint32_t w)
-{
-    uint32_t t = (R == 0) ? (w << 4) : (R == 1) ? (w << 2) : (R == 2) ? w : (w >> 2);
-    return (t & 0x30303030u) | 0x04040404u;
-}
-__device__ __forceinline__ uint32_t expand_pair(const ScaleLut& l, uint32_t sel)
-{
-    return __byte_perm(l.lut, l.lo, sel);
 }
 
 // ------------------------------------------------------------------ selector words (both GEMM paths)

@@ -205,39 +205,6 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t j)
     return (r >> 3) * 1024u + (r & 7u) * 128u + ((j ^ (r & 7u)) << 4);
 }
 
-}  // namespace moe_w2
-
-namespace moe_w2 {
-
-// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16.  A: 128 lanes = rows, K
-// packed two bf16 per 32-bit column (even k in the low half).
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate)
-{
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// 32 consecutive 32-bit columns of this warp's 32 TMEM lanes from registers,
-// completed before returning.  tcgen05.st may read its source registers until
-// tcgen05.wait::st, so the store and the wait are one asm statement and the
-// registers stay untouched in between.
-__device__ __forceinline__ void tmem_st32_sync(uint32_t taddr, const uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
-        "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
-        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
-        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
-        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
 // ------------------------------------------------------------------ block-scaled MMA (decode)
 //
 // tcgen05.mma kind::mxf4 (A and B packed e2m1, two per byte) with UE8M0 block
@@ -329,10 +296,7 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-}  // namespace moe_w2
-
-namespace moe_w2 {
-
+// ------------------------------------------------------------------ host side (route.cu)
 // 2-D tensor map [rows][cols] (row-major) of bf16 or uint8, box {box_cols, box_rows}.
 cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, bool bf16, int64_t rows, int64_t cols,
                          uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);

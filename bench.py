@@ -388,7 +388,8 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
     res["distinct_experts_per_step"] = round(float(np.mean([distinct[i] for i, _ in per_step])), 2)
     res["clocks"] = clk.summary()
     res["wall_s"] = round(wall, 3)
-    # decode: permute (+ x as e4m3 rows), the layer kernel (gate_up, down), combine;
+    # decode: permute (+ x as T16 bf16 or e2m1 digit rows), the layer kernel (gate_up, down), and the
+    # combine kernel after the block-scaled one;
     # prefill: permute, gather, gate_up, down, combine
     res["kernels_per_step"] = (2 if moe_w2.decode_kernel(T, k, H, I) == "decode_mma_kernel" else 3) if decode else 5
     # arithmetic of the layer's contractions: the block-scaled decode kernel multiplies e2m1

@@ -129,9 +129,9 @@ moe_w2_status moe_w2_permute(const int32_t *topk_ids, int32_t T, int32_t top_k, 
  * as 0 (MOE_W2_DEV_BAD_SCALE).  T <= 64 uses the decode kernels, which stream
  * the planes of every active expert once per step: steps of more than 16 pairs
  * with H and I multiples of 512 a block-scaled tcgen05 kernel (codes expanded
- * to e2m1, activations as two e4m3 rows), the rest a bf16 mma.sync kernel;
- * larger T the prefill kernels (TMA + tcgen05 with accumulators in tensor
- * memory).
+ * to packed e2m1, activations as five packed e2m1 digit rows, both scaled by
+ * UE8M0 bytes per 32 elements), the rest a bf16 mma.sync kernel; larger T the
+ * prefill kernels (TMA + tcgen05 with accumulators in tensor memory).
  */
 moe_w2_status moe_w2_forward(const void *x_bf16, const int32_t *topk_ids, const float *topk_weights,
                              const moe_w2_planes *w, int32_t T, int32_t top_k, void *y_bf16,
@@ -144,6 +144,9 @@ moe_w2_status moe_w2_forward(const void *x_bf16, const int32_t *topk_ids, const 
  *                 permutation, 1 = before the gate_up kernel(s), 2 = before the
  *                 down kernel(s), 3 = after the last kernel.  On the prefill
  *                 path the gather is part of phase 0..1 and the combine of 2..3.
+ *                 On the decode path one kernel runs gate_up and down (1..2)
+ *                 and 2..3 is the combine kernel (empty for the mma.sync
+ *                 kernel, which sums the slots itself).
  * cudaEventRecord failures return MOE_W2_ERR_CUDA.
  */
 moe_w2_status moe_w2_forward_traced(const void *x_bf16, const int32_t *topk_ids, const float *topk_weights,

@@ -455,7 +455,7 @@ def requant_bench(args, world, rank, local):
     import torch
     from bit_moe_expert_w2_gb300 import moe_w2
     dev = torch.device("cuda", local)
-    gu, dn = inputs.requant_inputs()
+    gu, dn = inputs.requant_inputs(experts=inputs.REQUANT_CASES[args.config])
     dgu = [torch.from_numpy(a).to(dev) for a in (gu.e2m1, gu.e4m3, gu.scale_2)]
     ddn = [torch.from_numpy(a).to(dev) for a in (dn.e2m1, dn.e4m3, dn.scale_2)]
     cgu = torch.empty((gu.e2m1.shape[0], gu.e2m1.shape[1], gu.e2m1.shape[2] // 2), dtype=torch.uint8, device=dev)
@@ -495,7 +495,7 @@ def requant_bench(args, world, rank, local):
     res = {"ms_per_step": ms / args.steps, "value": world * elems * args.steps / (ms / 1e3),
            "roofline": {"kernel": "requant_kernel", "bound": "hbm", "achieved": round(gbs, 1),
                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
-                        "peak_source": pk["source"], "traffic": ncu_traffic("requant_kernel", "requant_256")},
+                        "peak_source": pk["source"], "traffic": ncu_traffic("requant_kernel", args.config)},
            "clocks": clk.summary(), "gpu_launches": 2 * args.steps, "dtype": "int64 (exact)"}
 
     # end to end: the NVFP4 tensors from pinned host memory, requant, planes back to pinned host memory
@@ -528,7 +528,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=[*inputs.CONFIGS, inputs.REQUANT.name])
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=[*inputs.CONFIGS, *inputs.REQUANT_CASES])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -548,7 +548,7 @@ def main():
 
     world, rank, local = dist_setup(args)
     workload = workload_name(args.config)
-    if args.config == inputs.REQUANT.name:
+    if args.config in inputs.REQUANT_CASES:
         res, gu = requant_bench(args, world, rank, local)
         metric_unit = "elements/s"
     else:
@@ -565,7 +565,7 @@ def main():
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}}
     line.update(res)
     if not args.no_cpu_baseline and world == 1:
-        if args.config == inputs.REQUANT.name:
+        if args.config in inputs.REQUANT_CASES:
             v, n, el = oracle_requant_rate(gu, args.cpu_budget)
             line["cpu_baseline"] = {"value": round(v, 1), "unit": "elements/s", "cores": 1, "kind": "oracle",
                                     "sample": f"{n} whole gate/up tensors in {el:.1f} s"}
@@ -578,8 +578,11 @@ def main():
 
 def workload_name(config: str) -> str:
     """The workload string of a config, the same on both arms."""
-    if config == inputs.REQUANT.name:
-        return f"{inputs.REQUANT.name}: 256 experts NVFP4 gate/up 2x[2048x6144] + down [6144x2048] -> 2-bit planes"
+    if config in inputs.REQUANT_CASES:
+        r = inputs.REQUANT
+        n = inputs.REQUANT_CASES[config] or r.num_experts
+        return (f"{config}: {n} experts NVFP4 gate/up 2x[{r.inter}x{r.hidden}] + down [{r.hidden}x{r.inter}]"
+                " -> 2-bit planes")
     cfg = inputs.CONFIGS[config]
     return (f"{cfg.name}: H={cfg.hidden} I={cfg.inter} E={cfg.num_experts} top-{cfg.top_k} "
             f"T={cfg.tokens} routing={cfg.routing}")
@@ -588,7 +591,7 @@ def workload_name(config: str) -> str:
 def reference_arm(args, cores):
     """The oracle timed on this host's cores on a bounded sample of the workload."""
     budget = 90.0
-    if args.config == inputs.REQUANT.name:
+    if args.config in inputs.REQUANT_CASES:
         gu, _ = inputs.requant_inputs(experts=4)
         v, n, el = oracle_requant_rate(gu, budget / 3)
         unit, sample = "elements/s", f"{n} whole gate/up tensors of {args.config} in {el:.1f} s"

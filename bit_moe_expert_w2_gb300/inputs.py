@@ -85,6 +85,10 @@ CONFIGS = {
     "prefill_t1024_e32": LayerConfig("prefill_t1024_e32", 4096, 2048, 32, 8, 1024, -10, -6, "logits", 6),
 }
 REQUANT = RequantConfig("requant_256", 256, 2048, 6144, 4)
+# Re-quantizer workloads by name: experts drawn from REQUANT (None = all).  requant_16
+# is the first 16 experts of the same draw (each expert has its own child seed): the
+# same per-block kernel work on 1/16 of the data, for multi-pass profiler captures.
+REQUANT_CASES = {"requant_256": None, "requant_16": 16}
 
 
 def rng_for(seed: int) -> np.random.Generator:

@@ -54,3 +54,31 @@ def test_host_validation_without_device():
     assert L.moe_w2_requant(None, None, None, 0, 4, 64, None, None, None, None) == 0
     # permute: top_k out of range
     assert L.moe_w2_permute(None, 4, 0, 8, None, None, None, None, None) == 1
+
+
+def test_alignment_and_workspace_checks_answer_before_any_device_access():
+    """Fake device addresses are never dereferenced: alignment and workspace size
+    are checked on the host first (status 1 = invalid argument, 3 = workspace)."""
+    L = moe_w2.load()
+    A = 0x10000000            # 256-byte aligned stand-in addresses
+    p = moe_w2.Planes(A, A + 0x1000, A + 0x2000, A + 0x3000, 8, 512, 256)
+    need = moe_w2.workspace_size(2, 2, 8, 512, 256)
+    ok = dict(x=A, ids=A, w=A, y=A + 0x100000, ws=A + 0x200000)
+
+    def fwd(planes=p, nbytes=need, **kw):
+        a = {**ok, **kw}
+        return L.moe_w2_forward(a["x"], a["ids"], a["w"], ctypes.byref(planes), 2, 2, a["y"], a["ws"], nbytes,
+                                None, None)
+
+    assert fwd(ws=A + 0x200080) == 1                   # workspace not 256-byte aligned
+    assert fwd(x=A + 8) == 1                           # x not 16-byte aligned
+    assert fwd(y=A + 0x100004) == 1                    # y not 16-byte aligned
+    assert fwd(planes=moe_w2.Planes(A, A + 0x1008, A + 0x2000, A + 0x3000, 8, 512, 256)) == 1   # scales
+    assert fwd(planes=moe_w2.Planes(A, A + 0x1000, A + 0x2000, 0, 8, 512, 256)) == 1           # null plane
+    assert fwd(nbytes=need - 1) == 3                   # workspace one byte short
+    # requant: misaligned e2m1, e4m3 and codes pointers
+    assert L.moe_w2_requant(A + 8, A, A, 1, 4, 64, A, A, None, None) == 1
+    assert L.moe_w2_requant(A, A + 1, A, 1, 4, 64, A, A, None, None) == 1
+    assert L.moe_w2_requant(A, A, A, 1, 4, 64, A + 4, A, None, None) == 1
+    # permute: more pairs than the library takes
+    assert L.moe_w2_permute(A, 1 << 20, 16, 8, A, A, A, None, None) == 2

@@ -183,6 +183,13 @@ size_t moe_w2_forward_workspace_size(int32_t T, int32_t top_k, int32_t E, int32_
     return carve_workspace(nullptr, T, top_k, E, H, I).bytes;
 }
 
+int moe_w2_forward_path(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t I)
+{
+    if (T <= 0 || moe_w2_forward_workspace_size(T, top_k, E, H, I) == 0) return MOE_W2_PATH_NONE;
+    if (T > MOE_W2_DECODE_MAX_TOKENS) return MOE_W2_PATH_PREFILL;
+    return decode_use_mma((int64_t)T * top_k, H, I) ? MOE_W2_PATH_DECODE_MMA : MOE_W2_PATH_DECODE_BLOCK_SCALED;
+}
+
 moe_w2_status moe_w2_permute(const int32_t* topk_ids, int32_t T, int32_t top_k, int32_t E, int32_t* sorted_pairs,
                              int32_t* inv_pairs, int32_t* expert_offsets, uint32_t* dev_status, void* stream)
 {

@@ -22,7 +22,7 @@ DEV_BAD_EXPERT_ID = 1
 DEV_BAD_SCALE = 2
 DEV_BAD_NVFP4 = 4
 DECODE_MAX_TOKENS = 64
-DECODE_MMA_MAX_PAIRS = 16           # decode steps with at most this many pairs run decode_mma_kernel
+PATH_NONE, PATH_DECODE_MMA, PATH_DECODE_BLOCK_SCALED, PATH_PREFILL = 0, 1, 2, 3   # moe_w2_forward_path
 NOALLOC_WORKSPACE_BYTES = 8 << 20   # MOE_W2_NOALLOC_WORKSPACE_BYTES
 
 
@@ -38,11 +38,17 @@ class Planes(ctypes.Structure):
                 ("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32)]
 
 
+def forward_path(T: int, top_k: int, E: int, H: int, I: int) -> int:
+    """moe_w2_forward_path: which kernels moe_w2_forward runs for these sizes (PATH_*)."""
+    return int(load().moe_w2_forward_path(T, top_k, E, H, I))
+
+
 def decode_kernel(T: int, top_k: int, H: int, I: int) -> str:
-    """Name of the kernel that runs the layer of a decode step (T <= DECODE_MAX_TOKENS): the
-    block-scaled kernel needs more than DECODE_MMA_MAX_PAIRS pairs and H, I multiples of 512."""
-    small = T * top_k <= DECODE_MMA_MAX_PAIRS or H % 512 != 0 or I % 512 != 0
-    return "decode_mma_kernel" if small else "decode_layer_kernel"
+    """Name of the kernel that runs the layer of a decode step (T <= DECODE_MAX_TOKENS)."""
+    path = forward_path(T, top_k, 1, H, I)
+    if path not in (PATH_DECODE_MMA, PATH_DECODE_BLOCK_SCALED):
+        raise ValueError(f"T={T} top_k={top_k} H={H} I={I} is not a decode step")
+    return "decode_mma_kernel" if path == PATH_DECODE_MMA else "decode_layer_kernel"
 
 
 def lib_path() -> str:
@@ -66,6 +72,8 @@ def load(build_if_missing: bool = True):
     L.moe_w2_status_string.restype = ctypes.c_char_p
     L.moe_w2_forward_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.moe_w2_forward_workspace_size.restype = sz
+    L.moe_w2_forward_path.argtypes = [i32, i32, i32, i32, i32]
+    L.moe_w2_forward_path.restype = ctypes.c_int
     L.moe_w2_permute.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
     L.moe_w2_permute.restype = ctypes.c_int
     L.moe_w2_forward.argtypes = [vp, vp, vp, ctypes.POINTER(Planes), i32, i32, vp, vp, sz, vp, vp]

@@ -93,6 +93,19 @@ typedef struct {
  * initialisation: every call writes each part before reading it. */
 size_t moe_w2_forward_workspace_size(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t I);
 
+/* Which kernels moe_w2_forward runs for these sizes (host only, no device
+ * access): MOE_W2_PATH_DECODE_MMA for decode steps (T <= 64) of at most 16
+ * pairs, or with H or I not a multiple of 512 (the bf16 mma.sync kernel);
+ * MOE_W2_PATH_DECODE_BLOCK_SCALED for the other decode steps (the tcgen05
+ * block-scaled kernel and its combine); MOE_W2_PATH_PREFILL for T > 64 (the
+ * gather, the two tcgen05 GEMMs and the combine); MOE_W2_PATH_NONE when the
+ * sizes are invalid (moe_w2_forward_workspace_size would return 0) or T = 0. */
+#define MOE_W2_PATH_NONE 0
+#define MOE_W2_PATH_DECODE_MMA 1
+#define MOE_W2_PATH_DECODE_BLOCK_SCALED 2
+#define MOE_W2_PATH_PREFILL 3
+int moe_w2_forward_path(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t I);
+
 /*
  * Routing permutation ("The v0.24.0 port", "Our hooks", deterministic
  * unpermute bullet: valid sorted ids are a permutation of token*top_k+j).

@@ -82,3 +82,20 @@ def test_alignment_and_workspace_checks_answer_before_any_device_access():
     assert L.moe_w2_requant(A, A, A, 1, 4, 64, A + 4, A, None, None) == 1
     # permute: more pairs than the library takes
     assert L.moe_w2_permute(A, 1 << 20, 16, 8, A, A, A, None, None) == 2
+
+
+def test_forward_path_names_the_kernels_a_call_runs():
+    P = moe_w2
+    assert P.forward_path(1, 8, 256, 6144, 2048) == P.PATH_DECODE_MMA             # 8 pairs
+    assert P.forward_path(2, 8, 256, 6144, 2048) == P.PATH_DECODE_MMA             # 16 pairs
+    assert P.forward_path(3, 8, 256, 6144, 2048) == P.PATH_DECODE_BLOCK_SCALED    # 24 pairs
+    assert P.forward_path(32, 8, 256, 6144, 2048) == P.PATH_DECODE_BLOCK_SCALED
+    assert P.forward_path(64, 8, 256, 6144, 2048) == P.PATH_DECODE_BLOCK_SCALED
+    assert P.forward_path(65, 8, 256, 6144, 2048) == P.PATH_PREFILL
+    assert P.forward_path(8192, 8, 256, 4096, 2048) == P.PATH_PREFILL
+    assert P.forward_path(32, 8, 8, 768, 512) == P.PATH_DECODE_MMA                # H not a multiple of 512
+    assert P.forward_path(32, 8, 8, 512, 256) == P.PATH_DECODE_MMA                # I not a multiple of 512
+    assert P.forward_path(0, 8, 256, 6144, 2048) == P.PATH_NONE
+    assert P.forward_path(4, 2, 8, 500, 256) == P.PATH_NONE                       # invalid H
+    assert P.decode_kernel(1, 8, 6144, 2048) == "decode_mma_kernel"
+    assert P.decode_kernel(32, 8, 6144, 2048) == "decode_layer_kernel"

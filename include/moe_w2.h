@@ -99,7 +99,9 @@ size_t moe_w2_forward_workspace_size(int32_t T, int32_t top_k, int32_t E, int32_
  * MOE_W2_PATH_DECODE_BLOCK_SCALED for the other decode steps (the tcgen05
  * block-scaled kernel and its combine); MOE_W2_PATH_PREFILL for T > 64 (the
  * gather, the two tcgen05 GEMMs and the combine); MOE_W2_PATH_NONE when the
- * sizes are invalid (moe_w2_forward_workspace_size would return 0) or T = 0. */
+ * sizes are invalid (moe_w2_forward_workspace_size would return 0) or T = 0.
+ * The pages describe no such entry point: it keeps the dispatch rule in one
+ * place for bindings and benchmarks. */
 #define MOE_W2_PATH_NONE 0
 #define MOE_W2_PATH_DECODE_MMA 1
 #define MOE_W2_PATH_DECODE_BLOCK_SCALED 2

@@ -5,6 +5,9 @@ benchmark's ``cpu_baseline`` / ``--impl reference`` legs may use it; the library
 and its Python binding never import it.
 
 Everything here marshals numpy arrays; the arithmetic lives in ``oracle.c``.
+``oracle.c`` is built twice: single-threaded, and with OpenMP (``parallel=True``
+in the calls below), which runs independent blocks and tokens on all host
+threads and gives bitwise identical results.
 """
 from __future__ import annotations
 
@@ -18,8 +21,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle_moe_w2.so")
+_LIB_OMP_PATH = os.path.join(_HERE, "liboracle_moe_w2_omp.so")
 _lock = threading.Lock()
-_lib = None
+_libs = {}
 
 BAD_EXPERT_ID = 1
 BAD_SCALE = 2
@@ -28,22 +32,32 @@ BAD_NVFP4 = 4
 _CFLAGS = ["-O2", "-std=c11", "-Wall", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (plain C, no architecture flags)."""
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+def build(force: bool = False, parallel: bool | None = None) -> str:
+    """Compile the oracle with gcc (plain C, no architecture flags): the
+    single-threaded library, and the OpenMP one (``parallel`` None builds both
+    and returns the single-threaded path)."""
+    todo = [(False, _LIB_PATH), (True, _LIB_OMP_PATH)] if parallel is None else \
+        [(parallel, _LIB_OMP_PATH if parallel else _LIB_PATH)]
+    for omp, path in todo:
+        if force or not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
+            tmp = path + f".tmp{os.getpid()}"
+            subprocess.run(["gcc", *_CFLAGS, *(["-fopenmp"] if omp else []), "-o", tmp, _SRC, "-lm"], check=True)
+            os.replace(tmp, path)
+    return todo[-1][1] if parallel is not None else _LIB_PATH
 
 
-def lib():
-    global _lib
+def threads(parallel: bool = True) -> int:
+    """Host threads the oracle's loops use (1 for the single-threaded build)."""
+    return int(lib(parallel).oracle_threads())
+
+
+def lib(parallel: bool = False):
     with _lock:
-        if _lib is None:
-            L = ctypes.CDLL(build())
+        if parallel not in _libs:
+            L = ctypes.CDLL(build(parallel=parallel))
             vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
             L.oracle_version.restype = ctypes.c_int
+            L.oracle_threads.restype = ctypes.c_int
             L.oracle_e2m1_value.argtypes = [ctypes.c_uint]
             L.oracle_e2m1_value.restype = ctypes.c_double
             L.oracle_e4m3_value.argtypes = [ctypes.c_uint]
@@ -63,8 +77,8 @@ def lib():
             L.oracle_forward_tokens.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                 vp, i64, vp, vp]
             L.oracle_forward_tokens.restype = u32
-            _lib = L
-    return _lib
+            _libs[parallel] = L
+    return _libs[parallel]
 
 
 def _p(a: np.ndarray):
@@ -92,7 +106,7 @@ def bf16_to_double(h: int) -> float:
     return lib().oracle_bf16_to_double(h)
 
 
-def requant(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray):
+def requant(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray, parallel: bool = False):
     """e2m1 uint8 [n][rows][K/2], e4m3 uint8 [n][rows][K/16], scale_2 float32 [n]."""
     n, rows, half_k = e2m1.shape
     K = half_k * 2
@@ -101,11 +115,11 @@ def requant(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray):
     s2 = np.ascontiguousarray(scale_2, dtype=np.float32)
     codes = np.empty((n, rows, K // 4), np.uint8)
     scales = np.empty((n, rows, K // 32), np.uint8)
-    st = lib().oracle_requant(_p(e2m1), _p(e4m3), _p(s2), n, rows, K, _p(codes), _p(scales))
+    st = lib(parallel).oracle_requant(_p(e2m1), _p(e4m3), _p(s2), n, rows, K, _p(codes), _p(scales))
     return codes, scales, int(st)
 
 
-def requant_blocks(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray, block_ids):
+def requant_blocks(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray, block_ids, parallel: bool = False):
     """Selected blocks (flat index over n*rows*K/32) -> codes [nb][8], scales [nb]."""
     n, rows, half_k = e2m1.shape
     K = half_k * 2
@@ -113,7 +127,7 @@ def requant_blocks(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray, bloc
     codes = np.empty((len(ids), 8), np.uint8)
     scales = np.empty(len(ids), np.uint8)
     s2 = np.ascontiguousarray(scale_2, dtype=np.float32)
-    st = lib().oracle_requant_blocks(_p(np.ascontiguousarray(e2m1)), _p(np.ascontiguousarray(e4m3)),
+    st = lib(parallel).oracle_requant_blocks(_p(np.ascontiguousarray(e2m1)), _p(np.ascontiguousarray(e4m3)),
                                      _p(s2), rows, K, _p(ids), len(ids), _p(codes), _p(scales))
     return codes, scales, int(st)
 
@@ -130,7 +144,7 @@ def permute(ids: np.ndarray, E: int):
 
 
 def forward_tokens(x: np.ndarray, ids: np.ndarray, weights: np.ndarray, planes: dict,
-                   tokens=None, want_h: bool = False):
+                   tokens=None, want_h: bool = False, parallel: bool = False):
     """y (bf16 bits) for the listed tokens; x uint16 [T][H], ids int32 [T][k], weights f32 [T][k]."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
     ids = np.ascontiguousarray(ids, dtype=np.int32)
@@ -142,7 +156,7 @@ def forward_tokens(x: np.ndarray, ids: np.ndarray, weights: np.ndarray, planes: 
     tok = np.arange(T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
     y = np.empty((len(tok), H), np.uint16)
     h = np.empty((len(tok), k, I), np.uint16) if want_h else None
-    st = lib().oracle_forward_tokens(
+    st = lib(parallel).oracle_forward_tokens(
         _p(x), _p(ids), _p(weights),
         _p(planes["w13_codes"]), _p(planes["w13_scales"]), _p(planes["w2_codes"]), _p(planes["w2_scales"]),
         E, H, I, k, _p(tok), len(tok), _p(y), _p(h) if want_h else None)

@@ -3,9 +3,14 @@
  * re-quantizer.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the
  * benchmark's CPU-baseline leg load this library; the product path never does.
  *
- * Plain, single-threaded loops in f64 (and exact 128-bit integer sums where an
- * L2 comparison has to be exact).  No blocking, no fusion, no reordering beyond
- * what each definition states.  Shares no source with the CUDA library.
+ * Plain loops in f64 (and exact 128-bit integer sums where an L2 comparison has
+ * to be exact).  No blocking, no fusion, no reordering beyond what each
+ * definition states.  Shares no source with the CUDA library.
+ *
+ * The same source builds twice: single-threaded, and with OpenMP, where the
+ * loops over independent blocks (requant) and tokens (forward) run on several
+ * threads.  Every block and every token is computed by one thread with the
+ * same sequence of operations, so both builds give bitwise identical results.
  *
  * Sources (vLLM-Moet pages):
  *   [wiki]  "vLLM-Moet wiki", section "2-bit expert planes": codebook {-4,-1,1,4},
@@ -41,6 +46,17 @@
 #include <stdlib.h>
 #include <string.h>
 
+#ifdef _OPENMP
+#include <omp.h>
+/* independent iterations on all threads, status bits OR-reduced: blocks of 32
+ * elements are handed out 256 at a time, tokens one at a time */
+#define ORACLE_PARALLEL_FOR_BLOCKS _Pragma("omp parallel for schedule(dynamic, 256) reduction(|:st)")
+#define ORACLE_PARALLEL_FOR_TOKENS _Pragma("omp parallel for schedule(dynamic, 1) reduction(|:st)")
+#else
+#define ORACLE_PARALLEL_FOR_BLOCKS
+#define ORACLE_PARALLEL_FOR_TOKENS
+#endif
+
 #define ORACLE_BAD_EXPERT_ID 1u
 #define ORACLE_BAD_SCALE 2u
 #define ORACLE_BAD_NVFP4 4u
@@ -48,6 +64,16 @@
 typedef unsigned __int128 u128;
 
 int oracle_version(void) { return 1; }
+
+/* Threads the parallel loops use (1 in the single-threaded build). */
+int oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 static void oracle_fail(const char *what)
 {
@@ -220,11 +246,9 @@ uint32_t oracle_requant(const uint8_t *e2m1, const uint8_t *e4m3, const float *s
     if (K % 32 != 0) return 0x80000000u;
     uint32_t st = 0;
     int64_t blocks_per_tensor = rows * (K / 32);
-    for (int64_t t = 0; t < n; ++t)
-        for (int64_t b = 0; b < blocks_per_tensor; ++b) {
-            int64_t g = t * blocks_per_tensor + b;
-            st |= requant_block(e2m1 + g * 16, e4m3 + g * 2, scale_2[t], codes + g * 8, ue8m0 + g);
-        }
+    ORACLE_PARALLEL_FOR_BLOCKS
+    for (int64_t g = 0; g < n * blocks_per_tensor; ++g)
+        st |= requant_block(e2m1 + g * 16, e4m3 + g * 2, scale_2[g / blocks_per_tensor], codes + g * 8, ue8m0 + g);
     return st;
 }
 
@@ -236,6 +260,7 @@ uint32_t oracle_requant_blocks(const uint8_t *e2m1, const uint8_t *e4m3, const f
     if (K % 32 != 0) return 0x80000000u;
     uint32_t st = 0;
     int64_t blocks_per_tensor = rows * (K / 32);
+    ORACLE_PARALLEL_FOR_BLOCKS
     for (int64_t i = 0; i < nb; ++i) {
         int64_t g = block_ids[i];
         st |= requant_block(e2m1 + g * 16, e4m3 + g * 2, scale_2[g / blocks_per_tensor],
@@ -297,6 +322,52 @@ static double dot(const double *a, const double *b, int64_t n)
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* y of token t: y_out bf16 [H]; h_out (nullable) bf16 [k][I]. */
+static uint32_t forward_token(const uint16_t *x, const int32_t *ids, const float *weights,
+                              const uint8_t *w13_codes, const uint8_t *w13_scales,
+                              const uint8_t *w2_codes, const uint8_t *w2_scales,
+                              int32_t E, int32_t H, int32_t I, int32_t k, int64_t t,
+                              uint16_t *y_out, uint16_t *h_out)
+{
+    uint32_t st = 0;
+    double *xt = malloc(sizeof(double) * H), *row = malloc(sizeof(double) * (H > I ? H : I));
+    double *h = malloc(sizeof(double) * I), *acc = malloc(sizeof(double) * H);
+    if (!xt || !row || !h || !acc) oracle_fail("malloc");
+    for (int32_t i = 0; i < H; ++i) xt[i] = oracle_bf16_to_double(x[t * H + i]);
+    for (int32_t m = 0; m < H; ++m) acc[m] = 0.0;
+    for (int32_t j = 0; j < k; ++j) {
+        int32_t e = ids[t * k + j];
+        if (h_out)
+            for (int32_t n = 0; n < I; ++n) h_out[(int64_t)j * I + n] = 0;
+        if (e < 0 || e >= E) {
+            st |= ORACLE_BAD_EXPERT_ID;
+            continue;
+        }
+        double w = (double)weights[t * k + j];
+        for (int32_t n = 0; n < I; ++n) {
+            int64_t rg = (int64_t)e * 2 * I + n, ru = (int64_t)e * 2 * I + I + n;
+            st |= dequant_row(w13_codes + rg * (H / 4), w13_scales + rg * (H / 32), H, row);
+            double g = dot(row, xt, H);
+            st |= dequant_row(w13_codes + ru * (H / 4), w13_scales + ru * (H / 32), H, row);
+            double u = dot(row, xt, H);
+            uint16_t hb = oracle_bf16_from_double(silu(g) * u);
+            h[n] = oracle_bf16_to_double(hb);
+            if (h_out) h_out[(int64_t)j * I + n] = hb;
+        }
+        for (int32_t m = 0; m < H; ++m) {
+            int64_t r = (int64_t)e * H + m;
+            st |= dequant_row(w2_codes + r * (I / 4), w2_scales + r * (I / 32), I, row);
+            acc[m] += w * dot(row, h, I);
+        }
+    }
+    for (int32_t m = 0; m < H; ++m) y_out[m] = oracle_bf16_from_double(acc[m]);
+    free(xt);
+    free(row);
+    free(h);
+    free(acc);
+    return st;
+}
+
 /* y for the listed tokens.  x bf16 [T][H], ids/weights [T][k]; planes as in the
  * C ABI; y_out bf16 [ntok][H]; h_out (nullable) bf16 [ntok][k][I]. */
 uint32_t oracle_forward_tokens(const uint16_t *x, const int32_t *ids, const float *weights,
@@ -307,43 +378,9 @@ uint32_t oracle_forward_tokens(const uint16_t *x, const int32_t *ids, const floa
 {
     if (H % 32 || I % 32) return 0x80000000u;
     uint32_t st = 0;
-    double *xt = malloc(sizeof(double) * H), *row = malloc(sizeof(double) * (H > I ? H : I));
-    double *h = malloc(sizeof(double) * I), *acc = malloc(sizeof(double) * H);
-    if (!xt || !row || !h || !acc) oracle_fail("malloc");
-    for (int64_t it = 0; it < ntok; ++it) {
-        int64_t t = tokens[it];
-        for (int32_t i = 0; i < H; ++i) xt[i] = oracle_bf16_to_double(x[t * H + i]);
-        for (int32_t m = 0; m < H; ++m) acc[m] = 0.0;
-        for (int32_t j = 0; j < k; ++j) {
-            int32_t e = ids[t * k + j];
-            if (h_out)
-                for (int32_t n = 0; n < I; ++n) h_out[(it * k + j) * (int64_t)I + n] = 0;
-            if (e < 0 || e >= E) {
-                st |= ORACLE_BAD_EXPERT_ID;
-                continue;
-            }
-            double w = (double)weights[t * k + j];
-            for (int32_t n = 0; n < I; ++n) {
-                int64_t rg = (int64_t)e * 2 * I + n, ru = (int64_t)e * 2 * I + I + n;
-                st |= dequant_row(w13_codes + rg * (H / 4), w13_scales + rg * (H / 32), H, row);
-                double g = dot(row, xt, H);
-                st |= dequant_row(w13_codes + ru * (H / 4), w13_scales + ru * (H / 32), H, row);
-                double u = dot(row, xt, H);
-                uint16_t hb = oracle_bf16_from_double(silu(g) * u);
-                h[n] = oracle_bf16_to_double(hb);
-                if (h_out) h_out[(it * k + j) * (int64_t)I + n] = hb;
-            }
-            for (int32_t m = 0; m < H; ++m) {
-                int64_t r = (int64_t)e * H + m;
-                st |= dequant_row(w2_codes + r * (I / 4), w2_scales + r * (I / 32), I, row);
-                acc[m] += w * dot(row, h, I);
-            }
-        }
-        for (int32_t m = 0; m < H; ++m) y_out[it * H + m] = oracle_bf16_from_double(acc[m]);
-    }
-    free(xt);
-    free(row);
-    free(h);
-    free(acc);
+    ORACLE_PARALLEL_FOR_TOKENS
+    for (int64_t it = 0; it < ntok; ++it)
+        st |= forward_token(x, ids, weights, w13_codes, w13_scales, w2_codes, w2_scales, E, H, I, k, tokens[it],
+                            y_out + it * H, h_out ? h_out + it * k * (int64_t)I : NULL);
     return st;
 }

@@ -152,3 +152,39 @@ def test_bad_scale_byte_zeroes_its_block():
     planes["w2_scales"][1, :, :] = 0                  # every block of expert 1's down rows
     y, st = oracle.forward_tokens(lay.x, np.array([[1]], np.int32), np.array([[1.0]], np.float32), planes)
     assert np.all(oracle.bf16_bits_to_f64(y) == 0.0) and st == oracle.BAD_SCALE
+
+
+@pytest.mark.parametrize("s", [0, 1, 126, 252, 253, 254, 255])
+def test_ue8m0_validity_range_of_down_blocks(s):
+    # Bytes 1..252 scale by 2^(s-127); 0 and 253..255 are outside the accepted
+    # range (4 * 2^(s-127) must stay a normal bf16/fp32) and zero their block with
+    # status bit 2.  Near the top g = u = 2^-8 gives a small h, so 2^125 times it
+    # stays finite; near the bottom g = u = 1 keeps 2^-126 times it normal.
+    H = I = 32
+    planes = _constant_planes(1, H, I, 0, 127, 0, 127, 0, s)
+    g = u = 1.0 if s < 128 else 2.0 ** -8
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = _bf16_bits(g)[()]
+    y, st = oracle.forward_tokens(x, np.array([[0]], np.int32), np.array([[1.0]], np.float32), planes)
+    h = _bf16_round(g / (1.0 + np.exp(-g)) * u)
+    valid = 1 <= s <= 252
+    want = _bf16_round(32.0 * h * 2.0 ** (s - 127)) if valid else 0.0
+    got = oracle.bf16_bits_to_f64(y)
+    assert np.all(np.isfinite(got)) and np.all(got == want)
+    assert st == (0 if valid else oracle.BAD_SCALE)
+
+
+@pytest.mark.parametrize("s", [252, 253])
+def test_ue8m0_validity_range_of_gate_up_blocks(s):
+    # x = 2^-128 (a bf16 subnormal); at s = 252 g = u = 2^125 * 2^-128 = 1/8, at
+    # s = 253 the gate and up blocks count as zero, so h = 0 and y = 0.
+    H = I = 32
+    planes = _constant_planes(1, H, I, 0, s, 0, s, 0, 127)
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = 0x0020                                  # 32 * 2^-133 = 2^-128
+    assert oracle.bf16_bits_to_f64(x)[0, 0] == 2.0 ** -128
+    y, st = oracle.forward_tokens(x, np.array([[0]], np.int32), np.array([[1.0]], np.float32), planes)
+    g = u = 0.125
+    want = _bf16_round(32.0 * _bf16_round(g / (1.0 + np.exp(-g)) * u)) if s == 252 else 0.0
+    assert np.all(oracle.bf16_bits_to_f64(y) == want)
+    assert st == (0 if s == 252 else oracle.BAD_SCALE)

@@ -5,19 +5,26 @@
 
 Default workload: decode_t1 (H=6144, I=2048, E=256, top-8, T=1, Zipf(1.1)
 routing), the single-token decode step.  One step = one moe_w2_forward of one
-batch: permutation, gate_up with SiLU*up, down with the weighted combine.
+batch: permutation, gate_up with SiLU*up, down with the weighted combine.  The
+default single-GPU run also measures the other full-size workloads, decode_t32,
+prefill_t8192 and requant_256, and adds one object per workload under
+"configs" in the same JSON line (value, ms_per_step, roofline, e2e, cpu_baseline).
 
 Timing: inputs are resident in HBM; every step replays a captured CUDA graph of
 the forward, timed by CUDA events recorded on the launching stream around the
 replay (step time, `value`).  A second timed pass over the same steps replays
 graphs of moe_w2_forward_traced, whose phase events give each kernel's time (the
 roofline line); its step time is reported as ms_per_step_traced.  L2 is flushed
-(a 512 MiB write) before every step, outside the timed events.  Routings rotate over a pool, so consecutive steps
-touch different experts.  "e2e" times the same call with the step's inputs
+(a 512 MiB write) before every step, outside the timed events.  Routings rotate
+over a pool, so consecutive steps touch different experts.  SM clocks and
+throttle reasons are sampled with nvidia-smi (by the timed GPU's PCI bus id)
+from before the warm-up through the timed steps, with extra untimed replays
+before the timed ones so that at least ten samples fall under load.  "e2e" times the same call with the step's inputs
 copied from pinned host memory and y copied back inside the timed events.
 
---impl reference runs the CPU oracle (plain single-threaded C) on a bounded
-sample of the same workload on this host; it never touches the GPU.
+--impl reference runs the CPU oracle (plain C, single-threaded) on a bounded
+sample of the same workload on this host; it never touches the GPU.  Each
+cpu_baseline also reports the OpenMP build of the same oracle on all host cores.
 Multi-GPU (torchrun): independent replicas, one per GPU (the layer has no
 cross-GPU step on one box); value = all ranks' tokens / slowest rank's time.
 """
@@ -44,8 +51,19 @@ from bit_moe_expert_w2_gb300 import inputs  # noqa: E402
 
 METRIC = "w2 MoE layer tokens/s; plane HBM GB/s (decode), TFLOP/s (prefill) vs peak"
 DEFAULT_CONFIG = "decode_t1"
-TRACE_EAGER = os.environ.get("MOE_W2_BENCH_TRACE", "eager") == "eager"
+EXTRA_CONFIGS = ("decode_t32", "prefill_t8192", "requant_256")
+DEFAULT_STEPS = {"decode_t1": 4000, "decode_t32": 1000, "prefill_t8192": 100, "requant_256": 10,
+                 "decode_t1_e32": 4000, "prefill_t1024_e32": 400}
+EXTRA_STEPS = {"decode_t32": 500, "prefill_t8192": 50, "requant_256": 5}
 POOL = 16
+# every file each kernel's translation unit compiles: a capture is stale once any changed
+KERNEL_SOURCES = {
+    "decode_layer_kernel": ["bit_moe_expert_w2_gb300/csrc/decode.cu"],
+    "decode_mma_kernel": ["bit_moe_expert_w2_gb300/csrc/decode_mma.cu"],
+    "prefill_gate_up_kernel": ["bit_moe_expert_w2_gb300/csrc/prefill.cu"],
+    "requant_kernel": ["bit_moe_expert_w2_gb300/csrc/requant.cu"],
+}
+COMMON_SOURCES = ["bit_moe_expert_w2_gb300/csrc/common.cuh", "bit_moe_expert_w2_gb300/csrc/tc.cuh", "include/moe_w2.h"]
 
 
 def peaks():
@@ -58,20 +76,31 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def file_sha(rel: str) -> str:
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def sources_sha(rels) -> str:
+    """One hash over the listed files (path and contents, in order)."""
+    h = hashlib.sha256()
+    for rel in rels:
+        h.update(rel.encode() + b"\0")
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_sources(kernel: str):
+    return KERNEL_SOURCES[kernel] + COMMON_SOURCES
 
 
 def ncu_traffic(kernel: str, workload: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None if
-    the summary is missing or the kernel's source changed since the capture."""
+    the summary is missing or any file the kernel compiles changed since the capture."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             d = json.load(f)[kernel]
     except (OSError, KeyError, ValueError):
         return None
-    if d.get("workload") != workload or d.get("source_sha") != file_sha(d["source"]):
+    if d.get("workload") != workload or d.get("sources") != kernel_sources(kernel):
+        return None
+    if d.get("sources_sha") != sources_sha(d["sources"]):
         return None
     return d.get("traffic_bytes_per_launch")
 
@@ -79,20 +108,35 @@ def ncu_traffic(kernel: str, workload: str):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples of SM clock and throttle reasons of the timed GPU.
+
+    Started before the warm-up; each sample carries the host time it arrived, so
+    the summary can take the samples of a window (the timed steps, widened to the
+    warm replays just before them when the timed steps alone are too short)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 100
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, device_id: str):
+        self.device_id = device_id
         self.proc = None
-        self.lines = []
+        self.samples = []   # (host time, line)
 
-    def __enter__(self):
+    @staticmethod
+    def device_id_of(torch_device) -> str:
+        """nvidia-smi --id for a torch CUDA device: its PCI bus id (robust to CUDA_VISIBLE_DEVICES)."""
+        import torch
+        p = torch.cuda.get_device_properties(torch_device)
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+            return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+        except AttributeError:
+            return str(torch.device(torch_device).index or 0)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.device_id}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -102,9 +146,17 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.time(), line.strip()))
 
-    def __exit__(self, *a):
+    def wait_first(self, timeout_s: float = 5.0):
+        t0 = time.time()
+        while self.proc is not None and not self.samples and time.time() - t0 < timeout_s:
+            time.sleep(0.01)
+
+    def count_since(self, t0: float) -> int:
+        return sum(1 for t, _ in self.samples if t >= t0)
+
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -112,10 +164,17 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0: float, t1: float, warm0: float | None = None, want: int = 10):
+        """Median SM clock and the throttle reasons seen in [t0, t1]; with fewer than
+        `want` samples there, over [warm0, t1] (the warm replays right before)."""
+        def pick(a):
+            return [line for t, line in self.samples if a <= t <= t1 + self.PERIOD_MS / 1e3]
+        lines, window = pick(t0), "timed steps"
+        if len(lines) < want and warm0 is not None:
+            lines, window = pick(warm0), "warm replays and timed steps"
         sms, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -130,7 +189,7 @@ class ClockSampler:
         if not sms:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sms)}
+                "samples": len(sms), "window": window, "gpu": self.device_id}
 
 
 # ------------------------------------------------------------------ distributed
@@ -183,6 +242,39 @@ def oracle_layer_rate(lay: inputs.LayerInputs, budget_s: float, max_tokens: int 
             return done / el, done, el
 
 
+def oracle_layer_rate_all_cores(lay: inputs.LayerInputs, budget_s: float):
+    """Tokens/s of the OpenMP oracle on all host cores: rounds of one whole token
+    per thread (the workload's tokens in turn, repeated when it has fewer tokens
+    than threads), until the budget is spent."""
+    import oracle
+    threads = oracle.threads(parallel=True)
+    T = lay.x.shape[0]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        tok = (np.arange(done, done + threads) % T).astype(np.int64)
+        oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes, tokens=tok, parallel=True)
+        done += threads
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done / el, done, el, threads
+
+
+def oracle_requant_rate_all_cores(gu: inputs.Nvfp4Tensors, budget_s: float):
+    """Elements/s of the OpenMP oracle requant on all host cores, whole tensors in turn."""
+    import oracle
+    threads = oracle.threads(parallel=True)
+    done_el, t0, i = 0, time.perf_counter(), 0
+    n = gu.e2m1.shape[0]
+    while True:
+        sl = slice(i % n, i % n + 2)
+        oracle.requant(gu.e2m1[sl], gu.e4m3[sl], gu.scale_2[sl], parallel=True)
+        done_el += gu.e2m1[sl].size * 2
+        i += 2
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done_el / el, i, el, threads
+
+
 def oracle_requant_rate(gu: inputs.Nvfp4Tensors, budget_s: float):
     """Elements/s of the oracle requant on whole tensors (single thread)."""
     import oracle
@@ -200,7 +292,7 @@ def oracle_requant_rate(gu: inputs.Nvfp4Tensors, budget_s: float):
 
 # ------------------------------------------------------------------ layer benchmark
 
-def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
+def layer_bench(cfg: inputs.LayerConfig, steps, warmup, world, rank, local):
     import torch
     from bit_moe_expert_w2_gb300 import moe_w2
 
@@ -312,7 +404,7 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
             done += m
         return steps_total, per_step
 
-    def run_traced(nsteps, eager=TRACE_EAGER):
+    def run_traced(nsteps, eager=True):
         """Traced steps: per-phase times from the events between the kernels.  Eager
         launches (queued behind the L2 flush, so the GPU never waits on the host)
         by default; graph replays with event nodes otherwise."""
@@ -336,20 +428,28 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
             done += m
         return steps_total, tot
 
-    run_steps(max(args.warmup, 3), False)
-    run_traced(max(args.warmup, 3))
+    clk = ClockSampler(ClockSampler.device_id_of(dev)).start()
+    clk.wait_first()
+    run_steps(max(warmup, 3), False)
+    run_traced(max(warmup, 3))
+    # untimed replays until the clock sampler has seen the GPU under load for a while
+    warm0 = time.time()
+    while clk.count_since(warm0) < 10 and time.time() - warm0 < 5.0:
+        run_steps(pool, False)
     barrier(world)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        wall0 = time.perf_counter()
-        steps_ms, per_step = run_steps(args.steps, True)
-        torch.cuda.synchronize(dev)
-        wall = time.perf_counter() - wall0
-        traced_ms, phase_ms = run_traced(args.steps)
-        torch.cuda.synchronize(dev)
+    t_timed0 = time.time()
+    wall0 = time.perf_counter()
+    steps_ms, per_step = run_steps(steps, True)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    t_timed1 = time.time()
+    traced_ms, phase_ms = run_traced(steps)
+    torch.cuda.synchronize(dev)
+    clk.stop()
     barrier(world)
     steps_ms_max = max_over_ranks(steps_ms, world)
-    K = args.steps
+    K = steps
     value = world * T * K / (steps_ms_max / 1e3)
     st_val = int(status.item())
     if st_val != 0:
@@ -386,7 +486,7 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
         res["phase_ms_per_step"] = {"permute_gather": round(phase_ms[0] / K, 5), "gate_up": round(phase_ms[1] / K, 5),
                                     "down_combine": round(phase_ms[2] / K, 5)}
     res["distinct_experts_per_step"] = round(float(np.mean([distinct[i] for i, _ in per_step])), 2)
-    res["clocks"] = clk.summary()
+    res["clocks"] = clk.summary(t_timed0, t_timed1, warm0)
     res["wall_s"] = round(wall, 3)
     # decode: permute (+ x as T16 bf16 or e2m1 digit rows), the layer kernel (gate_up, down), and the
     # combine kernel after the block-scaled one;
@@ -433,8 +533,8 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
     stream.synchronize()
     e2e_ms, done = 0.0, 0
     barrier(world)
-    while done < args.steps:
-        m = min(pool, args.steps - done)
+    while done < steps:
+        m = min(pool, steps - done)
         with torch.cuda.stream(stream):
             for j in range(m):
                 flush.zero_()
@@ -444,18 +544,18 @@ def layer_bench(args, cfg: inputs.LayerConfig, world, rank, local):
         done += m
     e2e_ms = max_over_ranks(e2e_ms, world)
     bytes_in = batches[0][0].nbytes + batches[0][1].nbytes + batches[0][2].nbytes
-    res["e2e"] = {"value": round(world * T * args.steps / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+    res["e2e"] = {"value": round(world * T * steps / (e2e_ms / 1e3), 2), "unit": "tokens/s",
                   "h2d_bytes_per_step": int(bytes_in), "d2h_bytes_per_step": int(T * H * 2)}
-    res["gpu_launches"] = res["kernels_per_step"] * args.steps
+    res["gpu_launches"] = res["kernels_per_step"] * steps
     res["value"] = value
     return res, lay
 
 
-def requant_bench(args, world, rank, local):
+def requant_bench(name, steps, warmup, world, rank, local):
     import torch
     from bit_moe_expert_w2_gb300 import moe_w2
     dev = torch.device("cuda", local)
-    gu, dn = inputs.requant_inputs(experts=inputs.REQUANT_CASES[args.config])
+    gu, dn = inputs.requant_inputs(experts=inputs.REQUANT_CASES[name])
     dgu = [torch.from_numpy(a).to(dev) for a in (gu.e2m1, gu.e4m3, gu.scale_2)]
     ddn = [torch.from_numpy(a).to(dev) for a in (dn.e2m1, dn.e4m3, dn.scale_2)]
     cgu = torch.empty((gu.e2m1.shape[0], gu.e2m1.shape[1], gu.e2m1.shape[2] // 2), dtype=torch.uint8, device=dev)
@@ -465,7 +565,7 @@ def requant_bench(args, world, rank, local):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
 
     def step(e0=None, e1=None):
         if e0 is not None:
@@ -475,33 +575,43 @@ def requant_bench(args, world, rank, local):
         if e1 is not None:
             e1.record(stream)
 
+    clk = ClockSampler(ClockSampler.device_id_of(dev)).start()
+    clk.wait_first()
     with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
+        for _ in range(max(warmup, 3)):
             step()
     stream.synchronize()
-    barrier(world)
-    with ClockSampler(local) as clk:
+    warm0 = time.time()
+    while clk.count_since(warm0) < 10 and time.time() - warm0 < 5.0:
         with torch.cuda.stream(stream):
-            for e0, e1 in evs:
-                flush.zero_()
-                step(e0, e1)
+            step()
         stream.synchronize()
+    barrier(world)
+    t_timed0 = time.time()
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            flush.zero_()
+            step(e0, e1)
+    stream.synchronize()
+    t_timed1 = time.time()
+    clk.stop()
     ms = sum(a.elapsed_time(b) for a, b in evs)
     ms = max_over_ranks(ms, world)
     elems = gu.e2m1.size * 2 + dn.e2m1.size * 2
     moved = sum(a.nbytes for a in (gu.e2m1, gu.e4m3, dn.e2m1, dn.e4m3)) + elems // 4 + elems // 32
     pk = peaks()
-    gbs = moved * args.steps / (ms / 1e3) / 1e9
-    res = {"ms_per_step": ms / args.steps, "value": world * elems * args.steps / (ms / 1e3),
+    gbs = moved * steps / (ms / 1e3) / 1e9
+    res = {"ms_per_step": ms / steps, "value": world * elems * steps / (ms / 1e3),
            "roofline": {"kernel": "requant_kernel", "bound": "hbm", "achieved": round(gbs, 1),
                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
-                        "peak_source": pk["source"], "traffic": ncu_traffic("requant_kernel", args.config)},
-           "clocks": clk.summary(), "gpu_launches": 2 * args.steps, "dtype": "int64 (exact)"}
+                        "peak_source": pk["source"], "traffic": ncu_traffic("requant_kernel", name),
+                        "algorithmic_bytes_per_step": int(moved)},
+           "clocks": clk.summary(t_timed0, t_timed1, warm0), "gpu_launches": 2 * steps, "dtype": "int64 (exact)"}
 
     # end to end: the NVFP4 tensors from pinned host memory, requant, planes back to pinned host memory
     hin = [torch.from_numpy(a).pin_memory() for a in (gu.e2m1, gu.e4m3, gu.scale_2, dn.e2m1, dn.e4m3, dn.scale_2)]
     hout = [torch.empty(t.shape, dtype=torch.uint8).pin_memory() for t in (cgu, sgu, cdn, sdn)]
-    e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     with torch.cuda.stream(stream):
         for e0, e1 in e_evs:
             flush.zero_()
@@ -515,7 +625,7 @@ def requant_bench(args, world, rank, local):
             e1.record(stream)
     stream.synchronize()
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e_evs), world)
-    res["e2e"] = {"value": round(world * elems * args.steps / (e2e_ms / 1e3), 2), "unit": "elements/s",
+    res["e2e"] = {"value": round(world * elems * steps / (e2e_ms / 1e3), 2), "unit": "elements/s",
                   "h2d_bytes_per_step": int(sum(h.nbytes for h in hin)),
                   "d2h_bytes_per_step": int(sum(h.nbytes for h in hout))}
     if int(status.item()) != 0:
@@ -523,19 +633,49 @@ def requant_bench(args, world, rank, local):
     return res, gu
 
 
+def cpu_baseline(name, data, budget_s):
+    """The oracle on this host: one core (the reported value) and all cores."""
+    if name in inputs.REQUANT_CASES:
+        v, n, el = oracle_requant_rate(data, budget_s)
+        va, na, ela, thr = oracle_requant_rate_all_cores(data, budget_s / 2)
+        return {"value": round(v, 1), "unit": "elements/s", "cores": 1, "kind": "oracle",
+                "sample": f"{n} whole gate/up tensors of {name} in {el:.1f} s",
+                "all_cores": {"value": round(va, 1), "cores": thr,
+                              "sample": f"{na} whole gate/up tensors in {ela:.1f} s (OpenMP build)"}}
+    v, n, el = oracle_layer_rate(data, budget_s)
+    va, na, ela, thr = oracle_layer_rate_all_cores(data, budget_s / 2)
+    return {"value": round(v, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} whole tokens of {name} in {el:.1f} s",
+            "all_cores": {"value": round(va, 4), "cores": thr,
+                          "sample": f"{na} whole tokens in {ela:.1f} s (OpenMP build, one token per thread)"}}
+
+
+def run_config(name, steps, warmup, world, rank, local):
+    """(result dict, oracle input) of one workload."""
+    if name in inputs.REQUANT_CASES:
+        res, data = requant_bench(name, steps, warmup, world, rank, local)
+        res["unit"] = "elements/s"
+    else:
+        res, data = layer_bench(inputs.CONFIGS[name], steps, warmup, world, rank, local)
+        res["unit"] = "tokens/s"
+    return res, data
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=[*inputs.CONFIGS, *inputs.REQUANT_CASES])
+    ap.add_argument("--config", default=None, choices=[*inputs.CONFIGS, *inputs.REQUANT_CASES],
+                    help=f"one workload only (default: {DEFAULT_CONFIG}, plus {', '.join(EXTRA_CONFIGS)} on one GPU)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of single-core oracle work per workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-configs", action="store_true", help="only the headline workload")
     args = ap.parse_args()
+    headline = args.config or DEFAULT_CONFIG
     if args.steps is None:
-        args.steps = {"decode_t1": 4000, "decode_t32": 1000, "prefill_t8192": 100,
-                      "decode_t1_e32": 4000, "prefill_t1024_e32": 400}.get(args.config, 10)
+        args.steps = DEFAULT_STEPS.get(headline, 10)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -544,35 +684,35 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
+        args.config = headline
         return reference_arm(args, cores)
 
     world, rank, local = dist_setup(args)
-    workload = workload_name(args.config)
-    if args.config in inputs.REQUANT_CASES:
-        res, gu = requant_bench(args, world, rank, local)
-        metric_unit = "elements/s"
-    else:
-        cfg = inputs.CONFIGS[args.config]
-        res, lay = layer_bench(args, cfg, world, rank, local)
-        metric_unit = "tokens/s"
+    res, data = run_config(headline, args.steps, args.warmup, world, rank, local)
+    extras = {}
+    if args.config is None and world == 1 and not args.no_extra_configs:
+        for name in EXTRA_CONFIGS:
+            extras[name] = run_config(name, EXTRA_STEPS[name], args.warmup, world, rank, local)
     if rank != 0:
         return
-    line = {"metric": METRIC, "value": round(res.pop("value"), 3), "unit": metric_unit, "n_gpus": world,
+    line = {"metric": METRIC, "value": round(res.pop("value"), 3), "unit": res.pop("unit"), "n_gpus": world,
             "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(res.pop("ms_per_step"), 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": res.pop("dtype", "bf16"),
             "data": "synthetic (seeded; shapes of the pages' models)",
-            "config": {"workload": workload, "l2": "flushed before every step (512 MiB write, untimed)",
+            "config": {"workload": workload_name(headline), "l2": "flushed before every step (512 MiB write, untimed)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}}
     line.update(res)
     if not args.no_cpu_baseline and world == 1:
-        if args.config in inputs.REQUANT_CASES:
-            v, n, el = oracle_requant_rate(gu, args.cpu_budget)
-            line["cpu_baseline"] = {"value": round(v, 1), "unit": "elements/s", "cores": 1, "kind": "oracle",
-                                    "sample": f"{n} whole gate/up tensors in {el:.1f} s"}
-        else:
-            v, n, el = oracle_layer_rate(lay, args.cpu_budget)
-            line["cpu_baseline"] = {"value": round(v, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                    "sample": f"{n} whole tokens of {args.config} in {el:.1f} s"}
+        line["cpu_baseline"] = cpu_baseline(headline, data, args.cpu_budget)
+    if extras:
+        line["configs"] = {}
+        for name, (r, d) in extras.items():
+            obj = {"workload": workload_name(name), "value": round(r.pop("value"), 3), "unit": r.pop("unit"),
+                   "steps": EXTRA_STEPS[name], "ms_per_step": round(r.pop("ms_per_step"), 6)}
+            obj.update(r)
+            if not args.no_cpu_baseline:
+                obj["cpu_baseline"] = cpu_baseline(name, d, args.cpu_budget)
+            line["configs"][name] = obj
     print(json.dumps(line), flush=True)
 
 

@@ -29,10 +29,8 @@ def nvcc() -> str:
 
 
 def _flags():
-    # MOE_W2_NVCC_EXTRA: extra -D flags for tuning sweeps (pipeline shapes)
-    extra = os.environ.get("MOE_W2_NVCC_EXTRA", "").split()
     return [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
-            "-I", os.path.join(ROOT, "include"), "-I", CSRC, *extra]
+            "-I", os.path.join(ROOT, "include"), "-I", CSRC]
 
 
 def _needs_rebuild() -> bool:

@@ -11,12 +11,10 @@ namespace moe_w2 {
 namespace {
 
 constexpr int32_t kPrefillTileRows = 256;   // pairs per prefill tile (tcgen05 N <= 256)
-constexpr int32_t kDecodeTileRows = 3;      // pairs per decode tile (MMA N = 16: kActDigits rows per pair)
+constexpr int32_t kDecodeTileRows = 2;      // pairs per decode tile (MMA N = 16: kActDigits rows per pair)
 constexpr int32_t kDecodeMmaTileRows = 16;  // pairs per tile of the mma.sync decode kernel
 constexpr int64_t kDecodeMmaMaxPairs = 16;  // steps with at most this many pairs take the mma.sync kernel
 constexpr int64_t kDecodeTargetItems = 1200; // down items per step that keep every CTA busy
-constexpr int64_t kDecodeMinRange = 4;       // gate_up range: chunks (256 K) at least
-constexpr int64_t kDecodeMaxRanges = 1024;   // gate_up ranges at most, for a step with the fewest tiles
 constexpr int32_t kDecodeMinSegChunks = 2;   // at least 2 chunks of 256 K per decode item
 constexpr int64_t kDecodeMaxSegments = 16;   // K segments per row block
 
@@ -25,6 +23,14 @@ int g_cc_ok[kMaxDevices];   // 0 = unknown, 1 = ok, 2 = not sm_103
 std::mutex g_mu;
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+bool layer_shape_ok(int32_t E, int32_t H, int32_t I)
+{
+    return E >= 1 && E <= MOE_W2_MAX_EXPERTS && H >= 256 && I >= 256 && H % 256 == 0 && I % 256 == 0 &&
+           (int64_t)H * I <= ((int64_t)1 << 31);
+}
+
+}  // namespace
 
 moe_w2_status check_device()
 {
@@ -42,14 +48,6 @@ moe_w2_status check_device()
     }
     return g_cc_ok[dev] == 1 ? MOE_W2_OK : MOE_W2_ERR_DEVICE;
 }
-
-bool layer_shape_ok(int32_t E, int32_t H, int32_t I)
-{
-    return E >= 1 && E <= MOE_W2_MAX_EXPERTS && H >= 256 && I >= 256 && H % 256 == 0 && I % 256 == 0 &&
-           (int64_t)H * I <= ((int64_t)1 << 31);
-}
-
-}  // namespace
 
 std::mutex& init_mutex()
 {
@@ -74,19 +72,9 @@ int64_t max_tiles(int64_t P, int32_t E, bool decode)
 
 DecodeSplit decode_split(int64_t P, int32_t E, int32_t H, int32_t I)
 {
-    DecodeSplit d{};
-    // gate_up: the chunks of all (tile, 64-row block) units are cut into at most
-    // kDecodeMaxRanges ranges of at least kDecodeMinRange chunks (the device
-    // picks the count from the tile count).  A unit of nch chunks then meets at
-    // most ceil(nch / len) + 1 ranges, len the shortest range, which is at
-    // least the minimum and at least (chunks of ceil(P / kDecodeTileRows) tiles) / max ranges.
-    const int64_t nch_gu = H / 256, rbg = I / 64;
-    const int64_t tiles_min = std::max<int64_t>(1, (P + kDecodeTileRows - 1) / kDecodeTileRows);
-    const int64_t len = std::max<int64_t>(kDecodeMinRange, tiles_min * rbg * nch_gu / kDecodeMaxRanges);
-    d.gu_min_range = (int32_t)len;
-    d.s_gu = (int32_t)std::min<int64_t>(nch_gu, (nch_gu + len - 1) / len + 1);
     // down: each 128-row block's K in s_dn equal segments, as many as keep a
     // small step's down phase in several short items per CTA
+    DecodeSplit d{};
     const int64_t tiles = std::max<int64_t>(1, std::min<int64_t>(P, E));
     const int32_t nch_dn = I / 256;
     const int64_t rbd = H / 128;
@@ -144,7 +132,6 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
         w.sxd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * T * (H / 32)));
         w.hd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * P * (I / 2)));
         w.shd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * P * (I / 32)));
-        w.gu_part = reinterpret_cast<float*>(take(sizeof(float) * w.split.s_gu * P * 2 * I));
         w.stage = reinterpret_cast<float*>(take(sizeof(float) * w.split.s_dn * P * H));
     } else {
         w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * H));

@@ -30,15 +30,19 @@ __host__ __device__ __forceinline__ int t16_pos(int n) { return (n & ~15) | ((n 
 //   a = sum_r d_r * 2^(s_r - 127) + residual,
 // where row r encodes, rounded to the nearest e2m1 value, what rows 0..r-1 left
 // over, scaled so that the block's largest leftover maps into (3, 6].  A row
-// shrinks the leftover about tenfold: five rows put a matrix-vector product
-// within ~2e-5 (relative L2) of the one with the exact activations, and the
-// layer output (where h is rounded to bf16 in between) within ~3e-4; four rows
-// would leave ~1e-3 there.
+// shrinks the block's largest leftover at least threefold (about tenfold on
+// typical data), so the residual is bounded relative to the block's largest
+// element, not to each element.  Eight rows, measured on a CPU model of the
+// rows against the oracle, reproduce x and h exactly on normal activations and
+// on blocks with one element 2^8..2^12 times the others or with exact zeros
+// beside large values; six rows leave up to ~2.6e-4 (relative L2 of the layer
+// output) on those blocks and five ~8e-4.  Two pairs of eight rows fill the
+// MMA's N = 16, so the rows beyond five cost no MMAs.
 // Inside every group of 16 elements, packed position p (nibble p & 1 of byte
 // p >> 1 of the row) holds element fp4_elem(p) = 2 (p & 7) + (p >> 3): the code
 // expansion puts the even codes of a 16-code word in one TMEM column and the odd
 // codes in the next, and the MMA reads column j nibble i as K index 8 j + i.
-constexpr int kActDigits = 5;
+constexpr int kActDigits = 8;
 __host__ __device__ __forceinline__ int fp4_elem(int p) { return ((p & 7) << 1) | (p >> 3); }
 __host__ __device__ __forceinline__ int fp4_pos(int e) { return ((e & 1) << 3) | (e >> 1); }
 
@@ -215,15 +219,10 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // ------------------------------------------------------------------ workspace
-// Decode split of K for the block-scaled kernel: a work item is (tile of <= 3
-// pairs of one expert, 128 weight rows, a range of K chunks of 256).  For
-// gate_up the 128 rows are 64 gate rows and their 64 up rows; when the units
-// are fewer than the CTAs their chunks are cut into equal ranges of the whole
-// phase, one per CTA.  Down K is cut into equal segments per 128-row block.
-// Both keep every CTA of a small step busy.
+// Decode split of the down projection's K for the block-scaled kernel: each
+// 128-row block of W_down is cut into s_dn segments of l_dn chunks of 256, one
+// work item each, so that a small step still has work for every CTA.
 struct DecodeSplit {
-    int32_t s_gu;         // gate_up: contributing items per 64-row block at most (K = H in ranges)
-    int32_t gu_min_range; // gate_up: chunks per range at least (the kernel makes no shorter ranges)
     int32_t s_dn, l_dn;   // down: segments, chunks per segment (K = I)
 };
 DecodeSplit decode_split(int64_t P, int32_t E, int32_t H, int32_t I);
@@ -240,20 +239,19 @@ struct Workspace {
     int32_t* active_count; // [1]
     int4* tiles;           // GEMM tiles (expert, first slot, pairs, 0)
     int32_t* tile_count;   // [1]
-    int32_t* counters;     // decode, zeroed by the permutation kernel: per (tile, 64-row block of h) K
-                           // segments done, plus one once h of the block is written [max_tiles][I/64];
-                           // the item queue [1]
+    int32_t* counters;     // decode, zeroed by the permutation kernel.  Block-scaled kernel: per
+                           // (tile, 64-row block of h) the publications of its h [max_tiles][I/64],
+                           // then the item queue [1].  mma.sync kernel: see decode_counter_count
     // prefill, and the mma.sync decode kernel
     uint16_t* xa;          // activation rows, T16 layout: prefill in expert order [P][H], decode per token [T][H]
     uint16_t* h;           // SiLU(gate)*up rows in expert order, T16 layout [P][I]
     float* stage;          // per-pair outputs times router weight, slot t*k+j: prefill [P][H],
                            // decode [s_dn][P][H] (one slab per K segment of down)
     // decode
-    uint8_t* xd;           // e2m1 digit rows of x, kActDigits per token [5T][H/2]
-    uint8_t* sxd;          // their UE8M0 bytes [5T][H/32]
-    uint8_t* hd;           // e2m1 digit rows of h, kActDigits per pair (expert order) [5P][I/2]
-    uint8_t* shd;          // their UE8M0 bytes [5P][I/32]
-    float* gu_part;        // gate_up partial sums per K segment [s_gu][P][2I]
+    uint8_t* xd;           // e2m1 digit rows of x, kActDigits per token [8T][H/2]
+    uint8_t* sxd;          // their UE8M0 bytes [8T][H/32]
+    uint8_t* hd;           // e2m1 digit rows of h, kActDigits per pair (expert order) [8P][I/2]
+    uint8_t* shd;          // their UE8M0 bytes [8P][I/32]
     DecodeSplit split;
     size_t bytes;
 };
@@ -300,6 +298,9 @@ cudaError_t launch_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float
                            cudaStream_t s);
 
 int sm_count();
+// MOE_W2_OK when the current device has compute capability 10.3, else
+// MOE_W2_ERR_DEVICE (MOE_W2_ERR_CUDA if the query fails); cached per device.
+moe_w2_status check_device();
 
 // One-time set-up per device (kernel attributes, occupancy), safe under
 // concurrent calls: kernel attributes belong to a device's context, so each

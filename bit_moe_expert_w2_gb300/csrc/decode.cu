@@ -1,54 +1,53 @@
 // Decode path (T <= 64): the 2-bit planes of every active expert are streamed
-// from HBM once per layer and multiplied on the tensor cores in block-scaled FP8.
+// from HBM once per layer and multiplied on the tensor cores in block-scaled FP4
+// (tcgen05.mma kind::mxf4).
 //
 // vLLM-Moet, page "vLLM-Moet wiki", section "The kernels": codes expanded in
-// registers through a byte-permute lookup table and fed to block-scaled
-// tensor-core MMAs; section "FP4 recovery": decode is HBM-bound, the 2-bit read
-// is the cost.  Page "The v0.24.0 port", section "Benchmarks": tokens grouped by
-// expert, so each active expert's weights are read once per step however many
-// tokens use it.  Page "The v0.24.0 port", "Deterministic unpermute" bullet:
-// per-pair results are placed in their own slot and summed in a fixed order.
+// registers and fed to block-scaled tensor-core MMAs; section "FP4 recovery":
+// decode is HBM-bound, the 2-bit read is the cost.  Page "The v0.24.0 port",
+// section "Benchmarks": tokens grouped by expert, so each active expert's
+// weights are read once per step however many tokens use it.  Page "The
+// v0.24.0 port", "Deterministic unpermute" bullet: per-pair results are placed
+// in their own slot and summed in a fixed order.
 //
 // Why block-scaled fp4 operands (tcgen05.mma kind::mxf4, scale_vec::2X): a
 // weight is +-1 or +-4 times 2^(s-127) with one UE8M0 byte s per 32 K of a row,
 // which is an e2m1 value under an MX block scale.  The tensor core applies s
 // itself, so the expansion is one nibble per code, (c << 2) | 2: per 16-code
 // word one shift and two and-or operations, with no table.  Activations enter
-// as kActDigits rows of e2m1 digits each (fp4_elem order, digit_scale_byte),
-// which keeps a matrix-vector product within ~2e-4 of the exact one.  Packed
-// operands halve the MMAs (K = 64 each) and the tensor-memory bytes per code,
-// so a chunk covers 256 K of a row in the same 32 columns.
-
-// Work item = (tile of <= 3 pairs of one expert, 128 weight rows, K segment).
-// gate_up rows: 64 gate rows and the matching 64 up rows; down rows: 128 rows of
-// W_down.  Each CTA has six warps:
-//   warp 4     producer: takes items from a global queue, publishes them, and
-//              streams every 256-K chunk into a ring of shared-memory slots:
-//              code bytes by TMA (128 rows x 64 bytes, 64B-swizzled) with the
-//              16-byte scale group (2 chunks) of every weight row, the item's 16
-//              digit rows (written straight into the 128B-swizzled UMMA layout)
-//              and their scale groups by cp.async
+// as kActDigits rows of e2m1 digits each (fp4_elem order, digit_scale_byte).
+// Packed operands need one MMA of K = 64 per 64 codes of a row, so a 256-K
+// chunk of a row is 32 TMEM columns.
+//
+// Work items (one global queue, every gate_up unit before any down item):
+//   gate_up  (tile of <= 2 pairs of one expert, 64-row block): the block's 64
+//            gate rows and its 64 up rows over the whole K = H.  Its epilogue
+//            writes h = bf16(SiLU(g) * u) of those 64 elements as digit rows and
+//            publishes them with one release add per 32 elements.
+//   down     (tile, 128-row block of W_down, K segment of I): its epilogue
+//            writes w * (W_down h) into the pair's fp32 slot of that segment; a
+//            dependent combine kernel sums every token's slots in (j, segment)
+//            order into y.
+// Each CTA has six warps:
+//   warp 4     producer: takes items from the queue, publishes them, and streams
+//              every 256-K chunk into a ring of shared-memory slots: the code
+//              tile (128 rows x 64 bytes, 64B-swizzled) and the 16-byte scale
+//              group of every weight row by TMA (slot barrier full_a), and the
+//              tile's 16 activation digit rows (straight into the 128B-swizzled
+//              UMMA layout) with their scale groups by cp.async (full_b).  A
+//              down item's code chunks go out at once; its activation rows (h)
+//              only after the gate_up units that write them have published them.
 //   warps 0-3  consumers, one per TMEM lane quadrant and one thread per weight
-//              row: expand the row's 256 codes of a chunk to packed e2m1 and store
-//              them with the row's two scale words into TMEM, plus this
-//              quadrant's copy of the digit rows' scale words
+//              row: expand the row's 256 codes of a chunk to packed e2m1, store
+//              them with the row's two scale words and this quadrant's copy of
+//              the digit rows' scale words into TMEM; then the item epilogues
 //   warp 5     MMA issuer (one thread): 4 x tcgen05.mma (M=128, N=16, K=64) per
 //              chunk into one of two TMEM accumulators
-//   warp 6     finisher: the cross-CTA part of every gate_up epilogue
 // An item's accumulator is read by the consumer warps after the first chunk of
-// the next item (it is double-buffered), warp by warp with no CTA-wide barrier:
-//   gate_up  partial sums of the K segment -> gu_part; the finisher counts the
-//            segment, and the last of the S segments of a (tile, 64-row block)
-//            sums them in segment order, writes h = bf16(SiLU(g) * u) as digit
-//            rows and marks the block ready
-//   down     w * partial -> stage[segment][pair]
-// A separate combine kernel, launched as a programmatic dependent, sums every
-// token's slots in (j, segment) order and writes y.
-// A down item reads only the h row blocks of its K segment.  Its producer
-// publishes the item, then waits (bounded) until each of those blocks is marked
-// ready before loading its chunks, so the consumers see a down item coming and
-// store a pending gate_up epilogue before they block on its data.  Every wait is bounded; on a timeout the kernel raises the pipeline
-// status bit, drains its MMAs, frees its tensor memory and returns.
+// the next item (it is double-buffered), or before the next item when that is a
+// down item (whose data may wait for h: no epilogue is held across that wait).
+// Every wait is bounded; on a timeout the kernel raises the pipeline status bit,
+// drains its MMAs, frees its tensor memory and returns.
 #include <algorithm>
 
 #include "tc.cuh"
@@ -59,15 +58,14 @@ namespace {
 
 constexpr int kChunk = 256;                          // K per chunk: 4 MMAs of K = 64 (two scale blocks each)
 constexpr int kRows = 128;                           // weight rows per item (MMA M)
-constexpr int kTilePairs = 3;                        // pairs per tile
-constexpr int kN = 16;                               // MMA N: the digit rows of every pair (15), padded
+constexpr int kTilePairs = 2;                        // pairs per tile
+constexpr int kN = 16;                               // MMA N: the digit rows of the tile's pairs
 static_assert(kActDigits * kTilePairs <= kN, "a tile's digit rows must fit the MMA N");
 constexpr int kCWarps = 4;                           // consumer warps
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kFinisherWarp = 6;
-constexpr int kThreads = 7 * 32;
-constexpr int kSlots = 3;                            // chunk slots (3 measured faster than 4 or 5)
+constexpr int kThreads = 6 * 32;
+constexpr int kSlots = 4;                            // chunk slots
 constexpr uint32_t kCodeBytes = kRows * 64;          // 128 rows x 64 code bytes, 64B-swizzled
 constexpr uint32_t kBOff = kCodeBytes;               // 16 digit rows x 128 bytes (256 e2m1), 128B-swizzled
 constexpr uint32_t kSlotBytes = kBOff + kN * 128;    // 10240, a multiple of 1024
@@ -82,11 +80,9 @@ constexpr uint32_t kColSfa = 96;                     // stage s, word w, quadran
 constexpr uint32_t kColSfb = 112;                    // stage s, word w: column 112 + 8s + 4w
 // (scale-factor operands start on a 4-column boundary: an M = 128 tile's A
 // scales span 4 columns, one per lane quadrant; a chunk has two scale words)
-constexpr int32_t kHReady = 1 << 20;                 // added to a row block's counter once its h is written
+constexpr int32_t kHPublished = 2;                   // release adds per 64-element block of h (one per 32)
 
 struct LayerArgs {
-    const uint8_t* w13_scales;   // [E][2I][H/32]
-    const uint8_t* w2_scales;    // [E][H][I/32]
     int32_t H, I, T, k, E;
     DecodeSplit split;
     int64_t P;
@@ -94,69 +90,52 @@ struct LayerArgs {
     const int32_t* tile_count;
     const int32_t* sorted;
     const float* weights;
-    const int32_t* ids;
-    const uint8_t* xd;           // [5T][H/2] digit rows of x
-    const uint8_t* sxd;          // [5T][H/32]
-    uint8_t* hd;                 // [5P][I/2] digit rows of h
-    uint8_t* shd;                // [5P][I/32]
-    float* gu_part;              // [s_gu][P][2I]
+    const uint8_t* xd;           // [8T][H/2] digit rows of x
+    const uint8_t* sxd;          // [8T][H/32]
+    uint8_t* hd;                 // [8P][I/2] digit rows of h
+    uint8_t* shd;                // [8P][I/32]
     float* stage;                // [s_dn][P][H]
-    int32_t* gu_seg;             // [tiles][I/64]: contributing items done; + kHReady once h is written
+    int32_t* h_flag;             // [tiles][I/64]: release adds once h of the block is written
     int32_t* queue;
-    uint16_t* y;
     uint32_t* status;
 };
 
 struct SharedState {
-    uint64_t full[kSlots];       // producer -> consumers, MMA: slot filled (tx bytes + 32 cp.async arrivals)
+    uint64_t full_a[kSlots];     // producer -> consumers: code tile and weight-row scale groups landed (tx bytes)
+    uint64_t full_b[kSlots];     // producer -> consumers, MMA: digit rows and their scale groups landed (32 cp.async)
     uint64_t empty[kSlots];      // MMA commit -> producer: slot read
     uint64_t a_full[2];          // consumer warps -> MMA: A stage written
     uint64_t a_empty[2];         // MMA commit -> consumers: A stage read
     uint64_t d_full[2];          // MMA commit -> consumers: accumulator complete
     uint64_t d_empty[2];         // consumer warps -> MMA: accumulator read
+    uint64_t u_ready[2];         // up-row warps -> gate-row warps: up sums in u_buf
     uint64_t info_full[kInfo];   // producer -> consumers, MMA: item published
-    uint64_t info_empty[kInfo];  // consumers, MMA, finisher -> producer: item done with
-    uint64_t epi[kInfo];         // consumer warps -> finisher: item's partial sums stored
+    uint64_t info_empty[kInfo];  // consumers, MMA -> producer: item done with
     uint64_t drain;
     int info[kInfo][12];         // published items (Item fields; kind -1 at the end)
+    float u_buf[2][kTilePairs][64];
     uint32_t tmem;
     int abort_flag;
 };
 
 // A work item: one tile, 128 weight rows (gate_up: a 64-row block of gate and
 // of up; down: a 128-row block of W_down) and the K chunks [c0, c1).
-//   gate_up  K is cut into ranges of the whole phase's chunk sequence, one
-//            range per queue entry, of equal length; a range may start and end
-//            inside a row block, so a row block has cnt contributing items,
-//            seg = 0 .. cnt-1 in K order
-//   down     a row block's K is cut into s_dn segments of l_dn chunks
 struct Item {
     int kind;   // 1 gate_up, 0 down, -1 end
-    int ti, rb, seg, c0, c1, cnt, expert, q0, nrows;
+    int ti, rb, seg, c0, c1, expert, q0, nrows;
 };
 
 __device__ __forceinline__ void put_item(int* dst, const Item& m)
 {
     dst[0] = m.kind; dst[1] = m.ti; dst[2] = m.rb; dst[3] = m.seg; dst[4] = m.c0;
-    dst[5] = m.c1; dst[6] = m.cnt; dst[7] = m.expert; dst[8] = m.q0; dst[9] = m.nrows;
+    dst[5] = m.c1; dst[6] = m.expert; dst[7] = m.q0; dst[8] = m.nrows;
 }
 __device__ __forceinline__ Item get_item(const int* src)
 {
     Item m;
     m.kind = src[0]; m.ti = src[1]; m.rb = src[2]; m.seg = src[3]; m.c0 = src[4];
-    m.c1 = src[5]; m.cnt = src[6]; m.expert = src[7]; m.q0 = src[8]; m.nrows = src[9];
+    m.c1 = src[5]; m.expert = src[6]; m.q0 = src[7]; m.nrows = src[8];
     return m;
-}
-
-// Range r of n_ranges over c_total chunks: [r c_total / n_ranges, (r+1) c_total / n_ranges).
-__device__ __forceinline__ int64_t range_start(int64_t r, int64_t c_total, int64_t n_ranges)
-{
-    return r * c_total / n_ranges;
-}
-// The range holding chunk f (the last r with range_start(r) <= f).
-__device__ __forceinline__ int64_t range_of(int64_t f, int64_t c_total, int64_t n_ranges)
-{
-    return ((f + 1) * n_ranges - 1) / c_total;
 }
 
 __device__ __forceinline__ int32_t ld_acquire(const int32_t* p)
@@ -165,6 +144,14 @@ __device__ __forceinline__ int32_t ld_acquire(const int32_t* p)
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+// Add with release semantics at GPU scope: this thread's earlier writes, and
+// those it has observed (the warp's, after __syncwarp), are visible to a thread
+// that reads the new value with ld_acquire.
+__device__ __forceinline__ void red_release_add(int32_t* p, int32_t v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Position in a ring of N slots: slot q % N and phase bit (q / N) & 1 of the
 // running chunk count q, stepped without a division.
 template <uint32_t N>
@@ -181,8 +168,7 @@ struct RingPos {
 
 // Two words of packed e2m1 from one word of 16 codes: nibble n of r0 holds code
 // 2n and nibble n of r1 code 2n + 1, each as (c << 2) | 2 (c in bits 3:2: +1,
-// +4, -1, -4).  One shift and two and-or operations per word; the compiler
-// issues the shift as a multiply (FMA pipe).
+// +4, -1, -4).  One shift and two and-or operations per word.
 __device__ __forceinline__ void expand_fp4(uint32_t w, uint32_t& r0, uint32_t& r1)
 {
     asm("{\n\t.reg .b32 t0;\n\t"
@@ -210,97 +196,78 @@ __device__ __forceinline__ float pair_sum(const float (&v)[16], int j)
     return s;
 }
 
-// Consumer side of an item's epilogue, one warp (its 32 weight rows): the
-// accumulator rows as partial sums in global memory, then one arrival on the
-// item's epi barrier for the finisher warp.
-__device__ __noinline__ void epilogue_store(const LayerArgs& a, SharedState& sh, uint32_t tq, const Item& it, int n,
-                                            volatile int* abort)
+// h of one 32-element block and one pair (one value per lane, block element =
+// lane) as kActDigits digit rows of pair slot q: the lane's element sits at
+// packed position pos of the block; the other nibble of its byte belongs to
+// lane ^ 2, and the lane with the low nibble writes the byte.
+__device__ __forceinline__ void store_h_digits(const LayerArgs& a, int64_t q, int blk, float v)
 {
-    const int lane = threadIdx.x & 31, m = threadIdx.x;
-    const uint32_t b = (uint32_t)n & 1u;
+    const int lane = threadIdx.x & 31;
+    const int pos = (lane & 16) | fp4_pos(lane & 15);
+#pragma unroll
+    for (int d = 0; d < kActDigits; ++d) {
+        const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
+        const uint32_t sd = digit_scale_byte(__uint_as_float(amax_bits));
+        float qv;
+        const uint32_t nib = e2m1_digit(v * digit_inv_scale(sd), qv);
+        v -= qv * digit_scale(sd);
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, nib, 2);
+        const int64_t row = kActDigits * q + d;
+        if ((pos & 1) == 0) a.hd[row * (a.I / 2) + blk * 16 + (pos >> 1)] = (uint8_t)(nib | (other << 4));
+        if (lane == 0) a.shd[row * (a.I / 32) + blk] = (uint8_t)sd;
+    }
+}
+
+// Epilogue of an item on the consumer warps: item n of this CTA (accumulator
+// n & 1), and for gate_up its gn-th gate_up epilogue (u_buf and u_ready gn & 1).
+//   gate_up  warps 2-3 (the up rows) hand their sums to warps 0-1 through
+//            shared memory; warps 0-1 (the gate rows) form h = bf16(SiLU(g) * u)
+//            for 32 elements each, write its digit rows and publish them
+//   down     every warp writes w * (its rows of W_down h) into the pairs' slots
+// u_buf[gn & 1] is written again only for gate_up epilogue gn + 2, which the
+// up-row warps reach after the MMA took an A stage from the gate-row warps that
+// those wrote after they finished epilogue gn.
+__device__ __noinline__ void epilogue(const LayerArgs& a, SharedState& sh, uint32_t tq, const Item& it, int n,
+                                      int gn, volatile int* abort)
+{
+    const int lane = threadIdx.x & 31, m = threadIdx.x, warp = m >> 5;
+    const uint32_t b = (uint32_t)n & 1u, ph = ((uint32_t)n >> 1) & 1u;
+    const uint32_t ub = (uint32_t)gn & 1u, uph = ((uint32_t)gn >> 1) & 1u;
     // every lane waits (each acquires); the outcome is made warp-uniform before
     // the .sync.aligned tensor-memory load
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.d_full[b]), ((uint32_t)n >> 1) & 1u, abort))) return;
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.d_full[b]), ph, abort))) return;
     tc_fence_after();
     float v[16];
     tmem_ld16(tq + kColD + 16 * b, v);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&sh.d_empty[b]));
-    const int64_t P = a.P;
     if (it.kind == 1) {
-        const int I2 = 2 * a.I;
-        const int col = m < 64 ? 64 * it.rb + m : a.I + 64 * it.rb + (m - 64);
-        float* dst = a.gu_part + ((int64_t)it.seg * P + it.q0) * I2 + col;
+        if (warp >= 2) {
+#pragma unroll
+            for (int j = 0; j < kTilePairs; ++j) sh.u_buf[ub][j][m - 64] = pair_sum(v, j);
+            mbar_arrive(smem_u32(&sh.u_ready[ub]));   // every lane: its own stores are released
+            return;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.u_ready[ub]), uph, abort))) return;
+        const int blk = 2 * it.rb + warp;   // the 32 elements 64 rb + 32 warp + lane of h
 #pragma unroll
         for (int j = 0; j < kTilePairs; ++j)
-            if (j < it.nrows) dst[(int64_t)j * I2] = pair_sum(v, j);
+            if (j < it.nrows) {
+                const float g = pair_sum(v, j), u = sh.u_buf[ub][j][m];
+                const float hv = __bfloat162float(__float2bfloat16_rn(silu_f(g) * u));
+                store_h_digits(a, (int64_t)it.q0 + j, blk, hv);
+            }
+        __syncwarp();
+        if (lane == 0) red_release_add(a.h_flag + it.ti * (a.I / 64) + it.rb, 1);
     } else {
         const int row = 128 * it.rb + m;
 #pragma unroll
         for (int j = 0; j < kTilePairs; ++j)
             if (j < it.nrows) {
                 const int pr = __ldg(a.sorted + it.q0 + j);
-                a.stage[((int64_t)it.seg * P + pr) * a.H + row] = __ldg(a.weights + pr) * pair_sum(v, j);
+                a.stage[((int64_t)it.seg * a.P + pr) * a.H + row] = __ldg(a.weights + pr) * pair_sum(v, j);
             }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&sh.epi[(uint32_t)n % kInfo]));
-}
-
-// Finisher side of a gate_up item's epilogue (one warp), once the four
-// consumer warps have stored its partial sums: count the item at its
-// (tile, 64-row block); the last of the block's cnt items sums their partial
-// sums in K order, writes h = bf16(SiLU(g) * u) as digit rows and marks the
-// block ready.  The fence after the barrier wait orders every store the barrier
-// made visible to this warp before the counter update (fences are cumulative).
-__device__ __noinline__ void finish_gate_up(const LayerArgs& a, const Item& it)
-{
-    const int lane = threadIdx.x & 31;
-    const int64_t P = a.P;
-    int32_t* cnt = a.gu_seg + it.ti * (a.I / 64) + it.rb;
-    int last = 0;
-    if (lane == 0) {
-        __threadfence();
-        last = atomicAdd(cnt, 1) == it.cnt - 1;
-    }
-    if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    __threadfence();
-    const int I2 = 2 * a.I;
-    // indices 64 rb + 32 blk + lane; one activation scale block per blk.  The
-    // lane's element sits at packed position pos of the block; the other nibble
-    // of its byte belongs to lane ^ 2, and the lane with the low nibble writes.
-    const int pos = (lane & 16) | fp4_pos(lane & 15);
-    for (int blk = 0; blk < 2; ++blk) {
-        const int i = 64 * it.rb + 32 * blk + lane;
-        for (int j = 0; j < it.nrows; ++j) {
-            const int64_t q = it.q0 + j;
-            float g = 0.f, u = 0.f;
-#pragma unroll 4
-            for (int sg = 0; sg < it.cnt; ++sg) {   // contributing items in K order
-                const float* src = a.gu_part + ((int64_t)sg * P + q) * I2;
-                g += __ldcg(src + i);
-                u += __ldcg(src + a.I + i);
-            }
-            float v = __bfloat162float(__float2bfloat16_rn(silu_f(g) * u));
-#pragma unroll
-            for (int d = 0; d < kActDigits; ++d) {
-                const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
-                const uint32_t sd = digit_scale_byte(__uint_as_float(amax_bits));
-                float qv;
-                const uint32_t nib = e2m1_digit(v * digit_inv_scale(sd), qv);
-                v -= qv * digit_scale(sd);
-                const uint32_t other = __shfl_xor_sync(0xffffffffu, nib, 2);
-                const int64_t row = kActDigits * q + d;
-                if ((pos & 1) == 0) a.hd[row * (a.I / 2) + (i & ~31) / 2 + (pos >> 1)] = (uint8_t)(nib | (other << 4));
-                if (lane == 0) a.shd[row * (a.I / 32) + i / 32] = (uint8_t)sd;
-            }
-        }
-    }
-    __syncwarp();
-    if (lane == 0) {
-        __threadfence();
-        atomicAdd(cnt, kHReady);   // h of the block is ready
     }
 }
 
@@ -316,7 +283,8 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(smem_u32(&sh.full[s]), 1 + 32);
+            mbar_init(smem_u32(&sh.full_a[s]), 1);
+            mbar_init(smem_u32(&sh.full_b[s]), 32);
             mbar_init(smem_u32(&sh.empty[s]), 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -324,11 +292,11 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
             mbar_init(smem_u32(&sh.a_empty[s]), 1);
             mbar_init(smem_u32(&sh.d_full[s]), 1);
             mbar_init(smem_u32(&sh.d_empty[s]), kCWarps);
+            mbar_init(smem_u32(&sh.u_ready[s]), 64);
         }
         for (int s = 0; s < kInfo; ++s) {
             mbar_init(smem_u32(&sh.info_full[s]), 1);
-            mbar_init(smem_u32(&sh.info_empty[s]), kCWarps + 2);
-            mbar_init(smem_u32(&sh.epi[s]), kCWarps);
+            mbar_init(smem_u32(&sh.info_empty[s]), kCWarps + 1);
         }
         mbar_init(smem_u32(&sh.drain), 1);
         sh.abort_flag = 0;
@@ -359,25 +327,13 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
     const int n_tiles = *a.tile_count;
     const int rbg = a.I / 64, rbd = a.H / 128;
     const int nch_gu = a.H / kChunk, nch_dn = a.I / kChunk;
-    // gate_up: the chunk sequence of all (tile, 64-row block) units in ranges.
-    // With at least one unit per CTA every unit is one range (its whole K), so
-    // the units finish in queue order and the down items of early tiles find
-    // their h ready; with fewer units K is split into ranges no shorter than
-    // the host's minimum, which bounds the contributing items of a row block
-    // (the gu_part slots).
-    const int64_t n_units = (int64_t)n_tiles * rbg;
-    const int64_t c_gu = n_units * nch_gu;
-    const int64_t r_gu = c_gu <= 0                     ? 0
-                         : n_units >= (int64_t)gridDim.x ? n_units
-                                                         : max((int64_t)1, min((int64_t)gridDim.x, c_gu / a.split.gu_min_range));
+    const int64_t n_gu = (int64_t)n_tiles * rbg;
     const int64_t n_dn = (int64_t)n_tiles * rbd * a.split.s_dn;
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------ producer
-        // Queue entries [0, r_gu) are gate_up ranges, then down items; every
-        // gate_up range is handed out before any down item.
-        uint32_t q = 0;
         RingPos<kSlots> rp;
+        uint32_t issued = 0;   // chunk loads issued (ring positions 0 .. issued-1)
         int n = 0;
         bool ok = true;
         // publish one item; false when the pipeline gave up
@@ -393,42 +349,66 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
             ++n;
             return true;
         };
+        // wait (bounded) for a free slot at ring position p
+        auto slot_free = [&](const RingPos<kSlots>& p) {
+            int w = 1;
+            if (lane == 0) w = mbar_wait(smem_u32(&sh.empty[p.slot]), p.phase ^ 1u, abort);
+            return __shfl_sync(0xffffffffu, w, 0) != 0;
+        };
+        // the code tile and the weight rows' scale groups of chunk ch (lane 0)
+        auto load_codes = [&](const Item& m, int ch, uint32_t slot) {
+            const uint32_t base = ring_addr + slot * kSlotBytes, fb = smem_u32(&sh.full_a[slot]);
+            const uint32_t sfbase = sf_addr + slot * kSfSlotBytes;
+            // the 16-byte group of scale bytes (2 chunks) holding this chunk's two
+            // words, for every weight row; every slot gets its own copy, so a
+            // consumer reads words 2 (ch % 2) and 2 (ch % 2) + 1 of its own slot
+            const int gx = (ch & ~1) * 8;
+            mbar_arrive_expect_tx(fb, kCodeBytes + kRows * 16);
+            if (m.kind == 1) {
+                // one box holds the row block's 64 gate rows, then its 64 up rows
+                // (planes 2e and 2e + 1 of the w13 plane seen as 2E planes of I rows)
+                tma_load_3d(base, &gu_map, ch * 64, 64 * m.rb, 2 * m.expert, fb);
+                tma_load_3d(sfbase, &gu_sf_map, gx, 64 * m.rb, 2 * m.expert, fb);
+            } else {
+                const int rd = m.expert * a.H + 128 * m.rb;
+                tma_load_2d(base, &dn_map, ch * 64, rd, fb);
+                tma_load_2d(sfbase, &dn_sf_map, gx, rd, fb);
+            }
+        };
+        // the h blocks a down item reads (64 elements each; four per chunk) are
+        // published (bounded wait): lane r watches blocks 4 c0 + r, 4 c0 + r + 32, ...
+        auto h_ready = [&](const Item& m) {
+            const int32_t* hs = a.h_flag + m.ti * rbg;
+            const int hb0 = (kChunk / 64) * m.c0, hb1 = (kChunk / 64) * m.c1;
+            auto all_ready = [&]() {
+                bool r = true;
+                for (int hb = hb0 + lane; hb < hb1; hb += 32) r = r && ld_acquire(hs + hb) >= kHPublished;
+                return __all_sync(0xffffffffu, r);
+            };
+            if (!all_ready()) {
+                const long long t0 = clock64();
+                bool timed_out = false;
+                while (!all_ready()) {
+                    if (__shfl_sync(0xffffffffu, *abort, 0)) break;
+                    if (clock64() - t0 > kWaitLimitCycles) {
+                        timed_out = true;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+                if (timed_out && lane == 0) *abort = 1;
+            }
+            __syncwarp();   // every lane's copies come after the lanes' acquires
+            return __shfl_sync(0xffffffffu, *abort, 0) == 0;
+        };
         // stream the chunks of a published item into the ring
         auto stream = [&](const Item& m) {
-            if (m.kind == 0) {
-                // the h row blocks this K range reads (64 rows each; four per
-                // chunk) must be written before their rows are copied: lane r
-                // watches blocks 4 c0 + r, 4 c0 + r + 32, ...
-                const int32_t* hs = a.gu_seg + m.ti * rbg;
-                const int hb0 = (kChunk / 64) * m.c0, hb1 = (kChunk / 64) * m.c1;
-                auto all_ready = [&]() {
-                    bool r = true;
-                    for (int hb = hb0 + lane; hb < hb1; hb += 32) r = r && ld_acquire(hs + hb) >= kHReady;
-                    return __all_sync(0xffffffffu, r);
-                };
-                if (!all_ready()) {
-                    const long long t0 = clock64();
-                    bool timed_out = false;
-                    while (!all_ready()) {
-                        if (__shfl_sync(0xffffffffu, *abort, 0)) break;
-                        if (clock64() - t0 > kWaitLimitCycles) {
-                            timed_out = true;
-                            break;
-                        }
-                        __nanosleep(128);
-                    }
-                    if (timed_out && lane == 0) *abort = 1;
-                }
-                __syncwarp();   // every lane's copies come after the lanes' acquires
-                if (__shfl_sync(0xffffffffu, *abort, 0)) return false;
-            }
             const bool gu = m.kind == 1;
             // tokens of the tile's pairs (lane j < kTilePairs holds pair j's), gate_up only
             const int tok = (gu && lane < m.nrows) ? __ldg(a.sorted + m.q0 + lane) / a.k : 0;
             // this lane's copy sources: 4 pieces of 16 bytes of the digit rows
-            // (row n = p / 8 = kActDigits * pair + digit, piece p % 8), lanes < 16
+            // (row nb = p / 8 = kActDigits * pair + digit, piece p % 8), lanes < 16
             // one digit row's scale bytes
-            const int64_t erow = (int64_t)m.expert * (gu ? 2 * a.I : a.H);
             const uint8_t* act = gu ? a.xd : a.hd;
             const uint8_t* sact = gu ? a.sxd : a.shd;
             const int64_t kact = gu ? a.H : a.I;
@@ -449,37 +429,34 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 const int64_t row = (int64_t)kActDigits * (gu ? (int64_t)tj : (int64_t)(m.q0 + j)) + d;
                 if (lane < kN && j < m.nrows) sfb_src = sact + row * (kact / 32);
             }
-            for (int ch = m.c0; ch < m.c1; ++ch, ++q, rp.step()) {
-                const uint32_t slot = rp.slot;
-                int w = 1;
-                if (lane == 0) w = mbar_wait(smem_u32(&sh.empty[slot]), rp.phase ^ 1u, abort);
-                if (!__shfl_sync(0xffffffffu, w, 0)) return false;
-                const uint32_t base = ring_addr + slot * kSlotBytes, fb = smem_u32(&sh.full[slot]);
+            // the digit rows and their scale groups of chunk ch (every lane)
+            auto load_b = [&](int ch, uint32_t slot) {
+                const uint32_t base = ring_addr + slot * kSlotBytes;
                 const uint32_t sfbase = sf_addr + slot * kSfSlotBytes;
-                // the 16-byte group of scale bytes (2 chunks) holding this chunk's
-                // two words, for every weight row; every slot gets its own copy, so
-                // a consumer reads words 2 (ch % 2) and 2 (ch % 2) + 1 of its own slot
-                const int gx = (ch & ~1) * 8;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(fb, kCodeBytes + kRows * 16);
-                    if (gu) {
-                        // one box holds the row block's 64 gate rows, then its 64 up
-                        // rows (planes 2e and 2e + 1 of the w13 plane seen as 2E
-                        // planes of I rows)
-                        tma_load_3d(base, &gu_map, ch * 64, 64 * m.rb, 2 * m.expert, fb);
-                        tma_load_3d(sfbase, &gu_sf_map, gx, 64 * m.rb, 2 * m.expert, fb);
-                    } else {
-                        const int rd = (int)(erow + 128 * m.rb);
-                        tma_load_2d(base, &dn_map, ch * 64, rd, fb);
-                        tma_load_2d(sfbase, &dn_sf_map, gx, rd, fb);
-                    }
-                }
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (bsrc[i] != nullptr) cp_async16(base + bdst[i], bsrc[i] + ch * 128);
-                // the activation rows' scale groups (lanes < 16, one row each)
-                if (sfb_src != nullptr) cp_async16(sfbase + kSfbOff + lane * 16, sfb_src + gx);
-                cp_async_arrive_noinc(fb);
+                if (sfb_src != nullptr) cp_async16(sfbase + kSfbOff + lane * 16, sfb_src + (ch & ~1) * 8);
+                cp_async_arrive_noinc(smem_u32(&sh.full_b[slot]));
+            };
+            // down: the first chunks' code tiles go out before the wait for h
+            const int npre = gu ? 0 : min(m.c1 - m.c0, kSlots);
+            RingPos<kSlots> rp0 = rp;
+            int ch = m.c0;
+            for (int i = 0; i < npre; ++i, ++ch, rp.step()) {
+                if (!slot_free(rp)) return false;
+                if (lane == 0) load_codes(m, ch, rp.slot);
+            }
+            issued += (uint32_t)npre;
+            if (!gu) {
+                if (!h_ready(m)) return false;
+                for (int i = 0; i < npre; ++i, rp0.step()) load_b(m.c0 + i, rp0.slot);
+            }
+            for (; ch < m.c1; ++ch, rp.step()) {
+                if (!slot_free(rp)) return false;
+                if (lane == 0) load_codes(m, ch, rp.slot);
+                ++issued;
+                load_b(ch, rp.slot);
             }
             return true;
         };
@@ -487,32 +464,19 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
             int it = 0;
             if (lane == 0) it = atomicAdd(a.queue, 1);
             it = __shfl_sync(0xffffffffu, it, 0);
-            if (it < r_gu) {
-                // gate_up range: every piece inside one (tile, row block) unit is an item
-                const int64_t f0 = range_start(it, c_gu, r_gu), f1 = range_start(it + 1, c_gu, r_gu);
-                for (int64_t f = f0; f < f1 && ok;) {
-                    const int64_t u = f / nch_gu;
-                    Item m;
-                    m.kind = 1;
-                    m.ti = (int)(u / rbg);
-                    m.rb = (int)(u % rbg);
-                    m.c0 = (int)(f - u * nch_gu);
-                    m.c1 = (int)min((int64_t)nch_gu, m.c0 + (f1 - f));
-                    const int64_t first = range_of(u * nch_gu, c_gu, r_gu);
-                    m.seg = (int)(it - first);
-                    m.cnt = (int)(range_of((u + 1) * nch_gu - 1, c_gu, r_gu) - first + 1);
-                    const int4 t = a.tiles[m.ti];
-                    m.expert = t.x;
-                    m.q0 = t.y;
-                    m.nrows = t.z;
-                    ok = publish(m) && stream(m);
-                    f += m.c1 - m.c0;
-                }
-            } else if (it < r_gu + n_dn) {
+            Item m{};
+            if (it < n_gu) {
+                // gate_up unit: the (tile, 64-row block) over the whole K
+                m.kind = 1;
+                m.ti = (int)(it / rbg);
+                m.rb = (int)(it % rbg);
+                m.seg = 0;
+                m.c0 = 0;
+                m.c1 = nch_gu;
+            } else if (it < n_gu + n_dn) {
                 // down: (tile, segment, row block), so the first down items read
-                // the first h row blocks
-                const int64_t id = it - r_gu;
-                Item m;
+                // the first h blocks
+                const int64_t id = it - n_gu;
                 m.kind = 0;
                 m.ti = (int)(id / (rbd * a.split.s_dn));
                 const int rem = (int)(id % (rbd * a.split.s_dn));
@@ -520,21 +484,26 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 m.seg = rem / rbd;
                 m.c0 = m.seg * a.split.l_dn;
                 m.c1 = min(nch_dn, m.c0 + a.split.l_dn);
-                m.cnt = a.split.s_dn;
-                const int4 t = a.tiles[m.ti];
-                m.expert = t.x;
-                m.q0 = t.y;
-                m.nrows = t.z;
-                ok = publish(m) && stream(m);
             } else {
-                Item m{};
                 m.kind = -1;
                 publish(m);
                 break;
             }
+            const int4 t = a.tiles[m.ti];
+            m.expert = t.x;
+            m.q0 = t.y;
+            m.nrows = t.z;
+            ok = publish(m) && stream(m);
             if (!ok) break;
         }
         asm volatile("cp.async.wait_all;" ::: "memory");   // no copy of this warp outlives the CTA
+        if (*abort && lane == 0) {
+            // the consumers may have stopped before the last tiles landed: wait
+            // (bounded) for the tensor copies of the last kSlots positions
+            volatile int never = 0;
+            for (uint32_t pq = issued > (uint32_t)kSlots ? issued - kSlots : 0u; pq < issued; ++pq)
+                (void)mbar_wait(smem_u32(&sh.full_a[pq % kSlots]), (pq / kSlots) & 1u, &never);
+        }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -552,7 +521,8 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 bool ok = true;
                 for (int ch = m.c0; ch < m.c1; ++ch, ++q, rp.step()) {
                     const uint32_t slot = rp.slot, st = q & 1u;
-                    if (!mbar_wait2(smem_u32(&sh.full[slot]), rp.phase, smem_u32(&sh.a_full[st]), (q >> 1) & 1u, abort)) {
+                    if (!mbar_wait2(smem_u32(&sh.full_b[slot]), rp.phase, smem_u32(&sh.a_full[st]), (q >> 1) & 1u,
+                                    abort)) {
                         ok = false;
                         break;
                     }
@@ -579,26 +549,6 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
             volatile int never = 0;
             if (!mbar_wait(smem_u32(&sh.drain), 0u, &never)) *abort = 1;
         }
-    } else if (warp == kFinisherWarp) {
-        // ------------------------------------------------ finisher
-        for (int n = 0;; ++n) {
-            const uint32_t islot = (uint32_t)n % kInfo;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.info_full[islot]), ((uint32_t)n / kInfo) & 1u, abort)))
-                break;
-            const Item m = get_item(sh.info[islot]);
-            if (m.kind < 0) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sh.info_empty[islot]));
-                break;
-            }
-            // released only after this wait: the consumers cannot arrive for the
-            // item kInfo places later before this phase of epi[islot] is seen
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.epi[islot]), ((uint32_t)n / kInfo) & 1u, abort)))
-                break;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.info_empty[islot]));
-            if (m.kind == 1) finish_gate_up(a, m);
-        }
     } else {
         // ------------------------------------------------ consumers
         const int m = tid;   // weight row of the item
@@ -607,7 +557,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
         uint32_t q = 0, bad_scale = 0;
         RingPos<kSlots> rp;
         Item prev{};
-        int prev_n = 0, have_prev = 0;
+        int prev_n = 0, have_prev = 0, gn = 0;   // gn: gate_up epilogues done
         for (int n = 0;; ++n) {
             const uint32_t islot = (uint32_t)n % kInfo;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.info_full[islot]), ((uint32_t)n / kInfo) & 1u, abort)))
@@ -617,13 +567,14 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
             if (lane == 0) mbar_arrive(smem_u32(&sh.info_empty[islot]));
             if (cur.kind < 0) break;
             if (have_prev && cur.kind == 0) {   // before blocking on a down item's data
-                epilogue_store(a, sh, tq, prev, prev_n, abort);
+                epilogue(a, sh, tq, prev, prev_n, gn, abort);
+                gn += prev.kind;
                 have_prev = 0;
             }
             bool ok = true;
             for (int ch = cur.c0; ch < cur.c1; ++ch, ++q, rp.step()) {
                 const uint32_t slot = rp.slot, st = q & 1u;
-                const bool got = mbar_wait2(smem_u32(&sh.full[slot]), rp.phase, smem_u32(&sh.a_empty[st]),
+                const bool got = mbar_wait2(smem_u32(&sh.full_a[slot]), rp.phase, smem_u32(&sh.a_empty[st]),
                                             ((q >> 1) & 1u) ^ 1u, abort);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
@@ -641,10 +592,9 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                     wd[4 * u + 2] = v.z;
                     wd[4 * u + 3] = v.w;
                 }
-                // the chunk's two scale words of this row and of the digit rows
+                // the chunk's two scale words of this row
                 const uint32_t sfs = sf_addr + slot * kSfSlotBytes + 8u * (uint32_t)(ch & 1);
                 uint2 sfa = lds_u2(sfs + m * 16);
-                const uint2 sfb = lds_u2(sfs + kSfbOff + (lane & 15) * 16);
                 uint32_t r[32];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) expand_fp4(wd[i], r[2 * i], r[2 * i + 1]);
@@ -653,15 +603,21 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
 #pragma unroll
                     for (int t = 0; t < 8; ++t) {
                         uint32_t& wv = t < 4 ? sfa.x : sfa.y;
-                        const int sh = 8 * (t & 3);
-                        if (((wv >> sh) & 0xFFu) - 1u > 251u) {
+                        const int sh8 = 8 * (t & 3);
+                        if (((wv >> sh8) & 0xFFu) - 1u > 251u) {
 #pragma unroll
                             for (int c = 0; c < 4; ++c) r[4 * t + c] = 0u;
-                            wv = (wv & ~(0xFFu << sh)) | (127u << sh);
+                            wv = (wv & ~(0xFFu << sh8)) | (127u << sh8);
                             bad_scale = 1;
                         }
                     }
                 }
+                // the digit rows' scale words (this quadrant's copy) come with the rows
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.full_b[slot]), rp.phase, abort))) {
+                    ok = false;
+                    break;
+                }
+                const uint2 sfb = lds_u2(sfs + kSfbOff + (lane & 15) * 16);
                 tmem_st_stage4(tq + kColA + 32 * st, r, tq + kColSfa + 8 * st + warp, sfa.x,
                                tq + kColSfa + 8 * st + 4 + warp, sfa.y, tq + kColSfb + 8 * st, sfb.x,
                                tq + kColSfb + 8 * st + 4, sfb.y);
@@ -669,7 +625,8 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh.a_full[st]));
                 if (ch == cur.c0 && have_prev) {
-                    epilogue_store(a, sh, tq, prev, prev_n, abort);
+                    epilogue(a, sh, tq, prev, prev_n, gn, abort);
+                    gn += prev.kind;
                     have_prev = 0;
                 }
             }
@@ -678,7 +635,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
             prev_n = n;
             have_prev = 1;
         }
-        if (have_prev && !*abort) epilogue_store(a, sh, tq, prev, prev_n, abort);
+        if (have_prev && !*abort) epilogue(a, sh, tq, prev, prev_n, gn, abort);
         if (bad_scale) flag_status(a.status, MOE_W2_DEV_BAD_SCALE);
     }
 
@@ -733,8 +690,6 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     const int64_t mt = max_tiles(P, E, true);
 
     LayerArgs a{};
-    a.w13_scales = w.w13_scales;
-    a.w2_scales = w.w2_scales;
     a.H = H;
     a.I = I;
     a.T = T;
@@ -746,16 +701,13 @@ cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* we
     a.tile_count = ws.tile_count;
     a.sorted = ws.sorted;
     a.weights = weights;
-    a.ids = ids;
     a.xd = ws.xd;
     a.sxd = ws.sxd;
     a.hd = ws.hd;
     a.shd = ws.shd;
-    a.gu_part = ws.gu_part;
     a.stage = ws.stage;
-    a.gu_seg = ws.counters;                    // zeroed by the permutation kernel
-    a.queue = a.gu_seg + mt * (I / 64);
-    a.y = y;
+    a.h_flag = ws.counters;                    // zeroed by the permutation kernel
+    a.queue = a.h_flag + mt * (I / 64);
     a.status = status;
 
     // code tiles: 64 bytes (256 codes) x 128 rows, 64B-swizzled; gate_up as a

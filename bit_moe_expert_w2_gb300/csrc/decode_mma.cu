@@ -46,9 +46,7 @@ namespace moe_w2 {
 
 namespace {
 
-#ifndef MOE_W2_DEC_MIN_CTAS
-#define MOE_W2_DEC_MIN_CTAS 4        // CTAs per SM the register budget is sized for
-#endif
+constexpr int kMinCtasPerSm = 4;     // CTAs per SM the register budget is sized for
 constexpr int kChunk = 256;          // K elements per chunk
 constexpr int kWarps = 4;            // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;   // + the producer warp
@@ -270,7 +268,7 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, Sh
 // down index and is held by a running CTA, so the waits always end (each is
 // still bounded and gives up with the pipeline-timeout status bit).  Which CTA
 // runs an item never changes its result.
-__global__ void __launch_bounds__(kThreads, MOE_W2_DEC_MIN_CTAS)
+__global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
 decode_mma_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_constant__ CUtensorMap dn_map,
                     DecArgs gu, DecArgs dn, int32_t* __restrict__ gu_done, int32_t* __restrict__ queue)
 {

@@ -13,7 +13,7 @@ namespace moe_w2 {
 
 // Bit OR-ed into the device status when a pipeline wait gives up (a bug, never
 // expected): the kernel stops its work loop, releases tensor memory and returns.
-constexpr uint32_t kDevPipelineTimeout = 0x80000000u;
+constexpr uint32_t kDevPipelineTimeout = MOE_W2_DEV_PIPELINE_TIMEOUT;
 constexpr long long kWaitLimitCycles = 4000000000ll;   // ~2 s at 2 GHz
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)

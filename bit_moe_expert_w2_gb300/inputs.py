@@ -33,6 +33,17 @@ Recipe (all numpy PCG64 via ``default_rng(seed)``):
   * NVFP4 tensors: e2m1 nibbles uniform over all 16 codes (uniform random bytes,
     low nibble = even element), e4m3 block-16 scales 2^U(-6, 2) rounded to the
     nearest e4m3fn value (ties to even mantissa), scale_2 = 2^-8 per tensor.
+  * wide-range activations (parity cases for activations with a large dynamic
+    range inside a 32-element block, as real LLM activations have):
+    "outlier": standard normal, then in every aligned block of 32 one element
+    at a uniform position multiplied by 2^e, e uniform in [lo, hi];
+    "zeros": every element zero with probability 1/2, and every other block
+    multiplied by 2^10 (blocks mixing exact zeros with large values);
+    "both": the two applied one after the other.
+  * wide-range h: in every expert, for each aligned block of 32 rows of the
+    gate and up halves, one row (uniform position, the same row in gate and up)
+    gets its UE8M0 exponents raised by `boost`, so that h = SiLU(g) * u has one
+    element per 32 that is about 2^(2 boost) times the others.
 """
 from __future__ import annotations
 
@@ -133,6 +144,37 @@ def _softmax_rows(z: np.ndarray) -> np.ndarray:
     z = z - z.max(axis=1, keepdims=True)
     e = np.exp(z)
     return (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+def wide_range_activations(rng: np.random.Generator, T: int, H: int, mode: str = "outlier",
+                           lo: int = 8, hi: int = 12) -> np.ndarray:
+    """bf16 bits [T][H] with a large dynamic range inside 32-element blocks (see the recipe above)."""
+    x = rng.standard_normal((T, H), dtype=np.float32).reshape(T, H // 32, 32)
+    if mode in ("outlier", "both"):
+        pos = rng.integers(0, 32, size=(T, H // 32, 1))
+        mul = np.exp2(rng.integers(lo, hi + 1, size=(T, H // 32, 1))).astype(np.float32)
+        np.put_along_axis(x, pos, np.take_along_axis(x, pos, -1) * mul, -1)
+    if mode in ("zeros", "both"):
+        zero = rng.random((T, H // 32, 32)) < 0.5
+        big = rng.random((T, H // 32, 1)) < 0.5
+        x = np.where(zero, np.float32(0.0), np.where(big, x * np.float32(1024.0), x))
+    if mode not in ("outlier", "zeros", "both"):
+        raise ValueError(mode)
+    return f32_to_bf16_bits(x.reshape(T, H))
+
+
+def boost_gate_up_rows(rng: np.random.Generator, planes: dict, boost: int = 4) -> dict:
+    """Copy of the planes with one gate row and the matching up row per 32 rows of
+    every expert raised by `boost` in all their UE8M0 exponents (see the recipe above)."""
+    out = {k: v.copy() for k, v in planes.items()}
+    sc = out["w13_scales"]
+    E, two_i, _ = sc.shape
+    I = two_i // 2
+    for e in range(E):
+        rows = rng.integers(0, 32, size=I // 32) + 32 * np.arange(I // 32)
+        sc[e, rows] += np.uint8(boost)
+        sc[e, I + rows] += np.uint8(boost)
+    return out
 
 
 def routing_logits(rng: np.random.Generator, T: int, E: int, k: int):

@@ -21,6 +21,7 @@ OK = 0
 DEV_BAD_EXPERT_ID = 1
 DEV_BAD_SCALE = 2
 DEV_BAD_NVFP4 = 4
+DEV_PIPELINE_TIMEOUT = 0x80000000   # as a uint32; reads back as a negative int32 from a torch int32 tensor
 DECODE_MAX_TOKENS = 64
 PATH_NONE, PATH_DECODE_MMA, PATH_DECODE_BLOCK_SCALED, PATH_PREFILL = 0, 1, 2, 3   # moe_w2_forward_path
 NOALLOC_WORKSPACE_BYTES = 8 << 20   # MOE_W2_NOALLOC_WORKSPACE_BYTES

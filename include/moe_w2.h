@@ -67,6 +67,12 @@ typedef enum {
 #define MOE_W2_DEV_BAD_SCALE 2u       /* UE8M0 byte outside [1,252] in a plane: that block counts as 0 */
 #define MOE_W2_DEV_BAD_NVFP4 4u       /* requant input: e4m3 NaN in a block, or scale_2 not a positive
                                          finite number: the block's codes are 0x00 and its scale byte 0 */
+#define MOE_W2_DEV_PIPELINE_TIMEOUT 0x80000000u
+                                      /* a kernel's internal wait (a pipeline barrier, or a hand-over
+                                         between two phases of the layer) passed its limit of about
+                                         two seconds: the kernel stopped, freed its tensor memory and
+                                         returned, and the outputs of that call are not valid.  Never
+                                         expected; the stream and the context stay usable. */
 
 /* Limits checked on the host. */
 #define MOE_W2_MAX_EXPERTS 1024
@@ -181,13 +187,18 @@ moe_w2_status moe_w2_forward_traced(const void *x_bf16, const int32_t *topk_ids,
  * the library's device code holds it until the process exits.
  *   - Sizes whose moe_w2_forward_workspace_size() exceeds
  *     MOE_W2_NOALLOC_WORKSPACE_BYTES return MOE_W2_ERR_WORKSPACE and enqueue
- *     nothing (at H=6144, I=2048, E=256, top_k=8 that is T > 16).
- *   - The first call on each device looks up the array's address
- *     (cudaGetSymbolAddress, with that device current) and keeps it; make that
- *     first call before any stream capture starts.
+ *     nothing (at H=6144, I=2048, E=256, top_k=8 that is T > 28).
+ *   - The first call in each CUDA context (normally a device's primary
+ *     context) checks the device and looks up the array's address
+ *     (cudaGetSymbolAddress, with that device current), then keeps it for
+ *     that context; make that first call before any stream capture starts.
+ *     cudaDeviceReset destroys the context and the array with it: the next
+ *     call recognises the new context and looks the address up again.
  *   - Every call on a device uses the same array, so calls that may run at
  *     the same time race: order them (e.g. issue them on one stream).
- *   - Nothing in the array needs to start at zero.
+ *   - Nothing in the array needs to start at zero, and a call's results do
+ *     not depend on what earlier calls left in it: they are bitwise identical
+ *     to moe_w2_forward's on the same inputs.
  */
 #define MOE_W2_NOALLOC_WORKSPACE_BYTES (8u << 20)
 moe_w2_status moe_w2_forward_noalloc(const void *x_bf16, const int32_t *topk_ids, const float *topk_weights,

@@ -4,6 +4,7 @@ import torch
 
 REL_L2_TOL = 1e-3        # relative L2 error of the layer output vs the oracle
 MAX_ABS_FRAC_TOL = 1e-2  # max abs error / max |oracle output|
+PARITY_REPORT = []       # (case, rel L2, max abs / max|ref|) of every check, printed by conftest
 
 
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -31,6 +32,7 @@ def assert_close_layer(y_gpu_bits: np.ndarray, y_ref_bits: np.ndarray, what: str
     rel = np.linalg.norm(g - r) / max(denom, 1e-300)
     mx = np.max(np.abs(g - r)) if g.size else 0.0
     lim = MAX_ABS_FRAC_TOL * (np.max(np.abs(r)) if r.size else 0.0)
+    PARITY_REPORT.append((what, float(rel), float(mx / np.max(np.abs(r))) if lim > 0 else 0.0))
     assert rel <= REL_L2_TOL, f"{what}: rel L2 {rel:.3e} > {REL_L2_TOL}"
     assert mx <= lim, f"{what}: max abs {mx:.3e} > {lim:.3e}"
     return rel, mx

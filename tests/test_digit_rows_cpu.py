@@ -18,11 +18,15 @@ the kernel, and pins what the kernel's parity depends on:
   takes a value to within a factor of two of itself);
 - each row shrinks the block's largest leftover at least threefold (the
   largest rounding error at or below 6 is 1, and the scaled maximum exceeds 3);
-- on small layers, five rows keep the layer output within the 1e-3 relative
-  L2 bar against the oracle with room to spare, and the error falls from three
-  rows to six (H = I = 512, 64 tokens, top-2: 4.0e-3, 1.1e-3, 3.0e-4, 4e-6).
-  From seven rows on, x and h are reproduced exactly and what remains is this
-  model's own summation order against the oracle's (one bf16 output flip).
+- on small layers the error falls from three rows to six (H = I = 512, 64
+  tokens, top-2: 4.0e-3, 1.1e-3, 3.0e-4, 4e-6); from seven rows on x and h are
+  reproduced exactly and what remains is this model's own summation order
+  against the oracle's (a bf16 output flip now and then);
+- the rows bound the error relative to the block's largest element, so a block
+  with one large element (2^8..2^12 times the rest) or with exact zeros beside
+  large values needs more rows for its small elements: there five rows leave up
+  to ~8e-4 against the bar of 1e-3 and six ~2.6e-4, while eight (the kernel's
+  count) reproduce them exactly.
 """
 import numpy as np
 import pytest
@@ -94,22 +98,22 @@ def test_rows_reconstruct_exactly_and_shrink_the_leftover_threefold():
     rng = np.random.default_rng(7)
     x = _blocks(rng, 4096)
     amax0 = np.abs(x).max(-1)
-    vals, exps, left = digit_rows(x, 5)
+    vals, exps, left = digit_rows(x, 8)
     # exact reconstruction: the rows plus the leftover give the block back bit for bit
     assert np.array_equal(vals.sum(0) + left, x)
     # every row holds e2m1 values times its power-of-two scale, with a valid UE8M0 byte
-    for r in range(5):
+    for r in range(8):
         s = exps[r] + 127
         assert np.all((s >= 1) & (s <= 253))
         q = vals[r] / np.ldexp(1.0, exps[r].astype(int))[:, None]
         assert np.all(np.isin(np.abs(q), E2M1))
     # each row at least thirds the block's largest leftover
     prev = amax0
-    for r in range(5):
+    for r in range(8):
         rest = np.abs(x - vals[: r + 1].sum(0)).max(-1)
-        assert np.all(rest <= prev / 3.0)
+        assert np.all((rest <= prev / 3.0) | (rest == 0))
         prev = rest
-    assert np.all(prev <= amax0 / 3.0 ** 5)
+    assert np.all(prev <= amax0 / 3.0 ** 8)
 
 
 def test_the_scaled_block_maximum_lies_in_3_to_6():
@@ -149,9 +153,27 @@ def _layer_with_digit_rows(lay, W13, W2, rows: int) -> np.ndarray:
     return bf16_round(y)
 
 
-@pytest.mark.parametrize("case", [(512, 512, 2, 2, 64, 5), (512, 512, 4, 1, 17, 10)])
-def test_five_rows_keep_the_layer_within_the_bar_and_more_rows_help(case):
-    lay = inputs.small_layer_inputs(*case)
+def _wide(lay, kind):
+    """The layer with wide-range activations or h (the GPU parity tests' recipes)."""
+    if kind == "outlier x":
+        x = inputs.wide_range_activations(np.random.default_rng(16), lay.x.shape[0], lay.x.shape[1], "outlier")
+        return inputs.LayerInputs(lay.cfg, x, lay.ids, lay.weights, lay.planes)
+    if kind == "zeros and large x":
+        x = inputs.wide_range_activations(np.random.default_rng(17), lay.x.shape[0], lay.x.shape[1], "both")
+        return inputs.LayerInputs(lay.cfg, x, lay.ids, lay.weights, lay.planes)
+    if kind == "outlier h":
+        planes = inputs.boost_gate_up_rows(np.random.default_rng(18), lay.planes, boost=4)
+        return inputs.LayerInputs(lay.cfg, lay.x, lay.ids, lay.weights, planes)
+    return lay
+
+
+@pytest.mark.parametrize("case,kind,bound", [((512, 512, 2, 2, 64, 5), "normal", 1e-4),
+                                             ((512, 512, 4, 1, 17, 10), "normal", 1e-4),
+                                             ((512, 512, 4, 2, 16, 5), "outlier x", 1e-6),
+                                             ((512, 512, 4, 2, 16, 5), "zeros and large x", 1e-6),
+                                             ((512, 512, 4, 2, 16, 9), "outlier h", 1e-6)])
+def test_eight_rows_keep_the_layer_within_the_bar_and_more_rows_help(case, kind, bound):
+    lay = _wide(inputs.small_layer_inputs(*case), kind)
     ref_bits, st = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes)
     assert st == 0
     ref = (ref_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
@@ -159,8 +181,8 @@ def test_five_rows_keep_the_layer_within_the_bar_and_more_rows_help(case):
     W13 = [_dequant(pl["w13_codes"][e], pl["w13_scales"][e]) for e in range(pl["w13_codes"].shape[0])]
     W2 = [_dequant(pl["w2_codes"][e], pl["w2_scales"][e]) for e in range(pl["w2_codes"].shape[0])]
     rel = {}
-    for rows in (3, 4, 5, 6):
+    for rows in (3, 5, 8):
         y = _layer_with_digit_rows(lay, W13, W2, rows)
         rel[rows] = np.linalg.norm(y - ref) / np.linalg.norm(ref)
-    assert rel[3] > rel[4] > rel[5] > rel[6], rel
-    assert rel[5] <= 5e-4, rel
+    assert rel[3] > rel[5] > rel[8] or rel[8] == 0.0, rel
+    assert rel[8] <= bound, rel

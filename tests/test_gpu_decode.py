@@ -1,8 +1,11 @@
 """GPU parity of the decode path (T <= 64) of moe_w2_forward against the oracle.
 
 Bar: relative L2 <= 1e-3 and max abs <= 1e-2 * max|oracle| on the layer output
-(bf16), over every token for the small and single-token cases and over sampled
-tokens at T = 32; repeated runs must be bitwise identical.
+(bf16), over every token of every case (the full-size T = 32 step through the
+OpenMP build of the oracle); repeated runs must be bitwise identical.  Both
+decode kernels also run activations with a wide dynamic range inside each
+32-element block (one element 2^8..2^12 times the rest, blocks mixing zeros with
+large values) and layers whose h has one large element per 32.
 """
 import numpy as np
 import pytest
@@ -92,16 +95,54 @@ def test_decode_t1_full_size():
     y, st = _run(lay)
     ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes)
     assert st == rst == 0
-    assert_close_layer(y, ref, "decode T=1")
+    assert_close_layer(y, ref, "decode_t1 full size")
 
 
-def test_decode_t32_full_size_sampled(decode_t32):
+def test_decode_t32_full_size_all_tokens(decode_t32):
     lay, pd = decode_t32
     y, st = _run(lay, planes_dev=pd)
-    tokens = np.array([0, 13, 31])
-    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes, tokens=tokens)
+    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes, parallel=True)
     assert st == rst == 0
-    assert_close_layer(y[tokens], ref, "decode T=32")
+    assert_close_layer(y, ref, "decode_t32 full size, all 32 tokens")
+
+
+# Wide in-block dynamic range.  T = 4 top-2 (8 pairs) runs the mma.sync kernel,
+# T = 16 top-2 (32 pairs) the block-scaled one, whose activations enter as e2m1
+# digit rows with one scale per 32 elements.
+@pytest.mark.parametrize("T", [4, 16])
+@pytest.mark.parametrize("mode", ["outlier", "zeros", "both"])
+def test_wide_range_activations(T, mode):
+    lay = inputs.small_layer_inputs(512, 512, 8, 2, T, 40 + T)
+    x = inputs.wide_range_activations(np.random.default_rng(T), T, 512, mode)
+    lay = inputs.LayerInputs(lay.cfg, x, lay.ids, lay.weights, lay.planes)
+    y, st = _run(lay)
+    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes)
+    assert st == rst == 0
+    assert_close_layer(y, ref, f"{moe_w2.decode_kernel(T, 2, 512, 512)} wide-range x ({mode}) T={T}")
+
+
+@pytest.mark.parametrize("T", [4, 16])
+def test_wide_range_h(T):
+    lay = inputs.small_layer_inputs(512, 512, 8, 2, T, 50 + T)
+    planes = inputs.boost_gate_up_rows(np.random.default_rng(T), lay.planes, boost=4)
+    y, st = _run(lay, planes_dev=planes_to_dev(planes))
+    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, planes)
+    assert st == rst == 0
+    assert_close_layer(y, ref, f"{moe_w2.decode_kernel(T, 2, 512, 512)} wide-range h T={T}")
+
+
+@pytest.mark.parametrize("name", ["decode_t1", "decode_t32"])
+def test_full_size_wide_range(name, decode_t32):
+    # the full-size layers with outlier activations and h outliers at once
+    lay = decode_t32[0] if name == "decode_t32" else inputs.layer_inputs(inputs.CONFIGS[name])
+    T = lay.x.shape[0]
+    x = inputs.wide_range_activations(np.random.default_rng(7), T, lay.x.shape[1], "outlier")
+    planes = inputs.boost_gate_up_rows(np.random.default_rng(8), lay.planes, boost=4)
+    lay = inputs.LayerInputs(lay.cfg, x, lay.ids, lay.weights, planes)
+    y, st = _run(lay)
+    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, planes, parallel=True)
+    assert st == rst == 0
+    assert_close_layer(y, ref, f"{name} full size, wide-range x and h, all tokens")
 
 
 def test_decode_deterministic_repeats(decode_t32):

@@ -2,8 +2,10 @@
 
 Bar: relative L2 <= 1e-3 and max abs <= 1e-2 * max|oracle| of the layer output,
 over every token for small shapes (several 256-pair tiles with a ragged tail,
-many 16-pair tiles, duplicate and invalid ids, bad scale bytes) and over
-sampled tokens at T = 8192; repeated runs must be bitwise identical.
+many 16-pair tiles, duplicate and invalid ids, bad scale bytes) and, at
+T = 8192, over more than 256 tokens chosen so that every expert's first and last
+pair (its first and its last, ragged, tile) is checked, through the OpenMP build
+of the oracle; repeated runs must be bitwise identical.
 """
 import numpy as np
 import pytest
@@ -79,13 +81,31 @@ def prefill_full():
     return lay, planes_to_dev(lay.planes)
 
 
-def test_prefill_t8192_full_size_sampled(prefill_full):
+def coverage_tokens(ids: np.ndarray, E: int, extra: int, seed: int) -> np.ndarray:
+    """Tokens holding the first and the last pair (in expert-grouped order) of
+    every expert, plus `extra` more drawn at random, sorted and unique."""
+    T, k = ids.shape
+    flat = ids.reshape(-1)
+    chosen = set()
+    for e in range(E):
+        pairs = np.nonzero(flat == e)[0]          # increasing pair index = grouped order
+        if pairs.size:
+            chosen.update((int(pairs[0]) // k, int(pairs[-1]) // k))
+    rng = np.random.default_rng(seed)
+    chosen.update(int(t) for t in rng.choice(T, size=extra, replace=False))
+    return np.array(sorted(chosen), dtype=np.int64)
+
+
+def test_prefill_t8192_full_size_covering_every_expert(prefill_full):
     lay, pd = prefill_full
     y, st = _run(lay, planes_dev=pd)
-    tokens = np.array([0, 4095, 8191])
-    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes, tokens=tokens)
+    E = lay.cfg.num_experts
+    tokens = coverage_tokens(lay.ids, E, extra=160, seed=3)
+    hit = np.unique(lay.ids[tokens])
+    assert len(tokens) >= 256 and np.array_equal(hit, np.arange(E))
+    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes, tokens=tokens, parallel=True)
     assert st == rst == 0
-    assert_close_layer(y[tokens], ref, "prefill T=8192")
+    assert_close_layer(y[tokens], ref, f"prefill_t8192 full size, {len(tokens)} tokens covering all experts")
 
 
 def test_prefill_deterministic_repeats(prefill_full):

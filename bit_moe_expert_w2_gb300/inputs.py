@@ -33,6 +33,9 @@ Recipe (all numpy PCG64 via ``default_rng(seed)``):
   * NVFP4 tensors: e2m1 nibbles uniform over all 16 codes (uniform random bytes,
     low nibble = even element), e4m3 block-16 scales 2^U(-6, 2) rounded to the
     nearest e4m3fn value (ties to even mantissa), scale_2 = 2^-8 per tensor.
+  * FP8 block-quantised tensors (the fp8 loader's input): e4m3fn bytes uniform
+    over the 254 non-NaN codes, one f32 scale per 128 x 128 block drawn
+    log-uniform, 2^U(-14, -8), rounded to f32 (a general mantissa).
   * wide-range activations (parity cases for activations with a large dynamic
     range inside a 32-element block, as real LLM activations have):
     "outlier": standard normal, then in every aligned block of 32 one element
@@ -100,6 +103,8 @@ REQUANT = RequantConfig("requant_256", 256, 2048, 6144, 4)
 # is the first 16 experts of the same draw (each expert has its own child seed): the
 # same per-block kernel work on 1/16 of the data, for multi-pass profiler captures.
 REQUANT_CASES = {"requant_256": None, "requant_16": 16}
+# FP8 block-128 loader workloads: experts of gate/up [I][H] x 2 and down [H][I]
+REQUANT_FP8_CASES = {"requant_fp8_16": 16}
 
 
 def rng_for(seed: int) -> np.random.Generator:
@@ -296,3 +301,32 @@ def requant_inputs(cfg: RequantConfig = REQUANT, experts: int | None = None):
                       np.concatenate([t.e4m3 for t in dn_list]),
                       np.concatenate([t.scale_2 for t in dn_list]))
     return gu, dn
+
+
+# --------------------------------------------------------------------------- FP8
+
+@dataclasses.dataclass
+class Fp8Tensors:
+    w8: np.ndarray        # uint8 e4m3fn bytes [n][rows][K]
+    scales: np.ndarray    # float32 [n][ceil(rows/128)][ceil(K/128)]
+
+
+def fp8_tensors(rng: np.random.Generator, n: int, rows: int, K: int) -> Fp8Tensors:
+    b = random_bytes(rng, (n, rows, K))
+    nan = (b & 0x7F) == 0x7F
+    b[nan] = rng.integers(0, 0x7F, size=int(nan.sum()), dtype=np.uint8) | (b[nan] & 0x80)   # no NaN codes
+    sc = np.exp2(rng.uniform(-14.0, -8.0, size=(n, (rows + 127) // 128, (K + 127) // 128))).astype(np.float32)
+    return Fp8Tensors(b, sc)
+
+
+def requant_fp8_inputs(cfg: RequantConfig = REQUANT, experts: int = 16):
+    """The FP8 loader workload: (gate/up tensors, down tensors) of the first `experts`
+    experts, laid out as requant_inputs lays out the NVFP4 ones (a child seed each)."""
+    seeds = np.random.SeedSequence(cfg.seed + 100).spawn(cfg.num_experts)
+    gu, dn = [], []
+    for e in range(experts):
+        rng = np.random.default_rng(seeds[e])
+        gu.append(fp8_tensors(rng, 2, cfg.inter, cfg.hidden))
+        dn.append(fp8_tensors(rng, 1, cfg.hidden, cfg.inter))
+    cat = lambda ts: Fp8Tensors(np.concatenate([t.w8 for t in ts]), np.concatenate([t.scales for t in ts]))
+    return cat(gu), cat(dn)

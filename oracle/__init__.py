@@ -72,6 +72,8 @@ def lib(parallel: bool = False):
             L.oracle_requant.restype = u32
             L.oracle_requant_blocks.argtypes = [vp, vp, vp, i64, i64, vp, i64, vp, vp]
             L.oracle_requant_blocks.restype = u32
+            L.oracle_requant_fp8.argtypes = [vp, vp, i64, i64, i64, vp, vp]
+            L.oracle_requant_fp8.restype = u32
             L.oracle_permute.argtypes = [vp, i64, i32, i32, vp, vp, vp]
             L.oracle_permute.restype = u32
             L.oracle_forward_tokens.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -130,6 +132,18 @@ def requant_blocks(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray, bloc
     st = lib(parallel).oracle_requant_blocks(_p(np.ascontiguousarray(e2m1)), _p(np.ascontiguousarray(e4m3)),
                                      _p(s2), rows, K, _p(ids), len(ids), _p(codes), _p(scales))
     return codes, scales, int(st)
+
+
+def requant_fp8(w8: np.ndarray, scales: np.ndarray, parallel: bool = False):
+    """w8 uint8 (e4m3fn bytes) [n][rows][K], scales float32 [n][ceil(rows/128)][ceil(K/128)]."""
+    n, rows, K = w8.shape
+    w8 = np.ascontiguousarray(w8)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    assert sc.shape == (n, (rows + 127) // 128, (K + 127) // 128)
+    codes = np.empty((n, rows, K // 4), np.uint8)
+    ue8m0 = np.empty((n, rows, K // 32), np.uint8)
+    st = lib(parallel).oracle_requant_fp8(_p(w8), _p(sc), n, rows, K, _p(codes), _p(ue8m0))
+    return codes, ue8m0, int(st)
 
 
 def permute(ids: np.ndarray, E: int):

@@ -140,25 +140,16 @@ uint16_t oracle_bf16_from_double(double v)
 
 /* ------------------------------------------------------------------ requant */
 
-/* One block of 32 NVFP4 elements -> 8 code bytes and one UE8M0 byte. */
-static uint32_t requant_block(const uint8_t *nib_bytes, const uint8_t *e4m3_pair, float scale_2,
-                              uint8_t *codes_out, uint8_t *scale_out)
+/* Re-quantisation of one block of 32 exact values (each an f64 with at most 53
+ * significant bits, here at most 30) -> 8 code bytes and one UE8M0 byte, by
+ * readings R3 and R4.  Shared by the NVFP4 and FP8 loaders, which differ only
+ * in how they dequantise. */
+static void search_block(const double *x, uint8_t *codes_out, uint8_t *scale_out)
 {
-    double s2 = (double)scale_2;
-    double sc[2] = {oracle_e4m3_value(e4m3_pair[0]), oracle_e4m3_value(e4m3_pair[1])};
-    if (!(s2 > 0.0) || isinf(s2) || isnan(sc[0]) || isnan(sc[1])) {
-        memset(codes_out, 0, 8);
-        *scale_out = 0;
-        return ORACLE_BAD_NVFP4;
-    }
-
-    /* Exact f64 dequantisation: each product has at most 2+4+24 significant bits. */
-    double x[32], a[32];
+    double a[32];
     int neg[32];
     double amax = 0.0, min_nz = INFINITY;
     for (int i = 0; i < 32; ++i) {
-        unsigned nib = (nib_bytes[i / 2] >> (4 * (i % 2))) & 0xFu;
-        x[i] = oracle_e2m1_value(nib) * sc[i / 16] * s2;
         neg[i] = signbit(x[i]) ? 1 : 0;
         a[i] = fabs(x[i]);
         if (a[i] > amax) amax = a[i];
@@ -235,6 +226,50 @@ static uint32_t requant_block(const uint8_t *nib_bytes, const uint8_t *e4m3_pair
         codes_out[i / 4] |= (uint8_t)(code << (2 * (i % 4)));
     }
     *scale_out = (uint8_t)(u + 127);
+}
+
+/* One block of 32 NVFP4 elements -> 8 code bytes and one UE8M0 byte. */
+static uint32_t requant_block(const uint8_t *nib_bytes, const uint8_t *e4m3_pair, float scale_2,
+                              uint8_t *codes_out, uint8_t *scale_out)
+{
+    double s2 = (double)scale_2;
+    double sc[2] = {oracle_e4m3_value(e4m3_pair[0]), oracle_e4m3_value(e4m3_pair[1])};
+    if (!(s2 > 0.0) || isinf(s2) || isnan(sc[0]) || isnan(sc[1])) {
+        memset(codes_out, 0, 8);
+        *scale_out = 0;
+        return ORACLE_BAD_NVFP4;
+    }
+    /* Exact f64 dequantisation: each product has at most 2+4+24 significant bits. */
+    double x[32];
+    for (int i = 0; i < 32; ++i) {
+        unsigned nib = (nib_bytes[i / 2] >> (4 * (i % 2))) & 0xFu;
+        x[i] = oracle_e2m1_value(nib) * sc[i / 16] * s2;
+    }
+    search_block(x, codes_out, scale_out);
+    return 0;
+}
+
+/* One block of 32 FP8 elements (e4m3fn bytes) under one f32 block scale -> 8
+ * code bytes and one UE8M0 byte.  An e4m3 NaN in the block, or a scale that is
+ * not a positive finite number, makes the block invalid (codes 0x00, scale
+ * byte 0, status bit 4), as for NVFP4. */
+static uint32_t requant_block_fp8(const uint8_t *e4m3_bytes, float scale, uint8_t *codes_out, uint8_t *scale_out)
+{
+    double s = (double)scale;
+    int bad = !(s > 0.0) || isinf(s);
+    double x[32];
+    for (int i = 0; i < 32 && !bad; ++i) {
+        double v = oracle_e4m3_value(e4m3_bytes[i]);
+        if (isnan(v)) bad = 1;
+        /* exact: at most 4 + 24 significant bits */
+        x[i] = v * s;
+    }
+    if (bad) {
+        memset(codes_out, 0, 8);
+        *scale_out = 0;
+        return ORACLE_BAD_NVFP4;
+    }
+    search_block(x, codes_out, scale_out);
     return 0;
 }
 
@@ -265,6 +300,24 @@ uint32_t oracle_requant_blocks(const uint8_t *e2m1, const uint8_t *e4m3, const f
         int64_t g = block_ids[i];
         st |= requant_block(e2m1 + g * 16, e4m3 + g * 2, scale_2[g / blocks_per_tensor],
                             codes + i * 8, ue8m0 + i);
+    }
+    return st;
+}
+
+/* FP8 block-quantised tensors: e4m3 bytes [n][rows][K] with one f32 scale per
+ * 128 x 128 block, scales [n][ceil(rows/128)][ceil(K/128)] -> codes
+ * [n][rows][K/4], ue8m0 [n][rows][K/32].  Returns status bits. */
+uint32_t oracle_requant_fp8(const uint8_t *w8, const float *scales, int64_t n, int64_t rows, int64_t K,
+                            uint8_t *codes, uint8_t *ue8m0)
+{
+    if (K % 32 != 0) return 0x80000000u;
+    uint32_t st = 0;
+    int64_t bpr = K / 32, srows = (rows + 127) / 128, scols = (K + 127) / 128;
+    ORACLE_PARALLEL_FOR_BLOCKS
+    for (int64_t g = 0; g < n * rows * bpr; ++g) {
+        int64_t t = g / (rows * bpr), r = (g / bpr) % rows, b = g % bpr;
+        float s = scales[(t * srows + r / 128) * scols + (b * 32) / 128];
+        st |= requant_block_fp8(w8 + g * 32, s, codes + g * 8, ue8m0 + g);
     }
     return st;
 }

@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY.  Independent of ``oracle.c``: it follows the plain
 definition with no candidate window and no integer tricks.
 
 Definition followed (page "The v0.24.0 port", section "Our hooks", modelopt.py
-bullet; page "vLLM-Moet wiki", section "2-bit expert planes"): each NVFP4
-element is e2m1 x e4m3 x scale_2, an exact rational number; a block of 32 is
+and fp8.py bullets; page "vLLM-Moet wiki", section "2-bit expert planes"): each
+NVFP4 element is e2m1 x e4m3 x scale_2 and each FP8 element e4m3 x its f32
+128 x 128 block scale, an exact rational number; a block of 32 is
 re-quantized to codes from {-4,-1,1,4} times one UE8M0 scale 2^u, u in
 [-126,125], minimising the squared error.  With the scale fixed the error
 separates per element, so for every u each element takes its nearest code;
@@ -56,6 +57,11 @@ def requant_block(nibbles, e4m3_pair, scale_2: float):
         s_neg, s_mag = sc[i // 16]
         neg.append(n_neg != s_neg)
         mag.append(n_mag * s_mag * s2)
+    return _search(neg, mag)
+
+
+def _search(neg, mag):
+    """(codes[32], scale byte) minimising the exact squared error over all u."""
     best = None
     for u in range(-126, 126):
         step = Fraction(2) ** u
@@ -69,6 +75,17 @@ def requant_block(nibbles, e4m3_pair, scale_2: float):
     step = Fraction(2) ** u
     codes = [(int(n) << 1) | (1 if a > Fraction(5, 2) * step else 0) for n, a in zip(neg, mag)]
     return codes, u + 127
+
+
+def requant_block_fp8(e4m3_bytes, scale: float):
+    """32 e4m3fn bytes under one f32 block scale -> (codes[32], scale byte), or None when invalid."""
+    if not (scale > 0) or scale == float("inf"):
+        return None
+    vals = [e4m3(b) for b in e4m3_bytes]
+    if any(v is None for v in vals):
+        return None
+    s = f32(scale)
+    return _search([n for n, _ in vals], [m * s for _, m in vals])
 
 
 def nearest_codes_by_enumeration(values, u: int):

@@ -2,6 +2,7 @@
 // The entry points only enqueue work on the caller's stream; nothing here
 // allocates, frees or synchronises.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -11,10 +12,11 @@ namespace moe_w2 {
 namespace {
 
 constexpr int32_t kPrefillTileRows = 256;   // pairs per prefill tile (tcgen05 N <= 256)
-constexpr int32_t kDecodeTileRows = 2;      // pairs per decode tile (MMA N = 16: kActDigits rows per pair)
+constexpr int32_t kDecodeTileRows = 4;      // pairs per decode tile (MMA N = 32: kActDigits rows per pair)
 constexpr int32_t kDecodeMmaTileRows = 16;  // pairs per tile of the mma.sync decode kernel
 constexpr int64_t kDecodeMmaMaxPairs = 16;  // steps with at most this many pairs take the mma.sync kernel
 constexpr int64_t kDecodeTargetItems = 1200; // down items per step that keep every CTA busy
+constexpr int64_t kDecodeSplitMaxPairs = 32;  // steps of up to this many pairs may split gate_up K in two
 constexpr int32_t kDecodeMinSegChunks = 2;   // at least 2 chunks of 256 K per decode item
 constexpr int64_t kDecodeMaxSegments = 16;   // K segments per row block
 
@@ -47,6 +49,14 @@ moe_w2_status check_device()
         g_cc_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
     }
     return g_cc_ok[dev] == 1 ? MOE_W2_OK : MOE_W2_ERR_DEVICE;
+}
+
+std::atomic<int> g_force_timeout{0};
+
+DepWait dependency_wait()
+{
+    if (g_force_timeout.load(std::memory_order_relaxed)) return DepWait{1, 200000ll};
+    return DepWait{0, 4000000000ll};
 }
 
 std::mutex& init_mutex()
@@ -97,8 +107,9 @@ bool decode_use_mma(int64_t P, int32_t H, int32_t I)
 int64_t decode_counter_count(int64_t P, int32_t E, int32_t H, int32_t I)
 {
     if (decode_use_mma(P, H, I)) return H / 32 + max_tiles(P, E, true) + 1;   // row blocks of y, tiles, queue
+    // h publications and split-K arrivals per (tile, 64-row block), then the queue
     const int64_t mt = max_tiles(P, E, true);
-    return mt * (I / 64) + 1;
+    return 2 * mt * (I / 64) + 1;
 }
 
 Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I)
@@ -133,6 +144,8 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
         w.hd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * P * (I / 2)));
         w.shd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * P * (I / 32)));
         w.stage = reinterpret_cast<float*>(take(sizeof(float) * w.split.s_dn * P * H));
+        if (P <= kDecodeSplitMaxPairs)
+            w.gu_part = reinterpret_cast<float*>(take(sizeof(float) * 2 * P * 2 * I));
     } else {
         w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * H));
         w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
@@ -149,6 +162,12 @@ using namespace moe_w2;
 extern "C" {
 
 int moe_w2_version(void) { return (0 << 16) | 1; }
+
+moe_w2_status moe_w2_debug_force_pipeline_timeout(int32_t enable)
+{
+    g_force_timeout.store(enable != 0 ? 1 : 0, std::memory_order_relaxed);
+    return MOE_W2_OK;
+}
 
 const char* moe_w2_status_string(moe_w2_status s)
 {

@@ -252,6 +252,7 @@ struct Workspace {
     uint8_t* sxd;          // their UE8M0 bytes [8T][H/32]
     uint8_t* hd;           // e2m1 digit rows of h, kActDigits per pair (expert order) [8P][I/2]
     uint8_t* shd;          // their UE8M0 bytes [8P][I/32]
+    float* gu_part;        // gate_up partial sums of the two K halves [2][P][2I] (small steps only, else null)
     DecodeSplit split;
     size_t bytes;
 };
@@ -298,6 +299,16 @@ cudaError_t launch_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float
                            cudaStream_t s);
 
 int sm_count();
+
+// The cross-CTA dependency waits of the decode kernels (a down item waiting for
+// the h it reads): normally a target reached by the gate_up epilogues and a limit
+// of about two seconds; with the debug hook on (moe_w2_debug_force_pipeline_timeout)
+// an unreachable target and a limit of about 0.1 ms, so that the wait times out.
+struct DepWait {
+    int32_t bias;          // added to the target
+    long long limit;       // clock cycles
+};
+DepWait dependency_wait();
 // MOE_W2_OK when the current device has compute capability 10.3, else
 // MOE_W2_ERR_DEVICE (MOE_W2_ERR_CUDA if the query fails); cached per device.
 moe_w2_status check_device();

@@ -81,6 +81,7 @@ struct DecArgs {
     int32_t* counters;         // down: per 32-row block of y
     uint16_t* y;
     uint32_t* status;
+    DepWait dep;               // down items' wait for their tile's h: target bias and limit
 };
 
 struct SharedState {
@@ -334,10 +335,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_const
             const int id = is_gu ? it : it - n_gu;
             const int ti = id / P.row_blocks, rb = id % P.row_blocks;
             const int4 tile = P.tiles[ti];
-            if (!is_gu && lane == 0 && (int)ld_acquire(gu_done + ti) < gu.row_blocks) {
+            const int gu_target = gu.row_blocks + gu.dep.bias;
+            if (!is_gu && lane == 0 && (int)ld_acquire(gu_done + ti) < gu_target) {
                 const long long t0 = clock64();
-                while ((int)ld_acquire(gu_done + ti) < gu.row_blocks) {
-                    if (clock64() - t0 > kWaitLimitCycles) {
+                while ((int)ld_acquire(gu_done + ti) < gu_target) {
+                    if (clock64() - t0 > gu.dep.limit) {
                         *abort = 1;
                         break;
                     }
@@ -496,6 +498,7 @@ cudaError_t launch_decode_mma(const uint16_t* x, const int32_t* ids, const float
     gp.counters = ws.counters;
     gp.y = y;
     gp.status = status;
+    gp.dep = dependency_wait();
 
     DecArgs dp = gp;
     dp.codes = w.w2_codes;

@@ -83,6 +83,8 @@ def load(build_if_missing: bool = True):
     L.moe_w2_forward_noalloc.restype = ctypes.c_int
     L.moe_w2_requant.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
     L.moe_w2_requant.restype = ctypes.c_int
+    L.moe_w2_debug_force_pipeline_timeout.argtypes = [i32]
+    L.moe_w2_debug_force_pipeline_timeout.restype = ctypes.c_int
     _lib = L
     return L
 

@@ -224,6 +224,19 @@ moe_w2_status moe_w2_requant(const uint8_t *e2m1, const uint8_t *e4m3, const flo
                              int64_t n, int64_t rows, int64_t K, uint8_t *codes, uint8_t *ue8m0,
                              uint32_t *dev_status, void *stream);
 
+/*
+ * Test hook for the pipeline-timeout report; the pages describe no such entry
+ * point.  With enable != 0, every later moe_w2_forward call in this process
+ * (any thread, any device) that runs a decode kernel makes that kernel's
+ * cross-CTA dependency wait (a down item waiting for the h it reads)
+ * unsatisfiable with a limit of about 0.1 ms: the wait gives up, the kernel
+ * stops, frees its tensor memory and returns with MOE_W2_DEV_PIPELINE_TIMEOUT
+ * set in *dev_status, and y is not valid.  Nothing faults or hangs, and the
+ * stream and context stay usable.  enable = 0 (the default) restores normal
+ * operation for the calls that follow.  Always returns MOE_W2_OK.
+ */
+moe_w2_status moe_w2_debug_force_pipeline_timeout(int32_t enable);
+
 /* Human-readable name of a status code (static string). */
 const char *moe_w2_status_string(moe_w2_status s);
 

@@ -457,6 +457,27 @@ def layer_bench(cfg: inputs.LayerConfig, steps, warmup, world, rank, local):
 
     pk = peaks()
     plane_bytes = sum(distinct[i] * (w13_b + w2_b) for i, _ in per_step)
+    if decode:
+        # context for the roofline: a plain read of the same number of bytes (a torch
+        # reduction over a buffer of one step's mean plane bytes), L2 flushed and
+        # timed by events around the one launch like the step; at a few tens of MB
+        # the launch and the ramp of the memory system alone keep it well below peak
+        nb = int(plane_bytes / steps) // 64 * 64
+        rbuf = torch.ones(nb // 8, dtype=torch.int64, device=dev)
+        racc = torch.empty((), dtype=torch.int64, device=dev)
+        r_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in r_ev:
+                flush.zero_()
+                e0.record(stream)
+                torch.sum(rbuf, dim=0, out=racc)
+                e1.record(stream)
+        stream.synchronize()
+        r_us = sorted(a.elapsed_time(b) for a, b in r_ev[3:])[len(r_ev[3:]) // 2] * 1e3
+        same_size_read = {"bytes": nb, "us": round(r_us, 2), "gbs": round(nb / r_us / 1e3, 1),
+                          "frac": round(nb / r_us / 1e3 / pk["hbm_gbs"], 4),
+                          "how": "torch.sum over an int64 buffer of the step's plane bytes, L2 flushed, median of 17"}
+        del rbuf
     res = {"ms_per_step": steps_ms / K, "ms_per_step_traced": traced_ms / K}
     if decode:
         # one kernel streams the w13 and w2 planes of every active expert; its
@@ -468,7 +489,9 @@ def layer_bench(cfg: inputs.LayerConfig, steps, warmup, world, rank, local):
         res["roofline"] = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
                            "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                            "peak_source": pk["source"],
-                           "traffic": ncu_traffic(kname, cfg.name)}
+                           "traffic": ncu_traffic(kname, cfg.name),
+                           "algorithmic_bytes_per_step": int(plane_bytes / steps),
+                           "same_size_read": same_size_read}
         res["plane_gbs_step"] = round(plane_bytes / (steps_ms / 1e3) / 1e9, 1)
         res["plane_frac_step"] = round(plane_bytes / (steps_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)
     else:

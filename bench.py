@@ -51,10 +51,10 @@ from bit_moe_expert_w2_gb300 import inputs  # noqa: E402
 
 METRIC = "w2 MoE layer tokens/s; plane HBM GB/s (decode), TFLOP/s (prefill) vs peak"
 DEFAULT_CONFIG = "decode_t1"
-EXTRA_CONFIGS = ("decode_t32", "prefill_t8192", "requant_256")
+EXTRA_CONFIGS = ("decode_t32", "prefill_t8192", "requant_256", "requant_fp8_16")
 DEFAULT_STEPS = {"decode_t1": 4000, "decode_t32": 1000, "prefill_t8192": 100, "requant_256": 10,
                  "decode_t1_e32": 4000, "prefill_t1024_e32": 400}
-EXTRA_STEPS = {"decode_t32": 500, "prefill_t8192": 50, "requant_256": 5}
+EXTRA_STEPS = {"decode_t32": 500, "prefill_t8192": 50, "requant_256": 5, "requant_fp8_16": 5}
 POOL = 16
 # every file each kernel's translation unit compiles: a capture is stale once any changed
 KERNEL_SOURCES = {
@@ -62,6 +62,7 @@ KERNEL_SOURCES = {
     "decode_mma_kernel": ["bit_moe_expert_w2_gb300/csrc/decode_mma.cu"],
     "prefill_gate_up_kernel": ["bit_moe_expert_w2_gb300/csrc/prefill.cu"],
     "requant_kernel": ["bit_moe_expert_w2_gb300/csrc/requant.cu"],
+    "requant_fp8_kernel": ["bit_moe_expert_w2_gb300/csrc/requant.cu"],
 }
 COMMON_SOURCES = ["bit_moe_expert_w2_gb300/csrc/common.cuh", "bit_moe_expert_w2_gb300/csrc/tc.cuh", "include/moe_w2.h"]
 
@@ -270,6 +271,22 @@ def oracle_requant_rate_all_cores(gu: inputs.Nvfp4Tensors, budget_s: float):
         oracle.requant(gu.e2m1[sl], gu.e4m3[sl], gu.scale_2[sl], parallel=True)
         done_el += gu.e2m1[sl].size * 2
         i += 2
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done_el / el, i, el, threads
+
+
+def oracle_requant_fp8_rate(gu: inputs.Fp8Tensors, budget_s: float, parallel: bool = False):
+    """Elements/s of the oracle FP8 requant on whole tensors in turn (single thread, or all threads)."""
+    import oracle
+    threads = oracle.threads(parallel=True) if parallel else 1
+    done_el, t0, i = 0, time.perf_counter(), 0
+    n = gu.w8.shape[0]
+    while True:
+        sl = slice(i % n, i % n + 1)
+        oracle.requant_fp8(gu.w8[sl], gu.scales[sl], parallel=parallel)
+        done_el += gu.w8[sl].size
+        i += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             return done_el / el, i, el, threads
@@ -656,8 +673,93 @@ def requant_bench(name, steps, warmup, world, rank, local):
     return res, gu
 
 
+def requant_fp8_bench(name, steps, warmup, world, rank, local):
+    import torch
+    from bit_moe_expert_w2_gb300 import moe_w2
+    dev = torch.device("cuda", local)
+    gu, dn = inputs.requant_fp8_inputs(experts=inputs.REQUANT_FP8_CASES[name])
+    dt = [(torch.from_numpy(t.w8).to(dev), torch.from_numpy(t.scales).to(dev)) for t in (gu, dn)]
+    outs = [(torch.empty((t.w8.shape[0], t.w8.shape[1], t.w8.shape[2] // 4), dtype=torch.uint8, device=dev),
+             torch.empty((t.w8.shape[0], t.w8.shape[1], t.w8.shape[2] // 32), dtype=torch.uint8, device=dev))
+            for t in (gu, dn)]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for (w8, sc), (c, u) in zip(dt, outs):
+            moe_w2.requant_fp8(w8, sc, codes=c, ue8m0=u, status=status, stream=stream)
+
+    clk = ClockSampler(ClockSampler.device_id_of(dev)).start()
+    clk.wait_first()
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            step()
+    stream.synchronize()
+    warm0 = time.time()
+    while clk.count_since(warm0) < 10 and time.time() - warm0 < 5.0:
+        with torch.cuda.stream(stream):
+            step()
+        stream.synchronize()
+    barrier(world)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t_timed0 = time.time()
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+    stream.synchronize()
+    t_timed1 = time.time()
+    clk.stop()
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world)
+    elems = gu.w8.size + dn.w8.size
+    moved = elems + 4 * (gu.scales.size + dn.scales.size) + elems // 4 + elems // 32
+    pk = peaks()
+    gbs = moved * steps / (ms / 1e3) / 1e9
+    res = {"ms_per_step": ms / steps, "value": world * elems * steps / (ms / 1e3), "unit": "elements/s",
+           "roofline": {"kernel": "requant_fp8_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                        "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                        "peak_source": pk["source"], "traffic": ncu_traffic("requant_fp8_kernel", name),
+                        "algorithmic_bytes_per_step": int(moved)},
+           "clocks": clk.summary(t_timed0, t_timed1, warm0), "gpu_launches": 2 * steps, "dtype": "int64 (exact)"}
+    # end to end: FP8 tensors from pinned host memory, requant, planes back to pinned host memory
+    hin = [(torch.from_numpy(t.w8).pin_memory(), torch.from_numpy(t.scales).pin_memory()) for t in (gu, dn)]
+    hout = [(torch.empty(c.shape, dtype=torch.uint8).pin_memory(), torch.empty(u.shape, dtype=torch.uint8).pin_memory())
+            for c, u in outs]
+    e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in e_evs:
+            flush.zero_()
+            e0.record(stream)
+            for (w8, sc), (hw, hs) in zip(dt, hin):
+                w8.copy_(hw, non_blocking=True)
+                sc.copy_(hs, non_blocking=True)
+            step()
+            for (c, u), (hc, hu) in zip(outs, hout):
+                hc.copy_(c, non_blocking=True)
+                hu.copy_(u, non_blocking=True)
+            e1.record(stream)
+    stream.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e_evs), world)
+    res["e2e"] = {"value": round(world * elems * steps / (e2e_ms / 1e3), 2), "unit": "elements/s",
+                  "h2d_bytes_per_step": int(sum(a.nbytes + b.nbytes for a, b in hin)),
+                  "d2h_bytes_per_step": int(sum(a.nbytes + b.nbytes for a, b in hout))}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during the FP8 requant benchmark")
+    return res, gu
+
+
 def cpu_baseline(name, data, budget_s):
     """The oracle on this host: one core (the reported value) and all cores."""
+    if name in inputs.REQUANT_FP8_CASES:
+        v, n, el, _ = oracle_requant_fp8_rate(data, budget_s)
+        va, na, ela, thr = oracle_requant_fp8_rate(data, budget_s / 2, parallel=True)
+        return {"value": round(v, 1), "unit": "elements/s", "cores": 1, "kind": "oracle",
+                "sample": f"{n} whole tensors of {name} in {el:.1f} s",
+                "all_cores": {"value": round(va, 1), "cores": thr,
+                              "sample": f"{na} whole tensors in {ela:.1f} s (OpenMP build)"}}
     if name in inputs.REQUANT_CASES:
         v, n, el = oracle_requant_rate(data, budget_s)
         va, na, ela, thr = oracle_requant_rate_all_cores(data, budget_s / 2)
@@ -675,6 +777,8 @@ def cpu_baseline(name, data, budget_s):
 
 def run_config(name, steps, warmup, world, rank, local):
     """(result dict, oracle input) of one workload."""
+    if name in inputs.REQUANT_FP8_CASES:
+        return requant_fp8_bench(name, steps, warmup, world, rank, local)
     if name in inputs.REQUANT_CASES:
         res, data = requant_bench(name, steps, warmup, world, rank, local)
         res["unit"] = "elements/s"
@@ -689,7 +793,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default=None, choices=[*inputs.CONFIGS, *inputs.REQUANT_CASES],
+    ap.add_argument("--config", default=None,
+                    choices=[*inputs.CONFIGS, *inputs.REQUANT_CASES, *inputs.REQUANT_FP8_CASES],
                     help=f"one workload only (default: {DEFAULT_CONFIG}, plus {', '.join(EXTRA_CONFIGS)} on one GPU)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of single-core oracle work per workload")
@@ -741,6 +846,11 @@ def main():
 
 def workload_name(config: str) -> str:
     """The workload string of a config, the same on both arms."""
+    if config in inputs.REQUANT_FP8_CASES:
+        r = inputs.REQUANT
+        n = inputs.REQUANT_FP8_CASES[config]
+        return (f"{config}: {n} experts FP8 (e4m3, f32 128x128 block scales) gate/up 2x[{r.inter}x{r.hidden}] + "
+                f"down [{r.hidden}x{r.inter}] -> 2-bit planes")
     if config in inputs.REQUANT_CASES:
         r = inputs.REQUANT
         n = inputs.REQUANT_CASES[config] or r.num_experts
@@ -754,7 +864,12 @@ def workload_name(config: str) -> str:
 def reference_arm(args, cores):
     """The oracle timed on this host's cores on a bounded sample of the workload."""
     budget = 90.0
-    if args.config in inputs.REQUANT_CASES:
+    if args.config in inputs.REQUANT_FP8_CASES:
+        gu, _ = inputs.requant_fp8_inputs(experts=2)
+        v, n, el, _ = oracle_requant_fp8_rate(gu, budget / 3)
+        unit, sample = "elements/s", f"{n} whole tensors of {args.config} in {el:.1f} s"
+        steps = n
+    elif args.config in inputs.REQUANT_CASES:
         gu, _ = inputs.requant_inputs(experts=4)
         v, n, el = oracle_requant_rate(gu, budget / 3)
         unit, sample = "elements/s", f"{n} whole gate/up tensors of {args.config} in {el:.1f} s"

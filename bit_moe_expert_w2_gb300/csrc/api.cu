@@ -290,4 +290,22 @@ moe_w2_status moe_w2_requant(const uint8_t* e2m1, const uint8_t* e4m3, const flo
     return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
 }
 
+moe_w2_status moe_w2_requant_fp8(const uint8_t* w8, const float* scales, int64_t n, int64_t rows, int64_t K,
+                                 uint8_t* codes, uint8_t* ue8m0, uint32_t* dev_status, void* stream)
+{
+    if (n < 0 || rows < 0 || K < 0) return MOE_W2_ERR_INVALID_ARG;
+    if (K % 32 != 0) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
+    if (n == 0 || rows == 0 || K == 0) return MOE_W2_OK;
+    if (rows > ((int64_t)1 << 40) / K || n > ((int64_t)1 << 50) / (rows * K)) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
+    if (!w8 || !scales || !codes || !ue8m0) return MOE_W2_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(w8) & 15) != 0 || (reinterpret_cast<uintptr_t>(codes) & 7) != 0 ||
+        (reinterpret_cast<uintptr_t>(scales) & 3) != 0)
+        return MOE_W2_ERR_INVALID_ARG;
+    moe_w2_status st = check_device();
+    if (st != MOE_W2_OK) return st;
+    cudaError_t e = launch_requant_fp8(w8, scales, n, rows, K, codes, ue8m0, dev_status,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -298,6 +298,9 @@ cudaError_t launch_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float
                            int64_t rows, int64_t K, uint8_t* codes, uint8_t* ue8m0, uint32_t* status,
                            cudaStream_t s);
 
+cudaError_t launch_requant_fp8(const uint8_t* w8, const float* scales, int64_t n, int64_t rows, int64_t K,
+                               uint8_t* codes, uint8_t* ue8m0, uint32_t* status, cudaStream_t s);
+
 int sm_count();
 
 // The cross-CTA dependency waits of the decode kernels (a down item waiting for

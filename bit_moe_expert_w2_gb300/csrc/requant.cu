@@ -285,6 +285,110 @@ __global__ void __launch_bounds__(256) requant_kernel(const uint8_t* __restrict_
 
 }  // namespace
 
+// ------------------------------------------------------------------ FP8 block-128
+//
+// vLLM-Moet, page "The v0.24.0 port", section "Our hooks", fp8.py bullet: the FP8
+// block-quant loader re-quantizes fp8 weights with f32 block-128 scales to the
+// same codebook in float64.  Element x_i = e4m3_i * S, S the f32 scale of the
+// 128 x 128 block holding it; all 32 elements of an output block share S.
+//
+// Exact integer form: e4m3 magnitude = A_i * 2^-9 with A_i an integer below 2^18
+// (subnormals m, normals (8 + m) 2^(e-1)); S = s_m * 2^s_e with s_m the f32
+// integer significand.  So |x_i| = N_i * 2^c, N_i = A_i s_m < 2^42, c = s_e - 9.
+// For candidate u an element is at magnitude 4 iff N_i 2^(c - u + 1) > 5, and
+//   SSE(u) - sum x^2 = 4^u V(u) - 2^(u + 1 + c) W(u),
+// V = sum of v_i^2 (1 or 16), W = sum of N_i v_i (v_i 1 or 4).  Both terms are
+// scaled by 2^-e0, e0 = min(2 lo, lo + 1 + c), to integers below 2^104 and
+// compared in 128-bit arithmetic, candidates ascending, strictly smaller wins.
+// The window [floor(log2 min|x|) - 5, floor(log2 max|x|) + 1] clamped to
+// [-126, 125] is the one the NVFP4 path uses (same argument); within it every
+// shift below stays in range (c - u + 1 <= 6, u - c - 1 <= 43).
+__global__ void __launch_bounds__(256) requant_fp8_kernel(const uint8_t* __restrict__ w8,
+                                                          const float* __restrict__ scales, int64_t n_blocks,
+                                                          int64_t rows, int64_t bpr, int64_t srows, int64_t scols,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ ue8m0,
+                                                          uint32_t* status)
+{
+    uint32_t bad = 0;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n_blocks;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = g / (rows * bpr), r = (g / bpr) % rows, b = g % bpr;
+        const uint32_t sb = __float_as_uint(__ldg(scales + (t * srows + r / 128) * scols + (b * 32) / 128));
+        const uint4 q0 = __ldg(reinterpret_cast<const uint4*>(w8 + g * 32));
+        const uint4 q1 = __ldg(reinterpret_cast<const uint4*>(w8 + g * 32 + 16));
+        const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        // NaN codes (S.1111.111) anywhere, or a scale that is not positive finite
+        uint32_t nan = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t t7 = (wv[k] & 0x7F7F7F7Fu) + 0x01010101u;   // 0x80 per byte exactly when its low 7 bits are all ones
+            nan |= t7 & 0x80808080u;
+        }
+        if (nan != 0 || sb == 0u || sb >= 0x7F800000u) {
+            *reinterpret_cast<uint2*>(codes + g * 8) = make_uint2(0u, 0u);
+            ue8m0[g] = 0;
+            bad = 1;
+            continue;
+        }
+        const uint32_t es = sb >> 23;
+        const uint64_t sm = es == 0u ? (uint64_t)(sb & 0x7FFFFFu) : (uint64_t)((sb & 0x7FFFFFu) | 0x800000u);
+        const int c = (es == 0u ? -149 : (int)es - 150) - 9;
+        uint64_t N[32];
+        uint32_t negm = 0;
+        uint64_t nmax = 0, nmin = ~0ull;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t byte = (wv[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+            const uint32_t e = (byte >> 3) & 15u, m = byte & 7u;
+            const uint64_t A = e == 0u ? (uint64_t)m : (uint64_t)(8u + m) << (e - 1u);
+            N[i] = A * sm;
+            negm |= (byte >> 7) << i;
+            nmax = max(nmax, N[i]);
+            if (N[i] != 0ull) nmin = min(nmin, N[i]);
+        }
+        int best_u;
+        if (nmax == 0ull) {
+            best_u = -126;   // every candidate costs 32 * 4^u: the smallest scale
+        } else {
+            const int mhi = 63 - __clzll((long long)nmax) + c, mlo = 63 - __clzll((long long)nmin) + c;
+            const int hi = min(125, max(-126, mhi + 1));
+            const int lo = min(hi, max(-126, mlo - 5));
+            const int e0 = min(2 * lo, lo + 1 + c);
+            __int128 best = 0;
+            best_u = lo;
+            for (int u = lo; u <= hi; ++u) {
+                const int d = c - u + 1;
+                uint32_t V = 0;
+                unsigned __int128 W = 0;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const bool four = d >= 0 ? (N[i] << d) > 5ull : N[i] > (5ull << (-d));
+                    V += four ? 16u : 1u;
+                    W += four ? (unsigned __int128)N[i] * 4u : (unsigned __int128)N[i];
+                }
+                const __int128 G = ((__int128)V << (2 * u - e0)) - (__int128)(W << (u + 1 + c - e0));
+                if (u == lo || G < best) {
+                    best = G;
+                    best_u = u;
+                }
+            }
+        }
+        // codes at the chosen scale: 2-bit c = sign << 1 | magnitude 4
+        const int d = c - best_u + 1;
+        uint32_t lo_w = 0, hi_w = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const bool four = nmax != 0ull && (d >= 0 ? (N[i] << d) > 5ull : N[i] > (5ull << (-d)));
+            const uint32_t code = (((negm >> i) & 1u) << 1) | (four ? 1u : 0u);
+            if (i < 16) lo_w |= code << (2 * i);
+            else hi_w |= code << (2 * (i - 16));
+        }
+        *reinterpret_cast<uint2*>(codes + g * 8) = make_uint2(lo_w, hi_w);
+        ue8m0[g] = (uint8_t)(best_u + 127);
+    }
+    if (bad) flag_status(status, MOE_W2_DEV_BAD_NVFP4);
+}
+
 cudaError_t launch_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float* scale_2, int64_t n, int64_t rows,
                            int64_t K, uint8_t* codes, uint8_t* ue8m0, uint32_t* status, cudaStream_t s)
 {
@@ -294,6 +398,16 @@ cudaError_t launch_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float
     const int64_t want = (nb + 255) / 256;
     const int grid = (int)std::min<int64_t>(want, (int64_t)sm_count() * 8);
     requant_kernel<<<grid, 256, 0, s>>>(e2m1, e4m3, scale_2, nb, bpt, codes, ue8m0, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_requant_fp8(const uint8_t* w8, const float* scales, int64_t n, int64_t rows, int64_t K,
+                               uint8_t* codes, uint8_t* ue8m0, uint32_t* status, cudaStream_t s)
+{
+    const int64_t bpr = K / 32, n_blocks = n * rows * bpr;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((n_blocks + 255) / 256, (int64_t)sm_count() * 16));
+    requant_fp8_kernel<<<grid, 256, 0, s>>>(w8, scales, n_blocks, rows, bpr, (rows + 127) / 128, (K + 127) / 128, codes,
+                                            ue8m0, status);
     return cudaGetLastError();
 }
 

@@ -83,6 +83,8 @@ def load(build_if_missing: bool = True):
     L.moe_w2_forward_noalloc.restype = ctypes.c_int
     L.moe_w2_requant.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
     L.moe_w2_requant.restype = ctypes.c_int
+    L.moe_w2_requant_fp8.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp]
+    L.moe_w2_requant_fp8.restype = ctypes.c_int
     L.moe_w2_debug_force_pipeline_timeout.argtypes = [i32]
     L.moe_w2_debug_force_pipeline_timeout.restype = ctypes.c_int
     _lib = L
@@ -201,4 +203,24 @@ def requant(e2m1: torch.Tensor, e4m3: torch.Tensor, scale_2: torch.Tensor, codes
                           _ptr(status), _stream(stream))
     if st != OK:
         raise MoeW2Error(st, "moe_w2_requant")
+    return codes, ue8m0
+
+
+def requant_fp8(w8: torch.Tensor, scales: torch.Tensor, codes=None, ue8m0=None, status=None, stream=None):
+    """FP8 block-128: e4m3 bytes [n][rows][K] + f32 [n][ceil(rows/128)][ceil(K/128)]
+    -> (codes [n][rows][K/4], ue8m0 [n][rows][K/32])."""
+    L = load()
+    _check_cuda(w8, "w8", torch.uint8)
+    _check_cuda(scales, "scales", torch.float32)
+    n, rows, K = w8.shape
+    if tuple(scales.shape) != (n, (rows + 127) // 128, (K + 127) // 128):
+        raise ValueError(f"scales must be [{n}][{(rows + 127) // 128}][{(K + 127) // 128}], got {tuple(scales.shape)}")
+    if codes is None:
+        codes = torch.empty((n, rows, K // 4), dtype=torch.uint8, device=w8.device)
+    if ue8m0 is None:
+        ue8m0 = torch.empty((n, rows, K // 32), dtype=torch.uint8, device=w8.device)
+    st = L.moe_w2_requant_fp8(_ptr(w8), _ptr(scales), n, rows, K, _ptr(codes), _ptr(ue8m0), _ptr(status),
+                              _stream(stream))
+    if st != OK:
+        raise MoeW2Error(st, "moe_w2_requant_fp8")
     return codes, ue8m0

@@ -65,8 +65,9 @@ typedef enum {
 /* Bits OR-ed into *dev_status by the kernels. */
 #define MOE_W2_DEV_BAD_EXPERT_ID 1u   /* topk id outside [0,E): that pair contributes 0 */
 #define MOE_W2_DEV_BAD_SCALE 2u       /* UE8M0 byte outside [1,252] in a plane: that block counts as 0 */
-#define MOE_W2_DEV_BAD_NVFP4 4u       /* requant input: e4m3 NaN in a block, or scale_2 not a positive
-                                         finite number: the block's codes are 0x00 and its scale byte 0 */
+#define MOE_W2_DEV_BAD_NVFP4 4u       /* requant input (NVFP4 or FP8): e4m3 NaN in a block, or its scale_2 /
+                                         block scale not a positive finite number: the block's codes are
+                                         0x00 and its scale byte 0 */
 #define MOE_W2_DEV_PIPELINE_TIMEOUT 0x80000000u
                                       /* a kernel's internal wait (a pipeline barrier, or a hand-over
                                          between two phases of the layer) passed its limit of about
@@ -236,6 +237,25 @@ moe_w2_status moe_w2_requant(const uint8_t *e2m1, const uint8_t *e4m3, const flo
  * operation for the calls that follow.  Always returns MOE_W2_OK.
  */
 moe_w2_status moe_w2_debug_force_pipeline_timeout(int32_t enable);
+
+/*
+ * Load-time re-quantizer for FP8 block-quantised checkpoints ("The v0.24.0
+ * port", "Our hooks", fp8.py bullet): fp8 weights with f32 block-128 scales ->
+ * 2-bit planes.
+ *   w8      uint8 [n][rows][K]                       e4m3fn bytes
+ *   scales  float [n][ceil(rows/128)][ceil(K/128)]   one scale per 128 x 128 block
+ *                                                    (row block r/128, column block k/128)
+ *   codes   uint8 [n][rows][K/4]    output codes (plane format above)
+ *   ue8m0   uint8 [n][rows][K/32]   output UE8M0 bytes, s = u + 127
+ * Per block of 32 consecutive elements x_i = e4m3_i * S (exact), the output
+ * follows the same rule as moe_w2_requant (least squared error over u in
+ * [-126,125], nearest code, ties to magnitude 1 and to the smaller u, -0 -> -1).
+ * Bit-exact.  A block with an e4m3 NaN, or whose scale is not a positive finite
+ * number, gets codes 0x00 and scale byte 0 and sets MOE_W2_DEV_BAD_NVFP4.
+ * K must be a multiple of 32; w8 16-byte aligned, codes 8-byte aligned.
+ */
+moe_w2_status moe_w2_requant_fp8(const uint8_t *w8, const float *scales, int64_t n, int64_t rows, int64_t K,
+                                 uint8_t *codes, uint8_t *ue8m0, uint32_t *dev_status, void *stream);
 
 /* Human-readable name of a status code (static string). */
 const char *moe_w2_status_string(moe_w2_status s);

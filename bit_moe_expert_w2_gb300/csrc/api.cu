@@ -112,7 +112,7 @@ int64_t decode_counter_count(int64_t P, int32_t E, int32_t H, int32_t I)
     return 2 * mt * (I / 64) + 1;
 }
 
-Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I)
+Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I, bool cached)
 {
     Workspace w{};
     const int64_t P = (int64_t)T * k;
@@ -151,8 +151,67 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
         w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
         w.stage = reinterpret_cast<float*>(take(sizeof(float) * P * H));
     }
+    if (cached) w.ids_eff = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * P));
     w.bytes = off;
     return w;
+}
+
+// moe_w2_forward and its variants.  slot_of (nullable) is the residency table of
+// an expert cache: routed id -> slot of w, negative when not resident.
+moe_w2_status forward_impl(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                           const moe_w2_planes* w, const int32_t* slot_of, int32_t n_route, int32_t T, int32_t top_k,
+                           void* y_bf16, void* workspace, size_t workspace_bytes, uint32_t* misses,
+                           uint32_t* dev_status, void* stream, void* const* phase_events)
+{
+    if (!w || T < 0 || top_k < 1 || top_k > MOE_W2_MAX_TOP_K) return MOE_W2_ERR_INVALID_ARG;
+    if (w->num_experts < 1 || w->num_experts > MOE_W2_MAX_EXPERTS) return MOE_W2_ERR_INVALID_ARG;
+    if (!layer_shape_ok(w->num_experts, w->hidden, w->inter)) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)T * top_k > MOE_W2_MAX_PAIRS) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_W2_OK;
+    if (!x_bf16 || !topk_ids || !topk_weights || !y_bf16 || !workspace || !w->w13_codes || !w->w13_scales ||
+        !w->w2_codes || !w->w2_scales)
+        return MOE_W2_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MOE_W2_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x_bf16) & 15) != 0 || (reinterpret_cast<uintptr_t>(y_bf16) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(w->w13_codes) & 15) != 0 || (reinterpret_cast<uintptr_t>(w->w2_codes) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(w->w13_scales) & 15) != 0 || (reinterpret_cast<uintptr_t>(w->w2_scales) & 15) != 0)
+        return MOE_W2_ERR_INVALID_ARG;
+    const int32_t E = w->num_experts, H = w->hidden, I = w->inter;
+    const bool cached = slot_of != nullptr;
+    Workspace ws = carve_workspace(workspace, T, top_k, E, H, I, cached);
+    if (workspace_bytes < ws.bytes) return MOE_W2_ERR_WORKSPACE;
+    moe_w2_status st = check_device();
+    if (st != MOE_W2_OK) return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool decode = T <= MOE_W2_DECODE_MAX_TOKENS;
+    const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+    uint16_t* y = static_cast<uint16_t*>(y_bf16);
+    PhaseEvents ev{};
+    for (int i = 0; i < 4; ++i) ev.e[i] = phase_events ? static_cast<cudaEvent_t>(phase_events[i]) : nullptr;
+    if (ev.record(0, s) != cudaSuccess) return MOE_W2_ERR_CUDA;
+    const int64_t P = (int64_t)T * top_k;
+    const bool mma = decode && decode_use_mma(P, H, I);
+    PermuteSlots slots{};
+    if (cached) slots = PermuteSlots{slot_of, n_route, ws.ids_eff, misses};
+    cudaError_t e = launch_permute(topk_ids, slots, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active,
+                                   ws.active_count, ws.tiles, ws.tile_count,
+                                   !decode ? kPrefillTileRows : mma ? kDecodeMmaTileRows : kDecodeTileRows,
+                                   decode ? x : nullptr, mma ? ws.xa : nullptr, decode && !mma ? ws.xd : nullptr,
+                                   decode && !mma ? ws.sxd : nullptr, H, ws.counters,
+                                   decode ? (int32_t)decode_counter_count(P, E, H, I) : 0, decode ? y : nullptr,
+                                   dev_status, s);
+    if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
+    // the later kernels read the ids only to tell kept pairs from left-out ones
+    const int32_t* ids = cached ? ws.ids_eff : topk_ids;
+    if (mma)
+        e = launch_decode_mma(x, ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
+    else if (decode)
+        e = launch_decode(x, ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
+    else
+        e = launch_prefill(x, ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
+    if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
+    return ev.record(3, s) == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
 }
 
 }  // namespace moe_w2
@@ -206,7 +265,8 @@ moe_w2_status moe_w2_permute(const int32_t* topk_ids, int32_t T, int32_t top_k, 
     moe_w2_status st = check_device();
     if (st != MOE_W2_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_permute(topk_ids, T, top_k, E, sorted_pairs, inv_pairs, expert_offsets, nullptr, nullptr,
+    cudaError_t e = launch_permute(topk_ids, PermuteSlots{}, T, top_k, E, sorted_pairs, inv_pairs, expert_offsets,
+                                   nullptr, nullptr,
                                    nullptr, nullptr, 1, nullptr, nullptr, nullptr, nullptr, 0, nullptr, 0, nullptr,
                                    dev_status, s);
     return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
@@ -217,64 +277,48 @@ moe_w2_status moe_w2_forward_traced(const void* x_bf16, const int32_t* topk_ids,
                                     void* workspace, size_t workspace_bytes, uint32_t* dev_status, void* stream,
                                     void* const* phase_events)
 {
-    if (!w || T < 0 || top_k < 1 || top_k > MOE_W2_MAX_TOP_K) return MOE_W2_ERR_INVALID_ARG;
-    if (w->num_experts < 1 || w->num_experts > MOE_W2_MAX_EXPERTS) return MOE_W2_ERR_INVALID_ARG;
-    if (!layer_shape_ok(w->num_experts, w->hidden, w->inter)) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
-    if ((int64_t)T * top_k > MOE_W2_MAX_PAIRS) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
-    if (T == 0) return MOE_W2_OK;
-    if (!x_bf16 || !topk_ids || !topk_weights || !y_bf16 || !workspace || !w->w13_codes || !w->w13_scales ||
-        !w->w2_codes || !w->w2_scales)
-        return MOE_W2_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MOE_W2_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(x_bf16) & 15) != 0 || (reinterpret_cast<uintptr_t>(y_bf16) & 15) != 0 ||
-        (reinterpret_cast<uintptr_t>(w->w13_codes) & 15) != 0 || (reinterpret_cast<uintptr_t>(w->w2_codes) & 15) != 0 ||
-        (reinterpret_cast<uintptr_t>(w->w13_scales) & 15) != 0 || (reinterpret_cast<uintptr_t>(w->w2_scales) & 15) != 0)
-        return MOE_W2_ERR_INVALID_ARG;
-    const int32_t E = w->num_experts, H = w->hidden, I = w->inter;
-    Workspace ws = carve_workspace(workspace, T, top_k, E, H, I);
-    if (workspace_bytes < ws.bytes) return MOE_W2_ERR_WORKSPACE;
-    moe_w2_status st = check_device();
-    if (st != MOE_W2_OK) return st;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool decode = T <= MOE_W2_DECODE_MAX_TOKENS;
-    const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
-    uint16_t* y = static_cast<uint16_t*>(y_bf16);
-    PhaseEvents ev{};
-    for (int i = 0; i < 4; ++i) ev.e[i] = phase_events ? static_cast<cudaEvent_t>(phase_events[i]) : nullptr;
-    if (ev.record(0, s) != cudaSuccess) return MOE_W2_ERR_CUDA;
-    const int64_t P = (int64_t)T * top_k;
-    const bool mma = decode && decode_use_mma(P, H, I);
-    cudaError_t e = launch_permute(topk_ids, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active, ws.active_count,
-                                   ws.tiles, ws.tile_count,
-                                   !decode ? kPrefillTileRows : mma ? kDecodeMmaTileRows : kDecodeTileRows,
-                                   decode ? x : nullptr, mma ? ws.xa : nullptr, decode && !mma ? ws.xd : nullptr,
-                                   decode && !mma ? ws.sxd : nullptr, H, ws.counters,
-                                   decode ? (int32_t)decode_counter_count(P, E, H, I) : 0, decode ? y : nullptr,
-                                   dev_status, s);
-    if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
-    if (mma)
-        e = launch_decode_mma(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
-    else if (decode)
-        e = launch_decode(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
-    else
-        e = launch_prefill(x, topk_ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
-    if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
-    return ev.record(3, s) == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
+    return forward_impl(x_bf16, topk_ids, topk_weights, w, nullptr, 0, T, top_k, y_bf16, workspace, workspace_bytes,
+                        nullptr, dev_status, stream, phase_events);
 }
 
 moe_w2_status moe_w2_forward(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
                              const moe_w2_planes* w, int32_t T, int32_t top_k, void* y_bf16, void* workspace,
                              size_t workspace_bytes, uint32_t* dev_status, void* stream)
 {
-    return moe_w2_forward_traced(x_bf16, topk_ids, topk_weights, w, T, top_k, y_bf16, workspace, workspace_bytes,
-                                 dev_status, stream, nullptr);
+    return forward_impl(x_bf16, topk_ids, topk_weights, w, nullptr, 0, T, top_k, y_bf16, workspace, workspace_bytes,
+                        nullptr, dev_status, stream, nullptr);
+}
+
+size_t moe_w2_forward_cached_workspace_size(int32_t T, int32_t top_k, int32_t num_slots, int32_t H, int32_t I)
+{
+    if (moe_w2_forward_workspace_size(T, top_k, num_slots, H, I) == 0) return 0;
+    return carve_workspace(nullptr, T, top_k, num_slots, H, I, true).bytes;
+}
+
+moe_w2_status moe_w2_forward_cached(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                                    const moe_w2_planes* w, const int32_t* slot_of_expert,
+                                    int32_t num_routed_experts, int32_t T, int32_t top_k, void* y_bf16,
+                                    void* workspace, size_t workspace_bytes, uint32_t* miss_counter,
+                                    uint32_t* dev_status, void* stream)
+{
+    if (num_routed_experts < 1 || num_routed_experts > MOE_W2_MAX_ROUTED_EXPERTS) return MOE_W2_ERR_INVALID_ARG;
+    if (T > 0 && !slot_of_expert) return MOE_W2_ERR_INVALID_ARG;
+    return forward_impl(x_bf16, topk_ids, topk_weights, w, slot_of_expert, num_routed_experts, T, top_k, y_bf16,
+                        workspace, workspace_bytes, miss_counter, dev_status, stream, nullptr);
 }
 
 moe_w2_status moe_w2_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float* scale_2, int64_t n,
                              int64_t rows, int64_t K, uint8_t* codes, uint8_t* ue8m0, uint32_t* dev_status,
                              void* stream)
 {
+    return moe_w2_requant_ex(e2m1, e4m3, scale_2, n, rows, K, 0u, codes, ue8m0, dev_status, stream);
+}
+
+moe_w2_status moe_w2_requant_ex(const uint8_t* e2m1, const uint8_t* e4m3, const float* scale_2, int64_t n,
+                                int64_t rows, int64_t K, uint32_t options, uint8_t* codes, uint8_t* ue8m0,
+                                uint32_t* dev_status, void* stream)
+{
+    if ((options & ~MOE_W2_REQUANT_BALANCE_ZERO_SIGNS) != 0u) return MOE_W2_ERR_INVALID_ARG;
     if (n < 0 || rows < 0 || K < 0) return MOE_W2_ERR_INVALID_ARG;
     if (K % 32 != 0) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
     if (n == 0 || rows == 0 || K == 0) return MOE_W2_OK;
@@ -285,8 +329,27 @@ moe_w2_status moe_w2_requant(const uint8_t* e2m1, const uint8_t* e4m3, const flo
         return MOE_W2_ERR_INVALID_ARG;
     moe_w2_status st = check_device();
     if (st != MOE_W2_OK) return st;
-    cudaError_t e = launch_requant(e2m1, e4m3, scale_2, n, rows, K, codes, ue8m0, dev_status,
+    cudaError_t e = launch_requant(e2m1, e4m3, scale_2, n, rows, K, options, codes, ue8m0, dev_status,
                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
+}
+
+moe_w2_status moe_w2_requant_mxfp4(const uint8_t* e2m1, const uint8_t* scales, int64_t n, int64_t rows, int64_t K,
+                                   uint32_t options, uint8_t* codes, uint8_t* ue8m0, uint32_t* dev_status,
+                                   void* stream)
+{
+    if (n < 0 || rows < 0 || K < 0) return MOE_W2_ERR_INVALID_ARG;
+    if ((options & ~MOE_W2_REQUANT_BALANCE_ZERO_SIGNS) != 0u) return MOE_W2_ERR_INVALID_ARG;
+    if (K % 32 != 0) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
+    if (n == 0 || rows == 0 || K == 0) return MOE_W2_OK;
+    if (rows > ((int64_t)1 << 40) / K || n > ((int64_t)1 << 50) / (rows * K)) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
+    if (!e2m1 || !scales || !codes || !ue8m0) return MOE_W2_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(e2m1) & 15) != 0 || (reinterpret_cast<uintptr_t>(codes) & 7) != 0)
+        return MOE_W2_ERR_INVALID_ARG;
+    moe_w2_status st = check_device();
+    if (st != MOE_W2_OK) return st;
+    cudaError_t e = launch_requant_mxfp4(e2m1, scales, n, rows, K, options, codes, ue8m0, dev_status,
+                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
 }
 

@@ -253,11 +253,13 @@ struct Workspace {
     uint8_t* hd;           // e2m1 digit rows of h, kActDigits per pair (expert order) [8P][I/2]
     uint8_t* shd;          // their UE8M0 bytes [8P][I/32]
     float* gu_part;        // gate_up partial sums of the two K halves [2][P][2I] (small steps only, else null)
+    // behind an expert cache
+    int32_t* ids_eff;      // slot of each pair, -1 when left out [P] (null without a residency table)
     DecodeSplit split;
     size_t bytes;
 };
 
-Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I);
+Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I, bool cached = false);
 int64_t max_tiles(int64_t P, int32_t E, bool decode);
 int64_t decode_counter_count(int64_t P, int32_t E, int32_t H, int32_t I);
 
@@ -277,10 +279,19 @@ struct PhaseEvents {
     }
 };
 
-cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* sorted, int32_t* inv,
-                           int32_t* offsets, int32_t* active, int32_t* active_count, int4* tiles,
-                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16, uint8_t* xd,
-                           uint8_t* sxd, int32_t H, int32_t* counters, int32_t n_counters, uint16_t* y,
+// Expert residency of a step: routed id -> slot of the planes (all null: the
+// routed ids are the slots).
+struct PermuteSlots {
+    const int32_t* slot_of = nullptr;   // [n_route], negative: not resident
+    int32_t n_route = 0;
+    int32_t* ids_eff = nullptr;         // [P] out: slot per pair, -1 when left out
+    uint32_t* misses = nullptr;         // += pairs whose expert is not resident
+};
+
+cudaError_t launch_permute(const int32_t* ids, const PermuteSlots& slots, int32_t T, int32_t k, int32_t E,
+                           int32_t* sorted, int32_t* inv, int32_t* offsets, int32_t* active, int32_t* active_count,
+                           int4* tiles, int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16,
+                           uint8_t* xd, uint8_t* sxd, int32_t H, int32_t* counters, int32_t n_counters, uint16_t* y,
                            uint32_t* status, cudaStream_t s);
 
 cudaError_t launch_decode_mma(const uint16_t* x, const int32_t* ids, const float* weights,
@@ -294,9 +305,11 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
                            int32_t T, int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status,
                            cudaStream_t s, const PhaseEvents& ev);
 
-cudaError_t launch_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float* scale_2, int64_t n,
-                           int64_t rows, int64_t K, uint8_t* codes, uint8_t* ue8m0, uint32_t* status,
+cudaError_t launch_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float* scale_2, int64_t n, int64_t rows,
+                           int64_t K, uint32_t options, uint8_t* codes, uint8_t* ue8m0, uint32_t* status,
                            cudaStream_t s);
+cudaError_t launch_requant_mxfp4(const uint8_t* e2m1, const uint8_t* scales, int64_t n, int64_t rows, int64_t K,
+                                 uint32_t options, uint8_t* codes, uint8_t* ue8m0, uint32_t* status, cudaStream_t s);
 
 cudaError_t launch_requant_fp8(const uint8_t* w8, const float* scales, int64_t n, int64_t rows, int64_t K,
                                uint8_t* codes, uint8_t* ue8m0, uint32_t* status, cudaStream_t s);

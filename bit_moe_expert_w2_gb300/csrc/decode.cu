@@ -708,7 +708,8 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
                     ok = false;
                     break;
                 }
-                const uint2 sfb = lds_u2(ring_addr + kOffSfb + bp.slot * kSfbBytes + lane * 16 + 8u * (uint32_t)(ch & 1));
+                // (lane n holds B row n's words; lanes past N repeat rows of the slot)
+                const uint2 sfb = lds_u2(ring_addr + kOffSfb + bp.slot * kSfbBytes + (lane % kN) * 16 + 8u * (uint32_t)(ch & 1));
                 tmem_st_stage4(tq + kColA + 32 * st, r, tq + kColSfa + 8 * st + warp, sfa.x,
                                tq + kColSfa + 8 * st + 4 + warp, sfa.y, tq + kColSfb + 8 * st, sfb.x,
                                tq + kColSfb + 8 * st + 4, sfb.y);

@@ -14,6 +14,15 @@
 // tile.  Extra CTAs of the launch write x as the decode kernels read it: in T16
 // order (mma.sync kernel) or as rows of packed e2m1 digits with UE8M0 bytes per
 // 32 elements (block-scaled kernel, kActDigits rows per token).
+//
+// Behind an expert cache (page "vLLM-Moet wiki", BASE-cache paragraph; page "The
+// v0.24.0 port", section "Our hooks", BASE-cache bullet) the planes hold E
+// resident slots and a table maps each routed expert id to its slot, or to a
+// negative value when the expert is not resident.  The permutation then sorts
+// by slot; a pair whose expert is missing is left out like an invalid id (it
+// contributes zero) but raises no status bit: it adds one to the caller's miss
+// counter instead.  The slot of every pair (-1 when left out) goes to ids_eff,
+// which the later kernels read in place of the routed ids.
 #include <algorithm>
 
 #include "common.cuh"
@@ -24,6 +33,44 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+
+// Residency table of a step (null table: ids are slots already).
+struct SlotMap {
+    const int32_t* slot_of;   // [n_route] slot of each routed expert id, < 0 when not resident
+    int32_t n_route;
+    int32_t* ids_eff;         // [P] slot of each pair, -1 when it is left out (null: not written)
+    uint32_t* misses;         // pairs whose expert is not resident (null: not counted)
+};
+
+// Bin of a routed id: its slot in [0, E), or E when the pair is left out, with
+// `bad` set for an id or slot outside its range and `miss` for a missing expert.
+__device__ __forceinline__ int pair_bin(int e, const SlotMap& m, int32_t E, uint32_t& bad, uint32_t& miss)
+{
+    if (m.slot_of != nullptr) {
+        if ((unsigned)e >= (unsigned)m.n_route) {
+            bad = 1;
+            return E;
+        }
+        e = __ldg(m.slot_of + e);
+        if (e < 0) {
+            miss += 1;
+            return E;
+        }
+    }
+    if ((unsigned)e >= (unsigned)E) {
+        bad = 1;
+        return E;
+    }
+    return e;
+}
+
+// Adds the warp's missing pairs to the counter (one atomic per warp).
+__device__ __forceinline__ void count_misses(uint32_t miss, const SlotMap& m)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) miss += __shfl_xor_sync(0xffffffffu, miss, o);
+    if (m.misses != nullptr && miss != 0 && (threadIdx.x & 31) == 0) atomicAdd(m.misses, miss);
+}
 
 __device__ __forceinline__ uint32_t lanemask_lt()
 {
@@ -36,18 +83,21 @@ __device__ __forceinline__ uint32_t lanemask_lt()
 // pair p): the same outputs as the CTA path below, without its barriers.  Bins:
 // expert id, E for out-of-range ids, E + 1 for lanes past P (never stored).
 // Returns the number of valid pairs (to every lane).
-__device__ int warp_permute(const int32_t* __restrict__ ids, int32_t P, int32_t E, int32_t* __restrict__ sorted,
-                            int32_t* __restrict__ inv, int32_t* __restrict__ offsets, int32_t* __restrict__ active,
-                            int32_t* __restrict__ active_count, int4* __restrict__ tiles,
-                            int32_t* __restrict__ tile_count, int32_t tile_rows, int* s_bin, uint32_t* status)
+__device__ int warp_permute(const int32_t* __restrict__ ids, const SlotMap& map, int32_t P, int32_t E,
+                            int32_t* __restrict__ sorted, int32_t* __restrict__ inv, int32_t* __restrict__ offsets,
+                            int32_t* __restrict__ active, int32_t* __restrict__ active_count,
+                            int4* __restrict__ tiles, int32_t* __restrict__ tile_count, int32_t tile_rows,
+                            int* s_bin, uint32_t* status)
 {
     const int lane = threadIdx.x & 31;
     int b = E + 1;
+    uint32_t bad = 0, miss = 0;
     if (lane < P) {
-        const int e = __ldg(ids + lane);
-        b = (unsigned)e < (unsigned)E ? e : E;
+        b = pair_bin(__ldg(ids + lane), map, E, bad, miss);
+        if (map.ids_eff != nullptr) map.ids_eff[lane] = b < E ? b : -1;
     }
-    if (__any_sync(0xffffffffu, lane < P && b == E) && lane == 0) flag_status(status, MOE_W2_DEV_BAD_EXPERT_ID);
+    if (__any_sync(0xffffffffu, bad != 0) && lane == 0) flag_status(status, MOE_W2_DEV_BAD_EXPERT_ID);
+    count_misses(miss, map);
     // stable rank inside the bin, and the pairs of lower bins
     const uint32_t same = __match_any_sync(0xffffffffu, b);
     const int rank = __popc(same & lanemask_lt());
@@ -198,7 +248,7 @@ __device__ __forceinline__ void x_digits(const uint16_t* __restrict__ x, int64_t
 }
 
 __global__ void __launch_bounds__(kThreads) permute_kernel(
-    const int32_t* __restrict__ ids, int32_t P, int32_t E, int32_t* __restrict__ sorted,
+    const int32_t* __restrict__ ids, const SlotMap map, int32_t P, int32_t E, int32_t* __restrict__ sorted,
     int32_t* __restrict__ inv, int32_t* __restrict__ offsets, int32_t* __restrict__ active,
     int32_t* __restrict__ active_count, int4* __restrict__ tiles, int32_t* __restrict__ tile_count,
     int32_t tile_rows, const uint16_t* __restrict__ x, uint16_t* __restrict__ x_t16, uint8_t* __restrict__ xd,
@@ -231,7 +281,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
         __shared__ int s_bin[32];
         __shared__ int s_valid;
         if (threadIdx.x < 32) {
-            const int n_valid = warp_permute(ids, P, E, sorted, inv, offsets, active, active_count, tiles,
+            const int n_valid = warp_permute(ids, map, P, E, sorted, inv, offsets, active, active_count, tiles,
                                              tile_count, tile_rows, s_bin, status);
             if (threadIdx.x == 0) s_valid = n_valid;
         }
@@ -243,7 +293,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
     extern __shared__ int32_t smem[];
     __shared__ int3 warp_tmp[kWarps];
     int3 sh_tot;   // totals of the fused scan (same value in every thread)
-    const int nb = E + 1;                 // bin E collects out-of-range ids
+    const int nb = E + 1;                 // bin E collects the pairs left out
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // slices of 32-pair multiples, one per warp; only as many as P needs
     const int chunk = (((P + kWarps - 1) / kWarps) + 31) & ~31;
@@ -256,7 +306,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
 
     const int p0 = warp * chunk;
     const int p1 = min(P, p0 + chunk);
-    uint32_t bad = 0;
+    uint32_t bad = 0, miss = 0;
 
     // pass 1: counts per (slice, expert)
     for (int pb = p0; pb < p1; pb += 32 * 8) {
@@ -268,12 +318,14 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            if (pb + u * 32 + lane >= p1) continue;
-            int b = e[u];
-            if ((unsigned)b >= (unsigned)E) { b = E; bad = 1; }
+            const int p = pb + u * 32 + lane;
+            if (p >= p1) continue;
+            const int b = pair_bin(e[u], map, E, bad, miss);
+            if (map.ids_eff != nullptr) map.ids_eff[p] = b < E ? b : -1;
             atomicAdd(&cnt[warp * nb + b], 1);
         }
     }
+    count_misses(miss, map);
     __syncthreads();
 
     // per-expert totals; cnt becomes the exclusive prefix over slices
@@ -339,8 +391,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
             if (pb + u * 32 >= p1) break;   // warp-uniform
             const int p = pb + u * 32 + lane;
             const bool valid = p < p1;
-            int b = e[u];
-            if (valid && (unsigned)b >= (unsigned)E) b = E;
+            uint32_t bad2 = 0, miss2 = 0;   // counted in pass 1
+            const int b = valid ? pair_bin(e[u], map, E, bad2, miss2) : E;
             const int key = valid ? b : (nb + lane);
             const uint32_t mask = __match_any_sync(0xffffffffu, key);
             const int rank = __popc(mask & lt);
@@ -360,10 +412,10 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(
 
 }  // namespace
 
-cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* sorted, int32_t* inv,
-                           int32_t* offsets, int32_t* active, int32_t* active_count, int4* tiles,
-                           int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16, uint8_t* xd,
-                           uint8_t* sxd, int32_t H, int32_t* counters, int32_t n_counters, uint16_t* y,
+cudaError_t launch_permute(const int32_t* ids, const PermuteSlots& slots, int32_t T, int32_t k, int32_t E,
+                           int32_t* sorted, int32_t* inv, int32_t* offsets, int32_t* active, int32_t* active_count,
+                           int4* tiles, int32_t* tile_count, int32_t tile_rows, const uint16_t* x, uint16_t* x_t16,
+                           uint8_t* xd, uint8_t* sxd, int32_t H, int32_t* counters, int32_t n_counters, uint16_t* y,
                            uint32_t* status, cudaStream_t s)
 {
     const int32_t P = T * k;
@@ -384,7 +436,8 @@ cudaError_t launch_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, 
         n_blocks = (int64_t)T * H / 32;
         extra = (int)std::min<int64_t>((n_blocks * 16 + kThreads - 1) / kThreads, 4 * (int64_t)sm_count());
     }
-    permute_kernel<<<1 + extra, kThreads, smem, s>>>(ids, P, E, sorted, inv, offsets, active, active_count, tiles,
+    const SlotMap map{slots.slot_of, slots.n_route, slots.ids_eff, slots.misses};
+    permute_kernel<<<1 + extra, kThreads, smem, s>>>(ids, map, P, E, sorted, inv, offsets, active, active_count, tiles,
                                                      tile_count, tile_rows, x, x_t16, xd, sxd, H, n_blocks,
                                                      counters, n_counters, y, y ? (int64_t)T * H : 0, status);
     return cudaGetLastError();

@@ -26,6 +26,18 @@
 // kernel counts classes once (SWAR over nibbles), computes each class's
 // threshold exponent tau (the largest u at which it is at magnitude 4) once, and
 // evaluates each candidate from 14 integer comparisons against tau.
+//
+// MXFP4 (page "The v0.24.0 port", section "Our hooks", mxfp4.py bullet; page
+// "vLLM-Moet wiki": FP4 experts load by a codes remap): e2m1 elements with one
+// UE8M0 byte s per 32, x_i = e2m1_i * 2^(s-127), byte 255 = NaN.  This is the
+// NVFP4 case with Q_h = 1 and f_h = s - 128 in both halves, so the same kernel
+// serves it; the codes come out as a function of the e2m1 codes alone and the
+// byte moves with s, which is the remap.
+//
+// Zero-sign balancing (page "vLLM-Moet wiki", the Kimi-K2.7 paragraph: an export
+// writing every exact zero as +0 biases the codes): with the option, the exact
+// zeros of a block take the signs +,-,+,- ... in element order.  A zero is at
+// magnitude 1 for every u, so the scale search is unchanged.
 #include <algorithm>
 
 #include "common.cuh"
@@ -81,27 +93,64 @@ __device__ __forceinline__ Half decode_half(uint32_t b, uint32_t S, int es)
     return h;
 }
 
+// Zero-sign balancing of one block: w = the 4 words of 8 nibbles (element
+// order), zq = per half whether its scale is 0 (every element exactly zero);
+// sg = sign bits (bit 3 of each nibble), returned with the zeros' signs set to
+// +,-,+,- ... in element order.
+__device__ __forceinline__ void balance_zero_signs(const uint32_t (&w)[4], const bool (&zq)[2], uint32_t (&sg)[4])
+{
+    uint32_t par = 0;
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+        const uint32_t z = zq[wi >> 1] ? 0x88888888u : (~((w[wi] & 0x77777777u) + 0x77777777u) & 0x88888888u);
+        uint32_t bal = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t bit = 1u << (4 * k + 3);
+            if (z & bit) {
+                bal |= par ? bit : 0u;
+                par ^= 1u;
+            }
+        }
+        sg[wi] = (sg[wi] & ~z) | bal;
+    }
+}
+
+// kMx = false: NVFP4 (scale bytes = two e4m3 per block, scale_2 per tensor);
+// kMx = true: MXFP4 (scale bytes = one UE8M0 per block, scale_2 unused).
+template <bool kMx>
 __global__ void __launch_bounds__(256) requant_kernel(const uint8_t* __restrict__ e2m1,
-                                                      const uint8_t* __restrict__ e4m3,
+                                                      const uint8_t* __restrict__ scale_bytes,
                                                       const float* __restrict__ scale_2, int64_t n_blocks,
-                                                      int64_t blocks_per_tensor, uint8_t* __restrict__ codes,
-                                                      uint8_t* __restrict__ ue8m0, uint32_t* status)
+                                                      int64_t blocks_per_tensor, uint32_t balance,
+                                                      uint8_t* __restrict__ codes, uint8_t* __restrict__ ue8m0,
+                                                      uint32_t* status)
 {
     uint32_t bad_any = 0;
     for (int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < n_blocks;
          blk += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t tensor = blk / blocks_per_tensor;
-        const uint32_t sbits = __float_as_uint(__ldg(scale_2 + tensor));
         const uint4 nib = ldg_stream_u4(e2m1 + blk * 16);
-        const uint32_t sc = ldg_u16(e4m3 + blk * 2);
-
-        // scale_2 = S * 2^es
-        const uint32_t sE = (sbits >> 23) & 0xFFu, sM = sbits & 0x7FFFFFu;
-        const bool s2_bad = (sbits >> 31) != 0u || sE == 0xFFu || (sE == 0u && sM == 0u);
-        const uint32_t S = sE ? (sM | 0x800000u) : sM;
-        const int es = sE ? (int)sE - 150 : -149;
-
-        Half hf[2] = {decode_half(sc & 0xFFu, S, es), decode_half(sc >> 8, S, es)};
+        Half hf[2];
+        bool s2_bad = false;
+        if constexpr (kMx) {
+            const uint32_t sb = __ldg(scale_bytes + blk);
+            hf[0].Q = 1u;
+            hf[0].f = (int)sb - 128;   // n1 = 2|e2m1| carries the extra factor 2
+            hf[0].neg = 0u;
+            hf[0].nan = sb == 0xFFu;
+            hf[1] = hf[0];
+        } else {
+            const int64_t tensor = blk / blocks_per_tensor;
+            const uint32_t sbits = __float_as_uint(__ldg(scale_2 + tensor));
+            const uint32_t sc = ldg_u16(scale_bytes + blk * 2);
+            // scale_2 = S * 2^es
+            const uint32_t sE = (sbits >> 23) & 0xFFu, sM = sbits & 0x7FFFFFu;
+            s2_bad = (sbits >> 31) != 0u || sE == 0xFFu || (sE == 0u && sM == 0u);
+            const uint32_t S = sE ? (sM | 0x800000u) : sM;
+            const int es = sE ? (int)sE - 150 : -149;
+            hf[0] = decode_half(sc & 0xFFu, S, es);
+            hf[1] = decode_half(sc >> 8, S, es);
+        }
         if (s2_bad || hf[0].nan || hf[1].nan) {
             *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(0u, 0u);
             ue8m0[blk] = 0;
@@ -263,6 +312,13 @@ __global__ void __launch_bounds__(256) requant_kernel(const uint8_t* __restrict_
         }
 
         // codes: magnitude 4 iff class >= v0, sign = e2m1 sign xor e4m3 sign
+        uint32_t sg[4];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) sg[wi] = (w[wi] ^ (hf[wi >> 1].neg ? 0x88888888u : 0u)) & 0x88888888u;
+        if (balance) {
+            const bool zq[2] = {hf[0].Q == 0u, hf[1].Q == 0u};
+            balance_zero_signs(w, zq, sg);
+        }
         uint32_t out[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -272,8 +328,7 @@ __global__ void __launch_bounds__(256) requant_kernel(const uint8_t* __restrict_
                 const int wi = 2 * q + j, h = q;
                 const uint32_t ww = w[wi];
                 const uint32_t ge = ((ww & 0x77777777u) + (uint32_t)(8 - v0[h]) * 0x11111111u) & 0x88888888u;
-                const uint32_t sg = (ww ^ (hf[h].neg ? 0x88888888u : 0u)) & 0x88888888u;
-                half16[j] = pack_codes(ge, sg);
+                half16[j] = pack_codes(ge, sg[wi]);
             }
             out[q] = half16[0] | (half16[1] << 16);
         }
@@ -390,14 +445,27 @@ __global__ void __launch_bounds__(256) requant_fp8_kernel(const uint8_t* __restr
 }
 
 cudaError_t launch_requant(const uint8_t* e2m1, const uint8_t* e4m3, const float* scale_2, int64_t n, int64_t rows,
-                           int64_t K, uint8_t* codes, uint8_t* ue8m0, uint32_t* status, cudaStream_t s)
+                           int64_t K, uint32_t options, uint8_t* codes, uint8_t* ue8m0, uint32_t* status,
+                           cudaStream_t s)
 {
     const int64_t bpt = rows * (K / 32);
     const int64_t nb = n * bpt;
     if (nb == 0) return cudaSuccess;
     const int64_t want = (nb + 255) / 256;
     const int grid = (int)std::min<int64_t>(want, (int64_t)sm_count() * 8);
-    requant_kernel<<<grid, 256, 0, s>>>(e2m1, e4m3, scale_2, nb, bpt, codes, ue8m0, status);
+    requant_kernel<false><<<grid, 256, 0, s>>>(e2m1, e4m3, scale_2, nb, bpt, options & MOE_W2_REQUANT_BALANCE_ZERO_SIGNS,
+                                               codes, ue8m0, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_requant_mxfp4(const uint8_t* e2m1, const uint8_t* scales, int64_t n, int64_t rows, int64_t K,
+                                 uint32_t options, uint8_t* codes, uint8_t* ue8m0, uint32_t* status, cudaStream_t s)
+{
+    const int64_t nb = n * rows * (K / 32);
+    if (nb == 0) return cudaSuccess;
+    const int grid = (int)std::min<int64_t>((nb + 255) / 256, (int64_t)sm_count() * 8);
+    requant_kernel<true><<<grid, 256, 0, s>>>(e2m1, scales, nullptr, nb, nb, options & MOE_W2_REQUANT_BALANCE_ZERO_SIGNS,
+                                              codes, ue8m0, status);
     return cudaGetLastError();
 }
 

@@ -105,6 +105,8 @@ REQUANT = RequantConfig("requant_256", 256, 2048, 6144, 4)
 REQUANT_CASES = {"requant_256": None, "requant_16": 16}
 # FP8 block-128 loader workloads: experts of gate/up [I][H] x 2 and down [H][I]
 REQUANT_FP8_CASES = {"requant_fp8_16": 16}
+# MXFP4 loader workloads (e2m1 with UE8M0 block-32 scales), same expert shapes
+REQUANT_MXFP4_CASES = {"requant_mxfp4_16": 16}
 
 
 def rng_for(seed: int) -> np.random.Generator:
@@ -239,6 +241,32 @@ def small_layer_inputs(H: int, I: int, E: int, k: int, T: int, seed: int,
     return layer_inputs(cfg)
 
 
+@dataclasses.dataclass
+class CachedLayerInputs:
+    cfg: LayerConfig
+    x: np.ndarray         # bf16 bits [T][H]
+    ids: np.ndarray       # int32 [T][k] routed expert ids in [0, cfg.num_experts)
+    weights: np.ndarray   # float32 [T][k]
+    planes: dict          # planes of the S resident slots
+    slot_of: np.ndarray   # int32 [cfg.num_experts]: slot of each routed expert, -1 if not resident
+
+
+def cached_layer_inputs(cfg: LayerConfig, extra_slots: int = 0) -> CachedLayerInputs:
+    """A layer of cfg.num_experts routed experts behind an expert cache: activations and
+    routing first, then planes only for the step's routed experts plus `extra_slots`
+    others, placed at slots in a random order."""
+    rng = rng_for(cfg.seed)
+    x = activations(rng, cfg.tokens, cfg.hidden)
+    ids, weights = routing(rng, cfg)
+    used = np.unique(ids)
+    rest = np.setdiff1d(np.arange(cfg.num_experts), used)
+    resident = np.concatenate([used, rng.choice(rest, size=min(extra_slots, len(rest)), replace=False)])
+    slot_of = np.full(cfg.num_experts, -1, np.int32)
+    slot_of[resident] = rng.permutation(len(resident)).astype(np.int32)
+    planes = code_planes(rng, len(resident), cfg.hidden, cfg.inter, cfg.exp_lo, cfg.exp_hi)
+    return CachedLayerInputs(cfg, x, ids, weights, planes, slot_of)
+
+
 # --------------------------------------------------------------------------- NVFP4
 
 def _e4m3_positive_table():
@@ -329,4 +357,49 @@ def requant_fp8_inputs(cfg: RequantConfig = REQUANT, experts: int = 16):
         gu.append(fp8_tensors(rng, 2, cfg.inter, cfg.hidden))
         dn.append(fp8_tensors(rng, 1, cfg.hidden, cfg.inter))
     cat = lambda ts: Fp8Tensors(np.concatenate([t.w8 for t in ts]), np.concatenate([t.scales for t in ts]))
+    return cat(gu), cat(dn)
+
+
+# --------------------------------------------------------------------------- MXFP4
+
+@dataclasses.dataclass
+class Mxfp4Tensors:
+    e2m1: np.ndarray      # uint8 [n][rows][K/2], low nibble = even element
+    scales: np.ndarray    # uint8 UE8M0 bytes [n][rows][K/32]
+
+
+def mxfp4_tensors(rng: np.random.Generator, n: int, rows: int, K: int, plus_zero_frac: float = 0.0) -> Mxfp4Tensors:
+    """e2m1 nibbles uniform over all 16 values, scale exponents uniform in [-12, -2];
+    with plus_zero_frac > 0 that fraction of the elements is replaced by +0
+    (an export that writes every exact zero as +0)."""
+    e2m1 = random_bytes(rng, (n, rows, K // 2))
+    if plus_zero_frac > 0.0:
+        nib = np.stack([e2m1 & 0xF, e2m1 >> 4], axis=-1)
+        nib[rng.random(nib.shape) < plus_zero_frac] = 0
+        nib[nib == 8] = 0
+        e2m1 = (nib[..., 0] | (nib[..., 1] << 4)).astype(np.uint8)
+    sc = (127 + rng.integers(-12, -1, size=(n, rows, K // 32))).astype(np.uint8)
+    return Mxfp4Tensors(e2m1, sc)
+
+
+def plus_zero_nvfp4(rng: np.random.Generator, n: int, rows: int, K: int, zero_frac: float = 0.25) -> Nvfp4Tensors:
+    """NVFP4 tensors whose exact zeros are all +0 (nibble 0), about zero_frac of the elements."""
+    t = nvfp4_tensors(rng, n, rows, K)
+    nib = np.stack([t.e2m1 & 0xF, t.e2m1 >> 4], axis=-1)
+    nib[rng.random(nib.shape) < zero_frac] = 0
+    nib[nib == 8] = 0
+    t.e2m1 = (nib[..., 0] | (nib[..., 1] << 4)).astype(np.uint8)
+    return t
+
+
+def requant_mxfp4_inputs(cfg: RequantConfig = REQUANT, experts: int = 16):
+    """The MXFP4 loader workload: (gate/up tensors, down tensors) of the first `experts`
+    experts, laid out as requant_inputs lays out the NVFP4 ones (a child seed each)."""
+    seeds = np.random.SeedSequence(cfg.seed + 200).spawn(cfg.num_experts)
+    gu, dn = [], []
+    for e in range(experts):
+        rng = np.random.default_rng(seeds[e])
+        gu.append(mxfp4_tensors(rng, 2, cfg.inter, cfg.hidden))
+        dn.append(mxfp4_tensors(rng, 1, cfg.hidden, cfg.inter))
+    cat = lambda ts: Mxfp4Tensors(np.concatenate([t.e2m1 for t in ts]), np.concatenate([t.scales for t in ts]))
     return cat(gu), cat(dn)

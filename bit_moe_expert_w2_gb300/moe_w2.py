@@ -22,6 +22,7 @@ DEV_BAD_EXPERT_ID = 1
 DEV_BAD_SCALE = 2
 DEV_BAD_NVFP4 = 4
 DEV_PIPELINE_TIMEOUT = 0x80000000   # as a uint32; reads back as a negative int32 from a torch int32 tensor
+REQUANT_BALANCE_ZERO_SIGNS = 1       # option bit of requant (moe_w2_requant_ex) and requant_mxfp4
 DECODE_MAX_TOKENS = 64
 PATH_NONE, PATH_DECODE_MMA, PATH_DECODE_BLOCK_SCALED, PATH_PREFILL = 0, 1, 2, 3   # moe_w2_forward_path
 NOALLOC_WORKSPACE_BYTES = 8 << 20   # MOE_W2_NOALLOC_WORKSPACE_BYTES
@@ -81,8 +82,16 @@ def load(build_if_missing: bool = True):
     L.moe_w2_forward.restype = ctypes.c_int
     L.moe_w2_forward_noalloc.argtypes = [vp, vp, vp, ctypes.POINTER(Planes), i32, i32, vp, vp, vp]
     L.moe_w2_forward_noalloc.restype = ctypes.c_int
+    L.moe_w2_forward_cached_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.moe_w2_forward_cached_workspace_size.restype = sz
+    L.moe_w2_forward_cached.argtypes = [vp, vp, vp, ctypes.POINTER(Planes), vp, i32, i32, i32, vp, vp, sz, vp, vp, vp]
+    L.moe_w2_forward_cached.restype = ctypes.c_int
     L.moe_w2_requant.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
     L.moe_w2_requant.restype = ctypes.c_int
+    L.moe_w2_requant_ex.argtypes = [vp, vp, vp, i64, i64, i64, u32, vp, vp, vp, vp]
+    L.moe_w2_requant_ex.restype = ctypes.c_int
+    L.moe_w2_requant_mxfp4.argtypes = [vp, vp, i64, i64, i64, u32, vp, vp, vp, vp]
+    L.moe_w2_requant_mxfp4.restype = ctypes.c_int
     L.moe_w2_requant_fp8.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp]
     L.moe_w2_requant_fp8.restype = ctypes.c_int
     L.moe_w2_debug_force_pipeline_timeout.argtypes = [i32]
@@ -150,6 +159,39 @@ def forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
     return y
 
 
+def cached_workspace_size(T: int, top_k: int, num_slots: int, H: int, I: int) -> int:
+    return int(load().moe_w2_forward_cached_workspace_size(T, top_k, num_slots, H, I))
+
+
+def forward_cached(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, planes,
+                   slot_of_expert: torch.Tensor, misses=None, y=None, workspace=None, status=None,
+                   stream=None) -> torch.Tensor:
+    """moe_w2_forward_cached: the forward with planes of resident slots and a residency table
+    (int32 [num_routed], slot or negative); misses (device uint32 [1], optional) counts the
+    pairs whose expert is not resident."""
+    L = load()
+    _check_cuda(x, "x", torch.bfloat16)
+    _check_cuda(topk_ids, "topk_ids", torch.int32)
+    _check_cuda(topk_weights, "topk_weights", torch.float32)
+    _check_cuda(slot_of_expert, "slot_of_expert", torch.int32)
+    if misses is not None:
+        _check_cuda(misses, "misses")
+    p = planes if isinstance(planes, Planes) else make_planes(planes)
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    need = cached_workspace_size(T, k, p.num_experts, p.hidden, p.inter)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    st = L.moe_w2_forward_cached(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), ctypes.byref(p), _ptr(slot_of_expert),
+                                 slot_of_expert.numel(), T, k, _ptr(y), _ptr(workspace), workspace.numel(),
+                                 _ptr(misses), _ptr(status), _stream(stream))
+    if st != OK:
+        raise MoeW2Error(st, "moe_w2_forward_cached")
+    return y
+
+
 def forward_noalloc(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, planes, y=None,
                     status=None, stream=None) -> torch.Tensor:
     """moe_w2_forward_noalloc: the forward with its scratch in the library's own device array
@@ -187,8 +229,9 @@ def permute(topk_ids: torch.Tensor, E: int, status=None, stream=None):
 
 
 def requant(e2m1: torch.Tensor, e4m3: torch.Tensor, scale_2: torch.Tensor, codes=None, ue8m0=None,
-            status=None, stream=None):
-    """NVFP4 [n][rows][K/2] + [n][rows][K/16] + [n] -> (codes [n][rows][K/4], ue8m0 [n][rows][K/32])."""
+            status=None, stream=None, options: int = 0):
+    """NVFP4 [n][rows][K/2] + [n][rows][K/16] + [n] -> (codes [n][rows][K/4], ue8m0 [n][rows][K/32]).
+    options: REQUANT_BALANCE_ZERO_SIGNS or 0 (moe_w2_requant_ex)."""
     L = load()
     _check_cuda(e2m1, "e2m1", torch.uint8)
     _check_cuda(e4m3, "e4m3", torch.uint8)
@@ -199,10 +242,31 @@ def requant(e2m1: torch.Tensor, e4m3: torch.Tensor, scale_2: torch.Tensor, codes
         codes = torch.empty((n, rows, K // 4), dtype=torch.uint8, device=e2m1.device)
     if ue8m0 is None:
         ue8m0 = torch.empty((n, rows, K // 32), dtype=torch.uint8, device=e2m1.device)
-    st = L.moe_w2_requant(_ptr(e2m1), _ptr(e4m3), _ptr(scale_2), n, rows, K, _ptr(codes), _ptr(ue8m0),
-                          _ptr(status), _stream(stream))
+    st = L.moe_w2_requant_ex(_ptr(e2m1), _ptr(e4m3), _ptr(scale_2), n, rows, K, options, _ptr(codes), _ptr(ue8m0),
+                             _ptr(status), _stream(stream))
     if st != OK:
-        raise MoeW2Error(st, "moe_w2_requant")
+        raise MoeW2Error(st, "moe_w2_requant_ex")
+    return codes, ue8m0
+
+
+def requant_mxfp4(e2m1: torch.Tensor, scales: torch.Tensor, codes=None, ue8m0=None, status=None, stream=None,
+                  options: int = 0):
+    """MXFP4: e2m1 [n][rows][K/2] + UE8M0 bytes [n][rows][K/32] -> (codes [n][rows][K/4], ue8m0 [n][rows][K/32])."""
+    L = load()
+    _check_cuda(e2m1, "e2m1", torch.uint8)
+    _check_cuda(scales, "scales", torch.uint8)
+    n, rows, half_k = e2m1.shape
+    K = half_k * 2
+    if tuple(scales.shape) != (n, rows, K // 32):
+        raise ValueError(f"scales must be [{n}][{rows}][{K // 32}], got {tuple(scales.shape)}")
+    if codes is None:
+        codes = torch.empty((n, rows, K // 4), dtype=torch.uint8, device=e2m1.device)
+    if ue8m0 is None:
+        ue8m0 = torch.empty((n, rows, K // 32), dtype=torch.uint8, device=e2m1.device)
+    st = L.moe_w2_requant_mxfp4(_ptr(e2m1), _ptr(scales), n, rows, K, options, _ptr(codes), _ptr(ue8m0),
+                                _ptr(status), _stream(stream))
+    if st != OK:
+        raise MoeW2Error(st, "moe_w2_requant_mxfp4")
     return codes, ue8m0
 
 

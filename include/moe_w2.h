@@ -79,6 +79,7 @@ typedef enum {
 #define MOE_W2_MAX_EXPERTS 1024
 #define MOE_W2_MAX_TOP_K 16
 #define MOE_W2_MAX_PAIRS (1 << 21)    /* T * top_k */
+#define MOE_W2_MAX_ROUTED_EXPERTS (1 << 20)   /* length of a residency table (moe_w2_forward_cached) */
 #define MOE_W2_DECODE_MAX_TOKENS 64   /* T <= 64 runs the decode kernels, larger T the prefill kernels */
 
 /* Device pointers to one layer's planes (layout above). */
@@ -151,7 +152,7 @@ moe_w2_status moe_w2_permute(const int32_t *topk_ids, int32_t T, int32_t top_k, 
  * as 0 (MOE_W2_DEV_BAD_SCALE).  T <= 64 uses the decode kernels, which stream
  * the planes of every active expert once per step: steps of more than 16 pairs
  * with H and I multiples of 512 a block-scaled tcgen05 kernel (codes expanded
- * to packed e2m1, activations as five packed e2m1 digit rows, both scaled by
+ * to packed e2m1, activations as eight packed e2m1 digit rows, both scaled by
  * UE8M0 bytes per 32 elements), the rest a bf16 mma.sync kernel; larger T the
  * prefill kernels (TMA + tcgen05 with accumulators in tensor memory).
  */
@@ -207,6 +208,35 @@ moe_w2_status moe_w2_forward_noalloc(const void *x_bf16, const int32_t *topk_ids
                                      uint32_t *dev_status, void *stream);
 
 /*
+ * moe_w2_forward behind an expert cache ("vLLM-Moet wiki", BASE-cache
+ * paragraph; "The v0.24.0 port", "Our hooks", BASE-cache bullet): w holds
+ * num_slots = w->num_experts resident experts, and a residency table says
+ * where each routed expert is.
+ *   slot_of_expert      int32 [num_routed_experts] (device): slot in
+ *                       [0, w->num_experts) of each routed expert id, or any
+ *                       negative value when that expert is not resident
+ *   num_routed_experts  length of the table, 1 .. MOE_W2_MAX_ROUTED_EXPERTS;
+ *                       topk_ids are routed ids in [0, num_routed_experts)
+ *   miss_counter        device uint32 (NULL = do not count): the call adds the
+ *                       number of pairs whose expert is not resident
+ *   workspace           at least moe_w2_forward_cached_workspace_size() bytes
+ * A pair whose expert is not resident contributes 0 to y and sets no status
+ * bit: its step can be replayed once the caller has loaded the missing experts.
+ * A routed id outside [0, num_routed_experts) or a table entry >= num_slots is
+ * an invalid id (contributes 0, MOE_W2_DEV_BAD_EXPERT_ID).  Every other
+ * argument, check and result is as for moe_w2_forward; in particular y for a
+ * step with every expert resident is bitwise identical to moe_w2_forward's
+ * with the same experts' planes at any slots, since each pair's result and the
+ * fixed j-order sum do not depend on where its expert sits.
+ */
+size_t moe_w2_forward_cached_workspace_size(int32_t T, int32_t top_k, int32_t num_slots, int32_t H, int32_t I);
+moe_w2_status moe_w2_forward_cached(const void *x_bf16, const int32_t *topk_ids, const float *topk_weights,
+                                    const moe_w2_planes *w, const int32_t *slot_of_expert,
+                                    int32_t num_routed_experts, int32_t T, int32_t top_k, void *y_bf16,
+                                    void *workspace, size_t workspace_bytes, uint32_t *miss_counter,
+                                    uint32_t *dev_status, void *stream);
+
+/*
  * Load-time re-quantizer ("The v0.24.0 port", "Our hooks", modelopt.py
  * bullet): modelopt NVFP4 tensors -> 2-bit planes.
  *   e2m1     uint8 [n][rows][K/2]   two e2m1 nibbles per byte, low nibble = even element
@@ -224,6 +254,45 @@ moe_w2_status moe_w2_forward_noalloc(const void *x_bf16, const int32_t *topk_ids
 moe_w2_status moe_w2_requant(const uint8_t *e2m1, const uint8_t *e4m3, const float *scale_2,
                              int64_t n, int64_t rows, int64_t K, uint8_t *codes, uint8_t *ue8m0,
                              uint32_t *dev_status, void *stream);
+
+/*
+ * Option bits of the FP4 loaders (moe_w2_requant_ex, moe_w2_requant_mxfp4).
+ * MOE_W2_REQUANT_BALANCE_ZERO_SIGNS ("vLLM-Moet wiki", the Kimi-K2.7
+ * paragraph: an export that writes every exact zero as +0 would bias the
+ * codes): the elements of a block that are exactly zero get the signs
+ * +,-,+,- ... in element order (the first zero of the block +1, the second -1,
+ * ...) instead of their stored sign bits.  A zero is at magnitude 1 for every
+ * scale, so the scale byte and every other code are unchanged.  Other bits are
+ * reserved: a call with one of them set returns MOE_W2_ERR_INVALID_ARG.
+ */
+#define MOE_W2_REQUANT_BALANCE_ZERO_SIGNS 1u
+
+/* moe_w2_requant with option bits (options = 0: identical to moe_w2_requant). */
+moe_w2_status moe_w2_requant_ex(const uint8_t *e2m1, const uint8_t *e4m3, const float *scale_2,
+                                int64_t n, int64_t rows, int64_t K, uint32_t options, uint8_t *codes,
+                                uint8_t *ue8m0, uint32_t *dev_status, void *stream);
+
+/*
+ * Load-time re-quantizer for MXFP4 checkpoints ("The v0.24.0 port", "Our
+ * hooks", mxfp4.py bullet; "vLLM-Moet wiki": FP4 experts load by a codes
+ * remap): e2m1 elements with one UE8M0 scale byte per 32 -> 2-bit planes.
+ *   e2m1    uint8 [n][rows][K/2]    two nibbles per byte, low nibble = even element
+ *   scales  uint8 [n][rows][K/32]   UE8M0 bytes s, element value e2m1 * 2^(s-127)
+ *   codes   uint8 [n][rows][K/4]    output codes (plane format above)
+ *   ue8m0   uint8 [n][rows][K/32]   output UE8M0 bytes
+ *   options MOE_W2_REQUANT_BALANCE_ZERO_SIGNS or 0
+ * Same rule as moe_w2_requant (least squared error over u in [-126,125],
+ * nearest code, ties to magnitude 1 and to the smaller u, -0 -> -1).  Because
+ * the input scale is a power of two, the codes depend only on the block's
+ * e2m1 codes and the output byte is the input byte plus a shift that also
+ * depends only on them, except where the exponent range [-126,125] cuts the
+ * search.  Bit-exact.  Scale byte 255 (NaN) makes the block invalid: codes
+ * 0x00, scale byte 0, MOE_W2_DEV_BAD_NVFP4.  K must be a multiple of 32; e2m1
+ * 16-byte aligned, codes 8-byte aligned.
+ */
+moe_w2_status moe_w2_requant_mxfp4(const uint8_t *e2m1, const uint8_t *scales, int64_t n, int64_t rows, int64_t K,
+                                   uint32_t options, uint8_t *codes, uint8_t *ue8m0, uint32_t *dev_status,
+                                   void *stream);
 
 /*
  * Test hook for the pipeline-timeout report; the pages describe no such entry

@@ -72,6 +72,10 @@ def lib(parallel: bool = False):
             L.oracle_requant.restype = u32
             L.oracle_requant_blocks.argtypes = [vp, vp, vp, i64, i64, vp, i64, vp, vp]
             L.oracle_requant_blocks.restype = u32
+            L.oracle_requant_ex.argtypes = [vp, vp, vp, i64, i64, i64, u32, vp, vp]
+            L.oracle_requant_ex.restype = u32
+            L.oracle_requant_mxfp4.argtypes = [vp, vp, i64, i64, i64, u32, vp, vp]
+            L.oracle_requant_mxfp4.restype = u32
             L.oracle_requant_fp8.argtypes = [vp, vp, i64, i64, i64, vp, vp]
             L.oracle_requant_fp8.restype = u32
             L.oracle_permute.argtypes = [vp, i64, i32, i32, vp, vp, vp]
@@ -79,6 +83,9 @@ def lib(parallel: bool = False):
             L.oracle_forward_tokens.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                 vp, i64, vp, vp]
             L.oracle_forward_tokens.restype = u32
+            L.oracle_forward_tokens_cached.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                       vp, i64, vp, vp, vp]
+            L.oracle_forward_tokens_cached.restype = u32
             _libs[parallel] = L
     return _libs[parallel]
 
@@ -108,7 +115,10 @@ def bf16_to_double(h: int) -> float:
     return lib().oracle_bf16_to_double(h)
 
 
-def requant(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray, parallel: bool = False):
+BALANCE_ZERO_SIGNS = 1   # option bit of the FP4 loaders: exact zeros take alternating signs
+
+
+def requant(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray, parallel: bool = False, options: int = 0):
     """e2m1 uint8 [n][rows][K/2], e4m3 uint8 [n][rows][K/16], scale_2 float32 [n]."""
     n, rows, half_k = e2m1.shape
     K = half_k * 2
@@ -117,8 +127,21 @@ def requant(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray, parallel: b
     s2 = np.ascontiguousarray(scale_2, dtype=np.float32)
     codes = np.empty((n, rows, K // 4), np.uint8)
     scales = np.empty((n, rows, K // 32), np.uint8)
-    st = lib(parallel).oracle_requant(_p(e2m1), _p(e4m3), _p(s2), n, rows, K, _p(codes), _p(scales))
+    st = lib(parallel).oracle_requant_ex(_p(e2m1), _p(e4m3), _p(s2), n, rows, K, options, _p(codes), _p(scales))
     return codes, scales, int(st)
+
+
+def requant_mxfp4(e2m1: np.ndarray, scales: np.ndarray, parallel: bool = False, options: int = 0):
+    """MXFP4: e2m1 uint8 [n][rows][K/2], UE8M0 scale bytes uint8 [n][rows][K/32]."""
+    n, rows, half_k = e2m1.shape
+    K = half_k * 2
+    e2m1 = np.ascontiguousarray(e2m1)
+    sc = np.ascontiguousarray(scales, dtype=np.uint8)
+    assert sc.shape == (n, rows, K // 32)
+    codes = np.empty((n, rows, K // 4), np.uint8)
+    ue8m0 = np.empty((n, rows, K // 32), np.uint8)
+    st = lib(parallel).oracle_requant_mxfp4(_p(e2m1), _p(sc), n, rows, K, options, _p(codes), _p(ue8m0))
+    return codes, ue8m0, int(st)
 
 
 def requant_blocks(e2m1: np.ndarray, e4m3: np.ndarray, scale_2: np.ndarray, block_ids, parallel: bool = False):
@@ -175,6 +198,29 @@ def forward_tokens(x: np.ndarray, ids: np.ndarray, weights: np.ndarray, planes: 
         _p(planes["w13_codes"]), _p(planes["w13_scales"]), _p(planes["w2_codes"]), _p(planes["w2_scales"]),
         E, H, I, k, _p(tok), len(tok), _p(y), _p(h) if want_h else None)
     return (y, h, int(st)) if want_h else (y, int(st))
+
+
+def forward_tokens_cached(x: np.ndarray, ids: np.ndarray, weights: np.ndarray, planes: dict, slot_of: np.ndarray,
+                          tokens=None, want_h: bool = False, parallel: bool = False):
+    """The forward behind an expert cache: planes hold the resident slots, slot_of int32 [n_route]
+    maps routed ids to slots (negative: not resident).  -> (y, [h,] status, misses)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    weights = np.ascontiguousarray(weights, dtype=np.float32)
+    slot_of = np.ascontiguousarray(slot_of, dtype=np.int32)
+    T, H = x.shape
+    k = ids.shape[1]
+    E, two_i, _ = planes["w13_codes"].shape
+    I = two_i // 2
+    tok = np.arange(T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
+    y = np.empty((len(tok), H), np.uint16)
+    h = np.empty((len(tok), k, I), np.uint16) if want_h else None
+    misses = np.zeros(1, np.int64)
+    st = lib(parallel).oracle_forward_tokens_cached(
+        _p(x), _p(ids), _p(weights), _p(slot_of), len(slot_of),
+        _p(planes["w13_codes"]), _p(planes["w13_scales"]), _p(planes["w2_codes"]), _p(planes["w2_scales"]),
+        E, H, I, k, _p(tok), len(tok), _p(y), _p(h) if want_h else None, _p(misses))
+    return (y, h, int(st), int(misses[0])) if want_h else (y, int(st), int(misses[0]))
 
 
 def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:

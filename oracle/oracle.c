@@ -39,6 +39,23 @@
  *      the router weight multiplies the down projection; y = bf16(sum over j in
  *      j order); all sums in f64.  Expert ids outside [0,E) contribute nothing
  *      (status bit 1); a UE8M0 byte outside [1,252] zeroes its block (bit 2).
+ *   R9 expert cache ("vLLM-Moet wiki", BASE-cache paragraph; "The v0.24.0 port",
+ *      "Our hooks", BASE-cache bullet): the planes hold S slots and a table maps
+ *      each routed id in [0, n_route) to its slot, negative when the expert is
+ *      not resident.  A missing expert's pair contributes nothing and is counted
+ *      (no status bit); an id outside [0, n_route) or a slot >= S is an invalid
+ *      id (bit 1).
+ *   R10 MXFP4 checkpoints ("vLLM-Moet wiki": FP4 experts load by a codes remap;
+ *      "The v0.24.0 port", "Our hooks", mxfp4.py bullet): e2m1 elements with
+ *      one UE8M0 scale byte per 32, x_i = e2m1_i * 2^(s-127), byte 255 = NaN
+ *      (invalid block, bit 4).  The planes follow the same rule as R3/R4; as
+ *      the scale is a power of two the codes depend on the e2m1 codes alone and
+ *      the output byte is the input byte shifted, hence "remap".
+ *   R11 zero-sign balancing (page "vLLM-Moet wiki", the Kimi-K2.7 paragraph: an
+ *      export that writes every exact zero as +0 biases the codes): with the
+ *      option on, the exact zeros of a block take the signs +,-,+,- ... in
+ *      element order instead of their sign bits; nothing else changes (a zero
+ *      is at magnitude 1 for every u, so the scale search does not see it).
  */
 #include <math.h>
 #include <stdint.h>
@@ -144,14 +161,16 @@ uint16_t oracle_bf16_from_double(double v)
  * significant bits, here at most 30) -> 8 code bytes and one UE8M0 byte, by
  * readings R3 and R4.  Shared by the NVFP4 and FP8 loaders, which differ only
  * in how they dequantise. */
-static void search_block(const double *x, uint8_t *codes_out, uint8_t *scale_out)
+static void search_block(const double *x, int balance_zeros, uint8_t *codes_out, uint8_t *scale_out)
 {
     double a[32];
     int neg[32];
     double amax = 0.0, min_nz = INFINITY;
+    int zeros = 0;
     for (int i = 0; i < 32; ++i) {
         neg[i] = signbit(x[i]) ? 1 : 0;
         a[i] = fabs(x[i]);
+        if (balance_zeros && a[i] == 0.0) neg[i] = (zeros++) & 1;   /* reading R11 */
         if (a[i] > amax) amax = a[i];
         if (a[i] > 0.0 && a[i] < min_nz) min_nz = a[i];
     }
@@ -229,7 +248,7 @@ static void search_block(const double *x, uint8_t *codes_out, uint8_t *scale_out
 }
 
 /* One block of 32 NVFP4 elements -> 8 code bytes and one UE8M0 byte. */
-static uint32_t requant_block(const uint8_t *nib_bytes, const uint8_t *e4m3_pair, float scale_2,
+static uint32_t requant_block(const uint8_t *nib_bytes, const uint8_t *e4m3_pair, float scale_2, int balance,
                               uint8_t *codes_out, uint8_t *scale_out)
 {
     double s2 = (double)scale_2;
@@ -245,7 +264,25 @@ static uint32_t requant_block(const uint8_t *nib_bytes, const uint8_t *e4m3_pair
         unsigned nib = (nib_bytes[i / 2] >> (4 * (i % 2))) & 0xFu;
         x[i] = oracle_e2m1_value(nib) * sc[i / 16] * s2;
     }
-    search_block(x, codes_out, scale_out);
+    search_block(x, balance, codes_out, scale_out);
+    return 0;
+}
+
+/* One block of 32 MXFP4 elements (reading R10) -> 8 code bytes and one UE8M0 byte. */
+static uint32_t requant_block_mx(const uint8_t *nib_bytes, uint8_t s, int balance, uint8_t *codes_out,
+                                 uint8_t *scale_out)
+{
+    if (s == 0xFFu) {
+        memset(codes_out, 0, 8);
+        *scale_out = 0;
+        return ORACLE_BAD_NVFP4;
+    }
+    double x[32];
+    for (int i = 0; i < 32; ++i) {
+        unsigned nib = (nib_bytes[i / 2] >> (4 * (i % 2))) & 0xFu;
+        x[i] = ldexp(oracle_e2m1_value(nib), (int)s - 127);   /* exact */
+    }
+    search_block(x, balance, codes_out, scale_out);
     return 0;
 }
 
@@ -269,21 +306,46 @@ static uint32_t requant_block_fp8(const uint8_t *e4m3_bytes, float scale, uint8_
         *scale_out = 0;
         return ORACLE_BAD_NVFP4;
     }
-    search_block(x, codes_out, scale_out);
+    search_block(x, 0, codes_out, scale_out);
     return 0;
 }
 
+/* Option bit of the FP4 loaders: reading R11. */
+#define ORACLE_BALANCE_ZERO_SIGNS 1u
+
 /* Whole tensors: e2m1 [n][rows][K/2], e4m3 [n][rows][K/16], scale_2 [n]
  * -> codes [n][rows][K/4], ue8m0 [n][rows][K/32].  Returns status bits. */
-uint32_t oracle_requant(const uint8_t *e2m1, const uint8_t *e4m3, const float *scale_2,
-                        int64_t n, int64_t rows, int64_t K, uint8_t *codes, uint8_t *ue8m0)
+uint32_t oracle_requant_ex(const uint8_t *e2m1, const uint8_t *e4m3, const float *scale_2,
+                           int64_t n, int64_t rows, int64_t K, uint32_t options, uint8_t *codes, uint8_t *ue8m0)
 {
     if (K % 32 != 0) return 0x80000000u;
     uint32_t st = 0;
     int64_t blocks_per_tensor = rows * (K / 32);
+    int balance = (options & ORACLE_BALANCE_ZERO_SIGNS) != 0;
     ORACLE_PARALLEL_FOR_BLOCKS
     for (int64_t g = 0; g < n * blocks_per_tensor; ++g)
-        st |= requant_block(e2m1 + g * 16, e4m3 + g * 2, scale_2[g / blocks_per_tensor], codes + g * 8, ue8m0 + g);
+        st |= requant_block(e2m1 + g * 16, e4m3 + g * 2, scale_2[g / blocks_per_tensor], balance, codes + g * 8,
+                            ue8m0 + g);
+    return st;
+}
+
+uint32_t oracle_requant(const uint8_t *e2m1, const uint8_t *e4m3, const float *scale_2,
+                        int64_t n, int64_t rows, int64_t K, uint8_t *codes, uint8_t *ue8m0)
+{
+    return oracle_requant_ex(e2m1, e4m3, scale_2, n, rows, K, 0u, codes, ue8m0);
+}
+
+/* MXFP4 tensors (reading R10): e2m1 [n][rows][K/2], UE8M0 scales [n][rows][K/32]
+ * -> codes [n][rows][K/4], ue8m0 [n][rows][K/32].  Returns status bits. */
+uint32_t oracle_requant_mxfp4(const uint8_t *e2m1, const uint8_t *scales, int64_t n, int64_t rows, int64_t K,
+                              uint32_t options, uint8_t *codes, uint8_t *ue8m0)
+{
+    if (K % 32 != 0) return 0x80000000u;
+    uint32_t st = 0;
+    int balance = (options & ORACLE_BALANCE_ZERO_SIGNS) != 0;
+    ORACLE_PARALLEL_FOR_BLOCKS
+    for (int64_t g = 0; g < n * rows * (K / 32); ++g)
+        st |= requant_block_mx(e2m1 + g * 16, scales[g], balance, codes + g * 8, ue8m0 + g);
     return st;
 }
 
@@ -298,7 +360,7 @@ uint32_t oracle_requant_blocks(const uint8_t *e2m1, const uint8_t *e4m3, const f
     ORACLE_PARALLEL_FOR_BLOCKS
     for (int64_t i = 0; i < nb; ++i) {
         int64_t g = block_ids[i];
-        st |= requant_block(e2m1 + g * 16, e4m3 + g * 2, scale_2[g / blocks_per_tensor],
+        st |= requant_block(e2m1 + g * 16, e4m3 + g * 2, scale_2[g / blocks_per_tensor], 0,
                             codes + i * 8, ue8m0 + i);
     }
     return st;
@@ -376,7 +438,20 @@ static double dot(const double *a, const double *b, int64_t n)
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
 /* y of token t: y_out bf16 [H]; h_out (nullable) bf16 [k][I]. */
+/* Slot of a routed id under reading R9 (slot_of NULL: the id is the slot).
+ * Returns the slot, -1 for a missing expert, -2 for an invalid id. */
+static int32_t slot_of_pair(int32_t e, const int32_t *slot_of, int32_t n_route, int32_t S)
+{
+    if (slot_of) {
+        if (e < 0 || e >= n_route) return -2;
+        e = slot_of[e];
+        if (e < 0) return -1;
+    }
+    return (e >= 0 && e < S) ? e : -2;
+}
+
 static uint32_t forward_token(const uint16_t *x, const int32_t *ids, const float *weights,
+                              const int32_t *slot_of, int32_t n_route,
                               const uint8_t *w13_codes, const uint8_t *w13_scales,
                               const uint8_t *w2_codes, const uint8_t *w2_scales,
                               int32_t E, int32_t H, int32_t I, int32_t k, int64_t t,
@@ -389,10 +464,11 @@ static uint32_t forward_token(const uint16_t *x, const int32_t *ids, const float
     for (int32_t i = 0; i < H; ++i) xt[i] = oracle_bf16_to_double(x[t * H + i]);
     for (int32_t m = 0; m < H; ++m) acc[m] = 0.0;
     for (int32_t j = 0; j < k; ++j) {
-        int32_t e = ids[t * k + j];
+        int32_t e = slot_of_pair(ids[t * k + j], slot_of, n_route, E);
         if (h_out)
             for (int32_t n = 0; n < I; ++n) h_out[(int64_t)j * I + n] = 0;
-        if (e < 0 || e >= E) {
+        if (e == -1) continue;   /* not resident: contributes nothing */
+        if (e < 0) {
             st |= ORACLE_BAD_EXPERT_ID;
             continue;
         }
@@ -433,7 +509,34 @@ uint32_t oracle_forward_tokens(const uint16_t *x, const int32_t *ids, const floa
     uint32_t st = 0;
     ORACLE_PARALLEL_FOR_TOKENS
     for (int64_t it = 0; it < ntok; ++it)
-        st |= forward_token(x, ids, weights, w13_codes, w13_scales, w2_codes, w2_scales, E, H, I, k, tokens[it],
-                            y_out + it * H, h_out ? h_out + it * k * (int64_t)I : NULL);
+        st |= forward_token(x, ids, weights, NULL, 0, w13_codes, w13_scales, w2_codes, w2_scales, E, H, I, k,
+                            tokens[it], y_out + it * H, h_out ? h_out + it * k * (int64_t)I : NULL);
+    return st;
+}
+
+/* The same behind an expert cache (reading R9): planes of S = E slots, slot_of
+ * [n_route].  *misses (nullable) = pairs of the listed tokens whose expert is
+ * not resident. */
+uint32_t oracle_forward_tokens_cached(const uint16_t *x, const int32_t *ids, const float *weights,
+                                      const int32_t *slot_of, int32_t n_route,
+                                      const uint8_t *w13_codes, const uint8_t *w13_scales,
+                                      const uint8_t *w2_codes, const uint8_t *w2_scales,
+                                      int32_t E, int32_t H, int32_t I, int32_t k,
+                                      const int64_t *tokens, int64_t ntok, uint16_t *y_out, uint16_t *h_out,
+                                      int64_t *misses)
+{
+    if (H % 32 || I % 32 || !slot_of) return 0x80000000u;
+    uint32_t st = 0;
+    ORACLE_PARALLEL_FOR_TOKENS
+    for (int64_t it = 0; it < ntok; ++it)
+        st |= forward_token(x, ids, weights, slot_of, n_route, w13_codes, w13_scales, w2_codes, w2_scales, E, H, I,
+                            k, tokens[it], y_out + it * H, h_out ? h_out + it * k * (int64_t)I : NULL);
+    if (misses) {
+        int64_t m = 0;
+        for (int64_t it = 0; it < ntok; ++it)
+            for (int32_t j = 0; j < k; ++j)
+                m += slot_of_pair(ids[tokens[it] * k + j], slot_of, n_route, E) == -1;
+        *misses = m;
+    }
     return st;
 }

@@ -3,15 +3,18 @@
 TEST INFRASTRUCTURE ONLY.  Independent of ``oracle.c``: it follows the plain
 definition with no candidate window and no integer tricks.
 
-Definition followed (page "The v0.24.0 port", section "Our hooks", modelopt.py
-and fp8.py bullets; page "vLLM-Moet wiki", section "2-bit expert planes"): each
-NVFP4 element is e2m1 x e4m3 x scale_2 and each FP8 element e4m3 x its f32
-128 x 128 block scale, an exact rational number; a block of 32 is
+Definition followed (page "The v0.24.0 port", section "Our hooks", modelopt.py,
+fp8.py and mxfp4.py bullets; page "vLLM-Moet wiki", section "2-bit expert
+planes"): each NVFP4 element is e2m1 x e4m3 x scale_2, each FP8 element e4m3 x
+its f32 128 x 128 block scale and each MXFP4 element e2m1 x 2^(s-127), an
+exact rational number; a block of 32 is
 re-quantized to codes from {-4,-1,1,4} times one UE8M0 scale 2^u, u in
 [-126,125], minimising the squared error.  With the scale fixed the error
 separates per element, so for every u each element takes its nearest code;
 exact ties between codes go to magnitude 1, exact ties between scales to the
-smaller u, and the code's sign is the element's sign bit.
+smaller u, and the code's sign is the element's sign bit.  With zero-sign
+balancing (page "vLLM-Moet wiki", the Kimi-K2.7 paragraph) the exact zeros of
+the block take the signs +,-,+,- ... in element order instead.
 """
 from __future__ import annotations
 
@@ -45,7 +48,7 @@ def f32(v: float) -> Fraction:
     return Fraction(v)
 
 
-def requant_block(nibbles, e4m3_pair, scale_2: float):
+def requant_block(nibbles, e4m3_pair, scale_2: float, balance: bool = False):
     """nibbles: 32 ints; e4m3_pair: 2 bytes; -> (codes[32], scale byte) or None when invalid."""
     sc = [e4m3(b) for b in e4m3_pair]
     if any(s is None for s in sc) or not (scale_2 > 0) or scale_2 == float("inf"):
@@ -57,11 +60,26 @@ def requant_block(nibbles, e4m3_pair, scale_2: float):
         s_neg, s_mag = sc[i // 16]
         neg.append(n_neg != s_neg)
         mag.append(n_mag * s_mag * s2)
-    return _search(neg, mag)
+    return _search(neg, mag, balance)
 
 
-def _search(neg, mag):
+def requant_block_mx(nibbles, scale_byte: int, balance: bool = False):
+    """MXFP4: 32 e2m1 nibbles under one UE8M0 byte -> (codes[32], scale byte), or None for byte 255."""
+    if int(scale_byte) == 255:
+        return None
+    step = Fraction(2) ** (int(scale_byte) - 127)
+    vals = [e2m1(n) for n in nibbles]
+    return _search([n for n, _ in vals], [m * step for _, m in vals], balance)
+
+
+def _search(neg, mag, balance: bool = False):
     """(codes[32], scale byte) minimising the exact squared error over all u."""
+    if balance:
+        neg, z = list(neg), 0
+        for i, a in enumerate(mag):
+            if a == 0:
+                neg[i] = bool(z & 1)
+                z += 1
     best = None
     for u in range(-126, 126):
         step = Fraction(2) ** u

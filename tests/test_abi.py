@@ -99,3 +99,37 @@ def test_forward_path_names_the_kernels_a_call_runs():
     assert P.forward_path(4, 2, 8, 500, 256) == P.PATH_NONE                       # invalid H
     assert P.decode_kernel(1, 8, 6144, 2048) == "decode_mma_kernel"
     assert P.decode_kernel(32, 8, 6144, 2048) == "decode_layer_kernel"
+
+
+def test_cached_forward_host_checks():
+    """moe_w2_forward_cached: table length and pointer checks, and a workspace
+    that covers the per-pair slot ids (checked before any device access)."""
+    L = moe_w2.load()
+    A = 0x10000000
+    p = moe_w2.Planes(A, A + 0x1000, A + 0x2000, A + 0x3000, 8, 512, 256)
+    need = moe_w2.cached_workspace_size(2, 2, 8, 512, 256)
+    assert need >= moe_w2.workspace_size(2, 2, 8, 512, 256) + 4 * 4
+    assert moe_w2.cached_workspace_size(4, 2, 8, 500, 256) == 0
+
+    def fwd(table=A + 0x400000, n_route=300, nbytes=need, T=2):
+        return L.moe_w2_forward_cached(A, A, A, ctypes.byref(p), table, n_route, T, 2, A + 0x100000, A + 0x200000,
+                                       nbytes, None, None, None)
+
+    assert fwd(n_route=0) == 1                          # empty table
+    assert fwd(n_route=(1 << 20) + 1) == 1              # longer than the library takes
+    assert fwd(table=None) == 1                         # no table
+    assert fwd(nbytes=need - 1) == 3                    # no room for the slot ids
+    assert fwd(table=None, T=0) == 0                    # T = 0 is a no-op
+
+
+def test_fp4_loader_options_host_checks():
+    L = moe_w2.load()
+    A = 0x10000000
+    # reserved option bits are refused before any device access
+    assert L.moe_w2_requant_ex(A, A, A, 1, 4, 64, 2, A, A, None, None) == 1
+    assert L.moe_w2_requant_mxfp4(A, A, 1, 4, 64, 0x80, A, A, None, None) == 1
+    # MXFP4: K not a multiple of 32, misaligned e2m1 and codes, the empty call
+    assert L.moe_w2_requant_mxfp4(A, A, 1, 4, 48, 0, A, A, None, None) == 2
+    assert L.moe_w2_requant_mxfp4(A + 8, A, 1, 4, 64, 0, A, A, None, None) == 1
+    assert L.moe_w2_requant_mxfp4(A, A, 1, 4, 64, 0, A + 4, A, None, None) == 1
+    assert L.moe_w2_requant_mxfp4(None, None, 0, 4, 64, 1, None, None, None, None) == 0

@@ -51,10 +51,10 @@ from bit_moe_expert_w2_gb300 import inputs  # noqa: E402
 
 METRIC = "w2 MoE layer tokens/s; plane HBM GB/s (decode), TFLOP/s (prefill) vs peak"
 DEFAULT_CONFIG = "decode_t1"
-EXTRA_CONFIGS = ("decode_t32", "prefill_t8192", "requant_256", "requant_fp8_16")
+EXTRA_CONFIGS = ("decode_t32", "prefill_t8192", "requant_256", "requant_fp8_16", "requant_mxfp4_16")
 DEFAULT_STEPS = {"decode_t1": 4000, "decode_t32": 1000, "prefill_t8192": 100, "requant_256": 10,
                  "decode_t1_e32": 4000, "prefill_t1024_e32": 400}
-EXTRA_STEPS = {"decode_t32": 500, "prefill_t8192": 50, "requant_256": 5, "requant_fp8_16": 5}
+EXTRA_STEPS = {"decode_t32": 500, "prefill_t8192": 50, "requant_256": 5, "requant_fp8_16": 5, "requant_mxfp4_16": 5}
 POOL = 16
 # every file each kernel's translation unit compiles: a capture is stale once any changed
 KERNEL_SOURCES = {
@@ -276,16 +276,21 @@ def oracle_requant_rate_all_cores(gu: inputs.Nvfp4Tensors, budget_s: float):
             return done_el / el, i, el, threads
 
 
-def oracle_requant_fp8_rate(gu: inputs.Fp8Tensors, budget_s: float, parallel: bool = False):
-    """Elements/s of the oracle FP8 requant on whole tensors in turn (single thread, or all threads)."""
+def oracle_requant_fp8_rate(gu, budget_s: float, parallel: bool = False):
+    """Elements/s of the oracle FP8 or MXFP4 requant on whole tensors in turn (single thread, or all threads)."""
     import oracle
     threads = oracle.threads(parallel=True) if parallel else 1
     done_el, t0, i = 0, time.perf_counter(), 0
-    n = gu.w8.shape[0]
+    mx = isinstance(gu, inputs.Mxfp4Tensors)
+    n = gu.e2m1.shape[0] if mx else gu.w8.shape[0]
     while True:
         sl = slice(i % n, i % n + 1)
-        oracle.requant_fp8(gu.w8[sl], gu.scales[sl], parallel=parallel)
-        done_el += gu.w8[sl].size
+        if mx:
+            oracle.requant_mxfp4(gu.e2m1[sl], gu.scales[sl], parallel=parallel)
+            done_el += gu.e2m1[sl].size * 2
+        else:
+            oracle.requant_fp8(gu.w8[sl], gu.scales[sl], parallel=parallel)
+            done_el += gu.w8[sl].size
         i += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -673,22 +678,33 @@ def requant_bench(name, steps, warmup, world, rank, local):
     return res, gu
 
 
-def requant_fp8_bench(name, steps, warmup, world, rank, local):
+def loader_bench(name, steps, warmup, world, rank, local):
+    """The FP8 block-128 and MXFP4 loaders on their 16-expert workloads."""
     import torch
     from bit_moe_expert_w2_gb300 import moe_w2
     dev = torch.device("cuda", local)
-    gu, dn = inputs.requant_fp8_inputs(experts=inputs.REQUANT_FP8_CASES[name])
-    dt = [(torch.from_numpy(t.w8).to(dev), torch.from_numpy(t.scales).to(dev)) for t in (gu, dn)]
-    outs = [(torch.empty((t.w8.shape[0], t.w8.shape[1], t.w8.shape[2] // 4), dtype=torch.uint8, device=dev),
-             torch.empty((t.w8.shape[0], t.w8.shape[1], t.w8.shape[2] // 32), dtype=torch.uint8, device=dev))
-            for t in (gu, dn)]
+    fp8 = name in inputs.REQUANT_FP8_CASES
+    if fp8:
+        gu, dn = inputs.requant_fp8_inputs(experts=inputs.REQUANT_FP8_CASES[name])
+        arrays = [(t.w8, t.scales) for t in (gu, dn)]
+        K_of = lambda a: a.shape[2]
+        call, kernel = moe_w2.requant_fp8, "requant_fp8_kernel"
+    else:
+        gu, dn = inputs.requant_mxfp4_inputs(experts=inputs.REQUANT_MXFP4_CASES[name])
+        arrays = [(t.e2m1, t.scales) for t in (gu, dn)]
+        K_of = lambda a: a.shape[2] * 2
+        call, kernel = moe_w2.requant_mxfp4, "requant_kernel"
+    dt = [(torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev)) for a, b in arrays]
+    outs = [(torch.empty((a.shape[0], a.shape[1], K_of(a) // 4), dtype=torch.uint8, device=dev),
+             torch.empty((a.shape[0], a.shape[1], K_of(a) // 32), dtype=torch.uint8, device=dev))
+            for a, _ in arrays]
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
     def step():
-        for (w8, sc), (c, u) in zip(dt, outs):
-            moe_w2.requant_fp8(w8, sc, codes=c, ue8m0=u, status=status, stream=stream)
+        for (w, sc), (c, u) in zip(dt, outs):
+            call(w, sc, codes=c, ue8m0=u, status=status, stream=stream)
 
     clk = ClockSampler(ClockSampler.device_id_of(dev)).start()
     clk.wait_first()
@@ -714,18 +730,18 @@ def requant_fp8_bench(name, steps, warmup, world, rank, local):
     t_timed1 = time.time()
     clk.stop()
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world)
-    elems = gu.w8.size + dn.w8.size
-    moved = elems + 4 * (gu.scales.size + dn.scales.size) + elems // 4 + elems // 32
+    elems = sum(a.shape[0] * a.shape[1] * K_of(a) for a, _ in arrays)
+    moved = sum(a.nbytes + b.nbytes for a, b in arrays) + elems // 4 + elems // 32
     pk = peaks()
     gbs = moved * steps / (ms / 1e3) / 1e9
     res = {"ms_per_step": ms / steps, "value": world * elems * steps / (ms / 1e3), "unit": "elements/s",
-           "roofline": {"kernel": "requant_fp8_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+           "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1),
                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
-                        "peak_source": pk["source"], "traffic": ncu_traffic("requant_fp8_kernel", name),
+                        "peak_source": pk["source"], "traffic": ncu_traffic(kernel, name),
                         "algorithmic_bytes_per_step": int(moved)},
            "clocks": clk.summary(t_timed0, t_timed1, warm0), "gpu_launches": 2 * steps, "dtype": "int64 (exact)"}
-    # end to end: FP8 tensors from pinned host memory, requant, planes back to pinned host memory
-    hin = [(torch.from_numpy(t.w8).pin_memory(), torch.from_numpy(t.scales).pin_memory()) for t in (gu, dn)]
+    # end to end: the input tensors from pinned host memory, requant, planes back to pinned host memory
+    hin = [(torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory()) for a, b in arrays]
     hout = [(torch.empty(c.shape, dtype=torch.uint8).pin_memory(), torch.empty(u.shape, dtype=torch.uint8).pin_memory())
             for c, u in outs]
     e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
@@ -733,8 +749,8 @@ def requant_fp8_bench(name, steps, warmup, world, rank, local):
         for e0, e1 in e_evs:
             flush.zero_()
             e0.record(stream)
-            for (w8, sc), (hw, hs) in zip(dt, hin):
-                w8.copy_(hw, non_blocking=True)
+            for (w, sc), (hw, hs) in zip(dt, hin):
+                w.copy_(hw, non_blocking=True)
                 sc.copy_(hs, non_blocking=True)
             step()
             for (c, u), (hc, hu) in zip(outs, hout):
@@ -747,13 +763,13 @@ def requant_fp8_bench(name, steps, warmup, world, rank, local):
                   "h2d_bytes_per_step": int(sum(a.nbytes + b.nbytes for a, b in hin)),
                   "d2h_bytes_per_step": int(sum(a.nbytes + b.nbytes for a, b in hout))}
     if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} during the FP8 requant benchmark")
+        raise RuntimeError(f"device status {int(status.item())} during the {name} benchmark")
     return res, gu
 
 
 def cpu_baseline(name, data, budget_s):
     """The oracle on this host: one core (the reported value) and all cores."""
-    if name in inputs.REQUANT_FP8_CASES:
+    if name in inputs.REQUANT_FP8_CASES or name in inputs.REQUANT_MXFP4_CASES:
         v, n, el, _ = oracle_requant_fp8_rate(data, budget_s)
         va, na, ela, thr = oracle_requant_fp8_rate(data, budget_s / 2, parallel=True)
         return {"value": round(v, 1), "unit": "elements/s", "cores": 1, "kind": "oracle",
@@ -777,8 +793,8 @@ def cpu_baseline(name, data, budget_s):
 
 def run_config(name, steps, warmup, world, rank, local):
     """(result dict, oracle input) of one workload."""
-    if name in inputs.REQUANT_FP8_CASES:
-        return requant_fp8_bench(name, steps, warmup, world, rank, local)
+    if name in inputs.REQUANT_FP8_CASES or name in inputs.REQUANT_MXFP4_CASES:
+        return loader_bench(name, steps, warmup, world, rank, local)
     if name in inputs.REQUANT_CASES:
         res, data = requant_bench(name, steps, warmup, world, rank, local)
         res["unit"] = "elements/s"
@@ -794,7 +810,8 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=None,
-                    choices=[*inputs.CONFIGS, *inputs.REQUANT_CASES, *inputs.REQUANT_FP8_CASES],
+                    choices=[*inputs.CONFIGS, *inputs.REQUANT_CASES, *inputs.REQUANT_FP8_CASES,
+                             *inputs.REQUANT_MXFP4_CASES],
                     help=f"one workload only (default: {DEFAULT_CONFIG}, plus {', '.join(EXTRA_CONFIGS)} on one GPU)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of single-core oracle work per workload")
@@ -851,6 +868,11 @@ def workload_name(config: str) -> str:
         n = inputs.REQUANT_FP8_CASES[config]
         return (f"{config}: {n} experts FP8 (e4m3, f32 128x128 block scales) gate/up 2x[{r.inter}x{r.hidden}] + "
                 f"down [{r.hidden}x{r.inter}] -> 2-bit planes")
+    if config in inputs.REQUANT_MXFP4_CASES:
+        r = inputs.REQUANT
+        n = inputs.REQUANT_MXFP4_CASES[config]
+        return (f"{config}: {n} experts MXFP4 (e2m1, UE8M0 block-32 scales) gate/up 2x[{r.inter}x{r.hidden}] + "
+                f"down [{r.hidden}x{r.inter}] -> 2-bit planes")
     if config in inputs.REQUANT_CASES:
         r = inputs.REQUANT
         n = inputs.REQUANT_CASES[config] or r.num_experts
@@ -864,8 +886,9 @@ def workload_name(config: str) -> str:
 def reference_arm(args, cores):
     """The oracle timed on this host's cores on a bounded sample of the workload."""
     budget = 90.0
-    if args.config in inputs.REQUANT_FP8_CASES:
-        gu, _ = inputs.requant_fp8_inputs(experts=2)
+    if args.config in inputs.REQUANT_FP8_CASES or args.config in inputs.REQUANT_MXFP4_CASES:
+        fp8 = args.config in inputs.REQUANT_FP8_CASES
+        gu, _ = (inputs.requant_fp8_inputs if fp8 else inputs.requant_mxfp4_inputs)(experts=2)
         v, n, el, _ = oracle_requant_fp8_rate(gu, budget / 3)
         unit, sample = "elements/s", f"{n} whole tensors of {args.config} in {el:.1f} s"
         steps = n

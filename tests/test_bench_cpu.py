@@ -68,3 +68,6 @@ def test_every_workload_has_a_name_with_its_shape():
     for name, n in inputs.REQUANT_FP8_CASES.items():
         w = bench.workload_name(name)
         assert w.startswith(name + ":") and f"{n} experts FP8" in w
+    for name, n in inputs.REQUANT_MXFP4_CASES.items():
+        w = bench.workload_name(name)
+        assert w.startswith(name + ":") and f"{n} experts MXFP4" in w

@@ -96,8 +96,12 @@ def ncu_traffic(kernel: str, workload: str):
     the summary is missing or any file the kernel compiles changed since the capture."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
-            d = json.load(f)[kernel]
-    except (OSError, KeyError, ValueError):
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    # entries are keyed "kernel:workload" (a kernel measured on several workloads) or "kernel"
+    d = table.get(f"{kernel}:{workload}") or table.get(kernel)
+    if d is None:
         return None
     if d.get("workload") != workload or d.get("sources") != kernel_sources(kernel):
         return None

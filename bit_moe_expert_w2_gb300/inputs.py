@@ -403,3 +403,39 @@ def requant_mxfp4_inputs(cfg: RequantConfig = REQUANT, experts: int = 16):
         dn.append(mxfp4_tensors(rng, 1, cfg.hidden, cfg.inter))
     cat = lambda ts: Mxfp4Tensors(np.concatenate([t.e2m1 for t in ts]), np.concatenate([t.scales for t in ts]))
     return cat(gu), cat(dn)
+
+
+# --------------------------------------------------------------------------- FP4 layer
+
+def w4_planes(rng: np.random.Generator, E: int, H: int, I: int, scale_2: float = 2.0 ** -8) -> dict:
+    """NVFP4 expert planes of the FP4 layer, drawn as the NVFP4 loader workload is: e2m1
+    nibbles uniform over all 16 values, e4m3 block-16 scales log-uniform in [2^-6, 2^2],
+    one scale_2 per tensor (gate, up and down of every expert)."""
+    def part(rows, K):
+        e2m1 = random_bytes(rng, (E, rows, K // 2))
+        e4m3 = e4m3_round_positive(np.exp2(rng.uniform(-6.0, 2.0, size=(E, rows, K // 16))))
+        return e2m1, e4m3
+    w13_e2m1, w13_e4m3 = part(2 * I, H)
+    w2_e2m1, w2_e4m3 = part(H, I)
+    return {"w13_e2m1": w13_e2m1, "w13_e4m3": w13_e4m3,
+            "w13_scale_2": np.full((E, 2), scale_2, np.float32),
+            "w2_e2m1": w2_e2m1, "w2_e4m3": w2_e4m3,
+            "w2_scale_2": np.full(E, scale_2, np.float32)}
+
+
+@dataclasses.dataclass
+class W4LayerInputs:
+    cfg: LayerConfig
+    x: np.ndarray
+    ids: np.ndarray
+    weights: np.ndarray
+    planes: dict
+
+
+def w4_layer_inputs(cfg: LayerConfig) -> W4LayerInputs:
+    """Inputs of the FP4 layer for one configuration: planes, then activations, then routing."""
+    rng = rng_for(cfg.seed)
+    planes = w4_planes(rng, cfg.num_experts, cfg.hidden, cfg.inter)
+    x = activations(rng, cfg.tokens, cfg.hidden)
+    ids, weights = routing(rng, cfg)
+    return W4LayerInputs(cfg, x, ids, weights, planes)

@@ -83,6 +83,9 @@ def lib(parallel: bool = False):
             L.oracle_forward_tokens.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                 vp, i64, vp, vp]
             L.oracle_forward_tokens.restype = u32
+            L.oracle_forward_tokens_w4.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                   vp, i64, vp, vp]
+            L.oracle_forward_tokens_w4.restype = u32
             L.oracle_forward_tokens_cached.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32,
                                                        vp, i64, vp, vp, vp]
             L.oracle_forward_tokens_cached.restype = u32
@@ -221,6 +224,30 @@ def forward_tokens_cached(x: np.ndarray, ids: np.ndarray, weights: np.ndarray, p
         _p(planes["w13_codes"]), _p(planes["w13_scales"]), _p(planes["w2_codes"]), _p(planes["w2_scales"]),
         E, H, I, k, _p(tok), len(tok), _p(y), _p(h) if want_h else None, _p(misses))
     return (y, h, int(st), int(misses[0])) if want_h else (y, int(st), int(misses[0]))
+
+
+def forward_tokens_w4(x: np.ndarray, ids: np.ndarray, weights: np.ndarray, planes: dict,
+                      tokens=None, want_h: bool = False, parallel: bool = False):
+    """The FP4 layer: planes of NVFP4 experts (w13_e2m1 [E][2I][H/2], w13_e4m3 [E][2I][H/16],
+    w13_scale_2 f32 [E][2] (gate, up), w2_e2m1 [E][H][I/2], w2_e4m3 [E][H][I/16], w2_scale_2 f32 [E])."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    weights = np.ascontiguousarray(weights, dtype=np.float32)
+    T, H = x.shape
+    k = ids.shape[1]
+    E, two_i, _ = planes["w13_e2m1"].shape
+    I = two_i // 2
+    pl = {n: np.ascontiguousarray(planes[n]) for n in ("w13_e2m1", "w13_e4m3", "w2_e2m1", "w2_e4m3")}
+    s13 = np.ascontiguousarray(planes["w13_scale_2"], dtype=np.float32).reshape(E, 2)
+    s2 = np.ascontiguousarray(planes["w2_scale_2"], dtype=np.float32).reshape(E)
+    tok = np.arange(T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
+    y = np.empty((len(tok), H), np.uint16)
+    h = np.empty((len(tok), k, I), np.uint16) if want_h else None
+    st = lib(parallel).oracle_forward_tokens_w4(
+        _p(x), _p(ids), _p(weights), _p(pl["w13_e2m1"]), _p(pl["w13_e4m3"]), _p(s13),
+        _p(pl["w2_e2m1"]), _p(pl["w2_e4m3"]), _p(s2), E, H, I, k, _p(tok), len(tok), _p(y),
+        _p(h) if want_h else None)
+    return (y, h, int(st)) if want_h else (y, int(st))
 
 
 def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:

@@ -56,6 +56,11 @@
  *      option on, the exact zeros of a block take the signs +,-,+,- ... in
  *      element order instead of their sign bits; nothing else changes (a zero
  *      is at magnitude 1 for every u, so the scale search does not see it).
+ *   R12 the FP4 layer (page "vLLM-Moet wiki", "The kernels" and "FP4 recovery":
+ *      moe_w4_mm, the same forward over the NVFP4 experts): every weight is
+ *      e2m1 x e4m3 (its 16-element block) x scale_2 (per tensor: gate, up and
+ *      down of each expert have their own), dequantised exactly in f64; the
+ *      rest is R6.  An e4m3 NaN scale zeroes its 16 elements (bit 2).
  */
 #include <math.h>
 #include <stdint.h>
@@ -428,6 +433,66 @@ static uint32_t dequant_row(const uint8_t *codes, const uint8_t *scales, int64_t
     return st;
 }
 
+/* The rows of one layer's weights, whatever their storage: fills out with row r
+ * of gate/up (w13, r < 2I) or of down (w2) of slot e; returns status bits. */
+typedef struct {
+    uint32_t (*row)(const void *ctx, int w2, int64_t e, int64_t r, double *out);
+    const void *ctx;
+} RowSource;
+
+typedef struct {
+    const uint8_t *w13_codes, *w13_scales, *w2_codes, *w2_scales;
+    int32_t H, I;
+} Planes2;
+
+static uint32_t row2(const void *ctx, int w2, int64_t e, int64_t r, double *out)
+{
+    const Planes2 *p = (const Planes2 *)ctx;
+    if (!w2) {
+        int64_t g = e * 2 * p->I + r;
+        return dequant_row(p->w13_codes + g * (p->H / 4), p->w13_scales + g * (p->H / 32), p->H, out);
+    }
+    int64_t g = e * p->H + r;
+    return dequant_row(p->w2_codes + g * (p->I / 4), p->w2_scales + g * (p->I / 32), p->I, out);
+}
+
+/* One NVFP4 row of K weights (reading R12): w = e2m1 * e4m3(block of 16) * s2. */
+static uint32_t dequant_row_w4(const uint8_t *e2m1, const uint8_t *e4m3, double s2, int64_t K, double *out)
+{
+    uint32_t st = 0;
+    for (int64_t b = 0; b < K / 16; ++b) {
+        double sc = oracle_e4m3_value(e4m3[b]);
+        if (isnan(sc)) {
+            st |= ORACLE_BAD_SCALE;
+            sc = 0.0;
+        }
+        for (int64_t i = b * 16; i < b * 16 + 16; ++i) {
+            unsigned nib = (e2m1[i / 2] >> (4 * (i % 2))) & 0xFu;
+            out[i] = oracle_e2m1_value(nib) * sc * s2;   /* exact: at most 2 + 4 + 24 significant bits */
+        }
+    }
+    return st;
+}
+
+typedef struct {
+    const uint8_t *w13_e2m1, *w13_e4m3, *w2_e2m1, *w2_e4m3;
+    const float *w13_s2;   /* [E][2]: gate, up */
+    const float *w2_s2;    /* [E] */
+    int32_t H, I;
+} Planes4;
+
+static uint32_t row4(const void *ctx, int w2, int64_t e, int64_t r, double *out)
+{
+    const Planes4 *p = (const Planes4 *)ctx;
+    if (!w2) {
+        int64_t g = e * 2 * p->I + r;
+        double s2 = (double)p->w13_s2[2 * e + (r < p->I ? 0 : 1)];
+        return dequant_row_w4(p->w13_e2m1 + g * (p->H / 2), p->w13_e4m3 + g * (p->H / 16), s2, p->H, out);
+    }
+    int64_t g = e * p->H + r;
+    return dequant_row_w4(p->w2_e2m1 + g * (p->I / 2), p->w2_e4m3 + g * (p->I / 16), (double)p->w2_s2[e], p->I, out);
+}
+
 static double dot(const double *a, const double *b, int64_t n)
 {
     double s = 0.0;
@@ -451,9 +516,7 @@ static int32_t slot_of_pair(int32_t e, const int32_t *slot_of, int32_t n_route, 
 }
 
 static uint32_t forward_token(const uint16_t *x, const int32_t *ids, const float *weights,
-                              const int32_t *slot_of, int32_t n_route,
-                              const uint8_t *w13_codes, const uint8_t *w13_scales,
-                              const uint8_t *w2_codes, const uint8_t *w2_scales,
+                              const int32_t *slot_of, int32_t n_route, const RowSource *src,
                               int32_t E, int32_t H, int32_t I, int32_t k, int64_t t,
                               uint16_t *y_out, uint16_t *h_out)
 {
@@ -474,18 +537,16 @@ static uint32_t forward_token(const uint16_t *x, const int32_t *ids, const float
         }
         double w = (double)weights[t * k + j];
         for (int32_t n = 0; n < I; ++n) {
-            int64_t rg = (int64_t)e * 2 * I + n, ru = (int64_t)e * 2 * I + I + n;
-            st |= dequant_row(w13_codes + rg * (H / 4), w13_scales + rg * (H / 32), H, row);
+            st |= src->row(src->ctx, 0, e, n, row);
             double g = dot(row, xt, H);
-            st |= dequant_row(w13_codes + ru * (H / 4), w13_scales + ru * (H / 32), H, row);
+            st |= src->row(src->ctx, 0, e, (int64_t)I + n, row);
             double u = dot(row, xt, H);
             uint16_t hb = oracle_bf16_from_double(silu(g) * u);
             h[n] = oracle_bf16_to_double(hb);
             if (h_out) h_out[(int64_t)j * I + n] = hb;
         }
         for (int32_t m = 0; m < H; ++m) {
-            int64_t r = (int64_t)e * H + m;
-            st |= dequant_row(w2_codes + r * (I / 4), w2_scales + r * (I / 32), I, row);
+            st |= src->row(src->ctx, 1, e, m, row);
             acc[m] += w * dot(row, h, I);
         }
     }
@@ -506,11 +567,33 @@ uint32_t oracle_forward_tokens(const uint16_t *x, const int32_t *ids, const floa
                                const int64_t *tokens, int64_t ntok, uint16_t *y_out, uint16_t *h_out)
 {
     if (H % 32 || I % 32) return 0x80000000u;
+    Planes2 pl = {w13_codes, w13_scales, w2_codes, w2_scales, H, I};
+    RowSource src = {row2, &pl};
     uint32_t st = 0;
     ORACLE_PARALLEL_FOR_TOKENS
     for (int64_t it = 0; it < ntok; ++it)
-        st |= forward_token(x, ids, weights, NULL, 0, w13_codes, w13_scales, w2_codes, w2_scales, E, H, I, k,
-                            tokens[it], y_out + it * H, h_out ? h_out + it * k * (int64_t)I : NULL);
+        st |= forward_token(x, ids, weights, NULL, 0, &src, E, H, I, k, tokens[it], y_out + it * H,
+                            h_out ? h_out + it * k * (int64_t)I : NULL);
+    return st;
+}
+
+/* The FP4 layer (reading R12): NVFP4 planes w13_e2m1 [E][2I][H/2], w13_e4m3
+ * [E][2I][H/16], w13_s2 [E][2] (gate, up), w2_e2m1 [E][H][I/2], w2_e4m3
+ * [E][H][I/16], w2_s2 [E]; otherwise as oracle_forward_tokens. */
+uint32_t oracle_forward_tokens_w4(const uint16_t *x, const int32_t *ids, const float *weights,
+                                  const uint8_t *w13_e2m1, const uint8_t *w13_e4m3, const float *w13_s2,
+                                  const uint8_t *w2_e2m1, const uint8_t *w2_e4m3, const float *w2_s2,
+                                  int32_t E, int32_t H, int32_t I, int32_t k,
+                                  const int64_t *tokens, int64_t ntok, uint16_t *y_out, uint16_t *h_out)
+{
+    if (H % 32 || I % 32) return 0x80000000u;
+    Planes4 pl = {w13_e2m1, w13_e4m3, w2_e2m1, w2_e4m3, w13_s2, w2_s2, H, I};
+    RowSource src = {row4, &pl};
+    uint32_t st = 0;
+    ORACLE_PARALLEL_FOR_TOKENS
+    for (int64_t it = 0; it < ntok; ++it)
+        st |= forward_token(x, ids, weights, NULL, 0, &src, E, H, I, k, tokens[it], y_out + it * H,
+                            h_out ? h_out + it * k * (int64_t)I : NULL);
     return st;
 }
 
@@ -526,11 +609,13 @@ uint32_t oracle_forward_tokens_cached(const uint16_t *x, const int32_t *ids, con
                                       int64_t *misses)
 {
     if (H % 32 || I % 32 || !slot_of) return 0x80000000u;
+    Planes2 pl = {w13_codes, w13_scales, w2_codes, w2_scales, H, I};
+    RowSource src = {row2, &pl};
     uint32_t st = 0;
     ORACLE_PARALLEL_FOR_TOKENS
     for (int64_t it = 0; it < ntok; ++it)
-        st |= forward_token(x, ids, weights, slot_of, n_route, w13_codes, w13_scales, w2_codes, w2_scales, E, H, I,
-                            k, tokens[it], y_out + it * H, h_out ? h_out + it * k * (int64_t)I : NULL);
+        st |= forward_token(x, ids, weights, slot_of, n_route, &src, E, H, I, k, tokens[it], y_out + it * H,
+                            h_out ? h_out + it * k * (int64_t)I : NULL);
     if (misses) {
         int64_t m = 0;
         for (int64_t it = 0; it < ntok; ++it)

@@ -104,15 +104,15 @@ bool decode_use_mma(int64_t P, int32_t H, int32_t I)
     return P <= kDecodeMmaMaxPairs || H % 512 != 0 || I % 512 != 0;
 }
 
-int64_t decode_counter_count(int64_t P, int32_t E, int32_t H, int32_t I)
+int64_t decode_counter_count(int64_t P, int32_t E, int32_t H, int32_t I, bool mma)
 {
-    if (decode_use_mma(P, H, I)) return H / 32 + max_tiles(P, E, true) + 1;   // row blocks of y, tiles, queue
+    if (mma) return H / 32 + max_tiles(P, E, true) + 1;   // row blocks of y, tiles, queue
     // h publications and split-K arrivals per (tile, 64-row block), then the queue
     const int64_t mt = max_tiles(P, E, true);
     return 2 * mt * (I / 64) + 1;
 }
 
-Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I, bool cached)
+Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I, bool cached, bool w4)
 {
     Workspace w{};
     const int64_t P = (int64_t)T * k;
@@ -131,14 +131,14 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
     w.active_count = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * 2));
     w.tile_count = w.active_count + 1;
     w.tiles = reinterpret_cast<int4*>(take(sizeof(int4) * max_tiles(P, E, decode)));
-    if (decode && decode_use_mma(P, H, I)) {
-        w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * decode_counter_count(P, E, H, I)));
+    if (decode && (w4 || decode_use_mma(P, H, I))) {
+        w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * decode_counter_count(P, E, H, I, true)));
         w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * T * H));
         w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
         w.stage = reinterpret_cast<float*>(take(sizeof(float) * P * H));
     } else if (decode) {
         w.split = decode_split(P, E, H, I);
-        w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * decode_counter_count(P, E, H, I)));
+        w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * decode_counter_count(P, E, H, I, false)));
         w.xd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * T * (H / 2)));
         w.sxd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * T * (H / 32)));
         w.hd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * P * (I / 2)));
@@ -159,7 +159,7 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
 // moe_w2_forward and its variants.  slot_of (nullable) is the residency table of
 // an expert cache: routed id -> slot of w, negative when not resident.
 moe_w2_status forward_impl(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
-                           const moe_w2_planes* w, const int32_t* slot_of, int32_t n_route, int32_t T, int32_t top_k,
+                           const LayerPlanes* w, const int32_t* slot_of, int32_t n_route, int32_t T, int32_t top_k,
                            void* y_bf16, void* workspace, size_t workspace_bytes, uint32_t* misses,
                            uint32_t* dev_status, void* stream, void* const* phase_events)
 {
@@ -169,16 +169,19 @@ moe_w2_status forward_impl(const void* x_bf16, const int32_t* topk_ids, const fl
     if ((int64_t)T * top_k > MOE_W2_MAX_PAIRS) return MOE_W2_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return MOE_W2_OK;
     if (!x_bf16 || !topk_ids || !topk_weights || !y_bf16 || !workspace || !w->w13_codes || !w->w13_scales ||
-        !w->w2_codes || !w->w2_scales)
+        !w->w2_codes || !w->w2_scales || (w->w4 && (!w->w13_scale_2 || !w->w2_scale_2)))
         return MOE_W2_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MOE_W2_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(x_bf16) & 15) != 0 || (reinterpret_cast<uintptr_t>(y_bf16) & 15) != 0 ||
         (reinterpret_cast<uintptr_t>(w->w13_codes) & 15) != 0 || (reinterpret_cast<uintptr_t>(w->w2_codes) & 15) != 0 ||
         (reinterpret_cast<uintptr_t>(w->w13_scales) & 15) != 0 || (reinterpret_cast<uintptr_t>(w->w2_scales) & 15) != 0)
         return MOE_W2_ERR_INVALID_ARG;
+    if (w->w4 && ((reinterpret_cast<uintptr_t>(w->w13_scale_2) & 3) != 0 ||
+                  (reinterpret_cast<uintptr_t>(w->w2_scale_2) & 3) != 0))
+        return MOE_W2_ERR_INVALID_ARG;
     const int32_t E = w->num_experts, H = w->hidden, I = w->inter;
     const bool cached = slot_of != nullptr;
-    Workspace ws = carve_workspace(workspace, T, top_k, E, H, I, cached);
+    Workspace ws = carve_workspace(workspace, T, top_k, E, H, I, cached, w->w4);
     if (workspace_bytes < ws.bytes) return MOE_W2_ERR_WORKSPACE;
     moe_w2_status st = check_device();
     if (st != MOE_W2_OK) return st;
@@ -191,7 +194,8 @@ moe_w2_status forward_impl(const void* x_bf16, const int32_t* topk_ids, const fl
     for (int i = 0; i < 4; ++i) ev.e[i] = phase_events ? static_cast<cudaEvent_t>(phase_events[i]) : nullptr;
     if (ev.record(0, s) != cudaSuccess) return MOE_W2_ERR_CUDA;
     const int64_t P = (int64_t)T * top_k;
-    const bool mma = decode && decode_use_mma(P, H, I);
+    // the FP4 layer's decode steps all take the mma.sync kernel
+    const bool mma = decode && (w->w4 || decode_use_mma(P, H, I));
     PermuteSlots slots{};
     if (cached) slots = PermuteSlots{slot_of, n_route, ws.ids_eff, misses};
     cudaError_t e = launch_permute(topk_ids, slots, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active,
@@ -199,19 +203,35 @@ moe_w2_status forward_impl(const void* x_bf16, const int32_t* topk_ids, const fl
                                    !decode ? kPrefillTileRows : mma ? kDecodeMmaTileRows : kDecodeTileRows,
                                    decode ? x : nullptr, mma ? ws.xa : nullptr, decode && !mma ? ws.xd : nullptr,
                                    decode && !mma ? ws.sxd : nullptr, H, ws.counters,
-                                   decode ? (int32_t)decode_counter_count(P, E, H, I) : 0, decode ? y : nullptr,
+                                   decode ? (int32_t)decode_counter_count(P, E, H, I, mma) : 0, decode ? y : nullptr,
                                    dev_status, s);
     if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
     // the later kernels read the ids only to tell kept pairs from left-out ones
     const int32_t* ids = cached ? ws.ids_eff : topk_ids;
-    if (mma)
-        e = launch_decode_mma(x, ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
-    else if (decode)
-        e = launch_decode(x, ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
-    else
+    if (mma) {
+        e = launch_decode_mma(ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
+    } else if (decode) {
+        const moe_w2_planes p2{w->w13_codes, w->w13_scales, w->w2_codes, w->w2_scales, E, H, I};
+        e = launch_decode(x, ids, topk_weights, p2, T, top_k, ws, y, dev_status, s, ev);
+    } else {
         e = launch_prefill(x, ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
+    }
     if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
     return ev.record(3, s) == cudaSuccess ? MOE_W2_OK : MOE_W2_ERR_CUDA;
+}
+
+LayerPlanes planes_of(const moe_w2_planes* w)
+{
+    if (!w) return LayerPlanes{};
+    return LayerPlanes{false, w->w13_codes, w->w13_scales, w->w2_codes, w->w2_scales, nullptr, nullptr,
+                       w->num_experts, w->hidden, w->inter};
+}
+
+LayerPlanes planes_of(const moe_w4_planes* w)
+{
+    if (!w) return LayerPlanes{};
+    return LayerPlanes{true, w->w13_e2m1, w->w13_e4m3, w->w2_e2m1, w->w2_e4m3, w->w13_scale_2, w->w2_scale_2,
+                       w->num_experts, w->hidden, w->inter};
 }
 
 }  // namespace moe_w2
@@ -277,7 +297,9 @@ moe_w2_status moe_w2_forward_traced(const void* x_bf16, const int32_t* topk_ids,
                                     void* workspace, size_t workspace_bytes, uint32_t* dev_status, void* stream,
                                     void* const* phase_events)
 {
-    return forward_impl(x_bf16, topk_ids, topk_weights, w, nullptr, 0, T, top_k, y_bf16, workspace, workspace_bytes,
+    if (!w) return MOE_W2_ERR_INVALID_ARG;
+    const LayerPlanes p = planes_of(w);
+    return forward_impl(x_bf16, topk_ids, topk_weights, &p, nullptr, 0, T, top_k, y_bf16, workspace, workspace_bytes,
                         nullptr, dev_status, stream, phase_events);
 }
 
@@ -285,7 +307,25 @@ moe_w2_status moe_w2_forward(const void* x_bf16, const int32_t* topk_ids, const 
                              const moe_w2_planes* w, int32_t T, int32_t top_k, void* y_bf16, void* workspace,
                              size_t workspace_bytes, uint32_t* dev_status, void* stream)
 {
-    return forward_impl(x_bf16, topk_ids, topk_weights, w, nullptr, 0, T, top_k, y_bf16, workspace, workspace_bytes,
+    if (!w) return MOE_W2_ERR_INVALID_ARG;
+    const LayerPlanes p = planes_of(w);
+    return forward_impl(x_bf16, topk_ids, topk_weights, &p, nullptr, 0, T, top_k, y_bf16, workspace, workspace_bytes,
+                        nullptr, dev_status, stream, nullptr);
+}
+
+size_t moe_w4_forward_workspace_size(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t I)
+{
+    if (moe_w2_forward_workspace_size(T, top_k, E, H, I) == 0) return 0;
+    return carve_workspace(nullptr, T, top_k, E, H, I, false, true).bytes;
+}
+
+moe_w2_status moe_w4_forward(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                             const moe_w4_planes* w, int32_t T, int32_t top_k, void* y_bf16, void* workspace,
+                             size_t workspace_bytes, uint32_t* dev_status, void* stream)
+{
+    if (!w) return MOE_W2_ERR_INVALID_ARG;
+    const LayerPlanes p = planes_of(w);
+    return forward_impl(x_bf16, topk_ids, topk_weights, &p, nullptr, 0, T, top_k, y_bf16, workspace, workspace_bytes,
                         nullptr, dev_status, stream, nullptr);
 }
 
@@ -303,7 +343,9 @@ moe_w2_status moe_w2_forward_cached(const void* x_bf16, const int32_t* topk_ids,
 {
     if (num_routed_experts < 1 || num_routed_experts > MOE_W2_MAX_ROUTED_EXPERTS) return MOE_W2_ERR_INVALID_ARG;
     if (T > 0 && !slot_of_expert) return MOE_W2_ERR_INVALID_ARG;
-    return forward_impl(x_bf16, topk_ids, topk_weights, w, slot_of_expert, num_routed_experts, T, top_k, y_bf16,
+    if (!w) return MOE_W2_ERR_INVALID_ARG;
+    const LayerPlanes p = planes_of(w);
+    return forward_impl(x_bf16, topk_ids, topk_weights, &p, slot_of_expert, num_routed_experts, T, top_k, y_bf16,
                         workspace, workspace_bytes, miss_counter, dev_status, stream, nullptr);
 }
 

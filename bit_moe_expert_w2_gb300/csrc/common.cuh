@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -206,6 +207,66 @@ __device__ __forceinline__ SelConst sel_const_regs()
     return k;
 }
 
+// ------------------------------------------------------------------ NVFP4 weights (the FP4 layer)
+// A weight is e2m1 x e4m3 (one scale per 16 elements) x scale_2 (per tensor).
+// The product e2m1 x e4m3 has at most 2 + 4 significant bits and lies in
+// [2^-10, 2688], so it is exact in bf16; scale_2 multiplies the fp32
+// accumulator in the epilogue.  Per scale byte s, Fp4Lut holds the bf16 high
+// and low bytes of |e2m1 magnitude m| * e4m3(s) for m = 0..7 (bytes m of the
+// pair (hi0, hi1) and of (lo0, lo1)), the scale's sign in the high bytes; an
+// e4m3 NaN scale gives zeros (its block counts as 0).
+__host__ __device__ __forceinline__ uint4 make_fp4_lut(uint32_t s)
+{
+    const uint32_t E = (s >> 3) & 15u, m = s & 7u;
+    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+    if (E == 15u && m == 7u) return r;
+    // e4m3 = (E ? 8 + m : m) * 2^((E ? E : 1) - 10); e2m1 magnitudes in halves
+    const float sc = (float)(E ? 8u + m : m) * ldexpf(1.0f, (int)(E ? E : 1u) - 10) * ((s & 0x80u) ? -1.0f : 1.0f);
+    const float half_units[8] = {0.f, 1.f, 2.f, 3.f, 4.f, 6.f, 8.f, 12.f};
+    for (int i = 0; i < 8; ++i) {
+        float v = 0.5f * half_units[i] * sc;
+        uint32_t b;
+        memcpy(&b, &v, 4);
+        b >>= 16;   // exact: at most 6 significant bits
+        const uint32_t hi = (b >> 8) & 0xFFu, lo = b & 0xFFu;
+        if (i < 4) {
+            r.x |= hi << (8 * i);
+            r.z |= lo << (8 * i);
+        } else {
+            r.y |= hi << (8 * (i - 4));
+            r.w |= lo << (8 * (i - 4));
+        }
+    }
+    return r;
+}
+// 0x80 in every byte of w whose e4m3 value is NaN (low seven bits all ones).
+__host__ __device__ __forceinline__ uint32_t e4m3_nan_bytes(uint32_t w)
+{
+    return ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+}
+// Eight e2m1 nibbles w (byte b: element 2b low, element 2b+1 high) times their
+// block's scale (table L) -> four bf16 pairs:
+//   r0 = (e0, e4), r1 = (e1, e5), r2 = (e2, e6), r3 = (e3, e7)
+// which is the pair order of the T16 activation layout (and of the mma.sync A
+// fragments the decode kernel builds from it).  A byte-permute selector takes
+// one nibble per output byte from the low 16 bits, so the bytes are first
+// regrouped as (b0, b2 | b1, b3): the low half then holds the magnitudes of
+// elements 0, 1, 4, 5 and the high half those of 2, 3, 6, 7.  The nibble's sign
+// (bit 3 of it: bits 3, 19 of w for e0, e4; 7, 23 for e1, e5; 11, 27; 15, 31) is
+// moved to bits 15 and 31 of each pair and XOR-ed into the table's sign.
+__device__ __forceinline__ void fp4_word_bf16(uint32_t w, const uint4& L, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3)
+{
+    const uint32_t v = prmt(w, w, 0x3120u);                        // bytes b0, b2, b1, b3
+    const uint32_t sa = v & 0x7777u, sb = (v >> 16) & 0x7777u;     // magnitudes (e0 e1 e4 e5), (e2 e3 e6 e7)
+    const uint32_t ha = prmt(L.x, L.y, sa), la = prmt(L.z, L.w, sa);
+    const uint32_t hb = prmt(L.x, L.y, sb), lb = prmt(L.z, L.w, sb);
+    r0 = prmt(la, ha, 0x6240u) ^ ((w << 12) & 0x80008000u);   // e0, e4
+    r1 = prmt(la, ha, 0x7351u) ^ ((w << 8) & 0x80008000u);    // e1, e5
+    r2 = prmt(lb, hb, 0x6240u) ^ ((w << 4) & 0x80008000u);    // e2, e6
+    r3 = prmt(lb, hb, 0x7351u) ^ (w & 0x80008000u);           // e3, e7
+}
+
 // ------------------------------------------------------------------ mma.sync (decode)
 __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1)
 {
@@ -259,14 +320,26 @@ struct Workspace {
     size_t bytes;
 };
 
-Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I, bool cached = false);
+Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H, int32_t I, bool cached = false,
+                          bool w4 = false);
 int64_t max_tiles(int64_t P, int32_t E, bool decode);
-int64_t decode_counter_count(int64_t P, int32_t E, int32_t H, int32_t I);
+int64_t decode_counter_count(int64_t P, int32_t E, int32_t H, int32_t I, bool mma);
 
 // ------------------------------------------------------------------ launches
 // Optional profiling events recorded between phases (see moe_w2_forward_traced).
 // During stream capture the events become external record nodes, so each graph
 // replay records them and cudaEventElapsedTime works on replays.
+// One layer's expert weights as the layer kernels read them: the 2-bit planes,
+// or NVFP4 experts (the FP4 layer).  2-bit: codes [rows][K/4], UE8M0 scales
+// [rows][K/32].  NVFP4: e2m1 [rows][K/2], e4m3 [rows][K/16] and a per-tensor
+// scale_2 (w13: [E][2], gate then up; w2: [E]).
+struct LayerPlanes {
+    bool w4;
+    const uint8_t *w13_codes, *w13_scales, *w2_codes, *w2_scales;
+    const float *w13_scale_2, *w2_scale_2;
+    int32_t num_experts, hidden, inter;
+};
+
 struct PhaseEvents {
     cudaEvent_t e[4];
     cudaError_t record(int i, cudaStream_t s) const
@@ -294,14 +367,14 @@ cudaError_t launch_permute(const int32_t* ids, const PermuteSlots& slots, int32_
                            uint8_t* xd, uint8_t* sxd, int32_t H, int32_t* counters, int32_t n_counters, uint16_t* y,
                            uint32_t* status, cudaStream_t s);
 
-cudaError_t launch_decode_mma(const uint16_t* x, const int32_t* ids, const float* weights,
-                              const moe_w2_planes& w, int32_t T, int32_t k, const Workspace& ws, uint16_t* y,
-                              uint32_t* status, cudaStream_t s, const PhaseEvents& ev);
+cudaError_t launch_decode_mma(const int32_t* ids, const float* weights, const LayerPlanes& w, int32_t T, int32_t k,
+                              const Workspace& ws, uint16_t* y, uint32_t* status, cudaStream_t s,
+                              const PhaseEvents& ev);
 cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* weights,
                           const moe_w2_planes& w, int32_t T, int32_t k, const Workspace& ws, uint16_t* y,
                           uint32_t* status, cudaStream_t s, const PhaseEvents& ev);
 
-cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* weights, const moe_w2_planes& w,
+cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* weights, const LayerPlanes& w,
                            int32_t T, int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status,
                            cudaStream_t s, const PhaseEvents& ev);
 

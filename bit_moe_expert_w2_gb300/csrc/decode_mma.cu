@@ -38,7 +38,17 @@
 // the epilogue multiplies by the router weight and writes the pair's fp32 slot;
 // the last CTA to finish a 32-row block of y sums the k slots of every token in
 // j order and writes y (counter per row block, reset by the permutation kernel).
+//
+// The FP4 layer (page "vLLM-Moet wiki", "The kernels" and "FP4 recovery":
+// moe_w4_mm, the same forward over the NVFP4 experts at twice the plane bytes)
+// is the same kernel with kW4: a chunk row is 128 bytes of e2m1 nibbles and 16
+// e4m3 scale bytes (one per 16 elements); thread c of a quad owns the row's
+// elements 64c .. 64c+63 as before, and each 16-element block (two words)
+// becomes the same bf16 pairs (r, r+4), (r+8, r+12) through fp4_word_bf16 with
+// the block's scale folded into the table; scale_2 multiplies the fp32 results
+// in the epilogues.
 #include <algorithm>
+#include <type_traits>
 
 #include "tc.cuh"
 
@@ -51,11 +61,17 @@ constexpr int kChunk = 256;          // K elements per chunk
 constexpr int kWarps = 4;            // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;   // + the producer warp
 constexpr int kMaxNT = 2;            // n-tiles of 8 pairs per item (tiles of <= 16 pairs)
-constexpr int kSlots = 16;           // chunk slots (four per consumer warp; a power of two)
-constexpr uint32_t kSlotCodeBytes = 32 * 64;   // 32 rows x 64 code bytes
-constexpr uint32_t kSlotScaleBytes = 32 * 8;   // 32 rows x 8 UE8M0 bytes
-constexpr uint32_t kSlotBytes = kSlotCodeBytes + kSlotScaleBytes;   // a multiple of 128
-constexpr uint32_t kRingBytes = kSlots * kSlotBytes;
+// Chunk slots: 2-bit planes (kW4 false) or NVFP4 experts (true); both rings
+// take the same 36 KB of shared memory.
+template <bool kW4> struct Fmt {
+    static constexpr int kSlots = kW4 ? 8 : 16;                         // chunk slots
+    static constexpr uint32_t kRowBytes = kW4 ? 128 : 64;               // code bytes of a row per chunk
+    static constexpr uint32_t kRowScaleBytes = kW4 ? 16 : 8;            // scale bytes of a row per chunk
+    static constexpr uint32_t kSlotCodeBytes = 32 * kRowBytes;          // 32 rows
+    static constexpr uint32_t kSlotBytes = kSlotCodeBytes + 32 * kRowScaleBytes;   // a multiple of 128
+    static constexpr uint32_t kRingBytes = kSlots * kSlotBytes;
+    using Lut = std::conditional_t<kW4, uint4, uint2>;
+};
 constexpr int kInfo = 16;            // published items in flight
 constexpr uint32_t kConsumerBarrier = 1;       // named barrier id of the consumer warps
 
@@ -82,15 +98,18 @@ struct DecArgs {
     uint16_t* y;
     uint32_t* status;
     DepWait dep;               // down items' wait for their tile's h: target bias and limit
+    const float* scale_2;      // FP4 layer: per-tensor scale_2 of expert e at e * s2_stride (+1: up)
+    int32_t s2_stride;
 };
 
+template <bool kW4>
 struct SharedState {
-    uint64_t full[kSlots];      // producer -> consumers: slot filled (expect_tx arrival + 32 cp.async arrivals)
-    uint64_t empty[kSlots];     // consumer warp -> producer: slot read
+    uint64_t full[Fmt<kW4>::kSlots];   // producer -> consumers: slot filled (expect_tx arrival + 32 cp.async arrivals)
+    uint64_t empty[Fmt<kW4>::kSlots];  // consumer warp -> producer: slot read
     uint64_t info_full[kInfo];  // producer -> consumers: item published
     uint64_t info_empty[kInfo]; // consumer warps -> producer: item finished
     int4 info[kInfo];           // (item index, or -1 at the end; expert; first slot; pairs)
-    uint2 lut[256];
+    typename Fmt<kW4>::Lut lut[256];   // per scale byte: ScaleLut words, or the NVFP4 product table
     float red[kWarps][2][kMaxNT][32][4];
     int4 cur_info;              // the item the consumer warps work on
     int last_flag;
@@ -115,10 +134,12 @@ __device__ __forceinline__ uint32_t word_of(const uint4& q, int i)
 
 // One item on the consumer warps: K chunks ch = warp, warp + 4, ... from ring
 // slots (qbase + ch) % kSlots, then the split-K reduction and the epilogue.
-template <bool kGateUp, int NT>
-__device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, SharedState& sh, const uint8_t* ring,
-                                         uint32_t qbase, int q0, int nrows, int rb, uint32_t& lut_and)
+template <bool kGateUp, int NT, bool kW4>
+__device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, SharedState<kW4>& sh,
+                                         const uint8_t* ring, uint32_t qbase, int q0, int nrows, int rb, int expert,
+                                         uint32_t& lut_and)
 {
+    using F = Fmt<kW4>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
     const int nch = p.K / kChunk;
@@ -155,16 +176,68 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, Sh
     volatile int* abort = &sh.abort_flag;
     for (int ch = warp; ch < nch; ch += kWarps) {
         const uint32_t q = qbase + (uint32_t)ch;
-        const uint32_t slot = q % kSlots;
-        if (!mbar_wait(smem_u32(&sh.full[slot]), (q / kSlots) & 1u, abort)) break;
+        const uint32_t slot = q % F::kSlots;
+        if (!mbar_wait(smem_u32(&sh.full[slot]), (q / F::kSlots) & 1u, abort)) break;
         // plain (compiler-schedulable) shared loads: the wait above is a compiler barrier
-        const uint8_t* sp = ring + slot * kSlotBytes;
+        const uint8_t* sp = ring + slot * F::kSlotBytes;
+        if constexpr (kW4) {
+            // the row's 32 bytes of this thread (elements 64c..64c+63: four blocks of
+            // 16, two words each) and the four blocks' e4m3 bytes
+            uint4 qa[4][2];
+            uint32_t sw[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                qa[a][0] = *reinterpret_cast<const uint4*>(sp + srow[a] * 128 + c * 32);
+                qa[a][1] = *reinterpret_cast<const uint4*>(sp + srow[a] * 128 + c * 32 + 16);
+                sw[a] = *reinterpret_cast<const uint32_t*>(sp + F::kSlotCodeBytes + srow[a] * 16 + 4 * c);
+                if (e4m3_nan_bytes(sw[a]) != 0u) lut_and = 0u;
+            }
+            const uint16_t* bsrc[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) bsrc[nt] = brow[nt] + (int64_t)ch * kChunk;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint4 B0[NT], B1[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (kGateUp) {
+                        B0[nt] = __ldg(reinterpret_cast<const uint4*>(bsrc[nt] + i * 16));
+                        B1[nt] = __ldg(reinterpret_cast<const uint4*>(bsrc[nt] + i * 16 + 8));
+                    } else {
+                        B0[nt] = *reinterpret_cast<const uint4*>(bsrc[nt] + i * 16);
+                        B1[nt] = *reinterpret_cast<const uint4*>(bsrc[nt] + i * 16 + 8);
+                    }
+                }
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const uint4& va = qa[2 * mt][i >> 1];
+                    const uint4& vb = qa[2 * mt + 1][i >> 1];
+                    const uint4 La = sh.lut[(sw[2 * mt] >> (8 * i)) & 0xFFu];
+                    const uint4 Lb = sh.lut[(sw[2 * mt + 1] >> (8 * i)) & 0xFFu];
+                    // elements 0..7 of the block (word 2 (i % 2)) and 8..15 (the next word)
+                    uint32_t a_lo[4], a_hi[4], b_lo[4], b_hi[4];
+                    fp4_word_bf16(word_of(va, 2 * (i & 1)), La, a_lo[0], a_lo[1], a_lo[2], a_lo[3]);
+                    fp4_word_bf16(word_of(va, 2 * (i & 1) + 1), La, a_hi[0], a_hi[1], a_hi[2], a_hi[3]);
+                    fp4_word_bf16(word_of(vb, 2 * (i & 1)), Lb, b_lo[0], b_lo[1], b_lo[2], b_lo[3]);
+                    fp4_word_bf16(word_of(vb, 2 * (i & 1) + 1), Lb, b_hi[0], b_hi[1], b_hi[2], b_hi[3]);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const uint32_t afrag[4] = {a_lo[r], b_lo[r], a_hi[r], b_hi[r]};
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint4& Bv = (r < 2) ? B0[nt] : B1[nt];
+                            mma_bf16_16816(acc[mt][nt], afrag, (r & 1) ? Bv.z : Bv.x, (r & 1) ? Bv.w : Bv.y);
+                        }
+                    }
+                }
+            }
+        } else {
         uint4 qw[4];
         uint2 L[4][2];
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             qw[a] = *reinterpret_cast<const uint4*>(sp + srow[a] * 64 + c * 16);
-            const uint8_t* sb = sp + kSlotCodeBytes + srow[a] * 8 + 2 * c;
+            const uint8_t* sb = sp + F::kSlotCodeBytes + srow[a] * 8 + 2 * c;
             L[a][0] = sh.lut[sb[0]];
             L[a][1] = sh.lut[sb[1]];
             lut_and &= L[a][0].x & L[a][1].x;
@@ -209,6 +282,7 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, Sh
                     }
             }
         }
+        }   // 2-bit planes
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.empty[slot]));
     }
@@ -231,6 +305,16 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, Sh
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) s += sh.red[w][mt][nt][lane][e];
             v[e] = s;
+        }
+        if (kW4) {
+            // the tensors' scale_2: gate rows (accumulator rows g) and up rows (g + 8)
+            // of gate_up, or the down rows
+            const float s_lo = __ldg(p.scale_2 + (int64_t)expert * p.s2_stride);
+            const float s_hi = kGateUp ? __ldg(p.scale_2 + (int64_t)expert * p.s2_stride + 1) : s_lo;
+            v[0] *= s_lo;
+            v[1] *= s_lo;
+            v[2] *= s_hi;
+            v[3] *= s_hi;
         }
         if (kGateUp) {
             const int pos = t16_pos(rb * 16 + mt * 8 + g);
@@ -269,11 +353,13 @@ __device__ __forceinline__ void run_item(const DecArgs& p, const SelConst& k, Sh
 // down index and is held by a running CTA, so the waits always end (each is
 // still bounded and gives up with the pipeline-timeout status bit).  Which CTA
 // runs an item never changes its result.
+template <bool kW4>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
 decode_mma_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_constant__ CUtensorMap dn_map,
                     DecArgs gu, DecArgs dn, int32_t* __restrict__ gu_done, int32_t* __restrict__ queue)
 {
-    __shared__ SharedState sh;
+    using F = Fmt<kW4>;
+    __shared__ SharedState<kW4> sh;
     extern __shared__ uint8_t dyn_smem[];   // kRingBytes + 128 (aligned below)
     // 128-byte aligned ring; offsetting the shared array itself keeps the
     // pointer in the shared window (plain loads from it compile to shared loads)
@@ -282,11 +368,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_const
     const uint32_t ring_addr = smem_u32(dyn_smem) + pad;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int s = tid; s < 256; s += kThreads) {
-        ScaleLut l = make_lut((uint32_t)s);
-        sh.lut[s] = make_uint2(l.lut, l.lo);
+        if constexpr (kW4) {
+            sh.lut[s] = make_fp4_lut((uint32_t)s);
+        } else {
+            ScaleLut l = make_lut((uint32_t)s);
+            sh.lut[s] = make_uint2(l.lut, l.lo);
+        }
     }
     if (tid == 0) {
-        for (int s = 0; s < kSlots; ++s) {
+        for (int s = 0; s < F::kSlots; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1 + 32);
             mbar_init(smem_u32(&sh.empty[s]), 1);
         }
@@ -356,25 +446,28 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_const
             int64_t srow;
             if (is_gu) srow = ebase + (lane < 16 ? rb * 16 + lane : P.I + rb * 16 + (lane - 16));
             else srow = ebase + rb * 32 + lane;
-            const uint8_t* ssrc = P.scales + srow * (P.K / 32);
+            // scale bytes of the row: one per 32 elements (2-bit) or per 16 (NVFP4)
+            const uint8_t* ssrc = P.scales + srow * (P.K / (kW4 ? 16 : 32));
             const int nch = P.K / kChunk;
+            constexpr int rbytes = (int)F::kRowBytes;
             for (int ch = 0; ch < nch; ++ch, ++q) {
-                const uint32_t slot = q % kSlots;
-                if (lane == 0) ok = mbar_wait(smem_u32(&sh.empty[slot]), ((q / kSlots) & 1u) ^ 1u, abort);
+                const uint32_t slot = q % F::kSlots;
+                if (lane == 0) ok = mbar_wait(smem_u32(&sh.empty[slot]), ((q / F::kSlots) & 1u) ^ 1u, abort);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 const uint32_t fb = smem_u32(&sh.full[slot]);
-                const uint32_t dst = ring_addr + slot * kSlotBytes;
+                const uint32_t dst = ring_addr + slot * F::kSlotBytes;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(fb, kSlotCodeBytes);
+                    mbar_arrive_expect_tx(fb, F::kSlotCodeBytes);
                     if (is_gu) {
-                        tma_load_2d(dst, &gu_map, ch * 64, (int)(ebase + rb * 16), fb);
-                        tma_load_2d(dst + 16 * 64, &gu_map, ch * 64, (int)(ebase + P.I + rb * 16), fb);
+                        tma_load_2d(dst, &gu_map, ch * rbytes, (int)(ebase + rb * 16), fb);
+                        tma_load_2d(dst + 16 * rbytes, &gu_map, ch * rbytes, (int)(ebase + P.I + rb * 16), fb);
                     } else {
-                        tma_load_2d(dst, &dn_map, ch * 64, (int)(ebase + rb * 32), fb);
+                        tma_load_2d(dst, &dn_map, ch * rbytes, (int)(ebase + rb * 32), fb);
                     }
                 }
-                cp_async8(dst + kSlotCodeBytes + lane * 8, ssrc + ch * 8);
+                if constexpr (kW4) cp_async16(dst + F::kSlotCodeBytes + lane * 16, ssrc + ch * 16);
+                else cp_async8(dst + F::kSlotCodeBytes + lane * 8, ssrc + ch * 8);
                 cp_async_arrive_noinc(fb);
             }
             if (!ok) break;
@@ -405,8 +498,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_const
             if (sh.stop || info.x < 0) break;
             if (info.x < n_gu) {
                 const int rb = info.x % gu.row_blocks;
-                if (info.w <= 8) run_item<true, 1>(gu, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
-                else run_item<true, 2>(gu, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
+                if (info.w <= 8) run_item<true, 1, kW4>(gu, k, sh, ring, qbase, info.z, info.w, rb, info.y, lut_and);
+                else run_item<true, 2, kW4>(gu, k, sh, ring, qbase, info.z, info.w, rb, info.y, lut_and);
                 qbase += (uint32_t)(gu.K / kChunk);
                 // run_item ends with a consumer barrier after its h stores
                 if (tid == 0) {
@@ -415,8 +508,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_const
                 }
             } else {
                 const int rb = (info.x - n_gu) % dn.row_blocks;
-                if (info.w <= 8) run_item<false, 1>(dn, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
-                else run_item<false, 2>(dn, k, sh, ring, qbase, info.z, info.w, rb, lut_and);
+                if (info.w <= 8) run_item<false, 1, kW4>(dn, k, sh, ring, qbase, info.z, info.w, rb, info.y, lut_and);
+                else run_item<false, 2, kW4>(dn, k, sh, ring, qbase, info.z, info.w, rb, info.y, lut_and);
                 qbase += (uint32_t)(dn.K / kChunk);
                 // The last of the n_tiles items that wrote rows [32 rb, 32 rb + 32) of
                 // the pair slots sums them into y (fixed j order per token).  run_item
@@ -450,24 +543,23 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_const
     if (tid == 0 && *abort) flag_status(gu.status, kDevPipelineTimeout);
 }
 
-}  // namespace
-
-cudaError_t launch_decode_mma(const uint16_t* x, const int32_t* ids, const float* weights, const moe_w2_planes& w,
-                          int32_t T, int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status, cudaStream_t s,
-                          const PhaseEvents& ev)
+template <bool kW4>
+cudaError_t launch_decode_mma_fmt(const int32_t* ids, const float* weights, const LayerPlanes& w, int32_t T,
+                                  int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status, cudaStream_t s,
+                                  const PhaseEvents& ev)
 {
-    (void)x;
+    using F = Fmt<kW4>;
     const int32_t E = w.num_experts, H = w.hidden, I = w.inter;
     const int64_t P = (int64_t)T * k;
-    constexpr int kDyn = kRingBytes + 128;
+    constexpr int kDyn = F::kRingBytes + 128;
     static bool ready[kMaxDevices];
     static int occ_of[kMaxDevices];
     int dev = 0;
     cudaError_t e0 = once_per_device(ready, dev, [&](int d) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<kW4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
         if (e != cudaSuccess) return e;
         int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_mma_kernel, kThreads, kDyn);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_mma_kernel<kW4>, kThreads, kDyn);
         if (e != cudaSuccess) return e;
         occ_of[d] = std::max(occ, 1);
         return cudaSuccess;
@@ -499,6 +591,8 @@ cudaError_t launch_decode_mma(const uint16_t* x, const int32_t* ids, const float
     gp.y = y;
     gp.status = status;
     gp.dep = dependency_wait();
+    gp.scale_2 = w.w13_scale_2;
+    gp.s2_stride = 2;
 
     DecArgs dp = gp;
     dp.codes = w.w2_codes;
@@ -507,15 +601,21 @@ cudaError_t launch_decode_mma(const uint16_t* x, const int32_t* ids, const float
     dp.rows_per_expert = H;
     dp.row_blocks = H / 32;
     dp.act = ws.h;
+    dp.scale_2 = w.w2_scale_2;
+    dp.s2_stride = 1;
     int32_t* gu_done = ws.counters + H / 32;   // [tiles], zeroed by the permutation kernel
     int32_t* queue = gu_done + tiles;          // item queue, zeroed by the permutation kernel
 
-    // code tiles: 64 bytes (256 codes) x 16 rows (gate_up: gate and up halves
-    // separately) or x 32 rows (down)
+    // code tiles: one chunk of a row (64 bytes of 2-bit codes or 128 bytes of
+    // e2m1, 256 elements) x 16 rows (gate_up: gate and up halves separately) or
+    // x 32 rows (down)
+    constexpr int per_byte = kW4 ? 2 : 4;
     CUtensorMap gu_map, dn_map;
-    cudaError_t e = make_tmap_2d(&gu_map, w.w13_codes, false, (int64_t)E * 2 * I, H / 4, 64, 16, 0);
+    cudaError_t e = make_tmap_2d(&gu_map, w.w13_codes, false, (int64_t)E * 2 * I, H / per_byte, F::kRowBytes, 16, 0);
     if (e != cudaSuccess) return e;
-    if ((e = make_tmap_2d(&dn_map, w.w2_codes, false, (int64_t)E * H, I / 4, 64, 32, 0)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&dn_map, w.w2_codes, false, (int64_t)E * H, I / per_byte, F::kRowBytes, 32, 0)) !=
+        cudaSuccess)
+        return e;
 
     // at most occupancy x SMs (all resident at once when the GPU is otherwise
     // idle), and no more than the larger phase has items
@@ -532,9 +632,19 @@ cudaError_t launch_decode_mma(const uint16_t* x, const int32_t* ids, const float
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, decode_mma_kernel, gu_map, dn_map, gp, dp, gu_done, queue)) != cudaSuccess)
+    if ((e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<kW4>, gu_map, dn_map, gp, dp, gu_done, queue)) != cudaSuccess)
         return e;
     return ev.record(2, s);   // the combine is inside the kernel: phase 3 is empty
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mma(const int32_t* ids, const float* weights, const LayerPlanes& w, int32_t T, int32_t k,
+                              const Workspace& ws, uint16_t* y, uint32_t* status, cudaStream_t s,
+                              const PhaseEvents& ev)
+{
+    return w.w4 ? launch_decode_mma_fmt<true>(ids, weights, w, T, k, ws, y, status, s, ev)
+                : launch_decode_mma_fmt<false>(ids, weights, w, T, k, ws, y, status, s, ev);
 }
 
 }  // namespace moe_w2

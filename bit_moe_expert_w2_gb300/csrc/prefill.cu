@@ -29,7 +29,15 @@
 //   warps 6-9  epilogue: TMEM lanes 32*(warp % 4) .. +31
 //   warp 10    TMA producer of the raw code tiles: one superstage (4 stages,
 //              64 code bytes per A row) at a time, two superstages ahead
+//
+// The FP4 layer (page "vLLM-Moet wiki", "The kernels" and "FP4 recovery":
+// moe_w4_mm over the NVFP4 experts) is the same kernel with kW4: a superstage
+// is 2 stages (64 bytes of e2m1 per A row, 128 elements), the scale bytes are
+// e4m3 per 16 elements (8 per superstage, as for 2-bit), every 16-element
+// block becomes bf16 pairs through fp4_word_bf16 with its scale in the table,
+// and the epilogues multiply by the tensors' scale_2.
 #include <algorithm>
+#include <type_traits>
 
 #include "tc.cuh"
 
@@ -44,7 +52,7 @@ constexpr int kMaxN = 256;               // pairs per tile (UMMA N <= 256)
 constexpr int kBRows = 64;               // pair rows per B TMA box
 constexpr int kExpThreads = 128;
 constexpr int kThreads = 352;
-constexpr int kSuper = 4;                // stages per code superstage (256 K, 64 code bytes per row)
+constexpr int kSuper = 4;                // stages per code superstage (256 K, 64 code bytes per row; FP4: 2)
 constexpr int kCSlots = 2;               // code superstages in flight
 constexpr uint32_t kABytes = kRowsA * 128;
 constexpr uint32_t kBBytes = kMaxN * 128;
@@ -69,6 +77,8 @@ struct GemmParams {
     const int32_t* sorted;
     const float* weights;
     uint32_t* status;
+    const float* scale_2;    // FP4 layer: per-tensor scale_2 of expert e at e * s2_stride (+1: up)
+    int32_t s2_stride;
 };
 
 __device__ __forceinline__ uint32_t word_i(const uint4& q, int i)
@@ -77,7 +87,7 @@ __device__ __forceinline__ uint32_t word_i(const uint4& q, int i)
 }
 
 // Row pointers of expansion thread r for item `it` (codes and scales of its A row).
-template <bool kGateUp>
+template <bool kGateUp, bool kW4>
 __device__ __forceinline__ void item_row(const GemmParams& p, int it, int r, const uint8_t*& rc, const uint8_t*& rs)
 {
     const int4 tile = p.tiles[it / p.row_blocks];
@@ -86,15 +96,16 @@ __device__ __forceinline__ void item_row(const GemmParams& p, int it, int r, con
     if (kGateUp) row = (r & 1 ? p.I : 0) + rb * 64 + (r >> 1);
     else row = rb * kRowsA + r;
     const int64_t grow = (int64_t)tile.x * p.rows_per_expert + row;
-    rc = p.codes + grow * (p.K / 4);
-    rs = p.scales + grow * (p.K / 32);
+    rc = p.codes + grow * (p.K / (kW4 ? 2 : 4));
+    rs = p.scales + grow * (p.K / (kW4 ? 16 : 32));
 }
 
-template <bool kGateUp>
+template <bool kGateUp, bool kW4>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap,
                                                                       const __grid_constant__ CUtensorMap cmap,
                                                                       GemmParams p)
 {
+    constexpr int kSup = kW4 ? 2 : kSuper;   // stages per code superstage
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -104,15 +115,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     __shared__ __align__(8) uint64_t cempty_bar[kCSlots];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
-    __shared__ uint2 lut_tab[256];
+    __shared__ std::conditional_t<kW4, uint4, uint2> lut_tab[256];
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const uint32_t smem_base = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     for (int s = tid; s < 256; s += kThreads) {
-        ScaleLut l = make_lut((uint32_t)s);
-        lut_tab[s] = make_uint2(l.lut, l.lo);
+        if constexpr (kW4) {
+            lut_tab[s] = make_fp4_lut((uint32_t)s);
+        } else {
+            ScaleLut l = make_lut((uint32_t)s);
+            lut_tab[s] = make_uint2(l.lut, l.lo);
+        }
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -145,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     // items of this CTA: blockIdx.x + n * gridDim.x, n = 0 .. my_items-1
     const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
-    const int n_super = (nk + kSuper - 1) / kSuper;   // code superstages per item
+    const int n_super = (nk + kSup - 1) / kSup;   // code superstages per item
     const uint32_t code_base = smem_base + kStages * kStageBytes;
 
     if (warp < 4) {
@@ -158,12 +173,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         const int trow = kGateUp ? ((r & 1) * 64 + (r >> 1)) : r;
         const uint32_t trow_addr = (uint32_t)trow * kCodeRowBytes;
         const uint32_t swz = (uint32_t)((trow >> 1) & 3);   // 64-byte swizzle: chunk j at j ^ ((row / 2) % 4)
-        // scale bytes of superstage su of item n (one 8-byte load: 4 stages x 2 bytes)
+        // scale bytes of superstage su of item n (one 8-byte load: 4 stages x 2
+        // UE8M0 bytes, or 2 stages x 4 e4m3 bytes)
+        uint32_t nan_seen = 0;
         auto load_scales = [&](int n, int su, uint2& s0) {
             const int it = blockIdx.x + n * (int)gridDim.x;
             const uint8_t *rc, *rs;
-            item_row<kGateUp>(p, it, r, rc, rs);
-            s0 = __ldg(reinterpret_cast<const uint2*>(rs + su * kSuper * 2));
+            item_row<kGateUp, kW4>(p, it, r, rc, rs);
+            s0 = __ldg(reinterpret_cast<const uint2*>(rs + su * 8));
+            if (kW4) nan_seen |= e4m3_nan_bytes(s0.x) | e4m3_nan_bytes(s0.y);
         };
         int n = 0, su = 0;           // current (item, superstage)
         uint2 sa = make_uint2(0, 0);
@@ -183,11 +201,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
             const uint32_t cslot = u % kCSlots;
             if (!mbar_wait(smem_u32(&cfull_bar[cslot]), (u / kCSlots) & 1u, abort)) break;
             const uint32_t ctile = code_base + cslot * kCodeBytes + trow_addr;
-            const int s_end = min(kSuper, nk - su * kSuper);
+            const int s_end = min(kSup, nk - su * kSup);
 #pragma unroll
-            for (int s = 0; s < kSuper; ++s) {
+            for (int s = 0; s < kSup; ++s) {
                 if (s >= s_end) break;
                 const uint32_t slot = g % kStages, ph = (g / kStages) & 1u;
+                if constexpr (kW4) {
+                    // 32 bytes of e2m1 (64 elements: four blocks of 16) and their four e4m3 bytes
+                    const uint4 c0q = lds_u4(ctile + ((((uint32_t)(2 * s)) ^ swz) << 4));
+                    const uint4 c1q = lds_u4(ctile + ((((uint32_t)(2 * s + 1)) ^ swz) << 4));
+                    const uint32_t sw = s ? sa.y : sa.x;
+                    if (!mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t a_tile = smem_base + slot * kStageBytes;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4& cq = i < 2 ? c0q : c1q;
+                        const uint4 L = lut_tab[(sw >> (8 * i)) & 0xFFu];
+                        uint32_t lo[4], hi[4];   // elements 0..7 and 8..15 of block i
+                        fp4_word_bf16(word_i(cq, 2 * (i & 1)), L, lo[0], lo[1], lo[2], lo[3]);
+                        fp4_word_bf16(word_i(cq, 2 * (i & 1) + 1), L, hi[0], hi[1], hi[2], hi[3]);
+                        // T16 storage order of the block: (e0,e4)(e8,e12)(e1,e5)(e9,e13) | (e2,e6)(e10,e14)(e3,e7)(e11,e15)
+                        sts_u4(a_tile + sw128_offset(r, 2 * i), make_uint4(lo[0], hi[0], lo[1], hi[1]));
+                        sts_u4(a_tile + sw128_offset(r, 2 * i + 1), make_uint4(lo[2], hi[2], lo[3], hi[3]));
+                    }
+                } else {
                 const uint4 cq = lds_u4(ctile + ((((uint32_t)s) ^ swz) << 4));
                 const uint32_t cs = ((s & 2 ? sa.y : sa.x) >> (16 * (s & 1))) & 0xFFFFu;
                 if (!mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort)) {
@@ -214,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
                     sts_u4(a_tile + sw128_offset(r, 2 * i), c0);
                     sts_u4(a_tile + sw128_offset(r, 2 * i + 1), c1);
                 }
+                }   // 2-bit planes
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&full_bar[slot]));
                 ++g;
@@ -226,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
             sa = na;
             if (n >= my_items) break;
         }
-        if (lut_min == 0) flag_status(p.status, MOE_W2_DEV_BAD_SCALE);
+        if (lut_min == 0 || nan_seen != 0) flag_status(p.status, MOE_W2_DEV_BAD_SCALE);
     } else if (warp == 4) {
         // ------------------------------------------------ TMA producer (B tiles)
         if (lane == 0) {
@@ -295,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
                     const uint32_t fb = smem_u32(&cfull_bar[cslot]);
                     mbar_arrive_expect_tx(fb, kCodeBytes);
                     const uint32_t dst = code_base + cslot * kCodeBytes;
-                    const int x = su * (int)kCodeRowBytes;   // byte column of the superstage
+                    const int x = su * (int)kCodeRowBytes;   // byte column of the superstage (64 bytes either way)
                     if (kGateUp) {
                         tma_load_2d(dst, &cmap, x, (int)(ebase + rb * 64), fb);
                         tma_load_2d(dst + 64 * kCodeRowBytes, &cmap, x, (int)(ebase + p.I + rb * 64), fb);
@@ -316,12 +357,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
             const int rb = it % p.row_blocks;
             const int q0 = tile.y, nrows = tile.z;
             const uint32_t b = n & 1;
+            // FP4 layer: this row's tensor scale_2 (gate_up: gate rows even, up rows odd)
+            const float s2 = kW4 ? __ldg(p.scale_2 + (int64_t)tile.x * p.s2_stride + (kGateUp ? (r & 1) : 0)) : 1.f;
             if (!mbar_wait(smem_u32(&dfull_bar[b]), (n >> 1) & 1u, abort)) break;
             tc_fence_after();
             const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + b * kMaxN;
             for (int c0 = 0; c0 < nrows; c0 += 32) {
                 float v[32];
                 tmem_ld32(lane_base + c0, v);
+                if (kW4) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] *= s2;
+                }
                 if (kGateUp) {
                     const int nn = rb * 64 + (r >> 1);
                     const int pos = t16_pos(nn);
@@ -365,21 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     if (tid == 0 && abort_flag) flag_status(p.status, kDevPipelineTimeout);
 }
 
-}  // namespace
-
-cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* weights, const moe_w2_planes& w,
-                           int32_t T, int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status, cudaStream_t s,
-                           const PhaseEvents& ev)
+template <bool kW4>
+cudaError_t launch_prefill_fmt(const uint16_t* x, const int32_t* ids, const float* weights, const LayerPlanes& w,
+                               int32_t T, int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status,
+                               cudaStream_t s, const PhaseEvents& ev)
 {
     const int32_t E = w.num_experts, H = w.hidden, I = w.inter;
     const int64_t P = (int64_t)T * k;
     static bool ready[kMaxDevices];
     int dev = 0;
     cudaError_t e0 = once_per_device(ready, dev, [](int) {
-        cudaError_t e = cudaFuncSetAttribute(tc_expert_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(tc_expert_gemm_kernel<true, kW4>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
-        return cudaFuncSetAttribute(tc_expert_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(tc_expert_gemm_kernel<false, kW4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kSmemBytes);
     });
     if (e0 != cudaSuccess) return e0;
@@ -391,11 +437,13 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
     CUtensorMap xmap, hmap, c13map, c2map;
     if ((e = make_tmap_2d(&xmap, ws.xa, true, P, H, 64, kBRows, 128)) != cudaSuccess) return e;
     if ((e = make_tmap_2d(&hmap, ws.h, true, P, I, 64, kBRows, 128)) != cudaSuccess) return e;
-    // raw code tiles: 64 bytes (256 codes) x 64 rows (gate_up: gate and up halves) or 128 rows
-    if ((e = make_tmap_2d(&c13map, w.w13_codes, false, (int64_t)E * 2 * I, H / 4, kCodeRowBytes, 64, 64)) !=
+    // raw code tiles: 64 bytes (256 2-bit codes or 128 e2m1) x 64 rows (gate_up:
+    // gate and up halves) or 128 rows
+    constexpr int per_byte = kW4 ? 2 : 4;
+    if ((e = make_tmap_2d(&c13map, w.w13_codes, false, (int64_t)E * 2 * I, H / per_byte, kCodeRowBytes, 64, 64)) !=
         cudaSuccess)
         return e;
-    if ((e = make_tmap_2d(&c2map, w.w2_codes, false, (int64_t)E * H, I / 4, kCodeRowBytes, kRowsA, 64)) !=
+    if ((e = make_tmap_2d(&c2map, w.w2_codes, false, (int64_t)E * H, I / per_byte, kCodeRowBytes, kRowsA, 64)) !=
         cudaSuccess)
         return e;
 
@@ -415,8 +463,11 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
     gp.sorted = ws.sorted;
     gp.weights = weights;
     gp.status = status;
+    gp.scale_2 = w.w13_scale_2;
+    gp.s2_stride = 2;
     const int64_t max_items = max_tiles(P, E, false) * (I / 64);
-    tc_expert_gemm_kernel<true><<<(int)std::min<int64_t>(sms, max_items), kThreads, kSmemBytes, s>>>(xmap, c13map, gp);
+    tc_expert_gemm_kernel<true, kW4><<<(int)std::min<int64_t>(sms, max_items), kThreads, kSmemBytes, s>>>(xmap, c13map,
+                                                                                                        gp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     if ((e = ev.record(2, s)) != cudaSuccess) return e;
@@ -426,11 +477,24 @@ cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* w
     dp.K = I;
     dp.rows_per_expert = H;
     dp.row_blocks = H / kRowsA;
+    dp.scale_2 = w.w2_scale_2;
+    dp.s2_stride = 1;
     const int64_t max_items_d = max_tiles(P, E, false) * (H / kRowsA);
-    tc_expert_gemm_kernel<false><<<(int)std::min<int64_t>(sms, max_items_d), kThreads, kSmemBytes, s>>>(hmap, c2map, dp);
+    tc_expert_gemm_kernel<false, kW4><<<(int)std::min<int64_t>(sms, max_items_d), kThreads, kSmemBytes, s>>>(
+        hmap, c2map, dp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     return launch_combine(ws.stage, ids, T, k, E, H, 1, 0, false, y, s);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const uint16_t* x, const int32_t* ids, const float* weights, const LayerPlanes& w,
+                           int32_t T, int32_t k, const Workspace& ws, uint16_t* y, uint32_t* status, cudaStream_t s,
+                           const PhaseEvents& ev)
+{
+    return w.w4 ? launch_prefill_fmt<true>(x, ids, weights, w, T, k, ws, y, status, s, ev)
+                : launch_prefill_fmt<false>(x, ids, weights, w, T, k, ws, y, status, s, ev);
 }
 
 }  // namespace moe_w2

@@ -40,6 +40,13 @@ class Planes(ctypes.Structure):
                 ("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32)]
 
 
+class W4Planes(ctypes.Structure):
+    """moe_w4_planes: the FP4 layer's NVFP4 experts."""
+    _fields_ = [("w13_e2m1", ctypes.c_void_p), ("w13_e4m3", ctypes.c_void_p), ("w13_scale_2", ctypes.c_void_p),
+                ("w2_e2m1", ctypes.c_void_p), ("w2_e4m3", ctypes.c_void_p), ("w2_scale_2", ctypes.c_void_p),
+                ("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32)]
+
+
 def forward_path(T: int, top_k: int, E: int, H: int, I: int) -> int:
     """moe_w2_forward_path: which kernels moe_w2_forward runs for these sizes (PATH_*)."""
     return int(load().moe_w2_forward_path(T, top_k, E, H, I))
@@ -82,6 +89,10 @@ def load(build_if_missing: bool = True):
     L.moe_w2_forward.restype = ctypes.c_int
     L.moe_w2_forward_noalloc.argtypes = [vp, vp, vp, ctypes.POINTER(Planes), i32, i32, vp, vp, vp]
     L.moe_w2_forward_noalloc.restype = ctypes.c_int
+    L.moe_w4_forward_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.moe_w4_forward_workspace_size.restype = sz
+    L.moe_w4_forward.argtypes = [vp, vp, vp, ctypes.POINTER(W4Planes), i32, i32, vp, vp, sz, vp, vp]
+    L.moe_w4_forward.restype = ctypes.c_int
     L.moe_w2_forward_cached_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.moe_w2_forward_cached_workspace_size.restype = sz
     L.moe_w2_forward_cached.argtypes = [vp, vp, vp, ctypes.POINTER(Planes), vp, i32, i32, i32, vp, vp, sz, vp, vp, vp]
@@ -156,6 +167,45 @@ def forward(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
                           _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
     if st != OK:
         raise MoeW2Error(st, "moe_w2_forward")
+    return y
+
+
+def make_w4_planes(planes: dict) -> W4Planes:
+    """W4Planes from the CUDA tensors w13_e2m1 u8 [E][2I][H/2], w13_e4m3 u8 [E][2I][H/16],
+    w13_scale_2 f32 [E][2], w2_e2m1 u8 [E][H][I/2], w2_e4m3 u8 [E][H][I/16], w2_scale_2 f32 [E]."""
+    for k in ("w13_e2m1", "w13_e4m3", "w2_e2m1", "w2_e4m3"):
+        _check_cuda(planes[k], k, torch.uint8)
+    for k in ("w13_scale_2", "w2_scale_2"):
+        _check_cuda(planes[k], k, torch.float32)
+    E, two_i, h2 = planes["w13_e2m1"].shape
+    return W4Planes(planes["w13_e2m1"].data_ptr(), planes["w13_e4m3"].data_ptr(), planes["w13_scale_2"].data_ptr(),
+                    planes["w2_e2m1"].data_ptr(), planes["w2_e4m3"].data_ptr(), planes["w2_scale_2"].data_ptr(),
+                    E, h2 * 2, two_i // 2)
+
+
+def w4_workspace_size(T: int, top_k: int, E: int, H: int, I: int) -> int:
+    return int(load().moe_w4_forward_workspace_size(T, top_k, E, H, I))
+
+
+def forward_w4(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, planes, y=None,
+               workspace=None, status=None, stream=None) -> torch.Tensor:
+    """y = the FP4 layer(x) through moe_w4_forward (NVFP4 experts, see make_w4_planes)."""
+    L = load()
+    _check_cuda(x, "x", torch.bfloat16)
+    _check_cuda(topk_ids, "topk_ids", torch.int32)
+    _check_cuda(topk_weights, "topk_weights", torch.float32)
+    p = planes if isinstance(planes, W4Planes) else make_w4_planes(planes)
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    need = w4_workspace_size(T, k, p.num_experts, p.hidden, p.inter)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    st = L.moe_w4_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), ctypes.byref(p), T, k, _ptr(y),
+                          _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    if st != OK:
+        raise MoeW2Error(st, "moe_w4_forward")
     return y
 
 

@@ -326,6 +326,53 @@ moe_w2_status moe_w2_debug_force_pipeline_timeout(int32_t enable);
 moe_w2_status moe_w2_requant_fp8(const uint8_t *w8, const float *scales, int64_t n, int64_t rows, int64_t K,
                                  uint8_t *codes, uint8_t *ue8m0, uint32_t *dev_status, void *stream);
 
+/*
+ * The FP4 layer ("vLLM-Moet wiki", "The kernels" and "FP4 recovery": moe_w4_mm,
+ * the same MoE forward over the NVFP4 experts, at twice the 2-bit plane bytes):
+ * every weight is e2m1 x e4m3 (one scale per 16 consecutive K elements of a row)
+ * x scale_2 (one per tensor: gate, up and down of each expert), taken exactly.
+ *   w13_e2m1     uint8 [E][2I][H/2]   two nibbles per byte, low nibble = even element;
+ *                                     rows 0..I-1 gate, I..2I-1 up
+ *   w13_e4m3     uint8 [E][2I][H/16]  e4m3fn block scales
+ *   w13_scale_2  float [E][2]         gate's and up's scale_2 (device memory)
+ *   w2_e2m1      uint8 [E][H][I/2]
+ *   w2_e4m3      uint8 [E][H][I/16]
+ *   w2_scale_2   float [E]            down's scale_2 (device memory)
+ * These are the modelopt NVFP4 tensors as moe_w2_requant takes them, laid out
+ * per expert like the 2-bit planes.
+ */
+typedef struct {
+    const uint8_t *w13_e2m1;
+    const uint8_t *w13_e4m3;
+    const float *w13_scale_2;
+    const uint8_t *w2_e2m1;
+    const uint8_t *w2_e4m3;
+    const float *w2_scale_2;
+    int32_t num_experts; /* E */
+    int32_t hidden;      /* H, multiple of 256 */
+    int32_t inter;       /* I, multiple of 256 */
+} moe_w4_planes;
+
+/* Bytes of device workspace moe_w4_forward needs (0 if the sizes are invalid). */
+size_t moe_w4_forward_workspace_size(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t I);
+
+/*
+ * moe_w2_forward over NVFP4 experts: for every token t and slot j with
+ * e = topk_ids[t][j], g = W_gate[e] x_t, u = W_up[e] x_t, h = bf16(SiLU(g) u),
+ * y_t = bf16(sum_j topk_weights[t][j] (W_down[e] h)), with each W the exact
+ * NVFP4 value above (e2m1 x e4m3 products are exact in bf16; scale_2
+ * multiplies the fp32 accumulations).  Arguments, alignment, checks, status
+ * bits and determinism as for moe_w2_forward; the four byte planes and the two
+ * scale_2 arrays must be 16- and 4-byte aligned.  An e4m3 NaN scale makes its
+ * 16 weights count as 0 and sets MOE_W2_DEV_BAD_SCALE; scale_2 is used as
+ * given (a non-finite one gives non-finite outputs).  T <= 64 runs the bf16
+ * mma.sync decode kernel (every active expert's planes streamed once per
+ * step), larger T the TMA + tcgen05 prefill kernels.
+ */
+moe_w2_status moe_w4_forward(const void *x_bf16, const int32_t *topk_ids, const float *topk_weights,
+                             const moe_w4_planes *w, int32_t T, int32_t top_k, void *y_bf16,
+                             void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *moe_w2_status_string(moe_w2_status s);
 

@@ -133,3 +133,23 @@ def test_fp4_loader_options_host_checks():
     assert L.moe_w2_requant_mxfp4(A + 8, A, 1, 4, 64, 0, A, A, None, None) == 1
     assert L.moe_w2_requant_mxfp4(A, A, 1, 4, 64, 0, A + 4, A, None, None) == 1
     assert L.moe_w2_requant_mxfp4(None, None, 0, 4, 64, 1, None, None, None, None) == 0
+
+
+def test_w4_forward_host_checks():
+    """moe_w4_forward: the same host checks as moe_w2_forward, plus its scale_2 arrays."""
+    L = moe_w2.load()
+    A = 0x10000000
+    need = moe_w2.w4_workspace_size(2, 2, 8, 512, 256)
+    assert need > 0 and moe_w2.w4_workspace_size(2, 2, 8, 500, 256) == 0
+    ok = moe_w2.W4Planes(A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, A + 0x5000, 8, 512, 256)
+
+    def fwd(p=ok, nbytes=need, T=2):
+        return L.moe_w4_forward(A, A, A, ctypes.byref(p), T, 2, A + 0x100000, A + 0x200000, nbytes, None, None)
+
+    assert L.moe_w4_forward(A, A, A, None, 2, 2, A, A, need, None, None) == 1
+    assert fwd(p=moe_w2.W4Planes(A, A + 0x1000, 0, A + 0x3000, A + 0x4000, A + 0x5000, 8, 512, 256)) == 1   # no scale_2
+    assert fwd(p=moe_w2.W4Planes(A, A + 0x1000, A + 0x2002, A + 0x3000, A + 0x4000, A + 0x5000, 8, 512, 256)) == 1
+    assert fwd(p=moe_w2.W4Planes(A, A + 0x1008, A + 0x2000, A + 0x3000, A + 0x4000, A + 0x5000, 8, 512, 256)) == 1
+    assert fwd(p=moe_w2.W4Planes(A, A, A, A, A, A, 8, 500, 256)) == 2
+    assert fwd(nbytes=need - 1) == 3
+    assert fwd(T=0) == 0

@@ -51,10 +51,12 @@ from bit_moe_expert_w2_gb300 import inputs  # noqa: E402
 
 METRIC = "w2 MoE layer tokens/s; plane HBM GB/s (decode), TFLOP/s (prefill) vs peak"
 DEFAULT_CONFIG = "decode_t1"
-EXTRA_CONFIGS = ("decode_t32", "prefill_t8192", "requant_256", "requant_fp8_16", "requant_mxfp4_16")
+EXTRA_CONFIGS = ("decode_t32", "prefill_t8192", "w4_decode_t1_e64", "w4_prefill_t8192_e64", "requant_256",
+                 "requant_fp8_16", "requant_mxfp4_16")
 DEFAULT_STEPS = {"decode_t1": 4000, "decode_t32": 1000, "prefill_t8192": 100, "requant_256": 10,
                  "decode_t1_e32": 4000, "prefill_t1024_e32": 400}
-EXTRA_STEPS = {"decode_t32": 500, "prefill_t8192": 50, "requant_256": 5, "requant_fp8_16": 5, "requant_mxfp4_16": 5}
+EXTRA_STEPS = {"decode_t32": 500, "prefill_t8192": 50, "w4_decode_t1_e64": 2000, "w4_prefill_t8192_e64": 30,
+               "requant_256": 5, "requant_fp8_16": 5, "requant_mxfp4_16": 5}
 POOL = 16
 # every file each kernel's translation unit compiles: a capture is stale once any changed
 KERNEL_SOURCES = {
@@ -240,7 +242,8 @@ def oracle_layer_rate(lay: inputs.LayerInputs, budget_s: float, max_tokens: int 
     T = lay.x.shape[0]
     while True:
         tok = np.array([done % T], np.int64)
-        oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes, tokens=tok)
+        fwd = oracle.forward_tokens_w4 if "w13_e2m1" in lay.planes else oracle.forward_tokens
+        fwd(lay.x, lay.ids, lay.weights, lay.planes, tokens=tok)
         done += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (max_tokens is not None and done >= max_tokens):
@@ -257,7 +260,8 @@ def oracle_layer_rate_all_cores(lay: inputs.LayerInputs, budget_s: float):
     done, t0 = 0, time.perf_counter()
     while True:
         tok = (np.arange(done, done + threads) % T).astype(np.int64)
-        oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes, tokens=tok, parallel=True)
+        fwd = oracle.forward_tokens_w4 if "w13_e2m1" in lay.planes else oracle.forward_tokens
+        fwd(lay.x, lay.ids, lay.weights, lay.planes, tokens=tok, parallel=True)
         done += threads
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -318,12 +322,13 @@ def oracle_requant_rate(gu: inputs.Nvfp4Tensors, budget_s: float):
 
 # ------------------------------------------------------------------ layer benchmark
 
-def layer_bench(cfg: inputs.LayerConfig, steps, warmup, world, rank, local):
+def layer_bench(cfg: inputs.LayerConfig, steps, warmup, world, rank, local, w4: bool = False):
+    """The 2-bit layer (moe_w2_forward), or with w4 the FP4 layer (moe_w4_forward)."""
     import torch
     from bit_moe_expert_w2_gb300 import moe_w2
 
     dev = torch.device("cuda", local)
-    lay = inputs.layer_inputs(cfg)
+    lay = inputs.w4_layer_inputs(cfg) if w4 else inputs.layer_inputs(cfg)
     T, H, I, E, k = cfg.tokens, cfg.hidden, cfg.inter, cfg.num_experts, cfg.top_k
     decode = T <= moe_w2.DECODE_MAX_TOKENS
     pool = POOL if decode else 2
@@ -338,8 +343,8 @@ def layer_bench(cfg: inputs.LayerConfig, steps, warmup, world, rank, local):
         batches.append((x, ids, w))
 
     planes = {kk: torch.from_numpy(v).to(dev) for kk, v in lay.planes.items()}
-    P = moe_w2.make_planes(planes)
-    ws_bytes = moe_w2.workspace_size(T, k, E, H, I)
+    P = moe_w2.make_w4_planes(planes) if w4 else moe_w2.make_planes(planes)
+    ws_bytes = (moe_w2.w4_workspace_size if w4 else moe_w2.workspace_size)(T, k, E, H, I)
     work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -351,11 +356,18 @@ def layer_bench(cfg: inputs.LayerConfig, steps, warmup, world, rank, local):
     dev_batches = [to_dev(*b) for b in batches]
     ys = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(pool)]
     # algorithmic plane bytes each step reads: every distinct expert's four sections, once
-    w13_b = 2 * I * (H // 4 + H // 32)
-    w2_b = H * (I // 4 + I // 32)
+    # (FP4 layer: e2m1 and e4m3 bytes, and the three scale_2 floats)
+    if w4:
+        w13_b = 2 * I * (H // 2 + H // 16) + 8
+        w2_b = H * (I // 2 + I // 16) + 4
+    else:
+        w13_b = 2 * I * (H // 4 + H // 32)
+        w2_b = H * (I // 4 + I // 32)
     distinct = [len(np.unique(b[1][(b[1] >= 0) & (b[1] < E)])) for b in batches]
 
     L = moe_w2.load()
+    f_plain = L.moe_w4_forward if w4 else L.moe_w2_forward
+    f_traced = L.moe_w4_forward_traced if w4 else L.moe_w2_forward_traced
     stream = torch.cuda.Stream(device=dev)
     n_ev = 4
 
@@ -370,19 +382,19 @@ def layer_bench(cfg: inputs.LayerConfig, steps, warmup, world, rank, local):
     def call(i, evs, s):
         x, ids, w = dev_batches[i]
         ev_ptrs = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in evs])
-        st = L.moe_w2_forward_traced(moe_w2._ptr(x), moe_w2._ptr(ids), moe_w2._ptr(w), ctypes.byref(P), T, k,
-                                     moe_w2._ptr(ys[i]), moe_w2._ptr(work), work.numel(), moe_w2._ptr(status),
-                                     ctypes.c_void_p(s.cuda_stream), ev_ptrs)
+        st = f_traced(moe_w2._ptr(x), moe_w2._ptr(ids), moe_w2._ptr(w), ctypes.byref(P), T, k,
+                      moe_w2._ptr(ys[i]), moe_w2._ptr(work), work.numel(), moe_w2._ptr(status),
+                      ctypes.c_void_p(s.cuda_stream), ev_ptrs)
         if st != 0:
-            raise moe_w2.MoeW2Error(st, "moe_w2_forward_traced")
+            raise moe_w2.MoeW2Error(st, "forward (traced)")
 
     def call_plain(i, s):
         x, ids, w = dev_batches[i]
-        st = L.moe_w2_forward(moe_w2._ptr(x), moe_w2._ptr(ids), moe_w2._ptr(w), ctypes.byref(P), T, k,
-                              moe_w2._ptr(ys[i]), moe_w2._ptr(work), work.numel(), moe_w2._ptr(status),
-                              ctypes.c_void_p(s.cuda_stream))
+        st = f_plain(moe_w2._ptr(x), moe_w2._ptr(ids), moe_w2._ptr(w), ctypes.byref(P), T, k,
+                     moe_w2._ptr(ys[i]), moe_w2._ptr(work), work.numel(), moe_w2._ptr(status),
+                     ctypes.c_void_p(s.cuda_stream))
         if st != 0:
-            raise moe_w2.MoeW2Error(st, "moe_w2_forward")
+            raise moe_w2.MoeW2Error(st, "forward")
 
     # two graphs per pool entry: the plain forward (timed for the step time and
     # `value`) and the traced forward with phase events (timed for the per-kernel
@@ -509,7 +521,7 @@ def layer_bench(cfg: inputs.LayerConfig, steps, warmup, world, rank, local):
         # one kernel streams the w13 and w2 planes of every active expert; its
         # time is phase 1 (phase 2: the combine kernel, empty when the layer
         # kernel combines itself)
-        kname = moe_w2.decode_kernel(T, k, H, I)
+        kname = "decode_mma_kernel" if w4 else moe_w2.decode_kernel(T, k, H, I)
         layer_kernel_ms = phase_ms[1]
         achieved = plane_bytes / (layer_kernel_ms / 1e3) / 1e9
         res["roofline"] = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
@@ -540,11 +552,13 @@ def layer_bench(cfg: inputs.LayerConfig, steps, warmup, world, rank, local):
     # decode: permute (+ x as T16 bf16 or e2m1 digit rows), the layer kernel (gate_up, down), and the
     # combine kernel after the block-scaled one;
     # prefill: permute, gather, gate_up, down, combine
-    res["kernels_per_step"] = (2 if moe_w2.decode_kernel(T, k, H, I) == "decode_mma_kernel" else 3) if decode else 5
+    block_scaled = decode and not w4 and moe_w2.decode_kernel(T, k, H, I) == "decode_layer_kernel"
+    res["kernels_per_step"] = (3 if block_scaled else 2) if decode else 5
     # arithmetic of the layer's contractions: the block-scaled decode kernel multiplies e2m1
-    # weights by five e2m1 digit rows per activation row under UE8M0 block scales; the others bf16
-    block_scaled = decode and moe_w2.decode_kernel(T, k, H, I) == "decode_layer_kernel"
-    res["dtype"] = "e2m1 x e2m1 digits block-scaled, fp32 accumulation" if block_scaled else "bf16, fp32 accumulation"
+    # weights by eight e2m1 digit rows per activation row under UE8M0 block scales; the others
+    # bf16 (the FP4 layer's weights are the exact bf16 products e2m1 x e4m3)
+    res["dtype"] = ("e2m1 x e2m1 digits block-scaled, fp32 accumulation" if block_scaled
+                    else "bf16 (exact e2m1 x e4m3 weights), fp32 accumulation" if w4 else "bf16, fp32 accumulation")
 
     # end to end: pinned host inputs -> device -> forward -> y back to pinned host.  A step's
     # x, ids and weights sit back to back in one pinned buffer, so they cross in one copy
@@ -568,11 +582,11 @@ def layer_bench(cfg: inputs.LayerConfig, steps, warmup, world, rank, local):
     def e2e_step(i):
         e_start[i].record(stream)
         din.copy_(hin[i], non_blocking=True)
-        st = L.moe_w2_forward(moe_w2._ptr(dx), moe_w2._ptr(did), moe_w2._ptr(dw), ctypes.byref(P), T, k,
-                              moe_w2._ptr(dy), moe_w2._ptr(work), work.numel(), moe_w2._ptr(status),
-                              ctypes.c_void_p(stream.cuda_stream))
+        st = f_plain(moe_w2._ptr(dx), moe_w2._ptr(did), moe_w2._ptr(dw), ctypes.byref(P), T, k,
+                     moe_w2._ptr(dy), moe_w2._ptr(work), work.numel(), moe_w2._ptr(status),
+                     ctypes.c_void_p(stream.cuda_stream))
         if st != 0:
-            raise moe_w2.MoeW2Error(st, "moe_w2_forward")
+            raise moe_w2.MoeW2Error(st, "forward")
         hy[i].copy_(dy.view(torch.int16), non_blocking=True)
         e_end[i].record(stream)
 
@@ -802,6 +816,9 @@ def run_config(name, steps, warmup, world, rank, local):
     if name in inputs.REQUANT_CASES:
         res, data = requant_bench(name, steps, warmup, world, rank, local)
         res["unit"] = "elements/s"
+    elif name in inputs.W4_CONFIGS:
+        res, data = layer_bench(inputs.W4_CONFIGS[name], steps, warmup, world, rank, local, w4=True)
+        res["unit"] = "tokens/s"
     else:
         res, data = layer_bench(inputs.CONFIGS[name], steps, warmup, world, rank, local)
         res["unit"] = "tokens/s"
@@ -814,7 +831,7 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=None,
-                    choices=[*inputs.CONFIGS, *inputs.REQUANT_CASES, *inputs.REQUANT_FP8_CASES,
+                    choices=[*inputs.CONFIGS, *inputs.W4_CONFIGS, *inputs.REQUANT_CASES, *inputs.REQUANT_FP8_CASES,
                              *inputs.REQUANT_MXFP4_CASES],
                     help=f"one workload only (default: {DEFAULT_CONFIG}, plus {', '.join(EXTRA_CONFIGS)} on one GPU)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -882,6 +899,10 @@ def workload_name(config: str) -> str:
         n = inputs.REQUANT_CASES[config] or r.num_experts
         return (f"{config}: {n} experts NVFP4 gate/up 2x[{r.inter}x{r.hidden}] + down [{r.hidden}x{r.inter}]"
                 " -> 2-bit planes")
+    if config in inputs.W4_CONFIGS:
+        cfg = inputs.W4_CONFIGS[config]
+        return (f"{cfg.name}: FP4 layer (NVFP4 experts) H={cfg.hidden} I={cfg.inter} E={cfg.num_experts} "
+                f"top-{cfg.top_k} T={cfg.tokens} routing={cfg.routing}")
     cfg = inputs.CONFIGS[config]
     return (f"{cfg.name}: H={cfg.hidden} I={cfg.inter} E={cfg.num_experts} top-{cfg.top_k} "
             f"T={cfg.tokens} routing={cfg.routing}")
@@ -902,8 +923,10 @@ def reference_arm(args, cores):
         unit, sample = "elements/s", f"{n} whole gate/up tensors of {args.config} in {el:.1f} s"
         steps = n
     else:
-        cfg = inputs.CONFIGS[args.config]
-        lay = inputs.layer_inputs(cfg)
+        if args.config in inputs.W4_CONFIGS:
+            lay = inputs.w4_layer_inputs(inputs.W4_CONFIGS[args.config])
+        else:
+            lay = inputs.layer_inputs(inputs.CONFIGS[args.config])
         # warm-up tokens, then timed tokens until the step count or the budget is reached
         oracle_layer_rate(lay, float("inf"), max_tokens=max(args.warmup, 3))
         v, n, el = oracle_layer_rate(lay, budget, max_tokens=args.steps)

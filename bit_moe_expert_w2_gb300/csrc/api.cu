@@ -313,6 +313,17 @@ moe_w2_status moe_w2_forward(const void* x_bf16, const int32_t* topk_ids, const 
                         nullptr, dev_status, stream, nullptr);
 }
 
+moe_w2_status moe_w4_forward_traced(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                                    const moe_w4_planes* w, int32_t T, int32_t top_k, void* y_bf16,
+                                    void* workspace, size_t workspace_bytes, uint32_t* dev_status, void* stream,
+                                    void* const* phase_events)
+{
+    if (!w) return MOE_W2_ERR_INVALID_ARG;
+    const LayerPlanes p = planes_of(w);
+    return forward_impl(x_bf16, topk_ids, topk_weights, &p, nullptr, 0, T, top_k, y_bf16, workspace, workspace_bytes,
+                        nullptr, dev_status, stream, phase_events);
+}
+
 size_t moe_w4_forward_workspace_size(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t I)
 {
     if (moe_w2_forward_workspace_size(T, top_k, E, H, I) == 0) return 0;

@@ -105,6 +105,12 @@ REQUANT = RequantConfig("requant_256", 256, 2048, 6144, 4)
 REQUANT_CASES = {"requant_256": None, "requant_16": 16}
 # FP8 block-128 loader workloads: experts of gate/up [I][H] x 2 and down [H][I]
 REQUANT_FP8_CASES = {"requant_fp8_16": 16}
+# The FP4 layer (NVFP4 experts): a decode step and a prefill step of the 2-bit
+# layers' shapes over 64 experts (a step of T = 1 streams 8 experts whatever E is)
+W4_CONFIGS = {
+    "w4_decode_t1_e64": LayerConfig("w4_decode_t1_e64", 6144, 2048, 64, 8, 1, -10, -6, "zipf", 21),
+    "w4_prefill_t8192_e64": LayerConfig("w4_prefill_t8192_e64", 4096, 2048, 64, 8, 8192, -10, -6, "logits", 22),
+}
 # MXFP4 loader workloads (e2m1 with UE8M0 block-32 scales), same expert shapes
 REQUANT_MXFP4_CASES = {"requant_mxfp4_16": 16}
 
@@ -408,12 +414,13 @@ def requant_mxfp4_inputs(cfg: RequantConfig = REQUANT, experts: int = 16):
 # --------------------------------------------------------------------------- FP4 layer
 
 def w4_planes(rng: np.random.Generator, E: int, H: int, I: int, scale_2: float = 2.0 ** -8) -> dict:
-    """NVFP4 expert planes of the FP4 layer, drawn as the NVFP4 loader workload is: e2m1
-    nibbles uniform over all 16 values, e4m3 block-16 scales log-uniform in [2^-6, 2^2],
-    one scale_2 per tensor (gate, up and down of every expert)."""
+    """NVFP4 expert planes of the FP4 layer: e2m1 nibbles uniform over all 16 values,
+    e4m3 block-16 scale bytes uniform over the positive codes of [2^-6, 4) (bytes 0x08 ..
+    0x47: eight per binade, so the scales are close to log-uniform), one scale_2 per tensor
+    (gate, up and down of every expert)."""
     def part(rows, K):
         e2m1 = random_bytes(rng, (E, rows, K // 2))
-        e4m3 = e4m3_round_positive(np.exp2(rng.uniform(-6.0, 2.0, size=(E, rows, K // 16))))
+        e4m3 = rng.integers(0x08, 0x48, size=(E, rows, K // 16), dtype=np.uint8)
         return e2m1, e4m3
     w13_e2m1, w13_e4m3 = part(2 * I, H)
     w2_e2m1, w2_e4m3 = part(H, I)

@@ -93,6 +93,8 @@ def load(build_if_missing: bool = True):
     L.moe_w4_forward_workspace_size.restype = sz
     L.moe_w4_forward.argtypes = [vp, vp, vp, ctypes.POINTER(W4Planes), i32, i32, vp, vp, sz, vp, vp]
     L.moe_w4_forward.restype = ctypes.c_int
+    L.moe_w4_forward_traced.argtypes = [vp, vp, vp, ctypes.POINTER(W4Planes), i32, i32, vp, vp, sz, vp, vp, vp]
+    L.moe_w4_forward_traced.restype = ctypes.c_int
     L.moe_w2_forward_cached_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.moe_w2_forward_cached_workspace_size.restype = sz
     L.moe_w2_forward_cached.argtypes = [vp, vp, vp, ctypes.POINTER(Planes), vp, i32, i32, i32, vp, vp, sz, vp, vp, vp]

@@ -373,6 +373,12 @@ moe_w2_status moe_w4_forward(const void *x_bf16, const int32_t *topk_ids, const 
                              const moe_w4_planes *w, int32_t T, int32_t top_k, void *y_bf16,
                              void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream);
 
+/* moe_w4_forward with the four phase events of moe_w2_forward_traced (profiling). */
+moe_w2_status moe_w4_forward_traced(const void *x_bf16, const int32_t *topk_ids, const float *topk_weights,
+                                    const moe_w4_planes *w, int32_t T, int32_t top_k, void *y_bf16,
+                                    void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream,
+                                    void *const *phase_events);
+
 /* Human-readable name of a status code (static string). */
 const char *moe_w2_status_string(moe_w2_status s);
 

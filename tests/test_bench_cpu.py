@@ -68,6 +68,9 @@ def test_every_workload_has_a_name_with_its_shape():
     for name, n in inputs.REQUANT_FP8_CASES.items():
         w = bench.workload_name(name)
         assert w.startswith(name + ":") and f"{n} experts FP8" in w
+    for name, cfg in inputs.W4_CONFIGS.items():
+        w = bench.workload_name(name)
+        assert w.startswith(name + ":") and "FP4 layer" in w and f"H={cfg.hidden}" in w and f"E={cfg.num_experts}" in w
     for name, n in inputs.REQUANT_MXFP4_CASES.items():
         w = bench.workload_name(name)
         assert w.startswith(name + ":") and f"{n} experts MXFP4" in w

@@ -62,6 +62,7 @@ POOL = 16
 KERNEL_SOURCES = {
     "decode_layer_kernel": ["bit_moe_expert_w2_gb300/csrc/decode.cu"],
     "decode_mma_kernel": ["bit_moe_expert_w2_gb300/csrc/decode_mma.cu"],
+    "decode_stream_kernel": ["bit_moe_expert_w2_gb300/csrc/decode_stream.cu"],
     "prefill_gate_up_kernel": ["bit_moe_expert_w2_gb300/csrc/prefill.cu"],
     "requant_kernel": ["bit_moe_expert_w2_gb300/csrc/requant.cu"],
     "requant_fp8_kernel": ["bit_moe_expert_w2_gb300/csrc/requant.cu"],

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_w2.so")
-SOURCES = ["api.cu", "permute.cu", "route.cu", "decode.cu", "decode_mma.cu", "prefill.cu", "requant.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "permute.cu", "route.cu", "decode.cu", "decode_stream.cu", "decode_mma.cu", "prefill.cu", "requant.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

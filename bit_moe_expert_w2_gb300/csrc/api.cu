@@ -15,6 +15,7 @@ constexpr int32_t kPrefillTileRows = 256;   // pairs per prefill tile (tcgen05 N
 constexpr int32_t kDecodeTileRows = 4;      // pairs per decode tile (MMA N = 32: kActDigits rows per pair)
 constexpr int32_t kDecodeMmaTileRows = 16;  // pairs per tile of the mma.sync decode kernel
 constexpr int64_t kDecodeMmaMaxPairs = 16;  // steps with at most this many pairs take the mma.sync kernel
+constexpr int64_t kDecodeStreamMaxPairs = 16; // ... or, when selected, the stream-K kernel
 constexpr int64_t kDecodeTargetItems = 1200; // down items per step that keep every CTA busy
 constexpr int64_t kDecodeSplitMaxPairs = 32;  // steps of up to this many pairs may split gate_up K in two
 constexpr int32_t kDecodeMinSegChunks = 2;   // at least 2 chunks of 256 K per decode item
@@ -52,6 +53,7 @@ moe_w2_status check_device()
 }
 
 std::atomic<int> g_force_timeout{0};
+std::atomic<int> g_decode_stream{0};   // moe_w2_set_decode_stream
 
 DepWait dependency_wait()
 {
@@ -99,6 +101,13 @@ DecodeSplit decode_split(int64_t P, int32_t E, int32_t H, int32_t I)
 
 // The block-scaled kernel loads weight-row scale groups by TMA, whose rows
 // (H/32, I/32 bytes) must be multiples of 16 bytes.
+bool decode_use_stream(int64_t P, int32_t H, int32_t I)
+{
+    // (its scale tiles hold whole scale rows of at most 224 bytes)
+    return g_decode_stream.load(std::memory_order_relaxed) != 0 && P <= kDecodeStreamMaxPairs && H % 512 == 0 &&
+           I % 512 == 0 && H <= 7168 && I <= 7168;
+}
+
 bool decode_use_mma(int64_t P, int32_t H, int32_t I)
 {
     return P <= kDecodeMmaMaxPairs || H % 512 != 0 || I % 512 != 0;
@@ -131,7 +140,15 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
     w.active_count = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * 2));
     w.tile_count = w.active_count + 1;
     w.tiles = reinterpret_cast<int4*>(take(sizeof(int4) * max_tiles(P, E, decode)));
-    if (decode && (w4 || decode_use_mma(P, H, I))) {
+    if (decode && !w4 && decode_use_stream(P, H, I)) {
+        w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * stream_counter_count(P, H, I)));
+        w.xd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * T * (H / 2)));
+        w.sxd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * T * (H / 32)));
+        w.hd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * P * (I / 2)));
+        w.shd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * P * (I / 32)));
+        w.stage = reinterpret_cast<float*>(take(sizeof(float) * P * H));
+        w.gu_part = reinterpret_cast<float*>(take(sizeof(float) * 2 * stream_part_floats()));
+    } else if (decode && (w4 || decode_use_mma(P, H, I))) {
         w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * decode_counter_count(P, E, H, I, true)));
         w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * T * H));
         w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * P * I));
@@ -195,23 +212,31 @@ moe_w2_status forward_impl(const void* x_bf16, const int32_t* topk_ids, const fl
     if (ev.record(0, s) != cudaSuccess) return MOE_W2_ERR_CUDA;
     const int64_t P = (int64_t)T * top_k;
     // the FP4 layer's decode steps all take the mma.sync kernel
-    const bool mma = decode && (w->w4 || decode_use_mma(P, H, I));
+    const bool use_stream = decode && !w->w4 && decode_use_stream(P, H, I);
+    const bool mma = decode && !use_stream && (w->w4 || decode_use_mma(P, H, I));
+    const bool digits = decode && !mma;   // x as e2m1 digit rows for a block-scaled kernel
     PermuteSlots slots{};
     if (cached) slots = PermuteSlots{slot_of, n_route, ws.ids_eff, misses};
     cudaError_t e = launch_permute(topk_ids, slots, T, top_k, E, ws.sorted, ws.inv, ws.offsets, ws.active,
                                    ws.active_count, ws.tiles, ws.tile_count,
                                    !decode ? kPrefillTileRows : mma ? kDecodeMmaTileRows : kDecodeTileRows,
-                                   decode ? x : nullptr, mma ? ws.xa : nullptr, decode && !mma ? ws.xd : nullptr,
-                                   decode && !mma ? ws.sxd : nullptr, H, ws.counters,
-                                   decode ? (int32_t)decode_counter_count(P, E, H, I, mma) : 0, decode ? y : nullptr,
+                                   decode ? x : nullptr, mma ? ws.xa : nullptr, digits ? ws.xd : nullptr,
+                                   digits ? ws.sxd : nullptr, H, ws.counters,
+                                   !decode ? 0
+                                   : use_stream ? (int32_t)stream_counter_count(P, H, I)
+                                            : (int32_t)decode_counter_count(P, E, H, I, mma),
+                                   decode ? y : nullptr,
                                    dev_status, s);
     if (e != cudaSuccess) return MOE_W2_ERR_CUDA;
     // the later kernels read the ids only to tell kept pairs from left-out ones
     const int32_t* ids = cached ? ws.ids_eff : topk_ids;
-    if (mma) {
+    const moe_w2_planes p2{w->w13_codes, w->w13_scales, w->w2_codes, w->w2_scales, E, H, I};
+    if (use_stream) {
+        e = launch_decode_stream(ids, topk_ids, slot_of, n_route, topk_weights, p2, T, top_k, ws, y, dev_status, s,
+                                 ev);
+    } else if (mma) {
         e = launch_decode_mma(ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
     } else if (decode) {
-        const moe_w2_planes p2{w->w13_codes, w->w13_scales, w->w2_codes, w->w2_scales, E, H, I};
         e = launch_decode(x, ids, topk_weights, p2, T, top_k, ws, y, dev_status, s, ev);
     } else {
         e = launch_prefill(x, ids, topk_weights, *w, T, top_k, ws, y, dev_status, s, ev);
@@ -248,6 +273,12 @@ moe_w2_status moe_w2_debug_force_pipeline_timeout(int32_t enable)
     return MOE_W2_OK;
 }
 
+moe_w2_status moe_w2_set_decode_stream(int32_t enable)
+{
+    g_decode_stream.store(enable != 0 ? 1 : 0, std::memory_order_relaxed);
+    return MOE_W2_OK;
+}
+
 const char* moe_w2_status_string(moe_w2_status s)
 {
     switch (s) {
@@ -272,7 +303,9 @@ int moe_w2_forward_path(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t 
 {
     if (T <= 0 || moe_w2_forward_workspace_size(T, top_k, E, H, I) == 0) return MOE_W2_PATH_NONE;
     if (T > MOE_W2_DECODE_MAX_TOKENS) return MOE_W2_PATH_PREFILL;
-    return decode_use_mma((int64_t)T * top_k, H, I) ? MOE_W2_PATH_DECODE_MMA : MOE_W2_PATH_DECODE_BLOCK_SCALED;
+    const int64_t P = (int64_t)T * top_k;
+    if (decode_use_stream(P, H, I)) return MOE_W2_PATH_DECODE_STREAM;
+    return decode_use_mma(P, H, I) ? MOE_W2_PATH_DECODE_MMA : MOE_W2_PATH_DECODE_BLOCK_SCALED;
 }
 
 moe_w2_status moe_w2_permute(const int32_t* topk_ids, int32_t T, int32_t top_k, int32_t E, int32_t* sorted_pairs,

@@ -287,10 +287,19 @@ struct DecodeSplit {
     int32_t s_dn, l_dn;   // down: segments, chunks per segment (K = I)
 };
 DecodeSplit decode_split(int64_t P, int32_t E, int32_t H, int32_t I);
-// True when a decode step of P pairs takes the bf16 mma.sync decode kernel
-// (decode_mma.cu): few pairs, or H or I not a multiple of 512; otherwise the
-// block-scaled kernel (decode.cu) runs it.
+// Which decode kernel a step of P pairs of the 2-bit layer takes: at most 16
+// pairs with H and I multiples of 512 up to 7168, the stream-K block-scaled kernel
+// (decode_stream.cu); other shapes with H or I not a multiple of 512, the bf16
+// mma.sync kernel (decode_mma.cu); the rest, the block-scaled kernel
+// (decode.cu).  (The block-scaled kernels load weight-row scale groups by TMA,
+// whose rows, H/32 and I/32 bytes, must be multiples of 16 bytes.)
+bool decode_use_stream(int64_t P, int32_t H, int32_t I);
 bool decode_use_mma(int64_t P, int32_t H, int32_t I);
+// The stream-K decode kernel: counters it needs zeroed, and the floats of each
+// of its two partial-sum buffers (one CTA per SM, at most kMaxStreamGrid).
+constexpr int kMaxStreamGrid = 256;
+int64_t stream_counter_count(int64_t P, int32_t H, int32_t I);
+size_t stream_part_floats();
 
 struct Workspace {
     int32_t* sorted;       // [P]
@@ -313,7 +322,8 @@ struct Workspace {
     uint8_t* sxd;          // their UE8M0 bytes [8T][H/32]
     uint8_t* hd;           // e2m1 digit rows of h, kActDigits per pair (expert order) [8P][I/2]
     uint8_t* shd;          // their UE8M0 bytes [8P][I/32]
-    float* gu_part;        // gate_up partial sums of the two K halves [2][P][2I] (small steps only, else null)
+    float* gu_part;        // block-scaled kernel: gate_up partial sums of the two K halves [2][P][2I] (small
+                           // steps only, else null); stream-K kernel: its gate_up then down partial sums
     // behind an expert cache
     int32_t* ids_eff;      // slot of each pair, -1 when left out [P] (null without a residency table)
     DecodeSplit split;
@@ -370,6 +380,13 @@ cudaError_t launch_permute(const int32_t* ids, const PermuteSlots& slots, int32_
 cudaError_t launch_decode_mma(const int32_t* ids, const float* weights, const LayerPlanes& w, int32_t T, int32_t k,
                               const Workspace& ws, uint16_t* y, uint32_t* status, cudaStream_t s,
                               const PhaseEvents& ev);
+// ids: the pairs' experts as the permutation sorted them (cache slots behind an
+// expert cache); route_ids: the routed expert ids (the tiles' canonical order);
+// slot_of, n_route: the residency table behind an expert cache (else null, 0).
+cudaError_t launch_decode_stream(const int32_t* ids, const int32_t* route_ids, const int32_t* slot_of,
+                                 int32_t n_route, const float* weights, const moe_w2_planes& w, int32_t T, int32_t k,
+                                 const Workspace& ws, uint16_t* y, uint32_t* status, cudaStream_t s,
+                                 const PhaseEvents& ev);
 cudaError_t launch_decode(const uint16_t* x, const int32_t* ids, const float* weights,
                           const moe_w2_planes& w, int32_t T, int32_t k, const Workspace& ws, uint16_t* y,
                           uint32_t* status, cudaStream_t s, const PhaseEvents& ev);

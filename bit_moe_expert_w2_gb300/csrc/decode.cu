@@ -732,8 +732,9 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_con
     }
 
     tc_fence_before();
-    __syncthreads();
+    cta_barrier_all_threads();   // every thread done before tensor memory is freed
     if (warp == 0) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tm, kTmemCols);
     }

@@ -404,8 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     }
 
     tc_fence_before();
-    __syncthreads();
+    cta_barrier_all_threads();   // every thread done before tensor memory is freed
     if (warp == 0) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }

@@ -72,6 +72,42 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// CTA-wide barrier that counts threads, for the end of a kernel whose warps ran
+// roles on single lanes: __syncthreads (bar.sync) counts a warp at each of its
+// arrivals and its lanes may arrive apart after diverging, so it could release
+// before every warp is done; the non-aligned barrier.sync waits for all threads.
+__device__ __forceinline__ void cta_barrier_all_threads() { asm volatile("barrier.sync 0;" ::: "memory"); }
+
+// Bounded wait as mbar_wait for a thread off the critical path: it sleeps about
+// `ns` between polls, so that a warp that waits leaves its sub-partition's issue
+// slots to the warps that work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        __nanosleep(ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// The whole warp waits (bounded) while lane 0 alone polls, sleeping about `ns`
+// between polls; every lane gets lane 0's result, and the lanes' later accesses
+// are ordered after lane 0's observation of the phase (__syncwarp).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t ns)
+{
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_sleep(bar, parity, abort, ns) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
 // Both barriers' phases complete (bounded as mbar_wait); the two first polls are
 // issued back to back so that their latencies overlap.
 __device__ __forceinline__ bool mbar_wait2(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, volatile int* abort)

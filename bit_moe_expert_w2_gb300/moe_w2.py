@@ -24,7 +24,7 @@ DEV_BAD_NVFP4 = 4
 DEV_PIPELINE_TIMEOUT = 0x80000000   # as a uint32; reads back as a negative int32 from a torch int32 tensor
 REQUANT_BALANCE_ZERO_SIGNS = 1       # option bit of requant (moe_w2_requant_ex) and requant_mxfp4
 DECODE_MAX_TOKENS = 64
-PATH_NONE, PATH_DECODE_MMA, PATH_DECODE_BLOCK_SCALED, PATH_PREFILL = 0, 1, 2, 3   # moe_w2_forward_path
+PATH_NONE, PATH_DECODE_MMA, PATH_DECODE_BLOCK_SCALED, PATH_PREFILL, PATH_DECODE_STREAM = 0, 1, 2, 3, 4   # moe_w2_forward_path
 NOALLOC_WORKSPACE_BYTES = 8 << 20   # MOE_W2_NOALLOC_WORKSPACE_BYTES
 
 
@@ -55,9 +55,34 @@ def forward_path(T: int, top_k: int, E: int, H: int, I: int) -> int:
 def decode_kernel(T: int, top_k: int, H: int, I: int) -> str:
     """Name of the kernel that runs the layer of a decode step (T <= DECODE_MAX_TOKENS)."""
     path = forward_path(T, top_k, 1, H, I)
-    if path not in (PATH_DECODE_MMA, PATH_DECODE_BLOCK_SCALED):
+    names = {PATH_DECODE_MMA: "decode_mma_kernel", PATH_DECODE_BLOCK_SCALED: "decode_layer_kernel",
+             PATH_DECODE_STREAM: "decode_stream_kernel"}
+    if path not in names:
         raise ValueError(f"T={T} top_k={top_k} H={H} I={I} is not a decode step")
-    return "decode_mma_kernel" if path == PATH_DECODE_MMA else "decode_layer_kernel"
+    return names[path]
+
+
+def set_decode_stream(enable: bool) -> None:
+    """moe_w2_set_decode_stream: run decode steps of at most 16 pairs on the
+    stream-K kernel (True) or on the mma.sync kernel (False, the default)."""
+    load().moe_w2_set_decode_stream(1 if enable else 0)
+
+
+class decode_stream:
+    """Context manager: the stream-K kernel for the smallest decode steps inside
+    the block, the previous choice restored after it."""
+
+    def __init__(self, enable: bool = True):
+        self.enable = enable
+
+    def __enter__(self):
+        self.prev = forward_path(1, 1, 1, 512, 512) == PATH_DECODE_STREAM
+        set_decode_stream(self.enable)
+        return self
+
+    def __exit__(self, *exc):
+        set_decode_stream(self.prev)
+        return False
 
 
 def lib_path() -> str:
@@ -109,6 +134,8 @@ def load(build_if_missing: bool = True):
     L.moe_w2_requant_fp8.restype = ctypes.c_int
     L.moe_w2_debug_force_pipeline_timeout.argtypes = [i32]
     L.moe_w2_debug_force_pipeline_timeout.restype = ctypes.c_int
+    L.moe_w2_set_decode_stream.argtypes = [i32]
+    L.moe_w2_set_decode_stream.restype = ctypes.c_int
     _lib = L
     return L
 

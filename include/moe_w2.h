@@ -102,10 +102,13 @@ typedef struct {
 size_t moe_w2_forward_workspace_size(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t I);
 
 /* Which kernels moe_w2_forward runs for these sizes (host only, no device
- * access): MOE_W2_PATH_DECODE_MMA for decode steps (T <= 64) of at most 16
- * pairs, or with H or I not a multiple of 512 (the bf16 mma.sync kernel);
- * MOE_W2_PATH_DECODE_BLOCK_SCALED for the other decode steps (the tcgen05
- * block-scaled kernel and its combine); MOE_W2_PATH_PREFILL for T > 64 (the
+ * access): MOE_W2_PATH_DECODE_STREAM for decode steps (T <= 64) of at most 16
+ * pairs with H and I multiples of 512 (the stream-K tcgen05 block-scaled
+ * kernel, one CTA per SM, y summed in the same launch);
+ * MOE_W2_PATH_DECODE_MMA for decode steps with H or I not a multiple of 512
+ * (the bf16 mma.sync kernel); MOE_W2_PATH_DECODE_BLOCK_SCALED for the other
+ * decode steps (the tcgen05 block-scaled kernel and its combine);
+ * MOE_W2_PATH_PREFILL for T > 64 (the
  * gather, the two tcgen05 GEMMs and the combine); MOE_W2_PATH_NONE when the
  * sizes are invalid (moe_w2_forward_workspace_size would return 0) or T = 0.
  * The pages describe no such entry point: it keeps the dispatch rule in one
@@ -114,6 +117,7 @@ size_t moe_w2_forward_workspace_size(int32_t T, int32_t top_k, int32_t E, int32_
 #define MOE_W2_PATH_DECODE_MMA 1
 #define MOE_W2_PATH_DECODE_BLOCK_SCALED 2
 #define MOE_W2_PATH_PREFILL 3
+#define MOE_W2_PATH_DECODE_STREAM 4
 int moe_w2_forward_path(int32_t T, int32_t top_k, int32_t E, int32_t H, int32_t I);
 
 /*
@@ -306,6 +310,20 @@ moe_w2_status moe_w2_requant_mxfp4(const uint8_t *e2m1, const uint8_t *scales, i
  * operation for the calls that follow.  Always returns MOE_W2_OK.
  */
 moe_w2_status moe_w2_debug_force_pipeline_timeout(int32_t enable);
+
+/*
+ * Kernel choice for the smallest decode steps (at most 16 pairs, H and I
+ * multiples of 512 and at most 7168).  With enable != 0, every later call in
+ * this process (any thread, any device) runs such steps on the stream-K kernel
+ * (MOE_W2_PATH_DECODE_STREAM: one CTA per SM streams every active expert's
+ * planes, multiplied on the tensor cores in block-scaled FP4); with enable = 0
+ * (the default) they run on the mma.sync kernel (MOE_W2_PATH_DECODE_MMA).  Both
+ * compute the same layer ("vLLM-Moet wiki", section "The kernels") within the
+ * same error bound.  The workspace a step needs depends on the choice
+ * (moe_w2_forward_workspace_size answers for the current one; a forward given
+ * less returns MOE_W2_ERR_WORKSPACE).  Always returns MOE_W2_OK.
+ */
+moe_w2_status moe_w2_set_decode_stream(int32_t enable);
 
 /*
  * Load-time re-quantizer for FP8 block-quantised checkpoints ("The v0.24.0

@@ -95,10 +95,23 @@ def test_forward_path_names_the_kernels_a_call_runs():
     assert P.forward_path(8192, 8, 256, 4096, 2048) == P.PATH_PREFILL
     assert P.forward_path(32, 8, 8, 768, 512) == P.PATH_DECODE_MMA                # H not a multiple of 512
     assert P.forward_path(32, 8, 8, 512, 256) == P.PATH_DECODE_MMA                # I not a multiple of 512
+    assert P.forward_path(1, 8, 8, 512, 256) == P.PATH_DECODE_MMA
     assert P.forward_path(0, 8, 256, 6144, 2048) == P.PATH_NONE
     assert P.forward_path(4, 2, 8, 500, 256) == P.PATH_NONE                       # invalid H
     assert P.decode_kernel(1, 8, 6144, 2048) == "decode_mma_kernel"
     assert P.decode_kernel(32, 8, 6144, 2048) == "decode_layer_kernel"
+    with P.decode_stream():
+        # the stream-K kernel, where selected, takes steps of at most 16 pairs
+        # with H and I multiples of 512 (up to 7168)
+        assert P.forward_path(1, 8, 256, 6144, 2048) == P.PATH_DECODE_STREAM
+        assert P.forward_path(2, 8, 256, 6144, 2048) == P.PATH_DECODE_STREAM
+        assert P.forward_path(3, 8, 256, 6144, 2048) == P.PATH_DECODE_BLOCK_SCALED
+        assert P.forward_path(1, 8, 8, 512, 256) == P.PATH_DECODE_MMA
+        assert P.forward_path(1, 8, 8, 7680, 2048) == P.PATH_DECODE_MMA
+        assert P.decode_kernel(1, 8, 6144, 2048) == "decode_stream_kernel"
+        assert P.decode_kernel(1, 8, 6144, 1792) == "decode_mma_kernel"
+        assert P.workspace_size(1, 8, 256, 6144, 2048) > 0
+    assert P.forward_path(1, 8, 256, 6144, 2048) == P.PATH_DECODE_MMA
 
 
 def test_cached_forward_host_checks():

@@ -1,8 +1,8 @@
 """GPU parity of moe_w2_forward_cached, the forward behind an expert cache.
 
 The planes hold resident experts in slots and a residency table maps routed
-expert ids to slots (negative: not resident).  Checked on the three paths
-(mma.sync decode, block-scaled decode, prefill) and on the decode_t1 layer:
+expert ids to slots (negative: not resident).  Checked on the four paths
+(mma.sync, block-scaled and stream-K decode, prefill) and on the decode_t1 layer:
   * every expert resident, slots in a random order with free slots full of
     other weights: y bitwise equal to moe_w2_forward over the planes in expert
     order (the replay after a miss reproduces the resident forward), no misses;
@@ -24,8 +24,17 @@ pytestmark = pytest.mark.gpu
 
 BAD_EXPERT_ID = 1
 
-# (H, I, E, k, T): mma.sync decode, block-scaled decode, prefill
-SHAPES = [(256, 256, 8, 4, 2), (512, 512, 8, 4, 8), (256, 512, 8, 2, 80)]
+# (H, I, E, k, T, stream): mma.sync decode, block-scaled decode, prefill, and
+# the stream-K decode kernel (selected by moe_w2_set_decode_stream)
+SHAPES = [(256, 256, 8, 4, 2, False), (512, 512, 8, 4, 8, False), (256, 512, 8, 2, 80, False),
+          (512, 512, 8, 4, 2, True)]
+
+
+@pytest.fixture(autouse=True)
+def _decode_kernel_choice(request):
+    params = getattr(getattr(request.node, "callspec", None), "params", {})
+    with moe_w2.decode_stream(bool(params.get("stream", False))):
+        yield
 
 
 def _slot_planes(planes, slot_of, S, rng):
@@ -57,8 +66,8 @@ def _plain(lay, planes_dev):
     return from_dev_bf16(y), int(st.item())
 
 
-@pytest.mark.parametrize("H,I,E,k,T", SHAPES)
-def test_all_resident_is_bitwise_the_plain_forward(H, I, E, k, T):
+@pytest.mark.parametrize("H,I,E,k,T,stream", SHAPES)
+def test_all_resident_is_bitwise_the_plain_forward(H, I, E, k, T, stream):
     rng = np.random.default_rng(H + T)
     lay = inputs.small_layer_inputs(H, I, E, k, T, 70 + T)
     S = E + 5
@@ -69,8 +78,8 @@ def test_all_resident_is_bitwise_the_plain_forward(H, I, E, k, T):
     assert np.array_equal(y_c, y_p), f"{moe_w2.forward_path(T, k, S, H, I)}: cached y differs from the plain forward"
 
 
-@pytest.mark.parametrize("H,I,E,k,T", SHAPES)
-def test_missing_experts_contribute_zero_and_are_counted(H, I, E, k, T):
+@pytest.mark.parametrize("H,I,E,k,T,stream", SHAPES)
+def test_missing_experts_contribute_zero_and_are_counted(H, I, E, k, T, stream):
     rng = np.random.default_rng(H + T + 1)
     lay = inputs.small_layer_inputs(H, I, E, k, T, 80 + T)
     S = E
@@ -86,16 +95,16 @@ def test_missing_experts_contribute_zero_and_are_counted(H, I, E, k, T):
     assert_close_layer(y, ref, f"cached, {len(missing)} experts missing, T={T} H={H} I={I}")
 
 
-@pytest.mark.parametrize("H,I,E,k,T", SHAPES)
-def test_every_expert_missing_gives_zero(H, I, E, k, T):
+@pytest.mark.parametrize("H,I,E,k,T,stream", SHAPES)
+def test_every_expert_missing_gives_zero(H, I, E, k, T, stream):
     lay = inputs.small_layer_inputs(H, I, E, k, T, 90 + T)
     slot_of = np.full(E, -1, np.int32)
     y, st, m = _cached(lay, planes_to_dev(lay.planes), slot_of)
     assert st == 0 and m == T * k and (y == 0).all()
 
 
-@pytest.mark.parametrize("H,I,E,k,T", SHAPES)
-def test_ids_past_the_table_and_slots_past_the_planes(H, I, E, k, T):
+@pytest.mark.parametrize("H,I,E,k,T,stream", SHAPES)
+def test_ids_past_the_table_and_slots_past_the_planes(H, I, E, k, T, stream):
     rng = np.random.default_rng(H + T + 2)
     lay = inputs.small_layer_inputs(H, I, E, k, T, 100 + T)
     S = E

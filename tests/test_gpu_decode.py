@@ -28,6 +28,12 @@ def _run(lay: inputs.LayerInputs, planes_dev=None, ids=None, weights=None):
     return from_dev_bf16(y), int(st.item())
 
 
+@pytest.fixture
+def stream_kernel():
+    # the stream-K kernel for steps of at most 16 pairs (H, I multiples of 512)
+    with moe_w2.decode_stream():
+        yield
+
 def test_tiny_config_all_tokens():
     lay = inputs.layer_inputs(inputs.CONFIGS["tiny"])
     y, st = _run(lay)
@@ -67,21 +73,63 @@ def test_duplicates_invalid_ids_and_zero_weights():
     assert np.all(y[3] == 0)
 
 
-@pytest.mark.parametrize("H,I,T,seed", [(512, 256, 4, 12), (512, 512, 16, 13)])
-def test_bad_scale_bytes_zero_their_blocks(H, I, T, seed):
-    # (512, 256, T=4): the mma.sync kernel; (512, 512, T=16, 32 pairs): the block-scaled kernel
+@pytest.mark.parametrize("H,I,T,seed,kernel", [(512, 256, 4, 12, "decode_mma_kernel"),
+                                                (512, 512, 16, 13, "decode_layer_kernel"),
+                                                (512, 512, 4, 14, "decode_stream_kernel")])
+def test_bad_scale_bytes_zero_their_blocks(H, I, T, seed, kernel):
     lay = inputs.small_layer_inputs(H, I, 4, 2, T, seed)
-    assert moe_w2.decode_kernel(T, 2, H, I) == ("decode_mma_kernel" if I == 256 else "decode_layer_kernel")
     planes = {k: v.copy() for k, v in lay.planes.items()}
     planes["w13_scales"][1, 5, 3] = 0
     planes["w2_scales"][2, 7, 1] = 255
     planes["w2_scales"][0, 100, 0] = 253
     planes["w13_scales"][3, 2 * I - 1, H // 32 - 1] = 0   # last block of the last up row
-    y, st = _run(lay, planes_dev=planes_to_dev(planes))
+    with moe_w2.decode_stream(kernel == "decode_stream_kernel"):
+        assert moe_w2.decode_kernel(T, 2, H, I) == kernel
+        y, st = _run(lay, planes_dev=planes_to_dev(planes))
     ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, planes)
     assert rst == moe_w2.DEV_BAD_SCALE
     assert st & moe_w2.DEV_BAD_SCALE
     assert_close_layer(y, ref, "bad scales")
+
+
+# Steps of at most 16 pairs with H and I multiples of 512, where the stream-K
+# kernel is selected (one CTA per SM): small layers leave most CTAs without
+# chunks, and the larger ones cut row blocks between CTAs at many places.
+@pytest.mark.parametrize("H,I,E,k,T,seed", [(512, 512, 8, 2, 1, 70), (512, 512, 4, 1, 1, 71),
+                                            (1024, 512, 16, 4, 4, 72), (512, 1024, 64, 16, 1, 73),
+                                            (1536, 1024, 8, 8, 2, 74), (2048, 1536, 32, 8, 2, 75),
+                                            (6144, 2048, 16, 4, 4, 76), (4096, 2048, 32, 8, 1, 77)])
+@pytest.mark.usefixtures("stream_kernel")
+def test_stream_kernel_shapes_all_tokens(H, I, E, k, T, seed):
+    assert moe_w2.decode_kernel(T, k, H, I) == "decode_stream_kernel"
+    lay = inputs.small_layer_inputs(H, I, E, k, T, seed)
+    y, st = _run(lay)
+    ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes)
+    assert st == rst == 0
+    assert_close_layer(y, ref, f"stream kernel H{H} I{I} E{E} k{k} T{T}")
+
+
+@pytest.mark.usefixtures("stream_kernel")
+def test_stream_kernel_several_tiles_per_expert_and_invalid_ids():
+    # expert 2 takes 7 of the 16 pairs (two tiles of at most four), expert 5 four;
+    # ids -1 and 9 (E = 8) are left out and flagged
+    lay = inputs.small_layer_inputs(1024, 512, 8, 4, 4, 78)
+    ids = np.array([[2, 2, 2, 5], [2, 2, 5, 5], [5, -1, 1, 2], [2, 9, 0, 3]], dtype=np.int32)
+    assert moe_w2.decode_kernel(4, 4, 1024, 512) == "decode_stream_kernel"
+    y, st = _run(lay, ids=ids)
+    ref, rst = oracle.forward_tokens(lay.x, ids, lay.weights, lay.planes)
+    assert st == rst == moe_w2.DEV_BAD_EXPERT_ID
+    assert_close_layer(y, ref, "stream kernel, several tiles per expert, invalid ids")
+
+
+@pytest.mark.usefixtures("stream_kernel")
+def test_stream_kernel_no_valid_pair_gives_zeros():
+    lay = inputs.small_layer_inputs(512, 512, 8, 2, 2, 79)
+    assert moe_w2.decode_kernel(2, 2, 512, 512) == "decode_stream_kernel"
+    ids = np.full((2, 2), -1, dtype=np.int32)
+    y, st = _run(lay, ids=ids)
+    assert st == moe_w2.DEV_BAD_EXPERT_ID
+    assert np.all(y == 0)
 
 
 @pytest.fixture(scope="module")
@@ -90,12 +138,15 @@ def decode_t32():
     return lay, planes_to_dev(lay.planes)
 
 
-def test_decode_t1_full_size():
+@pytest.mark.parametrize("kernel", ["decode_mma_kernel", "decode_stream_kernel"])
+def test_decode_t1_full_size(kernel):
     lay = inputs.layer_inputs(inputs.CONFIGS["decode_t1"])
-    y, st = _run(lay)
+    with moe_w2.decode_stream(kernel == "decode_stream_kernel"):
+        assert moe_w2.decode_kernel(1, 8, 6144, 2048) == kernel
+        y, st = _run(lay)
     ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes)
     assert st == rst == 0
-    assert_close_layer(y, ref, "decode_t1 full size")
+    assert_close_layer(y, ref, f"decode_t1 full size, {kernel}")
 
 
 def test_decode_t32_full_size_all_tokens(decode_t32):
@@ -106,29 +157,37 @@ def test_decode_t32_full_size_all_tokens(decode_t32):
     assert_close_layer(y, ref, "decode_t32 full size, all 32 tokens")
 
 
-# Wide in-block dynamic range.  T = 4 top-2 (8 pairs) runs the mma.sync kernel,
-# T = 16 top-2 (32 pairs) the block-scaled one, whose activations enter as e2m1
-# digit rows with one scale per 32 elements.
-@pytest.mark.parametrize("T", [4, 16])
+# Wide in-block dynamic range.  T = 4 top-2 (8 pairs) runs the mma.sync kernel
+# (bf16 activations) or, selected, the stream-K kernel; T = 16 top-2 (32 pairs)
+# the block-scaled one: the last two take activations as e2m1 digit rows with
+# one scale per 32 elements.
+WIDE_CASES = [(4, "decode_mma_kernel"), (4, "decode_stream_kernel"), (16, "decode_layer_kernel")]
+
+
+@pytest.mark.parametrize("T,kernel", WIDE_CASES)
 @pytest.mark.parametrize("mode", ["outlier", "zeros", "both"])
-def test_wide_range_activations(T, mode):
+def test_wide_range_activations(T, kernel, mode):
     lay = inputs.small_layer_inputs(512, 512, 8, 2, T, 40 + T)
     x = inputs.wide_range_activations(np.random.default_rng(T), T, 512, mode)
     lay = inputs.LayerInputs(lay.cfg, x, lay.ids, lay.weights, lay.planes)
-    y, st = _run(lay)
+    with moe_w2.decode_stream(kernel == "decode_stream_kernel"):
+        assert moe_w2.decode_kernel(T, 2, 512, 512) == kernel
+        y, st = _run(lay)
     ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, lay.planes)
     assert st == rst == 0
-    assert_close_layer(y, ref, f"{moe_w2.decode_kernel(T, 2, 512, 512)} wide-range x ({mode}) T={T}")
+    assert_close_layer(y, ref, f"{kernel} wide-range x ({mode}) T={T}")
 
 
-@pytest.mark.parametrize("T", [4, 16])
-def test_wide_range_h(T):
+@pytest.mark.parametrize("T,kernel", WIDE_CASES)
+def test_wide_range_h(T, kernel):
     lay = inputs.small_layer_inputs(512, 512, 8, 2, T, 50 + T)
     planes = inputs.boost_gate_up_rows(np.random.default_rng(T), lay.planes, boost=4)
-    y, st = _run(lay, planes_dev=planes_to_dev(planes))
+    with moe_w2.decode_stream(kernel == "decode_stream_kernel"):
+        assert moe_w2.decode_kernel(T, 2, 512, 512) == kernel
+        y, st = _run(lay, planes_dev=planes_to_dev(planes))
     ref, rst = oracle.forward_tokens(lay.x, lay.ids, lay.weights, planes)
     assert st == rst == 0
-    assert_close_layer(y, ref, f"{moe_w2.decode_kernel(T, 2, 512, 512)} wide-range h T={T}")
+    assert_close_layer(y, ref, f"{kernel} wide-range h T={T}")
 
 
 @pytest.mark.parametrize("name", ["decode_t1", "decode_t32"])

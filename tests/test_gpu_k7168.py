@@ -3,7 +3,8 @@ paragraph: 384 experts, top-8, H = 7168, loaded through the NVFP4 re-quantizer
 with a zero-sign balancing fix).
 
 H = 7168 is 14 x 512, so both decode kernels and the prefill kernels take it:
-  * decode T = 1 (mma.sync kernel), T = 4 and T = 16 (block-scaled kernel), every
+  * decode T = 1 (mma.sync kernel and, selected, the stream-K kernel), T = 2
+    (stream-K kernel), T = 4 and T = 16 (block-scaled kernel), every
     token against the oracle, and prefill T = 72 on sampled tokens; the layer has
     384 routed experts of I = 2048 behind an expert cache holding the step's
     experts plus a few others (moe_w2_forward_cached), as a 384-expert layer
@@ -25,9 +26,15 @@ pytestmark = pytest.mark.gpu
 H, I, E, K_TOP = 7168, 2048, 384, 8
 
 
-@pytest.mark.parametrize("T,path", [(1, moe_w2.PATH_DECODE_MMA), (4, moe_w2.PATH_DECODE_BLOCK_SCALED),
+@pytest.mark.parametrize("T,path", [(1, moe_w2.PATH_DECODE_MMA), (1, moe_w2.PATH_DECODE_STREAM),
+                                    (2, moe_w2.PATH_DECODE_STREAM), (4, moe_w2.PATH_DECODE_BLOCK_SCALED),
                                     (16, moe_w2.PATH_DECODE_BLOCK_SCALED), (72, moe_w2.PATH_PREFILL)])
 def test_kimi_shaped_layer(T, path):
+    with moe_w2.decode_stream(path == moe_w2.PATH_DECODE_STREAM):
+        _kimi_shaped_layer(T, path)
+
+
+def _kimi_shaped_layer(T, path):
     cfg = inputs.LayerConfig(f"k7168_t{T}", H, I, E, K_TOP, T, -10, -6, "zipf", 300 + T)
     lay = inputs.cached_layer_inputs(cfg, extra_slots=8)
     S = lay.planes["w13_codes"].shape[0]

@@ -23,9 +23,12 @@ _CHILD = textwrap.dedent(
     import torch
     from bit_moe_expert_w2_gb300 import inputs, moe_w2
 
-    # (H, I, E, k, T, seed): 2 pairs and 6 pairs take the mma.sync decode
-    # kernel, 32 pairs the block-scaled one, 160 pairs the prefill kernels
-    cases = [(512, 512, 8, 2, 1, 21), (512, 512, 8, 2, 16, 22), (512, 512, 8, 2, 80, 23), (512, 512, 8, 2, 3, 24)]
+    # (H, I, E, k, T, seed): with the stream-K kernel selected, 2 pairs and 6
+    # pairs take it, 32 pairs the block-scaled kernel, 160 pairs the prefill
+    # kernels, and I = 256 the mma.sync decode kernel
+    moe_w2.set_decode_stream(True)
+    cases = [(512, 512, 8, 2, 1, 21), (512, 512, 8, 2, 16, 22), (512, 512, 8, 2, 80, 23), (512, 512, 8, 2, 3, 24),
+             (512, 256, 8, 2, 3, 25)]
     args = []
     for c in cases:
         lay = inputs.small_layer_inputs(*c)

@@ -14,8 +14,8 @@ namespace {
 constexpr int32_t kPrefillTileRows = 256;   // pairs per prefill tile (tcgen05 N <= 256)
 constexpr int32_t kDecodeTileRows = 4;      // pairs per decode tile (MMA N = 32: kActDigits rows per pair)
 constexpr int32_t kDecodeMmaTileRows = 16;  // pairs per tile of the mma.sync decode kernel
-constexpr int64_t kDecodeMmaMaxPairs = 16;  // steps with at most this many pairs take the mma.sync kernel
-constexpr int64_t kDecodeStreamMaxPairs = 16; // ... or, when selected, the stream-K kernel
+constexpr int64_t kDecodeStreamMaxPairs = 16; // steps with at most this many pairs take the stream-K kernel
+constexpr int64_t kDecodeMmaMaxPairs = 16;  // ... or, when it is deselected, the mma.sync kernel
 constexpr int64_t kDecodeTargetItems = 1200; // down items per step that keep every CTA busy
 constexpr int64_t kDecodeSplitMaxPairs = 32;  // steps of up to this many pairs may split gate_up K in two
 constexpr int32_t kDecodeMinSegChunks = 2;   // at least 2 chunks of 256 K per decode item
@@ -53,7 +53,7 @@ moe_w2_status check_device()
 }
 
 std::atomic<int> g_force_timeout{0};
-std::atomic<int> g_decode_stream{0};   // moe_w2_set_decode_stream
+std::atomic<int> g_decode_stream{1};   // moe_w2_set_decode_stream
 
 DepWait dependency_wait()
 {

@@ -35,31 +35,31 @@
 // SM count): a wait that cannot end gives up with the pipeline-timeout status.
 //
 // Roles (sixteen warps, one CTA per SM):
-//   warps 0-3   consumers, one per TMEM lane quadrant, one thread per weight row:
-//               expand the row's 256 codes of a chunk to packed e2m1 and store
+//   warps 0-7   consumers in two groups (group h: warps 4h..4h+3, one per TMEM
+//               lane quadrant, one thread per weight row) taking chunk h of
+//               every pair: expand the row's 256 codes to packed e2m1 and store
 //               them with the row's two scale words and the activation rows'
-//               scale words into the chunk's A stage in TMEM
-//   warps 4-7   epilogues (one per TMEM lane quadrant): read each run's
+//               scale words into one of the group's two A stages in TMEM
+//   warps 8-11  epilogues (one per TMEM lane quadrant): read each run's
 //               accumulators, hand them back, then finish their 32 rows
-//   warps 8-11  code producers, one pair of chunks in four each: stream the
-//               pair's code tile (128 rows x 128 bytes, 128B-swizzled) by TMA
-//               into an 8-slot ring, running ahead of the consumers (down chunks
-//               included: their codes do not wait for h); lane 1 of warp 8 sends
-//               every run's scale tile (the 128 rows' whole scale rows) into one
-//               of two buffers
-//   warps 12-13 activation producers, one pair of chunks in two each: per pair
-//               of the tile its digit rows (two 8 x 128-byte boxes, 128B-swizzled
-//               as the UMMA B operand) and their scale group by TMA into a
-//               4-slot ring; down chunks only once the h of their tiles is
-//               published
-//   warps 14-15 MMA issuers (one thread each): issuer q takes the chunks of a run
-//               with index q mod 2, four MMAs (M = 128, N = 32, K = 64) per chunk
-//               into its own accumulator of the run's set; four sets rotate over
-//               consecutive runs, so the MMAs run up to three row blocks ahead of
-//               the slowest epilogue
-// (A single thread issues one tensor copy every few hundred cycles whatever its
-// size, and one chunk's MMAs and commits in about as long: hence six producers
-// and two issuers.)
+//   warp 12     lane 0 streams every pair's code tile (128 rows x 128 bytes,
+//               128B-swizzled) by TMA into an 8-slot ring, running ahead of the
+//               consumers (down pairs included: their codes do not wait for h);
+//               lane 1 sends every run's scale tile (the 128 rows' whole scale
+//               rows) into one of two buffers
+//   warp 13     activation producer: per pair of the tile its digit rows of
+//               both chunks (one 8 x 128-byte x 2-chunk box, 128B-swizzled as
+//               the UMMA B operand) and their scale group by TMA into a ring
+//               sized for the step's largest tile (4 to 10 slots); down pairs
+//               only once the h of their tiles is published
+//   warps 14-15 MMA issuers (one thread each): issuer q takes the chunks of
+//               group q, four MMAs (M = 128, N = 32, K = 64) per chunk into its
+//               own accumulator of the run's set; four sets rotate over
+//               consecutive runs, so the MMAs run up to three row blocks ahead
+//               of the slowest epilogue
+// (A consumer's chunk is a chain of dependent steps, barrier polls, shared
+// loads, integer expansion at half rate, a TMEM store: two groups overlap two
+// chains per quadrant.)
 #include <algorithm>
 
 #include "tc.cuh"
@@ -73,38 +73,35 @@ constexpr int kRows = 128;                           // weight rows per row bloc
 constexpr int kTilePairs = 4;                        // pairs per tile
 constexpr int kN = 32;                               // MMA N: the digit rows of a tile's pairs
 static_assert(kActDigits * kTilePairs <= kN, "a tile's digit rows must fit the MMA N");
-constexpr int kCWarps = 4;                           // consumer warps 0-3
-constexpr int kEpiWarp0 = 4;                         // epilogue warps 4-7 (TMEM lane quadrants 0-3)
+constexpr int kGroups = 2;                           // consumer groups: group h takes chunk h of every pair
+constexpr int kCWarps = 8;                           // consumer warps 0-7 (group h: warps 4h..4h+3)
+constexpr int kEpiWarp0 = 8;                         // epilogue warps 8-11 (TMEM lane quadrants 0-3)
 constexpr int kEWarps = 4;
-constexpr int kCodeWarp0 = 8;                        // code producers: warps 8-11
-constexpr int kCodeWarps = 4;
-constexpr int kActWarp0 = 12;                        // activation producers: warps 12-13
-constexpr int kActWarps = 2;
-constexpr int kMmaWarp0 = 14;                        // MMA issuers: warps 14-15
-constexpr int kIssuers = 2;
+constexpr int kProdWarp = 12;                        // lane 0: code tiles, lane 1: scale tiles
+constexpr int kActWarp = 13;                         // activation producer
+constexpr int kMmaWarp0 = 14;                        // MMA issuers: warps 14-15 (issuer q feeds on group q)
+constexpr int kIssuers = kGroups;
 constexpr int kThreads = 16 * 32;
 constexpr int kAccSets = 4;                          // accumulator sets: runs g use set g % 4
-constexpr int kCSlots = 8;                           // code ring (pair-chunk tiles)
-constexpr int kBSlots = 4;                           // activation ring (pair-chunk tiles)
-constexpr int kStages = 5;                           // A stages in TMEM (one chunk each)
+constexpr int kCSlots = 8;                           // code ring (pair tiles)
+constexpr int kBSlotsMax = 12;                       // activation ring (pair tiles), sized per step
+constexpr int kGStages = 2;                          // A stages in TMEM per group (one chunk each)
 constexpr uint32_t kCodeBytes = kRows * 128;         // a pair of chunks: 128 rows x 128 code bytes, 128B-swizzled
 constexpr uint32_t kBTile = 8 * 128;                 // one pair's 8 digit rows of one chunk (a 128B swizzle atom)
-constexpr uint32_t kBSfOff = 2 * kTilePairs * kBTile;   // in a B slot: tiles (pair j, chunk h) at (2 j + h) kBTile,
-constexpr uint32_t kBSlotBytes = kBSfOff + 1024;        // then pair j's 8 x 16 scale bytes at kBSfOff + 128 j
+constexpr uint32_t kBRegion = 36 * 1024;             // the activation ring's bytes (4 slots of a 4-pair tile)
 constexpr uint32_t kOffB = kCSlots * kCodeBytes;     // activation slots (1024-aligned)
-constexpr uint32_t kOffS = kOffB + kBSlots * kBSlotBytes;   // two scale tiles of 128 rows x sb bytes
-static_assert(kCodeBytes % 1024 == 0 && kOffB % 1024 == 0 && kBSlotBytes % 1024 == 0,
-              "swizzled tiles need 1024-byte alignment");
-// every ring slot has a single producer (pair position s goes to producer s mod n)
-static_assert(kCSlots % kCodeWarps == 0 && kBSlots % kActWarps == 0, "producers own whole slots");
+constexpr uint32_t kOffS = kOffB + kBRegion;         // two scale tiles of 128 rows x sb bytes
+static_assert(kCodeBytes % 1024 == 0 && kOffB % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 constexpr int kMaxScaleRow = 224;                    // scale bytes of a row (H/32, I/32): H, I <= 7168
 constexpr uint32_t kTmemCols = 512;
-// accumulator of set s, issuer q: columns 32 (2 s + q); A stage st: 256 + 32 st;
-// scale words: A (stage st, word w, lane quadrant q) 416 + 8 st + 4 w + q, B
-// (stage st, word w) 456 + 8 st + 4 w (scale operands start on 4-column boundaries)
+// accumulator of set s, issuer q: columns 32 (2 s + q); A stage st (group h's
+// stage i is st = 2 h + i): 256 + 32 st; scale words: A (stage st, word w, lane
+// quadrant q) 384 + 8 st + 4 w + q, B (stage st, word w) 416 + 8 st + 4 w (scale
+// operands start on 4-column boundaries)
+constexpr int kStages = kGroups * kGStages;
 constexpr uint32_t kColA = 256;
-constexpr uint32_t kColSfa = 416;
-constexpr uint32_t kColSfb = 456;
+constexpr uint32_t kColSfa = 384;
+constexpr uint32_t kColSfb = 416;
 static_assert(32 * kIssuers * kAccSets <= kColA && kColA + 32 * kStages <= kColSfa &&
                   kColSfa + 8 * kStages <= kColSfb && kColSfb + 8 * kStages <= kTmemCols,
               "TMEM layout");
@@ -113,16 +110,14 @@ static_assert(32 * kIssuers * kAccSets <= kColA && kColA + 32 * kStages <= kColS
 constexpr uint32_t kProducerSleepNs = 64;
 constexpr uint32_t kEpiSleepNs = 100;
 constexpr uint32_t kIssuerSleepNs = 20;
+constexpr uint32_t kConsumerSleepNs = 32;
 constexpr int32_t kHPublished = 2;                   // release adds per 64-element block of h (one per 32)
 constexpr int kMaxStreamTiles = 32;                  // tiles of a step (at most one per pair)
 
 struct StreamArgs {
     int32_t H, I, T, k, E;
     int64_t P;
-    const int4* tiles;
-    const int32_t* tile_count;
-    const int32_t* sorted;
-    const float* weights;
+    const float* weights;        // [T][k] router weights
     const int32_t* ids;          // [T][k]: kept pairs (valid ids) for the final sum
     const int32_t* route_ids;    // [T][k]: routed expert ids (the order of the tiles' row blocks)
     const int32_t* slot_of;      // behind an expert cache: [n_route] slot of each routed id (else null)
@@ -151,23 +146,23 @@ struct TileInfo {
 };
 
 struct SharedState {
-    uint64_t full_c[kCSlots];    // code producers -> consumers: a pair of chunks' code tile landed
-    uint64_t empty_c[kCSlots];   // consumer warps -> code producer: slot read
-    uint64_t full_s[2];          // code producers -> consumers: a run's scale tile landed
-    uint64_t empty_s[2];         // consumer warps -> code producer: scale tile read
-    uint64_t full_b[kBSlots];    // activation producers -> consumers, issuers: digit rows landed
-    uint64_t empty_b[kBSlots];   // both issuers' commits -> activation producer: slot read
-    uint64_t a_full[kStages];    // consumer warps -> issuer: A stage written
-    uint64_t a_empty[kStages];   // MMA commit -> consumers: A stage read
+    uint64_t full_c[kCSlots];    // code producer -> consumers: a pair of chunks' code tile landed
+    uint64_t empty_c[kCSlots];   // the eight consumer warps -> code producer: slot read
+    uint64_t full_s[2];          // scale producer -> consumers: a run's scale tile landed
+    uint64_t empty_s[2];         // the eight consumer warps -> scale producer: scale tile read
+    uint64_t full_b[kBSlotsMax]; // activation producers -> consumers, issuers: digit rows landed
+    uint64_t empty_b[kBSlotsMax];   // both issuers' commits -> activation producer: slot read
+    uint64_t a_full[kStages];    // a group's four warps -> its issuer: A stage written
+    uint64_t a_empty[kStages];   // the issuer's commit -> its group: A stage read
     uint64_t d_full[kAccSets];   // both issuers' commits -> epilogue warps: accumulator set complete
     uint64_t d_empty[kAccSets];  // epilogue warps -> issuers: accumulator set read
     uint64_t u_full[2][2];       // up-row warp 2 + h -> gate-row warp h: up sums in u_box (per half h, slot)
     uint64_t u_free[2][2];       // gate-row warp h -> up-row warp 2 + h: u_box slot read
     uint64_t drain;
-    uint64_t tiles_ready;        // warp 0 -> activation producers, epilogue warps: tinfo written
     TileInfo tinfo[kMaxStreamTiles];   // by row-block position (routed-id order)
     int plane_of[kMaxStreamTiles];     // planes' expert index of each tile position
     int n_tiles;
+    int nmax;                          // pairs of the step's largest tile
     float u_box[2][2][kTilePairs][32];   // up-row sums of whole gate_up row blocks (half, slot)
     uint32_t tmem;
     int abort_flag;
@@ -250,6 +245,16 @@ static __device__ __noinline__ ScaleFix fix_scale_words(uint32_t x, uint32_t y)
     return f;
 }
 
+// Element j of a register array of kTilePairs values (selects, so that a
+// run-time j keeps the array in registers).
+__device__ __forceinline__ float pick(const float (&v)[kTilePairs], int j)
+{
+    float r = v[0];
+#pragma unroll
+    for (int i = 1; i < kTilePairs; ++i) r = j == i ? v[i] : r;
+    return r;
+}
+
 // A pair's accumulator row: the sum of its kActDigits digit columns.
 __device__ __forceinline__ float pair_sum(const float (&v)[32], int j)
 {
@@ -263,83 +268,122 @@ __device__ __forceinline__ float pair_sum(const float (&v)[32], int j)
 // lane) as kActDigits digit rows of pair slot q: the lane's element sits at
 // packed position pos of the block; the other nibble of its byte belongs to
 // lane ^ 2, and the lane with the low nibble writes the byte.
+// (Rolled loops here and in the epilogue: the epilogue runs a few times per
+// launch, each time mostly from cold instruction caches, so its code is kept
+// small rather than unrolled.)
 __device__ __forceinline__ void store_h_digits(const StreamArgs& a, int64_t q, int blk, float v)
 {
     const int lane = threadIdx.x & 31;
     const int pos = (lane & 16) | fp4_pos(lane & 15);
-#pragma unroll
-    for (int d = 0; d < kActDigits; ++d) {
+    const int hs = a.I / 2, ss = a.I / 32;   // bytes per digit row, per scale row
+    uint8_t* hp = a.hd + kActDigits * q * hs + blk * 16 + (pos >> 1);
+    uint8_t* sp = a.shd + kActDigits * q * ss + blk;
+#pragma unroll 1
+    for (int d = 0; d < kActDigits; ++d, hp += hs, sp += ss) {
         const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
         const uint32_t sd = digit_scale_byte(__uint_as_float(amax_bits));
         float qv;
-        const uint32_t nib = e2m1_digit(v * digit_inv_scale(sd), qv);
+        const uint32_t nib = e2m1_digit_hw(v * digit_inv_scale(sd), qv);
         v -= qv * digit_scale(sd);
         const uint32_t other = __shfl_xor_sync(0xffffffffu, nib, 2);
-        const int64_t row = kActDigits * q + d;
-        if ((pos & 1) == 0) a.hd[row * (a.I / 2) + blk * 16 + (pos >> 1)] = (uint8_t)(nib | (other << 4));
-        if (lane == 0) a.shd[row * (a.I / 32) + blk] = (uint8_t)sd;
+        if ((pos & 1) == 0) *hp = (uint8_t)(nib | (other << 4));
+        if (lane == 0) *sp = (uint8_t)sd;
     }
+}
+
+// The sum of pair j, row `row` of a row block over its parts rf..rl in range
+// order (slot 0 but for range rf, whose slot is slot_rf; loads four at a time,
+// so their latencies overlap).
+__device__ __noinline__ float part_total(const float* part, int rf, int rl, int slot_rf, int j, int row)
+{
+    auto ptr = [&](int rg) {
+        return part + (((int64_t)(rg * 2 + (rg == rf ? slot_rf : 0)) * kTilePairs + j) * kRows + row);
+    };
+    float t = 0.f;
+    int rg = rf;
+    for (; rg + 3 <= rl; rg += 4) {
+        const float x0 = __ldcg(ptr(rg)), x1 = __ldcg(ptr(rg + 1)), x2 = __ldcg(ptr(rg + 2)), x3 = __ldcg(ptr(rg + 3));
+        t += x0;
+        t += x1;
+        t += x2;
+        t += x3;
+    }
+    for (; rg <= rl; ++rg) t += __ldcg(ptr(rg));
+    return t;
 }
 
 // One of the two chunk sequences (gate_up or down) cut into nr equal ranges of
 // whole chunk pairs (the unit the code tiles come in; a row block holds an even
 // number of chunks), nr = min(grid, pairs) so that no range is empty (CTAs
 // b >= nr get none).  Chunk indices throughout.
+// (32-bit: a step has at most 32 tiles x 112 row blocks x 28 chunks, and the
+// products below stay under 2^24.)
 struct Seq {
-    int64_t n;    // chunks
+    int32_t n;    // chunks
     int32_t L;    // chunks per row block
     int32_t nr;   // ranges
-    __device__ __forceinline__ Seq(int64_t n_, int32_t L_, int32_t grid)
-        : n(n_), L(L_), nr((int32_t)(n_ / 2 < (int64_t)grid ? n_ / 2 : (int64_t)grid)) {}
-    __device__ __forceinline__ int64_t start(int64_t b) const { return b < nr ? 2 * (b * (n / 2) / nr) : n; }
+    __device__ __forceinline__ Seq(int32_t n_, int32_t L_, int32_t grid)
+        : n(n_), L(L_), nr(n_ / 2 < grid ? n_ / 2 : grid) {}
+    __device__ __forceinline__ int32_t start(int32_t b) const { return b < nr ? 2 * (b * (n / 2) / nr) : n; }
     // the range holding chunk i (the last range starting at or before its pair)
-    __device__ __forceinline__ int64_t range_of(int64_t i) const { return ((i / 2 + 1) * nr - 1) / (n / 2); }
+    __device__ __forceinline__ int32_t range_of(int32_t i) const { return ((i / 2 + 1) * nr - 1) / (n / 2); }
 };
 
-// A CTA's walk over its chunks: its gate_up range, then its down range.  Every
-// role steps through the same positions in order (next()), and keeps the index
-// g of the current run (consecutive chunks of one row block) and the position j
-// of the chunk in it.
-struct Walk {
-    int64_t g0, ng, d0, nd;    // range starts and lengths
-    int32_t Lg, Ld;
-    int p = -1, g = -1, j = 0;
+// A CTA's runs: its gate_up range, then its down range, cut at row block ends.
+// A run is the chunks of one row block inside the range, always whole pairs
+// (ranges hold whole pairs and row blocks an even number of chunks).  Every
+// role steps through the same runs in order (next()).
+struct RunIter {
+    int32_t g0, ng, d0, nd;    // range starts and lengths (chunks)
+    int32_t Lg, Ld;            // chunks per row block
+    int g = -1;                // run index (accumulator set g % kAccSets, scale buffer g % 2)
     int kind = 0;              // 1 gate_up, 0 down
-    int64_t R = 0;             // row block (tile-major within its sequence)
-    int c = 0;                 // chunk of the row block
-    bool first = false, last = false;
-    __device__ __forceinline__ int total() const { return (int)(ng + nd); }
-    __device__ __forceinline__ void next()
+    int32_t R = 0;             // row block (tile-major within its sequence)
+    int c0 = 0;                // first chunk of the run in the row block (even)
+    int npairs = 0;            // pairs of the run
+    int32_t pos = 0;           // position of its first chunk in the CTA's chunks
+    __device__ __forceinline__ bool next()
     {
-        ++p;
-        if (p < ng) {
-            if (p == 0) {
-                kind = 1;
-                R = g0 / Lg;
-                c = (int)(g0 % Lg);
-            } else if (++c == Lg) {
-                c = 0;
-                ++R;
-            }
-            first = p == 0 || c == 0;
-            last = p == ng - 1 || c == Lg - 1;
-        } else {
-            if (p == ng) {
-                kind = 0;
-                R = d0 / Ld;
-                c = (int)(d0 % Ld);
-            } else if (++c == Ld) {
-                c = 0;
-                ++R;
-            }
-            first = p == ng || c == 0;
-            last = p == ng + nd - 1 || c == Ld - 1;
-        }
-        if (first) {
-            ++g;
-            j = 0;
-        } else {
-            ++j;
+        const int32_t p = g < 0 ? 0 : pos + 2 * npairs;
+        if (p >= ng + nd) return false;
+        ++g;
+        pos = p;
+        const bool gu = p < ng;
+        const int32_t at = gu ? g0 + p : d0 + (p - ng), end = gu ? g0 + ng : d0 + nd;
+        const int32_t L = gu ? Lg : Ld;
+        kind = gu ? 1 : 0;
+        R = at / L;
+        c0 = at - R * L;
+        npairs = (((R + 1) * L < end ? (R + 1) * L : end) - at) / 2;
+        return true;
+    }
+};
+
+// The activation ring: slots of `stride` bytes in the kBRegion bytes at kOffB,
+// sized for the step's largest tile (nmax pairs) so that small tiles get a deep
+// ring: pair j's digit tile of chunk h at (2 j + h) kBTile of a slot, its 8 x 16
+// scale bytes at sfoff + 128 j.  The MMA reads B rows of all four pair groups
+// (kBWindow bytes from the slot start, past a small slot into the next), so the
+// slots are as many as keep that window of the last one inside the region (at
+// most kBSlotsMax).  Every role keeps its own position (slot, phase of its
+// barriers), advanced per pair.
+constexpr uint32_t kBWindow = 2 * kTilePairs * kBTile;
+static_assert(kBRegion >= kBWindow, "the MMA's B window fits the ring");
+struct BRing {
+    uint32_t stride, sfoff, nb;
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ explicit BRing(int nmax)
+        : stride(((uint32_t)nmax * (2 * kBTile + 8 * 16) + 1023u) & ~1023u),
+          sfoff((uint32_t)nmax * 2 * kBTile),
+          nb(1u + (kBRegion - kBWindow) / stride < (uint32_t)kBSlotsMax ? 1u + (kBRegion - kBWindow) / stride
+                                                                          : (uint32_t)kBSlotsMax)
+    {
+    }
+    __device__ __forceinline__ void advance()
+    {
+        if (++slot == nb) {
+            slot = 0;
+            phase ^= 1u;
         }
     }
 };
@@ -347,9 +391,8 @@ struct Walk {
 // A run (a row block's chunks inside this CTA's range) as the epilogue needs it.
 struct Run {
     int kind;
-    int64_t R;
+    int32_t R;
     int g;          // run index (accumulator set g % kAccSets)
-    int nchunks;    // chunks of the run (1: only issuer 0's accumulator was written)
 };
 
 // Epilogue of run `r` by one epilogue warp (TMEM lane quadrant qd = warp % 4,
@@ -369,8 +412,8 @@ struct Run {
 //            count that completes them (n_tiles) sums every token's slots of
 //            the 32 rows in j order into y.
 // wn: whole gate_up runs so far of this warp (the u_box slot sequence).
-__device__ __noinline__ void epilogue(const StreamArgs& a, SharedState& sh, uint32_t tq, const Run& r,
-                                      const Seq& sg, const Seq& sd, int n_tiles, int wn, volatile int* abort)
+__device__ __forceinline__ void epilogue(const StreamArgs& a, SharedState& sh, uint32_t tq, const Run r, const Seq sg,
+                                         const Seq sd, int n_tiles, int wn, volatile int* abort)
 {
     const int lane = threadIdx.x & 31, qd = (threadIdx.x >> 5) & 3, m = 32 * qd + lane;
     const uint32_t set = (uint32_t)r.g % kAccSets;
@@ -380,13 +423,13 @@ __device__ __noinline__ void epilogue(const StreamArgs& a, SharedState& sh, uint
     for (int i = 0; i < 32; ++i) v[i] = 0.f;
     if (ok) {
         tc_fence_after();
+        // both issuers wrote their accumulator (a run has at least one pair:
+        // one chunk of each group)
+        float v1[32];
         tmem_ld32(tq + 32u * (2u * set), v);
-        if (r.nchunks > 1) {
-            float v1[32];
-            tmem_ld32(tq + 32u * (2u * set + 1u), v1);
+        tmem_ld32(tq + 32u * (2u * set + 1u), v1);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] += v1[i];
-        }
+        for (int i = 0; i < 32; ++i) v[i] += v1[i];
         tc_fence_before();
     }
     __syncwarp();
@@ -399,32 +442,20 @@ __device__ __noinline__ void epilogue(const StreamArgs& a, SharedState& sh, uint
     const int ti = (int)(r.R / rbn), rb = (int)(r.R % rbn);
     const TileInfo& tile = sh.tinfo[ti];
     const int nrows = tile.nrows;
-    // the ranges rf..rl cut the row block; the part slot of range rg
-    const int64_t rf = sq.range_of(r.R * sq.L), rl = sq.range_of((r.R + 1) * sq.L - 1);
-    const int nparts = (int)(rl - rf + 1);
+    // the ranges rf..rl cut the row block.  A range keeps its part of the row
+    // block it starts in in slot 0 and of the one it ends in in slot 1: only the
+    // first range, rf, can start before this row block (slot 1 unless it starts
+    // exactly at the row block's first chunk), the others start inside it.
+    const int rf = sq.range_of(r.R * sq.L), rl = sq.range_of((r.R + 1) * sq.L - 1);
+    const int nparts = rl - rf + 1;
+    const int slot_rf = sq.start(rf) < r.R * sq.L ? 1 : 0;
     float s[kTilePairs];
 #pragma unroll
     for (int j = 0; j < kTilePairs; ++j) s[j] = pair_sum(v, j);
     float* part = gate_up ? a.part_g : a.part_d;
-    auto part_ptr = [&](int64_t rg, int j, int row) {
-        const int slot = (r.R == sq.start(rg) / sq.L) ? 0 : 1;
-        return part + (((rg * 2 + slot) * kTilePairs + j) * kRows + row);
-    };
-    // the row block's sum of pair j, row `row` over its parts in range order
-    // (loads four at a time, so their latencies overlap)
-    auto total = [&](int j, int row) {
-        float t = 0.f;
-        int64_t rg = rf;
-        for (; rg + 3 <= rl; rg += 4) {
-            const float x0 = __ldcg(part_ptr(rg, j, row)), x1 = __ldcg(part_ptr(rg + 1, j, row));
-            const float x2 = __ldcg(part_ptr(rg + 2, j, row)), x3 = __ldcg(part_ptr(rg + 3, j, row));
-            t += x0;
-            t += x1;
-            t += x2;
-            t += x3;
-        }
-        for (; rg <= rl; ++rg) t += __ldcg(part_ptr(rg, j, row));
-        return t;
+    auto part_ptr = [&](int rg, int j, int row) {
+        const int slot = rg == rf ? slot_rf : 0;
+        return part + (((int64_t)(rg * 2 + slot) * kTilePairs + j) * kRows + row);
     };
     int old = 0;
 
@@ -452,18 +483,22 @@ __device__ __noinline__ void epilogue(const StreamArgs& a, SharedState& sh, uint
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh.u_free[h][slot]));
         } else {
-            for (int j = 0; j < nrows; ++j) *part_ptr(blockIdx.x, j, m) = s[j];
+#pragma unroll
+            for (int j = 0; j < kTilePairs; ++j)
+                if (j < nrows) *part_ptr(blockIdx.x, j, m) = s[j];
             __syncwarp();   // the warp's stores come before lane 0's release
             if (lane == 0) old = atom_add_acq_rel(a.g_cnt + 2 * r.R + h, 1);
             if (__shfl_sync(0xffffffffu, old, 0) != 2 * nparts - 1) return;
             __syncwarp();   // the lanes' reads below come after lane 0's acquire
-            for (int j = 0; j < nrows; ++j) {
-                g[j] = total(j, 32 * h + lane);
-                u[j] = total(j, 64 + 32 * h + lane);
+#pragma unroll
+            for (int j = 0; j < kTilePairs; ++j) {
+                g[j] = j < nrows ? part_total(part, rf, rl, slot_rf, j, 32 * h + lane) : 0.f;
+                u[j] = j < nrows ? part_total(part, rf, rl, slot_rf, j, 64 + 32 * h + lane) : 0.f;
             }
         }
+#pragma unroll 1
         for (int j = 0; j < nrows; ++j) {
-            const float hv = __bfloat162float(__float2bfloat16_rn(silu_f(g[j]) * u[j]));
+            const float hv = __bfloat162float(__float2bfloat16_rn(silu_f(pick(g, j)) * pick(u, j)));
             store_h_digits(a, (int64_t)tile.q0 + j, 2 * rb + h, hv);
         }
         __syncwarp();
@@ -474,29 +509,56 @@ __device__ __noinline__ void epilogue(const StreamArgs& a, SharedState& sh, uint
     // down: this warp's 32 rows into the pairs' slots
     const int row = kRows * rb + m;
     if (nparts > 1) {
-        for (int j = 0; j < nrows; ++j) *part_ptr(blockIdx.x, j, m) = s[j];
+#pragma unroll
+        for (int j = 0; j < kTilePairs; ++j)
+            if (j < nrows) *part_ptr(blockIdx.x, j, m) = s[j];
         __syncwarp();
         if (lane == 0) old = atom_add_acq_rel(a.d_cnt + 4 * r.R + qd, 1);
         if (__shfl_sync(0xffffffffu, old, 0) != nparts - 1) return;
         __syncwarp();
-        for (int j = 0; j < nrows; ++j) s[j] = total(j, m);
+#pragma unroll
+        for (int j = 0; j < kTilePairs; ++j) s[j] = j < nrows ? part_total(part, rf, rl, slot_rf, j, m) : 0.f;
     }
-    for (int j = 0; j < nrows; ++j) a.stage[(int64_t)tile.pr[j] * a.H + row] = tile.w[j] * s[j];
+#pragma unroll
+    for (int j = 0; j < kTilePairs; ++j)
+        if (j < nrows) a.stage[(int64_t)tile.pr[j] * a.H + row] = tile.w[j] * s[j];
     __syncwarp();   // the warp's stores come before lane 0's release
     if (lane == 0) old = atom_add_acq_rel(a.y_cnt + 4 * rb + qd, 1);
     if (__shfl_sync(0xffffffffu, old, 0) != n_tiles - 1) return;
     __syncwarp();
     // every tile's slots of these 32 rows are written: y = their sum per token
     // in j order (pairs left out never wrote a slot and add nothing)
+    // (a token's ids and slots are loaded eight at a time, so their latencies
+    // overlap; a slot left out may hold anything and is not added)
     for (int t = 0; t < a.T; ++t) {
         float acc = 0.f;
-        for (int j = 0; j < a.k; ++j) {
-            const int e = __ldg(a.ids + t * a.k + j);
-            if ((unsigned)e < (unsigned)a.E) acc += __ldcg(a.stage + (int64_t)(t * a.k + j) * a.H + row);
+        for (int j0 = 0; j0 < a.k; j0 += 8) {
+            int e[8];
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + u;
+                e[u] = j < a.k ? __ldg(a.ids + t * a.k + j) : -1;
+                x[u] = j < a.k ? __ldcg(a.stage + (int64_t)(t * a.k + j) * a.H + row) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc = (unsigned)e[u] < (unsigned)a.E ? acc + x[u] : acc;
         }
         __nv_bfloat16 yb = __float2bfloat16_rn(acc);
         a.y[(int64_t)t * a.H + row] = *reinterpret_cast<uint16_t*>(&yb);
     }
+}
+
+// Three barriers' phases complete (bounded as mbar_wait); the first polls are
+// issued back to back so that their latencies overlap.
+__device__ __forceinline__ bool mbar_wait3(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, uint32_t b3,
+                                           uint32_t p3, volatile int* abort)
+{
+    const bool r1 = mbar_try_wait(b1, p1), r2 = mbar_try_wait(b2, p2), r3 = mbar_try_wait(b3, p3);
+    if (r1 && r2 && r3) return true;
+    return (r1 || mbar_wait_sleep(b1, p1, abort, kConsumerSleepNs)) &&
+           (r2 || mbar_wait_sleep(b2, p2, abort, kConsumerSleepNs)) &&
+           (r3 || mbar_wait_sleep(b3, p3, abort, kConsumerSleepNs));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -504,7 +566,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
                      const __grid_constant__ CUtensorMap gu_sf_map, const __grid_constant__ CUtensorMap dn_sf_map,
                      const __grid_constant__ CUtensorMap xd_map, const __grid_constant__ CUtensorMap sxd_map,
                      const __grid_constant__ CUtensorMap hd_map, const __grid_constant__ CUtensorMap shd_map,
-                     const StreamArgs a)
+                     const __grid_constant__ StreamArgs a)
 {
     __shared__ SharedState sh;
     extern __shared__ uint8_t dyn_smem[];   // kOffS + 2 * 128 * sb + 1024 (aligned below)
@@ -519,12 +581,12 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
             mbar_init(smem_u32(&sh.full_s[s]), 1);
             mbar_init(smem_u32(&sh.empty_s[s]), kCWarps);
         }
-        for (int s = 0; s < kBSlots; ++s) {
+        for (int s = 0; s < kBSlotsMax; ++s) {
             mbar_init(smem_u32(&sh.full_b[s]), 1);
             mbar_init(smem_u32(&sh.empty_b[s]), kIssuers);
         }
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&sh.a_full[s]), kCWarps);
+            mbar_init(smem_u32(&sh.a_full[s]), kCWarps / kGroups);
             mbar_init(smem_u32(&sh.a_empty[s]), 1);
         }
         for (int s = 0; s < kAccSets; ++s) {
@@ -537,7 +599,6 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
                 mbar_init(smem_u32(&sh.u_free[h][s]), 1);
             }
         mbar_init(smem_u32(&sh.drain), kIssuers);
-        mbar_init(smem_u32(&sh.tiles_ready), 1);
         sh.abort_flag = 0;
         mbar_fence_init();
     }
@@ -545,25 +606,27 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
         tmem_alloc(smem_u32(&sh.tmem), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == kCodeWarp0 && lane == 0) {
+    if (warp == kProdWarp && lane == 0) {
         prefetch_tmap(&gu_map);
         prefetch_tmap(&dn_map);
         prefetch_tmap(&gu_sf_map);
         prefetch_tmap(&dn_sf_map);
     }
-    if (warp == kActWarp0 && lane == 0) {
+    if (warp == kActWarp && lane == 0) {
         prefetch_tmap(&xd_map);
         prefetch_tmap(&sxd_map);
         prefetch_tmap(&hd_map);
         prefetch_tmap(&shd_map);
     }
     if (warp == 1) {
-        // The step's tiles in the order of their routed expert ids, from the
-        // routing itself (an input: no need to wait for the permutation kernel),
-        // so the code producers can start at once: each kept expert (ascending
-        // routed id) gets ceil(pairs / 4) tiles, as the permutation forms them.
-        // Behind an expert cache the planes' index of expert r is its slot.
-        // At most 32 pairs (one per lane).
+        // The step's tiles, from the routing itself (inputs: no need to wait for
+        // the permutation kernel), in the order of their routed expert ids: each
+        // kept expert gets ceil(pairs / 4) tiles and its pairs (ascending pair
+        // index) are split evenly over them, as the permutation splits them.  A
+        // tile's first row of h (q0) counts the kept pairs of smaller ids, so
+        // the plain and the cached forward lay h out alike.  Behind an expert
+        // cache the planes' index of expert r is its slot.  At most 32 pairs
+        // (one per lane).
         int r = -1, plane = -1;
         if (lane < a.P) {
             r = __ldg(a.route_ids + lane);
@@ -574,15 +637,36 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
         const int key = r >= 0 ? r : 0x7FFFFFFF;
         const uint32_t same = __match_any_sync(0xffffffffu, key);
         const bool lead = r >= 0 && (__ffs(same) - 1) == lane;
-        const int ntl = lead ? (__popc(same) + kTilePairs - 1) / kTilePairs : 0;
-        int before = 0, total = 0;
+        const int cnt = __popc(same);
+        const int ntl = lead ? (cnt + kTilePairs - 1) / kTilePairs : 0;
+        int before = 0, total = 0, pbefore = 0;
         for (int u = 0; u < 32; ++u) {
             const int ku = __shfl_sync(0xffffffffu, key, u), nu = __shfl_sync(0xffffffffu, ntl, u);
             before += ku < key ? nu : 0;
+            pbefore += ku < key ? 1 : 0;
             total += nu;
         }
-        for (int t = 0; t < ntl; ++t) sh.plane_of[before + t] = plane;
-        if (lane == 0) sh.n_tiles = total;
+        for (int t = 0; t < ntl; ++t) {
+            const int r0 = t * cnt / ntl, r1 = (t + 1) * cnt / ntl;
+            TileInfo& ti = sh.tinfo[before + t];
+            ti.q0 = pbefore + r0;
+            ti.nrows = r1 - r0;
+            uint32_t rest = same;   // the expert's pairs from its (r0 + j)-th on
+            for (int j = 0; j < r0; ++j) rest &= rest - 1u;
+            for (int j = 0; j < kTilePairs; ++j) {
+                const int pr = j < r1 - r0 ? __ffs(rest) - 1 : 0;
+                rest &= rest - 1u;
+                ti.pr[j] = pr;
+                ti.tok[j] = pr / a.k;
+                ti.w[j] = j < r1 - r0 ? __ldg(a.weights + pr) : 0.f;
+            }
+            sh.plane_of[before + t] = plane;
+        }
+        const int nm = __reduce_max_sync(0xffffffffu, lead ? (cnt + ntl - 1) / ntl : 0);
+        if (lane == 0) {
+            sh.n_tiles = total;
+            sh.nmax = nm > 0 ? nm : 1;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -591,83 +675,77 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
     volatile int* abort = &sh.abort_flag;
     const int n_tiles = sh.n_tiles;
     const int rbg = a.I / 64, rbd = a.H / 128;
-    const Seq sg((int64_t)n_tiles * rbg * (a.H / kChunk), a.H / kChunk, (int32_t)gridDim.x);
-    const Seq sd((int64_t)n_tiles * rbd * (a.I / kChunk), a.I / kChunk, (int32_t)gridDim.x);
-    Walk w0{};
-    w0.g0 = sg.start(blockIdx.x);
-    w0.ng = sg.start(blockIdx.x + 1) - w0.g0;
-    w0.d0 = sd.start(blockIdx.x);
-    w0.nd = sd.start(blockIdx.x + 1) - w0.d0;
-    w0.Lg = sg.L;
-    w0.Ld = sd.L;
-    const int total = w0.total();   // even: ranges hold whole chunk pairs
+    const Seq sg(n_tiles * rbg * (a.H / kChunk), a.H / kChunk, (int32_t)gridDim.x);
+    const Seq sd(n_tiles * rbd * (a.I / kChunk), a.I / kChunk, (int32_t)gridDim.x);
+    RunIter r0{};
+    r0.g0 = sg.start(blockIdx.x);
+    r0.ng = sg.start(blockIdx.x + 1) - r0.g0;
+    r0.d0 = sd.start(blockIdx.x);
+    r0.nd = sd.start(blockIdx.x + 1) - r0.d0;
+    r0.Lg = sg.L;
+    r0.Ld = sd.L;
     const uint32_t sbuf0 = ring_addr + kOffS;
     const uint32_t sbytes = (uint32_t)kRows * (uint32_t)a.sb;   // one scale tile
 
-    if (warp >= kCodeWarp0 && warp < kCodeWarp0 + kCodeWarps) {
-        // ------------------------------------------------ code producers (read only inputs)
-        // Lane 0 of producer w issues the pairs of chunks s = w mod kCodeWarps
-        // (one pair: 128 rows x 128 code bytes in one tensor copy); a single
-        // thread issues one tensor copy every few hundred cycles, so one
-        // producer could not keep the ring full.  Lane 1 of producer 0 issues
-        // every run's scale tile (every weight row's whole scale row in one
-        // copy), in run order: a buffer's next tile is then sent only once the
-        // tile before it was both sent and read, so no wait on the buffer can
-        // mistake an older phase for the one it waits for.
-        const int w = warp - kCodeWarp0;
+    if (warp == kProdWarp) {
+        // ------------------------------------------------ code and scale producers (read only inputs)
         if (lane == 0) {
-            Walk wk = w0;
-            int p = 0;
-            for (; p < total; ++p) {
-                wk.next();
-                const int sp = p >> 1;
-                if ((p & 1) || sp % kCodeWarps != w) continue;
-                const bool gu = wk.kind == 1;
-                const int rb = (int)(wk.R % (gu ? rbg : rbd));
-                const int e = sh.plane_of[wk.R / (gu ? rbg : rbd)];
-                const uint32_t slot = (uint32_t)sp % kCSlots;
-                if (!mbar_wait_sleep(smem_u32(&sh.empty_c[slot]), (((uint32_t)sp / kCSlots) & 1u) ^ 1u, abort,
-                                     kProducerSleepNs))
-                    break;
-                const uint32_t base = ring_addr + slot * kCodeBytes, fb = smem_u32(&sh.full_c[slot]);
-                mbar_arrive_expect_tx_relaxed(fb, kCodeBytes);
-                // chunks c, c + 1 of the row block: code bytes 64 c .. 64 c + 127 of every row
-                if (gu) {
-                    // 64 gate rows then their 64 up rows (planes 2e, 2e + 1 of the
-                    // w13 plane seen as 2E planes of I rows)
-                    tma_load_3d(base, &gu_map, wk.c * 64, 64 * rb, 2 * e, fb);
-                } else {
-                    tma_load_2d(base, &dn_map, wk.c * 64, e * a.H + kRows * rb, fb);
+            // every pair's code tile (128 rows x 128 code bytes: chunks c, c + 1)
+            // in one tensor copy, into ring slot sp % kCSlots
+            RunIter it = r0;
+            int sp = 0;
+            bool stop = false;
+            while (!stop && it.next()) {
+                const bool gu = it.kind == 1;
+                const int rb = (int)(it.R % (gu ? rbg : rbd));
+                const int e = sh.plane_of[it.R / (gu ? rbg : rbd)];
+                for (int jp = 0; jp < it.npairs; ++jp, ++sp) {
+                    const uint32_t slot = (uint32_t)sp % kCSlots;
+                    if (!mbar_wait_sleep(smem_u32(&sh.empty_c[slot]), (((uint32_t)sp / kCSlots) & 1u) ^ 1u, abort,
+                                         kProducerSleepNs)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t base = ring_addr + slot * kCodeBytes, fb = smem_u32(&sh.full_c[slot]);
+                    const int c = it.c0 + 2 * jp;
+                    mbar_arrive_expect_tx_relaxed(fb, kCodeBytes);
+                    // code bytes 64 c .. 64 c + 127 of every row
+                    if (gu) {
+                        // 64 gate rows then their 64 up rows (planes 2e, 2e + 1 of the
+                        // w13 plane seen as 2E planes of I rows)
+                        tma_load_3d(base, &gu_map, c * 64, 64 * rb, 2 * e, fb);
+                    } else {
+                        tma_load_2d(base, &dn_map, c * 64, e * a.H + kRows * rb, fb);
+                    }
                 }
             }
             if (*abort) {
                 // the consumers may have stopped before the last tiles landed: wait
-                // (bounded) for this producer's copies of the last ring positions
+                // (bounded) for the copies of the last ring positions
                 volatile int never = 0;
-                const int sp_end = (p + 1) >> 1;
-                for (int sq = sp_end > kCSlots ? sp_end - kCSlots : 0; sq < sp_end; ++sq)
-                    if (sq % kCodeWarps == w)
-                        (void)mbar_wait(smem_u32(&sh.full_c[sq % kCSlots]), ((uint32_t)sq / kCSlots) & 1u, &never);
+                for (int sq = sp > kCSlots ? sp - kCSlots : 0; sq < sp; ++sq)
+                    (void)mbar_wait(smem_u32(&sh.full_c[sq % kCSlots]), ((uint32_t)sq / kCSlots) & 1u, &never);
             }
-        } else if (lane == 1 && w == 0) {
-            // the run's scale tile into buffer g % 2, once run g - 2 is done with it
-            Walk wk = w0;
+        } else if (lane == 1) {
+            // every run's scale tile, in run order, into buffer g % 2 once run
+            // g - 2 is done with it: a buffer's next tile is sent only after the
+            // one before it was both sent and read, so no wait on the buffer can
+            // mistake an older phase for the one it waits for
+            RunIter it = r0;
             int last_g[2] = {-1, -1};   // the last run whose tile went to each buffer
-            for (int p = 0; p < total; ++p) {
-                wk.next();
-                if (!wk.first) continue;
-                const bool gu = wk.kind == 1;
-                const int rb = (int)(wk.R % (gu ? rbg : rbd));
-                const int e = sh.plane_of[wk.R / (gu ? rbg : rbd)];
-                const uint32_t b = (uint32_t)wk.g & 1u;
-                if (!mbar_wait_sleep(smem_u32(&sh.empty_s[b]), (((uint32_t)wk.g >> 1) & 1u) ^ 1u, abort,
+            while (it.next()) {
+                const bool gu = it.kind == 1;
+                const int rb = (int)(it.R % (gu ? rbg : rbd));
+                const int e = sh.plane_of[it.R / (gu ? rbg : rbd)];
+                const uint32_t b = (uint32_t)it.g & 1u;
+                if (!mbar_wait_sleep(smem_u32(&sh.empty_s[b]), (((uint32_t)it.g >> 1) & 1u) ^ 1u, abort,
                                      kProducerSleepNs))
                     break;
                 const uint32_t fs = smem_u32(&sh.full_s[b]);
                 mbar_arrive_expect_tx_relaxed(fs, kRows * (uint32_t)(gu ? a.H / 32 : a.I / 32));
                 if (gu) tma_load_3d(sbuf0 + b * sbytes, &gu_sf_map, 0, 64 * rb, 2 * e, fs);
                 else tma_load_2d(sbuf0 + b * sbytes, &dn_sf_map, 0, e * a.H + kRows * rb, fs);
-                last_g[b] = wk.g;
+                last_g[b] = it.g;
             }
             if (*abort) {
                 volatile int never = 0;
@@ -677,62 +755,25 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
             }
         }
     } else {
-        // Launched as a programmatic dependent of the permutation kernel:
-        // everything it writes (tiles, zeroed counters, x digits) is read only
-        // after this wait.
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        if (warp == 0) {
-            // the tiles' pairs (the permutation's tile list, put in the order
-            // above): first slot, pairs, their tokens and router weights
-            int key = 0;
-            int4 t4 = make_int4(0, 0, 0, 0);
-            if (lane < n_tiles) {
-                t4 = a.tiles[lane];
-                key = a.slot_of != nullptr ? __ldg(a.route_ids + __ldg(a.sorted + t4.y)) : t4.x;
-            }
-            int rank = 0;
-            for (int u = 0; u < n_tiles; ++u) {
-                const int ku = __shfl_sync(0xffffffffu, key, u);
-                rank += (ku < key || (ku == key && u < lane)) ? 1 : 0;
-            }
-            if (lane < n_tiles) {
-                TileInfo& ti = sh.tinfo[rank];
-                ti.q0 = t4.y;
-                ti.nrows = t4.z;
-                for (int j = 0; j < kTilePairs; ++j) {
-                    const int pr = j < t4.z ? __ldg(a.sorted + t4.y + j) : 0;
-                    ti.pr[j] = pr;
-                    ti.tok[j] = pr / a.k;
-                    ti.w[j] = j < t4.z ? __ldg(a.weights + pr) : 0.f;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.tiles_ready));
-        }
-        const bool tiles_ok = mbar_wait_warp(smem_u32(&sh.tiles_ready), 0u, abort, kProducerSleepNs);
-        if (warp >= kActWarp0 && warp < kActWarp0 + kActWarps) {
-            // ------------------------------------------------ activation producers
-            // (producer w issues the pairs of chunks s = w mod kActWarps: per pair
-            // of the tile, two digit-row boxes and one scale box)
-            const int w = warp - kActWarp0;
-            Walk wk = w0;
-            int p = 0;
-            bool waited_h = false;
-            for (; p < total && tiles_ok; ++p) {
-                wk.next();
-                const int sp = p >> 1;
-                if ((p & 1) || sp % kActWarps != w) continue;
-                const uint32_t slot = (uint32_t)sp % kBSlots;
-                int ok = 1;
-                if (lane == 0)
-                    ok = mbar_wait_sleep(smem_u32(&sh.empty_b[slot]), (((uint32_t)sp / kBSlots) & 1u) ^ 1u, abort,
-                                         kProducerSleepNs);
-                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-                if (wk.kind == 0 && !waited_h) {
+        // Launched as a programmatic dependent of the permutation kernel: what
+        // it writes (the x digits, zeroed counters) is read, by the activation
+        // producer and the epilogues, only after this wait.
+        if (warp == kActWarp || (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEWarps))
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (warp == kActWarp) {
+            // ------------------------------------------------ activation producer
+            // (per pair of the tile, one digit-row box of both chunks and one
+            // scale box)
+            RunIter it = r0;
+            BRing br(sh.nmax);
+            int sp = 0;
+            bool stop = false, waited_h = false;
+            while (!stop && it.next()) {
+                if (it.kind == 0 && !waited_h) {
                     // the down range reads h of every tile it touches: wait
                     // (bounded) until all of those 64-element blocks are published
                     waited_h = true;
-                    const int t0 = (int)(wk.d0 / wk.Ld / rbd), t1 = (int)((wk.d0 + wk.nd - 1) / wk.Ld / rbd);
+                    const int t0 = (int)(it.d0 / it.Ld / rbd), t1 = (int)((it.d0 + it.nd - 1) / it.Ld / rbd);
                     const int nf = (t1 - t0 + 1) * rbg;
                     const int32_t* hf = a.h_flag + (int64_t)t0 * rbg;
                     const int32_t target = kHPublished + a.dep.bias;
@@ -758,60 +799,78 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
                     if (__shfl_sync(0xffffffffu, *abort, 0)) break;
                     fence_proxy_async_global();
                 }
-                const TileInfo& tile = sh.tinfo[wk.R / (wk.kind == 1 ? rbg : rbd)];
-                const uint32_t fb = smem_u32(&sh.full_b[slot]);
-                if (lane == 0)
-                    mbar_arrive_expect_tx_relaxed(fb, (uint32_t)tile.nrows * (kActDigits * (2 * 128 + 16)));
-                __syncwarp();
-                if (lane < tile.nrows) {
-                    // pair `lane` of the tile: gate_up reads its token's rows of x, down its rows of h
-                    const int brow = kActDigits * (wk.kind == 1 ? tile.tok[lane] : tile.q0 + lane);
-                    const uint32_t base = ring_addr + kOffB + slot * kBSlotBytes;
-                    const CUtensorMap* dm = wk.kind == 1 ? &xd_map : &hd_map;
-                    tma_load_2d(base + (2 * lane) * kBTile, dm, wk.c * 128, brow, fb);
-                    tma_load_2d(base + (2 * lane + 1) * kBTile, dm, (wk.c + 1) * 128, brow, fb);
-                    tma_load_2d(base + kBSfOff + lane * (kActDigits * 16), wk.kind == 1 ? &sxd_map : &shd_map,
-                                wk.c * 8, brow, fb);
+                const TileInfo& tile = sh.tinfo[it.R / (it.kind == 1 ? rbg : rbd)];
+                for (int jp = 0; jp < it.npairs; ++jp, ++sp, br.advance()) {
+                    const uint32_t slot = br.slot;
+                    int ok = 1;
+                    if (lane == 0)
+                        ok = mbar_wait_sleep(smem_u32(&sh.empty_b[slot]), br.phase ^ 1u, abort, kProducerSleepNs);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&sh.full_b[slot]);
+                    if (lane == 0)
+                        mbar_arrive_expect_tx_relaxed(fb, (uint32_t)tile.nrows * (kActDigits * (2 * 128 + 16)));
+                    __syncwarp();
+                    if (lane < tile.nrows) {
+                        // pair `lane` of the tile: gate_up reads its token's rows of x, down its rows of h
+                        const int brow = kActDigits * (it.kind == 1 ? tile.tok[lane] : tile.q0 + lane);
+                        const int c = it.c0 + 2 * jp;
+                        const uint32_t base = ring_addr + kOffB + slot * br.stride;
+                        // {128 bytes, 8 rows, chunks c and c + 1}: chunk-major, pair lane's tiles
+                        tma_load_3d(base + (2 * lane) * kBTile, it.kind == 1 ? &xd_map : &hd_map, 0, brow, c,
+                                    fb);
+                        tma_load_2d(base + br.sfoff + lane * (kActDigits * 16), it.kind == 1 ? &sxd_map : &shd_map,
+                                    c * 8, brow, fb);
+                    }
                 }
             }
             if (*abort && lane == 0) {
                 volatile int never = 0;
-                const int sp_end = (p + 1) >> 1;
-                for (int sq = sp_end > kBSlots ? sp_end - kBSlots : 0; sq < sp_end; ++sq)
-                    if (sq % kActWarps == w)
-                        (void)mbar_wait(smem_u32(&sh.full_b[sq % kBSlots]), ((uint32_t)sq / kBSlots) & 1u, &never);
+                const int nb = (int)br.nb;
+                for (int sq = sp > nb ? sp - nb : 0; sq < sp; ++sq)
+                    (void)mbar_wait(smem_u32(&sh.full_b[sq % nb]), ((uint32_t)sq / (uint32_t)nb) & 1u, &never);
             }
         } else if (warp >= kMmaWarp0) {
             // ------------------------------------------------ MMA issuers
-            // Runs start on even positions, so issuer q takes the chunks p = q mod 2
-            // (its own accumulator of the run's set); each also commits the B
-            // slot it read, which is free once both chunks of the pair are done.
+            // Issuer q takes chunk q of every pair (its own accumulator of the run's
+            // set, its group's A stages); each also commits the B slot it read,
+            // which is free once both chunks of the pair are done.  (Issuers in
+            // separate warps: one warp issues its tcgen05.mma instructions one
+            // after the other.)
             const int q = warp - kMmaWarp0;
             if (lane == 0) {
-                Walk wk = w0;
-                for (int p = 0; p < total; ++p) {
-                    wk.next();
-                    const uint32_t set = (uint32_t)wk.g % kAccSets;
+                RunIter it = r0;
+                BRing br(sh.nmax);
+                int sp = 0;
+                bool stop = false;
+                while (!stop && it.next()) {
+                    const uint32_t set = (uint32_t)it.g % kAccSets;
                     // The accumulator set of run g is free once the epilogue of run
                     // g - kAccSets read it.  Both issuers wait at every run's start:
                     // d_full[set] takes one commit from each, so neither may commit
                     // for a later run of the set before the epilogue of this one
                     // has seen both of its commits.
-                    if (wk.first && wk.g >= kAccSets &&
-                        !mbar_wait_sleep(smem_u32(&sh.d_empty[set]), (((uint32_t)wk.g / kAccSets) - 1u) & 1u, abort,
+                    if (it.g >= kAccSets &&
+                        !mbar_wait_sleep(smem_u32(&sh.d_empty[set]), (((uint32_t)it.g / kAccSets) - 1u) & 1u, abort,
                                          kIssuerSleepNs))
                         break;
-                    if ((p & 1) == q) {
-                        const uint32_t st = (uint32_t)p % kStages, sp = (uint32_t)p >> 1, bs = sp % kBSlots;
-                        if (!mbar_wait_sleep(smem_u32(&sh.full_b[bs]), (sp / kBSlots) & 1u, abort, kIssuerSleepNs) ||
-                            !mbar_wait_sleep(smem_u32(&sh.a_full[st]), ((uint32_t)p / kStages) & 1u, abort,
-                                             kIssuerSleepNs))
+                    const uint32_t d = tm + 32u * (2u * set + (uint32_t)q);
+                    for (int jp = 0; jp < it.npairs; ++jp, ++sp, br.advance()) {
+                        const uint32_t st = (uint32_t)(kGStages * q) + (uint32_t)sp % kGStages, bs = br.slot;
+                        const bool ready = mbar_wait_sleep(smem_u32(&sh.full_b[bs]), br.phase, abort,
+                                                           kIssuerSleepNs) &&
+                                           mbar_wait_sleep(smem_u32(&sh.a_full[st]), ((uint32_t)sp / kGStages) & 1u,
+                                                           abort, kIssuerSleepNs);
+                        if (!ready) {
+                            stop = true;
                             break;
+                        }
                         tc_fence_after();
                         // this chunk's B tiles: pair j at (2 j + q) kBTile of the slot
-                        const uint64_t bd =
-                            smem_desc_sw128_sbo(ring_addr + kOffB + bs * kBSlotBytes + (uint32_t)q * kBTile, 2 * kBTile);
-                        const uint32_t d = tm + 32u * (2u * set + (uint32_t)q);
+                        const uint64_t bd = smem_desc_sw128_sbo(
+                            ring_addr + kOffB + bs * br.stride + (uint32_t)q * kBTile, 2 * kBTile);
                         // MMA t: K 64t..64t+63 of the chunk = A columns 8t..8t+7 of the
                         // stage, 32 bytes of every B row, scale word t / 2, bytes
                         // 2 (t % 2) and 2 (t % 2) + 1
@@ -820,11 +879,11 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
                             umma_mxf4_ts(d, tm + kColA + 32 * st + 8 * t, bd + 2 * t,
                                          idesc_mxf4(kRows, kN, 2 * (t & 1), 2 * (t & 1)),
                                          tm + kColSfa + 8 * st + 4 * (t >> 1), tm + kColSfb + 8 * st + 4 * (t >> 1),
-                                         (wk.j >= 2 || t != 0) ? 1u : 0u);
+                                         (jp > 0 || t != 0) ? 1u : 0u);
                         umma_commit(smem_u32(&sh.a_empty[st]));
                         umma_commit(smem_u32(&sh.empty_b[bs]));
                     }
-                    if (wk.last) umma_commit(smem_u32(&sh.d_full[set]));
+                    if (!stop) umma_commit(smem_u32(&sh.d_full[set]));
                 }
                 // every MMA of both issuers has completed before tensor memory is freed
                 umma_commit(smem_u32(&sh.drain));
@@ -834,77 +893,87 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
         } else if (warp >= kEpiWarp0) {
             // ------------------------------------------------ epilogue warps
             const uint32_t tq = tm + ((uint32_t)(32 * (warp & 3)) << 16);
-            Walk wk = w0;
-            int run_start = 0, wn = 0;
-            for (int p = 0; p < total; ++p) {
-                wk.next();
-                if (wk.first) run_start = p;
-                if (wk.last) {
-                    epilogue(a, sh, tq, Run{wk.kind, wk.R, wk.g, p - run_start + 1}, sg, sd, n_tiles, wn, abort);
-                    // whole gate_up row blocks use the u_box slots in turn
-                    if (wk.kind == 1 && sg.range_of(wk.R * sg.L) == sg.range_of((wk.R + 1) * sg.L - 1)) ++wn;
-                }
+            RunIter it = r0;
+            int wn = 0;
+            while (it.next()) {
+                epilogue(a, sh, tq, Run{it.kind, it.R, it.g}, sg, sd, n_tiles, wn, abort);
+                // whole gate_up row blocks use the u_box slots in turn
+                if (it.kind == 1 && sg.range_of(it.R * sg.L) == sg.range_of((it.R + 1) * sg.L - 1)) ++wn;
             }
         } else {
             // ------------------------------------------------ consumers
-            const int m = tid;   // weight row of the row block
-            const uint32_t tq = tm + ((uint32_t)(32 * warp) << 16);
+            const int h = warp / (kCWarps / kGroups), qd = warp & 3;   // group, lane quadrant
+            const int m = 32 * qd + lane;                               // weight row of the row block
+            const uint32_t tq = tm + ((uint32_t)(32 * qd) << 16);
             const uint32_t swz = (uint32_t)m & 7u;   // 128B swizzle of this code row
             uint32_t bad_scale = 0;
-            Walk wk = w0;
-            for (int p = 0; p < total; ++p) {
-                wk.next();
-                const uint32_t sp = (uint32_t)p >> 1, half = (uint32_t)p & 1u;
-                const uint32_t cs = sp % kCSlots, st = (uint32_t)p % kStages, bs = sp % kBSlots;
-                const uint32_t sb_run = (uint32_t)wk.g & 1u;
-                bool got = true;
-                if (wk.first) got = mbar_wait(smem_u32(&sh.full_s[sb_run]), ((uint32_t)wk.g >> 1) & 1u, abort);
-                got = got && mbar_wait2(smem_u32(&sh.full_c[cs]), (sp / kCSlots) & 1u, smem_u32(&sh.a_empty[st]),
-                                        (((uint32_t)p / kStages) & 1u) ^ 1u, abort);
-                if (!__all_sync(0xffffffffu, got)) break;
-                tc_fence_after();
-                // the row's 64 code bytes of this chunk (16-byte unit 4 half + u of
-                // the 128-byte row at (4 half + u) ^ swz) and its two scale words
-                const uint32_t sb = ring_addr + cs * kCodeBytes + m * 128;
-                uint32_t wd[16];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint4 v = lds_u4(sb + (((4u * half + (uint32_t)u) ^ swz) << 4));
-                    wd[4 * u] = v.x;
-                    wd[4 * u + 1] = v.y;
-                    wd[4 * u + 2] = v.z;
-                    wd[4 * u + 3] = v.w;
-                }
-                uint2 sfa = lds_u2(sbuf0 + sb_run * sbytes + (uint32_t)m * (uint32_t)(wk.kind == 1 ? a.H / 32 : a.I / 32) +
-                                   8u * (uint32_t)wk.c);
-                __syncwarp();
-                if (lane == 0) {
-                    if (half) mbar_arrive(smem_u32(&sh.empty_c[cs]));   // both chunks of the pair read
-                    if (wk.last) mbar_arrive(smem_u32(&sh.empty_s[sb_run]));
-                }
-                uint32_t r[32];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) expand_fp4(wd[i], r[2 * i], r[2 * i + 1]);
-                if (scale_word_suspect(sfa.x) | scale_word_suspect(sfa.y)) {
-                    // an invalid scale byte: that 32-element block (4 registers) counts as zero
-                    const ScaleFix f = fix_scale_words(sfa.x, sfa.y);
-                    sfa = make_uint2(f.x, f.y);
-                    if (f.mask) {
-                        bad_scale = 1;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = ((f.mask >> (i >> 2)) & 1u) ? 0u : r[i];
+            RunIter it = r0;
+            BRing br(sh.nmax);
+            int sp = 0;
+            bool stop = false;
+            while (!stop && it.next()) {
+                const uint32_t sbuf = (uint32_t)it.g & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.full_s[sbuf]), ((uint32_t)it.g >> 1) & 1u, abort)))
+                    break;
+                // the row's scale words of chunk c0 + h (8 bytes per chunk)
+                const uint32_t srow = sbuf0 + sbuf * sbytes +
+                                      (uint32_t)m * (uint32_t)(it.kind == 1 ? a.H / 32 : a.I / 32) +
+                                      8u * (uint32_t)(it.c0 + h);
+                for (int jp = 0; jp < it.npairs; ++jp, ++sp, br.advance()) {
+                    const uint32_t cs = (uint32_t)sp % kCSlots, bs = br.slot;
+                    const uint32_t st = (uint32_t)(kGStages * h) + (uint32_t)sp % kGStages;
+                    const bool got = mbar_wait3(smem_u32(&sh.full_c[cs]), ((uint32_t)sp / kCSlots) & 1u,
+                                                smem_u32(&sh.a_empty[st]), (((uint32_t)sp / kGStages) & 1u) ^ 1u,
+                                                smem_u32(&sh.full_b[bs]), br.phase, abort);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        stop = true;
+                        break;
                     }
+                    tc_fence_after();
+                    // the row's 64 code bytes of chunk h of the pair (16-byte unit
+                    // 4 h + u of the 128-byte row at (4 h + u) ^ swz), its two scale
+                    // words, and the digit rows' scale words (B row n = lane: its
+                    // 16-byte group of the pair at sfoff + 16 n, word h; rows of
+                    // pairs past the tile's read whatever lies there, and only
+                    // their own, unused, accumulator columns see it)
+                    const uint32_t cb = ring_addr + cs * kCodeBytes + (uint32_t)m * 128u;
+                    uint32_t wd[16];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint4 v = lds_u4(cb + (((4u * (uint32_t)h + (uint32_t)u) ^ swz) << 4));
+                        wd[4 * u] = v.x;
+                        wd[4 * u + 1] = v.y;
+                        wd[4 * u + 2] = v.z;
+                        wd[4 * u + 3] = v.w;
+                    }
+                    uint2 sfa = lds_u2(srow + 16u * (uint32_t)jp);
+                    const uint2 sfb =
+                        lds_u2(ring_addr + kOffB + bs * br.stride + br.sfoff + (uint32_t)lane * 16u + 8u * (uint32_t)h);
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&sh.empty_c[cs]));
+                        if (jp == it.npairs - 1) mbar_arrive(smem_u32(&sh.empty_s[sbuf]));
+                    }
+                    uint32_t r[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) expand_fp4(wd[i], r[2 * i], r[2 * i + 1]);
+                    if (scale_word_suspect(sfa.x) | scale_word_suspect(sfa.y)) {
+                        // an invalid scale byte: that 32-element block (4 registers) counts as zero
+                        const ScaleFix f = fix_scale_words(sfa.x, sfa.y);
+                        sfa = make_uint2(f.x, f.y);
+                        if (f.mask) {
+                            bad_scale = 1;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) r[i] = ((f.mask >> (i >> 2)) & 1u) ? 0u : r[i];
+                        }
+                    }
+                    tmem_st_stage4(tq + kColA + 32 * st, r, tq + kColSfa + 8 * st + (uint32_t)qd, sfa.x,
+                                   tq + kColSfa + 8 * st + 4 + (uint32_t)qd, sfa.y, tq + kColSfb + 8 * st, sfb.x,
+                                   tq + kColSfb + 8 * st + 4, sfb.y);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sh.a_full[st]));
                 }
-                // the digit rows' scale words (this quadrant's copy) come with the rows:
-                // B row n's 16-byte group of the chunk pair at kBSfOff + 16 n
-                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.full_b[bs]), (sp / kBSlots) & 1u, abort))) break;
-                const uint2 sfb = lds_u2(ring_addr + kOffB + bs * kBSlotBytes + kBSfOff + (lane % kN) * 16 + 8u * half);
-                tmem_st_stage4(tq + kColA + 32 * st, r, tq + kColSfa + 8 * st + warp, sfa.x,
-                               tq + kColSfa + 8 * st + 4 + warp, sfa.y, tq + kColSfb + 8 * st, sfb.x,
-                               tq + kColSfb + 8 * st + 4, sfb.y);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sh.a_full[st]));
             }
             if (bad_scale) flag_status(a.status, MOE_W2_DEV_BAD_SCALE);
         }
@@ -960,9 +1029,6 @@ cudaError_t launch_decode_stream(const int32_t* ids, const int32_t* route_ids, c
     a.k = k;
     a.E = E;
     a.P = P;
-    a.tiles = ws.tiles;
-    a.tile_count = ws.tile_count;
-    a.sorted = ws.sorted;
     a.weights = weights;
     a.ids = ids;
     a.route_ids = route_ids;
@@ -999,12 +1065,18 @@ cudaError_t launch_decode_stream(const int32_t* ids, const int32_t* route_ids, c
         return e;
     if ((e = make_tmap_2d(&dn_sf_map, w.w2_scales, false, (int64_t)E * H, I / 32, I / 32, 128, 0)) != cudaSuccess)
         return e;
-    // activation digit rows: boxes of one pair's 8 rows x 128 bytes (256 K),
-    // 128B-swizzled as the UMMA B operand, and their 16-byte scale groups (two chunks)
+    // activation digit rows ([rows][K/2] bytes) seen as {128 bytes of a chunk,
+    // row, chunk}, the chunk stride (128) below the row stride: a box of one
+    // pair's 8 rows x 2 chunks lands chunk-major, each chunk's 8 rows one
+    // 128B-swizzle atom of the UMMA B operand; and their 16-byte scale groups
+    // (two chunks)
     CUtensorMap xd_map, sxd_map, hd_map, shd_map;
-    if ((e = make_tmap_2d(&xd_map, ws.xd, false, (int64_t)kActDigits * T, H / 2, 128, kActDigits, 128)) != cudaSuccess ||
+    const int64_t xdims[3] = {128, (int64_t)kActDigits * T, H / kChunk}, xstr[2] = {H / 2, 128};
+    const int64_t hdims[3] = {128, (int64_t)kActDigits * P, I / kChunk}, hstr[2] = {I / 2, 128};
+    const uint32_t dbox[3] = {128, (uint32_t)kActDigits, 2};
+    if ((e = make_tmap_u8(&xd_map, ws.xd, 3, xdims, xstr, dbox, 128)) != cudaSuccess ||
         (e = make_tmap_2d(&sxd_map, ws.sxd, false, (int64_t)kActDigits * T, H / 32, 16, kActDigits, 0)) != cudaSuccess ||
-        (e = make_tmap_2d(&hd_map, ws.hd, false, (int64_t)kActDigits * P, I / 2, 128, kActDigits, 128)) != cudaSuccess ||
+        (e = make_tmap_u8(&hd_map, ws.hd, 3, hdims, hstr, dbox, 128)) != cudaSuccess ||
         (e = make_tmap_2d(&shd_map, ws.shd, false, (int64_t)kActDigits * P, I / 32, 16, kActDigits, 0)) != cudaSuccess)
         return e;
 

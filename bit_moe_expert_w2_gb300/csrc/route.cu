@@ -150,6 +150,30 @@ cudaError_t make_tmap_3d_u8(CUtensorMap* map, const void* base, int64_t planes, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_tmap_u8(CUtensorMap* map, const void* base, int rank, const int64_t* dims, const int64_t* strides,
+                         const uint32_t* box, int swizzle_bytes)
+{
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    if (rank < 1 || rank > 5) return cudaErrorInvalidValue;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = (cuuint64_t)dims[i];
+        bx[i] = box[i];
+        estr[i] = 1;
+        if (i > 0) st[i - 1] = (cuuint64_t)strides[i - 1];
+    }
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                          : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted, const int32_t* offsets, int32_t E, int32_t k,
                           int32_t H, int64_t P, uint16_t* xs, cudaStream_t s)
 {

@@ -355,6 +355,12 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, bool bf16, int64_t 
 // expert's w13 plane as two consecutive planes of I rows.
 cudaError_t make_tmap_3d_u8(CUtensorMap* map, const void* base, int64_t planes, int64_t rows, int64_t cols,
                             uint32_t box_cols, uint32_t box_rows, uint32_t box_planes, int swizzle_bytes);
+// Tensor map of uint8 elements of any rank (1-5): dims[0] contiguous, strides
+// (bytes, multiples of 16) of dims 1.. in any order, e.g. the digit rows of an
+// activation seen as {128 bytes of a chunk, row, chunk} with the chunk stride
+// (128) below the row stride, so that a box lands chunk-major.
+cudaError_t make_tmap_u8(CUtensorMap* map, const void* base, int rank, const int64_t* dims, const int64_t* strides,
+                         const uint32_t* box, int swizzle_bytes);
 cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted, const int32_t* offsets, int32_t E, int32_t k,
                           int32_t H, int64_t P, uint16_t* xs, cudaStream_t s);
 cudaError_t launch_combine(const float* stage, const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t H,

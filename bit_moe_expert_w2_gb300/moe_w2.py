@@ -64,7 +64,7 @@ def decode_kernel(T: int, top_k: int, H: int, I: int) -> str:
 
 def set_decode_stream(enable: bool) -> None:
     """moe_w2_set_decode_stream: run decode steps of at most 16 pairs on the
-    stream-K kernel (True) or on the mma.sync kernel (False, the default)."""
+    stream-K kernel (True, the default) or on the mma.sync kernel (False)."""
     load().moe_w2_set_decode_stream(1 if enable else 0)
 
 

@@ -313,13 +313,13 @@ moe_w2_status moe_w2_debug_force_pipeline_timeout(int32_t enable);
 
 /*
  * Kernel choice for the smallest decode steps (at most 16 pairs, H and I
- * multiples of 512 and at most 7168).  With enable != 0, every later call in
- * this process (any thread, any device) runs such steps on the stream-K kernel
- * (MOE_W2_PATH_DECODE_STREAM: one CTA per SM streams every active expert's
- * planes, multiplied on the tensor cores in block-scaled FP4); with enable = 0
- * (the default) they run on the mma.sync kernel (MOE_W2_PATH_DECODE_MMA).  Both
- * compute the same layer ("vLLM-Moet wiki", section "The kernels") within the
- * same error bound.  The workspace a step needs depends on the choice
+ * multiples of 512 and at most 7168).  With enable != 0 (the default), every
+ * later call in this process (any thread, any device) runs such steps on the
+ * stream-K kernel (MOE_W2_PATH_DECODE_STREAM: one CTA per SM streams every
+ * active expert's planes, multiplied on the tensor cores in block-scaled FP4);
+ * with enable = 0 they run on the mma.sync kernel (MOE_W2_PATH_DECODE_MMA).
+ * Both compute the same layer ("vLLM-Moet wiki", section "The kernels") within
+ * the same error bound.  The workspace a step needs depends on the choice
  * (moe_w2_forward_workspace_size answers for the current one; a forward given
  * less returns MOE_W2_ERR_WORKSPACE).  Always returns MOE_W2_OK.
  */

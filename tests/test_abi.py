@@ -86,8 +86,8 @@ def test_alignment_and_workspace_checks_answer_before_any_device_access():
 
 def test_forward_path_names_the_kernels_a_call_runs():
     P = moe_w2
-    assert P.forward_path(1, 8, 256, 6144, 2048) == P.PATH_DECODE_MMA             # 8 pairs
-    assert P.forward_path(2, 8, 256, 6144, 2048) == P.PATH_DECODE_MMA             # 16 pairs
+    assert P.forward_path(1, 8, 256, 6144, 2048) == P.PATH_DECODE_STREAM          # 8 pairs
+    assert P.forward_path(2, 8, 256, 6144, 2048) == P.PATH_DECODE_STREAM          # 16 pairs
     assert P.forward_path(3, 8, 256, 6144, 2048) == P.PATH_DECODE_BLOCK_SCALED    # 24 pairs
     assert P.forward_path(32, 8, 256, 6144, 2048) == P.PATH_DECODE_BLOCK_SCALED
     assert P.forward_path(64, 8, 256, 6144, 2048) == P.PATH_DECODE_BLOCK_SCALED
@@ -98,20 +98,20 @@ def test_forward_path_names_the_kernels_a_call_runs():
     assert P.forward_path(1, 8, 8, 512, 256) == P.PATH_DECODE_MMA
     assert P.forward_path(0, 8, 256, 6144, 2048) == P.PATH_NONE
     assert P.forward_path(4, 2, 8, 500, 256) == P.PATH_NONE                       # invalid H
-    assert P.decode_kernel(1, 8, 6144, 2048) == "decode_mma_kernel"
+    assert P.decode_kernel(1, 8, 6144, 2048) == "decode_stream_kernel"
     assert P.decode_kernel(32, 8, 6144, 2048) == "decode_layer_kernel"
-    with P.decode_stream():
-        # the stream-K kernel, where selected, takes steps of at most 16 pairs
-        # with H and I multiples of 512 (up to 7168)
-        assert P.forward_path(1, 8, 256, 6144, 2048) == P.PATH_DECODE_STREAM
-        assert P.forward_path(2, 8, 256, 6144, 2048) == P.PATH_DECODE_STREAM
-        assert P.forward_path(3, 8, 256, 6144, 2048) == P.PATH_DECODE_BLOCK_SCALED
-        assert P.forward_path(1, 8, 8, 512, 256) == P.PATH_DECODE_MMA
-        assert P.forward_path(1, 8, 8, 7680, 2048) == P.PATH_DECODE_MMA
-        assert P.decode_kernel(1, 8, 6144, 2048) == "decode_stream_kernel"
-        assert P.decode_kernel(1, 8, 6144, 1792) == "decode_mma_kernel"
+    # the stream-K kernel takes steps of at most 16 pairs with H and I multiples
+    # of 512 (up to 7168); the rest of the small steps the mma.sync kernel
+    assert P.forward_path(3, 8, 256, 6144, 2048) == P.PATH_DECODE_BLOCK_SCALED
+    assert P.forward_path(1, 8, 8, 7680, 2048) == P.PATH_DECODE_MMA
+    assert P.decode_kernel(1, 8, 6144, 1792) == "decode_mma_kernel"
+    with P.decode_stream(False):
+        # deselected: the mma.sync kernel takes them
+        assert P.forward_path(1, 8, 256, 6144, 2048) == P.PATH_DECODE_MMA
+        assert P.forward_path(2, 8, 256, 6144, 2048) == P.PATH_DECODE_MMA
+        assert P.decode_kernel(1, 8, 6144, 2048) == "decode_mma_kernel"
         assert P.workspace_size(1, 8, 256, 6144, 2048) > 0
-    assert P.forward_path(1, 8, 256, 6144, 2048) == P.PATH_DECODE_MMA
+    assert P.forward_path(1, 8, 256, 6144, 2048) == P.PATH_DECODE_STREAM
 
 
 def test_cached_forward_host_checks():

@@ -43,7 +43,8 @@ def test_tiny_config_all_tokens():
 
 
 # Steps of more than 16 pairs with H and I multiples of 512 run the block-scaled
-# tcgen05 kernel; the rest the mma.sync kernel (both kinds are listed).
+# tcgen05 kernel, at most 16 pairs the stream-K kernel, and H or I not a
+# multiple of 512 the mma.sync kernel (all three kinds are listed).
 @pytest.mark.parametrize("H,I,E,k,T,seed", [(256, 256, 4, 1, 1, 1), (512, 256, 8, 2, 3, 2), (768, 512, 16, 4, 17, 3),
                                             (1024, 768, 8, 8, 64, 4), (512, 512, 2, 2, 64, 5),
                                             (256, 1024, 64, 16, 40, 6), (1024, 512, 16, 4, 17, 7),
@@ -157,10 +158,10 @@ def test_decode_t32_full_size_all_tokens(decode_t32):
     assert_close_layer(y, ref, "decode_t32 full size, all 32 tokens")
 
 
-# Wide in-block dynamic range.  T = 4 top-2 (8 pairs) runs the mma.sync kernel
-# (bf16 activations) or, selected, the stream-K kernel; T = 16 top-2 (32 pairs)
-# the block-scaled one: the last two take activations as e2m1 digit rows with
-# one scale per 32 elements.
+# Wide in-block dynamic range.  T = 4 top-2 (8 pairs) runs the stream-K kernel
+# or, deselected, the mma.sync kernel (bf16 activations); T = 16 top-2 (32
+# pairs) the block-scaled one: it and the stream-K kernel take activations as
+# e2m1 digit rows with one scale per 32 elements.
 WIDE_CASES = [(4, "decode_mma_kernel"), (4, "decode_stream_kernel"), (16, "decode_layer_kernel")]
 
 

@@ -163,6 +163,7 @@ struct SharedState {
     int plane_of[kMaxStreamTiles];     // planes' expert index of each tile position
     int n_tiles;
     int nmax;                          // pairs of the step's largest tile
+    float w_of[32];                    // router weight of each pair
     float u_box[2][2][kTilePairs][32];   // up-row sums of whole gate_up row blocks (half, slot)
     uint32_t tmem;
     int abort_flag;
@@ -628,6 +629,9 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
         // cache the planes' index of expert r is its slot.  At most 32 pairs
         // (one per lane).
         int r = -1, plane = -1;
+        // (every lane's router weight is loaded beside its id, so the two
+        // loads' latencies overlap; the tiles pick them up from shared memory)
+        sh.w_of[lane] = lane < a.P ? __ldg(a.weights + lane) : 0.f;
         if (lane < a.P) {
             r = __ldg(a.route_ids + lane);
             if (a.slot_of != nullptr) plane = (unsigned)r < (unsigned)a.n_route ? __ldg(a.slot_of + r) : -1;
@@ -646,6 +650,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
             pbefore += ku < key ? 1 : 0;
             total += nu;
         }
+        __syncwarp();
         for (int t = 0; t < ntl; ++t) {
             const int r0 = t * cnt / ntl, r1 = (t + 1) * cnt / ntl;
             TileInfo& ti = sh.tinfo[before + t];
@@ -658,7 +663,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
                 rest &= rest - 1u;
                 ti.pr[j] = pr;
                 ti.tok[j] = pr / a.k;
-                ti.w[j] = j < r1 - r0 ? __ldg(a.weights + pr) : 0.f;
+                ti.w[j] = j < r1 - r0 ? sh.w_of[pr] : 0.f;
             }
             sh.plane_of[before + t] = plane;
         }

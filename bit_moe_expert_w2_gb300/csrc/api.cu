@@ -147,7 +147,7 @@ Workspace carve_workspace(void* base, int32_t T, int32_t k, int32_t E, int32_t H
         w.hd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * P * (I / 2)));
         w.shd = reinterpret_cast<uint8_t*>(take((size_t)kActDigits * P * (I / 32)));
         w.stage = reinterpret_cast<float*>(take(sizeof(float) * P * H));
-        w.gu_part = reinterpret_cast<float*>(take(sizeof(float) * 2 * stream_part_floats()));
+        w.gu_part = reinterpret_cast<float*>(take(sizeof(float) * stream_part_floats()));
     } else if (decode && (w4 || decode_use_mma(P, H, I))) {
         w.counters = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * decode_counter_count(P, E, H, I, true)));
         w.xa = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * T * H));

@@ -312,7 +312,7 @@ bool decode_use_mma(int64_t P, int32_t H, int32_t I);
 // of its two partial-sum buffers (one CTA per SM, at most kMaxStreamGrid).
 constexpr int kMaxStreamGrid = 256;
 int64_t stream_counter_count(int64_t P, int32_t H, int32_t I);
-size_t stream_part_floats();
+size_t stream_part_floats();   // floats of the stream-K kernel's partial sums (all phases)
 
 struct Workspace {
     int32_t* sorted;       // [P]
@@ -336,7 +336,8 @@ struct Workspace {
     uint8_t* hd;           // e2m1 digit rows of h, kActDigits per pair (expert order) [8P][I/2]
     uint8_t* shd;          // their UE8M0 bytes [8P][I/32]
     float* gu_part;        // block-scaled kernel: gate_up partial sums of the two K halves [2][P][2I] (small
-                           // steps only, else null); stream-K kernel: its gate_up then down partial sums
+                           // steps only, else null); stream-K kernel: the partial sums of cut row blocks,
+                           // per phase (stream_part_floats() floats)
     // behind an expert cache
     int32_t* ids_eff;      // slot of each pair, -1 when left out [P] (null without a residency table)
     DecodeSplit split;

@@ -34,25 +34,26 @@
 // The waits assume the grid's CTAs are co-resident (one per SM, sized to the
 // SM count): a wait that cannot end gives up with the pipeline-timeout status.
 //
-// Roles (sixteen warps, one CTA per SM):
+// Roles (twenty warps, one CTA per SM):
 //   warps 0-7   consumers in two groups (group h: warps 4h..4h+3, one per TMEM
 //               lane quadrant, one thread per weight row) taking chunk h of
 //               every pair: expand the row's 256 codes to packed e2m1 and store
 //               them with the row's two scale words and the activation rows'
 //               scale words into one of the group's two A stages in TMEM
-//   warps 8-11  epilogues (one per TMEM lane quadrant): read each run's
+//   warps 8-15  epilogues in two sets of four (one warp per TMEM lane quadrant),
+//               set e taking the runs g with g % 2 = e: read the run's
 //               accumulators, hand them back, then finish their 32 rows
-//   warp 12     lane 0 streams every pair's code tile (128 rows x 128 bytes,
+//   warp 16     lane 0 streams every pair's code tile (128 rows x 128 bytes,
 //               128B-swizzled) by TMA into an 8-slot ring, running ahead of the
 //               consumers (down pairs included: their codes do not wait for h);
 //               lane 1 sends every run's scale tile (the 128 rows' whole scale
 //               rows) into one of two buffers
-//   warp 13     activation producer: per pair of the tile its digit rows of
+//   warp 17     activation producer: per pair of the tile its digit rows of
 //               both chunks (one 8 x 128-byte x 2-chunk box, 128B-swizzled as
 //               the UMMA B operand) and their scale group by TMA into a ring
 //               sized for the step's largest tile (4 to 10 slots); down pairs
 //               only once the h of their tiles is published
-//   warps 14-15 MMA issuers (one thread each): issuer q takes the chunks of
+//   warps 18-19 MMA issuers (one thread each): issuer q takes the chunks of
 //               group q, four MMAs (M = 128, N = 32, K = 64) per chunk into its
 //               own accumulator of the run's set; four sets rotate over
 //               consecutive runs, so the MMAs run up to three row blocks ahead
@@ -75,20 +76,21 @@ constexpr int kN = 32;                               // MMA N: the digit rows of
 static_assert(kActDigits * kTilePairs <= kN, "a tile's digit rows must fit the MMA N");
 constexpr int kGroups = 2;                           // consumer groups: group h takes chunk h of every pair
 constexpr int kCWarps = 8;                           // consumer warps 0-7 (group h: warps 4h..4h+3)
-constexpr int kEpiWarp0 = 8;                         // epilogue warps 8-11 (TMEM lane quadrants 0-3)
-constexpr int kEWarps = 4;
-constexpr int kProdWarp = 12;                        // lane 0: code tiles, lane 1: scale tiles
-constexpr int kActWarp = 13;                         // activation producer
-constexpr int kMmaWarp0 = 14;                        // MMA issuers: warps 14-15 (issuer q feeds on group q)
+constexpr int kEpiWarp0 = 8;                         // epilogue warps 8-15: two sets (runs g, g % 2 = set) of four
+constexpr int kEWarps = 4;                           // warps of a set (TMEM lane quadrants 0-3)
+constexpr int kESets = 2;
+constexpr int kProdWarp = 16;                        // lane 0: code tiles, lane 1: scale tiles
+constexpr int kActWarp = 17;                         // activation producer
+constexpr int kMmaWarp0 = 18;                        // MMA issuers: warps 18-19 (issuer q feeds on group q)
 constexpr int kIssuers = kGroups;
-constexpr int kThreads = 16 * 32;
+constexpr int kThreads = 20 * 32;
 constexpr int kAccSets = 4;                          // accumulator sets: runs g use set g % 4
 constexpr int kCSlots = 8;                           // code ring (pair tiles)
 constexpr int kBSlotsMax = 12;                       // activation ring (pair tiles), sized per step
 constexpr int kGStages = 2;                          // A stages in TMEM per group (one chunk each)
 constexpr uint32_t kCodeBytes = kRows * 128;         // a pair of chunks: 128 rows x 128 code bytes, 128B-swizzled
 constexpr uint32_t kBTile = 8 * 128;                 // one pair's 8 digit rows of one chunk (a 128B swizzle atom)
-constexpr uint32_t kBRegion = 36 * 1024;             // the activation ring's bytes (4 slots of a 4-pair tile)
+constexpr uint32_t kBRegion = 35 * 1024;             // the activation ring's bytes (4 slots of a 4-pair tile)
 constexpr uint32_t kOffB = kCSlots * kCodeBytes;     // activation slots (1024-aligned)
 constexpr uint32_t kOffS = kOffB + kBRegion;         // two scale tiles of 128 rows x sb bytes
 static_assert(kCodeBytes % 1024 == 0 && kOffB % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -125,8 +127,7 @@ struct StreamArgs {
     uint8_t* hd;                 // [8P][I/2] digit rows of h
     uint8_t* shd;                // [8P][I/32]
     float* stage;                // [P][H] w * (W_down h) per pair
-    float* part_g;               // [grid][2][kTilePairs][128] gate_up partial sums
-    float* part_d;               // [grid][2][kTilePairs][128] down partial sums
+    float* part;                 // [phase][grid][2][kTilePairs][128] partial sums of cut row blocks
     int32_t* h_flag;             // [tiles][I/64] h publications (one per 32 elements)
     int32_t* g_cnt;              // [tiles][I/64][2] gate_up partials arrived, per 32 elements of h
     int32_t* d_cnt;              // [tiles][H/128][4] down partials arrived, per 32 rows
@@ -145,6 +146,24 @@ struct TileInfo {
     float w[kTilePairs];         // their router weights
 };
 
+// The step's work in phases, each a chunk sequence cut into gridDim.x ranges
+// (Seq below): gate_up of each tile group, then down of each tile group; a CTA
+// streams its range of each in that order.  With kTileGroups = 2 the first
+// group's h would be published while the second group's gate_up streams; it
+// measured slower than one group (44.7 against 43.7 us for 8 pairs, 62.1
+// against 60.1 for 16: every run adds an epilogue and a cut), so the tiles form
+// one group.  Row blocks keep their step-wide index (tile-major per projection)
+// for the counters; the cuts and part slots are per phase.
+constexpr int kTileGroups = 1;
+constexpr int kPhases = 2 * kTileGroups;
+struct PhaseTable {
+    int32_t start[kPhases], len[kPhases];   // this CTA's range of each phase (chunks of the phase)
+    int32_t n[kPhases];                      // chunks of each phase
+    int32_t rbase[kPhases];                  // row block (step-wide) of each phase's first
+    int32_t t0[kPhases];                     // first tile of each phase
+};
+constexpr size_t kPartPhaseFloats = (size_t)kMaxStreamGrid * 2 * kTilePairs * kRows;
+
 struct SharedState {
     uint64_t full_c[kCSlots];    // code producer -> consumers: a pair of chunks' code tile landed
     uint64_t empty_c[kCSlots];   // the eight consumer warps -> code producer: slot read
@@ -156,15 +175,16 @@ struct SharedState {
     uint64_t a_empty[kStages];   // the issuer's commit -> its group: A stage read
     uint64_t d_full[kAccSets];   // both issuers' commits -> epilogue warps: accumulator set complete
     uint64_t d_empty[kAccSets];  // epilogue warps -> issuers: accumulator set read
-    uint64_t u_full[2][2];       // up-row warp 2 + h -> gate-row warp h: up sums in u_box (per half h, slot)
-    uint64_t u_free[2][2];       // gate-row warp h -> up-row warp 2 + h: u_box slot read
+    uint64_t u_full[kESets][2][2];   // up-row warp 2 + h -> gate-row warp h of a set: up sums in u_box (half, slot)
+    uint64_t u_free[kESets][2][2];   // gate-row warp h -> up-row warp 2 + h: u_box slot read
     uint64_t drain;
     TileInfo tinfo[kMaxStreamTiles];   // by row-block position (routed-id order)
     int plane_of[kMaxStreamTiles];     // planes' expert index of each tile position
     int n_tiles;
     int nmax;                          // pairs of the step's largest tile
+    PhaseTable pt;                     // this CTA's ranges of the four phases
     float w_of[32];                    // router weight of each pair
-    float u_box[2][2][kTilePairs][32];   // up-row sums of whole gate_up row blocks (half, slot)
+    float u_box[kESets][2][2][kTilePairs][32];   // up-row sums of whole gate_up row blocks (set, half, slot)
     uint32_t tmem;
     int abort_flag;
 };
@@ -330,33 +350,42 @@ struct Seq {
     __device__ __forceinline__ int32_t range_of(int32_t i) const { return ((i / 2 + 1) * nr - 1) / (n / 2); }
 };
 
-// A CTA's runs: its gate_up range, then its down range, cut at row block ends.
-// A run is the chunks of one row block inside the range, always whole pairs
+// A CTA's runs, phase after phase, each phase's range cut at row block ends.  A
+// run is the chunks of one row block inside the range, always whole pairs
 // (ranges hold whole pairs and row blocks an even number of chunks).  Every
 // role steps through the same runs in order (next()).
 struct RunIter {
-    int32_t g0, ng, d0, nd;    // range starts and lengths (chunks)
+    const PhaseTable* pt;
     int32_t Lg, Ld;            // chunks per row block
     int g = -1;                // run index (accumulator set g % kAccSets, scale buffer g % 2)
-    int kind = 0;              // 1 gate_up, 0 down
-    int32_t R = 0;             // row block (tile-major within its sequence)
+    int ph = 0;                // phase
+    int kind = 1;              // 1 gate_up, 0 down
+    int32_t Rl = 0;            // row block within the phase
+    int32_t R = 0;             // row block, step-wide (tile-major within its projection)
     int c0 = 0;                // first chunk of the run in the row block (even)
     int npairs = 0;            // pairs of the run
-    int32_t pos = 0;           // position of its first chunk in the CTA's chunks
+    int32_t pos = 0;           // position of its first chunk in the CTA's range of the phase
     __device__ __forceinline__ bool next()
     {
-        const int32_t p = g < 0 ? 0 : pos + 2 * npairs;
-        if (p >= ng + nd) return false;
-        ++g;
-        pos = p;
-        const bool gu = p < ng;
-        const int32_t at = gu ? g0 + p : d0 + (p - ng), end = gu ? g0 + ng : d0 + nd;
-        const int32_t L = gu ? Lg : Ld;
-        kind = gu ? 1 : 0;
-        R = at / L;
-        c0 = at - R * L;
-        npairs = (((R + 1) * L < end ? (R + 1) * L : end) - at) / 2;
-        return true;
+        while (ph < kPhases) {
+            const int32_t s = pt->start[ph], n = pt->len[ph];
+            const int32_t p = pos + 2 * npairs;
+            if (p < n) {
+                ++g;
+                pos = p;
+                kind = ph < kTileGroups ? 1 : 0;
+                const int32_t L = kind ? Lg : Ld, at = s + p;
+                Rl = at / L;
+                c0 = at - Rl * L;
+                npairs = (((Rl + 1) * L < s + n ? (Rl + 1) * L : s + n) - at) / 2;
+                R = pt->rbase[ph] + Rl;
+                return true;
+            }
+            ++ph;
+            pos = 0;
+            npairs = 0;
+        }
+        return false;
     }
 };
 
@@ -392,8 +421,10 @@ struct BRing {
 // A run (a row block's chunks inside this CTA's range) as the epilogue needs it.
 struct Run {
     int kind;
-    int32_t R;
+    int32_t R;      // row block, step-wide
     int g;          // run index (accumulator set g % kAccSets)
+    int ph;         // phase
+    int32_t Rl;     // row block within the phase
 };
 
 // Epilogue of run `r` by one epilogue warp (TMEM lane quadrant qd = warp % 4,
@@ -412,11 +443,12 @@ struct Run {
 //            into the pairs' slots, then one count for these rows of y; the
 //            count that completes them (n_tiles) sums every token's slots of
 //            the 32 rows in j order into y.
-// wn: whole gate_up runs so far of this warp (the u_box slot sequence).
-__device__ __forceinline__ void epilogue(const StreamArgs& a, SharedState& sh, uint32_t tq, const Run r, const Seq sg,
-                                         const Seq sd, int n_tiles, int wn, volatile int* abort)
+// wn: whole gate_up runs so far of this warp's set (the u_box slot sequence).
+__device__ __forceinline__ void epilogue(const StreamArgs& a, SharedState& sh, uint32_t tq, const Run r, int n_tiles,
+                                         int wn, volatile int* abort)
 {
     const int lane = threadIdx.x & 31, qd = (threadIdx.x >> 5) & 3, m = 32 * qd + lane;
+    const int es = ((threadIdx.x >> 5) - kEpiWarp0) / kEWarps;   // epilogue set
     const uint32_t set = (uint32_t)r.g % kAccSets;
     const bool ok = mbar_wait_warp(smem_u32(&sh.d_full[set]), ((uint32_t)r.g / kAccSets) & 1u, abort, kEpiSleepNs);
     float v[32];
@@ -438,7 +470,7 @@ __device__ __forceinline__ void epilogue(const StreamArgs& a, SharedState& sh, u
     if (!ok) return;
 
     const bool gate_up = r.kind == 1;
-    const Seq& sq = gate_up ? sg : sd;
+    const Seq sq(sh.pt.n[r.ph], gate_up ? a.H / kChunk : a.I / kChunk, (int32_t)gridDim.x);
     const int rbn = gate_up ? a.I / 64 : a.H / 128;   // row blocks per tile
     const int ti = (int)(r.R / rbn), rb = (int)(r.R % rbn);
     const TileInfo& tile = sh.tinfo[ti];
@@ -447,13 +479,13 @@ __device__ __forceinline__ void epilogue(const StreamArgs& a, SharedState& sh, u
     // block it starts in in slot 0 and of the one it ends in in slot 1: only the
     // first range, rf, can start before this row block (slot 1 unless it starts
     // exactly at the row block's first chunk), the others start inside it.
-    const int rf = sq.range_of(r.R * sq.L), rl = sq.range_of((r.R + 1) * sq.L - 1);
+    const int rf = sq.range_of(r.Rl * sq.L), rl = sq.range_of((r.Rl + 1) * sq.L - 1);
     const int nparts = rl - rf + 1;
-    const int slot_rf = sq.start(rf) < r.R * sq.L ? 1 : 0;
+    const int slot_rf = sq.start(rf) < r.Rl * sq.L ? 1 : 0;
     float s[kTilePairs];
 #pragma unroll
     for (int j = 0; j < kTilePairs; ++j) s[j] = pair_sum(v, j);
-    float* part = gate_up ? a.part_g : a.part_d;
+    float* part = a.part + (size_t)r.ph * kPartPhaseFloats;
     auto part_ptr = [&](int rg, int j, int row) {
         const int slot = rg == rf ? slot_rf : 0;
         return part + (((int64_t)(rg * 2 + slot) * kTilePairs + j) * kRows + row);
@@ -468,21 +500,21 @@ __device__ __forceinline__ void epilogue(const StreamArgs& a, SharedState& sh, u
             const uint32_t ph = ((uint32_t)wn >> 1) & 1u;
             if (qd >= 2) {
                 // up rows: hand the sums to the gate warp of this half
-                if (!mbar_wait_warp(smem_u32(&sh.u_free[h][slot]), ph ^ 1u, abort, kEpiSleepNs)) return;
+                if (!mbar_wait_warp(smem_u32(&sh.u_free[es][h][slot]), ph ^ 1u, abort, kEpiSleepNs)) return;
 #pragma unroll
-                for (int j = 0; j < kTilePairs; ++j) sh.u_box[h][slot][j][lane] = s[j];
+                for (int j = 0; j < kTilePairs; ++j) sh.u_box[es][h][slot][j][lane] = s[j];
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sh.u_full[h][slot]));
+                if (lane == 0) mbar_arrive(smem_u32(&sh.u_full[es][h][slot]));
                 return;
             }
-            if (!mbar_wait_warp(smem_u32(&sh.u_full[h][slot]), ph, abort, kEpiSleepNs)) return;
+            if (!mbar_wait_warp(smem_u32(&sh.u_full[es][h][slot]), ph, abort, kEpiSleepNs)) return;
 #pragma unroll
             for (int j = 0; j < kTilePairs; ++j) {
                 g[j] = s[j];
-                u[j] = sh.u_box[h][slot][j][lane];
+                u[j] = sh.u_box[es][h][slot][j][lane];
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.u_free[h][slot]));
+            if (lane == 0) mbar_arrive(smem_u32(&sh.u_free[es][h][slot]));
         } else {
 #pragma unroll
             for (int j = 0; j < kTilePairs; ++j)
@@ -562,6 +594,10 @@ __device__ __forceinline__ bool mbar_wait3(uint32_t b1, uint32_t p1, uint32_t b2
            (r3 || mbar_wait_sleep(b3, p3, abort, kConsumerSleepNs));
 }
 
+// shared memory of a CTA: the static state and the rings at the largest scale rows
+static_assert(sizeof(SharedState) + kOffS + 2 * kRows * kMaxScaleRow + 1024 <= 227 * 1024,
+              "the CTA's shared memory fits an SM");
+
 __global__ void __launch_bounds__(kThreads, 1)
 decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_constant__ CUtensorMap dn_map,
                      const __grid_constant__ CUtensorMap gu_sf_map, const __grid_constant__ CUtensorMap dn_sf_map,
@@ -594,11 +630,12 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
             mbar_init(smem_u32(&sh.d_full[s]), kIssuers);
             mbar_init(smem_u32(&sh.d_empty[s]), kEWarps);
         }
-        for (int h = 0; h < 2; ++h)
-            for (int s = 0; s < 2; ++s) {
-                mbar_init(smem_u32(&sh.u_full[h][s]), 1);
-                mbar_init(smem_u32(&sh.u_free[h][s]), 1);
-            }
+        for (int e = 0; e < kESets; ++e)
+            for (int h = 0; h < 2; ++h)
+                for (int s = 0; s < 2; ++s) {
+                    mbar_init(smem_u32(&sh.u_full[e][h][s]), 1);
+                    mbar_init(smem_u32(&sh.u_free[e][h][s]), 1);
+                }
         mbar_init(smem_u32(&sh.drain), kIssuers);
         sh.abort_flag = 0;
         mbar_fence_init();
@@ -680,15 +717,29 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
     volatile int* abort = &sh.abort_flag;
     const int n_tiles = sh.n_tiles;
     const int rbg = a.I / 64, rbd = a.H / 128;
-    const Seq sg(n_tiles * rbg * (a.H / kChunk), a.H / kChunk, (int32_t)gridDim.x);
-    const Seq sd(n_tiles * rbd * (a.I / kChunk), a.I / kChunk, (int32_t)gridDim.x);
+    const int32_t Lg = a.H / kChunk, Ld = a.I / kChunk;
+    if (tid == 0) {
+        // this CTA's ranges of the four phases
+        for (int p = 0; p < kPhases; ++p) {
+            const bool gu = p < kTileGroups;
+            const int gi = p % kTileGroups;   // tile group: tiles [gi n / G, (gi + 1) n / G) rounded up
+            const int t0 = (gi * n_tiles + kTileGroups - 1) / kTileGroups;
+            const int nt = ((gi + 1) * n_tiles + kTileGroups - 1) / kTileGroups - t0;
+            const int rbn = gu ? rbg : rbd;
+            const int32_t L = gu ? Lg : Ld;
+            const Seq q(nt * rbn * L, L, (int32_t)gridDim.x);
+            sh.pt.n[p] = q.n;
+            sh.pt.t0[p] = t0;
+            sh.pt.rbase[p] = t0 * rbn;
+            sh.pt.start[p] = q.start(blockIdx.x);
+            sh.pt.len[p] = q.start(blockIdx.x + 1) - sh.pt.start[p];
+        }
+    }
+    __syncthreads();
     RunIter r0{};
-    r0.g0 = sg.start(blockIdx.x);
-    r0.ng = sg.start(blockIdx.x + 1) - r0.g0;
-    r0.d0 = sd.start(blockIdx.x);
-    r0.nd = sd.start(blockIdx.x + 1) - r0.d0;
-    r0.Lg = sg.L;
-    r0.Ld = sd.L;
+    r0.pt = &sh.pt;
+    r0.Lg = Lg;
+    r0.Ld = Ld;
     const uint32_t sbuf0 = ring_addr + kOffS;
     const uint32_t sbytes = (uint32_t)kRows * (uint32_t)a.sb;   // one scale tile
 
@@ -763,7 +814,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
         // Launched as a programmatic dependent of the permutation kernel: what
         // it writes (the x digits, zeroed counters) is read, by the activation
         // producer and the epilogues, only after this wait.
-        if (warp == kActWarp || (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEWarps))
+        if (warp == kActWarp || (warp >= kEpiWarp0 && warp < kEpiWarp0 + kESets * kEWarps))
             asm volatile("griddepcontrol.wait;" ::: "memory");
         if (warp == kActWarp) {
             // ------------------------------------------------ activation producer
@@ -772,13 +823,15 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
             RunIter it = r0;
             BRing br(sh.nmax);
             int sp = 0;
-            bool stop = false, waited_h = false;
+            bool stop = false;
+            int waited_ph = -1;   // the down phase whose h was last waited for
             while (!stop && it.next()) {
-                if (it.kind == 0 && !waited_h) {
-                    // the down range reads h of every tile it touches: wait
-                    // (bounded) until all of those 64-element blocks are published
-                    waited_h = true;
-                    const int t0 = (int)(it.d0 / it.Ld / rbd), t1 = (int)((it.d0 + it.nd - 1) / it.Ld / rbd);
+                if (it.kind == 0 && it.ph != waited_ph) {
+                    // the down range of this phase reads h of every tile it touches:
+                    // wait (bounded) until all of those 64-element blocks are published
+                    waited_ph = it.ph;
+                    const int32_t ds = sh.pt.start[it.ph], dn = sh.pt.len[it.ph];
+                    const int t0 = sh.pt.t0[it.ph] + ds / Ld / rbd, t1 = sh.pt.t0[it.ph] + (ds + dn - 1) / Ld / rbd;
                     const int nf = (t1 - t0 + 1) * rbg;
                     const int32_t* hf = a.h_flag + (int64_t)t0 * rbg;
                     const int32_t target = kHPublished + a.dep.bias;
@@ -897,13 +950,20 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
             }
         } else if (warp >= kEpiWarp0) {
             // ------------------------------------------------ epilogue warps
+            // set e takes the runs g with g % kESets == e, so one run's epilogue
+            // overlaps the next one's
             const uint32_t tq = tm + ((uint32_t)(32 * (warp & 3)) << 16);
+            const int es = (warp - kEpiWarp0) / kEWarps;
             RunIter it = r0;
             int wn = 0;
             while (it.next()) {
-                epilogue(a, sh, tq, Run{it.kind, it.R, it.g}, sg, sd, n_tiles, wn, abort);
+                if (it.g % kESets != es) continue;
+                epilogue(a, sh, tq, Run{it.kind, it.R, it.g, it.ph, it.Rl}, n_tiles, wn, abort);
                 // whole gate_up row blocks use the u_box slots in turn
-                if (it.kind == 1 && sg.range_of(it.R * sg.L) == sg.range_of((it.R + 1) * sg.L - 1)) ++wn;
+                if (it.kind == 1) {
+                    const Seq q(sh.pt.n[it.ph], Lg, (int32_t)gridDim.x);
+                    if (q.range_of(it.Rl * Lg) == q.range_of((it.Rl + 1) * Lg - 1)) ++wn;
+                }
             }
         } else {
             // ------------------------------------------------ consumers
@@ -1004,7 +1064,7 @@ int64_t stream_counter_count(int64_t P, int32_t H, int32_t I)
     return P * (3 * (I / 64) + 4 * (H / 128)) + 4 * (H / 128);
 }
 
-size_t stream_part_floats() { return (size_t)kMaxStreamGrid * 2 * kTilePairs * kRows; }
+size_t stream_part_floats() { return (size_t)kPhases * kPartPhaseFloats; }
 
 cudaError_t launch_decode_stream(const int32_t* ids, const int32_t* route_ids, const int32_t* slot_of,
                                  int32_t n_route, const float* weights, const moe_w2_planes& w, int32_t T, int32_t k,
@@ -1042,8 +1102,7 @@ cudaError_t launch_decode_stream(const int32_t* ids, const int32_t* route_ids, c
     a.hd = ws.hd;
     a.shd = ws.shd;
     a.stage = ws.stage;
-    a.part_g = ws.gu_part;
-    a.part_d = ws.gu_part + stream_part_floats();
+    a.part = ws.gu_part;
     // counters, zeroed by the permutation kernel: [P][I/64] h flags, [P][I/64][2]
     // gate_up arrivals, [P][H/128][4] down arrivals, [H/128][4] y quarter blocks
     a.h_flag = ws.counters;

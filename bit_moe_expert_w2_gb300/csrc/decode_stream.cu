@@ -352,38 +352,65 @@ struct Seq {
 
 // A CTA's runs, phase after phase, each phase's range cut at row block ends.  A
 // run is the chunks of one row block inside the range, always whole pairs
-// (ranges hold whole pairs and row blocks an even number of chunks).  Every
-// role steps through the same runs in order (next()).
+// (ranges hold whole pairs and row blocks an even number of chunks).  In each
+// range the row blocks cut by its ends come first and the whole ones after: a
+// cut row block's other part belongs to the neighbouring CTA, which also takes
+// it first, so both parts are done early, and the range's last epilogue (the
+// one the next phase or y waits for) needs no other CTA.  Every role steps
+// through the same runs in order (next()).
 struct RunIter {
     const PhaseTable* pt;
     int32_t Lg, Ld;            // chunks per row block
     int g = -1;                // run index (accumulator set g % kAccSets, scale buffer g % 2)
     int ph = 0;                // phase
+    int k = -1;                // run of the current phase's range
     int kind = 1;              // 1 gate_up, 0 down
     int32_t Rl = 0;            // row block within the phase
     int32_t R = 0;             // row block, step-wide (tile-major within its projection)
     int c0 = 0;                // first chunk of the run in the row block (even)
     int npairs = 0;            // pairs of the run
-    int32_t pos = 0;           // position of its first chunk in the CTA's range of the phase
+    // run kk of the range [s, s + n) of a phase with row blocks of L chunks: the
+    // row blocks cut by the range's ends first, then the whole ones
+    __device__ __forceinline__ bool range_run(int32_t s, int32_t n, int32_t L, int kk)
+    {
+        if (n <= 0) return false;
+        const int32_t e = s + n, Rs = s / L, Re = (e - 1) / L;
+        int32_t lo, hi;
+        if (Rs == Re) {
+            if (kk > 0) return false;
+            Rl = Rs;
+            lo = s;
+            hi = e;
+        } else {
+            const bool hc = s != Rs * L, tc = e != (Re + 1) * L;   // head, tail row block cut
+            const int ncut = (hc ? 1 : 0) + (tc ? 1 : 0);
+            if (kk < ncut) {
+                Rl = (kk == 0 && hc) ? Rs : Re;
+                lo = Rl == Rs ? s : Re * L;
+                hi = Rl == Rs ? (Rs + 1) * L : e;
+            } else {
+                Rl = Rs + (hc ? 1 : 0) + (kk - ncut);
+                if (Rl > Re - (tc ? 1 : 0)) return false;
+                lo = Rl * L;
+                hi = lo + L;
+            }
+        }
+        c0 = lo - Rl * L;
+        npairs = (hi - lo) / 2;
+        return true;
+    }
     __device__ __forceinline__ bool next()
     {
+        ++k;
         while (ph < kPhases) {
-            const int32_t s = pt->start[ph], n = pt->len[ph];
-            const int32_t p = pos + 2 * npairs;
-            if (p < n) {
+            kind = ph < kTileGroups ? 1 : 0;
+            if (range_run(pt->start[ph], pt->len[ph], kind ? Lg : Ld, k)) {
                 ++g;
-                pos = p;
-                kind = ph < kTileGroups ? 1 : 0;
-                const int32_t L = kind ? Lg : Ld, at = s + p;
-                Rl = at / L;
-                c0 = at - Rl * L;
-                npairs = (((Rl + 1) * L < s + n ? (Rl + 1) * L : s + n) - at) / 2;
                 R = pt->rbase[ph] + Rl;
                 return true;
             }
             ++ph;
-            pos = 0;
-            npairs = 0;
+            k = 0;
         }
         return false;
     }

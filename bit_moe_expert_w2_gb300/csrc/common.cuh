@@ -85,6 +85,18 @@ __device__ __forceinline__ uint32_t e2m1_digit_hw(float v, float& val)
     val = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
     return n;
 }
+// Two digits at once (lo into the low nibble, hi into the high nibble of the
+// returned byte), as two e2m1_digit_hw: one conversion for both values.
+__device__ __forceinline__ uint32_t e2m1x2_digits_hw(float lo, float hi, float& qlo, float& qhi)
+{
+    uint32_t n, h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}" : "=r"(n) : "f"(hi), "f"(lo));
+    n &= ((n & 0x7u) != 0u ? 0x0Fu : 0u) | ((n & 0x70u) != 0u ? 0xF0u : 0u);   // a zero keeps no sign
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(n));
+    qlo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+    qhi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+    return n;
+}
 
 // ------------------------------------------------------------------ status
 __device__ __forceinline__ void flag_status(uint32_t* st, uint32_t bits)

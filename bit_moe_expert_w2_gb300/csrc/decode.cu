@@ -240,7 +240,7 @@ __device__ __forceinline__ void store_h_digits(const LayerArgs& a, int64_t q, in
         const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
         const uint32_t sd = digit_scale_byte(__uint_as_float(amax_bits));
         float qv;
-        const uint32_t nib = e2m1_digit(v * digit_inv_scale(sd), qv);
+        const uint32_t nib = e2m1_digit_hw(v * digit_inv_scale(sd), qv);
         v -= qv * digit_scale(sd);
         const uint32_t other = __shfl_xor_sync(0xffffffffu, nib, 2);
         const int64_t row = kActDigits * q + d;

@@ -237,11 +237,11 @@ __device__ __forceinline__ void x_digits(const uint16_t* __restrict__ x, int64_t
         const uint32_t s = digit_scale_byte(amax);
         const float inv = digit_inv_scale(s), sc = digit_scale(s);
         float q0, q1;
-        const uint32_t n0 = e2m1_digit(v[0] * inv, q0), n1 = e2m1_digit(v[1] * inv, q1);
+        const uint32_t nn = e2m1x2_digits_hw(v[0] * inv, v[1] * inv, q0, q1);
         v[0] -= q0 * sc;
         v[1] -= q1 * sc;
         if (live) {
-            xd[(kActDigits * t + d) * (H / 2) + c * 16 + r] = (uint8_t)(n0 | (n1 << 4));
+            xd[(kActDigits * t + d) * (H / 2) + c * 16 + r] = (uint8_t)nn;
             if (r == 0) sxd[(kActDigits * t + d) * bpr + c] = (uint8_t)s;
         }
     }

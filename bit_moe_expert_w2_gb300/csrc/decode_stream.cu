@@ -1014,9 +1014,10 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
                 for (int jp = 0; jp < it.npairs; ++jp, ++sp, br.advance()) {
                     const uint32_t cs = (uint32_t)sp % kCSlots, bs = br.slot;
                     const uint32_t st = (uint32_t)(kGStages * h) + (uint32_t)sp % kGStages;
-                    const bool got = mbar_wait3(smem_u32(&sh.full_c[cs]), ((uint32_t)sp / kCSlots) & 1u,
-                                                smem_u32(&sh.a_empty[st]), (((uint32_t)sp / kGStages) & 1u) ^ 1u,
-                                                smem_u32(&sh.full_b[bs]), br.phase, abort);
+                    // the code tile and the stage first: the expansion does not need
+                    // the activation rows, whose scale words are stored last
+                    const bool got = mbar_wait2(smem_u32(&sh.full_c[cs]), ((uint32_t)sp / kCSlots) & 1u,
+                                                smem_u32(&sh.a_empty[st]), (((uint32_t)sp / kGStages) & 1u) ^ 1u, abort);
                     if (!__all_sync(0xffffffffu, got)) {
                         stop = true;
                         break;
@@ -1039,8 +1040,6 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
                         wd[4 * u + 3] = v.w;
                     }
                     uint2 sfa = lds_u2(srow + 16u * (uint32_t)jp);
-                    const uint2 sfb =
-                        lds_u2(ring_addr + kOffB + bs * br.stride + br.sfoff + (uint32_t)lane * 16u + 8u * (uint32_t)h);
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(smem_u32(&sh.empty_c[cs]));
@@ -1059,9 +1058,16 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
                             for (int i = 0; i < 32; ++i) r[i] = ((f.mask >> (i >> 2)) & 1u) ? 0u : r[i];
                         }
                     }
-                    tmem_st_stage4(tq + kColA + 32 * st, r, tq + kColSfa + 8 * st + (uint32_t)qd, sfa.x,
-                                   tq + kColSfa + 8 * st + 4 + (uint32_t)qd, sfa.y, tq + kColSfb + 8 * st, sfb.x,
-                                   tq + kColSfb + 8 * st + 4, sfb.y);
+                    tmem_st_a_sfa(tq + kColA + 32 * st, r, tq + kColSfa + 8 * st + (uint32_t)qd, sfa.x,
+                                  tq + kColSfa + 8 * st + 4 + (uint32_t)qd, sfa.y);
+                    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.full_b[bs]), br.phase, abort))) {
+                        tmem_st_sfb_wait(r, sfa.x, sfa.y, tq + kColSfb + 8 * st, 0u, tq + kColSfb + 8 * st + 4, 0u);
+                        stop = true;
+                        break;
+                    }
+                    const uint2 sfb =
+                        lds_u2(ring_addr + kOffB + bs * br.stride + br.sfoff + (uint32_t)lane * 16u + 8u * (uint32_t)h);
+                    tmem_st_sfb_wait(r, sfa.x, sfa.y, tq + kColSfb + 8 * st, sfb.x, tq + kColSfb + 8 * st + 4, sfb.y);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&sh.a_full[st]));

@@ -315,6 +315,30 @@ __device__ __forceinline__ void tmem_st_stage4(uint32_t ta, const uint32_t (&r)[
         : "memory");
 }
 
+// tmem_st_stage4 in two halves: the A stage and its two scale words now (not
+// waited for), the B scale words later, when they have come, and then the wait
+// for all six stores.  The registers of the first half are read until the
+// wait, so the second asm takes them as inputs too (they stay untouched).
+__device__ __forceinline__ void tmem_st_a_sfa(uint32_t ta, const uint32_t (&r)[32], uint32_t tsa0, uint32_t sa0,
+                                              uint32_t tsa1, uint32_t sa1)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%33], {%34};\n"
+        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%35], {%36};" ::"r"(ta),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(tsa0), "r"(sa0), "r"(tsa1), "r"(sa1)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_sfb_wait(const uint32_t (&r)[32], uint32_t sa0, uint32_t sa1, uint32_t tsb0,
+                                                 uint32_t sb0, uint32_t tsb1, uint32_t sb1)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%32], {%33};\n"
+        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%34], {%35};\n"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(tsb0), "r"(sb0), "r"(tsb1), "r"(sb1), "r"(sa0), "r"(sa1)
+        : "memory");
+}
+
 // 16 consecutive fp32 columns of this warp's 32 TMEM lanes (load and wait in one asm).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 {

@@ -774,7 +774,21 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
         // ------------------------------------------------ code and scale producers (read only inputs)
         if (lane == 0) {
             // every pair's code tile (128 rows x 128 code bytes: chunks c, c + 1)
-            // in one tensor copy, into ring slot sp % kCSlots
+            // in one tensor copy, into ring slot sp % kCSlots; first the scale
+            // tile of run 0 (the scale lane, below, takes the runs after it), so
+            // that it does not wait behind the ring's first code tiles
+            {
+                RunIter f = r0;
+                if (f.next()) {
+                    const bool gu = f.kind == 1;
+                    const int rb = (int)(f.R % (gu ? rbg : rbd));
+                    const int e = sh.plane_of[f.R / (gu ? rbg : rbd)];
+                    const uint32_t fs = smem_u32(&sh.full_s[0]);
+                    mbar_arrive_expect_tx_relaxed(fs, kRows * (uint32_t)(gu ? a.H / 32 : a.I / 32));
+                    if (gu) tma_load_3d(sbuf0, &gu_sf_map, 0, 64 * rb, 2 * e, fs);
+                    else tma_load_2d(sbuf0, &dn_sf_map, 0, e * a.H + kRows * rb, fs);
+                }
+            }
             RunIter it = r0;
             int sp = 0;
             bool stop = false;
@@ -817,6 +831,10 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap gu_map, const __grid_co
             RunIter it = r0;
             int last_g[2] = {-1, -1};   // the last run whose tile went to each buffer
             while (it.next()) {
+                if (it.g == 0) {   // sent by the code lane
+                    last_g[0] = 0;
+                    continue;
+                }
                 const bool gu = it.kind == 1;
                 const int rb = (int)(it.R % (gu ? rbg : rbd));
                 const int e = sh.plane_of[it.R / (gu ? rbg : rbd)];
